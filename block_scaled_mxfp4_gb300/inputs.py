@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for the block-scaled MXFP4 GEMM.
+
+This module only *produces bytes*: packed fp4x2 E2M1 operands, row-major E8M0
+scales and bf16 C.  It holds none of the GEMM's arithmetic, so both the CUDA
+path and the CPU oracle can consume what it makes without sharing code.
+
+Formats (page "asm_f4gemm -- driving aiter's gfx950 MXFP4 GEMM code objects",
+section "Data layouts"):
+  * A [M, K/2] and B [N, K/2] bytes, row-major; byte i of a row holds element
+    2i in the low nibble and element 2i+1 in the high nibble.
+  * E2M1 codes: bit 3 is the sign, bits 2..0 index the magnitudes
+    {0, .5, 1, 1.5, 2, 3, 4, 6}.
+  * One E8M0 scale byte per 32 consecutive K elements, row-major [rows, K/32].
+
+Workloads are the five shapes of the GB300 target list (tiny, decode, mid,
+large, skinny-M wide-K), plus an identity case.  Values follow each recipe:
+  * tiny:   codes uniform over all 16, scale exponent uniform in {-4..4}.
+  * others: x ~ N(0,1) (skinny: U[-1,1]); per 1x32 block the scale exponent is
+    s = floor(log2(max|x| / 6)) (s = 0 for an all-zero block, clamped to
+    [-127, 127]); the element code is x / 2^s rounded to nearest E2M1 with
+    ties to the even mantissa and saturation at +-6; the sign bit copies
+    sign(x).
+Draw order within a workload: A, then B, then C, each drawn row-chunk by
+row-chunk in C order from one numpy PCG64 generator seeded per workload.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+_ROW_CHUNK = 1024
+
+
+@dataclasses.dataclass
+class Problem:
+    """One GEMM instance: D = alpha * A . B^T + beta * C (all host numpy)."""
+
+    name: str
+    M: int
+    N: int
+    K: int
+    A: np.ndarray            # uint8 [M, K/2] packed E2M1
+    B: np.ndarray            # uint8 [N, K/2] packed E2M1
+    SA: np.ndarray           # uint8 [M, K/32] E8M0
+    SB: np.ndarray           # uint8 [N, K/32] E8M0
+    C: Optional[np.ndarray]  # uint16 [M, N] bf16 bits, or None
+    alpha: float
+    beta: float
+    seed: int
+
+
+def pack_fp4(codes: np.ndarray) -> np.ndarray:
+    """Pack 4-bit codes [rows, K] into bytes [rows, K/2]: even k -> low nibble."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    assert codes.ndim == 2 and codes.shape[1] % 2 == 0
+    lo = codes[:, 0::2] & 0xF
+    hi = codes[:, 1::2] & 0xF
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def unpack_fp4(packed: np.ndarray) -> np.ndarray:
+    """Inverse of pack_fp4: bytes [rows, K/2] -> codes [rows, K]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    out = np.empty((packed.shape[0], packed.shape[1] * 2), dtype=np.uint8)
+    out[:, 0::2] = packed & 0xF
+    out[:, 1::2] = packed >> 4
+    return out
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even) and return the bits.
+
+    Used only to turn the N(0, sigma) draws for C into bf16 input bytes.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    r = r.astype(np.uint16)
+    r[nan] = 0x7FC0
+    return r
+
+
+def _block_scale_exponents(x: np.ndarray) -> np.ndarray:
+    """s = floor(log2(blockmax / 6)) per 1x32 block, 0 for all-zero blocks."""
+    rows, K = x.shape
+    amax = np.abs(x).reshape(rows, K // 32, 32).max(axis=2)
+    _, e = np.frexp(amax / 6.0)           # amax/6 = f * 2^e, f in [0.5, 1)
+    s = (e - 1).astype(np.int64)          # exact floor(log2(.)) for > 0
+    s[amax == 0] = 0
+    return np.clip(s, -127, 127)
+
+
+def _e2m1_codes_rne_sat(y: np.ndarray) -> np.ndarray:
+    """Nearest-even E2M1 magnitude code of |y| with saturation at 6.
+
+    Decision points are the midpoints of {0,.5,1,1.5,2,3,4,6}; a tie goes to
+    the neighbour whose mantissa bit is 0 (codes 0,2,4,6).
+    """
+    a = np.abs(y)
+    code = ((a > 0.25).astype(np.uint8) + (a >= 0.75) + (a > 1.25) + (a >= 1.75)
+            + (a > 2.5) + (a >= 3.5) + (a > 5.0))
+    return code.astype(np.uint8)
+
+
+def quantize_rows(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Quantise float64 rows [rows, K] (K % 32 == 0) to (packed codes, E8M0)."""
+    rows, K = x.shape
+    assert K % 32 == 0
+    s = _block_scale_exponents(x)
+    y = np.ldexp(x.reshape(rows, K // 32, 32), -s[:, :, None]).reshape(rows, K)
+    mag = _e2m1_codes_rne_sat(y)
+    sign = np.signbit(x).astype(np.uint8) << 3
+    codes = mag | sign
+    return pack_fp4(codes), (s + 127).astype(np.uint8)
+
+
+def _quantized_operand(rng: np.random.Generator, rows: int, K: int, dist: str):
+    packed = np.empty((rows, K // 2), dtype=np.uint8)
+    scales = np.empty((rows, K // 32), dtype=np.uint8)
+    for r0 in range(0, rows, _ROW_CHUNK):
+        r1 = min(rows, r0 + _ROW_CHUNK)
+        if dist == "normal":
+            x = rng.standard_normal((r1 - r0, K))
+        elif dist == "uniform":
+            x = rng.uniform(-1.0, 1.0, size=(r1 - r0, K))
+        else:
+            raise ValueError(dist)
+        packed[r0:r1], scales[r0:r1] = quantize_rows(x)
+    return packed, scales
+
+
+def _uniform_code_operand(rng: np.random.Generator, rows: int, K: int):
+    codes = rng.integers(0, 16, size=(rows, K), dtype=np.uint8)
+    scales = (rng.integers(-4, 5, size=(rows, K // 32)) + 127).astype(np.uint8)
+    return pack_fp4(codes), scales
+
+
+def _bf16_normal(rng: np.random.Generator, rows: int, cols: int, sigma: float):
+    out = np.empty((rows, cols), dtype=np.uint16)
+    for r0 in range(0, rows, _ROW_CHUNK):
+        r1 = min(rows, r0 + _ROW_CHUNK)
+        x = sigma * rng.standard_normal((r1 - r0, cols))
+        out[r0:r1] = f32_to_bf16_bits(x.astype(np.float32))
+    return out
+
+
+# name -> (M, N, K, seed, value recipe, alpha, beta, C sigma or None)
+WORKLOADS = {
+    "tiny":   (128, 256, 512, 0, "codes", 1.0, 0.0, None),
+    "decode": (1, 8192, 8192, 1, "normal", 1.0, 0.0, None),
+    "mid":    (512, 1024, 2048, 2, "normal", 0.5, 0.5, 1.0),
+    "large":  (8192, 8192, 8192, 3, "normal", 1.0, 0.0, None),
+    "skinny": (64, 7168, 16384, 4, "uniform", 1.0, 1.0, 0.1),
+}
+
+
+def make_problem(name: str, M: int, N: int, K: int, seed: int, values: str,
+                 alpha: float, beta: float, c_sigma: Optional[float]) -> Problem:
+    """Draw one problem of any shape with one of the workload value recipes."""
+    if K % 32 != 0:
+        raise ValueError("K must be a multiple of 32 (one E8M0 scale per 32)")
+    rng = np.random.default_rng(seed)
+    if values == "codes":
+        A, SA = _uniform_code_operand(rng, M, K)
+        B, SB = _uniform_code_operand(rng, N, K)
+    else:
+        A, SA = _quantized_operand(rng, M, K, values)
+        B, SB = _quantized_operand(rng, N, K, values)
+    C = _bf16_normal(rng, M, N, c_sigma) if c_sigma is not None else None
+    return Problem(name, M, N, K, A, B, SA, SB, C, float(alpha), float(beta), seed)
+
+
+def workload(name: str) -> Problem:
+    M, N, K, seed, values, alpha, beta, c_sigma = WORKLOADS[name]
+    return make_problem(name, M, N, K, seed, values, alpha, beta, c_sigma)
+
+
+def identity_problem(M: int = 128, N: int = 256, K: int = 512, seed: int = 0) -> Problem:
+    """B[n, k] = 1 iff n == k (code 2, scale code 127); A as in 'tiny'.
+
+    With all scales 127 the product is D[m, n] = A[m, n] for n < min(N, K).
+    """
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(M, K), dtype=np.uint8)
+    A = pack_fp4(codes)
+    SA = np.full((M, K // 32), 127, dtype=np.uint8)
+    bcodes = np.zeros((N, K), dtype=np.uint8)
+    idx = np.arange(min(N, K))
+    bcodes[idx, idx] = 2
+    B = pack_fp4(bcodes)
+    SB = np.full((N, K // 32), 127, dtype=np.uint8)
+    return Problem("identity", M, N, K, A, B, SA, SB, None, 1.0, 0.0, seed)

@@ -1,0 +1,195 @@
+"""CPU oracle for the block-scaled MXFP4 GEMM (test infrastructure only).
+
+Only the tests, the package smoke check and the benchmark's CPU-baseline leg
+may import this package; the product path never does.
+
+Two independent exact evaluations of
+
+    D[M,N] (bf16) = alpha * A[M,K] (mxfp4) * B[N,K]^T (mxfp4) + beta * C[M,N]
+
+are offered (page "asm_f4gemm -- driving aiter's gfx950 MXFP4 GEMM code
+objects", sections "Data layouts" and "Verification"):
+
+* ``gemm`` / ``gemm_sampled``: the plain C oracle in ``oracle.c`` (decode each
+  element, accumulate in double in k order, round once to bf16).
+* ``dequant`` + ``acc_numpy``: dequantise with numpy from the page's value
+  list and ``np.ldexp``, then one float64 matrix product (a library routine
+  used as one step).  Both are exact at the test sizes, so their double sums
+  agree bit for bit.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", *GCC_FLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def bind(path: str) -> ctypes.CDLL:
+    """Load a compiled copy of oracle.c and declare its signatures."""
+    L = ctypes.CDLL(path)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    L.oracle_e2m1_value.restype = ctypes.c_double
+    L.oracle_e2m1_value.argtypes = [ctypes.c_uint]
+    L.oracle_e8m0_value.restype = ctypes.c_double
+    L.oracle_e8m0_value.argtypes = [ctypes.c_uint]
+    L.oracle_bf16_rne.restype = ctypes.c_uint16
+    L.oracle_bf16_rne.argtypes = [ctypes.c_double]
+    L.oracle_bf16_to_double.restype = ctypes.c_double
+    L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_fp4_code.restype = ctypes.c_uint
+    L.oracle_fp4_code.argtypes = [u8p, ctypes.c_int64]
+    L.oracle_host_cores.restype = ctypes.c_int
+    L.oracle_host_cores.argtypes = []
+    L.oracle_gemm.restype = i64
+    L.oracle_gemm.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              u8p, i64, u8p, i64, u8p, i64, u8p, i64,
+                              ctypes.c_double, ctypes.c_double, u16p, i64,
+                              u16p, i64, dp, dp, ctypes.c_int]
+    L.oracle_gemm_sampled.restype = i64
+    L.oracle_gemm_sampled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      u8p, i64, u8p, i64, u8p, i64, u8p, i64,
+                                      ctypes.c_double, ctypes.c_double, u16p, i64,
+                                      ctypes.POINTER(ctypes.c_int64), i64,
+                                      u16p, dp, dp, ctypes.c_int]
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = bind(build())
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray], ctype):
+    if a is None:
+        return ctypes.POINTER(ctype)()
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(code)
+
+
+def e8m0_value(code: int) -> float:
+    return lib().oracle_e8m0_value(code)
+
+
+def fp4_code(packed_row: np.ndarray, k: int) -> int:
+    """Code of element k of a packed row, as the oracle unpacks it."""
+    row = np.ascontiguousarray(packed_row, dtype=np.uint8)
+    return int(lib().oracle_fp4_code(_ptr(row, ctypes.c_uint8), int(k)))
+
+
+def bf16_rne(x: float) -> int:
+    return int(lib().oracle_bf16_rne(float(x)))
+
+
+def bf16_to_double(bits: int) -> float:
+    return lib().oracle_bf16_to_double(int(bits))
+
+
+def host_cores() -> int:
+    return lib().oracle_host_cores()
+
+
+def _check_operands(A, B, SA, SB, M, N, K):
+    for name, arr, rows, cols in (("A", A, M, K // 2), ("B", B, N, K // 2),
+                                  ("SA", SA, M, K // 32), ("SB", SB, N, K // 32)):
+        if arr.dtype != np.uint8 or arr.ndim != 2 or arr.shape[0] < rows or arr.shape[1] < cols:
+            raise ValueError(f"{name}: bad shape {arr.shape} / dtype {arr.dtype}")
+
+
+def gemm(A, B, SA, SB, M, N, K, alpha=1.0, beta=0.0, C=None, want_acc=False,
+         nthreads=0):
+    """Full oracle GEMM. Returns (D bf16 bits [M,N], acc or None, sum|ab| [M,N], inexact)."""
+    A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
+    _check_operands(A, B, SA, SB, M, N, K)
+    Cc = None if beta == 0.0 or C is None else np.ascontiguousarray(C, dtype=np.uint16)
+    D = np.zeros((M, N), dtype=np.uint16)
+    acc = np.zeros((M, N), dtype=np.float64) if want_acc else None
+    sabs = np.zeros((M, N), dtype=np.float64)
+    r = lib().oracle_gemm(M, N, K, _ptr(A, ctypes.c_uint8), A.shape[1] * 2,
+                          _ptr(B, ctypes.c_uint8), B.shape[1] * 2,
+                          _ptr(SA, ctypes.c_uint8), SA.shape[1],
+                          _ptr(SB, ctypes.c_uint8), SB.shape[1],
+                          float(alpha), float(beta), _ptr(Cc, ctypes.c_uint16),
+                          0 if Cc is None else Cc.shape[1],
+                          _ptr(D, ctypes.c_uint16), N, _ptr(acc, ctypes.c_double),
+                          _ptr(sabs, ctypes.c_double), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_gemm rejected its arguments")
+    return D, acc, sabs, int(r)
+
+
+def gemm_sampled(A, B, SA, SB, M, N, K, pairs, alpha=1.0, beta=0.0, C=None,
+                 nthreads=0):
+    """Oracle at (m, n) pairs [P, 2]. Returns (D bits [P], acc [P], sum|ab| [P], inexact)."""
+    A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
+    _check_operands(A, B, SA, SB, M, N, K)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    Cc = None if beta == 0.0 or C is None else np.ascontiguousarray(C, dtype=np.uint16)
+    P = pairs.shape[0]
+    D = np.zeros(P, dtype=np.uint16)
+    acc = np.zeros(P, dtype=np.float64)
+    sabs = np.zeros(P, dtype=np.float64)
+    r = lib().oracle_gemm_sampled(M, N, K, _ptr(A, ctypes.c_uint8), A.shape[1] * 2,
+                                  _ptr(B, ctypes.c_uint8), B.shape[1] * 2,
+                                  _ptr(SA, ctypes.c_uint8), SA.shape[1],
+                                  _ptr(SB, ctypes.c_uint8), SB.shape[1],
+                                  float(alpha), float(beta), _ptr(Cc, ctypes.c_uint16),
+                                  0 if Cc is None else Cc.shape[1],
+                                  pairs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), P,
+                                  _ptr(D, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
+                                  _ptr(sabs, ctypes.c_double), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_gemm_sampled rejected its arguments")
+    return D, acc, sabs, int(r)
+
+
+# --- second exact evaluation: numpy dequantisation + one float64 product ----
+
+_E2M1_LIST = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def dequant(packed: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
+    """float64 [rows, K] values: page value list x 2^(e-127) per 1x32 block."""
+    packed = np.asarray(packed, dtype=np.uint8)[:, : K // 2]
+    codes = np.empty((packed.shape[0], K), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    mag = _E2M1_LIST[codes & 7]
+    val = np.where(codes & 8, -mag, mag)
+    e = np.asarray(scales, dtype=np.int64)[:, : K // 32]
+    sc = np.where(e == 255, np.nan, np.ldexp(1.0, (e - 127).astype(np.int32)))
+    return val * np.repeat(sc, 32, axis=1)
+
+
+def acc_numpy(A, B, SA, SB, K) -> np.ndarray:
+    """sum_k a(m,k) b(n,k) as one float64 matmul of the dequantised operands."""
+    return dequant(A, SA, K) @ dequant(B, SB, K).T

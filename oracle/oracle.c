@@ -1,0 +1,328 @@
+/*
+ * Plain CPU oracle for the block-scaled MXFP4 GEMM.
+ *
+ *     D[M,N] (bf16) = alpha * A[M,K] (mxfp4) * B[N,K]^T (mxfp4) + beta * C[M,N]
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * CPU-baseline leg of the benchmark may load this file.  It shares no code,
+ * header, table or helper with the CUDA path.
+ *
+ * It is written from the page "asm_f4gemm -- driving aiter's gfx950 MXFP4
+ * GEMM code objects":
+ *   - the GEMM formula at the top of the page;
+ *   - section "Data layouts": A/B are [rows, K/2] bytes, element 2i in the low
+ *     nibble and 2i+1 in the high nibble, E2M1 magnitudes {0,.5,1,1.5,2,3,4,6}
+ *     with the sign in bit 3; E8M0 value = 2^(e-127), one scale per 32 K;
+ *   - section "Verification": the reference accumulates in double over the
+ *     dequantised operands, and the only error left is the bf16 rounding.
+ * And from the page "CDNA4 dense MFMA builtins", section "Mixed-precision with
+ * scaling": each per-block scale is applied to the inputs before they are
+ * accumulated.
+ *
+ * Steps, in the order the definition gives them:
+ *   1. unpack the nibble of element k (low nibble for even k);
+ *   2. decode it with the page's value list and sign bit;
+ *   3. decode the block's E8M0 scale as 2^(e-127);
+ *   4. accumulate a(m,k) * b(n,k) in double, in k order;
+ *   5. y = alpha * acc + beta * C[m][n] in double;
+ *   6. round y once, straight from double, to bf16 (nearest, ties to even).
+ *
+ * Exactness: every product is an integer multiple of 2^(ea+eb-256) (E2M1
+ * values are multiples of 1/2), so the double sum is exact, in any order,
+ * whenever sum|a*b| / min-granule < 2^52.  The oracle checks that bound for
+ * every output and checks with an exact product/sum test that step 5 did not
+ * round; outputs that fail either check are counted and reported.
+ *
+ * Readings where the pages are silent or at odds:
+ *   - E8M0 code 0: the page writes both 2^(e-127) and "0 -> 2^-126"; the
+ *     formula is taken (code 0 -> 2^-127).  Code 255 decodes to NaN.
+ *   - D is rounded to nearest, ties to even (the MFMA page's rounding mode).
+ *   - C is bf16.  C is not read when beta == 0 (it may be NULL).
+ */
+#define _GNU_SOURCE
+#include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* Step 2: the E2M1 magnitudes in the order the page lists them, indexed by
+ * bits 2..0 of the code; bit 3 is the sign. */
+static const double kE2M1Magnitude[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double oracle_e2m1_value(unsigned code)
+{
+    double mag = kE2M1Magnitude[code & 7u];
+    return (code & 8u) ? -mag : mag;
+}
+
+/* Step 3: E8M0 is a bare biased exponent. */
+double oracle_e8m0_value(unsigned code)
+{
+    code &= 0xFFu;
+    if (code == 0xFFu)
+        return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/* Step 1: element k of a packed row. */
+static unsigned nibble(const uint8_t *row, int64_t k)
+{
+    uint8_t byte = row[k >> 1];
+    return (k & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 0xFu);
+}
+
+/* Exported for the nibble-order check: the code of element k of a row. */
+unsigned oracle_fp4_code(const uint8_t *row, int64_t k)
+{
+    return nibble(row, k);
+}
+
+/* bf16 bits -> double (exact). */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    int sign = bits >> 15;
+    int e = (bits >> 7) & 0xFF;
+    int f = bits & 0x7F;
+    double v;
+    if (e == 0xFF)
+        v = f ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -133);
+    else
+        v = ldexp((double)(128 + f), e - 134);
+    return sign ? -v : v;
+}
+
+/*
+ * Step 6: round a double to the nearest bf16, ties to even, in one step.
+ * bf16 has 8 significand bits and exponents down to 2^-126 (subnormals below
+ * that, spaced 2^-133).  With q the exponent of the spacing at |x|, the
+ * result is n * 2^q for the nearest-even integer n to |x| / 2^q, and its bit
+ * pattern is (q + 133) * 128 + n (this also carries n = 256 into the next
+ * binade and overflows into the infinity pattern 0x7F80).
+ */
+uint16_t oracle_bf16_rne(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a) || a >= 0x1p128)
+        return (uint16_t)(sign | 0x7F80u);
+    int E;
+    frexp(a, &E);                       /* a = f * 2^E, f in [0.5, 1) */
+    int q = (E - 1 > -126 ? E - 1 : -126) - 7;
+    double r = ldexp(a, -q);            /* exact: scaling by a power of two */
+    double n = floor(r);
+    double frac = r - n;                /* exact */
+    if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0))
+        n += 1.0;
+    long bits = (long)(q + 133) * 128L + (long)n;
+    if (bits >= 0x7F80L)
+        return (uint16_t)(sign | 0x7F80u);
+    return (uint16_t)(sign | (uint16_t)bits);
+}
+
+/* Exact-arithmetic checks used for step 5. */
+static int two_sum_exact(double a, double b, double s)
+{
+    double bb = s - a;
+    double err = (a - (s - bb)) + (b - bb);
+    return err == 0.0;
+}
+
+struct gemm_job {
+    int M, N, K;
+    const uint8_t *A; int64_t lda_bytes;
+    const uint8_t *B; int64_t ldb_bytes;
+    const uint8_t *SA; int64_t ldsa;
+    const uint8_t *SB; int64_t ldsb;
+    double alpha, beta;
+    const uint16_t *C; int64_t ldc;
+    uint16_t *D; int64_t ldd;
+    double *acc_out;   /* [M*N] or NULL */
+    double *abs_out;   /* [M*N] or NULL */
+    const int64_t *pairs; int64_t npairs;   /* sampled mode: (m, n) pairs */
+    int64_t next;      /* work counter */
+    pthread_mutex_t lock;
+    int64_t inexact;   /* outputs that failed an exactness check */
+};
+
+/* Steps 1-6 for one output element. */
+static int one_output(struct gemm_job *j, int m, int n, uint16_t *d,
+                      double *acc_o, double *abs_o)
+{
+    const uint8_t *arow = j->A + (int64_t)m * j->lda_bytes;
+    const uint8_t *brow = j->B + (int64_t)n * j->ldb_bytes;
+    const uint8_t *sarow = j->SA + (int64_t)m * j->ldsa;
+    const uint8_t *sbrow = j->SB + (int64_t)n * j->ldsb;
+    double acc = 0.0, sabs = 0.0;
+    int min_g = 1 << 30;               /* min over products of ea+eb-256 */
+    for (int64_t k = 0; k < j->K; ++k) {
+        unsigned ca = nibble(arow, k), cb = nibble(brow, k);
+        unsigned ea = sarow[k / 32], eb = sbrow[k / 32];
+        double a = oracle_e2m1_value(ca) * oracle_e8m0_value(ea);
+        double b = oracle_e2m1_value(cb) * oracle_e8m0_value(eb);
+        double p = a * b;
+        acc += p;
+        sabs += fabs(p);
+        if (p != 0.0) {
+            int g = (int)ea + (int)eb - 256;
+            if (g < min_g)
+                min_g = g;
+        }
+    }
+    int exact = 1;
+    if (sabs != 0.0 && !(isfinite(sabs) && sabs < ldexp(1.0, 52 + min_g)))
+        exact = 0;
+    double y;
+    if (j->beta != 0.0) {
+        double c = oracle_bf16_to_double(j->C[(int64_t)m * j->ldc + n]);
+        double p1 = j->alpha * acc;
+        double p2 = j->beta * c;
+        if (fma(j->alpha, acc, -p1) != 0.0 || fma(j->beta, c, -p2) != 0.0)
+            exact = 0;
+        y = p1 + p2;
+        if (!two_sum_exact(p1, p2, y))
+            exact = 0;
+    } else {
+        y = j->alpha * acc;
+        if (fma(j->alpha, acc, -y) != 0.0)
+            exact = 0;
+    }
+    *d = oracle_bf16_rne(y);
+    if (acc_o)
+        *acc_o = acc;
+    if (abs_o)
+        *abs_o = sabs;
+    return exact;
+}
+
+static void *worker(void *arg)
+{
+    struct gemm_job *j = (struct gemm_job *)arg;
+    int64_t total = j->pairs ? j->npairs : (int64_t)j->M;
+    int64_t local_inexact = 0;
+    for (;;) {
+        pthread_mutex_lock(&j->lock);
+        int64_t i = j->next++;
+        pthread_mutex_unlock(&j->lock);
+        if (i >= total)
+            break;
+        if (j->pairs) {
+            int m = (int)j->pairs[2 * i], n = (int)j->pairs[2 * i + 1];
+            if (!one_output(j, m, n, &j->D[i], j->acc_out ? &j->acc_out[i] : NULL,
+                            j->abs_out ? &j->abs_out[i] : NULL))
+                ++local_inexact;
+        } else {
+            int m = (int)i;
+            for (int n = 0; n < j->N; ++n) {
+                int64_t o = (int64_t)m * j->N + n;
+                if (!one_output(j, m, n, &j->D[(int64_t)m * j->ldd + n],
+                                j->acc_out ? &j->acc_out[o] : NULL,
+                                j->abs_out ? &j->abs_out[o] : NULL))
+                    ++local_inexact;
+            }
+        }
+    }
+    pthread_mutex_lock(&j->lock);
+    j->inexact += local_inexact;
+    pthread_mutex_unlock(&j->lock);
+    return NULL;
+}
+
+/* Threads this process may run on (its CPU affinity set). */
+int oracle_host_cores(void)
+{
+    cpu_set_t set;
+    if (sched_getaffinity(0, sizeof(set), &set) == 0)
+        return CPU_COUNT(&set);
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static int64_t run(struct gemm_job *j, int nthreads)
+{
+    if (nthreads <= 0)
+        nthreads = oracle_host_cores();
+    pthread_mutex_init(&j->lock, NULL);
+    j->next = 0;
+    j->inexact = 0;
+    pthread_t *t = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i)
+        if (pthread_create(&t[i], NULL, worker, j) == 0)
+            ++started;
+    if (started == 0)
+        worker(j);
+    for (int i = 0; i < started; ++i)
+        pthread_join(t[i], NULL);
+    free(t);
+    pthread_mutex_destroy(&j->lock);
+    return j->inexact;
+}
+
+/*
+ * Full GEMM.  A: uint8 [M, lda/2] (lda in fp4 elements, as the page's
+ * kernarg block counts A/B strides), B likewise, SA/SB: uint8 E8M0 with row
+ * strides in bytes, C: bf16 bits [M, ldc] (ignored when beta == 0), D: bf16
+ * bits [M, ldd].  acc_out / abs_out (optional, [M*N] dense) receive the
+ * exact double sum and sum|a*b| per output.  Returns the number of outputs
+ * whose exactness checks failed (0 means every D is the correctly rounded
+ * exact result), or -1 on bad arguments.
+ */
+int64_t oracle_gemm(int M, int N, int K,
+                    const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                    const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                    double alpha, double beta, const uint16_t *C, int64_t ldc,
+                    uint16_t *D, int64_t ldd, double *acc_out, double *abs_out,
+                    int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || (lda & 1) || (ldb & 1))
+        return -1;
+    if (beta != 0.0 && C == NULL)
+        return -1;
+    struct gemm_job j;
+    memset(&j, 0, sizeof(j));
+    j.M = M; j.N = N; j.K = K;
+    j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;
+    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
+    j.D = D; j.ldd = ldd; j.acc_out = acc_out; j.abs_out = abs_out;
+    return run(&j, nthreads);
+}
+
+/*
+ * Sampled GEMM: the same computation at npairs (m, n) positions given as
+ * pairs[2*i], pairs[2*i+1].  D, acc_out and abs_out are indexed by i.
+ */
+int64_t oracle_gemm_sampled(int M, int N, int K,
+                            const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                            const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                            double alpha, double beta, const uint16_t *C, int64_t ldc,
+                            const int64_t *pairs, int64_t npairs,
+                            uint16_t *D, double *acc_out, double *abs_out, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || (lda & 1) || (ldb & 1))
+        return -1;
+    if (beta != 0.0 && C == NULL)
+        return -1;
+    for (int64_t i = 0; i < npairs; ++i)
+        if (pairs[2 * i] < 0 || pairs[2 * i] >= M || pairs[2 * i + 1] < 0 ||
+            pairs[2 * i + 1] >= N)
+            return -1;
+    struct gemm_job j;
+    memset(&j, 0, sizeof(j));
+    j.M = M; j.N = N; j.K = K;
+    j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;
+    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
+    j.D = D; j.ldd = 0; j.acc_out = acc_out; j.abs_out = abs_out;
+    j.pairs = pairs; j.npairs = npairs;
+    return run(&j, nthreads);
+}

@@ -1,0 +1,75 @@
+"""Planted mistakes in the oracle must fail a pin.
+
+Each mutant is a copy of oracle.c with one plausible mistake (a dropped
+term, a wrong sign, index or bias, a transposed operand, a double rounding),
+compiled on the CPU into a temporary library.  The pins of
+test_oracle_pins run against it, and at least one must fail.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "nibble_order_swapped": (
+        "return (k & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 0xFu);",
+        "return (k & 1) ? (unsigned)(byte & 0xFu) : (unsigned)(byte >> 4);"),
+    "sign_bit_wrong": (
+        "return (code & 8u) ? -mag : mag;", "return (code & 4u) ? -mag : mag;"),
+    "table_3_4_swapped": (
+        "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 4.0, 3.0, 6.0}"),
+    "e8m0_bias_off_by_one": (
+        "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 126);"),
+    "scale_b_dropped": (
+        "double b = oracle_e2m1_value(cb) * oracle_e8m0_value(eb);",
+        "double b = oracle_e2m1_value(cb);"),
+    "scale_block_16": (
+        "unsigned ea = sarow[k / 32], eb = sbrow[k / 32];",
+        "unsigned ea = sarow[k / 16], eb = sbrow[k / 32];"),
+    "scale_a_indexed_by_n": (
+        "const uint8_t *sarow = j->SA + (int64_t)m * j->ldsa;",
+        "const uint8_t *sarow = j->SA + (int64_t)(n % j->M) * j->ldsa;"),
+    "last_k_dropped": (
+        "for (int64_t k = 0; k < j->K; ++k) {", "for (int64_t k = 0; k + 1 < j->K; ++k) {"),
+    "beta_term_dropped": ("y = p1 + p2;", "y = p1;"),
+    "alpha_ignored": ("double p1 = j->alpha * acc;", "double p1 = acc;"),
+    "alpha_beta_swapped": (
+        "double p1 = j->alpha * acc;\n        double p2 = j->beta * c;",
+        "double p1 = j->beta * acc;\n        double p2 = j->alpha * c;"),
+    "double_rounding_via_float": (
+        "*d = oracle_bf16_rne(y);", "*d = oracle_bf16_rne((double)(float)y);"),
+    "ties_away_from_zero": (
+        "if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0))", "if (frac >= 0.5)"),
+    "no_subnormal_clamp": (
+        "int q = (E - 1 > -126 ? E - 1 : -126) - 7;", "int q = E - 1 - 7;"),
+    "transposed_d_store": (
+        "if (!one_output(j, m, n, &j->D[(int64_t)m * j->ldd + n],",
+        "if (!one_output(j, m, n, &j->D[(int64_t)(n % j->M) * j->ldd + (m % j->N)],"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, f"mutation site for {name} not found"
+    src = tmp_path / "oracle_mutant.c"
+    src.write_text(source.replace(old, new))
+    so = tmp_path / "liboracle_mutant.so"
+    subprocess.check_call(["gcc", *oracle.GCC_FLAGS, str(src), "-o", str(so), "-lm"])
+    monkeypatch.setattr(oracle, "_lib", oracle.bind(str(so)))
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(oracle)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"mutant {name} passed every pin"

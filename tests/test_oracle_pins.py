@@ -1,0 +1,416 @@
+"""Pins for the CPU oracle: things the pages and the mathematics fix.
+
+Every check here compares the oracle with something other than itself:
+golden values the page prints, closed forms, a brute force in exact rational
+arithmetic with its own decode and its own rounding search, and a library
+float64 matrix product.  ``test_oracle_mutants`` then plants plausible
+mistakes in copies of oracle.c and shows that each one fails a check.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# --- exact references written from the format definitions -----------------
+
+def page_e2m1_values():
+    """E2M1 code -> Fraction, from the page's value list (golden fixture)."""
+    return {int(c): Fraction(v) if v not in ("-0.0",) else Fraction(0)
+            for c, v in read_golden("e2m1_values.txt")}
+
+
+def bf16_bits_to_fraction(bits):
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    v = Fraction(f, 2 ** 133) if e == 0 else Fraction(128 + f) * Fraction(2) ** (e - 134)
+    return -v if bits & 0x8000 else v
+
+
+_BF16_POS = None
+
+
+def bf16_positive_table():
+    """Every non-negative finite bf16 value in increasing order, with its bits."""
+    global _BF16_POS
+    if _BF16_POS is None:
+        _BF16_POS = [(bf16_bits_to_fraction(b), b) for b in range(0x7F80)]
+    return _BF16_POS
+
+
+def bf16_rne_by_search(y: Fraction) -> int:
+    """Nearest bf16 to an exact rational by searching the value set; ties to
+    the neighbour with an even bit pattern; beyond the largest finite value
+    by half a spacing -> infinity."""
+    table = bf16_positive_table()
+    a = abs(y)
+    sign = 0x8000 if y < 0 else 0
+    top = table[-1][0]
+    half_gap = (top - table[-2][0]) / 2
+    if a >= top + half_gap:
+        return sign | 0x7F80
+    lo, hi = 0, len(table) - 1
+    while lo < hi:                      # first entry >= a
+        mid = (lo + hi) // 2
+        if table[mid][0] < a:
+            lo = mid + 1
+        else:
+            hi = mid
+    v_hi, b_hi = table[lo]
+    if v_hi == a or lo == 0:
+        return sign | b_hi
+    v_lo, b_lo = table[lo - 1]
+    d_lo, d_hi = a - v_lo, v_hi - a
+    if d_lo < d_hi:
+        return sign | b_lo
+    if d_hi < d_lo:
+        return sign | b_hi
+    return sign | (b_lo if b_lo % 2 == 0 else b_hi)
+
+
+def page_decode_row(packed_row, K):
+    """Codes of a packed row per the page: element 2i low nibble, 2i+1 high."""
+    codes = []
+    for i in range(K // 2):
+        byte = int(packed_row[i])
+        codes.append(byte & 0xF)
+        codes.append(byte >> 4)
+    return codes
+
+
+def brute_force_gemm(A, B, SA, SB, M, N, K, alpha, beta, C):
+    """Exact rational D (as bf16 bits) from the definition, pure Python."""
+    vals = page_e2m1_values()
+    two = Fraction(2)
+    ra = [page_decode_row(A[m], K) for m in range(M)]
+    rb = [page_decode_row(B[n], K) for n in range(N)]
+    D = np.zeros((M, N), dtype=np.uint16)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                a = vals[ra[m][k]] * two ** (int(SA[m, k // 32]) - 127)
+                b = vals[rb[n][k]] * two ** (int(SB[n, k // 32]) - 127)
+                acc += a * b
+            y = Fraction(alpha) * acc
+            if beta != 0.0:
+                y += Fraction(beta) * bf16_bits_to_fraction(int(C[m, n]))
+            D[m, n] = bf16_rne_by_search(y)
+    return D
+
+
+def same_value(d1, d2):
+    """bf16 bit arrays equal by value (+0 == -0)."""
+    d1 = np.asarray(d1, dtype=np.uint16)
+    d2 = np.asarray(d2, dtype=np.uint16)
+    z1 = (d1 & 0x7FFF) == 0
+    z2 = (d2 & 0x7FFF) == 0
+    return bool(np.all((d1 == d2) | (z1 & z2)))
+
+
+def bf16_to_f64(bits):
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def random_case(rng, M, N, K, scale_lo=120, scale_hi=134):
+    A = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    SA = rng.integers(scale_lo, scale_hi + 1, size=(M, K // 32)).astype(np.uint8)
+    SB = rng.integers(scale_lo, scale_hi + 1, size=(N, K // 32)).astype(np.uint8)
+    # C: bf16 with exponents 2^-8 .. 2^8 (fields 119..135), either sign, so
+    # that alpha * acc + beta * C stays exact in double at these sizes.
+    e = rng.integers(119, 136, size=(M, N)).astype(np.uint16)
+    f = rng.integers(0, 128, size=(M, N)).astype(np.uint16)
+    sgn = rng.integers(0, 2, size=(M, N)).astype(np.uint16)
+    C = (sgn << 15) | (e << 7) | f
+    return A, B, SA, SB, C
+
+
+# --- check functions (shared with the mutant test) -------------------------
+
+def check_e2m1_golden(o):
+    for code, v in read_golden("e2m1_values.txt"):
+        got = o.e2m1_value(int(code))
+        assert got == float(v) and math.copysign(1, got) == math.copysign(1, float(v)), code
+
+
+def check_e2m1_bitfields(o):
+    # OCP E2M1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0;
+    # exponent 0 is subnormal: m * 0.5.
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        v = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + m / 2)
+        assert o.e2m1_value(code) == (-v if s else v)
+
+
+def check_e8m0(o):
+    for code, v in read_golden("e8m0_values.txt"):
+        got = o.e8m0_value(int(code, 16))
+        if v == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(v), code
+    for e in range(1, 255):
+        assert o.e8m0_value(e) == math.ldexp(1.0, e - 127)
+
+
+def check_nibble_order(o):
+    for byte, even, odd in read_golden("nibble_order.txt"):
+        row = np.array([0x00, int(byte, 16), 0x00], dtype=np.uint8)
+        assert o.fp4_code(row, 2) == int(even)
+        assert o.fp4_code(row, 3) == int(odd)
+
+
+def check_bf16_golden(o):
+    for hx, bits, *_ in read_golden("bf16_rounding.txt"):
+        assert o.bf16_rne(float.fromhex(hx)) == int(bits, 16), hx
+
+
+def check_bf16_roundtrip(o):
+    for b in range(0, 0x10000, 7):
+        if (b & 0x7F80) == 0x7F80 and (b & 0x7F):
+            continue                                 # NaN patterns
+        assert o.bf16_rne(o.bf16_to_double(b)) == b, hex(b)
+
+
+def check_bf16_midpoints(o, n=3000):
+    rng = np.random.default_rng(11)
+    for b in rng.integers(1, 0x7F7F, size=n):
+        b = int(b)
+        lo, hi = bf16_bits_to_fraction(b), bf16_bits_to_fraction(b + 1)
+        mid = (lo + hi) / 2
+        want = b if b % 2 == 0 else b + 1
+        assert o.bf16_rne(float(mid)) == want
+        eps = (hi - lo) / 1024
+        assert o.bf16_rne(float(mid - eps)) == b
+        assert o.bf16_rne(float(mid + eps)) == b + 1
+
+
+def check_identity(o):
+    from block_scaled_mxfp4_gb300 import inputs
+    p = inputs.identity_problem()
+    D, _, _, inexact = o.gemm(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K)
+    assert inexact == 0
+    vals = page_e2m1_values()
+    for m in range(p.M):
+        codes = page_decode_row(p.A[m], p.K)
+        want = np.array([float(vals[codes[n]]) for n in range(p.N)])
+        assert np.array_equal(bf16_to_f64(D[m]), want), m
+
+
+def check_identity_scaled(o):
+    # B = I with unit scales, A with random scales: D[m,n] = a(m, n) exactly.
+    from block_scaled_mxfp4_gb300 import inputs
+    rng = np.random.default_rng(5)
+    p = inputs.identity_problem(M=8, N=64, K=64, seed=5)
+    SA = rng.integers(120, 135, size=(8, 2)).astype(np.uint8)
+    D, _, _, _ = o.gemm(p.A, p.B, SA, p.SB, 8, 64, 64)
+    vals = page_e2m1_values()
+    for m in range(8):
+        codes = page_decode_row(p.A[m], 64)
+        want = [float(vals[codes[n]] * Fraction(2) ** (int(SA[m, n // 32]) - 127))
+                for n in range(64)]
+        assert np.array_equal(bf16_to_f64(D[m]), np.array(want))
+
+
+def check_alpha_beta(o):
+    rng = np.random.default_rng(3)
+    M, N, K = 6, 10, 64
+    A, B, SA, SB, C = random_case(rng, M, N, K)
+    zeroA = np.zeros_like(A)
+    # A = 0: D = round(beta * C); beta = 2^-1 keeps it exact.
+    D, _, _, _ = o.gemm(zeroA, B, SA, SB, M, N, K, alpha=1.0, beta=0.5, C=C)
+    want = np.array([[o.bf16_rne(0.5 * o.bf16_to_double(int(c))) for c in row] for row in C])
+    assert same_value(D, want)
+    # alpha = 0, beta = 1: D = C.
+    D, _, _, _ = o.gemm(A, B, SA, SB, M, N, K, alpha=0.0, beta=1.0, C=C)
+    assert same_value(D, C)
+    # D(alpha = 2^j) = 2^j * D(alpha = 1) away from overflow / subnormals.
+    D1, acc, _, _ = o.gemm(A, B, SA, SB, M, N, K, alpha=1.0, want_acc=True)
+    D8, _, _, _ = o.gemm(A, B, SA, SB, M, N, K, alpha=8.0)
+    assert np.array_equal(bf16_to_f64(D8), 8.0 * bf16_to_f64(D1))
+    # beta = 0 never reads C, even if it holds NaN.
+    Cnan = np.full((M, N), 0x7FC0, dtype=np.uint16)
+    D0, _, _, _ = o.gemm(A, B, SA, SB, M, N, K, alpha=1.0, beta=0.0, C=Cnan)
+    assert same_value(D0, D1)
+    # beta = 1, alpha = 1 adds C (exact here): D = round(acc + C).
+    D2, _, _, inexact = o.gemm(A, B, SA, SB, M, N, K, alpha=1.0, beta=1.0, C=C)
+    want = np.array([[o.bf16_rne(acc[m, n] + o.bf16_to_double(int(C[m, n])))
+                      for n in range(N)] for m in range(M)])
+    assert same_value(D2, want)
+
+
+def check_brute_force(o, cases=24):
+    rng = np.random.default_rng(2024)
+    shapes = [(1, 1, 32), (2, 3, 64), (3, 2, 96), (4, 4, 32), (1, 4, 128), (4, 1, 64)]
+    for i in range(cases):
+        M, N, K = shapes[i % len(shapes)]
+        A, B, SA, SB, C = random_case(rng, M, N, K)
+        alpha = [1.0, 0.5, -2.0, 0.75][i % 4]
+        beta = [0.0, 1.0, 0.5, -0.25][(i // 4) % 4]
+        D, _, _, inexact = o.gemm(A, B, SA, SB, M, N, K, alpha=alpha, beta=beta, C=C)
+        assert inexact == 0, (i, M, N, K)
+        want = brute_force_gemm(A, B, SA, SB, M, N, K, alpha, beta, C)
+        assert same_value(D, want), (i, M, N, K)
+
+
+def check_all_code_pairs(o):
+    # K = 32: A row m holds code ca at k = 0, B row n holds code cb at k = 0;
+    # every (ca, cb) pair and several scale pairs; D = round(va*vb*2^(ea+eb-254)).
+    vals = page_e2m1_values()
+    M = N = 16
+    K = 32
+    A = np.zeros((M, K // 2), dtype=np.uint8)
+    B = np.zeros((N, K // 2), dtype=np.uint8)
+    A[:, 0] = np.arange(16, dtype=np.uint8)          # element 0 = code m
+    B[:, 0] = np.arange(16, dtype=np.uint8)
+    for ea, eb in ((127, 127), (125, 131), (140, 100), (1, 254), (60, 60)):
+        SA = np.full((M, 1), ea, dtype=np.uint8)
+        SB = np.full((N, 1), eb, dtype=np.uint8)
+        D, _, _, _ = o.gemm(A, B, SA, SB, M, N, K)
+        for ca in range(16):
+            for cb in range(16):
+                y = vals[ca] * vals[cb] * Fraction(2) ** (ea + eb - 254)
+                assert same_value([D[ca, cb]], [bf16_rne_by_search(y)]), (ca, cb, ea, eb)
+
+
+def check_numpy_crosscheck(o):
+    from block_scaled_mxfp4_gb300 import inputs
+    for name in ("tiny",):
+        p = inputs.workload(name)
+        _, acc, _, inexact = o.gemm(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, want_acc=True)
+        assert inexact == 0
+        assert np.array_equal(acc, o.acc_numpy(p.A, p.B, p.SA, p.SB, p.K))
+    rng = np.random.default_rng(9)
+    A, B, SA, SB, _ = random_case(rng, 37, 29, 320)
+    _, acc, _, inexact = o.gemm(A, B, SA, SB, 37, 29, 320, want_acc=True)
+    assert inexact == 0
+    assert np.array_equal(acc, o.acc_numpy(A, B, SA, SB, 320))
+
+
+def check_rounding_is_only_error(o):
+    # The page reports max_rel_err 0.003891 without split-K: one bf16
+    # rounding of the exact result, whose worst case is 1/257.
+    (_, page_val), = read_golden("verification_error.txt")
+    worst = Fraction(1, 257)
+    assert round(float(worst), 6) == float(page_val)
+    x = 1.0 + 2.0 ** -8
+    assert abs(o.bf16_to_double(o.bf16_rne(x)) - x) / x == float(worst)
+    rng = np.random.default_rng(21)
+    A, B, SA, SB, _ = random_case(rng, 24, 40, 256)
+    D, acc, _, _ = o.gemm(A, B, SA, SB, 24, 40, 256, want_acc=True)
+    nz = acc != 0
+    rel = np.abs(bf16_to_f64(D)[nz] - acc[nz]) / np.abs(acc[nz])
+    assert rel.max() <= float(worst)
+
+
+def check_sampled_matches_full(o):
+    rng = np.random.default_rng(4)
+    M, N, K = 9, 13, 96
+    A, B, SA, SB, C = random_case(rng, M, N, K)
+    D, acc, sabs, _ = o.gemm(A, B, SA, SB, M, N, K, alpha=0.5, beta=1.0, C=C, want_acc=True)
+    pairs = np.array([(m, n) for m in range(M) for n in range(N)])[::3]
+    Ds, accs, sabss, _ = o.gemm_sampled(A, B, SA, SB, M, N, K, pairs, alpha=0.5, beta=1.0, C=C)
+    assert np.array_equal(Ds, D[pairs[:, 0], pairs[:, 1]])
+    assert np.array_equal(accs, acc[pairs[:, 0], pairs[:, 1]])
+    assert np.array_equal(sabss, sabs[pairs[:, 0], pairs[:, 1]])
+
+
+def check_gemm_single_rounding(o):
+    # Three 32-blocks whose products sum to 1 + 2^-8 + 2^-26: just above the
+    # bf16 tie between 1 and 1 + 2^-7, so one rounding gives 1 + 2^-7, while
+    # a float intermediate would land on the tie and give 1.0.
+    K = 96
+    A = np.zeros((1, K // 2), dtype=np.uint8)
+    B = np.zeros((1, K // 2), dtype=np.uint8)
+    for blk in range(3):
+        A[0, blk * 16] = 0x02                 # element 32*blk = 1.0
+        B[0, blk * 16] = 0x02
+    SA = np.array([[127, 119, 114]], dtype=np.uint8)
+    SB = np.array([[127, 127, 114]], dtype=np.uint8)
+    D, acc, _, inexact = o.gemm(A, B, SA, SB, 1, 1, K, want_acc=True)
+    exact = Fraction(1) + Fraction(1, 2 ** 8) + Fraction(1, 2 ** 26)
+    assert inexact == 0 and acc[0, 0] == float(exact)
+    assert int(D[0, 0]) == bf16_rne_by_search(exact) == 0x3F81
+
+
+ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
+              check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
+              check_identity, check_identity_scaled, check_alpha_beta,
+              check_brute_force, check_all_code_pairs, check_numpy_crosscheck,
+              check_rounding_is_only_error, check_sampled_matches_full]
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(oracle_mod, check):
+    check(oracle_mod)
+
+
+def test_exactness_violation_is_reported(oracle_mod):
+    # Scales 2^-126 and 2^127 in one row make sum|ab| / granule exceed 2^52:
+    # the double sum may round, and the oracle must say so.
+    K = 64
+    A = np.full((1, K // 2), 0x77, dtype=np.uint8)       # all 6.0
+    B = np.full((1, K // 2), 0x11, dtype=np.uint8)       # all 0.5
+    SA = np.array([[1, 254]], dtype=np.uint8)
+    SB = np.array([[127, 127]], dtype=np.uint8)
+    _, _, _, inexact = oracle_mod.gemm(A, B, SA, SB, 1, 1, K)
+    assert inexact == 1
+    # A non-dyadic alpha makes alpha * acc round in double: reported too.
+    SA2 = np.array([[127, 127]], dtype=np.uint8)
+    _, _, _, inexact = oracle_mod.gemm(A, B, SA2, SB, 1, 1, K, alpha=0.1)
+    assert inexact == 1
+    _, _, _, inexact = oracle_mod.gemm(A, B, SA2, SB, 1, 1, K, alpha=0.5)
+    assert inexact == 0
+
+
+def test_inexact_outputs_are_flagged_and_within_one_ulp(oracle_mod):
+    # beta * C many binades below alpha * acc: y = p1 + p2 rounds in double,
+    # the oracle must flag it, and it is still within 1 bf16 ulp of exact.
+    rng = np.random.default_rng(77)
+    M, N, K = 4, 4, 32
+    A, B, SA, SB, _ = random_case(rng, M, N, K)
+    C = np.full((M, N), 0x0301, dtype=np.uint16)         # ~2^-120
+    D, _, _, inexact = oracle_mod.gemm(A, B, SA, SB, M, N, K, alpha=0.75, beta=-0.25, C=C)
+    assert inexact > 0
+    want = brute_force_gemm(A, B, SA, SB, M, N, K, 0.75, -0.25, C)
+    assert np.all(np.abs(D.astype(np.int64) - want.astype(np.int64)) <= 1)
+
+
+def test_rejects_bad_arguments(oracle_mod):
+    A = np.zeros((2, 16), dtype=np.uint8)
+    S = np.full((2, 1), 127, dtype=np.uint8)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm(A, A, S, S, 2, 2, 33)                 # K % 32 != 0
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_sampled(A, A, S, S, 2, 2, 32, [(2, 0)])  # m out of range
+
+
+def test_workload_generator_rules():
+    """The generator follows the stated recipe (scale rule, saturation, RNE)."""
+    from block_scaled_mxfp4_gb300 import inputs
+    vals = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    # Ties go to the even mantissa, large values saturate.
+    y = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 100.0, 0.2, 0.3])
+    want = [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, 6.0, 0.0, 0.5]
+    got = [vals[c] for c in inputs._e2m1_codes_rne_sat(y)]
+    assert got == want
+    # Scale exponent floor(log2(amax/6)); the block max saturates to 6.
+    x = np.zeros((1, 32))
+    x[0, 3] = -13.0                      # 13/6 in [2, 4): s = 1, 13/2 = 6.5 -> 6
+    x[0, 4] = 1.0                        # 1/2 = 0.5 -> code 1
+    packed, sc = inputs.quantize_rows(x)
+    assert sc[0, 0] == 128
+    codes = inputs.unpack_fp4(packed)[0]
+    assert codes[3] == 8 | 7 and codes[4] == 1 and codes[0] == 0
+    # Same seed -> same bytes.
+    p1, p2 = inputs.workload("tiny"), inputs.workload("tiny")
+    assert np.array_equal(p1.A, p2.A) and np.array_equal(p1.SB, p2.SB)
+    assert p1.SA.min() >= 123 and p1.SA.max() <= 131

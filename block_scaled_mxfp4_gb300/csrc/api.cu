@@ -1,0 +1,521 @@
+// C ABI of the block-scaled MXFP4 GEMM: argument checks, the tile / split-K
+// plan, TMA tensor maps and the launch sequence (scale relayout -> GEMM ->
+// optional split-K reduce).  Declared in include/mxfp4_gemm.h.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/mxfp4_gemm.h"
+#include "internal.h"
+
+using namespace mxfp4;
+
+namespace {
+
+constexpr int kMaxSplit = 16;
+constexpr int kDefaultSms = 152;
+constexpr size_t kAlign = 256;
+
+std::atomic<long long> g_wait_limit{1LL << 32};
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct DeviceInfo {
+    bool valid = false;
+    bool sm103 = false;
+    int sms = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+// Current device's properties, cached; nullptr if no device is usable.
+const DeviceInfo *current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.valid) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        d.sm103 = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.valid = true;
+    }
+    return &d;
+}
+
+int device_sms_or_default()
+{
+    const DeviceInfo *d = current_device();
+    return (d && d->sms > 0) ? d->sms : kDefaultSms;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D uint8 view [rows, K/2] of a packed operand with row stride ld/2 bytes;
+// box 128 bytes x box_rows, 128-byte swizzle, zero fill out of bounds.
+bool encode_operand(CUtensorMap *map, const void *base, int rows, int K, int64_t ld, int box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld / 2)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Candidate {
+    int tile_n;
+    int stages;
+    int ctas_per_sm;
+};
+
+// Tile / swap / split-K choice.  Candidates are scored as the page's section
+// "Tile selection heuristic" scores its tiles: fewest waves (ceil(tiles /
+// resident CTA slots)), then the fullest last wave, then the larger
+// tile_m*tile_n/(tile_m+tile_n); the fixed candidate order breaks ties.
+// When the tiles do not fill the resident slots, K is split so they do
+// (at least kMinKtPerSplit stages per split, at most 16 splits).
+int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape)
+{
+    if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_req < 0 || split_req > kMaxSplit)
+        return MXFP4_ERR_INVALID_ARG;
+    if (sms <= 0)
+        sms = kDefaultSms;
+    const int swap = (M <= 64 && N > M) ? 1 : 0;
+    const int64_t P = swap ? N : M;
+    const int64_t Q = swap ? M : N;
+    const int kt = (K + kTileK - 1) / kTileK;
+
+    Candidate cands[3];
+    int nc = 0;
+    if (swap) {
+        cands[nc++] = {64, 4, 2};
+    } else {
+        cands[nc++] = {256, 4, 1};
+        cands[nc++] = {128, 6, 1};
+        if (Q <= 64)
+            cands[nc++] = {64, 8, 1};
+    }
+    int best = -1;
+    int64_t best_waves = 0;
+    double best_occ = 0, best_ratio = 0;
+    for (int i = 0; i < nc; ++i) {
+        const int64_t tiles = ((P + kTileM - 1) / kTileM) * ((Q + cands[i].tile_n - 1) / cands[i].tile_n);
+        const int64_t slots = static_cast<int64_t>(sms) * cands[i].ctas_per_sm;
+        const int64_t waves = (tiles + slots - 1) / slots;
+        const double occ = static_cast<double>(tiles) / static_cast<double>(waves * slots);
+        const double ratio = static_cast<double>(kTileM * cands[i].tile_n) / (kTileM + cands[i].tile_n);
+        bool better = best < 0 || waves < best_waves ||
+                      (waves == best_waves && (occ > best_occ + 1e-12 ||
+                                               (occ > best_occ - 1e-12 && ratio > best_ratio)));
+        if (better) {
+            best = i;
+            best_waves = waves;
+            best_occ = occ;
+            best_ratio = ratio;
+        }
+    }
+    const Candidate c = cands[best];
+    const int64_t gx = (P + kTileM - 1) / kTileM;
+    const int64_t gy = (Q + c.tile_n - 1) / c.tile_n;
+    if (gy > 65535 || gx > 0x7FFFFFFF)
+        return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    const int64_t tiles = gx * gy;
+    const int64_t slots = static_cast<int64_t>(sms) * c.ctas_per_sm;
+
+    int split = 1;
+    if (split_req > 0) {
+        split = split_req;
+    } else if (tiles < slots) {
+        const int kMinKtPerSplit = swap ? 4 : 4;
+        int64_t s = slots / tiles;
+        if (s > kMaxSplit)
+            s = kMaxSplit;
+        if (s > kt / kMinKtPerSplit)
+            s = kt / kMinKtPerSplit;
+        split = s < 1 ? 1 : static_cast<int>(s);
+    }
+    if (split > kt)
+        split = kt;
+    const int per = (kt + split - 1) / split;
+    split = (kt + per - 1) / per;   // every split gets >= 1 stage
+
+    out->swap_ab = swap;
+    out->tile_m = kTileM;
+    out->tile_n = c.tile_n;
+    out->tile_k = kTileK;
+    out->stages = c.stages;
+    out->split_k = split;
+    out->k_tiles_per_split = per;
+    out->grid_x = static_cast<int>(gx);
+    out->grid_y = static_cast<int>(gy);
+    out->grid_z = split;
+    out->workspace_bytes =
+        split > 1 ? align_up(static_cast<size_t>(split) * static_cast<size_t>(M) *
+                             static_cast<size_t>(N) * sizeof(float))
+                  : 0;
+    if (shape) {
+        shape->tile_n = c.tile_n;
+        shape->stages = c.stages;
+        shape->swap = swap;
+    }
+    return MXFP4_OK;
+}
+
+int check_device()
+{
+    const DeviceInfo *d = current_device();
+    if (!d)
+        return MXFP4_ERR_CUDA;
+    return d->sm103 ? MXFP4_OK : MXFP4_ERR_ARCH;
+}
+
+int check_common(const void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+                 const void *B, int64_t ldb, float beta, int M, int N, int K, int split_k)
+{
+    if (!D || !A || !B)
+        return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_k < 0 || split_k > kMaxSplit)
+        return MXFP4_ERR_INVALID_ARG;
+    if (lda < K || ldb < K || ldd < N)
+        return MXFP4_ERR_INVALID_ARG;
+    if (beta != 0.0f && (!C || ldc < N))
+        return MXFP4_ERR_INVALID_ARG;
+    if ((lda % 32) != 0 || (ldb % 32) != 0 || !aligned(A, 16) || !aligned(B, 16))
+        return MXFP4_ERR_MISALIGNED;
+    return MXFP4_OK;
+}
+
+// Scale relayout (if needed) has been done; run the GEMM (+ reduce).
+int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+             const void *B, int64_t ldb, const uint8_t *sfA, const uint8_t *sfB, float alpha,
+             float beta, int M, int N, int K, const mxfp4_plan &plan, const GemmShape &shape,
+             float *partials, int sms, cudaStream_t stream)
+{
+    const bool swap = shape.swap != 0;
+    CUtensorMap tmP, tmQ;
+    const void *Pp = swap ? B : A;
+    const void *Qp = swap ? A : B;
+    const int Prows = swap ? N : M, Qrows = swap ? M : N;
+    const int64_t ldP = swap ? ldb : lda, ldQ = swap ? lda : ldb;
+    if (!encode_operand(&tmP, Pp, Prows, K, ldP, kTileM) ||
+        !encode_operand(&tmQ, Qp, Qrows, K, ldQ, shape.tile_n))
+        return MXFP4_ERR_CUDA;
+
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.sfP = swap ? sfB : sfA;
+    a.sfQ = swap ? sfA : sfB;
+    a.sf_rb_stride = sf_groups(K) * kSfAtomBytes;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.kt_total = (K + kTileK - 1) / kTileK;
+    a.kt_per_split = plan.k_tiles_per_split;
+    a.split_k = plan.split_k;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.C = static_cast<const uint16_t *>(beta != 0.0f ? C : nullptr);
+    a.ldc = ldc;
+    a.D = static_cast<uint16_t *>(D);
+    a.ldd = ldd;
+    a.ws = partials;
+    a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
+               (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
+    a.stream_p = swap ? 1 : 0;
+    a.wait_limit = g_wait_limit.load();
+
+    dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
+    if (launch_gemm(a, tmP, tmQ, shape, grid, stream) != cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    if (plan.split_k > 1) {
+        if (launch_splitk_reduce(partials, plan.split_k, M, N, alpha, beta, a.C, ldc, a.D, ldd, sms,
+                                 stream) != cudaSuccess)
+            return MXFP4_ERR_CUDA;
+    }
+    return MXFP4_OK;
+}
+
+struct Layout {
+    size_t sfa, sfb, partials, total;
+};
+
+Layout workspace_layout(int M, int N, int K, const mxfp4_plan &plan)
+{
+    Layout l;
+    l.sfa = 0;
+    l.sfb = align_up(sf_relaid_bytes(M, K));
+    l.partials = l.sfb + align_up(sf_relaid_bytes(N, K));
+    l.total = l.partials + plan.workspace_bytes;
+    return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char *mxfp4_strerror(int status)
+{
+    switch (status) {
+    case MXFP4_OK: return "ok";
+    case MXFP4_ERR_INVALID_ARG: return "invalid argument";
+    case MXFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MXFP4_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case MXFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    case MXFP4_ERR_CUDA: return "CUDA runtime error";
+    case MXFP4_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case MXFP4_ERR_ARCH: return "device is not sm_103";
+    default: return "unknown status";
+    }
+}
+
+void mxfp4_set_wait_limit(long long cycles) { g_wait_limit.store(cycles > 0 ? cycles : 1); }
+
+int mxfp4_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out)
+{
+    if (!out)
+        return MXFP4_ERR_INVALID_ARG;
+    if (num_sms <= 0)
+        num_sms = device_sms_or_default();
+    return make_plan(M, N, K, split_k, num_sms, out, nullptr);
+}
+
+size_t mxfp4_scale_relayout_size(int rows, int K)
+{
+    if (rows < 1 || K < 32 || (K % 32) != 0)
+        return 0;
+    return sf_relaid_bytes(rows, K);
+}
+
+size_t mxfp4_gemm_prepacked_workspace_size(int M, int N, int K, int split_k)
+{
+    mxfp4_plan plan;
+    if (make_plan(M, N, K, split_k, device_sms_or_default(), &plan, nullptr) != MXFP4_OK)
+        return 0;
+    return plan.workspace_bytes;
+}
+
+size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k)
+{
+    mxfp4_plan plan;
+    if (make_plan(M, N, K, split_k, device_sms_or_default(), &plan, nullptr) != MXFP4_OK)
+        return 0;
+    return workspace_layout(M, N, K, plan).total;
+}
+
+int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld_src, void *stream)
+{
+    if (!dst || !src || rows < 1 || K < 32 || (K % 32) != 0 || ld_src < K / 32)
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(dst, 16))
+        return MXFP4_ERR_MISALIGNED;
+    if (sf_row_blocks(rows) > 0x7FFFFFFF)
+        return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    if (launch_scale_relayout(static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src), rows, K,
+                              ld_src, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    return MXFP4_OK;
+}
+
+int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
+                         int64_t lda, const void *B, int64_t ldb, const void *scaleA_relaid,
+                         const void *scaleB_relaid, float alpha, float beta, int M, int N, int K,
+                         int split_k, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int st = check_common(D, ldd, C, ldc, A, lda, B, ldb, beta, M, N, K, split_k);
+    if (st != MXFP4_OK)
+        return st;
+    if (!scaleA_relaid || !scaleB_relaid)
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(scaleA_relaid, 16) || !aligned(scaleB_relaid, 16))
+        return MXFP4_ERR_MISALIGNED;
+    st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    const int sms = device_sms_or_default();
+    mxfp4_plan plan;
+    GemmShape shape;
+    st = make_plan(M, N, K, split_k, sms, &plan, &shape);
+    if (st != MXFP4_OK)
+        return st;
+    if (plan.workspace_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.workspace_bytes)
+            return MXFP4_ERR_WORKSPACE;
+        if (!aligned(workspace, kAlign))
+            return MXFP4_ERR_MISALIGNED;
+    }
+    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, static_cast<const uint8_t *>(scaleA_relaid),
+                    static_cast<const uint8_t *>(scaleB_relaid), alpha, beta, M, N, K, plan, shape,
+                    static_cast<float *>(workspace), sms, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+               const void *B, int64_t ldb, const void *scaleA, int64_t ld_sa, const void *scaleB,
+               int64_t ld_sb, float alpha, float beta, int M, int N, int K, int split_k,
+               void *workspace, size_t workspace_bytes, void *stream)
+{
+    int st = check_common(D, ldd, C, ldc, A, lda, B, ldb, beta, M, N, K, split_k);
+    if (st != MXFP4_OK)
+        return st;
+    if (!scaleA || !scaleB || ld_sa < K / 32 || ld_sb < K / 32)
+        return MXFP4_ERR_INVALID_ARG;
+    if (!workspace)
+        return MXFP4_ERR_WORKSPACE;
+    if (!aligned(workspace, kAlign))
+        return MXFP4_ERR_MISALIGNED;
+    st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    const int sms = device_sms_or_default();
+    mxfp4_plan plan;
+    GemmShape shape;
+    st = make_plan(M, N, K, split_k, sms, &plan, &shape);
+    if (st != MXFP4_OK)
+        return st;
+    const Layout l = workspace_layout(M, N, K, plan);
+    if (workspace_bytes < l.total)
+        return MXFP4_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_scale_relayout(ws + l.sfa, static_cast<const uint8_t *>(scaleA), M, K, ld_sa, s) !=
+            cudaSuccess ||
+        launch_scale_relayout(ws + l.sfb, static_cast<const uint8_t *>(scaleB), N, K, ld_sb, s) !=
+            cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, ws + l.sfa, ws + l.sfb, alpha, beta, M, N, K,
+                    plan, shape, reinterpret_cast<float *>(ws + l.partials), sms, s);
+}
+
+size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
+{
+    const size_t ws = mxfp4_gemm_workspace_size(M, N, K, split_k);
+    if (ws == 0)
+        return 0;
+    const size_t mn2 = align_up(static_cast<size_t>(M) * N * 2);
+    return align_up(static_cast<size_t>(M) * K / 2) + align_up(static_cast<size_t>(N) * K / 2) +
+           align_up(static_cast<size_t>(M) * K / 32) + align_up(static_cast<size_t>(N) * K / 32) +
+           (with_c ? mn2 : 0) + mn2 + ws;
+}
+
+int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
+                    const void *scaleA_host, const void *scaleB_host, float alpha, float beta,
+                    int M, int N, int K, int split_k, void *device_arena, size_t arena_bytes,
+                    void *stream)
+{
+    if (!D_host || !A_host || !B_host || !scaleA_host || !scaleB_host || !device_arena)
+        return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_k < 0 || split_k > kMaxSplit)
+        return MXFP4_ERR_INVALID_ARG;
+    if (beta != 0.0f && !C_host)
+        return MXFP4_ERR_INVALID_ARG;
+    if ((K % 32) != 0)
+        return MXFP4_ERR_MISALIGNED;
+    if (!aligned(device_arena, kAlign))
+        return MXFP4_ERR_MISALIGNED;
+    const int with_c = beta != 0.0f;
+    const size_t need = mxfp4_gemm_host_arena_size(M, N, K, split_k, with_c);
+    if (need == 0 || arena_bytes < need)
+        return MXFP4_ERR_WORKSPACE;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    uint8_t *p = static_cast<uint8_t *>(device_arena);
+    const size_t a_b = static_cast<size_t>(M) * K / 2, b_b = static_cast<size_t>(N) * K / 2;
+    const size_t sa_b = static_cast<size_t>(M) * K / 32, sb_b = static_cast<size_t>(N) * K / 32;
+    const size_t mn2 = static_cast<size_t>(M) * N * 2;
+    uint8_t *dA = p;
+    p += align_up(a_b);
+    uint8_t *dB = p;
+    p += align_up(b_b);
+    uint8_t *dSA = p;
+    p += align_up(sa_b);
+    uint8_t *dSB = p;
+    p += align_up(sb_b);
+    uint8_t *dC = nullptr;
+    if (with_c) {
+        dC = p;
+        p += align_up(mn2);
+    }
+    uint8_t *dD = p;
+    p += align_up(mn2);
+    uint8_t *ws = p;
+    const size_t ws_bytes = arena_bytes - static_cast<size_t>(p - static_cast<uint8_t *>(device_arena));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dA, A_host, a_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dB, B_host, b_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dSA, scaleA_host, sa_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dSB, scaleB_host, sb_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        (with_c && cudaMemcpyAsync(dC, C_host, mn2, cudaMemcpyHostToDevice, s) != cudaSuccess))
+        return MXFP4_ERR_CUDA;
+    st = mxfp4_gemm(dD, N, dC, N, dA, K, dB, K, dSA, K / 32, dSB, K / 32, alpha, beta, M, N, K,
+                    split_k, ws, ws_bytes, stream);
+    if (st != MXFP4_OK)
+        return st;
+    if (cudaMemcpyAsync(D_host, dD, mn2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    return MXFP4_OK;
+}
+
+int mxfp4_device_status(int *status, int reset)
+{
+    if (!status)
+        return MXFP4_ERR_INVALID_ARG;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    return read_device_status(status, reset) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream)
+{
+    if (limit_cycles <= 0)
+        return MXFP4_ERR_INVALID_ARG;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    return launch_wait_probe(limit_cycles, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
+}  // extern "C"

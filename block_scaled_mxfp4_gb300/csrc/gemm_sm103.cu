@@ -1,0 +1,407 @@
+// Block-scaled MXFP4 GEMM on sm_103a tensor cores (tcgen05 kind::mxf4).
+//
+//   D[M,N] = alpha * A[M,K] . B[N,K]^T + beta * C[M,N]          (page "asm_f4gemm
+//   -- driving aiter's gfx950 MXFP4 GEMM code objects", formula and section
+//   "Data layouts"; each E8M0 scale multiplies its 32 inputs before they are
+//   accumulated, page "CDNA4 dense MFMA builtins", section "Mixed-precision
+//   with scaling").
+//
+// One CTA computes one 128 x BN output tile over a range of K (a split):
+//   warp 4  TMA producer: per 256-K stage, one 128x128-byte tile of P, one
+//           BNx128-byte tile of Q (128-byte swizzle), and the stage's relaid
+//           scale atoms by 1-D bulk copy, into an S-stage shared-memory ring
+//           guarded by full/empty mbarriers;
+//   warp 5  allocates tensor memory; one thread copies the stage's scales into
+//           TMEM (tcgen05.cp) and issues four K=64 block-scaled MMAs into an
+//           fp32 TMEM accumulator, then commits the stage back to the producer;
+//   warps 0-3  epilogue: tcgen05.ld the accumulator (warp w owns TMEM lanes
+//           32w..32w+31 = tile rows), apply alpha/beta with C, round to bf16
+//           and store; with split-K they store fp32 partials instead.
+// With swap (skinny M), P = B and Q = A, so the tile holds D^T: TMEM lane = n,
+// column = m, and a warp's 32 lanes write 32 consecutive n of one row of D.
+//
+// Scale-factor placement in TMEM (one 32-bit column word per lane holds the
+// scales of 4 consecutive 32-K blocks; lane i, column c <-> row 32c + i of a
+// 128-row block, replicated in the four lane groups).  A K=64 instruction uses
+// two consecutive bytes of those words, chosen by the scale-factor id (0 or 2).
+// Every stage has its own TMEM scale slot, so a slot is rewritten only after
+// the MMAs that read it have committed.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mxfp4 {
+
+__device__ int g_device_status = 0;
+
+template <int BN, int STAGES>
+struct Cfg {
+    static constexpr int BM = kTileM;
+    static constexpr int P_BYTES = BM * 128;
+    static constexpr int Q_BYTES = BN * 128;
+    static constexpr int NQ = BN >= 128 ? BN / 128 : 1;      // 128-row scale blocks of Q
+    static constexpr int SFP_BYTES = 2 * kSfAtomBytes;       // 2 atoms per 256-K stage
+    static constexpr int SFQ_BYTES = NQ * 2 * kSfAtomBytes;
+    static constexpr int STAGE_BYTES = P_BYTES + Q_BYTES + SFP_BYTES + SFQ_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int SF_COLS_P = 8;                      // 2 groups x 4 columns
+    static constexpr int SF_COLS_Q = 8 * NQ;
+    static constexpr int SF_COLS = SF_COLS_P + SF_COLS_Q;
+    static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                     : TMEM_USED <= 64  ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256
+                                                        : 512;
+    static_assert(TMEM_USED <= 512, "tensor memory budget");
+    static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
+{
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Epilogue of one 32-column chunk of one row (no swap): v[i] is the fp32
+// accumulator of D[m][n0 + i].
+__device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int z, int m, int n0,
+                                                const uint32_t (&r)[32])
+{
+    if (a.split_k > 1) {
+        float *dst = a.ws + (static_cast<int64_t>(z) * a.M + m) * a.N + n0;
+        if ((a.N & 3) == 0 && n0 + 32 <= a.N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<uint4 *>(dst + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < a.N; ++i)
+                dst[i] = __uint_as_float(r[i]);
+        }
+        return;
+    }
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = a.alpha * __uint_as_float(r[i]);
+    const bool full = n0 + 32 <= a.N;
+    if (a.beta != 0.0f) {
+        const uint16_t *c = a.C + static_cast<int64_t>(m) * a.ldc + n0;
+        if (a.vec_ok && full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint4 w = *reinterpret_cast<const uint4 *>(c + i);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[i + 2 * j] = fmaf(a.beta, bf16_bits_to_float(ww[j] & 0xFFFF), v[i + 2 * j]);
+                    v[i + 2 * j + 1] = fmaf(a.beta, bf16_bits_to_float(ww[j] >> 16), v[i + 2 * j + 1]);
+                }
+            }
+        } else {
+            for (int i = 0; i < 32 && n0 + i < a.N; ++i)
+                v[i] = fmaf(a.beta, bf16_bits_to_float(c[i]), v[i]);
+        }
+    }
+    uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
+    if (a.vec_ok && full) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8)
+            *reinterpret_cast<uint4 *>(d + i) =
+                make_uint4(pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
+                           pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]));
+    } else {
+        for (int i = 0; i < 32 && n0 + i < a.N; ++i) {
+            __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
+            d[i] = *reinterpret_cast<uint16_t *>(&b);
+        }
+    }
+}
+
+// Epilogue of one 32-column chunk with swap: r[i] is the accumulator of
+// D[m0 + i][n] (one n per lane, consecutive across the warp).
+__device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int z, int m0, int n,
+                                                const uint32_t (&r)[32])
+{
+    if (n >= a.N)
+        return;
+    const int mcount = min(32, a.M - m0);
+    if (a.split_k > 1) {
+        float *dst = a.ws + (static_cast<int64_t>(z) * a.M + m0) * a.N + n;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < mcount)
+                dst[static_cast<int64_t>(i) * a.N] = __uint_as_float(r[i]);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (i < mcount) {
+            const int64_t m = m0 + i;
+            float v = a.alpha * __uint_as_float(r[i]);
+            if (a.beta != 0.0f)
+                v = fmaf(a.beta, bf16_bits_to_float(a.C[m * a.ldc + n]), v);
+            __nv_bfloat16 b = __float2bfloat16_rn(v);
+            a.D[m * a.ldd + n] = *reinterpret_cast<uint16_t *>(&b);
+        }
+    }
+}
+
+template <int BN, int STAGES, bool SWAP>
+__global__ void __launch_bounds__(192, 1)
+    gemm_mxf4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmP,
+                     const __grid_constant__ CUtensorMap tmQ)
+{
+    using Cf = Cfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment of the ring (128-byte swizzle atoms).
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cf::STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int p0 = blockIdx.x * kTileM;
+    const int q0 = blockIdx.y * BN;
+    const int z = blockIdx.z;
+    const int kt0 = z * a.kt_per_split;
+    const int nkt = min(a.kt_per_split, a.kt_total - kt0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, Cf::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tensormap(&tmP);
+        prefetch_tensormap(&tmQ);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0 && nkt > 0) {
+            const uint64_t pol_p = a.stream_p ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_last();
+            const uint8_t *sfp = a.sfP + static_cast<int64_t>(p0 / kSfRowBlock) * a.sf_rb_stride;
+            const uint8_t *sfq = a.sfQ + static_cast<int64_t>(q0 / kSfRowBlock) * a.sf_rb_stride;
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int i = 0; i < nkt; ++i) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_limit,
+                               &g_device_status))
+                    break;
+                uint8_t *st = smem + stage * Cf::STAGE_BYTES;
+                const int kt = kt0 + i;
+                mbar_arrive_expect_tx(&full[stage], Cf::STAGE_BYTES);
+                tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
+                tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
+                const int64_t sf_off = static_cast<int64_t>(kt) * 2 * kSfAtomBytes;
+                bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES, sfp + sf_off, Cf::SFP_BYTES, &full[stage],
+                          pol_p);
+#pragma unroll
+                for (int r = 0; r < Cf::NQ; ++r)
+                    bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES + Cf::SFP_BYTES + r * 2 * kSfAtomBytes,
+                              sfq + r * a.sf_rb_stride + sf_off, 2 * kSfAtomBytes, &full[stage],
+                              pol_q);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (*abort_flag) {
+                // Let the copies already issued land before the CTA exits.
+                for (int i = max(0, issued - STAGES); i < issued; ++i)
+                    mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------------------------- MMA issuer --
+        if (lane == 0 && nkt > 0) {
+            const uint32_t idesc = idesc_mxf4(kTileM, BN);
+            const uint32_t t_sf = tmem + BN;
+            // A 64-row Q tile uses the upper or lower half of its 128-row atom.
+            const uint32_t q_off = BN < 128 ? static_cast<uint32_t>((q0 % kSfRowBlock) / 32) : 0u;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int i = 0; i < nkt; ++i) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
+                    break;
+                tc_fence_after();
+                uint8_t *st = smem + stage * Cf::STAGE_BYTES;
+                const uint32_t sfp_t = t_sf + stage * Cf::SF_COLS;
+                const uint32_t sfq_t = sfp_t + Cf::SF_COLS_P;
+                const uint32_t sfp_s = smem_addr(st + Cf::P_BYTES + Cf::Q_BYTES);
+                const uint32_t sfq_s = sfp_s + Cf::SFP_BYTES;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    tmem_cp_32x128b_x4(sfp_t + g * 4, sdesc_sf_block(sfp_s + g * kSfAtomBytes));
+#pragma unroll
+                    for (int r = 0; r < Cf::NQ; ++r)
+                        tmem_cp_32x128b_x4(sfq_t + g * 4 * Cf::NQ + r * 4,
+                                           sdesc_sf_block(sfq_s + r * 2 * kSfAtomBytes +
+                                                          g * kSfAtomBytes));
+                }
+                const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(st));
+                const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + Cf::P_BYTES));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t sf_id = (j & 1) * 2;
+                    mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_sf_ids(idesc, sf_id, sf_id),
+                             sfp_t + (j >> 1) * 4, sfq_t + (j >> 1) * 4 * Cf::NQ + q_off,
+                             (i > 0 || j > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            mma_commit(acc_full);
+            if (*abort_flag)
+                mbar_wait_drain(acc_full, 0, a.wait_limit);   // MMAs in flight land first
+        }
+    } else {
+        // ------------------------------------------------------ epilogue --
+        bool ok = nkt > 0 && mbar_wait(acc_full, 0, abort_flag, a.wait_limit, &g_device_status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            const int row = warp * 32 + lane;
+            const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                if (SWAP && q0 + c0 >= a.M)
+                    break;                                   // padding columns of D^T
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + c0, r);
+                tmem_ld_wait();
+                if (!SWAP) {
+                    const int m = p0 + row;
+                    if (m < a.M && q0 + c0 < a.N)
+                        store_row_chunk(a, z, m, q0 + c0, r);
+                } else {
+                    store_col_chunk(a, z, q0 + c0, p0 + row, r);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cf::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------- host side --
+
+template <int BN, int STAGES, bool SWAP>
+static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                              dim3 grid, cudaStream_t stream)
+{
+    using Cf = Cfg<BN, STAGES>;
+    auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP>;
+    // Opt in to the large dynamic shared memory once per device.
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = 1;
+    }
+    kern<<<grid, 192, Cf::SMEM_BYTES, stream>>>(a, tmP, tmQ);
+    return cudaGetLastError();
+}
+
+size_t gemm_smem_bytes(const GemmShape &s)
+{
+    switch (s.tile_n) {
+    case 256: return s.stages == 4 ? Cfg<256, 4>::SMEM_BYTES : 0;
+    case 128: return s.stages == 6 ? Cfg<128, 6>::SMEM_BYTES : 0;
+    case 64:
+        return s.stages == 4 ? Cfg<64, 4>::SMEM_BYTES : s.stages == 8 ? Cfg<64, 8>::SMEM_BYTES : 0;
+    default: return 0;
+    }
+}
+
+cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                        const GemmShape &s, dim3 grid, cudaStream_t stream)
+{
+    if (!s.swap) {
+        if (s.tile_n == 256 && s.stages == 4)
+            return launch_cfg<256, 4, false>(a, tmP, tmQ, grid, stream);
+        if (s.tile_n == 128 && s.stages == 6)
+            return launch_cfg<128, 6, false>(a, tmP, tmQ, grid, stream);
+        if (s.tile_n == 64 && s.stages == 8)
+            return launch_cfg<64, 8, false>(a, tmP, tmQ, grid, stream);
+    } else {
+        if (s.tile_n == 64 && s.stages == 4)
+            return launch_cfg<64, 4, true>(a, tmP, tmQ, grid, stream);
+        if (s.tile_n == 64 && s.stages == 8)
+            return launch_cfg<64, 8, true>(a, tmP, tmQ, grid, stream);
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
+// Test hook: one wait on an mbarrier nobody arrives at.
+__global__ void wait_probe_kernel(long long limit)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait(&bar, 0, &abort_flag, limit, &g_device_status);
+}
+
+cudaError_t launch_wait_probe(long long limit, cudaStream_t stream)
+{
+    wait_probe_kernel<<<1, 32, 0, stream>>>(limit);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_status(int *status, int reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_device_status, sizeof(int));
+    if (e != cudaSuccess || !reset)
+        return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+}
+
+}  // namespace mxfp4

@@ -1,0 +1,70 @@
+// Internal launchers shared by the translation units of the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mxfp4 {
+
+constexpr int kTileM = 128;        // MMA M (rows of the MMA-A operand per tile)
+constexpr int kTileK = 256;        // K elements per pipeline stage = 128 bytes per row
+constexpr int kSfAtomBytes = 512;  // 128 rows x 4 scale blocks of the tcgen05 layout
+constexpr int kSfRowBlock = 128;
+
+// Relaid scale buffer geometry (see mxfp4_scale_relayout): 128-row blocks
+// (the count rounded up to an even number so a 256-row tile never reads past
+// the end) times 2*ceil(K/256) atoms of 512 bytes.
+inline int64_t sf_groups(int K) { return 2 * ((static_cast<int64_t>(K) + kTileK - 1) / kTileK); }
+inline int64_t sf_row_blocks(int rows) { return 2 * ((static_cast<int64_t>(rows) + 255) / 256); }
+inline size_t sf_relaid_bytes(int rows, int K)
+{
+    return static_cast<size_t>(sf_row_blocks(rows) * sf_groups(K) * kSfAtomBytes);
+}
+
+// Arguments of one GEMM launch.  "P" is the operand whose rows feed the MMA's
+// M side (A, or B when swapped), "Q" the operand on the MMA's N side.
+struct GemmArgs {
+    const uint8_t *sfP;     // relaid scales of P
+    const uint8_t *sfQ;     // relaid scales of Q
+    int64_t sf_rb_stride;   // bytes per 128-row block of relaid scales
+    int M, N, K;
+    int kt_total;           // ceil(K / 256)
+    int kt_per_split;
+    int split_k;
+    float alpha, beta;
+    const uint16_t *C;      // bf16 bits
+    int64_t ldc;
+    uint16_t *D;            // bf16 bits
+    int64_t ldd;
+    float *ws;              // fp32 partials [split_k][M][N] (split_k > 1)
+    int vec_ok;             // D (and C) allow aligned 16-byte row accesses
+    int stream_p;           // P is read once: hint L2 evict-first
+    long long wait_limit;   // SM cycles before a wait gives up
+};
+
+struct GemmShape {
+    int tile_n;
+    int stages;
+    int swap;
+};
+
+// Dynamic shared memory one GEMM configuration needs (0 if unsupported).
+size_t gemm_smem_bytes(const GemmShape &s);
+
+cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                        const GemmShape &s, dim3 grid, cudaStream_t stream);
+
+cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
+                                  cudaStream_t stream);
+
+cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float alpha, float beta,
+                                 const uint16_t *C, int64_t ldc, uint16_t *D, int64_t ldd,
+                                 int sms, cudaStream_t stream);
+
+cudaError_t launch_wait_probe(long long limit, cudaStream_t stream);
+
+cudaError_t read_device_status(int *status, int reset);
+
+}  // namespace mxfp4

@@ -1,0 +1,125 @@
+// Scale-factor relayout and split-K reduction kernels.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mxfp4 {
+
+// ------------------------------------------------------- scale relayout --
+//
+// Row-major E8M0 scales [rows, K/32] (one per 32 K elements; page "asm_f4gemm
+// -- driving aiter's gfx950 MXFP4 GEMM code objects", section "Data layouts",
+// "A_scale / B_scale", which also pads with 0x7F = 1.0) -> 512-byte atoms of
+// 128 rows x 4 blocks.  Atom (rb, g) sits at (rb * groups + g) * 512; inside
+// it, row 32j + i and block b sit at byte 16i + 4j + b, so that one 16-byte
+// line holds rows i, i+32, i+64, i+96 -- the 32x128b source shape that
+// tcgen05.cp replicates into the four TMEM lane groups.
+//
+// One CTA of 128 threads handles one 128-row block and up to kGroupsPerCta
+// atoms along K; thread t writes the 4-byte word t of each atom, so a warp's
+// stores are contiguous.
+constexpr int kGroupsPerCta = 8;
+
+__global__ void __launch_bounds__(128)
+    scale_relayout_kernel(uint8_t *__restrict__ dst, const uint8_t *__restrict__ src, int rows,
+                          int kblocks, int64_t ld, int64_t groups)
+{
+    const int t = threadIdx.x;
+    const int i = t >> 2;                 // line inside the atom
+    const int j = t & 3;                  // which of the 4 rows of the line
+    const int64_t rb = blockIdx.x;
+    const int64_t row = rb * 128 + 32 * j + i;
+    const int64_t g0 = static_cast<int64_t>(blockIdx.y) * kGroupsPerCta;
+    const uint8_t *srow = src + row * ld;
+    for (int64_t g = g0; g < min(g0 + kGroupsPerCta, groups); ++g) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int64_t kb = g * 4 + b;
+            const uint32_t v = (row < rows && kb < kblocks) ? srow[kb] : 0x7Fu;
+            word |= v << (8 * b);
+        }
+        reinterpret_cast<uint32_t *>(dst + (rb * groups + g) * kSfAtomBytes)[t] = word;
+    }
+}
+
+cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
+                                  cudaStream_t stream)
+{
+    const int64_t groups = sf_groups(K);
+    const int64_t rblocks = sf_row_blocks(rows);
+    dim3 grid(static_cast<unsigned>(rblocks),
+              static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
+    scale_relayout_kernel<<<grid, 128, 0, stream>>>(dst, src, rows, K / 32, ld, groups);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------- split-K reduce --
+//
+// D[m][n] = bf16(alpha * sum_{z=0..split-1} ws[z][m][n] + beta * C[m][n]),
+// summing the fp32 partials in the fixed order z = 0, 1, ..., so the result
+// does not depend on scheduling (the page's bf16-atomic split-K, section
+// "Verification", loses precision; this keeps fp32 until the one rounding).
+// Each thread owns 4 consecutive n of one row.
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float v)
+{
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t *>(&b);
+}
+
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float *__restrict__ ws, int split, int M, int N, float alpha,
+                         float beta, const uint16_t *__restrict__ C, int64_t ldc,
+                         uint16_t *__restrict__ D, int64_t ldd)
+{
+    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
+    const int64_t total = quads * M;
+    const int64_t plane = static_cast<int64_t>(M) * N;
+    const bool vec = (N & 3) == 0;
+    for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < total;
+         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = q / quads;
+        const int n = static_cast<int>(q - m * quads) * 4;
+        const int cnt = min(4, N - n);
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *p = ws + m * N + n;
+        if (vec) {
+            for (int z = 0; z < split; ++z) {
+                const float4 v = __ldcs(reinterpret_cast<const float4 *>(p + z * plane));
+                s[0] += v.x;
+                s[1] += v.y;
+                s[2] += v.z;
+                s[3] += v.w;
+            }
+        } else {
+            for (int z = 0; z < split; ++z)
+                for (int i = 0; i < cnt; ++i)
+                    s[i] += p[z * plane + i];
+        }
+        for (int i = 0; i < cnt; ++i) {
+            float v = alpha * s[i];
+            if (beta != 0.0f)
+                v = fmaf(beta, __uint_as_float(static_cast<uint32_t>(C[m * ldc + n + i]) << 16), v);
+            D[m * ldd + n + i] = to_bf16_bits(v);
+        }
+    }
+}
+
+cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float alpha, float beta,
+                                 const uint16_t *C, int64_t ldc, uint16_t *D, int64_t ldd, int sms,
+                                 cudaStream_t stream)
+{
+    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4 * M;
+    int64_t blocks = (quads + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, split, M, N, alpha,
+                                                                            beta, C, ldc, D, ldd);
+    return cudaGetLastError();
+}
+
+}  // namespace mxfp4

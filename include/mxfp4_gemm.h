@@ -1,0 +1,190 @@
+/*
+ * mxfp4_gemm.h -- C ABI of the GB300 (sm_103a) block-scaled MXFP4 GEMM.
+ *
+ *     D[M,N] (bf16) = alpha * A[M,K] (mxfp4) * B[N,K]^T (mxfp4) + beta * C[M,N] (bf16)
+ *
+ * The operation and its operand formats are those of the page "asm_f4gemm --
+ * driving aiter's gfx950 MXFP4 GEMM code objects" (the formula at the top,
+ * section "Data layouts", section "Kernel ABI"):
+ *   - A [M, K/2] and B [N, K/2]: packed fp4x2 E2M1 bytes, row-major; byte i
+ *     of a row holds element 2i in its low nibble and 2i+1 in its high nibble;
+ *     magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}, sign in bit 3.
+ *   - scaleA [M, K/32] and scaleB [N, K/32]: one E8M0 byte (value 2^(e-127))
+ *     per 32 consecutive K elements of a row, row-major.
+ *   - C, D: bf16 [M, N] row-major.
+ * Each scale multiplies its 32 inputs before they are accumulated (page
+ * "CDNA4 dense MFMA builtins", section "Mixed-precision with scaling").
+ * Products accumulate in fp32; D is rounded once to bf16 (nearest even).
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller unless an
+ *     entry point says otherwise.  The library never allocates, frees or
+ *     retains them, never synchronises the device, and enqueues work on
+ *     `stream` only (a cudaStream_t; NULL is the legacy default stream).
+ *   - A/B row strides (lda, ldb) are counted in fp4 ELEMENTS, as the page's
+ *     kernarg block counts them (stride in bytes = ld / 2).  Scale row strides
+ *     (ld_sa, ld_sb) are in bytes.  C/D strides (ldc, ldd) are in elements.
+ *   - Every argument is validated before anything is enqueued; on an error
+ *     the call returns a negative mxfp4_status and enqueues nothing.  Errors
+ *     raised by the CUDA runtime at launch return MXFP4_ERR_CUDA.  Waits
+ *     inside the kernels are bounded: one that runs out records
+ *     MXFP4_ERR_TIMEOUT in a device status word (mxfp4_device_status) and
+ *     the kernel returns instead of hanging.
+ *   - Only sm_103 devices are accepted (MXFP4_ERR_ARCH otherwise).
+ *   - Functions are safe to call from several host threads.
+ */
+#ifndef MXFP4_GEMM_H
+#define MXFP4_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mxfp4_status {
+    MXFP4_OK = 0,
+    MXFP4_ERR_INVALID_ARG = -1,       /* null pointer, bad size or stride */
+    MXFP4_ERR_UNSUPPORTED_SHAPE = -2, /* shape outside what the kernels take */
+    MXFP4_ERR_MISALIGNED = -3,        /* pointer or stride breaks a 16-byte rule */
+    MXFP4_ERR_WORKSPACE = -4,         /* workspace missing or too small */
+    MXFP4_ERR_CUDA = -5,              /* the CUDA runtime reported an error */
+    MXFP4_ERR_TIMEOUT = -6,           /* a bounded in-kernel wait ran out */
+    MXFP4_ERR_ARCH = -7               /* current device is not sm_103 */
+} mxfp4_status;
+
+/* The launch configuration mxfp4_gemm would use for a shape (host only). */
+typedef struct mxfp4_plan {
+    int swap_ab;            /* 1: computes D^T = B . A^T (skinny M) */
+    int tile_m;             /* MMA M rows per tile (rows of A, or of B if swapped) */
+    int tile_n;             /* MMA N columns per tile */
+    int tile_k;             /* K elements per pipeline stage */
+    int stages;             /* shared-memory ring depth */
+    int split_k;            /* K splits; > 1 adds the fp32 reduce kernel */
+    int k_tiles_per_split;  /* tile_k blocks handled by one split */
+    int grid_x, grid_y, grid_z;
+    size_t workspace_bytes; /* what mxfp4_gemm needs for this plan */
+} mxfp4_plan;
+
+/*
+ * Choose tile, swap and split-K for a shape (the tile heuristic of the page's
+ * section "Tile selection heuristic": fewest waves over the SMs, then SM
+ * occupancy of the last wave, then tile area over perimeter; ties resolved by
+ * a fixed candidate order).  split_k = 0 lets the heuristic choose; 1..16
+ * forces that many splits (clamped to the number of K blocks).  num_sms = 0
+ * uses the current device's SM count (or 152 when no device is visible).
+ * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
+ */
+int mxfp4_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out);
+
+/*
+ * Bytes of device workspace mxfp4_gemm needs: the two relaid scale buffers
+ * plus, when the plan splits K, the fp32 partial sums [split, M, N].
+ * Returns 0 for invalid sizes.
+ */
+size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k);
+
+/*
+ * Bytes of a relaid scale buffer for `rows` rows of K elements:
+ * ceil(rows/128) * 2*ceil(K/256) * 512.
+ */
+size_t mxfp4_scale_relayout_size(int rows, int K);
+
+/*
+ * Relayout of E8M0 scales (page section "Data layouts", subsection
+ * "A_scale / B_scale": one scale per 32 K, padded with 0x7F = 1.0) from
+ * row-major [rows, K/32] (row stride ld_src bytes) into the tcgen05
+ * block-scale layout the GEMM stages into tensor memory: 512-byte atoms of
+ * 128 rows x 4 scale blocks, atom (rb, g) at byte (rb * 2*ceil(K/256) + g)*512,
+ * and inside an atom row r = 32*j + i, block b at byte 16*i + 4*j + b.
+ * Rows >= rows and blocks >= K/32 are filled with 0x7F.
+ * dst: device, mxfp4_scale_relayout_size(rows, K) bytes, 16-byte aligned.
+ * Use it to prepack weight scales once for mxfp4_gemm_prepacked.
+ */
+int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld_src,
+                         void *stream);
+
+/*
+ * The GEMM (page formula; section "Kernel ABI" for the argument set).
+ *   D       bf16 [M, ldd]           output; ldd >= N
+ *   C       bf16 [M, ldc] or NULL   read only when beta != 0; may alias D
+ *                                   only with ldc == ldd
+ *   A       uint8 [M, lda/2]        lda >= K, lda % 32 == 0 (16-byte rows)
+ *   B       uint8 [N, ldb/2]        ldb >= K, ldb % 32 == 0
+ *   scaleA  uint8 [M, ld_sa]        ld_sa >= K/32
+ *   scaleB  uint8 [N, ld_sb]        ld_sb >= K/32
+ *   M, N >= 1; K >= 32, K % 32 == 0 (the scale block).  A, B 16-byte aligned.
+ *   split_k  0 = heuristic, else 1..16.  Splits reduce in fp32 in a fixed
+ *            order, so results are bitwise reproducible run to run.
+ *   workspace  device, >= mxfp4_gemm_workspace_size(M, N, K, split_k) bytes,
+ *              256-byte aligned; contents need not be initialised.
+ */
+int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
+               const void *A, int64_t lda, const void *B, int64_t ldb,
+               const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,
+               float alpha, float beta, int M, int N, int K, int split_k,
+               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * As mxfp4_gemm, with both scale buffers already in the relaid layout
+ * produced by mxfp4_scale_relayout (scaleA for M rows, scaleB for N rows, at
+ * the same K).  The workspace then only holds the split-K partials:
+ * mxfp4_gemm_prepacked_workspace_size bytes (0 is valid when split_k == 1).
+ */
+int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc,
+                         const void *A, int64_t lda, const void *B, int64_t ldb,
+                         const void *scaleA_relaid, const void *scaleB_relaid,
+                         float alpha, float beta, int M, int N, int K, int split_k,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+size_t mxfp4_gemm_prepacked_workspace_size(int M, int N, int K, int split_k);
+
+/*
+ * End-to-end call on HOST buffers: copies A, B, scaleA, scaleB (and C when
+ * beta != 0) from host memory into `device_arena`, runs mxfp4_gemm there and
+ * copies D back to host memory, all enqueued on `stream` (cudaMemcpyAsync
+ * per buffer; pinned host memory makes the copies asynchronous).  Host
+ * arrays are dense (ld = K for A/B, K/32 for scales, N for C/D).  The call
+ * returns after enqueueing; synchronise `stream` before reading D_host.
+ * device_arena: >= mxfp4_gemm_host_arena_size(M, N, K, split_k, beta != 0)
+ * bytes of device memory, 256-byte aligned, owned by the caller.
+ */
+int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
+                    const void *scaleA_host, const void *scaleB_host,
+                    float alpha, float beta, int M, int N, int K, int split_k,
+                    void *device_arena, size_t arena_bytes, void *stream);
+
+size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
+
+/*
+ * Read the device status word that bounded waits write on timeout into
+ * *status (MXFP4_OK or MXFP4_ERR_TIMEOUT); if reset != 0 clear it.
+ * Synchronous (it copies one int from the device).
+ */
+int mxfp4_device_status(int *status, int reset);
+
+/*
+ * Test hook for the bounded waits: launches one CTA that waits on an
+ * mbarrier nothing ever arrives at, with a limit of `limit_cycles` SM clock
+ * cycles, through the same wait routine the GEMM uses.  The wait runs out,
+ * records MXFP4_ERR_TIMEOUT in the device status word and the kernel
+ * returns.  The page has no counterpart: this exists so tests can show a
+ * stuck wait ends cleanly without faulting the GPU.
+ */
+int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream);
+
+/* Set the in-kernel wait limit in SM clock cycles (default 2^32, ~2 s). */
+void mxfp4_set_wait_limit(long long cycles);
+
+/* Human-readable name of a status code (never NULL). */
+const char *mxfp4_strerror(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int mxfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GEMM_H */

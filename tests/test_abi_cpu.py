@@ -1,0 +1,158 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library loads, exports every function the public header declares, and
+its host logic (plan heuristic, workspace sizes, argument validation that
+returns before any device call) behaves as documented.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import block_scaled_mxfp4_gb300 as mx
+from block_scaled_mxfp4_gb300 import build as mxbuild
+
+
+@pytest.fixture(scope="module")
+def L():
+    mxbuild.build()
+    return mx.lib()
+
+
+def test_library_exports_every_header_symbol(L):
+    names = mx.header_functions()
+    assert len(names) >= 14
+    out = subprocess.run(["nm", "-D", "--defined-only", mx.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in names:
+        assert n in exported, n
+        assert getattr(L, n) is not None
+
+
+def test_library_is_sm103a_only():
+    # One -gencode, no PTX for other targets.
+    assert mxbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_version_and_strerror(L):
+    assert mx.mxfp4_version() == 10000
+    for code in range(-7, 1):
+        s = mx.mxfp4_strerror(code)
+        assert s and s != "unknown status"
+    assert mx.mxfp4_strerror(-99) == "unknown status"
+
+
+WORKLOADS = {"tiny": (128, 256, 512), "decode": (1, 8192, 8192), "mid": (512, 1024, 2048),
+             "large": (8192, 8192, 8192), "skinny": (64, 7168, 16384)}
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_plan_invariants(L, name):
+    M, N, K = WORKLOADS[name]
+    for split in range(0, 17):
+        p = mx.mxfp4_plan_gemm(M, N, K, split, 152)
+        kt = -(-K // p.tile_k)
+        assert p.tile_m == 128 and p.tile_k == 256
+        assert p.split_k >= 1 and p.split_k <= 16
+        assert p.k_tiles_per_split * (p.split_k - 1) < kt <= p.k_tiles_per_split * p.split_k
+        if split:
+            assert p.split_k <= split
+        P, Q = (N, M) if p.swap_ab else (M, N)
+        assert p.grid_x == -(-P // 128) and p.grid_y == -(-Q // p.tile_n)
+        assert p.grid_z == p.split_k
+        want_ws = 0 if p.split_k == 1 else p.split_k * M * N * 4
+        assert p.workspace_bytes >= want_ws
+    # Skinny M swaps; large uses the widest tile and no split.
+    p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
+    assert p.swap_ab == (1 if M <= 64 else 0)
+    if name == "large":
+        assert (p.tile_n, p.split_k) == (256, 1)
+
+
+def test_plan_heuristic_prefers_fewer_waves(L):
+    # 8192^2 output: 128x256 tiles need 14 waves on 152 SMs, 128x128 need 27.
+    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).tile_n == 256
+    # 512x1024: both fit in one wave; 128x128 fills more SMs.
+    assert mx.mxfp4_plan_gemm(512, 1024, 2048, 0, 152).tile_n == 128
+    # Deterministic.
+    a = mx.mxfp4_plan_gemm(300, 2048, 1024, 0, 152).as_dict()
+    b = mx.mxfp4_plan_gemm(300, 2048, 1024, 0, 152).as_dict()
+    assert a == b
+
+
+def test_sizes(L):
+    assert mx.mxfp4_scale_relayout_size(1, 32) == 2 * 2 * 512
+    assert mx.mxfp4_scale_relayout_size(256, 512) == 2 * 4 * 512
+    assert mx.mxfp4_scale_relayout_size(257, 512) == 4 * 4 * 512
+    assert mx.mxfp4_scale_relayout_size(0, 512) == 0
+    assert mx.mxfp4_scale_relayout_size(5, 48) == 0
+    assert mx.mxfp4_gemm_workspace_size(0, 1, 32, 0) == 0
+    assert mx.mxfp4_gemm_workspace_size(1, 1, 32, 17) == 0
+    ws = mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4)
+    assert ws >= mx.mxfp4_scale_relayout_size(1, 8192) + mx.mxfp4_scale_relayout_size(8192, 8192) \
+        + 4 * 8192 * 4
+
+
+def _call_gemm(L, **kw):
+    args = dict(D=0x1000, ldd=256, C=None, ldc=0, A=0x2000, lda=512, B=0x3000, ldb=512,
+                SA=0x4000, ld_sa=16, SB=0x5000, ld_sb=16, alpha=1.0, beta=0.0, M=128, N=256,
+                K=512, split=0, ws=0x10000, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return L.mxfp4_gemm(args["D"], args["ldd"], args["C"], args["ldc"], args["A"], args["lda"],
+                        args["B"], args["ldb"], args["SA"], args["ld_sa"], args["SB"],
+                        args["ld_sb"], args["alpha"], args["beta"], args["M"], args["N"],
+                        args["K"], args["split"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=None), -1), (dict(A=None), -1), (dict(B=None), -1),
+    (dict(SA=None), -1), (dict(SB=None), -1),
+    (dict(M=0), -1), (dict(N=0), -1), (dict(K=0), -1), (dict(K=48, lda=64, ldb=64), -1),
+    (dict(lda=256), -1), (dict(ldb=500), -1), (dict(ldd=255), -1),
+    (dict(ld_sa=15), -1), (dict(ld_sb=1), -1),
+    (dict(beta=1.0), -1), (dict(beta=1.0, C=0x6000, ldc=100), -1),
+    (dict(split=17), -1), (dict(split=-1), -1),
+    (dict(lda=528), -3), (dict(ldb=520), -3), (dict(A=0x2008), -3), (dict(B=0x3004), -3),
+    (dict(ws=None), -4), (dict(ws=0x10010), -3),
+])
+def test_gemm_argument_validation(L, kw, status):
+    # These return before any device call, so they run without a GPU.
+    assert _call_gemm(L, **kw) == status
+
+
+def test_other_entry_points_validate_before_device(L):
+    assert L.mxfp4_scale_relayout(None, 0x1000, 4, 64, 2, None) == -1
+    assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 48, 2, None) == -1
+    assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 64, 1, None) == -1
+    assert L.mxfp4_scale_relayout(0x1008, 0x2000, 4, 64, 2, None) == -3
+    assert L.mxfp4_gemm_prepacked(0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, None, 0x5000,
+                                  1.0, 0.0, 128, 256, 512, 0, None, 0, None) == -1
+    assert L.mxfp4_gemm_prepacked(0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, 0x4008, 0x5000,
+                                  1.0, 0.0, 128, 256, 512, 0, None, 0, None) == -3
+    assert L.mxfp4_gemm_host(None, None, 1, 1, 1, 1, 1.0, 0.0, 1, 1, 32, 0, 0x1000, 1 << 20,
+                             None) == -1
+    assert L.mxfp4_gemm_host(1, None, 1, 1, 1, 1, 1.0, 1.0, 1, 1, 32, 0, 0x1000, 1 << 20,
+                             None) == -1
+    assert L.mxfp4_gemm_host(1, None, 1, 1, 1, 1, 1.0, 0.0, 1, 1, 32, 0, 0x1000, 16, None) == -4
+    assert L.mxfp4_wait_timeout_probe(0, None) == -1
+    assert L.mxfp4_device_status(None, 0) == -1
+    plan = mx.Plan()
+    assert L.mxfp4_plan_gemm(1, 1, 33, 0, 152, ctypes.byref(plan)) == -1
+    assert L.mxfp4_plan_gemm(1, 1, 32, 0, 152, None) == -1
+
+
+def test_no_device_reports_cuda_error_not_crash(L):
+    # With arguments valid, the first device query fails cleanly on a machine
+    # without a GPU (and succeeds on one), never crashes.
+    if os.environ.get("CUDA_VISIBLE_DEVICES", None) is None:
+        try:
+            import torch
+            has_gpu = torch.cuda.is_available()
+        except Exception:
+            has_gpu = False
+        if has_gpu:
+            pytest.skip("a GPU is visible")
+    st = ctypes.c_int(123)
+    assert L.mxfp4_device_status(ctypes.byref(st), 0) in (-5, -7)

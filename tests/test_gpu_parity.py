@@ -1,0 +1,319 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every comparison is element by element within the stated bound (see
+parity_util).  Full comparisons at the sizes the oracle finishes in seconds;
+at the full large / skinny sizes, sampled outputs (tile edges + random).
+"""
+import numpy as np
+import pytest
+
+import block_scaled_mxfp4_gb300 as mx
+from block_scaled_mxfp4_gb300 import inputs
+from parity_util import (Dev, assert_within_bound, bf16_bits_to_f64, d_to_bits, run_gemm,
+                         sample_pairs)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    from block_scaled_mxfp4_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mx.mxfp4_device_status(reset=True)
+    yield
+    assert mx.mxfp4_device_status() == 0, "a bounded wait timed out during the tests"
+
+
+_PROBLEMS = {}
+
+
+def problem(name):
+    if name not in _PROBLEMS:
+        _PROBLEMS[name] = inputs.identity_problem() if name == "identity" else inputs.workload(name)
+    return _PROBLEMS[name]
+
+
+def full_oracle(oracle_mod, p, alpha=None, beta=None):
+    alpha = p.alpha if alpha is None else alpha
+    beta = p.beta if beta is None else beta
+    D, _, sabs, inexact = oracle_mod.gemm(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, alpha=alpha,
+                                          beta=beta, C=p.C)
+    assert inexact == 0
+    return D, sabs
+
+
+# --------------------------------------------------------------- relayout --
+
+def relayout_reference(S, rows, K):
+    """tcgen05 scale layout written from its description: 512-byte atoms of
+    128 rows x 4 blocks; row 32j + i, block b at byte 16i + 4j + b; atoms
+    row-block major; rows padded to a multiple of 256, blocks to 8 per 256 K,
+    with 0x7F."""
+    kb = K // 32
+    groups = 2 * (-(-K // 256))
+    rblocks = 2 * (-(-rows // 256))
+    out = np.full(rblocks * groups * 512, 0x7F, dtype=np.uint8)
+    for rb in range(rblocks):
+        for g in range(groups):
+            base = (rb * groups + g) * 512
+            for i in range(32):
+                for j in range(4):
+                    r = rb * 128 + 32 * j + i
+                    for b in range(4):
+                        k = g * 4 + b
+                        if r < rows and k < kb:
+                            out[base + 16 * i + 4 * j + b] = S[r, k]
+    return out
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (128, 512), (300, 288), (64, 16384 // 8), (257, 1024)])
+def test_scale_relayout_bytes(rows, K):
+    rng = np.random.default_rng(rows * 7 + K)
+    ld = K // 32 + 3
+    S = rng.integers(0, 256, size=(rows, ld), dtype=np.uint8)
+    src = torch.from_numpy(S).cuda()
+    size = mx.mxfp4_scale_relayout_size(rows, K)
+    dst = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    mx.mxfp4_scale_relayout(dst, src, rows, K, ld)
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy()
+    want = relayout_reference(S, rows, K)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------- scale placement probes --
+
+def _ones_problem(M, N, K):
+    A = np.full((M, K // 2), 0x22, dtype=np.uint8)        # every element 1.0
+    B = np.full((N, K // 2), 0x22, dtype=np.uint8)
+    SA = np.full((M, K // 32), 127, dtype=np.uint8)
+    SB = np.full((N, K // 32), 127, dtype=np.uint8)
+    return inputs.Problem("probe", M, N, K, A, B, SA, SB, None, 1.0, 0.0, 0)
+
+
+@pytest.mark.parametrize("M,N", [(128, 256), (256, 128), (16, 256), (1, 200)])
+def test_single_scale_probes(M, N):
+    """One doubled scale at (row r, block kb) adds exactly 32 to the outputs
+    of row r (A) or column r (B): pins which TMEM scale word feeds which row
+    and K block, for the plain and the swapped mapping."""
+    K = 512
+    rows_a = sorted(r for r in {0, 1, 31, 32, 97, M - 1} if r < M)
+    rows_b = sorted(r for r in {0, 5, 33, 64, 127, 128, 200, N - 1} if r < N)
+    bad = []
+    for which, rows in (("A", rows_a), ("B", rows_b)):
+        for r in rows:
+            for kb in (0, 1, 2, 3, 5, 8, 13, 15):
+                p = _ones_problem(M, N, K)
+                (p.SA if which == "A" else p.SB)[r, kb] = 128
+                D = bf16_bits_to_f64(run_gemm(Dev(p)))
+                want = np.full((M, N), float(K))
+                if which == "A":
+                    want[r, :] += 32
+                else:
+                    want[:, r] += 32
+                if not np.array_equal(D, want):
+                    wrong = np.argwhere(D != want)
+                    bad.append((which, r, kb, len(wrong), wrong[:4].tolist(),
+                                D[tuple(wrong[0])]))
+    assert not bad, bad
+
+
+# ------------------------------------------------------------ workloads --
+
+def test_tiny_full(oracle_mod):
+    p = problem("tiny")
+    Dref, sabs = full_oracle(oracle_mod, p)
+    assert_within_bound(run_gemm(Dev(p)), Dref, sabs, p.alpha, "tiny")
+
+
+def test_identity_exact():
+    p = problem("identity")
+    D = bf16_bits_to_f64(run_gemm(Dev(p)))
+    codes = inputs.unpack_fp4(p.A)
+    vals = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    want = np.where(codes & 8, -vals[codes & 7], vals[codes & 7])[:, : p.N]
+    assert np.array_equal(D, want)
+
+
+def test_mid_full(oracle_mod):
+    p = problem("mid")
+    Dref, sabs = full_oracle(oracle_mod, p)
+    dev = Dev(p)
+    for split in (0, 1, 2, 4):
+        assert_within_bound(run_gemm(dev, split_k=split), Dref, sabs, p.alpha, f"mid s={split}")
+
+
+@pytest.mark.parametrize("split", [0, 1, 2, 4, 8, 16])
+def test_decode_split_sweep(oracle_mod, split):
+    p = problem("decode")
+    if "decode_ref" not in _PROBLEMS:
+        _PROBLEMS["decode_ref"] = full_oracle(oracle_mod, p)
+    Dref, sabs = _PROBLEMS["decode_ref"]
+    if "decode_dev" not in _PROBLEMS:
+        _PROBLEMS["decode_dev"] = Dev(p)
+    D = run_gemm(_PROBLEMS["decode_dev"], split_k=split)
+    assert_within_bound(D, Dref, sabs, p.alpha, f"decode s={split}")
+
+
+@pytest.mark.parametrize("split", [0, 1, 2, 4, 8])
+def test_skinny_split_sweep(oracle_mod, split):
+    p = problem("skinny")
+    if "skinny_ref" not in _PROBLEMS:
+        rows = [0, 1, 31, 32, 63]
+        pairs = np.array([(m, n) for m in rows for n in range(p.N)], dtype=np.int64)
+        pairs = np.unique(np.concatenate([pairs, sample_pairs(p.M, p.N, 3000, 4)]), axis=0)
+        Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs,
+                                                       alpha=p.alpha, beta=p.beta, C=p.C)
+        assert inexact == 0
+        _PROBLEMS["skinny_ref"] = (pairs, Dr, sabs)
+        _PROBLEMS["skinny_dev"] = Dev(p)
+    pairs, Dr, sabs = _PROBLEMS["skinny_ref"]
+    D = run_gemm(_PROBLEMS["skinny_dev"], split_k=split)
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, f"skinny s={split}")
+
+
+def test_large_sampled(oracle_mod):
+    p = problem("large")
+    pairs = sample_pairs(p.M, p.N, 4000, 3)
+    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs,
+                                                   alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    D = run_gemm(Dev(p))
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "large")
+    assert not np.isnan(bf16_bits_to_f64(D)).any()
+
+
+# ----------------------------------------------------------- edge cases --
+
+EDGE_SHAPES = [
+    (1, 16, 32), (7, 40, 96), (63, 200, 288), (65, 300, 256), (129, 520, 1024),
+    (300, 2048, 1024), (1, 4096, 2048), (2, 129, 64), (200, 37, 160), (130, 130, 544),
+]
+
+
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_edge_shapes(oracle_mod, M, N, K):
+    p = inputs.make_problem("edge", M, N, K, seed=M * 131 + N * 7 + K, values="codes",
+                            alpha=1.0, beta=1.0, c_sigma=1.0)
+    Dref, sabs = full_oracle(oracle_mod, p)
+    dev = Dev(p)
+    for split in (0, 1, 3):
+        assert_within_bound(run_gemm(dev, split_k=split), Dref, sabs, p.alpha,
+                            f"{M}x{N}x{K} s={split}")
+
+
+def test_alpha_beta_forms(oracle_mod):
+    p = inputs.make_problem("ab", 96, 160, 256, seed=8, values="normal", alpha=1.0, beta=0.0,
+                            c_sigma=1.0)
+    dev = Dev(p)
+    for alpha, beta in ((1.0, 0.0), (0.5, 0.5), (-2.0, 1.0), (0.0, 1.0), (1.0, -1.0)):
+        Dref, sabs = full_oracle(oracle_mod, p, alpha=alpha, beta=beta)
+        assert_within_bound(run_gemm(dev, alpha=alpha, beta=beta), Dref, sabs, alpha,
+                            f"alpha={alpha} beta={beta}")
+    # alpha = 0, beta = 1 returns C exactly.
+    D = run_gemm(dev, alpha=0.0, beta=1.0)
+    assert np.array_equal(bf16_bits_to_f64(D), bf16_bits_to_f64(p.C))
+
+
+def test_beta_zero_ignores_nan_c():
+    p = problem("tiny")
+    dev = Dev(p)
+    ref = run_gemm(dev)
+    dev.C = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 0), dtype=torch.uint8,
+                     device="cuda")
+    mx.mxfp4_gemm(D, p.N, dev.C, p.N, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32, dev.SB,
+                  p.K // 32, 1.0, 0.0, p.M, p.N, p.K, 0, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), ref)
+
+
+def test_strides_and_in_place(oracle_mod):
+    M, N, K = 130, 200, 512
+    p = inputs.make_problem("strided", M, N, K, seed=12, values="normal", alpha=0.5, beta=1.0,
+                            c_sigma=1.0)
+    Dref, sabs = full_oracle(oracle_mod, p)
+    pad_k, pad_s, pad_n = 64, 5, 24
+    A = torch.zeros((M, (K + pad_k) // 2), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((N, (K + pad_k) // 2), dtype=torch.uint8, device="cuda")
+    A[:, : K // 2] = torch.from_numpy(p.A).cuda()
+    B[:, : K // 2] = torch.from_numpy(p.B).cuda()
+    SA = torch.zeros((M, K // 32 + pad_s), dtype=torch.uint8, device="cuda")
+    SB = torch.zeros((N, K // 32 + pad_s), dtype=torch.uint8, device="cuda")
+    SA[:, : K // 32] = torch.from_numpy(p.SA).cuda()
+    SB[:, : K // 32] = torch.from_numpy(p.SB).cuda()
+    # D aliases C (in-place beta), both with a padded row stride.
+    DC = torch.zeros((M, N + pad_n), dtype=torch.bfloat16, device="cuda")
+    DC[:, :N] = torch.from_numpy(p.C.view(np.int16)).cuda().view(torch.bfloat16)
+    ws = torch.empty(mx.mxfp4_gemm_workspace_size(M, N, K, 0), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm(DC, N + pad_n, DC, N + pad_n, A, K + pad_k, B, K + pad_k, SA, K // 32 + pad_s,
+                  SB, K // 32 + pad_s, p.alpha, p.beta, M, N, K, 0, ws, ws.numel())
+    torch.cuda.synchronize()
+    got = d_to_bits(DC[:, :N])
+    assert_within_bound(got, Dref, sabs, p.alpha, "strided in-place")
+    assert np.all(d_to_bits(DC[:, N:]) == 0)
+
+
+def test_split_k_is_deterministic():
+    p = problem("decode") if "decode" in _PROBLEMS else inputs.workload("decode")
+    dev = Dev(p)
+    a = run_gemm(dev, split_k=8)
+    b = run_gemm(dev, split_k=8)
+    assert np.array_equal(a, b)
+
+
+def test_prepacked_and_host_entry_points_match():
+    p = problem("mid")
+    dev = Dev(p)
+    ref = run_gemm(dev)
+    M, N, K = p.M, p.N, p.K
+    sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device="cuda")
+    sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_scale_relayout(sfa, dev.SA, M, K, K // 32)
+    mx.mxfp4_scale_relayout(sfb, dev.SB, N, K, K // 32)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, 0)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm_prepacked(D, N, dev.C, N, dev.A, K, dev.B, K, sfa, sfb, p.alpha, p.beta,
+                            M, N, K, 0, ws, wsb)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), ref)
+    # Host buffers in, host buffer out.
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hA, hB, hSA, hSB = pin(p.A), pin(p.B), pin(p.SA), pin(p.SB)
+    hC = pin(p.C.view(np.int16))
+    hD = torch.zeros((M, N), dtype=torch.int16).pin_memory()
+    arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, 0, True)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm_host(hD, hC, hA, hB, hSA, hSB, p.alpha, p.beta, M, N, K, 0, arena, arena_b)
+    torch.cuda.synchronize()
+    assert np.array_equal(hD.numpy().view(np.uint16), ref)
+
+
+def test_device_errors_are_reported():
+    p = problem("tiny")
+    dev = Dev(p)
+    D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
+    need = mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.mxfp4_gemm(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32, dev.SB,
+                      p.K // 32, 1.0, 0.0, p.M, p.N, p.K, 0, ws, need - 1)
+    assert e.value.status == -4
+
+
+def test_bounded_wait_times_out_cleanly():
+    """A wait nothing satisfies gives up after its limit, records
+    MXFP4_ERR_TIMEOUT and returns; the context stays usable."""
+    assert mx.mxfp4_device_status(reset=True) == 0
+    mx.mxfp4_wait_timeout_probe(2_000_000)            # ~1 ms of SM cycles
+    torch.cuda.synchronize()
+    assert mx.mxfp4_device_status(reset=True) == -6
+    assert mx.mxfp4_device_status() == 0
+    p = problem("tiny")
+    D = run_gemm(Dev(p))
+    assert not np.isnan(bf16_bits_to_f64(D)).any()

@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 block-scaled MXFP4 GEMM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--split-k S]
+    python bench.py --impl reference ...     # the CPU oracle on a bounded sample
+
+One step is the whole hot path on one batch of resident inputs: relayout of
+both scale matrices into the tcgen05 layout, the tcgen05 GEMM, and the split-K
+reduce when K is split.  Steps are timed with CUDA events on the launching
+stream; L2 is flushed (a 512 MiB write) between timed steps, outside the
+events.  Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs
+an independent replica of the workload (the GEMM needs no exchange), the
+barrier + max over ranks times the job, and value counts all ranks' FLOPs.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP4 peak / HBM roofline"
+UNIT = "TFLOP/s"
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 / dense bf16 tensor rate
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="large",
+                    choices=["tiny", "decode", "mid", "large", "skinny"])
+    ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_geometry(p):
+    flops = 2.0 * p.M * p.N * p.K
+    algo_bytes = (p.M * p.K // 2 + p.N * p.K // 2 + p.M * p.K // 32 + p.N * p.K // 32
+                  + 2 * p.M * p.N + (2 * p.M * p.N if p.beta != 0.0 else 0))
+    return flops, algo_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed work runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx_ = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        # Samples "under load": SM clock within the upper part of its range.
+        loaded = [s for s in sm if s >= 0.5 * (max(mx_) if mx_ else 1)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i - 5] for r in rows for i in range(5, 9)
+                          if r[i].lower() in ("active", "1")})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx_) if mx_ else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def oracle_throughput(p, seconds, seed):
+    """Time the CPU oracle (as it stands) on sampled outputs of the workload:
+    returns (TFLOP/s, threads, sample description)."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(seed)
+
+    def run(count):
+        pairs = np.stack([rng.integers(0, p.M, count), rng.integers(0, p.N, count)], axis=1)
+        t0 = time.perf_counter()
+        oracle.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs, alpha=p.alpha,
+                            beta=p.beta, C=p.C)
+        return time.perf_counter() - t0
+
+    cores = oracle.host_cores()
+    probe = max(cores * 4, 64)
+    t = run(probe)
+    count = int(max(probe, probe * seconds / max(t, 1e-6)))
+    t = run(count)
+    flops = 2.0 * p.K * count
+    desc = (f"{count} random (m, n) outputs of the {p.M}x{p.N}x{p.K} workload, full K each "
+            f"({flops / 2:.3g} MACs, {t:.1f} s)")
+    return flops / t / 1e12, cores, desc, t
+
+
+def run_reference(args, rank):
+    """Reference arm: the CPU oracle, timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    from block_scaled_mxfp4_gb300 import inputs
+    p = inputs.workload(args.workload)
+    per_step = 4.0 if args.steps <= 20 else max(0.5, 80.0 / args.steps)
+    for i in range(args.warmup):
+        oracle_throughput(p, min(per_step, 1.0), 1000 + i)
+    vals, times, desc, cores = [], [], "", 0
+    for i in range(args.steps):
+        v, cores, desc, t = oracle_throughput(p, per_step, 2000 + i)
+        vals.append(v)
+        times.append(t)
+    value = len(vals) / sum(1.0 / v for v in vals)        # total FLOPs / total time
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} M={p.M} N={p.N} K={p.K}",
+                   "M": p.M, "N": p.N, "K": p.K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    import block_scaled_mxfp4_gb300 as mx
+    from block_scaled_mxfp4_gb300 import build, inputs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    build.build()
+    mx.lib()
+
+    p = inputs.workload(args.workload)
+    flops, algo_bytes = workload_geometry(p)
+    dev = torch.device("cuda", local_rank)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    A, B, SA, SB = to_dev(p.A), to_dev(p.B), to_dev(p.SA), to_dev(p.SB)
+    C = None if p.C is None else to_dev(p.C.view(np.int16)).view(torch.bfloat16)
+    M, N, K = p.M, p.N, p.K
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device=dev)
+    sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device=dev)
+    wsb = mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, args.split_k)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    plan = mx.mxfp4_plan_gemm(M, N, K, args.split_k, 0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mx.mxfp4_scale_relayout(sfa, SA, M, K, K // 32, stream)
+        mx.mxfp4_scale_relayout(sfb, SB, N, K, K // 32, stream)
+
+    def gemm():
+        mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
+                                args.split_k, ws, wsb, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+        gemm()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        gemm()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    if dist:
+        dist.barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    tot_ms = sum(step_ms)
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    if dist:
+        t = torch.tensor([tot_ms, gemm_avg], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms, gemm_avg = float(t[0]), float(t[1])
+    ms_per_step = tot_ms / args.steps
+    value = world * flops * args.steps / (tot_ms * 1e-3) / 1e12
+    launches_per_step = 3 + (1 if plan.split_k > 1 else 0)
+
+    # ---- end to end: host buffers through the C ABI, copies in the timed region
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hA, hB, hSA, hSB = pin(p.A), pin(p.B), pin(p.SA), pin(p.SB)
+    hC = pin(p.C.view(np.int16)) if p.C is not None else None
+    hD = torch.empty((M, N), dtype=torch.int16).pin_memory()
+    arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, args.split_k, p.beta != 0.0)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        mx.mxfp4_gemm_host(hD, hC, hA, hB, hSA, hSB, p.alpha, p.beta, M, N, K, args.split_k,
+                           arena, arena_b, stream)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    h2d = hA.numel() + hB.numel() + hSA.numel() + hSB.numel() + (hC.numel() * 2 if hC is not None else 0)
+    d2h = hD.numel() * 2
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    if args.workload in ("large", "mid", "tiny"):
+        peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        roof = {"bound": "tensor", "achieved": flops / (gemm_avg * 1e-3) / 1e12, "peak": peak,
+                "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
+                               f"{FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio)"}
+    else:
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": algo_bytes / (gemm_avg * 1e-3) / 1e9, "peak": peak,
+                "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = ("gemm_mxf4_kernel" + (" + splitk_reduce_kernel" if plan.split_k > 1 else ""))
+    roof["kernel_ms"] = gemm_avg
+    roof["algorithmic_bytes"] = algo_bytes
+    roof["flops"] = flops
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_throughput(p, 12.0, 7)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4", "data": "synthetic",
+        "config": {"workload": f"{args.workload} M={M} N={N} K={K}", "M": M, "N": N, "K": K,
+                   "alpha": p.alpha, "beta": p.beta, "seed": p.seed,
+                   "split_k": plan.split_k, "swap_ab": plan.swap_ab,
+                   "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
+                   "grid": [plan.grid_x, plan.grid_y, plan.grid_z],
+                   "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "step": "scale relayout A + scale relayout B + GEMM"
+                           + (" + split-K reduce" if plan.split_k > 1 else ""),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "api": "mxfp4_gemm_host (pinned host buffers)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_loop": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -87,7 +87,8 @@ size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k);
 
 /*
  * Bytes of a relaid scale buffer for `rows` rows of K elements:
- * ceil(rows/128) * 2*ceil(K/256) * 512.
+ * 2*ceil(rows/256) * 2*ceil(K/256) * 512 (row blocks of 128, their count
+ * rounded up to even so a 256-row tile never reads past the end).
  */
 size_t mxfp4_scale_relayout_size(int rows, int K);
 

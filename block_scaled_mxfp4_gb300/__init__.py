@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "Mxfp4Error", "lib", "library_path", "header_functions",
-    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_host", "mxfp4_scale_relayout",
+    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host", "mxfp4_scale_relayout",
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
     "mxfp4_wait_timeout_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
                                  f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp4_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
                                            f32, f32, i32, i32, i32, i32, vp, sz, vp]),
+            "mxfp4_gemm_noalloc": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                         f32, f32, i32, i32, i32, i32, vp]),
             "mxfp4_gemm_host": (i32, [vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32,
                                       vp, sz, vp]),
             "mxfp4_device_status": (i32, [ctypes.POINTER(ctypes.c_int), i32]),
@@ -165,6 +167,18 @@ def mxfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alp
     return _check(lib().mxfp4_gemm(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
                                    ld_sa, _p(scaleB), ld_sb, alpha, beta, M, N, K, split_k,
                                    _p(workspace), workspace_bytes, _stream(stream)), "mxfp4_gemm")
+
+
+def mxfp4_gemm_noalloc(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha,
+                       beta, M, N, K, split_k, stream=None):
+    """mxfp4_gemm without a workspace argument, for callers that cannot
+    allocate device memory: scratch comes from a fixed array in the library's
+    device image (MXFP4_NOALLOC_SCRATCH_BYTES).  Calls that overlap on the GPU
+    share that array and must be serialised by the caller."""
+    return _check(lib().mxfp4_gemm_noalloc(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb,
+                                           _p(scaleA), ld_sa, _p(scaleB), ld_sb, alpha, beta,
+                                           M, N, K, split_k, _stream(stream)),
+                  "mxfp4_gemm_noalloc")
 
 
 def mxfp4_gemm_prepacked(D, ldd, C, ldc, A, lda, B, ldb, scaleA_relaid, scaleB_relaid, alpha,

@@ -159,6 +159,28 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
 
 /*
+ * mxfp4_gemm for callers that cannot allocate device memory (the page has no
+ * counterpart: it exists for users whose allocator is owned by someone else
+ * or who may not synchronise the device through a cudaMalloc mid-run).  Same
+ * arguments and results as mxfp4_gemm minus the workspace: the scratch (relaid
+ * scales, split-K partials) lives in one array of MXFP4_NOALLOC_SCRATCH_BYTES
+ * inside the library's device image, held by every GPU that loads the library
+ * until exit.  Shapes whose mxfp4_gemm_workspace_size exceeds it are rejected
+ * with MXFP4_ERR_WORKSPACE before anything is enqueued.  The first call on a
+ * device looks up the array's device address (a runtime query); make that
+ * first call before capturing the stream into a graph.  All calls share the
+ * array: calls that overlap on the GPU race on it and must be serialised by
+ * the caller.  Each call rewrites all the scratch it reads, so leftovers from
+ * the previous call never leak into a result.
+ */
+#define MXFP4_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int mxfp4_gemm_noalloc(void *D, int64_t ldd, const void *C, int64_t ldc,
+                       const void *A, int64_t lda, const void *B, int64_t ldb,
+                       const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,
+                       float alpha, float beta, int M, int N, int K, int split_k, void *stream);
+
+/*
  * Read the device status word that bounded waits write on timeout into
  * *status (MXFP4_OK or MXFP4_ERR_TIMEOUT); if reset != 0 clear it.
  * Synchronous (it copies one int from the device).

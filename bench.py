@@ -4,9 +4,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--split-k S]
     python bench.py --impl reference ...     # the CPU oracle on a bounded sample
 
-One step is the whole hot path on one batch of resident inputs: relayout of
-both scale matrices into the tcgen05 layout, the tcgen05 GEMM, and the split-K
-reduce when K is split.  Steps are timed with CUDA events on the launching
+One step is the whole hot path on one batch of resident inputs: one
+mxfp4_gemm call -- the tcgen05 GEMM, which builds the tcgen05 scale layout
+from the row-major E8M0 scales itself, plus the split-K reduce when K is
+split.  (--prepacked times the other form: both scale relayout kernels and
+the GEMM on relaid scales.)  Steps are timed with CUDA events on the launching
 stream; L2 is flushed (a 512 MiB write) between timed steps, outside the
 events.  Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs
 an independent replica of the workload (the GEMM needs no exchange), the
@@ -43,6 +45,8 @@ def parse_args():
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prepacked", action="store_true",
+                    help="step = scale relayout A + B kernels + GEMM on relaid scales")
     return ap.parse_args()
 
 
@@ -215,19 +219,28 @@ def main():
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device=dev)
     sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device=dev)
-    wsb = mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, args.split_k)
-    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     plan = mx.mxfp4_plan_gemm(M, N, K, args.split_k, 0)
+    # When mxfp4_gemm would run a relayout pass, issue the same three kernels
+    # through the public calls so the GEMM kernel gets its own events.
+    split_form = args.prepacked or plan.relayout_pass
+    wsb = (mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, args.split_k) if split_form
+           else mx.mxfp4_gemm_workspace_size(M, N, K, args.split_k))
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        mx.mxfp4_scale_relayout(sfa, SA, M, K, K // 32, stream)
-        mx.mxfp4_scale_relayout(sfb, SB, N, K, K // 32, stream)
+        if split_form:
+            mx.mxfp4_scale_relayout(sfa, SA, M, K, K // 32, stream)
+            mx.mxfp4_scale_relayout(sfb, SB, N, K, K // 32, stream)
 
     def gemm():
-        mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
-                                args.split_k, ws, wsb, stream)
+        if split_form:
+            mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
+                                    args.split_k, ws, wsb, stream)
+        else:
+            mx.mxfp4_gemm(D, N, C, N, A, K, B, K, SA, K // 32, SB, K // 32, p.alpha, p.beta,
+                          M, N, K, args.split_k, ws, wsb, stream)
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
@@ -266,7 +279,8 @@ def main():
         tot_ms, gemm_avg = float(t[0]), float(t[1])
     ms_per_step = tot_ms / args.steps
     value = world * flops * args.steps / (tot_ms * 1e-3) / 1e12
-    launches_per_step = 3 + (1 if plan.split_k > 1 else 0)
+    launches_per_step = (3 if split_form else 1) + \
+        (1 if plan.split_k > 1 else 0)
 
     # ---- end to end: host buffers through the C ABI, copies in the timed region
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -315,7 +329,9 @@ def main():
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = None
-    roof["kernel"] = ("gemm_mxf4_kernel" + (" + splitk_reduce_kernel" if plan.split_k > 1 else ""))
+    roof["kernel"] = ("gemm_mxf4_kernel" + (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
+                      + (" (scales relaid by the relayout kernel, timed outside this figure)"
+                         if split_form else " (scale layout built in-kernel)"))
     roof["kernel_ms"] = gemm_avg
     roof["algorithmic_bytes"] = algo_bytes
     roof["flops"] = flops
@@ -335,7 +351,11 @@ def main():
                    "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
                    "grid": [plan.grid_x, plan.grid_y, plan.grid_z],
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
-                   "step": "scale relayout A + scale relayout B + GEMM"
+                   "step": ("scale relayout A + scale relayout B + GEMM on relaid scales"
+                            if args.prepacked else
+                            "mxfp4_gemm: scale relayout A + B kernels + GEMM on relaid scales"
+                            if plan.relayout_pass else
+                            "mxfp4_gemm: GEMM with in-kernel scale relayout")
                            + (" + split-K reduce" if plan.split_k > 1 else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,

@@ -1,7 +1,10 @@
 // C ABI of the block-scaled MXFP4 GEMM: argument checks, the tile / split-K
-// plan, TMA tensor maps and the launch sequence (scale relayout -> GEMM ->
-// optional split-K reduce).  Declared in include/mxfp4_gemm.h.
+// plan, TMA tensor maps and the launch sequence (GEMM -> optional split-K
+// reduce; the scale relayout runs inside the GEMM, or beforehand through
+// mxfp4_scale_relayout for prepacked scales).  Declared in include/mxfp4_gemm.h.
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -150,7 +153,17 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
             best_ratio = ratio;
         }
     }
-    const Candidate c = cands[best];
+    Candidate c = cands[best];
+    // Tuning override for sweeps: MXFP4_TILE="tile_n:stages" picks another
+    // compiled configuration of the same swap mode (ignored if there is none).
+    if (const char *env = std::getenv("MXFP4_TILE")) {
+        int tn = 0, st = 0;
+        if (std::sscanf(env, "%d:%d", &tn, &st) == 2) {
+            GemmShape probe{tn, st, swap};
+            if (gemm_smem_bytes(probe) > 0 && gemm_config_exists(probe))
+                c = {tn, st, gemm_smem_bytes(probe) * 2 <= 227 * 1024 ? 2 : 1};
+        }
+    }
     const int64_t gx = (P + kTileM - 1) / kTileM;
     const int64_t gy = (Q + c.tile_n - 1) / c.tile_n;
     if (gy > 65535 || gx > 0x7FFFFFFF)
@@ -189,6 +202,11 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         split > 1 ? align_up(static_cast<size_t>(split) * static_cast<size_t>(M) *
                              static_cast<size_t>(N) * sizeof(float))
                   : 0;
+    // With enough tiles to fill the GPU the GEMM is compute-bound: mxfp4_gemm
+    // then relays the row-major scales out in a separate pass (a few us) so
+    // the mainloop can move whole scale atoms with bulk copies.  Skinny and
+    // small shapes build the atoms inside the GEMM instead (no extra launches).
+    out->relayout_pass = (!swap && tiles >= sms) ? 1 : 0;
     if (shape) {
         shape->tile_n = c.tile_n;
         shape->stages = c.stages;
@@ -222,10 +240,18 @@ int check_common(const void *D, int64_t ldd, const void *C, int64_t ldc, const v
 }
 
 // Scale relayout (if needed) has been done; run the GEMM (+ reduce).
+// Scales as the kernel will read them: row-major [rows, ld] (atoms built in
+// the kernel) or already relaid into atoms.
+struct Scales {
+    const uint8_t *a, *b;
+    int64_t ld_a, ld_b;
+    bool rowmajor;
+};
+
 int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
-             const void *B, int64_t ldb, const uint8_t *sfA, const uint8_t *sfB, float alpha,
-             float beta, int M, int N, int K, const mxfp4_plan &plan, const GemmShape &shape,
-             float *partials, int sms, cudaStream_t stream)
+             const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M, int N,
+             int K, const mxfp4_plan &plan, const GemmShape &shape, float *partials, int sms,
+             cudaStream_t stream)
 {
     const bool swap = shape.swap != 0;
     CUtensorMap tmP, tmQ;
@@ -239,9 +265,18 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
 
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    a.sfP = swap ? sfB : sfA;
-    a.sfQ = swap ? sfA : sfB;
+    a.sfP = swap ? sc.b : sc.a;
+    a.sfQ = swap ? sc.a : sc.b;
     a.sf_rb_stride = sf_groups(K) * kSfAtomBytes;
+    a.sf_rowmajor = sc.rowmajor ? 1 : 0;
+    a.ldsP = swap ? sc.ld_b : sc.ld_a;
+    a.ldsQ = swap ? sc.ld_a : sc.ld_b;
+    a.sf_vec8 = sc.rowmajor && aligned(sc.a, 8) && aligned(sc.b, 8) && (sc.ld_a % 8) == 0 &&
+                (sc.ld_b % 8) == 0;
+    a.sf_async = sc.rowmajor && aligned(sc.a, 4) && aligned(sc.b, 4) && (sc.ld_a % 4) == 0 &&
+                 (sc.ld_b % 4) == 0;
+    a.rowsP = Prows;
+    a.rowsQ = Qrows;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -271,19 +306,6 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     return MXFP4_OK;
 }
 
-struct Layout {
-    size_t sfa, sfb, partials, total;
-};
-
-Layout workspace_layout(int M, int N, int K, const mxfp4_plan &plan)
-{
-    Layout l;
-    l.sfa = 0;
-    l.sfb = align_up(sf_relaid_bytes(M, K));
-    l.partials = l.sfb + align_up(sf_relaid_bytes(N, K));
-    l.total = l.partials + plan.workspace_bytes;
-    return l;
-}
 
 }  // namespace
 
@@ -337,7 +359,10 @@ size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k)
     mxfp4_plan plan;
     if (make_plan(M, N, K, split_k, device_sms_or_default(), &plan, nullptr) != MXFP4_OK)
         return 0;
-    return workspace_layout(M, N, K, plan).total;
+    size_t ws = plan.workspace_bytes;
+    if (plan.relayout_pass)
+        ws += align_up(sf_relaid_bytes(M, K)) + align_up(sf_relaid_bytes(N, K));
+    return ws;
 }
 
 int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld_src, void *stream)
@@ -357,6 +382,31 @@ int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld
     return MXFP4_OK;
 }
 
+// Shared body of mxfp4_gemm and mxfp4_gemm_prepacked after their own checks.
+static int gemm_entry(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M,
+                      int N, int K, int split_k, void *workspace, size_t workspace_bytes,
+                      void *stream)
+{
+    const int sms = device_sms_or_default();
+    mxfp4_plan plan;
+    GemmShape shape;
+    int st = make_plan(M, N, K, split_k, sms, &plan, &shape);
+    if (st != MXFP4_OK)
+        return st;
+    if (plan.workspace_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.workspace_bytes)
+            return MXFP4_ERR_WORKSPACE;
+        if (!aligned(workspace, kAlign))
+            return MXFP4_ERR_MISALIGNED;
+    }
+    st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
+                    static_cast<float *>(workspace), sms, static_cast<cudaStream_t>(stream));
+}
+
 int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
                          int64_t lda, const void *B, int64_t ldb, const void *scaleA_relaid,
                          const void *scaleB_relaid, float alpha, float beta, int M, int N, int K,
@@ -369,24 +419,10 @@ int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const
         return MXFP4_ERR_INVALID_ARG;
     if (!aligned(scaleA_relaid, 16) || !aligned(scaleB_relaid, 16))
         return MXFP4_ERR_MISALIGNED;
-    st = check_device();
-    if (st != MXFP4_OK)
-        return st;
-    const int sms = device_sms_or_default();
-    mxfp4_plan plan;
-    GemmShape shape;
-    st = make_plan(M, N, K, split_k, sms, &plan, &shape);
-    if (st != MXFP4_OK)
-        return st;
-    if (plan.workspace_bytes > 0) {
-        if (!workspace || workspace_bytes < plan.workspace_bytes)
-            return MXFP4_ERR_WORKSPACE;
-        if (!aligned(workspace, kAlign))
-            return MXFP4_ERR_MISALIGNED;
-    }
-    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, static_cast<const uint8_t *>(scaleA_relaid),
-                    static_cast<const uint8_t *>(scaleB_relaid), alpha, beta, M, N, K, plan, shape,
-                    static_cast<float *>(workspace), sms, static_cast<cudaStream_t>(stream));
+    const Scales sc{static_cast<const uint8_t *>(scaleA_relaid),
+                    static_cast<const uint8_t *>(scaleB_relaid), 0, 0, false};
+    return gemm_entry(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, split_k, workspace,
+                      workspace_bytes, stream);
 }
 
 int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
@@ -399,37 +435,43 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
         return st;
     if (!scaleA || !scaleB || ld_sa < K / 32 || ld_sb < K / 32)
         return MXFP4_ERR_INVALID_ARG;
-    if (!workspace)
-        return MXFP4_ERR_WORKSPACE;
-    if (!aligned(workspace, kAlign))
+    if (workspace && !aligned(workspace, kAlign))
         return MXFP4_ERR_MISALIGNED;
-    st = check_device();
-    if (st != MXFP4_OK)
-        return st;
     const int sms = device_sms_or_default();
     mxfp4_plan plan;
     GemmShape shape;
     st = make_plan(M, N, K, split_k, sms, &plan, &shape);
     if (st != MXFP4_OK)
         return st;
-    const Layout l = workspace_layout(M, N, K, plan);
-    if (workspace_bytes < l.total)
+    const size_t sfa_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(M, K)) : 0;
+    const size_t sfb_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(N, K)) : 0;
+    const size_t need = plan.workspace_bytes + sfa_bytes + sfb_bytes;
+    if (need > 0 && (!workspace || workspace_bytes < need))
         return MXFP4_ERR_WORKSPACE;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    st = check_device();
+    if (st != MXFP4_OK)
+        return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_scale_relayout(ws + l.sfa, static_cast<const uint8_t *>(scaleA), M, K, ld_sa, s) !=
-            cudaSuccess ||
-        launch_scale_relayout(ws + l.sfb, static_cast<const uint8_t *>(scaleB), N, K, ld_sb, s) !=
-            cudaSuccess)
-        return MXFP4_ERR_CUDA;
-    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, ws + l.sfa, ws + l.sfb, alpha, beta, M, N, K,
-                    plan, shape, reinterpret_cast<float *>(ws + l.partials), sms, s);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *partials = plan.workspace_bytes ? reinterpret_cast<float *>(ws) : nullptr;
+    Scales sc{static_cast<const uint8_t *>(scaleA), static_cast<const uint8_t *>(scaleB), ld_sa,
+              ld_sb, true};
+    if (plan.relayout_pass) {
+        uint8_t *sfa = ws + plan.workspace_bytes;
+        uint8_t *sfb = sfa + sfa_bytes;
+        if (launch_scale_relayout(sfa, sc.a, M, K, ld_sa, s) != cudaSuccess ||
+            launch_scale_relayout(sfb, sc.b, N, K, ld_sb, s) != cudaSuccess)
+            return MXFP4_ERR_CUDA;
+        sc = Scales{sfa, sfb, 0, 0, false};
+    }
+    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
+                    partials, sms, s);
 }
 
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
 {
     const size_t ws = mxfp4_gemm_workspace_size(M, N, K, split_k);
-    if (ws == 0)
+    if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_k < 0 || split_k > kMaxSplit)
         return 0;
     const size_t mn2 = align_up(static_cast<size_t>(M) * N * 2);
     return align_up(static_cast<size_t>(M) * K / 2) + align_up(static_cast<size_t>(N) * K / 2) +

@@ -155,6 +155,71 @@ __device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int z, int m0
     }
 }
 
+// Row-major scales -> one lane's share of a 128-row block for stage kt: rows
+// row0 + lane + 32j (j = 0..3), K blocks 8kt .. 8kt+7 as two 4-byte words
+// (byte b of word g = block 8kt + 4g + b).  Missing rows / blocks read 0x7F.
+__device__ __forceinline__ void load_sf_rows(const uint8_t *S, int64_t ld, int rows, int kblocks,
+                                             int row0, int kt, int vec8, int lane,
+                                             uint32_t (&w)[4][2])
+{
+    const int kb0 = kt * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = row0 + lane + 32 * j;
+        if (r < rows) {
+            const uint8_t *p = S + static_cast<int64_t>(r) * ld + kb0;
+            if (vec8 && kb0 + 8 <= kblocks) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+                w[j][0] = v.x;
+                w[j][1] = v.y;
+            } else {
+                uint32_t x[2] = {0u, 0u};
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const uint32_t v = (kb0 + b < kblocks) ? static_cast<uint32_t>(p[b]) : 0x7Fu;
+                    x[b >> 2] |= v << (8 * (b & 3));
+                }
+                w[j][0] = x[0];
+                w[j][1] = x[1];
+            }
+        } else {
+            w[j][0] = w[j][1] = 0x7F7F7F7Fu;
+        }
+    }
+}
+
+// Asynchronous form of load_sf_rows + store_sf_lines: each 4-byte scale word
+// goes straight from global memory to its place in the atom (row lane + 32j,
+// word g -> atom g, line lane, word j).  Missing rows / blocks are zero-filled
+// (their operand data is zero-filled by TMA too, so the product is 0).
+__device__ __forceinline__ void copy_sf_rows_async(uint8_t *atoms, const uint8_t *S, int64_t ld,
+                                                   int rows, int kblocks, int row0, int kt,
+                                                   int lane)
+{
+    const int kb0 = kt * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = row0 + lane + 32 * j;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int have = kblocks - (kb0 + 4 * g);
+            const uint32_t bytes = (r < rows && have > 0) ? static_cast<uint32_t>(min(have, 4)) : 0u;
+            const uint8_t *src = bytes ? S + static_cast<int64_t>(r) * ld + kb0 + 4 * g : S;
+            cp_async_4(atoms + g * kSfAtomBytes + 16 * lane + 4 * j, src, bytes);
+        }
+    }
+}
+
+// Line `lane` of the two atoms of a stage: 16 bytes = rows lane, lane+32,
+// lane+64, lane+96, four K blocks each.
+__device__ __forceinline__ void store_sf_lines(uint8_t *atoms, const uint32_t (&w)[4][2], int lane)
+{
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+        *reinterpret_cast<uint4 *>(atoms + g * kSfAtomBytes + 16 * lane) =
+            make_uint4(w[0][g], w[1][g], w[2][g], w[3][g]);
+}
+
 template <int BN, int STAGES, bool SWAP>
 __global__ void __launch_bounds__(192, 1)
     gemm_mxf4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmP,
@@ -181,7 +246,7 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], !a.sf_rowmajor ? 1 : a.sf_async ? 33 : 2);
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
@@ -203,7 +268,102 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 4) {
         // ------------------------------------------------------ producer --
-        if (lane == 0 && nkt > 0) {
+        if (a.sf_rowmajor && a.sf_async && nkt > 0) {
+            // Whole warp: lane 0 issues the operand TMAs; every lane copies its
+            // lines of the stage's scale atoms with 4-byte cp.async straight
+            // from the row-major scales, and the stage's full barrier counts
+            // one arrival per lane once that lane's copies have landed.
+            const uint64_t pol_p = a.stream_p ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_last();
+            const int kblocks = a.K / 32;
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int i = 0; i < nkt; ++i) {
+                const bool ok =
+                    mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_limit, &g_device_status);
+                if (!__all_sync(0xffffffffu, ok))
+                    break;
+                uint8_t *st = smem + stage * Cf::STAGE_BYTES;
+                const int kt = kt0 + i;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES + Cf::Q_BYTES);
+                    tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
+                    tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
+                }
+                uint8_t *sf_s = st + Cf::P_BYTES + Cf::Q_BYTES;
+                copy_sf_rows_async(sf_s, a.sfP, a.ldsP, a.rowsP, kblocks, p0, kt, lane);
+#pragma unroll
+                for (int r = 0; r < Cf::NQ; ++r)
+                    copy_sf_rows_async(sf_s + Cf::SFP_BYTES + r * 2 * kSfAtomBytes, a.sfQ, a.ldsQ,
+                                       a.rowsQ, kblocks, q0 + r * kSfRowBlock, kt, lane);
+                cp_async_mbar_arrive(&full[stage]);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (lane == 0 && *abort_flag) {
+                for (int i = max(0, issued - STAGES); i < issued; ++i)
+                    mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
+            }
+        } else if (a.sf_rowmajor && nkt > 0) {
+            // Whole warp: lane 0 issues the operand TMAs; every lane builds its
+            // lines of the stage's scale atoms from row-major scales it loaded
+            // one stage ahead (so the global loads overlap the ring wait).
+            const uint64_t pol_p = a.stream_p ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_last();
+            const int kblocks = a.K / 32;
+            uint32_t wp[4][2];
+            uint32_t wq[Cf::NQ][4][2];
+            auto load_sf = [&](int kt) {
+                load_sf_rows(a.sfP, a.ldsP, a.rowsP, kblocks, p0, kt, a.sf_vec8, lane, wp);
+#pragma unroll
+                for (int r = 0; r < Cf::NQ; ++r)
+                    load_sf_rows(a.sfQ, a.ldsQ, a.rowsQ, kblocks, q0 + r * kSfRowBlock, kt,
+                                 a.sf_vec8, lane, wq[r]);
+            };
+            load_sf(kt0);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int i = 0; i < nkt; ++i) {
+                const bool ok =
+                    mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_limit, &g_device_status);
+                if (!__all_sync(0xffffffffu, ok))
+                    break;
+                uint8_t *st = smem + stage * Cf::STAGE_BYTES;
+                const int kt = kt0 + i;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES + Cf::Q_BYTES);
+                    tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
+                    tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
+                }
+                uint8_t *sf_s = st + Cf::P_BYTES + Cf::Q_BYTES;
+                store_sf_lines(sf_s, wp, lane);
+#pragma unroll
+                for (int r = 0; r < Cf::NQ; ++r)
+                    store_sf_lines(sf_s + Cf::SFP_BYTES + r * 2 * kSfAtomBytes, wq[r], lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&full[stage]);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (i + 1 < nkt)
+                    load_sf(kt + 1);
+            }
+            if (lane == 0 && *abort_flag) {
+                for (int i = max(0, issued - STAGES); i < issued; ++i)
+                    mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
+            }
+        } else if (lane == 0 && nkt > 0) {
+            // Prepacked scales: one thread issues the operand TMAs and 1-D bulk
+            // copies of the stage's relaid scale atoms.
             const uint64_t pol_p = a.stream_p ? l2_policy_evict_first() : l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_last();
             const uint8_t *sfp = a.sfP + static_cast<int64_t>(p0 / kSfRowBlock) * a.sf_rb_stride;
@@ -246,12 +406,17 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t idesc = idesc_mxf4(kTileM, BN);
             const uint32_t t_sf = tmem + BN;
             // A 64-row Q tile uses the upper or lower half of its 128-row atom.
-            const uint32_t q_off = BN < 128 ? static_cast<uint32_t>((q0 % kSfRowBlock) / 32) : 0u;
+            // (Row-major scales are built relative to q0, so no offset there.)
+            const uint32_t q_off = (BN < 128 && !a.sf_rowmajor)
+                                       ? static_cast<uint32_t>((q0 % kSfRowBlock) / 32)
+                                       : 0u;
             int stage = 0;
             uint32_t phase = 0;
             for (int i = 0; i < nkt; ++i) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
                     break;
+                if (a.sf_rowmajor)
+                    fence_proxy_async_smem();   // scale atoms were written by threads
                 tc_fence_after();
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;
                 const uint32_t sfp_t = t_sf + stage * Cf::SF_COLS;
@@ -353,6 +518,14 @@ size_t gemm_smem_bytes(const GemmShape &s)
         return s.stages == 4 ? Cfg<64, 4>::SMEM_BYTES : s.stages == 8 ? Cfg<64, 8>::SMEM_BYTES : 0;
     default: return 0;
     }
+}
+
+bool gemm_config_exists(const GemmShape &s)
+{
+    if (!s.swap)
+        return (s.tile_n == 256 && s.stages == 4) || (s.tile_n == 128 && s.stages == 6) ||
+               (s.tile_n == 64 && s.stages == 8);
+    return s.tile_n == 64 && (s.stages == 4 || s.stages == 8);
 }
 
 cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,

@@ -26,9 +26,14 @@ inline size_t sf_relaid_bytes(int rows, int K)
 // Arguments of one GEMM launch.  "P" is the operand whose rows feed the MMA's
 // M side (A, or B when swapped), "Q" the operand on the MMA's N side.
 struct GemmArgs {
-    const uint8_t *sfP;     // relaid scales of P
-    const uint8_t *sfQ;     // relaid scales of Q
-    int64_t sf_rb_stride;   // bytes per 128-row block of relaid scales
+    const uint8_t *sfP;     // scales of P: relaid atoms, or row-major if sf_rowmajor
+    const uint8_t *sfQ;     // scales of Q, same form
+    int64_t sf_rb_stride;   // relaid: bytes per 128-row block of atoms
+    int sf_rowmajor;        // 1: scales are row-major E8M0 [rows, ld] (atoms built in-kernel)
+    int sf_vec8;            // row-major scales allow aligned 8-byte loads per stage
+    int sf_async;           // row-major scales allow 4-byte cp.async (aligned rows)
+    int64_t ldsP, ldsQ;     // row-major: row strides in bytes
+    int rowsP, rowsQ;       // rows of P and Q
     int M, N, K;
     int kt_total;           // ceil(K / 256)
     int kt_per_split;
@@ -52,6 +57,9 @@ struct GemmShape {
 
 // Dynamic shared memory one GEMM configuration needs (0 if unsupported).
 size_t gemm_smem_bytes(const GemmShape &s);
+
+// Whether (tile_n, stages, swap) is one of the compiled configurations.
+bool gemm_config_exists(const GemmShape &s);
 
 cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
                         const GemmShape &s, dim3 grid, cudaStream_t stream);

@@ -55,9 +55,11 @@ extern "C" int mxfp4_gemm_noalloc(void *D, int64_t ldd, const void *C, int64_t l
                                   int64_t ld_sa, const void *scaleB, int64_t ld_sb, float alpha,
                                   float beta, int M, int N, int K, int split_k, void *stream)
 {
+    mxfp4_plan plan;
+    const int st = mxfp4_plan_gemm(M, N, K, split_k, 0, &plan);
+    if (st != MXFP4_OK)
+        return st;
     const size_t need = mxfp4_gemm_workspace_size(M, N, K, split_k);
-    if (need == 0)
-        return MXFP4_ERR_INVALID_ARG;
     if (need > static_cast<size_t>(MXFP4_NOALLOC_SCRATCH_BYTES))
         return MXFP4_ERR_WORKSPACE;   // this shape needs more scratch than the fixed array
     void *scratch = scratch_on_current_device();

@@ -15,31 +15,51 @@ namespace mxfp4 {
 // line holds rows i, i+32, i+64, i+96 -- the 32x128b source shape that
 // tcgen05.cp replicates into the four TMEM lane groups.
 //
-// One CTA of 128 threads handles one 128-row block and up to kGroupsPerCta
-// atoms along K; thread t writes the 4-byte word t of each atom, so a warp's
-// stores are contiguous.
-constexpr int kGroupsPerCta = 8;
+// One CTA of 256 threads handles one 128-row block and up to kGroupsPerCta
+// atoms along K: it reads the 128 x (4*kGroupsPerCta) scale bytes with
+// consecutive threads on consecutive words of a row, stages them in shared
+// memory (rows padded to an odd word count, so the column reads below hit 32
+// different banks), and writes the atoms as 16-byte lines, consecutive
+// threads on consecutive lines.
+constexpr int kGroupsPerCta = 16;
+constexpr int kRelayoutThreads = 256;
 
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kRelayoutThreads)
     scale_relayout_kernel(uint8_t *__restrict__ dst, const uint8_t *__restrict__ src, int rows,
-                          int kblocks, int64_t ld, int64_t groups)
+                          int kblocks, int64_t ld, int64_t groups, int vec4)
 {
+    __shared__ uint32_t tile[128][kGroupsPerCta + 1];
     const int t = threadIdx.x;
-    const int i = t >> 2;                 // line inside the atom
-    const int j = t & 3;                  // which of the 4 rows of the line
     const int64_t rb = blockIdx.x;
-    const int64_t row = rb * 128 + 32 * j + i;
     const int64_t g0 = static_cast<int64_t>(blockIdx.y) * kGroupsPerCta;
-    const uint8_t *srow = src + row * ld;
-    for (int64_t g = g0; g < min(g0 + kGroupsPerCta, groups); ++g) {
-        uint32_t word = 0;
+    const int ng = static_cast<int>(groups - g0 < kGroupsPerCta ? groups - g0 : kGroupsPerCta);
+
+    for (int e = t; e < 128 * kGroupsPerCta; e += kRelayoutThreads) {
+        const int r = e / kGroupsPerCta;
+        const int w = e % kGroupsPerCta;
+        const int64_t row = rb * 128 + r;
+        const int64_t kb = (g0 + w) * 4;
+        uint32_t word = 0x7F7F7F7Fu;
+        if (row < rows && w < ng) {
+            const uint8_t *p = src + row * ld + kb;
+            if (vec4 && kb + 4 <= kblocks) {
+                word = __ldg(reinterpret_cast<const uint32_t *>(p));
+            } else {
+                word = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int64_t kb = g * 4 + b;
-            const uint32_t v = (row < rows && kb < kblocks) ? srow[kb] : 0x7Fu;
-            word |= v << (8 * b);
+                for (int b = 0; b < 4; ++b)
+                    word |= (kb + b < kblocks ? static_cast<uint32_t>(p[b]) : 0x7Fu) << (8 * b);
+            }
         }
-        reinterpret_cast<uint32_t *>(dst + (rb * groups + g) * kSfAtomBytes)[t] = word;
+        tile[r][w] = word;
+    }
+    __syncthreads();
+    uint8_t *out = dst + (rb * groups + g0) * kSfAtomBytes;
+    for (int e = t; e < ng * 32; e += kRelayoutThreads) {
+        const int atom = e / 32;
+        const int i = e % 32;
+        reinterpret_cast<uint4 *>(out + atom * kSfAtomBytes)[i] =
+            make_uint4(tile[i][atom], tile[i + 32][atom], tile[i + 64][atom], tile[i + 96][atom]);
     }
 }
 
@@ -48,9 +68,11 @@ cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, in
 {
     const int64_t groups = sf_groups(K);
     const int64_t rblocks = sf_row_blocks(rows);
+    const int vec4 = (reinterpret_cast<uintptr_t>(src) % 4 == 0) && (ld % 4 == 0);
     dim3 grid(static_cast<unsigned>(rblocks),
               static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
-    scale_relayout_kernel<<<grid, 128, 0, stream>>>(dst, src, rows, K / 32, ld, groups);
+    scale_relayout_kernel<<<grid, kRelayoutThreads, 0, stream>>>(dst, src, rows, K / 32, ld, groups,
+                                                                 vec4);
     return cudaGetLastError();
 }
 

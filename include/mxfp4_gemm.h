@@ -64,7 +64,10 @@ typedef struct mxfp4_plan {
     int split_k;            /* K splits; > 1 adds the fp32 reduce kernel */
     int k_tiles_per_split;  /* tile_k blocks handled by one split */
     int grid_x, grid_y, grid_z;
-    size_t workspace_bytes; /* what mxfp4_gemm needs for this plan */
+    size_t workspace_bytes; /* split-K partials (what mxfp4_gemm_prepacked needs) */
+    int relayout_pass;      /* 1: mxfp4_gemm relays the scales out in a separate
+                               pass into its workspace (compute-bound shapes);
+                               0: the GEMM builds the scale layout itself */
 } mxfp4_plan;
 
 /*
@@ -79,9 +82,11 @@ typedef struct mxfp4_plan {
 int mxfp4_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out);
 
 /*
- * Bytes of device workspace mxfp4_gemm needs: the two relaid scale buffers
- * plus, when the plan splits K, the fp32 partial sums [split, M, N].
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace mxfp4_gemm needs: the fp32 partial sums
+ * [split, M, N] when the plan splits K, plus both relaid scale buffers when
+ * the plan has a relayout pass; 0 when neither applies (then the workspace
+ * may be NULL).  Returns 0 for invalid sizes too (mxfp4_plan_gemm tells them
+ * apart).
  */
 size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k);
 
@@ -119,7 +124,11 @@ int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld
  *   split_k  0 = heuristic, else 1..16.  Splits reduce in fp32 in a fixed
  *            order, so results are bitwise reproducible run to run.
  *   workspace  device, >= mxfp4_gemm_workspace_size(M, N, K, split_k) bytes,
- *              256-byte aligned; contents need not be initialised.
+ *              256-byte aligned, contents need not be initialised; NULL when
+ *              that size is 0.
+ * The scales are read row-major.  Compute-bound shapes (plan.relayout_pass)
+ * first relay them out into the workspace with the relayout kernel; the
+ * others build the tcgen05 scale layout inside the GEMM itself.
  */
 int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -130,8 +139,9 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
 /*
  * As mxfp4_gemm, with both scale buffers already in the relaid layout
  * produced by mxfp4_scale_relayout (scaleA for M rows, scaleB for N rows, at
- * the same K).  The workspace then only holds the split-K partials:
- * mxfp4_gemm_prepacked_workspace_size bytes (0 is valid when split_k == 1).
+ * the same K); the GEMM then copies whole scale atoms with bulk copies.  The
+ * workspace holds the split-K partials: mxfp4_gemm_prepacked_workspace_size
+ * bytes (plan.workspace_bytes).
  */
 int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc,
                          const void *A, int64_t lda, const void *B, int64_t ldb,

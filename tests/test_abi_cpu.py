@@ -90,9 +90,15 @@ def test_sizes(L):
     assert mx.mxfp4_scale_relayout_size(5, 48) == 0
     assert mx.mxfp4_gemm_workspace_size(0, 1, 32, 0) == 0
     assert mx.mxfp4_gemm_workspace_size(1, 1, 32, 17) == 0
-    ws = mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4)
-    assert ws >= mx.mxfp4_scale_relayout_size(1, 8192) + mx.mxfp4_scale_relayout_size(8192, 8192) \
-        + 4 * 8192 * 4
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 4 * 8192 * 4
+    # The large shape relays its scales out first: workspace = both relaid buffers.
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 0)
+    assert p.relayout_pass == 1
+    assert mx.mxfp4_gemm_workspace_size(8192, 8192, 8192, 1) == \
+        2 * mx.mxfp4_scale_relayout_size(8192, 8192)
+    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 0).relayout_pass == 0
+    assert mx.mxfp4_gemm_workspace_size(128, 256, 512, 1) == 0
+    assert mx.mxfp4_gemm_host_arena_size(8192, 8192, 8192, 1, False) > 0
 
 
 def _call_gemm(L, **kw):
@@ -115,7 +121,7 @@ def _call_gemm(L, **kw):
     (dict(beta=1.0), -1), (dict(beta=1.0, C=0x6000, ldc=100), -1),
     (dict(split=17), -1), (dict(split=-1), -1),
     (dict(lda=528), -3), (dict(ldb=520), -3), (dict(A=0x2008), -3), (dict(B=0x3004), -3),
-    (dict(ws=None), -4), (dict(ws=0x10010), -3),
+    (dict(ws=None, split=4), -4), (dict(ws=0x10010), -3), (dict(wsb=1000, split=2), -4),
 ])
 def test_gemm_argument_validation(L, kw, status):
     # These return before any device call, so they run without a GPU.

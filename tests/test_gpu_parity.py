@@ -191,6 +191,7 @@ def test_large_sampled(oracle_mod):
 EDGE_SHAPES = [
     (1, 16, 32), (7, 40, 96), (63, 200, 288), (65, 300, 256), (129, 520, 1024),
     (300, 2048, 1024), (1, 4096, 2048), (2, 129, 64), (200, 37, 160), (130, 130, 544),
+    (5, 64, 128), (33, 100, 384), (257, 300, 384), (2000, 2600, 288),
 ]
 
 
@@ -298,12 +299,19 @@ def test_device_errors_are_reported():
     p = problem("tiny")
     dev = Dev(p)
     D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
-    need = mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 0)
+    need = mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 2)     # split-K partials
+    assert need > 0
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     with pytest.raises(mx.Mxfp4Error) as e:
         mx.mxfp4_gemm(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32, dev.SB,
-                      p.K // 32, 1.0, 0.0, p.M, p.N, p.K, 0, ws, need - 1)
+                      p.K // 32, 1.0, 0.0, p.M, p.N, p.K, 2, ws, need - 1)
     assert e.value.status == -4
+    # Without split the GEMM needs no workspace at all.
+    assert mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 1) == 0
+    mx.mxfp4_gemm(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32, dev.SB,
+                  p.K // 32, 1.0, 0.0, p.M, p.N, p.K, 1, None, 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), run_gemm(dev, split_k=1))
 
 
 def test_bounded_wait_times_out_cleanly():

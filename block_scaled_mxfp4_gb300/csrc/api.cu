@@ -3,6 +3,7 @@
 // reduce; the scale relayout runs inside the GEMM, or beforehand through
 // mxfp4_scale_relayout for prepacked scales).  Declared in include/mxfp4_gemm.h.
 #include <atomic>
+#include <chrono>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -101,18 +102,109 @@ bool encode_operand(CUtensorMap *map, const void *base, int rows, int K, int64_t
     return r == CUDA_SUCCESS;
 }
 
+// 2-D uint8 view [rows, K/32] of row-major E8M0 scales (row stride ld bytes);
+// box 16 bytes (16 scale blocks = two 256-K stages) x box_rows, no swizzle.
+bool encode_scales(CUtensorMap *map, const void *base, int rows, int K, int64_t ld, int box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Relaid scale atoms viewed as 2-D uint32 [atoms, 128] (one 512-byte atom per
+// row); a box of 2 rows = the two atoms of one 256-K stage of a 128-row block.
+bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const int64_t atoms = sf_row_blocks(rows) * sf_groups(K);
+    cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(atoms)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kSfAtomBytes)};
+    cuuint32_t box[2] = {128u, 2u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct Candidate {
     int tile_n;
     int stages;
     int ctas_per_sm;
+    int nacc;               // accumulator buffers of the persistent form
 };
+
+// Stream-K schedule for `slots` resident CTAs (see Sched in internal.h).
+struct SkPlan {
+    int tiles_p, tiles_q, kt, ctas, dp_waves, sk_tile0, pcols;
+    long long sk_units;
+    size_t partial_bytes;
+};
+
+SkPlan stream_k_plan(int64_t P, int64_t Q, int K, int tile_n, int64_t slots)
+{
+    SkPlan k;
+    k.tiles_p = static_cast<int>((P + kTileM - 1) / kTileM);
+    k.tiles_q = static_cast<int>((Q + tile_n - 1) / tile_n);
+    k.kt = (K + kTileK - 1) / kTileK;
+    const int64_t T = static_cast<int64_t>(k.tiles_p) * k.tiles_q;
+    if (slots > kMaxPersistentCtas)
+        slots = kMaxPersistentCtas;
+    if (T >= slots) {
+        k.dp_waves = static_cast<int>(T / slots);
+        k.ctas = static_cast<int>(slots);
+    } else {
+        k.dp_waves = 0;
+        const int64_t units = T * k.kt;
+        k.ctas = static_cast<int>(units < slots ? units : slots);
+    }
+    k.sk_tile0 = k.dp_waves * k.ctas;
+    k.sk_units = (T - k.sk_tile0) * static_cast<long long>(k.kt);
+    // A partial holds the tile's columns that exist (Q can be narrower than a
+    // tile: a skinny M has only M of the swapped tile's columns).
+    k.pcols = static_cast<int>(Q < tile_n ? Q : tile_n);
+    k.partial_bytes =
+        k.sk_units > 0 ? static_cast<size_t>(k.ctas) * k.pcols * kTileM * sizeof(float) : 0;
+    return k;
+}
 
 // Tile / swap / split-K choice.  Candidates are scored as the page's section
 // "Tile selection heuristic" scores its tiles: fewest waves (ceil(tiles /
 // resident CTA slots)), then the fullest last wave, then the larger
 // tile_m*tile_n/(tile_m+tile_n); the fixed candidate order breaks ties.
-// When the tiles do not fill the resident slots, K is split so they do
-// (at least kMinKtPerSplit stages per split, at most 16 splits).
+// split_k >= 1 runs one CTA per (tile, K split) and, for split_k > 1, the
+// fixed-order fp32 reduce.  split_k == 0 picks the split itself: 1 when the
+// tiles fill at least half a wave, else enough splits to fill the resident
+// CTA slots, each split keeping at least kMinSplitStages K stages.
+// MXFP4_KERNEL=persistent|pair (a tuning / test override, read per call)
+// routes split_k == 0 to the persistent stream-K kernel or, for shapes of at
+// least 256 x 256 without swap, the CTA-pair kernel instead.
+constexpr int kMinSplitStages = 8;
+
+enum class KernelChoice { Auto, Persistent, Pair };
+
+KernelChoice kernel_override()
+{
+    const char *env = std::getenv("MXFP4_KERNEL");
+    if (!env)
+        return KernelChoice::Auto;
+    if (std::strcmp(env, "persistent") == 0)
+        return KernelChoice::Persistent;
+    if (std::strcmp(env, "pair") == 0)
+        return KernelChoice::Pair;
+    return KernelChoice::Auto;
+}
+
 int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape)
 {
     if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_req < 0 || split_req > kMaxSplit)
@@ -123,16 +215,21 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     const int64_t P = swap ? N : M;
     const int64_t Q = swap ? M : N;
     const int kt = (K + kTileK - 1) / kTileK;
+    const KernelChoice choice = split_req == 0 ? kernel_override() : KernelChoice::Auto;
+    const int64_t tiles256 = ((static_cast<int64_t>(M) + 255) / 256) * ((static_cast<int64_t>(N) + 255) / 256);
+    const bool use_pair = choice == KernelChoice::Pair && !swap && M >= 256 && N >= 256;
+    const bool persistent = choice == KernelChoice::Persistent || use_pair;
 
     Candidate cands[3];
     int nc = 0;
     if (swap) {
-        cands[nc++] = {64, 4, 2};
+        // Persistent: one 8-stage CTA per SM; one-tile split: two 4-stage CTAs.
+        cands[nc++] = persistent ? Candidate{64, 8, 1, 2} : Candidate{64, 4, 2, 2};
     } else {
-        cands[nc++] = {256, 4, 1};
-        cands[nc++] = {128, 6, 1};
+        cands[nc++] = {256, 4, 1, 1};
+        cands[nc++] = {128, 6, 1, 2};
         if (Q <= 64)
-            cands[nc++] = {64, 8, 1};
+            cands[nc++] = {64, 8, 1, 2};
     }
     int best = -1;
     int64_t best_waves = 0;
@@ -159,9 +256,12 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     if (const char *env = std::getenv("MXFP4_TILE")) {
         int tn = 0, st = 0;
         if (std::sscanf(env, "%d:%d", &tn, &st) == 2) {
-            GemmShape probe{tn, st, swap};
-            if (gemm_smem_bytes(probe) > 0 && gemm_config_exists(probe))
-                c = {tn, st, gemm_smem_bytes(probe) * 2 <= 227 * 1024 ? 2 : 1};
+            const int nacc = tn == 256 ? 1 : 2;
+            GemmShape probe{tn, st, swap, persistent ? 1 : 0, nacc, 1};
+            const bool have = persistent ? gemm_persistent_smem_bytes(probe) > 0
+                                             : (gemm_smem_bytes(probe) > 0 && gemm_config_exists(probe));
+            if (have)
+                c = {tn, st, gemm_smem_bytes(probe) * 2 <= 227 * 1024 ? 2 : 1, nacc};
         }
     }
     const int64_t gx = (P + kTileM - 1) / kTileM;
@@ -174,14 +274,13 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     int split = 1;
     if (split_req > 0) {
         split = split_req;
-    } else if (tiles < slots) {
-        const int kMinKtPerSplit = swap ? 4 : 4;
-        int64_t s = slots / tiles;
+    } else if (!persistent && 2 * tiles < slots) {
+        const int64_t by_slots = slots / tiles;
+        const int64_t by_k = kt / kMinSplitStages;
+        int64_t s = by_slots < by_k ? by_slots : by_k;
         if (s > kMaxSplit)
             s = kMaxSplit;
-        if (s > kt / kMinKtPerSplit)
-            s = kt / kMinKtPerSplit;
-        split = s < 1 ? 1 : static_cast<int>(s);
+        split = s > 1 ? static_cast<int>(s) : 1;
     }
     if (split > kt)
         split = kt;
@@ -198,19 +297,55 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     out->grid_x = static_cast<int>(gx);
     out->grid_y = static_cast<int>(gy);
     out->grid_z = split;
-    out->workspace_bytes =
-        split > 1 ? align_up(static_cast<size_t>(split) * static_cast<size_t>(M) *
-                             static_cast<size_t>(N) * sizeof(float))
-                  : 0;
+    size_t partials = split > 1 ? static_cast<size_t>(split) * static_cast<size_t>(M) *
+                                      static_cast<size_t>(N) * sizeof(float)
+                                : 0;
+    // Persistent stream-K over all resident CTA slots (override only).
+    out->persistent = persistent ? 1 : 0;
+    out->ctas = 0;
+    out->dp_waves = 0;
+    out->sk_units = 0;
+    if (out->persistent) {
+        const SkPlan k = stream_k_plan(P, Q, K, c.tile_n, slots);
+        out->split_k = 1;
+        out->k_tiles_per_split = kt;
+        out->ctas = k.ctas;
+        out->dp_waves = k.dp_waves;
+        out->sk_units = k.sk_units;
+        out->grid_x = k.ctas;
+        out->grid_y = 1;
+        out->grid_z = 1;
+        partials = k.partial_bytes;
+    }
+    out->pair = use_pair;
+    if (use_pair) {
+        out->tile_m = 256;
+        out->tile_n = 256;
+        out->stages = 6;
+        out->dp_waves = static_cast<int>((tiles256 + sms / 2 - 1) / (sms / 2));
+        out->sk_units = 0;
+        out->ctas = 2 * static_cast<int>(tiles256 < sms / 2 ? tiles256 : sms / 2);
+        out->grid_x = out->ctas;
+        partials = 0;
+    }
+    // Every workspace starts with the reserved stream-K flag bytes.
+    out->workspace_bytes = partials ? kFlagBytes + align_up(partials) : 0;
     // With enough tiles to fill the GPU the GEMM is compute-bound: mxfp4_gemm
     // then relays the row-major scales out in a separate pass (a few us) so
     // the mainloop can move whole scale atoms with bulk copies.  Skinny and
     // small shapes build the atoms inside the GEMM instead (no extra launches).
-    out->relayout_pass = (!swap && tiles >= sms) ? 1 : 0;
+    // (The persistent kernel stages row-major scales by TMA itself; the
+    // CTA-pair kernel reads relaid atoms.)
+    out->relayout_pass = (use_pair || (!persistent && !swap && tiles >= sms)) ? 1 : 0;
     if (shape) {
         shape->tile_n = c.tile_n;
         shape->stages = c.stages;
         shape->swap = swap;
+        shape->persistent = out->persistent;
+        shape->nacc = c.nacc;
+        shape->ctas_per_sm = c.ctas_per_sm;
+        shape->pair = use_pair;
+        shape->pair_ctas = out->ctas;
     }
     return MXFP4_OK;
 }
@@ -248,11 +383,61 @@ struct Scales {
     bool rowmajor;
 };
 
+std::atomic<unsigned> g_epoch{0};
+std::once_flag g_epoch_once;
+
+// Next per-call flag value for the stream-K handshake (never 0).  The count
+// starts from a clock-derived value so that a fresh workspace holding small
+// integers does not look ready by chance; stale flags of earlier calls hold
+// earlier values and never match.
+int next_epoch()
+{
+    std::call_once(g_epoch_once, [] {
+        const auto t = std::chrono::steady_clock::now().time_since_epoch().count();
+        g_epoch.store(static_cast<unsigned>((t ^ (t >> 29)) * 2654435761u) | 0x40000000u);
+    });
+    unsigned e = ++g_epoch;
+    while ((e & 0x7FFFFFFFu) == 0)
+        e = ++g_epoch;
+    return static_cast<int>(e & 0x7FFFFFFFu);
+}
+
+// ws: workspace base (flags at offset 0, partials after kFlagBytes), or
+// nullptr when the plan needs none.
 int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
              const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M, int N,
-             int K, const mxfp4_plan &plan, const GemmShape &shape, float *partials, int sms,
+             int K, const mxfp4_plan &plan, const GemmShape &shape, uint8_t *ws, int sms,
              cudaStream_t stream)
 {
+    float *partials = ws ? reinterpret_cast<float *>(ws + kFlagBytes) : nullptr;
+    if (shape.pair) {
+        if (sc.rowmajor)
+            return MXFP4_ERR_INVALID_ARG;            // the pair kernel reads relaid atoms
+        CUtensorMap tmA, tmB, tmSA, tmSB;
+        if (!encode_operand(&tmA, A, M, K, lda, kTileM) || !encode_operand(&tmB, B, N, K, ldb, kTileM) ||
+            !encode_atoms(&tmSA, sc.a, M, K) || !encode_atoms(&tmSB, sc.b, N, K))
+            return MXFP4_ERR_CUDA;
+        GemmArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        a.kt_total = (K + kTileK - 1) / kTileK;
+        a.alpha = alpha;
+        a.beta = beta;
+        a.C = static_cast<const uint16_t *>(beta != 0.0f ? C : nullptr);
+        a.ldc = ldc;
+        a.D = static_cast<uint16_t *>(D);
+        a.ldd = ldd;
+        a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
+                   (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
+        a.wait_limit = g_wait_limit.load();
+        const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
+        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB, stream) !=
+            cudaSuccess)
+            return MXFP4_ERR_CUDA;
+        return MXFP4_OK;
+    }
     const bool swap = shape.swap != 0;
     CUtensorMap tmP, tmQ;
     const void *Pp = swap ? B : A;
@@ -275,6 +460,12 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
                 (sc.ld_b % 8) == 0;
     a.sf_async = sc.rowmajor && aligned(sc.a, 4) && aligned(sc.b, 4) && (sc.ld_a % 4) == 0 &&
                  (sc.ld_b % 4) == 0;
+    // The persistent kernel prefers one 2-D TMA per pair of stages for
+    // row-major scales (16-byte aligned rows), over per-word copies.
+    a.sf_tma = shape.persistent && sc.rowmajor && aligned(sc.a, 16) && aligned(sc.b, 16) &&
+               (sc.ld_a % 16) == 0 && (sc.ld_b % 16) == 0;
+    if (a.sf_tma)
+        a.sf_async = 0;
     a.rowsP = Prows;
     a.rowsQ = Qrows;
     a.M = M;
@@ -295,6 +486,41 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.stream_p = swap ? 1 : 0;
     a.wait_limit = g_wait_limit.load();
 
+    if (shape.persistent) {
+        // The plan assumed shape.ctas_per_sm resident CTAs per SM; if the
+        // occupancy calculator allows fewer here, shrink the grid so every
+        // CTA is resident (the stream-K handshake waits on other CTAs).
+        int64_t slots = static_cast<int64_t>(sms) * shape.ctas_per_sm;
+        const int occ = gemm_persistent_occupancy(shape);
+        if (occ <= 0)
+            return MXFP4_ERR_CUDA;
+        if (occ < shape.ctas_per_sm)
+            slots = static_cast<int64_t>(sms) * occ;
+        const SkPlan k = stream_k_plan(Prows, Qrows, K, shape.tile_n, slots);
+        if (k.partial_bytes && !ws)
+            return MXFP4_ERR_WORKSPACE;
+        Sched sch;
+        sch.tiles_p = k.tiles_p;
+        sch.tiles_q = k.tiles_q;
+        sch.kt = k.kt;
+        sch.ctas = k.ctas;
+        sch.dp_waves = k.dp_waves;
+        sch.sk_tile0 = k.sk_tile0;
+        sch.sk_units = k.sk_units;
+        sch.group = k.tiles_p < 8 ? k.tiles_p : 8;
+        sch.flags = ws ? reinterpret_cast<int *>(ws) : nullptr;
+        sch.partials = partials;
+        sch.pcols = k.pcols;
+        sch.epoch = next_epoch();
+        CUtensorMap tmSP = tmP, tmSQ = tmQ;   // unused unless a.sf_tma
+        if (a.sf_tma &&
+            (!encode_scales(&tmSP, a.sfP, Prows, K, a.ldsP, kTileM) ||
+             !encode_scales(&tmSQ, a.sfQ, Qrows, K, a.ldsQ, shape.tile_n)))
+            return MXFP4_ERR_CUDA;
+        if (launch_gemm_persistent(a, sch, tmP, tmQ, tmSP, tmSQ, shape, stream) != cudaSuccess)
+            return MXFP4_ERR_CUDA;
+        return MXFP4_OK;
+    }
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     if (launch_gemm(a, tmP, tmQ, shape, grid, stream) != cudaSuccess)
         return MXFP4_ERR_CUDA;
@@ -361,7 +587,8 @@ size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k)
         return 0;
     size_t ws = plan.workspace_bytes;
     if (plan.relayout_pass)
-        ws += align_up(sf_relaid_bytes(M, K)) + align_up(sf_relaid_bytes(N, K));
+        ws = (ws ? ws : kFlagBytes) + align_up(sf_relaid_bytes(M, K)) +
+             align_up(sf_relaid_bytes(N, K));
     return ws;
 }
 
@@ -404,7 +631,8 @@ static int gemm_entry(void *D, int64_t ldd, const void *C, int64_t ldc, const vo
     if (st != MXFP4_OK)
         return st;
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
-                    static_cast<float *>(workspace), sms, static_cast<cudaStream_t>(stream));
+                    plan.workspace_bytes ? static_cast<uint8_t *>(workspace) : nullptr, sms,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
@@ -445,7 +673,11 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
         return st;
     const size_t sfa_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(M, K)) : 0;
     const size_t sfb_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(N, K)) : 0;
-    const size_t need = plan.workspace_bytes + sfa_bytes + sfb_bytes;
+    // Layout: [flags + partials (plan.workspace_bytes)][relaid A][relaid B];
+    // the flag bytes are reserved even when only the relaid buffers are used.
+    const size_t head = plan.workspace_bytes ? plan.workspace_bytes
+                                             : (plan.relayout_pass ? kFlagBytes : 0);
+    const size_t need = head + sfa_bytes + sfb_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need))
         return MXFP4_ERR_WORKSPACE;
     st = check_device();
@@ -453,11 +685,10 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *partials = plan.workspace_bytes ? reinterpret_cast<float *>(ws) : nullptr;
     Scales sc{static_cast<const uint8_t *>(scaleA), static_cast<const uint8_t *>(scaleB), ld_sa,
               ld_sb, true};
     if (plan.relayout_pass) {
-        uint8_t *sfa = ws + plan.workspace_bytes;
+        uint8_t *sfa = ws + head;
         uint8_t *sfb = sfa + sfa_bytes;
         if (launch_scale_relayout(sfa, sc.a, M, K, ld_sa, s) != cudaSuccess ||
             launch_scale_relayout(sfb, sc.b, N, K, ld_sb, s) != cudaSuccess)
@@ -465,7 +696,7 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
         sc = Scales{sfa, sfb, 0, 0, false};
     }
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
-                    partials, sms, s);
+                    plan.workspace_bytes ? ws : nullptr, sms, s);
 }
 
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)

@@ -71,27 +71,13 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Epilogue of one 32-column chunk of one row (no swap): v[i] is the fp32
-// accumulator of D[m][n0 + i].
-__device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int z, int m, int n0,
-                                                const uint32_t (&r)[32])
+// D[m][n0 .. n0+31] = bf16(alpha * v + beta * C), vector stores when the
+// whole chunk is inside the row and the pointers allow it.
+__device__ __forceinline__ void store_d_row(const GemmArgs &a, int m, int n0, float (&v)[32])
 {
-    if (a.split_k > 1) {
-        float *dst = a.ws + (static_cast<int64_t>(z) * a.M + m) * a.N + n0;
-        if ((a.N & 3) == 0 && n0 + 32 <= a.N) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<uint4 *>(dst + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
-        } else {
-            for (int i = 0; i < 32 && n0 + i < a.N; ++i)
-                dst[i] = __uint_as_float(r[i]);
-        }
-        return;
-    }
-    float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-        v[i] = a.alpha * __uint_as_float(r[i]);
+        v[i] *= a.alpha;
     const bool full = n0 + 32 <= a.N;
     if (a.beta != 0.0f) {
         const uint16_t *c = a.C + static_cast<int64_t>(m) * a.ldc + n0;
@@ -126,8 +112,52 @@ __device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int z, int m,
     }
 }
 
-// Epilogue of one 32-column chunk with swap: r[i] is the accumulator of
-// D[m0 + i][n] (one n per lane, consecutive across the warp).
+// D[m0 + i][n] = bf16(alpha * v[i] + beta * C) for the valid i (swap: one n
+// per lane, consecutive across the warp).
+__device__ __forceinline__ void store_d_col(const GemmArgs &a, int m0, int n, const float (&v)[32])
+{
+    if (n >= a.N)
+        return;
+    const int mcount = min(32, a.M - m0);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (i < mcount) {
+            const int64_t m = m0 + i;
+            float x = a.alpha * v[i];
+            if (a.beta != 0.0f)
+                x = fmaf(a.beta, bf16_bits_to_float(a.C[m * a.ldc + n]), x);
+            __nv_bfloat16 b = __float2bfloat16_rn(x);
+            a.D[m * a.ldd + n] = *reinterpret_cast<uint16_t *>(&b);
+        }
+    }
+}
+
+// One-tile kernel epilogue of one 32-column chunk of one row (no swap): r[i]
+// is the fp32 accumulator of D[m][n0 + i]; with split-K it goes to the
+// partials instead.
+__device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int z, int m, int n0,
+                                                const uint32_t (&r)[32])
+{
+    if (a.split_k > 1) {
+        float *dst = a.ws + (static_cast<int64_t>(z) * a.M + m) * a.N + n0;
+        if ((a.N & 3) == 0 && n0 + 32 <= a.N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<uint4 *>(dst + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < a.N; ++i)
+                dst[i] = __uint_as_float(r[i]);
+        }
+        return;
+    }
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+    store_d_row(a, m, n0, v);
+}
+
+// Same with swap: r[i] is the accumulator of D[m0 + i][n].
 __device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int z, int m0, int n,
                                                 const uint32_t (&r)[32])
 {
@@ -142,17 +172,11 @@ __device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int z, int m0
                 dst[static_cast<int64_t>(i) * a.N] = __uint_as_float(r[i]);
         return;
     }
+    float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        if (i < mcount) {
-            const int64_t m = m0 + i;
-            float v = a.alpha * __uint_as_float(r[i]);
-            if (a.beta != 0.0f)
-                v = fmaf(a.beta, bf16_bits_to_float(a.C[m * a.ldc + n]), v);
-            __nv_bfloat16 b = __float2bfloat16_rn(v);
-            a.D[m * a.ldd + n] = *reinterpret_cast<uint16_t *>(&b);
-        }
-    }
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+    store_d_col(a, m0, n, v);
 }
 
 // Row-major scales -> one lane's share of a 128-row block for stage kt: rows
@@ -485,6 +509,13 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+}  // namespace mxfp4
+
+#include "gemm_persistent.cuh"
+#include "gemm_pair.cuh"
+
+namespace mxfp4 {
+
 // ----------------------------------------------------------- host side --
 
 template <int BN, int STAGES, bool SWAP>
@@ -545,6 +576,131 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
             return launch_cfg<64, 8, true>(a, tmP, tmQ, grid, stream);
     }
     return cudaErrorInvalidConfiguration;
+}
+
+template <int BN, int STAGES, bool SWAP, int NACC, int NSLOT>
+static cudaError_t launch_persistent_cfg(const GemmArgs &a, const Sched &sch,
+                                         const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                                         const CUtensorMap &tmSP, const CUtensorMap &tmSQ,
+                                         cudaStream_t stream)
+{
+    using PC = PCfg<BN, STAGES, NACC, NSLOT>;
+    auto kern = gemm_mxf4_persistent<BN, STAGES, SWAP, NACC, NSLOT>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = 1;
+    }
+    kern<<<sch.ctas, 192, PC::SMEM_BYTES, stream>>>(a, sch, tmP, tmQ, tmSP, tmSQ);
+    return cudaGetLastError();
+}
+
+template <int BN, int STAGES, bool SWAP, int NACC, int NSLOT>
+static int occupancy_cfg()
+{
+    // The occupancy calculator is slow on the host: ask once per device.
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < 64 && cached[dev] > 0)
+        return cached[dev];
+    using PC = PCfg<BN, STAGES, NACC, NSLOT>;
+    auto kern = gemm_mxf4_persistent<BN, STAGES, SWAP, NACC, NSLOT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 192, PC::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    // Tensor memory: each resident CTA holds TMEM_COLS of the SM's 512.
+    const int by_tmem = 512 / PC::TMEM_COLS;
+    const int occ = n < by_tmem ? n : by_tmem;
+    if (dev >= 0 && dev < 64)
+        cached[dev] = occ;
+    return occ;
+}
+
+// Compiled persistent configurations:
+// (tile_n, stages, swap, accumulator buffers, scale staging slots).
+#define MXFP4_PERSISTENT_CONFIGS(X) \
+    X(256, 4, false, 1, 3)          \
+    X(128, 6, false, 2, 3)          \
+    X(64, 8, false, 2, 4)           \
+    X(64, 8, true, 2, 4)
+
+size_t gemm_persistent_smem_bytes(const GemmShape &s)
+{
+#define X(BN, ST, SW, NA, NS)                                                    \
+    if (s.tile_n == BN && s.stages == ST && (s.swap != 0) == SW && s.nacc == NA) \
+        return PCfg<BN, ST, NA, NS>::SMEM_BYTES;
+    MXFP4_PERSISTENT_CONFIGS(X)
+#undef X
+    return 0;
+}
+
+int gemm_persistent_occupancy(const GemmShape &s)
+{
+#define X(BN, ST, SW, NA, NS)                                                    \
+    if (s.tile_n == BN && s.stages == ST && (s.swap != 0) == SW && s.nacc == NA) \
+        return occupancy_cfg<BN, ST, SW, NA, NS>();
+    MXFP4_PERSISTENT_CONFIGS(X)
+#undef X
+    return 0;
+}
+
+cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sch, const CUtensorMap &tmP,
+                                   const CUtensorMap &tmQ, const CUtensorMap &tmSP,
+                                   const CUtensorMap &tmSQ, const GemmShape &s, cudaStream_t stream)
+{
+#define X(BN, ST, SW, NA, NS)                                                    \
+    if (s.tile_n == BN && s.stages == ST && (s.swap != 0) == SW && s.nacc == NA) \
+        return launch_persistent_cfg<BN, ST, SW, NA, NS>(a, sch, tmP, tmQ, tmSP, tmSQ, stream);
+    MXFP4_PERSISTENT_CONFIGS(X)
+#undef X
+    return cudaErrorInvalidConfiguration;
+}
+
+constexpr int kPairStages = 6;
+
+size_t gemm_pair_smem_bytes() { return PairCfg<kPairStages>::SMEM_BYTES; }
+
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
+                             const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream)
+{
+    using PC = PairCfg<kPairStages>;
+    auto kern = gemm_mxf4_pair<kPairStages>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = 1;
+    }
+    PairSched ps;
+    ps.tiles_p = tiles_p;
+    ps.tiles_q = tiles_q;
+    ps.kt = a.kt_total;
+    ps.group = tiles_p < 8 ? tiles_p : 8;
+    kern<<<ctas, 192, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
+    return cudaGetLastError();
 }
 
 // Test hook: one wait on an mbarrier nobody arrives at.

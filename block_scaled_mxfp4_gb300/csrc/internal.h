@@ -16,8 +16,8 @@ constexpr int kSfRowBlock = 128;
 // Relaid scale buffer geometry (see mxfp4_scale_relayout): 128-row blocks
 // (the count rounded up to an even number so a 256-row tile never reads past
 // the end) times 2*ceil(K/256) atoms of 512 bytes.
-inline int64_t sf_groups(int K) { return 2 * ((static_cast<int64_t>(K) + kTileK - 1) / kTileK); }
-inline int64_t sf_row_blocks(int rows) { return 2 * ((static_cast<int64_t>(rows) + 255) / 256); }
+__host__ __device__ inline int64_t sf_groups(int K) { return 2 * ((static_cast<int64_t>(K) + kTileK - 1) / kTileK); }
+__host__ __device__ inline int64_t sf_row_blocks(int rows) { return 2 * ((static_cast<int64_t>(rows) + 255) / 256); }
 inline size_t sf_relaid_bytes(int rows, int K)
 {
     return static_cast<size_t>(sf_row_blocks(rows) * sf_groups(K) * kSfAtomBytes);
@@ -32,6 +32,7 @@ struct GemmArgs {
     int sf_rowmajor;        // 1: scales are row-major E8M0 [rows, ld] (atoms built in-kernel)
     int sf_vec8;            // row-major scales allow aligned 8-byte loads per stage
     int sf_async;           // row-major scales allow 4-byte cp.async (aligned rows)
+    int sf_tma;             // row-major scales allow 2-D TMA (16-byte aligned rows)
     int64_t ldsP, ldsQ;     // row-major: row strides in bytes
     int rowsP, rowsQ;       // rows of P and Q
     int M, N, K;
@@ -53,7 +54,36 @@ struct GemmShape {
     int tile_n;
     int stages;
     int swap;
+    int persistent;         // 1: stream-K persistent kernel (gemm_mxf4_persistent)
+    int nacc;               // persistent: TMEM accumulator buffers (1 or 2)
+    int ctas_per_sm;        // resident CTAs per SM the plan assumed
+    int pair;               // 1: CTA-pair kernel (256 x 256 tiles, cta_group::2)
+    int pair_ctas;          // pair kernel: grid size (2 x pairs)
 };
+
+// Work schedule of the persistent stream-K kernel.  Tile t (raster below)
+// covers rows [128p, 128p+128) of P and [tile_n q, ...) of Q.  CTA c first
+// takes whole tiles c, c+G, ... (dp_waves of them), then the K-stage units
+// [c*S/G, (c+1)*S/G) of the remaining tiles (S = sk_units), in order.
+struct Sched {
+    int tiles_p, tiles_q;   // output tiles along P and Q
+    int kt;                 // K stages per tile
+    int ctas;               // G
+    int dp_waves;           // whole tiles per CTA before the stream-K part
+    int sk_tile0;           // first stream-K tile (= dp_waves * G)
+    long long sk_units;     // (tiles - sk_tile0) * kt
+    int group;              // raster: groups of `group` tile rows along P
+    int *flags;             // [G] per-CTA partial-ready flags
+    float *partials;        // [G][pcols][128] fp32 partial tiles
+    int pcols;              // columns per partial slot: tile_n, or Q's rows if fewer
+    int epoch;              // this call's flag value (never 0)
+};
+
+// Every workspace layout starts with this many bytes reserved for the
+// stream-K flags (nothing else is ever written there), so flags left by one
+// call can only hold an earlier call's epoch.
+constexpr size_t kFlagBytes = 4096;
+constexpr int kMaxPersistentCtas = static_cast<int>(kFlagBytes / sizeof(int));
 
 // Dynamic shared memory one GEMM configuration needs (0 if unsupported).
 size_t gemm_smem_bytes(const GemmShape &s);
@@ -63,6 +93,22 @@ bool gemm_config_exists(const GemmShape &s);
 
 cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
                         const GemmShape &s, dim3 grid, cudaStream_t stream);
+
+cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sched, const CUtensorMap &tmP,
+                                   const CUtensorMap &tmQ, const CUtensorMap &tmSP,
+                                   const CUtensorMap &tmSQ, const GemmShape &s,
+                                   cudaStream_t stream);
+
+// CTA-pair kernel (relaid scales): grid = ctas (even), tiles of 256 x 256.
+size_t gemm_pair_smem_bytes();
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
+                             const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream);
+
+// Persistent configuration: dynamic smem (0 if not compiled) and resident
+// CTAs per SM the occupancy calculator allows (0 on error).
+size_t gemm_persistent_smem_bytes(const GemmShape &s);
+int gemm_persistent_occupancy(const GemmShape &s);
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
                                   cudaStream_t stream);

@@ -68,14 +68,25 @@ typedef struct mxfp4_plan {
     int relayout_pass;      /* 1: mxfp4_gemm relays the scales out in a separate
                                pass into its workspace (compute-bound shapes);
                                0: the GEMM builds the scale layout itself */
+    int persistent;         /* 1: persistent stream-K kernel (MXFP4_KERNEL override) */
+    int ctas;               /* persistent: CTAs (all resident at once) */
+    int dp_waves;           /* persistent: whole tiles per CTA before stream-K */
+    long long sk_units;     /* persistent: K stages shared out stream-K */
+    int pair;               /* 1: CTA-pair kernel (256 x 256 tiles over two SMs;
+                               MXFP4_KERNEL override) */
 } mxfp4_plan;
 
 /*
  * Choose tile, swap and split-K for a shape (the tile heuristic of the page's
  * section "Tile selection heuristic": fewest waves over the SMs, then SM
  * occupancy of the last wave, then tile area over perimeter; ties resolved by
- * a fixed candidate order).  split_k = 0 lets the heuristic choose; 1..16
- * forces that many splits (clamped to the number of K blocks).  num_sms = 0
+ * a fixed candidate order).  split_k = 0 lets the heuristic choose: no split
+ * when the tiles fill at least half a wave, else enough splits to fill the
+ * SMs with at least 8 K stages each; 1..16 forces that many splits (clamped
+ * to the number of K blocks).  The environment variable MXFP4_KERNEL, read at
+ * each call, overrides the kernel for split_k = 0 (tuning and tests only):
+ * "persistent" = persistent stream-K kernel, "pair" = CTA-pair kernel for
+ * M, N >= 256 without swap.  num_sms = 0
  * uses the current device's SM count (or 152 when no device is visible).
  * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
  */
@@ -173,7 +184,7 @@ size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
  * counterpart: it exists for users whose allocator is owned by someone else
  * or who may not synchronise the device through a cudaMalloc mid-run).  Same
  * arguments and results as mxfp4_gemm minus the workspace: the scratch (relaid
- * scales, split-K partials) lives in one array of MXFP4_NOALLOC_SCRATCH_BYTES
+ * scales, split-K / stream-K partials) lives in one array of MXFP4_NOALLOC_SCRATCH_BYTES
  * inside the library's device image, held by every GPU that loads the library
  * until exit.  Shapes whose mxfp4_gemm_workspace_size exceeds it are rejected
  * with MXFP4_ERR_WORKSPACE before anything is enqueued.  The first call on a
@@ -183,7 +194,7 @@ size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
  * the caller.  Each call rewrites all the scratch it reads, so leftovers from
  * the previous call never leak into a result.
  */
-#define MXFP4_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define MXFP4_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 int mxfp4_gemm_noalloc(void *D, int64_t ldd, const void *C, int64_t ldc,
                        const void *A, int64_t lda, const void *B, int64_t ldb,

@@ -57,18 +57,64 @@ def test_plan_invariants(L, name):
         assert p.tile_m == 128 and p.tile_k == 256
         assert p.split_k >= 1 and p.split_k <= 16
         assert p.k_tiles_per_split * (p.split_k - 1) < kt <= p.k_tiles_per_split * p.split_k
-        if split:
-            assert p.split_k <= split
         P, Q = (N, M) if p.swap_ab else (M, N)
+        tiles = -(-P // 128) * -(-Q // p.tile_n)
+        if split == 0:
+            # Automatic split: none when the tiles fill half a wave, else as
+            # many as fill the resident CTA slots with >= 8 K stages each.
+            slots = 152 * (2 if p.swap_ab else 1)
+            assert p.persistent == 0 and p.pair == 0
+            want = 1 if 2 * tiles >= slots else max(1, min(slots // tiles, kt // 8, 16, kt))
+            per = -(-kt // want)
+            assert p.split_k == -(-kt // per)
+            assert p.grid_z == p.split_k
+            continue
+        assert p.persistent == 0 and p.split_k <= split
         assert p.grid_x == -(-P // 128) and p.grid_y == -(-Q // p.tile_n)
         assert p.grid_z == p.split_k
-        want_ws = 0 if p.split_k == 1 else p.split_k * M * N * 4
+        want_ws = 0 if p.split_k == 1 else 4096 + p.split_k * M * N * 4
         assert p.workspace_bytes >= want_ws
     # Skinny M swaps; large uses the widest tile and no split.
     p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
     assert p.swap_ab == (1 if M <= 64 else 0)
     if name == "large":
-        assert (p.tile_n, p.split_k) == (256, 1)
+        assert (p.tile_n, p.split_k, p.persistent) == (256, 1, 0)
+    if name in ("decode", "skinny"):
+        assert p.split_k == {"decode": 4, "skinny": 5}[name]
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_plan_invariants_persistent_override(L, name, monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "persistent")
+    M, N, K = WORKLOADS[name]
+    p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
+    kt = -(-K // p.tile_k)
+    P, Q = (N, M) if p.swap_ab else (M, N)
+    tiles = -(-P // 128) * -(-Q // p.tile_n)
+    # Persistent stream-K: every tile either whole (dp waves) or in the
+    # shared K-stage pool; at most one CTA per resident slot.
+    assert p.persistent == 1 and p.split_k == 1 and p.pair == 0
+    assert (p.grid_x, p.grid_y, p.grid_z) == (p.ctas, 1, 1)
+    slots = 152 * (2 if p.swap_ab else 1)
+    assert 1 <= p.ctas <= slots
+    assert p.dp_waves * p.ctas + p.sk_units // kt == tiles
+    assert p.sk_units % kt == 0
+    if p.sk_units:
+        assert p.workspace_bytes >= 4096 + p.ctas * min(Q, p.tile_n) * 128 * 4
+    if name == "large":
+        assert (p.tile_n, p.dp_waves, p.ctas) == (256, 13, 152)
+    # An explicit split ignores the override.
+    assert mx.mxfp4_plan_gemm(M, N, K, 1, 152).persistent == 0
+
+
+def test_plan_pair_override(L, monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "pair")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert p.pair == 1 and (p.tile_m, p.tile_n) == (256, 256) and p.ctas == 152
+    assert p.relayout_pass == 1 and p.workspace_bytes == 0
+    # Shapes the pair kernel does not take stay on the automatic path.
+    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152).pair == 0
+    assert mx.mxfp4_plan_gemm(128, 8192, 8192, 0, 152).pair == 0
 
 
 def test_plan_heuristic_prefers_fewer_waves(L):
@@ -90,12 +136,15 @@ def test_sizes(L):
     assert mx.mxfp4_scale_relayout_size(5, 48) == 0
     assert mx.mxfp4_gemm_workspace_size(0, 1, 32, 0) == 0
     assert mx.mxfp4_gemm_workspace_size(1, 1, 32, 17) == 0
-    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 4 * 8192 * 4
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 4096 + 4 * 8192 * 4
+    # The decode shape splits K four ways: partials [4, 1, 8192] in fp32.
+    p = mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152)
+    assert p.split_k == 4 and p.workspace_bytes == 4096 + 4 * 8192 * 4
     # The large shape relays its scales out first: workspace = both relaid buffers.
     p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 0)
     assert p.relayout_pass == 1
     assert mx.mxfp4_gemm_workspace_size(8192, 8192, 8192, 1) == \
-        2 * mx.mxfp4_scale_relayout_size(8192, 8192)
+        4096 + 2 * mx.mxfp4_scale_relayout_size(8192, 8192)
     assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 0).relayout_pass == 0
     assert mx.mxfp4_gemm_workspace_size(128, 256, 512, 1) == 0
     assert mx.mxfp4_gemm_host_arena_size(8192, 8192, 8192, 1, False) > 0

@@ -325,3 +325,70 @@ def test_bounded_wait_times_out_cleanly():
     p = problem("tiny")
     D = run_gemm(Dev(p))
     assert not np.isnan(bf16_bits_to_f64(D)).any()
+
+
+# ------------------------------------------------------ CTA-pair kernel --
+
+@pytest.fixture
+def force_pair(monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "pair")
+    yield
+
+
+@pytest.mark.parametrize("M,N", [(256, 256), (512, 512)])
+def test_pair_kernel_single_scale_probes(force_pair, M, N):
+    """Scale placement through the two-SM MMA: each CTA's scale-A rows and the
+    full scale-B must reach the right accumulator rows / columns."""
+    assert mx.mxfp4_plan_gemm(M, N, 512, 0, 0).pair == 1
+    K = 512
+    bad = []
+    for which, rows in (("A", [0, 31, 127, 128, 200, M - 1]), ("B", [0, 64, 127, 128, 255, N - 1])):
+        for r in rows:
+            for kb in (0, 3, 8, 15):
+                p = _ones_problem(M, N, K)
+                (p.SA if which == "A" else p.SB)[r, kb] = 128
+                D = bf16_bits_to_f64(run_gemm(Dev(p)))
+                want = np.full((M, N), float(K))
+                if which == "A":
+                    want[r, :] += 32
+                else:
+                    want[:, r] += 32
+                if not np.array_equal(D, want):
+                    wrong = np.argwhere(D != want)
+                    bad.append((which, r, kb, len(wrong), wrong[:4].tolist(), D[tuple(wrong[0])]))
+    assert not bad, bad
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 520, 1024), (1000, 700, 288),
+                                   (512, 1024, 2048)])
+def test_pair_kernel_parity(force_pair, oracle_mod, M, N, K):
+    p = inputs.make_problem("pair", M, N, K, seed=M + N + K, values="codes", alpha=0.5,
+                            beta=1.0, c_sigma=1.0)
+    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).pair == 1
+    Dref, sabs = full_oracle(oracle_mod, p)
+    assert_within_bound(run_gemm(Dev(p)), Dref, sabs, p.alpha, f"pair {M}x{N}x{K}")
+
+
+# ---------------------------------------------- persistent stream-K kernel --
+
+@pytest.fixture
+def force_persistent(monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "persistent")
+    yield
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (512, 1024, 2048), (1, 4096, 2048),
+                                   (64, 3072, 8192), (63, 200, 288), (129, 520, 1024),
+                                   (2000, 2600, 288), (257, 300, 384)])
+def test_persistent_kernel_parity(force_persistent, oracle_mod, M, N, K):
+    """Whole tiles and stream-K shares of tiles (partials, epoch flags and the
+    fix-up) against the oracle, with and without swap."""
+    p = inputs.make_problem("sk", M, N, K, seed=3 * M + N + K, values="codes", alpha=0.5,
+                            beta=1.0, c_sigma=1.0)
+    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).persistent == 1
+    Dref, sabs = full_oracle(oracle_mod, p)
+    dev = Dev(p)
+    first = run_gemm(dev)
+    assert_within_bound(first, Dref, sabs, p.alpha, f"persistent {M}x{N}x{K}")
+    # A second call reuses the workspace (flags of the earlier epoch).
+    assert np.array_equal(run_gemm(dev), first)

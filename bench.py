@@ -329,7 +329,9 @@ def main():
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = None
-    roof["kernel"] = ("gemm_mxf4_kernel" + (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
+    kname = ("gemv_mxf4_kernel" if plan.gemv else "gemm_mxf4_pair" if plan.pair else
+             "gemm_mxf4_persistent" if plan.persistent else "gemm_mxf4_kernel")
+    roof["kernel"] = (kname + (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
                       + (" (scales relaid by the relayout kernel, timed outside this figure)"
                          if split_form else " (scale layout built in-kernel)"))
     roof["kernel_ms"] = gemm_avg

@@ -137,6 +137,27 @@ bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K)
     return r == CUDA_SUCCESS;
 }
 
+// Relaid scale atoms viewed as 3-D uint32 [row blocks][k-groups][128]; a box
+// of 2 x 2 atoms = both 128-row blocks of a 256-row tile for one 256-K stage,
+// in smem order (row block, k-group).
+bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const int64_t groups = sf_groups(K);
+    cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(groups),
+                          static_cast<cuuint64_t>(sf_row_blocks(rows))};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kSfAtomBytes),
+                             static_cast<cuuint64_t>(groups * kSfAtomBytes)};
+    cuuint32_t box[3] = {128u, 2u, 2u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct Candidate {
     int tile_n;
     int stages;
@@ -186,12 +207,15 @@ SkPlan stream_k_plan(int64_t P, int64_t Q, int K, int tile_n, int64_t slots)
 // fixed-order fp32 reduce.  split_k == 0 picks the split itself: 1 when the
 // tiles fill at least half a wave, else enough splits to fill the resident
 // CTA slots, each split keeping at least kMinSplitStages K stages.
-// MXFP4_KERNEL=persistent|pair (a tuning / test override, read per call)
-// routes split_k == 0 to the persistent stream-K kernel or, for shapes of at
-// least 256 x 256 without swap, the CTA-pair kernel instead.
+// Shapes whose 256 x 256 tiles fill every SM pair at least once run the
+// CTA-pair kernel instead (split_k == 0 only).  MXFP4_KERNEL=persistent|pair
+// (a tuning / test override, read per call) routes split_k == 0 to the
+// persistent stream-K kernel or, for shapes of at least 256 x 256 without
+// swap, the CTA-pair kernel; MXFP4_KERNEL=gemv runs M <= 2 (N >= 4 * SMs) on
+// the CUDA-core GEMV kernel.
 constexpr int kMinSplitStages = 8;
 
-enum class KernelChoice { Auto, Persistent, Pair };
+enum class KernelChoice { Auto, Persistent, Pair, Gemv };
 
 KernelChoice kernel_override()
 {
@@ -202,6 +226,8 @@ KernelChoice kernel_override()
         return KernelChoice::Persistent;
     if (std::strcmp(env, "pair") == 0)
         return KernelChoice::Pair;
+    if (std::strcmp(env, "gemv") == 0)
+        return KernelChoice::Gemv;
     return KernelChoice::Auto;
 }
 
@@ -217,8 +243,17 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     const int kt = (K + kTileK - 1) / kTileK;
     const KernelChoice choice = split_req == 0 ? kernel_override() : KernelChoice::Auto;
     const int64_t tiles256 = ((static_cast<int64_t>(M) + 255) / 256) * ((static_cast<int64_t>(N) + 255) / 256);
-    const bool use_pair = choice == KernelChoice::Pair && !swap && M >= 256 && N >= 256;
+    // The CTA-pair kernel takes shapes whose 256 x 256 tiles fill at least one
+    // wave of SM pairs (and any shape of at least 256 x 256 when forced).
+    const bool pair_fits = !swap && M >= 256 && N >= 256;
+    const bool use_pair = pair_fits && (choice == KernelChoice::Pair ||
+                                        (choice == KernelChoice::Auto && split_req == 0 &&
+                                         tiles256 >= (sms > 0 ? sms : kDefaultSms) / 2));
     const bool persistent = choice == KernelChoice::Persistent || use_pair;
+    // M <= 2 with enough 4-row groups of B to give every SM a warp: the GEMV
+    // kernel (override only until it beats the tensor-core split path).
+    const bool use_gemv = choice == KernelChoice::Gemv && split_req == 0 && M <= kGemvMaxM &&
+                          (static_cast<int64_t>(N) + 3) / 4 >= (sms > 0 ? sms : kDefaultSms);
 
     Candidate cands[3];
     int nc = 0;
@@ -318,6 +353,26 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         partials = k.partial_bytes;
     }
     out->pair = use_pair;
+    out->gemv = use_gemv ? 1 : 0;
+    if (use_gemv) {
+        int ctas = 0, threads = 0;
+        gemv_launch_shape(N, sms > 0 ? sms : kDefaultSms, &ctas, &threads);
+        out->swap_ab = 0;
+        out->tile_m = M;
+        out->tile_n = 4;
+        out->tile_k = 1024;
+        out->stages = 1;
+        out->split_k = 1;
+        out->k_tiles_per_split = (K + 1023) / 1024;
+        out->grid_x = ctas;
+        out->grid_y = 1;
+        out->grid_z = 1;
+        out->persistent = 0;
+        out->ctas = ctas;
+        out->dp_waves = 0;
+        out->sk_units = 0;
+        partials = 0;
+    }
     if (use_pair) {
         out->tile_m = 256;
         out->tile_n = 256;
@@ -336,7 +391,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     // small shapes build the atoms inside the GEMM instead (no extra launches).
     // (The persistent kernel stages row-major scales by TMA itself; the
     // CTA-pair kernel reads relaid atoms.)
-    out->relayout_pass = (use_pair || (!persistent && !swap && tiles >= sms)) ? 1 : 0;
+    out->relayout_pass = (use_pair || (!use_gemv && !persistent && !swap && tiles >= sms)) ? 1 : 0;
     if (shape) {
         shape->tile_n = c.tile_n;
         shape->stages = c.stages;
@@ -345,6 +400,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         shape->nacc = c.nacc;
         shape->ctas_per_sm = c.ctas_per_sm;
         shape->pair = use_pair;
+        shape->gemv = use_gemv ? 1 : 0;
         shape->pair_ctas = out->ctas;
     }
     return MXFP4_OK;
@@ -410,12 +466,35 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
              cudaStream_t stream)
 {
     float *partials = ws ? reinterpret_cast<float *>(ws + kFlagBytes) : nullptr;
+    if (shape.gemv) {
+        GemvArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.A = static_cast<const uint8_t *>(A);
+        g.B = static_cast<const uint8_t *>(B);
+        g.SA = sc.a;
+        g.SB = sc.b;
+        g.lda_bytes = lda / 2;
+        g.ldb_bytes = ldb / 2;
+        g.ld_sa = sc.ld_a;
+        g.ld_sb = sc.ld_b;
+        g.sf_relaid = sc.rowmajor ? 0 : 1;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.alpha = alpha;
+        g.beta = beta;
+        g.C = static_cast<const uint16_t *>(beta != 0.0f ? C : nullptr);
+        g.ldc = ldc;
+        g.D = static_cast<uint16_t *>(D);
+        g.ldd = ldd;
+        return launch_gemv(g, sms, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    }
     if (shape.pair) {
         if (sc.rowmajor)
             return MXFP4_ERR_INVALID_ARG;            // the pair kernel reads relaid atoms
         CUtensorMap tmA, tmB, tmSA, tmSB;
         if (!encode_operand(&tmA, A, M, K, lda, kTileM) || !encode_operand(&tmB, B, N, K, ldb, kTileM) ||
-            !encode_atoms(&tmSA, sc.a, M, K) || !encode_atoms(&tmSB, sc.b, N, K))
+            !encode_atoms(&tmSA, sc.a, M, K) || !encode_atoms_3d(&tmSB, sc.b, N, K))
             return MXFP4_ERR_CUDA;
         GemmArgs a;
         std::memset(&a, 0, sizeof(a));

@@ -6,24 +6,40 @@
 // [128r, 128r+128) of the tile's A panel and rows [128r, 128r+128) of its B
 // panel (half of N) in its own shared memory, and its own 128 rows x 256
 // columns of the fp32 accumulator in its own tensor memory.  Per 256-K stage
-// each CTA therefore stages 16 KB of A and 16 KB of B for 128 x 256 x 256
-// multiply-adds -- two thirds of the one-CTA 128 x 256 tile's 48 KB -- which
-// is what lets the ring keep the tensor pipe fed from L2.
+// each CTA therefore stages 16 KB of A and 16 KB of B (plus 3 KB of scale
+// atoms) for 128 x 256 x 256 multiply-adds, against 48 KB for a one-CTA
+// 128 x 256 tile: the ring holds six stages instead of four, which is what
+// keeps the tensor pipe fed across the L2 round trip.
 //
-//   warp 4 (each CTA)  TMA producer: its A half, its B half, its 128 rows of
-//                      scale-A atoms and all 256 rows of scale-B atoms; every
-//                      copy is counted on the LEADER's full barrier (the
-//                      cta_group::2 form of the TMA signals the pair), which
-//                      only the leader arrives on, expecting both CTAs' bytes.
-//   warp 5 (leader)    waits on its full barrier, copies both CTAs' scale atoms
-//                      into their own tensor memory (tcgen05.cp.cta_group::2),
-//                      issues four K=64 M=256 MMAs, commits the stage to BOTH
-//                      CTAs' empty barriers, and each tile to both CTAs'
+// Roles (448 threads = 14 warps per CTA):
+//   warps 4, 6, 7 (each CTA)  TMA producers: A half, B half, and the scale
+//                      atoms (this CTA's 128 rows of scale-A, all 256 rows of
+//                      scale-B in one 3-D box).  Every copy completes its bytes
+//                      on the LEADER's full barrier (the cta_group::2 form of
+//                      the TMA); only the leader's three producers arrive on
+//                      it, each expecting its copy's bytes for both CTAs.  A
+//                      thread waits out each copy instruction it issues
+//                      (hundreds of cycles), hence three issuing warps.
+//   warps 12, 13 (leader)  scale copiers: once a stage has landed, each issues
+//                      three tcgen05.cp.cta_group::2 (both CTAs' atoms into
+//                      their own tensor memory) and commits them to the
+//                      stage's sf_ready barrier.  Copies issued by a thread
+//                      other than the MMA issuer run alongside the MMAs.
+//   warp 5 (leader)    waits for a stage's operands and scales, issues four
+//                      K=64 M=256 MMAs and commits the stage to BOTH CTAs'
+//                      empty barriers, and each tile to both CTAs'
 //                      accumulator-full barriers.
-//   warps 0-3 (each)   drain their CTA's accumulator rows, release the
-//                      leader's accumulator (4 warps x 2 CTAs), store D.
+//   warps 0-3 / 8-11 (each CTA)  epilogue, columns 0-127 / 128-255: read the
+//                      accumulator (warp w owns TMEM lanes 32(w%4)..+31 =
+//                      tile rows), form alpha*acc + beta*C and round once to
+//                      bf16 in registers, release the accumulator to the
+//                      leader (8 warps x 2 CTAs), then store D -- so the next
+//                      tile's MMAs do not wait for the stores.
 // Persistent over tiles: pair i takes tiles i, i + pairs, ...  Scales are
-// relaid atoms (read through a 2-D uint32 view: 128 words = one atom).
+// relaid atoms (a 2-D uint32 view for scale-A, 3-D for scale-B: 128 words =
+// one atom).  A scale slot in tensor memory (one per stage) is rewritten only
+// after the stage's full barrier completed again, i.e. after the producers
+// saw the MMAs that read it commit.
 #pragma once
 
 namespace mxfp4 {
@@ -34,15 +50,18 @@ struct PairCfg {
     static constexpr int B_BYTES = kTileM * 128;          // this CTA's half of N
     static constexpr int SFA_BYTES = 2 * kSfAtomBytes;    // 128 rows, 2 k-groups
     static constexpr int SFB_BYTES = 4 * kSfAtomBytes;    // 256 rows, 2 k-groups
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;
     static constexpr int SF_COLS_A = 8;                   // 2 groups x 4 columns
     static constexpr int SF_COLS_B = 16;                  // 2 groups x 2 blocks x 4 columns
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
     static constexpr int TMEM_USED = 256 + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+    static constexpr int THREADS = 448;
+    static constexpr int EPI_WARPS = 8;                   // per CTA
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -64,8 +83,65 @@ __device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int 
     qt = within / gh;
 }
 
+// One epilogue thread's 128 columns of one accumulator row, rounded: out[j]
+// holds columns n0 + 2j and n0 + 2j + 1 as packed bf16.  Stores them to D
+// row m (16-byte stores when the row segment is whole and aligned).
+__device__ __forceinline__ void pair_store_row(const GemmArgs &a, int m, int n0,
+                                               const uint32_t (&out)[64])
+{
+    if (m >= a.M || n0 >= a.N)
+        return;
+    uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
+    if (a.vec_ok && n0 + 128 <= a.N) {
+#pragma unroll
+        for (int j = 0; j < 64; j += 4)
+            *reinterpret_cast<uint4 *>(d + 2 * j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            if (n0 + 2 * j < a.N)
+                d[2 * j] = static_cast<uint16_t>(out[j] & 0xFFFFu);
+            if (n0 + 2 * j + 1 < a.N)
+                d[2 * j + 1] = static_cast<uint16_t>(out[j] >> 16);
+        }
+    }
+}
+
+// alpha * acc (+ beta * C) for 32 columns of row m starting at n, rounded once.
+__device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n, const uint32_t (&r)[32],
+                                                 uint32_t *out16)
+{
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = a.alpha * __uint_as_float(r[i]);
+    if (a.beta != 0.0f && m < a.M) {
+        const uint16_t *c = a.C + static_cast<int64_t>(m) * a.ldc + n;
+        if (a.vec_ok && n + 32 <= a.N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(c + i);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[i + 2 * j] = fmaf(a.beta, bf16_bits_to_float(ww[j] & 0xFFFF), v[i + 2 * j]);
+                    v[i + 2 * j + 1] = fmaf(a.beta, bf16_bits_to_float(ww[j] >> 16), v[i + 2 * j + 1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (n + i < a.N)
+                    v[i] = fmaf(a.beta, bf16_bits_to_float(c[i]), v[i]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        out16[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+}
+
 template <int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
@@ -76,10 +152,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + PC::RING_BYTES);   // leader's are used
     uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = empty + STAGES;
+    uint64_t *sf_ready = empty + STAGES;                                    // leader's are used
+    uint64_t *acc_full = sf_ready + STAGES;
     uint64_t *acc_empty = acc_full + 1;                                      // leader's is used
-    uint64_t *drain = acc_empty + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *drain = acc_empty + 1;                                         // [3]: MMA, copiers
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -89,15 +166,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
     const int tiles = ps.tiles_p * ps.tiles_q;
+    const int my_tiles = pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);          // the leader's expect-tx arrival (both CTAs' bytes)
+            mbar_init(&full[s], 3);          // the leader's three producers (both CTAs' bytes)
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 2);      // the leader's two scale copiers
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 8);             // four epilogue warps in each CTA
-        mbar_init(drain, 1);
+        mbar_init(acc_empty, 2 * PC::EPI_WARPS);
+        for (int i = 0; i < 3; ++i)
+            mbar_init(&drain[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -116,21 +196,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int64_t groups = sf_groups(a.K);
+    const int total_stages = my_tiles * ps.kt;
 
-    if (warp == 4) {
-        // ------------------------------------------------------ producer --
+    if (warp == 4 || warp == 6 || warp == 7) {
+        // ------------------------------------------------------ producers --
         if (lane == 0) {
+            const int role = warp == 4 ? 0 : warp - 5;   // 0: A, 1: B, 2: scales
             const uint64_t pol = l2_policy_evict_last();
+            const uint32_t bytes = role == 0 ? PC::A_BYTES : role == 1 ? PC::B_BYTES : PC::SF_BYTES;
             int stage = 0;
             uint32_t phase = 0;
+            int issued = 0;
             bool stop = false;
             for (int t = pair; t < tiles && !stop; t += npairs) {
                 int pt, qt;
                 pair_tile_coords(ps, t, pt, qt);
                 const int arow = pt * 256 + static_cast<int>(rank) * kTileM;
                 const int brow = qt * 256 + static_cast<int>(rank) * kTileM;
-                const int64_t sfa_atom = static_cast<int64_t>(pt * 2 + rank) * groups;
-                const int64_t sfb_atom0 = static_cast<int64_t>(qt * 2) * groups;
+                const int sfa_atom = static_cast<int>(static_cast<int64_t>(pt * 2 + rank) * groups);
                 for (int kt = 0; kt < ps.kt; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_limit,
                                    &g_device_status)) {
@@ -139,26 +222,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     }
                     uint8_t *st = smem + stage * PC::STAGE_BYTES;
                     const uint32_t lbar = map_to_rank(smem_addr(&full[stage]), 0);
-                    // Only the leader arrives, expecting both CTAs' bytes: a
-                    // cluster-scope arrive from the peer costs ~0.5 us a stage.
-                    // The peer's copies just complete their bytes on the
-                    // leader's barrier (it cannot start the next phase of this
-                    // stage before the leader's MMAs have freed it).
+                    // Only the leader arrives (a cluster-scope arrive from the
+                    // peer costs ~0.5 us); the peer's copies just complete
+                    // their bytes on the leader's barrier, which cannot start
+                    // this stage's next phase before the MMAs freed the stage.
                     if (leader)
-                        mbar_arrive_expect_tx(&full[stage], 2 * PC::STAGE_BYTES);
-                    tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
-                    tma_load_2d_pair(st + PC::A_BYTES, &tmB, lbar, kt * 128, brow, pol);
-                    uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
-                    tma_load_2d_pair(sf, &tmSA, lbar, 0, static_cast<int>(sfa_atom + 2 * kt), pol);
-                    tma_load_2d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0,
-                                     static_cast<int>(sfb_atom0 + 2 * kt), pol);
-                    tma_load_2d_pair(sf + PC::SFA_BYTES + 2 * kSfAtomBytes, &tmSB, lbar, 0,
-                                     static_cast<int>(sfb_atom0 + groups + 2 * kt), pol);
+                        mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+                    if (role == 0) {
+                        tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
+                    } else if (role == 1) {
+                        tma_load_2d_pair(st + PC::A_BYTES, &tmB, lbar, kt * 128, brow, pol);
+                    } else {
+                        uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
+                        tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
+                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, 2 * qt, pol);
+                    }
+                    ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
+            }
+            if (*abort_flag && leader) {
+                // Let the copies already issued land before the CTA exits.
+                for (int i = max(0, issued - STAGES); i < issued; ++i)
+                    mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
+            }
+        }
+    } else if (warp == 12 || warp == 13) {
+        // ------------------------------------------ scale copiers (leader) --
+        if (leader && lane == 0) {
+            const int which = warp - 12;
+            const uint32_t t_sf = tmem + 256;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int i = 0; i < total_stages; ++i) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
+                    break;
+                tc_fence_after();
+                const uint32_t sfa_t = t_sf + stage * PC::SF_COLS;
+                const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
+                const uint32_t sfa_s = smem_addr(smem + stage * PC::STAGE_BYTES + PC::A_BYTES + PC::B_BYTES);
+                const uint32_t sfb_s = sfa_s + PC::SFA_BYTES;
+                // Scale-B atom (k-group g, row block r) -> columns g*8 + r*4.
+                if (which == 0) {
+                    tmem_cp_32x128b_x4_pair(sfa_t, sdesc_sf_block(sfa_s));
+                    tmem_cp_32x128b_x4_pair(sfa_t + 4, sdesc_sf_block(sfa_s + kSfAtomBytes));
+                    tmem_cp_32x128b_x4_pair(sfb_t, sdesc_sf_block(sfb_s));
+                } else {
+                    tmem_cp_32x128b_x4_pair(sfb_t + 4, sdesc_sf_block(sfb_s + 2 * kSfAtomBytes));
+                    tmem_cp_32x128b_x4_pair(sfb_t + 8, sdesc_sf_block(sfb_s + kSfAtomBytes));
+                    tmem_cp_32x128b_x4_pair(sfb_t + 12, sdesc_sf_block(sfb_s + 3 * kSfAtomBytes));
+                }
+                mma_commit_pair(&sf_ready[stage], 0x1);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (*abort_flag) {
+                mma_commit_pair(&drain[1 + which], 0x1);
+                mbar_wait_drain(&drain[1 + which], 0, a.wait_limit);
             }
         }
     } else if (warp == 5) {
@@ -170,40 +295,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             uint32_t phase = 0;
             uint32_t acc_phase = 0;
             bool stop = false;
-            // Scale atoms of stage s into that stage's tensor-memory slot.
-            auto sf_copy = [&](int s) {
-                uint8_t *st = smem + s * PC::STAGE_BYTES;
-                const uint32_t sfa_t = t_sf + s * PC::SF_COLS;
-                const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
-                const uint32_t sfa_s = smem_addr(st + PC::A_BYTES + PC::B_BYTES);
-                const uint32_t sfb_s = sfa_s + PC::SFA_BYTES;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    tmem_cp_32x128b_x4_pair(sfa_t + g * 4, sdesc_sf_block(sfa_s + g * kSfAtomBytes));
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-                        tmem_cp_32x128b_x4_pair(
-                            sfb_t + g * 8 + r * 4,
-                            sdesc_sf_block(sfb_s + r * 2 * kSfAtomBytes + g * kSfAtomBytes));
-                }
-            };
             for (int t = pair; t < tiles && !stop; t += npairs) {
                 if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, a.wait_limit,
                                &g_device_status))
                     break;
                 tc_fence_after();
-                // tcgen05.cp and tcgen05.mma execute in issue order on the
-                // tensor pipe, so issuing the next stage's scale copies ahead
-                // of this stage's MMAs gains nothing (measured slower); the
-                // plain order keeps one full-barrier wait per stage.
                 for (int kt = 0; kt < ps.kt; ++kt) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit,
+                                   &g_device_status) ||
+                        !mbar_wait(&sf_ready[stage], phase, abort_flag, a.wait_limit,
                                    &g_device_status)) {
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    sf_copy(stage);
                     uint8_t *st = smem + stage * PC::STAGE_BYTES;
                     const uint32_t sfa_t = t_sf + stage * PC::SF_COLS;
                     const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
@@ -226,14 +331,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 acc_phase ^= 1u;
             }
             if (*abort_flag) {
-                mma_commit_pair(drain, 0x1);
-                mbar_wait_drain(drain, 0, a.wait_limit);
+                mma_commit_pair(&drain[0], 0x1);
+                mbar_wait_drain(&drain[0], 0, a.wait_limit);
             }
         }
     } else {
         // ------------------------------------------------------ epilogue --
-        const int row = warp * 32 + lane;
+        // warps 0-3: columns 0-127, warps 8-11: columns 128-255.
+        const int quarter = warp & 3;
+        const int half = warp >> 3;
+        const int row = quarter * 32 + lane;
         const uint32_t lead_acc_empty = map_to_rank(smem_addr(acc_empty), 0);
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
         uint32_t acc_phase = 0;
         for (int t = pair; t < tiles; t += npairs) {
             bool ok = mbar_wait(acc_full, acc_phase, abort_flag, a.wait_limit, &g_device_status);
@@ -245,28 +354,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             int pt, qt;
             pair_tile_coords(ps, t, pt, qt);
             const int m = pt * 256 + static_cast<int>(rank) * kTileM + row;
-            const int n0 = qt * 256;
-            const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-            for (int c0 = 0; c0 < 256; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c0, r);
-                tmem_ld_wait();
-                if (c0 == 256 - 32) {
-                    // Accumulator rows of this warp read: release them to the leader.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(lead_acc_empty);
-                }
-                if (m < a.M && n0 + c0 < a.N) {
-                    float v[32];
+            const int n0 = qt * 256 + half * 128;
+            uint32_t out[64];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = __uint_as_float(r[i]);
-                    store_d_row(a, m, n0 + c0, v);
-                }
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_ld_wait();
+                pair_round_chunk(a, m, n0 + c * 32, r, out + c * 16);
             }
+            // This warp's accumulator cells are read (tcgen05.wait::ld has
+            // returned, so no TMEM read is outstanding): release them to the
+            // leader.  No memory fence is needed for that, and a cluster-scope
+            // release arrive costs ~1000 cycles, so the leader's warps arrive
+            // locally and the peer's with a relaxed remote arrive.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(acc_empty);
+                else
+                    mbar_arrive_cluster_relaxed(lead_acc_empty);
+            }
+            pair_store_row(a, m, n0, out);
         }
     }
 

@@ -7,16 +7,27 @@
 //   with scaling").
 //
 // One CTA computes one 128 x BN output tile over a range of K (a split):
-//   warp 4  TMA producer: per 256-K stage, one 128x128-byte tile of P, one
-//           BNx128-byte tile of Q (128-byte swizzle), and the stage's relaid
-//           scale atoms by 1-D bulk copy, into an S-stage shared-memory ring
-//           guarded by full/empty mbarriers;
-//   warp 5  allocates tensor memory; one thread copies the stage's scales into
-//           TMEM (tcgen05.cp) and issues four K=64 block-scaled MMAs into an
-//           fp32 TMEM accumulator, then commits the stage back to the producer;
-//   warps 0-3  epilogue: tcgen05.ld the accumulator (warp w owns TMEM lanes
-//           32w..32w+31 = tile rows), apply alpha/beta with C, round to bf16
-//           and store; with split-K they store fp32 partials instead.
+//   warps 4, 6, 7  TMA producers: per 256-K stage, one 128x128-byte tile of P
+//           (warp 4), one BNx128-byte tile of Q (warp 6; 128-byte swizzle) and
+//           the stage's relaid scale atoms by 1-D bulk copy (warp 7), into an
+//           S-stage shared-memory ring guarded by full/empty mbarriers.  Each
+//           issuing thread waits out its own copy instructions (a few hundred
+//           cycles apiece), so spreading them over three warps keeps the ring
+//           ahead of the tensor core.  With row-major scales warp 4 alone
+//           issues both tiles and builds the atoms;
+//   warps 0-3  scale writers during the main loop: each lane reads its line
+//           of the stage's atoms from shared memory and writes it with
+//           tcgen05.st into its own TMEM lane (warp w owns lanes 32w..32w+31,
+//           so the four warps lay down the four replicas), then the warp
+//           arrives on the stage's sf_full barrier.  This keeps tcgen05.cp,
+//           which occupies the tensor pipe for tens of cycles per copy, off
+//           the MMA's critical path;
+//   warp 5  allocates tensor memory; one thread waits for a stage's operands
+//           and scales and issues four K=64 block-scaled MMAs into an fp32
+//           TMEM accumulator, then commits the stage back to the producers;
+//   warps 0-3  then the epilogue: tcgen05.ld the accumulator (warp w owns TMEM
+//           lanes 32w..32w+31 = tile rows), apply alpha/beta with C, round to
+//           bf16 and store; with split-K they store fp32 partials instead.
 // With swap (skinny M), P = B and Q = A, so the tile holds D^T: TMEM lane = n,
 // column = m, and a warp's 32 lanes write 32 consecutive n of one row of D.
 //
@@ -24,8 +35,9 @@
 // scales of 4 consecutive 32-K blocks; lane i, column c <-> row 32c + i of a
 // 128-row block, replicated in the four lane groups).  A K=64 instruction uses
 // two consecutive bytes of those words, chosen by the scale-factor id (0 or 2).
-// Every stage has its own TMEM scale slot, so a slot is rewritten only after
-// the MMAs that read it have committed.
+// Every stage has its own TMEM scale slot.  A slot is rewritten only after the
+// stage's full barrier completed again, which needs the producers to have
+// seen the stage's previous MMAs commit, so no write overtakes a read.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -38,13 +50,15 @@ __device__ int g_device_status = 0;
 template <int BN, int STAGES>
 struct Cfg {
     static constexpr int BM = kTileM;
+    static constexpr int BN_COLS = BN;
+    static constexpr int STAGE_COUNT = STAGES;
     static constexpr int P_BYTES = BM * 128;
     static constexpr int Q_BYTES = BN * 128;
     static constexpr int NQ = BN >= 128 ? BN / 128 : 1;      // 128-row scale blocks of Q
     static constexpr int SFP_BYTES = 2 * kSfAtomBytes;       // 2 atoms per 256-K stage
     static constexpr int SFQ_BYTES = NQ * 2 * kSfAtomBytes;
     static constexpr int STAGE_BYTES = P_BYTES + Q_BYTES + SFP_BYTES + SFQ_BYTES;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static constexpr int SF_COLS_P = 8;                      // 2 groups x 4 columns
     static constexpr int SF_COLS_Q = 8 * NQ;
@@ -244,8 +258,68 @@ __device__ __forceinline__ void store_sf_lines(uint8_t *atoms, const uint32_t (&
             make_uint4(w[0][g], w[1][g], w[2][g], w[3][g]);
 }
 
+// Scale writers (warps 0-3): for each stage of the ring, once its copies have
+// landed, lane i of warp w reads line i of the stage's atoms (16 bytes = rows
+// i, i+32, i+64, i+96 of a 128-row block, four K blocks each) and writes it to
+// TMEM lane 32w + i of the stage's scale slot: P's two atoms to columns
+// [0, 8), Q's atoms (K group g, row block r) to columns 8 + (g*NQ + r)*4.
+// t_lane = TMEM base address with this warp's lane quarter in its lane field.
+template <class Cf>
+__device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full, uint64_t *sf_full,
+                                                   uint32_t t_lane, int nkt, int lane,
+                                                   volatile int *abort_flag, long long limit)
+{
+    constexpr int STAGES = Cf::STAGE_COUNT;
+    const uint32_t t_sf = t_lane + Cf::BN_COLS;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < nkt; ++i) {
+        bool ok = mbar_wait(&full[stage], phase, abort_flag, limit, &g_device_status);
+        if (!__all_sync(0xffffffffu, ok))
+            return;
+        const uint8_t *sf_s = smem + stage * Cf::STAGE_BYTES + Cf::P_BYTES + Cf::Q_BYTES;
+        uint32_t wp[8];
+        uint32_t wq[8 * Cf::NQ];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sf_s + g * kSfAtomBytes + 16 * lane);
+            wp[4 * g] = v.x;
+            wp[4 * g + 1] = v.y;
+            wp[4 * g + 2] = v.z;
+            wp[4 * g + 3] = v.w;
+#pragma unroll
+            for (int r = 0; r < Cf::NQ; ++r) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(
+                    sf_s + Cf::SFP_BYTES + r * 2 * kSfAtomBytes + g * kSfAtomBytes + 16 * lane);
+                const int o = (g * Cf::NQ + r) * 4;
+                wq[o] = u.x;
+                wq[o + 1] = u.y;
+                wq[o + 2] = u.z;
+                wq[o + 3] = u.w;
+            }
+        }
+        const uint32_t slot = t_sf + stage * Cf::SF_COLS;
+        tmem_st_32x32b_x8(slot, wp);
+        if constexpr (Cf::NQ == 2)
+            tmem_st_32x32b_x16(slot + Cf::SF_COLS_P, wq);
+        else
+            tmem_st_32x32b_x8(slot + Cf::SF_COLS_P, wq);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sf_full[stage]);
+        if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+constexpr int kGemmThreads = 256;
+
 template <int BN, int STAGES, bool SWAP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_mxf4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmP,
                      const __grid_constant__ CUtensorMap tmQ)
 {
@@ -256,7 +330,8 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cf::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = empty + STAGES;
+    uint64_t *sf_full = empty + STAGES;
+    uint64_t *acc_full = sf_full + STAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -270,8 +345,9 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], !a.sf_rowmajor ? 1 : a.sf_async ? 33 : 2);
+            mbar_init(&full[s], !a.sf_rowmajor ? 3 : a.sf_async ? 33 : 2);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], 4);
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
@@ -290,9 +366,9 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 4 || warp >= 6) {
         // ------------------------------------------------------ producer --
-        if (a.sf_rowmajor && a.sf_async && nkt > 0) {
+        if (a.sf_rowmajor && a.sf_async && nkt > 0 && warp == 4) {
             // Whole warp: lane 0 issues the operand TMAs; every lane copies its
             // lines of the stage's scale atoms with 4-byte cp.async straight
             // from the row-major scales, and the stage's full barrier counts
@@ -332,7 +408,7 @@ __global__ void __launch_bounds__(192, 1)
                 for (int i = max(0, issued - STAGES); i < issued; ++i)
                     mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
             }
-        } else if (a.sf_rowmajor && nkt > 0) {
+        } else if (a.sf_rowmajor && nkt > 0 && warp == 4) {
             // Whole warp: lane 0 issues the operand TMAs; every lane builds its
             // lines of the stage's scale atoms from row-major scales it loaded
             // one stage ahead (so the global loads overlap the ring wait).
@@ -385,9 +461,11 @@ __global__ void __launch_bounds__(192, 1)
                 for (int i = max(0, issued - STAGES); i < issued; ++i)
                     mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
             }
-        } else if (lane == 0 && nkt > 0) {
-            // Prepacked scales: one thread issues the operand TMAs and 1-D bulk
-            // copies of the stage's relaid scale atoms.
+        } else if (!a.sf_rowmajor && lane == 0 && nkt > 0) {
+            // Prepacked scales: three threads (warps 4, 6, 7) issue the P tile,
+            // the Q tile and the 1-D bulk copies of the stage's relaid scale
+            // atoms; each arrives on the stage's full barrier with its bytes.
+            const int role = warp == 4 ? 0 : warp - 5;
             const uint64_t pol_p = a.stream_p ? l2_policy_evict_first() : l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_last();
             const uint8_t *sfp = a.sfP + static_cast<int64_t>(p0 / kSfRowBlock) * a.sf_rb_stride;
@@ -401,17 +479,24 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;
                 const int kt = kt0 + i;
-                mbar_arrive_expect_tx(&full[stage], Cf::STAGE_BYTES);
-                tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
-                tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
-                const int64_t sf_off = static_cast<int64_t>(kt) * 2 * kSfAtomBytes;
-                bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES, sfp + sf_off, Cf::SFP_BYTES, &full[stage],
-                          pol_p);
+                if (role == 0) {
+                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES);
+                    tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
+                } else if (role == 1) {
+                    mbar_arrive_expect_tx(&full[stage], Cf::Q_BYTES);
+                    tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], Cf::SFP_BYTES + Cf::SFQ_BYTES);
+                    const int64_t sf_off = static_cast<int64_t>(kt) * 2 * kSfAtomBytes;
+                    bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES, sfp + sf_off, Cf::SFP_BYTES,
+                              &full[stage], pol_p);
 #pragma unroll
-                for (int r = 0; r < Cf::NQ; ++r)
-                    bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES + Cf::SFP_BYTES + r * 2 * kSfAtomBytes,
-                              sfq + r * a.sf_rb_stride + sf_off, 2 * kSfAtomBytes, &full[stage],
-                              pol_q);
+                    for (int r = 0; r < Cf::NQ; ++r)
+                        bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES + Cf::SFP_BYTES +
+                                      r * 2 * kSfAtomBytes,
+                                  sfq + r * a.sf_rb_stride + sf_off, 2 * kSfAtomBytes,
+                                  &full[stage], pol_q);
+                }
                 ++issued;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -437,25 +522,13 @@ __global__ void __launch_bounds__(192, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int i = 0; i < nkt; ++i) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
+                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status) ||
+                    !mbar_wait(&sf_full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
                     break;
-                if (a.sf_rowmajor)
-                    fence_proxy_async_smem();   // scale atoms were written by threads
                 tc_fence_after();
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;
                 const uint32_t sfp_t = t_sf + stage * Cf::SF_COLS;
                 const uint32_t sfq_t = sfp_t + Cf::SF_COLS_P;
-                const uint32_t sfp_s = smem_addr(st + Cf::P_BYTES + Cf::Q_BYTES);
-                const uint32_t sfq_s = sfp_s + Cf::SFP_BYTES;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    tmem_cp_32x128b_x4(sfp_t + g * 4, sdesc_sf_block(sfp_s + g * kSfAtomBytes));
-#pragma unroll
-                    for (int r = 0; r < Cf::NQ; ++r)
-                        tmem_cp_32x128b_x4(sfq_t + g * 4 * Cf::NQ + r * 4,
-                                           sdesc_sf_block(sfq_s + r * 2 * kSfAtomBytes +
-                                                          g * kSfAtomBytes));
-                }
                 const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(st));
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + Cf::P_BYTES));
 #pragma unroll
@@ -476,6 +549,10 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_wait_drain(acc_full, 0, a.wait_limit);   // MMAs in flight land first
         }
     } else {
+        // ------------------------------------------------- scale writers --
+        if (nkt > 0)
+            write_stage_scales<Cf>(smem, full, sf_full, tmem + (static_cast<uint32_t>(warp * 32) << 16),
+                                   nkt, lane, abort_flag, a.wait_limit);
         // ------------------------------------------------------ epilogue --
         bool ok = nkt > 0 && mbar_wait(acc_full, 0, abort_flag, a.wait_limit, &g_device_status);
         ok = __all_sync(0xffffffffu, ok);
@@ -536,7 +613,7 @@ static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const C
             return e;
         configured[dev] = 1;
     }
-    kern<<<grid, 192, Cf::SMEM_BYTES, stream>>>(a, tmP, tmQ);
+    kern<<<grid, kGemmThreads, Cf::SMEM_BYTES, stream>>>(a, tmP, tmQ);
     return cudaGetLastError();
 }
 
@@ -699,7 +776,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
     ps.tiles_q = tiles_q;
     ps.kt = a.kt_total;
     ps.group = tiles_p < 8 ? tiles_p : 8;
-    kern<<<ctas, 192, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
+    kern<<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
     return cudaGetLastError();
 }
 

@@ -59,6 +59,7 @@ struct GemmShape {
     int ctas_per_sm;        // resident CTAs per SM the plan assumed
     int pair;               // 1: CTA-pair kernel (256 x 256 tiles, cta_group::2)
     int pair_ctas;          // pair kernel: grid size (2 x pairs)
+    int gemv;               // 1: GEMV kernel for M <= 2 (gemv.cu)
 };
 
 // Work schedule of the persistent stream-K kernel.  Tile t (raster below)
@@ -109,6 +110,24 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
 // CTAs per SM the occupancy calculator allows (0 on error).
 size_t gemm_persistent_smem_bytes(const GemmShape &s);
 int gemm_persistent_occupancy(const GemmShape &s);
+
+// GEMV form for M <= 2 (gemv.cu).  Scales row-major ([rows, ld] bytes) or,
+// with sf_relaid, the relaid atoms of mxfp4_scale_relayout.
+struct GemvArgs {
+    const uint8_t *A, *B, *SA, *SB;
+    int64_t lda_bytes, ldb_bytes;   // row strides of the packed operands (bytes)
+    int64_t ld_sa, ld_sb;           // row-major scales: row strides (bytes)
+    int sf_relaid;
+    int M, N, K;
+    float alpha, beta;
+    const uint16_t *C;
+    int64_t ldc;
+    uint16_t *D;
+    int64_t ldd;
+};
+constexpr int kGemvMaxM = 2;
+void gemv_launch_shape(int N, int sms, int *ctas, int *threads);
+cudaError_t launch_gemv(const GemvArgs &g, int sms, cudaStream_t stream);
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
                                   cudaStream_t stream);

@@ -74,19 +74,23 @@ typedef struct mxfp4_plan {
     long long sk_units;     /* persistent: K stages shared out stream-K */
     int pair;               /* 1: CTA-pair kernel (256 x 256 tiles over two SMs;
                                MXFP4_KERNEL override) */
+    int gemv;               /* 1: CUDA-core GEMV kernel for M <= 2 (tile_m = M,
+                               tile_n = 4 rows of B per warp, tile_k = 1024) */
 } mxfp4_plan;
 
 /*
  * Choose tile, swap and split-K for a shape (the tile heuristic of the page's
  * section "Tile selection heuristic": fewest waves over the SMs, then SM
  * occupancy of the last wave, then tile area over perimeter; ties resolved by
- * a fixed candidate order).  split_k = 0 lets the heuristic choose: no split
- * when the tiles fill at least half a wave, else enough splits to fill the
- * SMs with at least 8 K stages each; 1..16 forces that many splits (clamped
- * to the number of K blocks).  The environment variable MXFP4_KERNEL, read at
+ * a fixed candidate order).  split_k = 0 lets the heuristic choose: the
+ * CTA-pair kernel (256 x 256 tiles over two SMs) when those tiles fill every
+ * SM pair at least once; else no split when the tiles fill at least half a
+ * wave, or enough splits to fill the SMs with at least 8 K stages each.
+ * 1..16 forces that many splits (clamped to the number of K blocks).  The environment variable MXFP4_KERNEL, read at
  * each call, overrides the kernel for split_k = 0 (tuning and tests only):
  * "persistent" = persistent stream-K kernel, "pair" = CTA-pair kernel for
- * M, N >= 256 without swap.  num_sms = 0
+ * M, N >= 256 without swap, "gemv" = CUDA-core GEMV kernel for M <= 2 and
+ * N >= 4 * SMs.  num_sms = 0
  * uses the current device's SM count (or 152 when no device is visible).
  * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
  */

@@ -54,7 +54,7 @@ def test_plan_invariants(L, name):
     for split in range(0, 17):
         p = mx.mxfp4_plan_gemm(M, N, K, split, 152)
         kt = -(-K // p.tile_k)
-        assert p.tile_m == 128 and p.tile_k == 256
+        assert p.tile_m == (256 if p.pair else 128) and p.tile_k == 256
         assert p.split_k >= 1 and p.split_k <= 16
         assert p.k_tiles_per_split * (p.split_k - 1) < kt <= p.k_tiles_per_split * p.split_k
         P, Q = (N, M) if p.swap_ab else (M, N)
@@ -63,7 +63,13 @@ def test_plan_invariants(L, name):
             # Automatic split: none when the tiles fill half a wave, else as
             # many as fill the resident CTA slots with >= 8 K stages each.
             slots = 152 * (2 if p.swap_ab else 1)
-            assert p.persistent == 0 and p.pair == 0
+            if p.pair:
+                # 256 x 256 tiles filling all 76 SM pairs at least once.
+                assert not p.swap_ab and M >= 256 and N >= 256
+                assert -(-M // 256) * -(-N // 256) >= 76
+                assert (p.tile_m, p.tile_n, p.split_k, p.ctas) == (256, 256, 1, 152)
+                continue
+            assert p.persistent == 0
             want = 1 if 2 * tiles >= slots else max(1, min(slots // tiles, kt // 8, 16, kt))
             per = -(-kt // want)
             assert p.split_k == -(-kt // per)
@@ -74,11 +80,14 @@ def test_plan_invariants(L, name):
         assert p.grid_z == p.split_k
         want_ws = 0 if p.split_k == 1 else 4096 + p.split_k * M * N * 4
         assert p.workspace_bytes >= want_ws
-    # Skinny M swaps; large uses the widest tile and no split.
+    # Skinny M swaps (the GEMV form has no swap); large uses the pair kernel.
     p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
     assert p.swap_ab == (1 if M <= 64 else 0)
     if name == "large":
-        assert (p.tile_n, p.split_k, p.persistent) == (256, 1, 0)
+        assert (p.pair, p.tile_m, p.tile_n, p.split_k) == (1, 256, 256, 1)
+    else:
+        assert p.pair == 0
+    assert p.gemv == 0
     if name in ("decode", "skinny"):
         assert p.split_k == {"decode": 4, "skinny": 5}[name]
 
@@ -105,6 +114,7 @@ def test_plan_invariants_persistent_override(L, name, monkeypatch):
         assert (p.tile_n, p.dp_waves, p.ctas) == (256, 13, 152)
     # An explicit split ignores the override.
     assert mx.mxfp4_plan_gemm(M, N, K, 1, 152).persistent == 0
+    assert mx.mxfp4_plan_gemm(M, N, K, 1, 152).pair == 0
 
 
 def test_plan_pair_override(L, monkeypatch):
@@ -119,7 +129,7 @@ def test_plan_pair_override(L, monkeypatch):
 
 def test_plan_heuristic_prefers_fewer_waves(L):
     # 8192^2 output: 128x256 tiles need 14 waves on 152 SMs, 128x128 need 27.
-    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).tile_n == 256
+    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 152).tile_n == 256
     # 512x1024: both fit in one wave; 128x128 fills more SMs.
     assert mx.mxfp4_plan_gemm(512, 1024, 2048, 0, 152).tile_n == 128
     # Deterministic.
@@ -211,3 +221,17 @@ def test_no_device_reports_cuda_error_not_crash(L):
             pytest.skip("a GPU is visible")
     st = ctypes.c_int(123)
     assert L.mxfp4_device_status(ctypes.byref(st), 0) in (-5, -7)
+
+
+def test_plan_gemv_override(L, monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "gemv")
+    for M, N, K in ((1, 8192, 8192), (2, 4096, 1056), (1, 608, 32)):
+        p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
+        # CUDA-core GEMV: 4 rows of B per warp, one launch over the whole K.
+        assert p.gemv == 1 and (p.tile_m, p.tile_n, p.tile_k, p.split_k) == (M, 4, 1024, 1)
+        assert p.workspace_bytes == 0 and p.relayout_pass == 0 and p.pair == 0
+        assert p.k_tiles_per_split == -(-K // 1024) and p.grid_x == p.ctas >= 1
+    # Shapes it does not take stay on the tensor-core path.
+    assert mx.mxfp4_plan_gemm(3, 8192, 8192, 0, 152).gemv == 0
+    assert mx.mxfp4_plan_gemm(1, 600, 8192, 0, 152).gemv == 0
+    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 2, 152).gemv == 0

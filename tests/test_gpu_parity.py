@@ -392,3 +392,61 @@ def test_persistent_kernel_parity(force_persistent, oracle_mod, M, N, K):
     assert_within_bound(first, Dref, sabs, p.alpha, f"persistent {M}x{N}x{K}")
     # A second call reuses the workspace (flags of the earlier epoch).
     assert np.array_equal(run_gemm(dev), first)
+
+
+# ------------------------------------------------ GEMV kernel (M <= 2) --
+
+GEMV_SHAPES = [(1, 8192, 8192), (2, 8190, 1056), (1, 610, 96), (2, 4096, 4128), (1, 4099, 32)]
+
+
+@pytest.fixture
+def force_gemv(monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "gemv")
+    yield
+
+
+@pytest.mark.parametrize("M,N,K", GEMV_SHAPES)
+def test_gemv_parity(force_gemv, oracle_mod, M, N, K):
+    """The CUDA-core GEMV form (automatic split, M <= 2): ragged N (not a
+    multiple of the 4 rows a warp takes), K tails that are not a multiple of
+    the 1024-element chunk, alpha/beta with C; run-to-run identical; the
+    prepacked entry point (relaid scales) gives the same bits."""
+    p = inputs.make_problem("gemv", M, N, K, seed=M * 7 + N + K, values="codes", alpha=0.5,
+                            beta=1.0, c_sigma=1.0)
+    plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
+    assert plan.gemv == 1 and plan.workspace_bytes == 0
+    Dref, sabs = full_oracle(oracle_mod, p)
+    dev = Dev(p)
+    got = run_gemm(dev)
+    assert_within_bound(got, Dref, sabs, p.alpha, f"gemv {M}x{N}x{K}")
+    assert np.array_equal(run_gemm(dev), got)
+    sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device="cuda")
+    sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_scale_relayout(sfa, dev.SA, M, K, K // 32)
+    mx.mxfp4_scale_relayout(sfb, dev.SB, N, K, K // 32)
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.mxfp4_gemm_prepacked(D, N, dev.C, N, dev.A, K, dev.B, K, sfa, sfb, p.alpha, p.beta,
+                            M, N, K, 0, None, 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), got)
+
+
+def test_gemv_strided_operands(force_gemv, oracle_mod):
+    """Row strides larger than the data (A, B, scales, C, D) through the GEMV."""
+    M, N, K = 2, 1200, 640
+    p = inputs.make_problem("gemv-ld", M, N, K, seed=77, values="normal", alpha=1.0, beta=-0.5,
+                            c_sigma=1.0)
+    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).gemv == 1
+    Dref, sabs = full_oracle(oracle_mod, p)
+    pad = lambda a, extra: np.ascontiguousarray(np.pad(a, ((0, 0), (0, extra))))
+    d = lambda a: torch.from_numpy(a).cuda()
+    A, B = d(pad(p.A, 16)), d(pad(p.B, 48))                 # +32 / +96 K elements
+    SA, SB = d(pad(p.SA, 5)), d(pad(p.SB, 3))
+    C = d(pad(p.C.view(np.int16), 8)).view(torch.bfloat16)
+    D = torch.full((M, N + 24), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.mxfp4_gemm(D, N + 24, C, N + 8, A, (K // 2 + 16) * 2, B, (K // 2 + 48) * 2, SA,
+                  K // 32 + 5, SB, K // 32 + 3, p.alpha, p.beta, M, N, K, 0, None, 0)
+    torch.cuda.synchronize()
+    got = d_to_bits(D[:, :N].contiguous())
+    assert_within_bound(got, Dref, sabs, p.alpha, "gemv strided")
+    assert torch.isnan(D[:, N:].float()).all()                # padding untouched

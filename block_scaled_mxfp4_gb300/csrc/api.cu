@@ -510,6 +510,7 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.ldd = ldd;
         a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
                    (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
+        a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
         a.wait_limit = g_wait_limit.load();
         const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
         if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB, stream) !=
@@ -562,6 +563,7 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.ws = partials;
     a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
                (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
+    a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
     a.stream_p = swap ? 1 : 0;
     a.wait_limit = g_wait_limit.load();
 

@@ -85,14 +85,27 @@ __device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int 
 
 // One epilogue thread's 128 columns of one accumulator row, rounded: out[j]
 // holds columns n0 + 2j and n0 + 2j + 1 as packed bf16.  Stores them to D
-// row m (16-byte stores when the row segment is whole and aligned).
+// row m: 32-byte stores when the row segment is whole and aligned, with a
+// short pause after every 64 bytes.  The stores overlap the next tile's main
+// loop, and global stores share the memory-instruction queue with the
+// mbarrier polls of the producer, copier and MMA threads: a burst of 64 KB of
+// stores per CTA delays those polls by thousands of cycles, so the epilogue
+// uses the widest stores and spreads them out.
 __device__ __forceinline__ void pair_store_row(const GemmArgs &a, int m, int n0,
                                                const uint32_t (&out)[64])
 {
     if (m >= a.M || n0 >= a.N)
         return;
     uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
-    if (a.vec_ok && n0 + 128 <= a.N) {
+    if (a.vec32_ok && n0 + 128 <= a.N) {
+#pragma unroll
+        for (int j = 0; j < 64; j += 8) {
+            st_global_v8(d + 2 * j, out[j], out[j + 1], out[j + 2], out[j + 3], out[j + 4],
+                         out[j + 5], out[j + 6], out[j + 7]);
+            if ((j & 15) == 8)
+                __nanosleep(400);
+        }
+    } else if (a.vec_ok && n0 + 128 <= a.N) {
 #pragma unroll
         for (int j = 0; j < 64; j += 4)
             *reinterpret_cast<uint4 *>(d + 2 * j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);

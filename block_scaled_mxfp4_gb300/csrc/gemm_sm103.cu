@@ -112,7 +112,15 @@ __device__ __forceinline__ void store_d_row(const GemmArgs &a, int m, int n0, fl
         }
     }
     uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
-    if (a.vec_ok && full) {
+    if (a.vec32_ok && full) {
+        // 32-byte stores: half the store instructions of 16-byte ones.
+#pragma unroll
+        for (int i = 0; i < 32; i += 16)
+            st_global_v8(d + i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
+                         pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]),
+                         pack_bf16x2(v[i + 8], v[i + 9]), pack_bf16x2(v[i + 10], v[i + 11]),
+                         pack_bf16x2(v[i + 12], v[i + 13]), pack_bf16x2(v[i + 14], v[i + 15]));
+    } else if (a.vec_ok && full) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8)
             *reinterpret_cast<uint4 *>(d + i) =

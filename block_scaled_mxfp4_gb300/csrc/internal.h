@@ -46,6 +46,7 @@ struct GemmArgs {
     int64_t ldd;
     float *ws;              // fp32 partials [split_k][M][N] (split_k > 1)
     int vec_ok;             // D (and C) allow aligned 16-byte row accesses
+    int vec32_ok;           // D allows aligned 32-byte row stores
     int stream_p;           // P is read once: hint L2 evict-first
     long long wait_limit;   // SM cycles before a wait gives up
 };

@@ -450,3 +450,45 @@ def test_gemv_strided_operands(force_gemv, oracle_mod):
     got = d_to_bits(D[:, :N].contiguous())
     assert_within_bound(got, Dref, sabs, p.alpha, "gemv strided")
     assert torch.isnan(D[:, N:].float()).all()                # padding untouched
+
+
+# ------------------------------------------------------ split-K reduce --
+
+def test_splitk_reduce_kernel_for_large_grids(oracle_mod):
+    """A wide grid (over 1000 output tiles) split two ways: the fixed-order
+    fp32 reduce completes every tile (same bound, sampled)."""
+    M, N, K = 4224, 8192, 512
+    p = inputs.make_problem("wide", M, N, K, seed=9, values="normal", alpha=1.0, beta=0.0,
+                            c_sigma=None)
+    plan = mx.mxfp4_plan_gemm(M, N, K, 2, 0)
+    assert plan.split_k == 2 and plan.grid_x * plan.grid_y > 1024
+    pairs = sample_pairs(M, N, 3000, 11)
+    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
+                                                   alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    D = run_gemm(Dev(p), split_k=2)
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "wide s=2")
+
+
+@pytest.mark.parametrize("kernel", ["auto", "pair"])
+def test_d_only_16_byte_aligned(oracle_mod, monkeypatch, kernel):
+    """D whose rows are 16- but not 32-byte aligned (base offset 8 elements,
+    ldd % 16 == 8): the epilogues fall back from 32- to 16-byte stores."""
+    if kernel == "pair":
+        monkeypatch.setenv("MXFP4_KERNEL", "pair")
+    M, N, K = 384, 512, 512
+    p = inputs.make_problem("d16", M, N, K, seed=31, values="codes", alpha=1.0, beta=1.0,
+                            c_sigma=1.0)
+    Dref, sabs = full_oracle(oracle_mod, p)
+    dev = Dev(p)
+    ldd = N + 24
+    buf = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D = buf[:, 8:8 + N]
+    assert D.data_ptr() % 32 == 16
+    wsb = mx.mxfp4_gemm_workspace_size(M, N, K, 0)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm(D, ldd, dev.C, N, dev.A, K, dev.B, K, dev.SA, K // 32, dev.SB, K // 32,
+                  p.alpha, p.beta, M, N, K, 0, ws, wsb)
+    torch.cuda.synchronize()
+    assert_within_bound(d_to_bits(D.contiguous()), Dref, sabs, p.alpha, f"d16 {kernel}")
+    assert torch.isnan(buf[:, :8].float()).all() and torch.isnan(buf[:, 8 + N:].float()).all()

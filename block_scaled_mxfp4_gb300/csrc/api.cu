@@ -690,6 +690,27 @@ int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld
     return MXFP4_OK;
 }
 
+int mxfp4_scale_relayout2(void *dst_a, const void *src_a, int rows_a, int64_t ld_a, void *dst_b,
+                          const void *src_b, int rows_b, int64_t ld_b, int K, void *stream)
+{
+    if (!dst_a || !src_a || !dst_b || !src_b || rows_a < 1 || rows_b < 1 || K < 32 ||
+        (K % 32) != 0 || ld_a < K / 32 || ld_b < K / 32)
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(dst_a, 16) || !aligned(dst_b, 16))
+        return MXFP4_ERR_MISALIGNED;
+    if (sf_row_blocks(rows_a) + sf_row_blocks(rows_b) > 0x7FFFFFFF)
+        return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    if (launch_scale_relayout2(static_cast<uint8_t *>(dst_a), static_cast<const uint8_t *>(src_a),
+                               rows_a, ld_a, static_cast<uint8_t *>(dst_b),
+                               static_cast<const uint8_t *>(src_b), rows_b, ld_b, K,
+                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    return MXFP4_OK;
+}
+
 // Shared body of mxfp4_gemm and mxfp4_gemm_prepacked after their own checks.
 static int gemm_entry(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
                       const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M,
@@ -771,8 +792,7 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
     if (plan.relayout_pass) {
         uint8_t *sfa = ws + head;
         uint8_t *sfb = sfa + sfa_bytes;
-        if (launch_scale_relayout(sfa, sc.a, M, K, ld_sa, s) != cudaSuccess ||
-            launch_scale_relayout(sfb, sc.b, N, K, ld_sb, s) != cudaSuccess)
+        if (launch_scale_relayout2(sfa, sc.a, M, ld_sa, sfb, sc.b, N, ld_sb, K, s) != cudaSuccess)
             return MXFP4_ERR_CUDA;
         sc = Scales{sfa, sfb, 0, 0, false};
     }

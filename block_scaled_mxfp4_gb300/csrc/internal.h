@@ -132,6 +132,10 @@ cudaError_t launch_gemv(const GemvArgs &g, int sms, cudaStream_t stream);
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
                                   cudaStream_t stream);
+// Both operands' scales (same K) in one launch.
+cudaError_t launch_scale_relayout2(uint8_t *dst0, const uint8_t *src0, int rows0, int64_t ld0,
+                                   uint8_t *dst1, const uint8_t *src1, int rows1, int64_t ld1,
+                                   int K, cudaStream_t stream);
 
 cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float alpha, float beta,
                                  const uint16_t *C, int64_t ldc, uint16_t *D, int64_t ldd,

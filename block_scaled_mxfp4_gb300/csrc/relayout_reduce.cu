@@ -15,7 +15,8 @@ namespace mxfp4 {
 // line holds rows i, i+32, i+64, i+96 -- the 32x128b source shape that
 // tcgen05.cp replicates into the four TMEM lane groups.
 //
-// One CTA of 256 threads handles one 128-row block and up to kGroupsPerCta
+// One CTA of 256 threads handles one 128-row block (of either operand when
+// both are relaid in one launch) and up to kGroupsPerCta
 // atoms along K: it reads the 128 x (4*kGroupsPerCta) scale bytes with
 // consecutive threads on consecutive words of a row, stages them in shared
 // memory (rows padded to an odd word count, so the column reads below hit 32
@@ -24,13 +25,28 @@ namespace mxfp4 {
 constexpr int kGroupsPerCta = 16;
 constexpr int kRelayoutThreads = 256;
 
+// One or two operands per launch: row blocks [0, rblocks0) of grid x belong to
+// operand 0, the rest to operand 1 (both have the same K).
+struct RelayoutJob {
+    uint8_t *dst[2];
+    const uint8_t *src[2];
+    int rows[2];
+    int64_t ld[2];
+    int64_t rblocks0;
+    int vec4[2];
+};
+
 __global__ void __launch_bounds__(kRelayoutThreads)
-    scale_relayout_kernel(uint8_t *__restrict__ dst, const uint8_t *__restrict__ src, int rows,
-                          int kblocks, int64_t ld, int64_t groups, int vec4)
+    scale_relayout_kernel(const RelayoutJob job, int kblocks, int64_t groups)
 {
     __shared__ uint32_t tile[128][kGroupsPerCta + 1];
     const int t = threadIdx.x;
-    const int64_t rb = blockIdx.x;
+    const int op = static_cast<int64_t>(blockIdx.x) < job.rblocks0 ? 0 : 1;
+    const int64_t rb = static_cast<int64_t>(blockIdx.x) - (op ? job.rblocks0 : 0);
+    const uint8_t *src = job.src[op];
+    const int rows = job.rows[op];
+    const int64_t ld = job.ld[op];
+    const int vec4 = job.vec4[op];
     const int64_t g0 = static_cast<int64_t>(blockIdx.y) * kGroupsPerCta;
     const int ng = static_cast<int>(groups - g0 < kGroupsPerCta ? groups - g0 : kGroupsPerCta);
 
@@ -54,7 +70,7 @@ __global__ void __launch_bounds__(kRelayoutThreads)
         tile[r][w] = word;
     }
     __syncthreads();
-    uint8_t *out = dst + (rb * groups + g0) * kSfAtomBytes;
+    uint8_t *out = job.dst[op] + (rb * groups + g0) * kSfAtomBytes;
     for (int e = t; e < ng * 32; e += kRelayoutThreads) {
         const int atom = e / 32;
         const int i = e % 32;
@@ -63,17 +79,53 @@ __global__ void __launch_bounds__(kRelayoutThreads)
     }
 }
 
+static cudaError_t launch_relayout_job(RelayoutJob &job, int nops, int K, cudaStream_t stream)
+{
+    const int64_t groups = sf_groups(K);
+    int64_t total = 0;
+    for (int i = 0; i < nops; ++i) {
+        job.vec4[i] = (reinterpret_cast<uintptr_t>(job.src[i]) % 4 == 0) && (job.ld[i] % 4 == 0);
+        total += sf_row_blocks(job.rows[i]);
+    }
+    job.rblocks0 = sf_row_blocks(job.rows[0]);
+    if (nops == 1) {
+        job.dst[1] = job.dst[0];
+        job.src[1] = job.src[0];
+        job.rows[1] = job.rows[0];
+        job.ld[1] = job.ld[0];
+        job.vec4[1] = job.vec4[0];
+    }
+    dim3 grid(static_cast<unsigned>(total),
+              static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
+    scale_relayout_kernel<<<grid, kRelayoutThreads, 0, stream>>>(job, K / 32, groups);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
                                   cudaStream_t stream)
 {
-    const int64_t groups = sf_groups(K);
-    const int64_t rblocks = sf_row_blocks(rows);
-    const int vec4 = (reinterpret_cast<uintptr_t>(src) % 4 == 0) && (ld % 4 == 0);
-    dim3 grid(static_cast<unsigned>(rblocks),
-              static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
-    scale_relayout_kernel<<<grid, kRelayoutThreads, 0, stream>>>(dst, src, rows, K / 32, ld, groups,
-                                                                 vec4);
-    return cudaGetLastError();
+    RelayoutJob job{};
+    job.dst[0] = dst;
+    job.src[0] = src;
+    job.rows[0] = rows;
+    job.ld[0] = ld;
+    return launch_relayout_job(job, 1, K, stream);
+}
+
+cudaError_t launch_scale_relayout2(uint8_t *dst0, const uint8_t *src0, int rows0, int64_t ld0,
+                                   uint8_t *dst1, const uint8_t *src1, int rows1, int64_t ld1,
+                                   int K, cudaStream_t stream)
+{
+    RelayoutJob job{};
+    job.dst[0] = dst0;
+    job.src[0] = src0;
+    job.rows[0] = rows0;
+    job.ld[0] = ld0;
+    job.dst[1] = dst1;
+    job.src[1] = src1;
+    job.rows[1] = rows1;
+    job.ld[1] = ld1;
+    return launch_relayout_job(job, 2, K, stream);
 }
 
 // --------------------------------------------------------- split-K reduce --

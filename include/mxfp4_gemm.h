@@ -127,6 +127,16 @@ int mxfp4_scale_relayout(void *dst, const void *src, int rows, int K, int64_t ld
                          void *stream);
 
 /*
+ * mxfp4_scale_relayout of both operands' scales (the same K) in one launch:
+ * src_a [rows_a, ld_a] -> dst_a and src_b [rows_b, ld_b] -> dst_b, each dst
+ * mxfp4_scale_relayout_size(rows, K) bytes, 16-byte aligned, not overlapping.
+ * Same layout, fill and errors as mxfp4_scale_relayout; mxfp4_gemm uses it
+ * for its relayout pass.
+ */
+int mxfp4_scale_relayout2(void *dst_a, const void *src_a, int rows_a, int64_t ld_a, void *dst_b,
+                          const void *src_b, int rows_b, int64_t ld_b, int K, void *stream);
+
+/*
  * The GEMM (page formula; section "Kernel ABI" for the argument set).
  *   D       bf16 [M, ldd]           output; ldd >= N
  *   C       bf16 [M, ldc] or NULL   read only when beta != 0; may alias D

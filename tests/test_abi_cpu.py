@@ -192,6 +192,12 @@ def test_other_entry_points_validate_before_device(L):
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 48, 2, None) == -1
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 64, 1, None) == -1
     assert L.mxfp4_scale_relayout(0x1008, 0x2000, 4, 64, 2, None) == -3
+    r2 = L.mxfp4_scale_relayout2
+    assert r2(None, 0x2000, 4, 2, 0x3000, 0x4000, 4, 2, 64, None) == -1
+    assert r2(0x1000, 0x2000, 4, 2, 0x3000, 0x4000, 0, 2, 64, None) == -1
+    assert r2(0x1000, 0x2000, 4, 2, 0x3000, 0x4000, 4, 1, 64, None) == -1
+    assert r2(0x1000, 0x2000, 4, 2, 0x3000, 0x4000, 4, 2, 48, None) == -1
+    assert r2(0x1000, 0x2000, 4, 2, 0x3008, 0x4000, 4, 2, 64, None) == -3
     assert L.mxfp4_gemm_prepacked(0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, None, 0x5000,
                                   1.0, 0.0, 128, 256, 512, 0, None, 0, None) == -1
     assert L.mxfp4_gemm_prepacked(0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, 0x4008, 0x5000,

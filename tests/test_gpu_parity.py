@@ -84,6 +84,23 @@ def test_scale_relayout_bytes(rows, K):
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("rows_a,rows_b,K", [(1, 8192, 1024), (300, 257, 288), (129, 64, 64)])
+def test_scale_relayout2_bytes(rows_a, rows_b, K):
+    """Both operands in one launch: each destination holds exactly what the
+    single-operand relayout writes (different row strides, ragged rows)."""
+    rng = np.random.default_rng(rows_a + 3 * rows_b + K)
+    ld_a, ld_b = K // 32 + 1, K // 32 + 5
+    Sa = rng.integers(0, 256, size=(rows_a, ld_a), dtype=np.uint8)
+    Sb = rng.integers(0, 256, size=(rows_b, ld_b), dtype=np.uint8)
+    da = torch.zeros(mx.mxfp4_scale_relayout_size(rows_a, K), dtype=torch.uint8, device="cuda")
+    db = torch.zeros(mx.mxfp4_scale_relayout_size(rows_b, K), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_scale_relayout2(da, torch.from_numpy(Sa).cuda(), rows_a, ld_a,
+                             db, torch.from_numpy(Sb).cuda(), rows_b, ld_b, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(da.cpu().numpy(), relayout_reference(Sa, rows_a, K))
+    assert np.array_equal(db.cpu().numpy(), relayout_reference(Sb, rows_b, K))
+
+
 # ------------------------------------------------- scale placement probes --
 
 def _ones_problem(M, N, K):

@@ -4,13 +4,14 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--split-k S]
     python bench.py --impl reference ...     # the CPU oracle on a bounded sample
 
-One step is the whole hot path on one batch of resident inputs: one
-mxfp4_gemm call -- the tcgen05 GEMM, which builds the tcgen05 scale layout
-from the row-major E8M0 scales itself, plus the split-K reduce when K is
-split.  (--prepacked times the other form: both scale relayout kernels and
-the GEMM on relaid scales.)  Steps are timed with CUDA events on the launching
-stream; L2 is flushed (a 512 MiB write) between timed steps, outside the
-events.  Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs
+One step is the whole hot path on one batch of resident inputs, as
+mxfp4_gemm runs it: for compute-bound shapes the scale relayout of A and B
+(one launch) and the GEMM on relaid scales (issued through the public calls
+so the GEMM kernel has its own events); otherwise the GEMM that builds the
+tcgen05 scale layout itself, plus the split-K reduce when K is split.
+(--prepacked always times the relayout + prepacked form.)  Steps are timed
+with CUDA events on the launching stream; L2 is flushed (a 512 MiB write)
+between timed steps, outside the events.  Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs
 an independent replica of the workload (the GEMM needs no exchange), the
 barrier + max over ranks times the job, and value counts all ranks' FLOPs.
 """
@@ -32,6 +33,52 @@ METRIC = "MXFP4 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP4 peak / HB
 UNIT = "TFLOP/s"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 / dense bf16 tensor rate
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise max of a list of floats over all ranks (the job's time is
+    the slowest replica's); the values themselves without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def replica_throughput(world, flops_per_step, steps, total_ms):
+    """Whole-job TFLOP/s: each of `world` replicas ran `steps` GEMMs of
+    `flops_per_step`, and the job took the slowest rank's `total_ms`."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
+KERNEL_SOURCES = ("gemm_pair.cuh", "gemm_sm103.cu", "gemm_persistent.cuh", "ptx.cuh",
+                  "internal.h", "api.cu")
+
+
+def kernel_sources_sha1():
+    """Hash of the GEMM kernels' sources: DRAM counters taken for one version
+    are only reported while the sources are unchanged."""
+    import hashlib
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_scaled_mxfp4_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes (read + write) of one launch of `kernel` on `workload` from
+    profiles/traffic.json (an ncu counter capture), or None if there is no
+    capture for these sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel") != kernel or rec.get("sources_sha1") != kernel_sources_sha1():
+        return None
+    return rec["dram_bytes_read"] + rec["dram_bytes_write"]
 
 
 def parse_args():
@@ -272,12 +319,9 @@ def main():
     gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     tot_ms = sum(step_ms)
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
-    if dist:
-        t = torch.tensor([tot_ms, gemm_avg], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms, gemm_avg = float(t[0]), float(t[1])
+    tot_ms, gemm_avg = max_over_ranks([tot_ms, gemm_avg], dist, dev)
     ms_per_step = tot_ms / args.steps
-    value = world * flops * args.steps / (tot_ms * 1e-3) / 1e12
+    value = replica_throughput(world, flops, args.steps, tot_ms)
     launches_per_step = (2 if split_form else 1) + \
         (1 if plan.split_k > 1 else 0)
 
@@ -303,10 +347,30 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([e2e_ms], dist, dev)[0]
+    # A plain streaming read of the same bytes after the same flush: the
+    # floor a single pass over this much data reaches on this GPU.
+    stream_floor = None
+    if args.workload in ("decode", "skinny"):
+        src = torch.ones(algo_bytes // 8, dtype=torch.int64, device=dev)
+        sink = torch.zeros(1, dtype=torch.int32, device=dev)
+        fts = []
+        for i in range(23):
+            flush.fill_(i & 0xFF)
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            mx.mxfp4_stream_read_probe(src, algo_bytes // 16 * 16, sink, stream)
+            f1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                fts.append(f0.elapsed_time(f1))
+        fl = statistics.median(fts)
+        stream_floor = {"what": "mxfp4_stream_read_probe (one streaming read of the "
+                                "algorithmic bytes, 16-byte loads from every SM) after the "
+                                "same 512 MiB flush",
+                        "us": fl * 1e3, "GB/s": algo_bytes / (fl * 1e-3) / 1e9,
+                        "gemm_over_floor": gemm_avg / fl}
+        del src
     h2d = hA.numel() + hB.numel() + hSA.numel() + hSB.numel() + (hC.numel() * 2 if hC is not None else 0)
     d2h = hD.numel() * 2
 
@@ -327,9 +391,14 @@ def main():
         roof = {"bound": "hbm", "achieved": algo_bytes / (gemm_avg * 1e-3) / 1e9, "peak": peak,
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
     kname = ("gemv_mxf4_kernel" if plan.gemv else "gemm_mxf4_pair" if plan.pair else
              "gemm_mxf4_persistent" if plan.persistent else "gemm_mxf4_kernel")
+    roof["traffic"] = recorded_traffic(args.workload, kname)
+    roof["traffic_source"] = ("profiles/traffic.json (ncu dram__bytes_read.sum + "
+                              "dram__bytes_write.sum of one launch, same kernel sources)"
+                              if roof["traffic"] is not None else None)
+    if stream_floor is not None:
+        roof["stream_floor"] = stream_floor
     roof["kernel"] = (kname + (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
                       + (" (scales relaid by the relayout kernel, timed outside this figure)"
                          if split_form else " (scale layout built in-kernel)"))
@@ -361,7 +430,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": replica_throughput(world, flops, 1, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "api": "mxfp4_gemm_host (pinned host buffers)"},
         "gpu_launches": launches_per_step * args.steps,

@@ -21,7 +21,7 @@ __all__ = [
     "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host", "mxfp4_scale_relayout", "mxfp4_scale_relayout2",
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
-    "mxfp4_wait_timeout_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
+    "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
     "gemm", "Plan",
 ]
 
@@ -91,6 +91,7 @@ def lib() -> ctypes.CDLL:
                                       vp, sz, vp]),
             "mxfp4_device_status": (i32, [ctypes.POINTER(ctypes.c_int), i32]),
             "mxfp4_wait_timeout_probe": (i32, [ctypes.c_longlong, vp]),
+            "mxfp4_stream_read_probe": (i32, [vp, sz, vp, vp]),
             "mxfp4_set_wait_limit": (None, [ctypes.c_longlong]),
             "mxfp4_strerror": (ctypes.c_char_p, [i32]),
             "mxfp4_version": (i32, []),
@@ -215,6 +216,11 @@ def mxfp4_device_status(reset=False) -> int:
 def mxfp4_wait_timeout_probe(limit_cycles, stream=None):
     return _check(lib().mxfp4_wait_timeout_probe(limit_cycles, _stream(stream)),
                   "mxfp4_wait_timeout_probe")
+
+
+def mxfp4_stream_read_probe(src, nbytes, sink, stream=None):
+    return _check(lib().mxfp4_stream_read_probe(_p(src), nbytes, _p(sink), _stream(stream)),
+                  "mxfp4_stream_read_probe")
 
 
 def mxfp4_set_wait_limit(cycles):

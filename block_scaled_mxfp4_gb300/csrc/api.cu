@@ -892,4 +892,19 @@ int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream)
                : MXFP4_ERR_CUDA;
 }
 
+int mxfp4_stream_read_probe(const void *src, size_t bytes, void *sink, void *stream)
+{
+    if (!src || !sink || bytes < 16)
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(sink, 4))
+        return MXFP4_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    return launch_stream_read(src, bytes, static_cast<unsigned *>(sink), device_sms_or_default(),
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
 }  // extern "C"

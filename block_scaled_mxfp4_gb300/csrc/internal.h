@@ -143,6 +143,9 @@ cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float
 
 cudaError_t launch_wait_probe(long long limit, cudaStream_t stream);
 
+cudaError_t launch_stream_read(const void *src, size_t bytes, unsigned *sink, int sms,
+                               cudaStream_t stream);
+
 cudaError_t read_device_status(int *status, int reset);
 
 }  // namespace mxfp4

@@ -142,7 +142,13 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v)
     return *reinterpret_cast<uint16_t *>(&b);
 }
 
-__global__ void __launch_bounds__(256)
+constexpr int kReduceThreads = 128;
+constexpr int kReduceMaxSplit = 16;
+
+// Each thread owns 4 consecutive n of one row and loads all its split
+// partials before adding them (in split order), so a thread waits for one
+// memory round trip rather than one per split.
+__global__ void __launch_bounds__(kReduceThreads)
     splitk_reduce_kernel(const float *__restrict__ ws, int split, int M, int N, float alpha,
                          float beta, const uint16_t *__restrict__ C, int64_t ldc,
                          uint16_t *__restrict__ D, int64_t ldd)
@@ -159,12 +165,19 @@ __global__ void __launch_bounds__(256)
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         const float *p = ws + m * N + n;
         if (vec) {
-            for (int z = 0; z < split; ++z) {
-                const float4 v = __ldcs(reinterpret_cast<const float4 *>(p + z * plane));
-                s[0] += v.x;
-                s[1] += v.y;
-                s[2] += v.z;
-                s[3] += v.w;
+            float4 v[kReduceMaxSplit];
+#pragma unroll
+            for (int z = 0; z < kReduceMaxSplit; ++z)
+                if (z < split)
+                    v[z] = __ldcs(reinterpret_cast<const float4 *>(p + z * plane));
+#pragma unroll
+            for (int z = 0; z < kReduceMaxSplit; ++z) {
+                if (z < split) {
+                    s[0] += v[z].x;
+                    s[1] += v[z].y;
+                    s[2] += v[z].z;
+                    s[3] += v[z].w;
+                }
             }
         } else {
             for (int z = 0; z < split; ++z)
@@ -184,15 +197,17 @@ cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float
                                  const uint16_t *C, int64_t ldc, uint16_t *D, int64_t ldd, int sms,
                                  cudaStream_t stream)
 {
+    if (split > kReduceMaxSplit)
+        return cudaErrorInvalidValue;
     const int64_t quads = (static_cast<int64_t>(N) + 3) / 4 * M;
-    int64_t blocks = (quads + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+    int64_t blocks = (quads + kReduceThreads - 1) / kReduceThreads;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 16;
     if (blocks > cap)
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, split, M, N, alpha,
-                                                                            beta, C, ldc, D, ldd);
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(
+        ws, split, M, N, alpha, beta, C, ldc, D, ldd);
     return cudaGetLastError();
 }
 

@@ -232,6 +232,17 @@ int mxfp4_device_status(int *status, int reset);
  */
 int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream);
 
+/*
+ * Measurement hook: reads `bytes` (rounded down to a multiple of 16) of the
+ * device buffer `src` (16-byte aligned) once with 16-byte loads from every
+ * SM, several in flight per thread -- the time a single streaming pass over
+ * that much data takes on this GPU, the floor for the GEMM's bandwidth-bound
+ * shapes.  `sink` is a device word the kernel may write (practically never).
+ * The pages have no counterpart.  Returns MXFP4_OK, MXFP4_ERR_INVALID_ARG
+ * (null pointer or bytes < 16), MXFP4_ERR_MISALIGNED or a device error.
+ */
+int mxfp4_stream_read_probe(const void *src, size_t bytes, void *sink, void *stream);
+
 /* Set the in-kernel wait limit in SM clock cycles (default 2^32, ~2 s). */
 void mxfp4_set_wait_limit(long long cycles);
 

@@ -192,6 +192,9 @@ def test_other_entry_points_validate_before_device(L):
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 48, 2, None) == -1
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 64, 1, None) == -1
     assert L.mxfp4_scale_relayout(0x1008, 0x2000, 4, 64, 2, None) == -3
+    assert L.mxfp4_stream_read_probe(None, 64, 0x1000, None) == -1
+    assert L.mxfp4_stream_read_probe(0x1000, 8, 0x2000, None) == -1
+    assert L.mxfp4_stream_read_probe(0x1008, 64, 0x2000, None) == -3
     r2 = L.mxfp4_scale_relayout2
     assert r2(None, 0x2000, 4, 2, 0x3000, 0x4000, 4, 2, 64, None) == -1
     assert r2(0x1000, 0x2000, 4, 2, 0x3000, 0x4000, 0, 2, 64, None) == -1

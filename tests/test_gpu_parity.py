@@ -509,3 +509,14 @@ def test_d_only_16_byte_aligned(oracle_mod, monkeypatch, kernel):
     torch.cuda.synchronize()
     assert_within_bound(d_to_bits(D.contiguous()), Dref, sabs, p.alpha, f"d16 {kernel}")
     assert torch.isnan(buf[:, :8].float()).all() and torch.isnan(buf[:, 8 + N:].float()).all()
+
+
+def test_stream_read_probe_runs():
+    """The streaming-read measurement hook reads a buffer and returns cleanly
+    (including a byte count that is not a multiple of the grid's stride)."""
+    buf = torch.ones((40 << 20) // 8 + 3, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for nbytes in (16, 4096 + 16, buf.numel() * 8 // 16 * 16):
+        mx.mxfp4_stream_read_probe(buf, nbytes, sink)
+    torch.cuda.synchronize()
+    assert mx.mxfp4_device_status() == 0

@@ -4,16 +4,19 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--split-k S]
     python bench.py --impl reference ...     # the CPU oracle on a bounded sample
 
-One step is the whole hot path on one batch of resident inputs, as
-mxfp4_gemm runs it: for compute-bound shapes the scale relayout of A and B
-(one launch) and the GEMM on relaid scales (issued through the public calls
-so the GEMM kernel has its own events); otherwise the GEMM that builds the
-tcgen05 scale layout itself, plus the split-K reduce when K is split.
-(--prepacked always times the relayout + prepacked form.)  Steps are timed
+One step is the whole hot path on one batch of resident inputs: one
+mxfp4_gemm call, as a user makes it -- for compute-bound shapes the scale
+relayout of A and B (one launch) and the GEMM on the relaid scales, launched
+as its programmatic dependent; otherwise the GEMM that builds the tcgen05
+scale layout itself, plus the split-K reduce (a dependent launch) when K is
+split.  (--prepacked times mxfp4_scale_relayout2 + mxfp4_gemm_prepacked.)
+The roofline's kernel time is the GEMM alone on relaid scales, timed in a
+second event loop when the step holds more than the GEMM.  Steps are timed
 with CUDA events on the launching stream; L2 is flushed (a 512 MiB write)
-between timed steps, outside the events.  Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs
-an independent replica of the workload (the GEMM needs no exchange), the
-barrier + max over ranks times the job, and value counts all ranks' FLOPs.
+between timed steps, outside the events.  Rank 0 prints one JSON line.  With
+N > 1 (torchrun) every rank runs an independent replica of the workload (the
+GEMM needs no exchange), the barrier + max over ranks times the job, and
+value counts all ranks' FLOPs.
 """
 from __future__ import annotations
 
@@ -267,36 +270,41 @@ def main():
     sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device=dev)
     sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device=dev)
     plan = mx.mxfp4_plan_gemm(M, N, K, args.split_k, 0)
-    # When mxfp4_gemm would run a relayout pass, issue the same two kernels
-    # through the public calls so the GEMM kernel gets its own events.
-    split_form = args.prepacked or plan.relayout_pass
-    wsb = (mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, args.split_k) if split_form
-           else mx.mxfp4_gemm_workspace_size(M, N, K, args.split_k))
+    wsb = mx.mxfp4_gemm_workspace_size(M, N, K, args.split_k)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    wpb = mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, args.split_k)
+    wp = torch.empty(max(wpb, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # Compute-bound shapes relay the scales out first (plan.relayout_pass); the
+    # roofline then needs the GEMM kernel alone, timed on relaid scales.
+    gemm_alone = args.prepacked or plan.relayout_pass
+    mx.mxfp4_scale_relayout2(sfa, SA, M, K // 32, sfb, SB, N, K // 32, K, stream)
 
     def step():
-        if split_form:
+        if args.prepacked:
             mx.mxfp4_scale_relayout2(sfa, SA, M, K // 32, sfb, SB, N, K // 32, K, stream)
-
-    def gemm():
-        if split_form:
             mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
-                                    args.split_k, ws, wsb, stream)
+                                    args.split_k, wp, wpb, stream)
         else:
             mx.mxfp4_gemm(D, N, C, N, A, K, B, K, SA, K // 32, SB, K // 32, p.alpha, p.beta,
                           M, N, K, args.split_k, ws, wsb, stream)
 
+    def gemm_kernel():
+        mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
+                                args.split_k, wp, wpb, stream)
+
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
         step()
-        gemm()
+        if gemm_alone:
+            flush.fill_(1)
+            gemm_kernel()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     torch.cuda.synchronize()
@@ -308,21 +316,30 @@ def main():
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
-        gemm()
-        ev[i][2].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    # The GEMM kernel alone (relaid scales, same flush) for the roofline, when
+    # the step holds more than the GEMM and its reduce.
+    if gemm_alone:
+        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            kev[i][0].record(stream)
+            gemm_kernel()
+            kev[i][1].record(stream)
+        torch.cuda.synchronize()
     clocks = sampler.stop()
     if dist:
         dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    gemm_ms = ([kev[i][0].elapsed_time(kev[i][1]) for i in range(args.steps)] if gemm_alone
+               else step_ms)
     tot_ms = sum(step_ms)
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     tot_ms, gemm_avg = max_over_ranks([tot_ms, gemm_avg], dist, dev)
     ms_per_step = tot_ms / args.steps
     value = replica_throughput(world, flops, args.steps, tot_ms)
-    launches_per_step = (2 if split_form else 1) + \
+    launches_per_step = (2 if plan.relayout_pass or args.prepacked else 1) + \
         (1 if plan.split_k > 1 else 0)
 
     # ---- end to end: host buffers through the C ABI, copies in the timed region
@@ -400,8 +417,8 @@ def main():
     if stream_floor is not None:
         roof["stream_floor"] = stream_floor
     roof["kernel"] = (kname + (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
-                      + (" (scales relaid by the relayout kernel, timed outside this figure)"
-                         if split_form else " (scale layout built in-kernel)"))
+                      + (" (GEMM alone on relaid scales, timed in its own loop)"
+                         if gemm_alone else " (scale layout built in-kernel)"))
     roof["kernel_ms"] = gemm_avg
     roof["algorithmic_bytes"] = algo_bytes
     roof["flops"] = flops
@@ -421,12 +438,14 @@ def main():
                    "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
                    "grid": [plan.grid_x, plan.grid_y, plan.grid_z],
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
-                   "step": ("scale relayout of A and B (one launch) + GEMM on relaid scales"
+                   "step": ("mxfp4_scale_relayout2 + mxfp4_gemm_prepacked"
                             if args.prepacked else
-                            "mxfp4_gemm: scale relayout of A and B (one launch) + GEMM on relaid scales"
+                            "one mxfp4_gemm call: scale relayout of A and B (one launch) + GEMM "
+                            "on relaid scales (launched as its dependent)"
                             if plan.relayout_pass else
-                            "mxfp4_gemm: GEMM with in-kernel scale relayout")
-                           + (" + split-K reduce" if plan.split_k > 1 else ""),
+                            "one mxfp4_gemm call: GEMM with in-kernel scale layout")
+                           + (" + split-K reduce (launched as its dependent)"
+                              if plan.split_k > 1 else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -434,6 +453,9 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "api": "mxfp4_gemm_host (pinned host buffers)"},
         "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_note": "our kernels in the timed step loop; the roofline's GEMM-alone loop "
+                             "(same count of GEMM launches) runs after it" if gemm_alone else
+                             "our kernels in the timed step loop",
         "clocks": clocks,
         "wall_s_timed_loop": t_wall,
     }

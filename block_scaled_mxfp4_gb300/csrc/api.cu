@@ -463,7 +463,7 @@ int next_epoch()
 int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
              const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M, int N,
              int K, const mxfp4_plan &plan, const GemmShape &shape, uint8_t *ws, int sms,
-             cudaStream_t stream)
+             cudaStream_t stream, bool after_relayout = false)
 {
     float *partials = ws ? reinterpret_cast<float *>(ws + kFlagBytes) : nullptr;
     if (shape.gemv) {
@@ -513,7 +513,8 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
         a.wait_limit = g_wait_limit.load();
         const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
-        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB, stream) !=
+        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
+                             after_relayout, stream) !=
             cudaSuccess)
             return MXFP4_ERR_CUDA;
         return MXFP4_OK;
@@ -797,7 +798,8 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
         sc = Scales{sfa, sfb, 0, 0, false};
     }
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
-                    plan.workspace_bytes ? ws : nullptr, sms, s);
+                    plan.workspace_bytes ? ws : nullptr, sms, s,
+                    plan.relayout_pass != 0);
 }
 
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)

@@ -216,6 +216,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
         if (lane == 0) {
             const int role = warp == 4 ? 0 : warp - 5;   // 0: A, 1: B, 2: scales
             const uint64_t pol = l2_policy_evict_last();
+            // Launched right after the scale relayout (programmatic stream
+            // serialisation), only the relaid scales depend on it.
+            if (role == 2)
+                pdl_wait_prerequisites();
             const uint32_t bytes = role == 0 ? PC::A_BYTES : role == 1 ? PC::B_BYTES : PC::SF_BYTES;
             int stage = 0;
             uint32_t phase = 0;

@@ -373,6 +373,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // A split-K reduce launched after this kernel may start its prologue; it
+    // waits for this grid's completion before reading the partials.
+    if (threadIdx.x == 0)
+        pdl_launch_dependents();
 
     if (warp == 4 || warp >= 6) {
         // ------------------------------------------------------ producer --
@@ -764,7 +768,8 @@ size_t gemm_pair_smem_bytes() { return PairCfg<kPairStages>::SMEM_BYTES; }
 
 cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
                              const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream)
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
+                             cudaStream_t stream)
 {
     using PC = PairCfg<kPairStages>;
     auto kern = gemm_mxf4_pair<kPairStages>;
@@ -784,8 +789,24 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
     ps.tiles_q = tiles_q;
     ps.kt = a.kt_total;
     ps.group = tiles_p < 8 ? tiles_p : 8;
-    kern<<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
-    return cudaGetLastError();
+    if (!after_relayout) {
+        kern<<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
+        return cudaGetLastError();
+    }
+    // Right after this library's scale relayout: programmatic stream
+    // serialisation lets the GEMM's prologue and operand loads overlap the
+    // relayout; only the scale producers wait for it (griddepcontrol.wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(PC::THREADS);
+    cfg.dynamicSmemBytes = PC::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, ps, tmA, tmB, tmSA, tmSB);
 }
 
 // Test hook: one wait on an mbarrier nobody arrives at.

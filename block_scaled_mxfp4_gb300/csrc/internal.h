@@ -103,9 +103,12 @@ cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sched, const 
 
 // CTA-pair kernel (relaid scales): grid = ctas (even), tiles of 256 x 256.
 size_t gemm_pair_smem_bytes();
+// after_relayout: launched right after this library's scale relayout on the
+// same stream (programmatic dependent launch; only the scale loads wait).
 cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
                              const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream);
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
+                             cudaStream_t stream);
 
 // Persistent configuration: dynamic smem (0 if not compiled) and resident
 // CTAs per SM the occupancy calculator allows (0 on error).

@@ -276,6 +276,20 @@ __device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, 
                  : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream (launched
+// with programmatic stream serialisation) start its prologue now; and, in
+// that kernel, wait until this one has completed and its writes are visible.
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prerequisites()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------ descriptors --
 
 // Shared-memory matrix descriptor (tcgen05 format): K-major operand tile of

@@ -2,6 +2,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mxfp4 {
 
@@ -41,6 +42,10 @@ __global__ void __launch_bounds__(kRelayoutThreads)
 {
     __shared__ uint32_t tile[128][kGroupsPerCta + 1];
     const int t = threadIdx.x;
+    // The GEMM that follows may start its prologue (it waits for this grid
+    // before reading the relaid scales).
+    if (t == 0)
+        pdl_launch_dependents();
     const int op = static_cast<int64_t>(blockIdx.x) < job.rblocks0 ? 0 : 1;
     const int64_t rb = static_cast<int64_t>(blockIdx.x) - (op ? job.rblocks0 : 0);
     const uint8_t *src = job.src[op];
@@ -153,6 +158,9 @@ __global__ void __launch_bounds__(kReduceThreads)
                          float beta, const uint16_t *__restrict__ C, int64_t ldc,
                          uint16_t *__restrict__ D, int64_t ldd)
 {
+    // Launched right after the GEMM with programmatic stream serialisation:
+    // the partials are complete and visible once the GEMM grid has finished.
+    pdl_wait_prerequisites();
     const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
     const int64_t total = quads * M;
     const int64_t plane = static_cast<int64_t>(M) * N;
@@ -206,9 +214,21 @@ cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(
-        ws, split, M, N, alpha, beta, C, ldc, D, ldd);
-    return cudaGetLastError();
+    // Programmatic stream serialisation: the reduce grid is scheduled while
+    // the GEMM (which triggers early) still runs and waits in-kernel for its
+    // completion, hiding the launch gap between the two.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, split, M, N, alpha, beta, C, ldc, D,
+                              ldd);
 }
 
 }  // namespace mxfp4

@@ -16,6 +16,9 @@ objects", sections "Data layouts" and "Verification"):
   list and ``np.ldexp``, then one float64 matrix product (a library routine
   used as one step).  Both are exact at the test sizes, so their double sums
   agree bit for bit.
+
+``quantize`` is the oracle of the MXFP4 quantiser (bf16 rows -> packed E2M1
+codes + E8M0 scales) that produces the GEMM's operands.
 """
 from __future__ import annotations
 
@@ -75,6 +78,8 @@ def bind(path: str) -> ctypes.CDLL:
                                       ctypes.c_double, ctypes.c_double, u16p, i64,
                                       ctypes.POINTER(ctypes.c_int64), i64,
                                       u16p, dp, dp, ctypes.c_int]
+    L.oracle_quantize.restype = ctypes.c_int
+    L.oracle_quantize.argtypes = [ctypes.c_int, ctypes.c_int, u16p, i64, u8p, i64, u8p, i64]
     return L
 
 
@@ -193,3 +198,18 @@ def dequant(packed: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
 def acc_numpy(A, B, SA, SB, K) -> np.ndarray:
     """sum_k a(m,k) b(n,k) as one float64 matmul of the dequantised operands."""
     return dequant(A, SA, K) @ dequant(B, SB, K).T
+
+
+def quantize(X_bits, rows, K):
+    """MXFP4 quantisation of bf16 rows (see oracle.c): returns (packed codes
+    uint8 [rows, K/2], scale codes uint8 [rows, K/32])."""
+    X = np.ascontiguousarray(X_bits, dtype=np.uint16)
+    if X.ndim != 2 or X.shape[0] < rows or X.shape[1] < K:
+        raise ValueError(f"X: bad shape {X.shape}")
+    Q = np.zeros((rows, K // 2), dtype=np.uint8)
+    S = np.zeros((rows, K // 32), dtype=np.uint8)
+    r = lib().oracle_quantize(rows, K, _ptr(X, ctypes.c_uint16), X.shape[1],
+                              _ptr(Q, ctypes.c_uint8), K // 2, _ptr(S, ctypes.c_uint8), K // 32)
+    if r != 0:
+        raise ValueError("oracle_quantize rejected the sizes")
+    return Q, S

@@ -326,3 +326,93 @@ int64_t oracle_gemm_sampled(int M, int N, int K,
     j.pairs = pairs; j.npairs = npairs;
     return run(&j, nthreads);
 }
+
+
+/* ------------------------------------------------------------------------
+ * MXFP4 quantisation of bf16 rows: the step before the GEMM that produces its
+ * operands (the asm_f4gemm page lists operand generation among its reference
+ * helpers, section "Files", without stating the rule; the rule here is the
+ * one the benchmark workloads are built with).  For each 1x32 block of a row:
+ *   1. amax = largest |x| of the block (bf16 values, exact in double);
+ *   2. s = floor(log2(amax / 6)) -- the largest integer with 6 * 2^s <= amax
+ *      (s = 0 when amax == 0), clamped to [-127, 127]; scale code = s + 127;
+ *   3. y = |x| / 2^s (exact), rounded to the nearest E2M1 magnitude
+ *      {0, .5, 1, 1.5, 2, 3, 4, 6} (section "Data layouts"), ties to the
+ *      magnitude with an even code, y >= 6 saturating to 6;
+ *   4. the sign bit (bit 3) copies the sign of x, so a negative x that
+ *      rounds to 0 gives code 8 (-0);
+ *   5. codes are packed two per byte, element 2i in the low nibble.
+ * Readings where the rule is silent: the rounding mode (nearest, ties to
+ * even, as the MFMA page states for its conversions), saturation at 6, and
+ * the sign of zero.  Inputs are finite.
+ * ------------------------------------------------------------------------ */
+
+/* Step 2: the largest s with 6 * 2^s <= amax, found by exact comparisons. */
+static int quant_exponent(double amax)
+{
+    if (amax == 0.0)
+        return 0;
+    int e = 0;
+    frexp(amax, &e);
+    int s = e - 3;
+    while (ldexp(6.0, s) > amax)
+        --s;
+    while (ldexp(6.0, s + 1) <= amax)
+        ++s;
+    if (s < -127)
+        s = -127;
+    if (s > 127)
+        s = 127;
+    return s;
+}
+
+/* Step 3: nearest magnitude code 0..7, ties to the even code. */
+static unsigned quant_magnitude_code(double y)
+{
+    if (y >= 6.0)
+        return 7u;
+    unsigned best = 0u;
+    double best_d = y;   /* distance to magnitude 0 */
+    for (unsigned c = 1u; c < 8u; ++c) {
+        const double d = fabs(y - kE2M1Magnitude[c]);
+        if (d < best_d || (d == best_d && (c & 1u) == 0u)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* Quantise rows [rows, K] of bf16 bits (row stride ldx elements) into packed
+ * codes Q (row stride ldq bytes) and scale codes S (row stride lds bytes).
+ * Returns 0, or -1 for bad sizes. */
+int oracle_quantize(int rows, int K, const uint16_t *X, int64_t ldx, uint8_t *Q, int64_t ldq,
+                    uint8_t *S, int64_t lds)
+{
+    if (rows < 0 || K < 0 || (K % 32) != 0 || ldx < K || ldq < K / 2 || lds < K / 32)
+        return -1;
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *x = X + (int64_t)r * ldx;
+        for (int b = 0; b < K / 32; ++b) {
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                const double v = fabs(oracle_bf16_to_double(x[b * 32 + i]));
+                if (v > amax)
+                    amax = v;
+            }
+            const int s = quant_exponent(amax);
+            S[(int64_t)r * lds + b] = (uint8_t)(s + 127);
+            for (int i = 0; i < 32; i += 2) {
+                unsigned code[2];
+                for (int h = 0; h < 2; ++h) {
+                    const double v = oracle_bf16_to_double(x[b * 32 + i + h]);
+                    code[h] = quant_magnitude_code(ldexp(fabs(v), -s));
+                    if (signbit(v))
+                        code[h] |= 8u;
+                }
+                Q[(int64_t)r * ldq + (b * 32 + i) / 2] = (uint8_t)(code[0] | (code[1] << 4));
+            }
+        }
+    }
+    return 0;
+}

@@ -45,6 +45,19 @@ MUTANTS = {
         "if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0))", "if (frac >= 0.5)"),
     "no_subnormal_clamp": (
         "int q = (E - 1 > -126 ? E - 1 : -126) - 7;", "int q = E - 1 - 7;"),
+    "quant_ties_to_odd": (
+        "if (d < best_d || (d == best_d && (c & 1u) == 0u)) {",
+        "if (d < best_d || (d == best_d && (c & 1u) == 1u)) {"),
+    "quant_exponent_rounded_up": (
+        "while (ldexp(6.0, s + 1) <= amax)", "while (ldexp(4.0, s + 1) <= amax)"),
+    "quant_scale_bias_126": (
+        "S[(int64_t)r * lds + b] = (uint8_t)(s + 127);", "S[(int64_t)r * lds + b] = (uint8_t)(s + 126);"),
+    "quant_nibbles_swapped": (
+        "(uint8_t)(code[0] | (code[1] << 4));", "(uint8_t)(code[1] | (code[0] << 4));"),
+    "quant_amax_half_block": (
+        "for (int i = 0; i < 32; ++i) {\n                const double v = fabs(",
+        "for (int i = 0; i < 16; ++i) {\n                const double v = fabs("),
+    "quant_sign_dropped_for_zero": ("if (signbit(v))", "if (v < 0.0)"),
     "transposed_d_store": (
         "if (!one_output(j, m, n, &j->D[(int64_t)m * j->ldd + n],",
         "if (!one_output(j, m, n, &j->D[(int64_t)(n % j->M) * j->ldd + (m % j->N)],"),

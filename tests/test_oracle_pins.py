@@ -341,11 +341,104 @@ def check_gemm_single_rounding(o):
     assert int(D[0, 0]) == bf16_rne_by_search(exact) == 0x3F81
 
 
+# ------------------------------------------------------------- quantiser --
+
+def _bf16_bits(values):
+    from block_scaled_mxfp4_gb300 import inputs
+    return inputs.f32_to_bf16_bits(np.asarray(values, dtype=np.float32))
+
+
+def check_quant_golden(o):
+    rows = read_golden("quantize_rounding.txt")
+    for x, code in rows:
+        blk = np.zeros((1, 32), dtype=np.float32)
+        blk[0, 0] = 6.0                      # block max 6 -> scale exponent 0
+        blk[0, 1] = float(x)
+        Q, S = o.quantize(_bf16_bits(blk), 1, 32)
+        assert S[0, 0] == 127, (x, S[0, 0])
+        got = int(Q[0, 0] >> 4)              # element 1: high nibble of byte 0
+        assert got == int(code), (x, got, code)
+
+
+def check_quant_scale_rule(o):
+    # 6 * 2^s <= amax < 6 * 2^(s+1) for every block (s = code - 127), s = 0
+    # for an all-zero block, and the clamp at +-127.
+    rng = np.random.default_rng(7)
+    rows, K = 24, 256
+    x = rng.standard_normal((rows, K)) * np.ldexp(1.0, rng.integers(-60, 60, size=(rows, 1)))
+    x[3, 32:64] = 0.0
+    x[5, :32] = np.ldexp(1.0, -133)          # tiny: clamps to s = -127
+    x[6, :32] = 5.9375                       # bf16-exact, just below 6
+    x[7, :32] = 6.0
+    x[8, :32] = -12.0
+    bits = _bf16_bits(x)
+    Q, S = o.quantize(bits, rows, K)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for r in range(rows):
+        for b in range(K // 32):
+            amax = float(np.max(np.abs(xv[r, 32 * b:32 * b + 32])))
+            s = int(S[r, b]) - 127
+            if amax == 0.0:
+                assert s == 0
+            elif s == -127:
+                assert amax < 6.0 * 2.0 ** -126
+            else:
+                assert 6.0 * 2.0 ** s <= amax < 6.0 * 2.0 ** (s + 1), (r, b, amax, s)
+    assert S[6, 0] == 126 and S[7, 0] == 127 and S[8, 0] == 128
+
+
+def check_quant_nearest_brute_force(o):
+    # Every element's code is the nearest of the 16 E2M1 values to x / 2^s
+    # (exact rational distances), ties to the even code, saturating at 6,
+    # with the sign of x.
+    from fractions import Fraction
+    rng = np.random.default_rng(8)
+    rows, K = 6, 128
+    x = rng.standard_normal((rows, K)) * 3.0
+    x[0, :8] = [0.25, -0.25, 2.5, -3.5, 5.0, 0.75, -0.0, 0.0]
+    bits = _bf16_bits(x)
+    Q, S = o.quantize(bits, rows, K)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    mags = [Fraction(v) for v in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    for r in range(rows):
+        for k in range(K):
+            s = int(S[r, k // 32]) - 127
+            y = abs(Fraction(xv[r, k])) / Fraction(2) ** s
+            if y >= 6:
+                want = 7
+            else:
+                d = [abs(y - m) for m in mags]
+                best = min(d)
+                cands = [c for c in range(8) if d[c] == best]
+                want = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+            if np.signbit(xv[r, k]):
+                want |= 8
+            byte = int(Q[r, k // 2])
+            got = (byte >> 4) if k % 2 else (byte & 0xF)
+            assert got == want, (r, k, xv[r, k], s, got, want)
+
+
+def check_quant_matches_generator(o):
+    # The package's input generator implements the same rule independently
+    # (numpy); on bf16-representable data both give the same bytes.
+    from block_scaled_mxfp4_gb300 import inputs
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((40, 512)) * np.ldexp(1.0, rng.integers(-8, 8, size=(40, 1))))
+    bits = _bf16_bits(x)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Qg, Sg = inputs.quantize_rows(xv)
+    Qo, So = o.quantize(bits, 40, 512)
+    assert np.array_equal(So, Sg)
+    assert np.array_equal(Qo, Qg)
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
               check_brute_force, check_all_code_pairs, check_numpy_crosscheck,
-              check_rounding_is_only_error, check_sampled_matches_full]
+              check_rounding_is_only_error, check_sampled_matches_full,
+              check_quant_golden, check_quant_scale_rule, check_quant_nearest_brute_force,
+              check_quant_matches_generator]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

@@ -59,12 +59,12 @@ KERNEL_SOURCES = ("gemm_pair.cuh", "gemm_sm103.cu", "gemm_persistent.cuh", "ptx.
                   "internal.h", "api.cu")
 
 
-def kernel_sources_sha1():
-    """Hash of the GEMM kernels' sources: DRAM counters taken for one version
-    are only reported while the sources are unchanged."""
+def kernel_sources_sha1(names=KERNEL_SOURCES):
+    """Hash of the kernels' sources (the GEMM's by default): DRAM counters
+    taken for one version are only reported while the sources are unchanged."""
     import hashlib
     h = hashlib.sha1()
-    for name in KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "block_scaled_mxfp4_gb300", "csrc", name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
@@ -79,7 +79,9 @@ def recorded_traffic(workload, kernel):
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel") != kernel or rec.get("sources_sha1") != kernel_sources_sha1():
+    if not rec or rec.get("kernel") != kernel:
+        return None
+    if rec.get("sources_sha1") != kernel_sources_sha1(tuple(rec.get("sources", KERNEL_SOURCES))):
         return None
     return rec["dram_bytes_read"] + rec["dram_bytes_write"]
 
@@ -91,7 +93,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large",
-                    choices=["tiny", "decode", "mid", "large", "skinny"])
+                    choices=["tiny", "decode", "mid", "large", "skinny", "quantize"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -210,6 +212,9 @@ def run_reference(args, rank):
     if rank != 0:
         return
     from block_scaled_mxfp4_gb300 import inputs
+    if args.workload == "quantize":
+        run_reference_quantize(args)
+        return
     p = inputs.workload(args.workload)
     per_step = 4.0 if args.steps <= 20 else max(0.5, 80.0 / args.steps)
     for i in range(args.warmup):
@@ -235,6 +240,152 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+QUANT_ROWS, QUANT_K = 8192, 8192     # the large GEMM's activations, bf16
+
+
+def run_reference_quantize(args):
+    """Reference arm of --workload quantize: the oracle quantiser on one host
+    thread, each step a bounded sample of rows of the same input."""
+    import numpy as np
+
+    import oracle
+    from block_scaled_mxfp4_gb300 import inputs
+    rows, K = QUANT_ROWS, QUANT_K
+    xbits = inputs.f32_to_bf16_bits(
+        np.random.default_rng(5).standard_normal((rows, K), dtype=np.float32))
+    nrows = 64
+    per_elem = 2 + 17 / 32
+    for i in range(args.warmup):
+        oracle.quantize(xbits[i * nrows % rows:][:nrows], nrows, K)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.quantize(xbits[(i * nrows) % rows:][:nrows], nrows, K)
+        times.append(time.perf_counter() - t0)
+    value = args.steps * nrows * K * per_elem / sum(times) / 1e9
+    line = {
+        "impl": "reference", "metric": "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)",
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"quantize rows={rows} K={K}", "rows": rows, "K": K},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: {nrows} rows of the {rows}x{K} input"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_quantize(args, world, rank, local_rank):
+    """--workload quantize: mxfp4_quantize of bf16 [8192, 8192] N(0,1)
+    activations into the GEMM's operand format; bandwidth-bound, reported in
+    GB/s of algorithmic bytes (2 in, 17/32 out per element) against the HBM
+    copy peak, with the CPU oracle on a bounded sample beside it."""
+    import numpy as np
+    import torch
+
+    import block_scaled_mxfp4_gb300 as mx
+    from block_scaled_mxfp4_gb300 import build, inputs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    rows, K = QUANT_ROWS, QUANT_K
+    rng = np.random.default_rng(5)
+    xbits = inputs.f32_to_bf16_bits(rng.standard_normal((rows, K), dtype=np.float32))
+    X = torch.from_numpy(xbits.view(np.int16)).to(dev)
+    Q = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    S = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = rows * K * 2 + rows * K // 2 + rows * K // 32
+
+    def step():
+        mx.mxfp4_quantize(Q, K, S, K // 32, X, K, rows, K, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    tot_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    tot_ms = max_over_ranks([tot_ms], dist, dev)[0]
+    ms = tot_ms / args.steps
+    value = world * nbytes * args.steps / (tot_ms * 1e-3) / 1e9
+    # end to end: host bf16 in, host codes and scales out, copies timed
+    hX = torch.from_numpy(xbits.view(np.int16)).pin_memory()
+    hQ = torch.empty((rows, K // 2), dtype=torch.uint8).pin_memory()
+    hS = torch.empty((rows, K // 32), dtype=torch.uint8).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        X.copy_(hX, non_blocking=True)
+        step()
+        hQ.copy_(Q, non_blocking=True)
+        hS.copy_(S, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / args.e2e_steps], dist, dev)[0]
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        nrows = 256
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            oracle.quantize(xbits[reps * nrows % rows:][:nrows], nrows, K)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * nrows * K * (2 + 17 / 32) / dt / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{reps} x {nrows} rows of the {rows}x{K} input "
+                                           f"({dt:.1f} s, one thread)"}
+    line = {
+        "metric": "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16->mxfp4", "data": "synthetic",
+        "config": {"workload": f"quantize rows={rows} K={K}", "rows": rows, "K": K,
+                   "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("quantize", "quantize_kernel"),
+                     "kernel": "quantize_kernel", "kernel_ms": ms,
+                     "algorithmic_bytes": nbytes, "peak_source": f"{peak_src} HBM copy bandwidth"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": rows * K * 2, "d2h_bytes_per_step": rows * K // 2 + rows * K // 32,
+                "ms_per_step": e2e_ms, "api": "mxfp4_quantize (pinned host copies around it)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -243,6 +394,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.workload == "quantize":
+        run_quantize(args, world, rank, local_rank)
         return
 
     import numpy as np

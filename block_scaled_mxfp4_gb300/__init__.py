@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "Mxfp4Error", "lib", "library_path", "header_functions",
-    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host", "mxfp4_scale_relayout", "mxfp4_scale_relayout2",
+    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host", "mxfp4_scale_relayout", "mxfp4_scale_relayout2", "mxfp4_quantize",
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
             "mxfp4_gemm_host_arena_size": (sz, [i32, i32, i32, i32, i32]),
             "mxfp4_scale_relayout": (i32, [vp, vp, i32, i32, i64, vp]),
             "mxfp4_scale_relayout2": (i32, [vp, vp, i32, i64, vp, vp, i32, i64, i32, vp]),
+            "mxfp4_quantize": (i32, [vp, i64, vp, i64, vp, i64, i32, i32, vp]),
             "mxfp4_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                  f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp4_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
@@ -170,6 +171,11 @@ def mxfp4_scale_relayout2(dst_a, src_a, rows_a, ld_a, dst_b, src_b, rows_b, ld_b
     return _check(lib().mxfp4_scale_relayout2(_p(dst_a), _p(src_a), rows_a, ld_a, _p(dst_b),
                                               _p(src_b), rows_b, ld_b, K, _stream(stream)),
                   "mxfp4_scale_relayout2")
+
+
+def mxfp4_quantize(Q, ldq, S, lds, X, ldx, rows, K, stream=None):
+    return _check(lib().mxfp4_quantize(_p(Q), ldq, _p(S), lds, _p(X), ldx, rows, K,
+                                       _stream(stream)), "mxfp4_quantize")
 
 
 def mxfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,

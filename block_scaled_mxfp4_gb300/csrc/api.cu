@@ -894,6 +894,24 @@ int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream)
                : MXFP4_ERR_CUDA;
 }
 
+int mxfp4_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, int64_t ldx,
+                   int rows, int K, void *stream)
+{
+    if (!Q || !S || !X || rows < 1 || K < 32 || (K % 32) != 0 || ldx < K || ldq < K ||
+        lds < K / 32)
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || (ldx % 8) != 0 || !aligned(Q, 16) || (ldq % 32) != 0)
+        return MXFP4_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    return launch_quantize(static_cast<uint8_t *>(Q), ldq / 2, static_cast<uint8_t *>(S), lds,
+                           static_cast<const uint16_t *>(X), ldx, rows, K, device_sms_or_default(),
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
 int mxfp4_stream_read_probe(const void *src, size_t bytes, void *sink, void *stream)
 {
     if (!src || !sink || bytes < 16)

@@ -149,6 +149,12 @@ cudaError_t launch_wait_probe(long long limit, cudaStream_t stream);
 cudaError_t launch_stream_read(const void *src, size_t bytes, unsigned *sink, int sms,
                                cudaStream_t stream);
 
+// MXFP4 quantiser (quantize.cu): X bf16 [rows, ldx] -> Q [rows, ldq_bytes],
+// S [rows, lds]; K % 32 == 0, X rows and Q rows 16-byte aligned.
+cudaError_t launch_quantize(uint8_t *Q, int64_t ldq_bytes, uint8_t *S, int64_t lds,
+                            const uint16_t *X, int64_t ldx, int rows, int K, int sms,
+                            cudaStream_t stream);
+
 cudaError_t read_device_status(int *status, int reset);
 
 }  // namespace mxfp4

@@ -1,0 +1,128 @@
+// MXFP4 quantiser: bf16 rows [rows, K] -> packed E2M1 codes [rows, K/2] and
+// E8M0 scale codes [rows, K/32] -- the operands mxfp4_gemm takes.
+//
+// Per 1x32 block (the workloads' operand rule; E2M1 values and nibble order
+// from page "asm_f4gemm -- driving aiter's gfx950 MXFP4 GEMM code objects",
+// section "Data layouts"):
+//   s = floor(log2(amax / 6)), the largest integer with 6 * 2^s <= amax
+//       (s = 0 for an all-zero block), clamped to [-127, 127]; scale = s + 127;
+//   code_i = x_i / 2^s rounded to the nearest E2M1 value, ties to even,
+//       saturating at +-6, sign copied from x_i; element 2i in the low nibble.
+//
+// One thread per block: it loads the block's 64 bytes (four 16-byte loads;
+// a warp covers 2 KB of a row contiguously), takes amax with packed bf16
+// max, derives s from amax's exponent and leading significand bits (6 * 2^s
+// <= 1.m * 2^E  <=>  s <= E + 2 - [1.m < 1.5] ... see below), scales by the
+// exact power of two 2^-s, and converts pairs with cvt.rn.satfinite.e2m1x2
+// (round to nearest even, saturating at the largest finite value 6).  The
+// 16 bytes of codes go out in one store (coalesced across the warp), the
+// scale byte beside them.  Bandwidth-bound: 2 bytes in, 17/32 bytes out per
+// element.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mxfp4 {
+
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+// Largest s with 6 * 2^s <= a for a finite a > 0 (float bits): a = f * 2^e
+// with f in [1, 2) (or a subnormal), and 6 * 2^s = 1.5 * 2^(s + 2), so
+// s = e - 2 when f >= 1.5, else e - 3.
+__device__ __forceinline__ int block_exponent(float amax)
+{
+    if (amax == 0.0f)
+        return 0;
+    const uint32_t bits = __float_as_uint(amax);
+    const int biased = static_cast<int>((bits >> 23) & 0xFFu);
+    int s;
+    if (biased == 0) {
+        s = -127;                                   // below 2^-126: clamps
+    } else {
+        const int e = biased - 127;
+        s = (bits & 0x400000u) ? e - 2 : e - 3;     // f >= 1.5 iff the top significand bit is set
+    }
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// Two floats -> one byte of two E2M1 codes: `lo` in bits 0-3, `hi` in 4-7.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_kernel(uint8_t *__restrict__ Q, int64_t ldq_bytes, uint8_t *__restrict__ S,
+                    int64_t lds, const uint16_t *__restrict__ X, int64_t ldx, int rows, int kblocks)
+{
+    const int64_t total = static_cast<int64_t>(rows) * kblocks;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = g / kblocks;
+        const int b = static_cast<int>(g - r * kblocks);
+        const uint4 *src = reinterpret_cast<const uint4 *>(X + r * ldx + b * 32);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldcs(src + i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        // amax over the 32 magnitudes (sign bits cleared, compared as floats)
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        const int s = block_exponent(amax);
+        // 2^-s as a float (s in [-127, 127]: 2^127 is normal, 2^-127 subnormal)
+        const float inv = s == 127 ? __uint_as_float(0x00400000u)
+                                   : __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+        uint32_t out[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t x2 = w[4 * q + j];            // elements 2i (low), 2i+1 (high)
+                word |= e2m1x2(bf16_lo(x2) * inv, bf16_hi(x2) * inv) << (8 * j);
+            }
+            out[q] = word;
+        }
+        *reinterpret_cast<uint4 *>(Q + r * ldq_bytes + b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+        S[r * lds + b] = static_cast<uint8_t>(s + 127);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(uint8_t *Q, int64_t ldq_bytes, uint8_t *S, int64_t lds,
+                            const uint16_t *X, int64_t ldx, int rows, int K, int sms,
+                            cudaStream_t stream)
+{
+    const int kblocks = K / 32;
+    const int64_t total = static_cast<int64_t>(rows) * kblocks;
+    int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    quantize_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
+        Q, ldq_bytes, S, lds, X, ldx, rows, kblocks);
+    return cudaGetLastError();
+}
+
+}  // namespace mxfp4

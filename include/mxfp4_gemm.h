@@ -233,6 +233,26 @@ int mxfp4_device_status(int *status, int reset);
 int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream);
 
 /*
+ * MXFP4 quantiser: bf16 rows -> the operand format mxfp4_gemm takes.
+ *   X  bf16 [rows, ldx]     input, ldx >= K elements, ldx % 8 == 0, 16-byte aligned
+ *   Q  uint8 [rows, ldq/2]  output codes, packed two per byte (element 2i in the
+ *                           low nibble); ldq >= K counted in fp4 elements like
+ *                           lda, ldq % 32 == 0, 16-byte aligned
+ *   S  uint8 [rows, lds]    output E8M0 scale codes, one per 1x32 block, lds >= K/32
+ * Per block: s = floor(log2(amax / 6)) (the largest integer with
+ * 6 * 2^s <= amax; 0 for an all-zero block), clamped to [-127, 127], scale code
+ * s + 127; each element is x / 2^s rounded to the nearest E2M1 value (ties to
+ * even, saturating at +-6) with the sign of x (so small negatives give -0).
+ * This is the quantisation rule the benchmark workloads' operands follow; the
+ * asm_f4gemm page lists operand generation among its reference helpers
+ * (section "Files") without stating it.  Inputs must be finite.  rows >= 1,
+ * K >= 32, K % 32 == 0.  Errors: MXFP4_ERR_INVALID_ARG (null pointer, sizes,
+ * strides), MXFP4_ERR_MISALIGNED, device errors.  Enqueued on `stream`.
+ */
+int mxfp4_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, int64_t ldx,
+                   int rows, int K, void *stream);
+
+/*
  * Measurement hook: reads `bytes` (rounded down to a multiple of 16) of the
  * device buffer `src` (16-byte aligned) once with 16-byte loads from every
  * SM, several in flight per thread -- the time a single streaming pass over

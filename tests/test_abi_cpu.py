@@ -195,6 +195,15 @@ def test_other_entry_points_validate_before_device(L):
     assert L.mxfp4_stream_read_probe(None, 64, 0x1000, None) == -1
     assert L.mxfp4_stream_read_probe(0x1000, 8, 0x2000, None) == -1
     assert L.mxfp4_stream_read_probe(0x1008, 64, 0x2000, None) == -3
+    qz = L.mxfp4_quantize
+    assert qz(None, 64, 0x2000, 2, 0x3000, 64, 4, 64, None) == -1
+    assert qz(0x1000, 64, 0x2000, 2, 0x3000, 64, 4, 48, None) == -1      # K % 32
+    assert qz(0x1000, 32, 0x2000, 2, 0x3000, 64, 4, 64, None) == -1      # ldq < K
+    assert qz(0x1000, 64, 0x2000, 1, 0x3000, 64, 4, 64, None) == -1      # lds < K/32
+    assert qz(0x1000, 64, 0x2000, 2, 0x3000, 64, 0, 64, None) == -1      # rows
+    assert qz(0x1000, 64, 0x2000, 2, 0x3008, 64, 4, 64, None) == -3      # X alignment
+    assert qz(0x1000, 64, 0x2000, 2, 0x3000, 68, 4, 64, None) == -3      # ldx % 8
+    assert qz(0x1000, 80, 0x2000, 2, 0x3000, 64, 4, 64, None) == -3      # ldq % 32
     r2 = L.mxfp4_scale_relayout2
     assert r2(None, 0x2000, 4, 2, 0x3000, 0x4000, 4, 2, 64, None) == -1
     assert r2(0x1000, 0x2000, 4, 2, 0x3000, 0x4000, 0, 2, 64, None) == -1

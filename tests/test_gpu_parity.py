@@ -520,3 +520,84 @@ def test_stream_read_probe_runs():
         mx.mxfp4_stream_read_probe(buf, nbytes, sink)
     torch.cuda.synchronize()
     assert mx.mxfp4_device_status() == 0
+
+
+# ------------------------------------------------------------- quantiser --
+
+def _quantize_gpu(Xbits, rows, K, ldx=None, ldq=None, lds=None):
+    ldx = ldx or K
+    ldq = ldq or K
+    lds = lds or K // 32
+    Xp = np.zeros((rows, ldx), dtype=np.uint16)
+    Xp[:, :K] = Xbits
+    X = torch.from_numpy(Xp.view(np.int16)).cuda()
+    Q = torch.full((rows, ldq // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    S = torch.full((rows, lds), 0x5A, dtype=torch.uint8, device="cuda")
+    mx.mxfp4_quantize(Q, ldq, S, lds, X, ldx, rows, K)
+    torch.cuda.synchronize()
+    return Q.cpu().numpy(), S.cpu().numpy()
+
+
+def _bf16(x):
+    return inputs.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (37, 96), (128, 1024), (5, 4128), (300, 512)])
+def test_quantize_matches_oracle(oracle_mod, rows, K):
+    """Codes and scales bit for bit against the oracle on rows whose
+    magnitudes span 2^-60 .. 2^60."""
+    rng = np.random.default_rng(rows * 1000 + K)
+    x = rng.standard_normal((rows, K)) * np.ldexp(1.0, rng.integers(-60, 60, size=(rows, 1)))
+    bits = _bf16(x)
+    Qw, Sw = oracle_mod.quantize(bits, rows, K)
+    Qg, Sg = _quantize_gpu(bits, rows, K)
+    assert np.array_equal(Sg, Sw)
+    assert np.array_equal(Qg, Qw)
+
+
+def test_quantize_special_blocks(oracle_mod):
+    """All-zero and negative-zero blocks, every rounding tie, saturation at
+    the block maximum, bf16 subnormals and values near the bf16 maximum."""
+    K = 32 * 12
+    x = np.zeros((4, K), dtype=np.float64)
+    x[0, 32:64] = -0.0
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -2.5, -5.0, 6.0])
+    x[0, 64:64 + ties.size] = ties                               # scale 0: ties as they stand
+    x[0, 96:96 + ties.size] = ties * 2.0 ** 20                   # same ties at another scale
+    x[1, :32] = np.linspace(-11.9, 11.9, 32)                     # max in [6, 12): saturates
+    x[1, 32:64] = np.ldexp(1.0, -133) * np.arange(1, 33)         # bf16 subnormals
+    x[1, 64:96] = 3.0e38 * np.linspace(-1, 1, 32)                # near the bf16 maximum
+    x[2] = np.where(np.arange(K) % 2, -1e-30, 1e-30)             # tiny against nothing
+    x[3] = np.random.default_rng(4).standard_normal(K) * 0.01
+    x[3, ::7] = -0.0
+    bits = _bf16(x)
+    Qw, Sw = oracle_mod.quantize(bits, 4, K)
+    Qg, Sg = _quantize_gpu(bits, 4, K)
+    assert np.array_equal(Sg, Sw)
+    assert np.array_equal(Qg, Qw)
+
+
+def test_quantize_strided_leaves_padding(oracle_mod):
+    rows, K = 9, 256
+    x = np.random.default_rng(6).standard_normal((rows, K))
+    bits = _bf16(x)
+    Qw, Sw = oracle_mod.quantize(bits, rows, K)
+    Qg, Sg = _quantize_gpu(bits, rows, K, ldx=K + 24, ldq=K + 64, lds=K // 32 + 5)
+    assert np.array_equal(Qg[:, :K // 2], Qw) and np.array_equal(Sg[:, :K // 32], Sw)
+    assert (Qg[:, K // 2:] == 0xA5).all() and (Sg[:, K // 32:] == 0x5A).all()
+
+
+def test_quantize_then_gemm(oracle_mod):
+    """bf16 activations and weights through the quantiser, then the GEMM:
+    equal to the oracle GEMM on the oracle-quantised operands."""
+    M, N, K = 96, 320, 1024
+    rng = np.random.default_rng(12)
+    xa, xb = _bf16(rng.standard_normal((M, K))), _bf16(rng.standard_normal((N, K)))
+    QA, SA = _quantize_gpu(xa, M, K)
+    QB, SB = _quantize_gpu(xb, N, K)
+    QAo, SAo = oracle_mod.quantize(xa, M, K)
+    QBo, SBo = oracle_mod.quantize(xb, N, K)
+    assert np.array_equal(QA, QAo) and np.array_equal(SB, SBo)
+    p = inputs.Problem("qgemm", M, N, K, QA, QB, SA, SB, None, 1.0, 0.0, 12)
+    Dref, sabs = full_oracle(oracle_mod, p)
+    assert_within_bound(run_gemm(Dev(p)), Dref, sabs, 1.0, "quantised operands")

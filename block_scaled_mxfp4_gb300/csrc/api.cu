@@ -138,9 +138,10 @@ bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K)
 }
 
 // Relaid scale atoms viewed as 3-D uint32 [row blocks][k-groups][128]; a box
-// of 2 x 2 atoms = both 128-row blocks of a 256-row tile for one 256-K stage,
-// in smem order (row block, k-group).
-bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K)
+// of 2 k-groups x box_rb row blocks = the 128-row blocks a pair tile's B rows
+// touch for one 256-K stage, in smem order (row block, k-group); a tile that
+// starts inside a block reads past its last rows (zero fill beyond the end).
+bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K, int box_rb)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
@@ -150,7 +151,7 @@ bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K)
                           static_cast<cuuint64_t>(sf_row_blocks(rows))};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kSfAtomBytes),
                              static_cast<cuuint64_t>(groups * kSfAtomBytes)};
-    cuuint32_t box[3] = {128u, 2u, 2u};
+    cuuint32_t box[3] = {128u, 2u, static_cast<cuuint32_t>(box_rb)};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -373,13 +374,21 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         out->sk_units = 0;
         partials = 0;
     }
+    int pair_n = 256;
     if (use_pair) {
+        // Tile N: 256 (one accumulator) or 192 (two accumulators, so a tile's
+        // MMAs overlap the previous tile's epilogue); MXFP4_PAIR_N overrides.
+        if (const char *env = std::getenv("MXFP4_PAIR_N"))
+            pair_n = std::atoi(env) == 192 ? 192 : 256;
+        const int64_t ptiles = ((static_cast<int64_t>(M) + 255) / 256) *
+                               ((static_cast<int64_t>(N) + pair_n - 1) / pair_n);
+        const int64_t pairs = sms / 2;
         out->tile_m = 256;
-        out->tile_n = 256;
-        out->stages = 6;
-        out->dp_waves = static_cast<int>((tiles256 + sms / 2 - 1) / (sms / 2));
+        out->tile_n = pair_n;
+        out->stages = pair_n == 192 ? 7 : 6;
+        out->dp_waves = static_cast<int>((ptiles + pairs - 1) / pairs);
         out->sk_units = 0;
-        out->ctas = 2 * static_cast<int>(tiles256 < sms / 2 ? tiles256 : sms / 2);
+        out->ctas = 2 * static_cast<int>(ptiles < pairs ? ptiles : pairs);
         out->grid_x = out->ctas;
         partials = 0;
     }
@@ -393,7 +402,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     // CTA-pair kernel reads relaid atoms.)
     out->relayout_pass = (use_pair || (!use_gemv && !persistent && !swap && tiles >= sms)) ? 1 : 0;
     if (shape) {
-        shape->tile_n = c.tile_n;
+        shape->tile_n = use_pair ? pair_n : c.tile_n;
         shape->stages = c.stages;
         shape->swap = swap;
         shape->persistent = out->persistent;
@@ -493,8 +502,10 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         if (sc.rowmajor)
             return MXFP4_ERR_INVALID_ARG;            // the pair kernel reads relaid atoms
         CUtensorMap tmA, tmB, tmSA, tmSB;
-        if (!encode_operand(&tmA, A, M, K, lda, kTileM) || !encode_operand(&tmB, B, N, K, ldb, kTileM) ||
-            !encode_atoms(&tmSA, sc.a, M, K) || !encode_atoms_3d(&tmSB, sc.b, N, K))
+        const int bn = shape.tile_n;
+        if (!encode_operand(&tmA, A, M, K, lda, kTileM) ||
+            !encode_operand(&tmB, B, N, K, ldb, bn / 2) || !encode_atoms(&tmSA, sc.a, M, K) ||
+            !encode_atoms_3d(&tmSB, sc.b, N, K, 2))
             return MXFP4_ERR_CUDA;
         GemmArgs a;
         std::memset(&a, 0, sizeof(a));
@@ -512,8 +523,8 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
                    (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
         a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
         a.wait_limit = g_wait_limit.load();
-        const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
-        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
+        const int tiles_p = (M + 255) / 256, tiles_q = (N + bn - 1) / bn;
+        if (launch_gemm_pair(a, bn, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
                              after_relayout, stream) !=
             cudaSuccess)
             return MXFP4_ERR_CUDA;

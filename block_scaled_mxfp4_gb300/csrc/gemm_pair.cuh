@@ -1,74 +1,100 @@
 // CTA-pair (2-SM) form of the block-scaled MXFP4 GEMM for large shapes
 // (included by gemm_sm103.cu).
 //
-// A cluster of two CTAs computes one 256 x 256 output tile with
+// A cluster of two CTAs computes one 256 x BN output tile with
 // tcgen05.mma.cta_group::2 (M = 256): CTA r of the pair holds rows
-// [128r, 128r+128) of the tile's A panel and rows [128r, 128r+128) of its B
-// panel (half of N) in its own shared memory, and its own 128 rows x 256
+// [128r, 128r+128) of the tile's A panel and rows [r*BN/2, (r+1)*BN/2) of its
+// B panel (half of N) in its own shared memory, and its own 128 rows x BN
 // columns of the fp32 accumulator in its own tensor memory.  Per 256-K stage
-// each CTA therefore stages 16 KB of A and 16 KB of B (plus 3 KB of scale
-// atoms) for 128 x 256 x 256 multiply-adds, against 48 KB for a one-CTA
-// 128 x 256 tile: the ring holds six stages instead of four, which is what
-// keeps the tensor pipe fed across the L2 round trip.
+// each CTA therefore stages 16 KB of A and BN/2 x 128 bytes of B (plus the
+// stage's scale atoms) for 128 x BN x 256 multiply-adds -- against 48 KB for
+// a one-CTA 128 x 256 tile -- so that six or seven stages fit, enough to
+// keep the tensor pipe fed across the TMA round trip.
+//
+// Two shapes are compiled:
+//   BN = 256, one accumulator, 6 stages, one tensor-memory scale slot per
+//       stage;
+//   BN = 192, two accumulators (2 x 192 columns), 7 stages and five scale
+//       slots (the rest of the 512 tensor-memory columns): the MMAs of a tile
+//       run while the epilogue drains the previous one, instead of waiting
+//       for it.  A 192-row B tile starts 0 or 64 rows into a 128-row scale
+//       block, so its scale-B base column is offset by 0 or 2.
 //
 // Roles (448 threads = 14 warps per CTA):
 //   warps 4, 6, 7 (each CTA)  TMA producers: A half, B half, and the scale
-//                      atoms (this CTA's 128 rows of scale-A, all 256 rows of
-//                      scale-B in one 3-D box).  Every copy completes its bytes
-//                      on the LEADER's full barrier (the cta_group::2 form of
-//                      the TMA); only the leader's three producers arrive on
-//                      it, each expecting its copy's bytes for both CTAs.  A
-//                      thread waits out each copy instruction it issues
-//                      (hundreds of cycles), hence three issuing warps.
-//   warps 12, 13 (leader)  scale copiers: once a stage has landed, each issues
-//                      three tcgen05.cp.cta_group::2 (both CTAs' atoms into
-//                      their own tensor memory) and commits them to the
-//                      stage's sf_ready barrier.  Copies issued by a thread
-//                      other than the MMA issuer run alongside the MMAs.
-//   warp 5 (leader)    waits for a stage's operands and scales, issues four
-//                      K=64 M=256 MMAs and commits the stage to BOTH CTAs'
+//                      atoms (this CTA's 128 rows of scale-A; all BN rows of
+//                      scale-B in one 3-D box of 2 K-groups x 2 row blocks).
+//                      Every copy completes its bytes on the LEADER's full
+//                      barrier (the cta_group::2 form of the TMA); only
+//                      the leader's three producers arrive on it, each
+//                      expecting its copy's bytes for both CTAs.  A thread
+//                      waits out each copy instruction it issues (hundreds of
+//                      cycles), hence three issuing warps.
+//   warps 12, 13 (leader)  scale copiers: once a stage has landed (and, with
+//                      fewer scale slots than stages, once the MMAs that last
+//                      read the slot have completed) each issues half of the
+//                      stage's tcgen05.cp.cta_group::2 (both CTAs' atoms into their
+//                      own tensor memory) and commits them to the stage's
+//                      sf_ready barrier.  Copies issued by a thread other than
+//                      the MMA issuer run alongside the MMAs.
+//   warp 5 (leader)    waits for an accumulator buffer to be free, then per
+//                      stage for the operands and scales; issues four K=64
+//                      M=256 N=BN MMAs and commits the stage to BOTH CTAs'
 //                      empty barriers, and each tile to both CTAs'
 //                      accumulator-full barriers.
-//   warps 0-3 / 8-11 (each CTA)  epilogue, columns 0-127 / 128-255: read the
-//                      accumulator (warp w owns TMEM lanes 32(w%4)..+31 =
-//                      tile rows), form alpha*acc + beta*C and round once to
-//                      bf16 in registers, release the accumulator to the
-//                      leader (8 warps x 2 CTAs), then store D -- so the next
-//                      tile's MMAs do not wait for the stores.
+//   warps 0-3 / 8-11 (each CTA)  epilogue, columns [0, BN/2) / [BN/2, BN):
+//                      read the accumulator (warp w owns TMEM lanes
+//                      32(w%4)..+31 = tile rows), form alpha*acc + beta*C and
+//                      round once to bf16 in registers, release the buffer to
+//                      the leader (8 warps x 2 CTAs), then store D -- so the
+//                      next tile's MMAs do not wait for the stores.
 // Persistent over tiles: pair i takes tiles i, i + pairs, ...  Scales are
 // relaid atoms (a 2-D uint32 view for scale-A, 3-D for scale-B: 128 words =
-// one atom).  A scale slot in tensor memory (one per stage) is rewritten only
-// after the stage's full barrier completed again, i.e. after the producers
-// saw the MMAs that read it commit.
+// one atom).  A scale slot in tensor memory is rewritten only after the MMAs
+// that read it completed: with a slot per stage that is implied by the
+// stage's full barrier (the producers waited for the stage's previous MMAs);
+// with S slots the copier waits for the empty barrier of the stage S back.
 #pragma once
 
 namespace mxfp4 {
 
-template <int STAGES>
+template <int STAGES, int BN, int NACC>
 struct PairCfg {
+    static constexpr int B_ROWS = BN / 2;                 // this CTA's rows of the B tile
     static constexpr int A_BYTES = kTileM * 128;          // 128 rows x 128 bytes
-    static constexpr int B_BYTES = kTileM * 128;          // this CTA's half of N
+    static constexpr int B_BYTES = B_ROWS * 128;
+    static constexpr int SFB_RB = 2;                      // 128-row scale blocks a tile can touch
     static constexpr int SFA_BYTES = 2 * kSfAtomBytes;    // 128 rows, 2 k-groups
-    static constexpr int SFB_BYTES = 4 * kSfAtomBytes;    // 256 rows, 2 k-groups
+    static constexpr int SFB_BYTES = SFB_RB * 2 * kSfAtomBytes;
     static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;
     static constexpr int SF_COLS_A = 8;                   // 2 groups x 4 columns
-    static constexpr int SF_COLS_B = 16;                  // 2 groups x 2 blocks x 4 columns
+    static constexpr int SF_COLS_B = 8 * SFB_RB;          // 2 groups x SFB_RB blocks x 4 columns
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    static constexpr int TMEM_USED = 256 + STAGES * SF_COLS;
+    // One scale slot per stage if the accumulators leave room, else as many
+    // as fit in the 512 tensor-memory columns.
+    static constexpr int SF_FIT = (512 - NACC * BN) / SF_COLS;
+    static constexpr int SF_SLOTS = SF_FIT < STAGES ? SF_FIT : STAGES;
+    static constexpr int SF_COPIES = 2 + 2 * SFB_RB;      // tcgen05.cp per stage
+    static constexpr int HALF = BN / 2;                   // columns per epilogue warp
+    static constexpr int TMEM_USED = NACC * BN + SF_SLOTS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static constexpr int THREADS = 448;
     static constexpr int EPI_WARPS = 8;                   // per CTA
+    static_assert(BN == 256 || BN == 192, "tile N");
+    static_assert(SF_SLOTS >= 2, "scale slots");
+    static_assert(NACC == 1 || NACC == 2, "accumulator buffers");
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(HALF % 16 == 0, "epilogue columns");
 };
 
 struct PairSched {
-    int tiles_p, tiles_q;   // 256 x 256 output tiles
+    int tiles_p, tiles_q;   // 256 x BN output tiles
     int kt;                 // K stages per tile
     int group;              // raster: groups of `group` tile rows
 };
@@ -83,7 +109,7 @@ __device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int 
     qt = within / gh;
 }
 
-// One epilogue thread's 128 columns of one accumulator row, rounded: out[j]
+// One epilogue thread's HALF columns of one accumulator row, rounded: out[j]
 // holds columns n0 + 2j and n0 + 2j + 1 as packed bf16.  Stores them to D
 // row m: 32-byte stores when the row segment is whole and aligned, with a
 // short pause after every 64 bytes.  The stores overlap the next tile's main
@@ -91,27 +117,28 @@ __device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int 
 // mbarrier polls of the producer, copier and MMA threads: a burst of 64 KB of
 // stores per CTA delays those polls by thousands of cycles, so the epilogue
 // uses the widest stores and spreads them out.
+template <int HALF>
 __device__ __forceinline__ void pair_store_row(const GemmArgs &a, int m, int n0,
-                                               const uint32_t (&out)[64])
+                                               const uint32_t (&out)[HALF / 2])
 {
     if (m >= a.M || n0 >= a.N)
         return;
     uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
-    if (a.vec32_ok && n0 + 128 <= a.N) {
+    if (a.vec32_ok && n0 + HALF <= a.N) {
 #pragma unroll
-        for (int j = 0; j < 64; j += 8) {
+        for (int j = 0; j < HALF / 2; j += 8) {
             st_global_v8(d + 2 * j, out[j], out[j + 1], out[j + 2], out[j + 3], out[j + 4],
                          out[j + 5], out[j + 6], out[j + 7]);
             if ((j & 15) == 8)
                 __nanosleep(400);
         }
-    } else if (a.vec_ok && n0 + 128 <= a.N) {
+    } else if (a.vec_ok && n0 + HALF <= a.N) {
 #pragma unroll
-        for (int j = 0; j < 64; j += 4)
+        for (int j = 0; j < HALF / 2; j += 4)
             *reinterpret_cast<uint4 *>(d + 2 * j) = make_uint4(out[j], out[j + 1], out[j + 2], out[j + 3]);
     } else {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < HALF / 2; ++j) {
             if (n0 + 2 * j < a.N)
                 d[2 * j] = static_cast<uint16_t>(out[j] & 0xFFFFu);
             if (n0 + 2 * j + 1 < a.N)
@@ -120,19 +147,21 @@ __device__ __forceinline__ void pair_store_row(const GemmArgs &a, int m, int n0,
     }
 }
 
-// alpha * acc (+ beta * C) for 32 columns of row m starting at n, rounded once.
-__device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n, const uint32_t (&r)[32],
-                                                 uint32_t *out16)
+// alpha * acc (+ beta * C) for W (16 or 32) columns of row m starting at n,
+// rounded once; out receives W / 2 packed bf16 pairs.
+template <int W>
+__device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n, const uint32_t (&r)[W],
+                                                 uint32_t *out)
 {
-    float v[32];
+    float v[W];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < W; ++i)
         v[i] = a.alpha * __uint_as_float(r[i]);
     if (a.beta != 0.0f && m < a.M) {
         const uint16_t *c = a.C + static_cast<int64_t>(m) * a.ldc + n;
-        if (a.vec_ok && n + 32 <= a.N) {
+        if (a.vec_ok && n + W <= a.N) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
+            for (int i = 0; i < W; i += 8) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(c + i);
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -143,32 +172,32 @@ __device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < W; ++i)
                 if (n + i < a.N)
                     v[i] = fmaf(a.beta, bf16_bits_to_float(c[i]), v[i]);
         }
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-        out16[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    for (int j = 0; j < W / 2; ++j)
+        out[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 }
 
-template <int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
+template <int STAGES, int BN, int NACC>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
 {
-    using PC = PairCfg<STAGES>;
+    using PC = PairCfg<STAGES, BN, NACC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + PC::RING_BYTES);   // leader's are used
     uint64_t *empty = full + STAGES;
     uint64_t *sf_ready = empty + STAGES;                                    // leader's are used
-    uint64_t *acc_full = sf_ready + STAGES;
-    uint64_t *acc_empty = acc_full + 1;                                      // leader's is used
-    uint64_t *drain = acc_empty + 1;                                         // [3]: MMA, copiers
+    uint64_t *acc_full = sf_ready + STAGES;                                 // [NACC]
+    uint64_t *acc_empty = acc_full + NACC;                                  // [NACC], leader's used
+    uint64_t *drain = acc_empty + NACC;                                     // [3]: MMA, copiers
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -187,8 +216,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 2);      // the leader's two scale copiers
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 2 * PC::EPI_WARPS);
+        for (int i = 0; i < NACC; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 2 * PC::EPI_WARPS);
+        }
         for (int i = 0; i < 3; ++i)
             mbar_init(&drain[i], 1);
         *abort_flag = 0;
@@ -229,8 +260,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
                 int pt, qt;
                 pair_tile_coords(ps, t, pt, qt);
                 const int arow = pt * 256 + static_cast<int>(rank) * kTileM;
-                const int brow = qt * 256 + static_cast<int>(rank) * kTileM;
+                const int brow = qt * BN + static_cast<int>(rank) * PC::B_ROWS;
                 const int sfa_atom = static_cast<int>(static_cast<int64_t>(pt * 2 + rank) * groups);
+                const int sfb_rb = (qt * BN) / kSfRowBlock;
                 for (int kt = 0; kt < ps.kt; ++kt) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_limit,
                                    &g_device_status)) {
@@ -252,7 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
                     } else {
                         uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
                         tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
-                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, 2 * qt, pol);
+                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, sfb_rb, pol);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -271,26 +303,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
         // ------------------------------------------ scale copiers (leader) --
         if (leader && lane == 0) {
             const int which = warp - 12;
-            const uint32_t t_sf = tmem + 256;
+            const uint32_t t_sf = tmem + NACC * BN;
             int stage = 0;
             uint32_t phase = 0;
             for (int i = 0; i < total_stages; ++i) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
                     break;
+                if (PC::SF_SLOTS < STAGES && i >= PC::SF_SLOTS) {
+                    // The slot's previous reader: the MMAs of stage i - SF_SLOTS.
+                    const int j = i - PC::SF_SLOTS;
+                    if (!mbar_wait(&empty[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u,
+                                   abort_flag, a.wait_limit, &g_device_status))
+                        break;
+                }
                 tc_fence_after();
-                const uint32_t sfa_t = t_sf + stage * PC::SF_COLS;
+                const uint32_t sfa_t = t_sf + (i % PC::SF_SLOTS) * PC::SF_COLS;
                 const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
                 const uint32_t sfa_s = smem_addr(smem + stage * PC::STAGE_BYTES + PC::A_BYTES + PC::B_BYTES);
                 const uint32_t sfb_s = sfa_s + PC::SFA_BYTES;
-                // Scale-B atom (k-group g, row block r) -> columns g*8 + r*4.
-                if (which == 0) {
-                    tmem_cp_32x128b_x4_pair(sfa_t, sdesc_sf_block(sfa_s));
-                    tmem_cp_32x128b_x4_pair(sfa_t + 4, sdesc_sf_block(sfa_s + kSfAtomBytes));
-                    tmem_cp_32x128b_x4_pair(sfb_t, sdesc_sf_block(sfb_s));
-                } else {
-                    tmem_cp_32x128b_x4_pair(sfb_t + 4, sdesc_sf_block(sfb_s + 2 * kSfAtomBytes));
-                    tmem_cp_32x128b_x4_pair(sfb_t + 8, sdesc_sf_block(sfb_s + kSfAtomBytes));
-                    tmem_cp_32x128b_x4_pair(sfb_t + 12, sdesc_sf_block(sfb_s + 3 * kSfAtomBytes));
+                // Copy c: c < 2 -> scale-A k-group c; else scale-B atom
+                // (k-group g, row block rb) -> columns g*4*SFB_RB + rb*4.
+#pragma unroll
+                for (int c = 0; c < PC::SF_COPIES; ++c) {
+                    if ((c & 1) != which)
+                        continue;
+                    if (c < 2) {
+                        tmem_cp_32x128b_x4_pair(sfa_t + c * 4, sdesc_sf_block(sfa_s + c * kSfAtomBytes));
+                    } else {
+                        const int g = (c - 2) / PC::SFB_RB;
+                        const int rb = (c - 2) % PC::SFB_RB;
+                        tmem_cp_32x128b_x4_pair(
+                            sfb_t + g * 4 * PC::SFB_RB + rb * 4,
+                            sdesc_sf_block(sfb_s + (rb * 2 + g) * kSfAtomBytes));
+                    }
                 }
                 mma_commit_pair(&sf_ready[stage], 0x1);
                 if (++stage == STAGES) {
@@ -306,18 +351,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
     } else if (warp == 5) {
         // ------------------------------------------------ MMA (leader) --
         if (leader && lane == 0) {
-            const uint32_t idesc = idesc_mxf4(256, 256);
-            const uint32_t t_sf = tmem + 256;
+            const uint32_t idesc = idesc_mxf4(256, BN);
+            const uint32_t t_sf = tmem + NACC * BN;
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t acc_phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;         // bit b: parity of buffer b's next use
+            int i = 0;                      // stages consumed so far (scale slot index)
             bool stop = false;
             for (int t = pair; t < tiles && !stop; t += npairs) {
-                if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, a.wait_limit,
-                               &g_device_status))
+                if (!mbar_wait(&acc_empty[acc], ((acc_phase >> acc) & 1u) ^ 1u, abort_flag,
+                               a.wait_limit, &g_device_status))
                     break;
                 tc_fence_after();
-                for (int kt = 0; kt < ps.kt; ++kt) {
+                int pt, qt;
+                pair_tile_coords(ps, t, pt, qt);
+                const uint32_t q_off = static_cast<uint32_t>(((qt * BN) % kSfRowBlock) / 32);
+                const uint32_t d_tmem = tmem + acc * BN;
+                for (int kt = 0; kt < ps.kt; ++kt, ++i) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit,
                                    &g_device_status) ||
                         !mbar_wait(&sf_ready[stage], phase, abort_flag, a.wait_limit,
@@ -327,16 +378,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
                     }
                     tc_fence_after();
                     uint8_t *st = smem + stage * PC::STAGE_BYTES;
-                    const uint32_t sfa_t = t_sf + stage * PC::SF_COLS;
+                    const uint32_t sfa_t = t_sf + (i % PC::SF_SLOTS) * PC::SF_COLS;
                     const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(st));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + PC::A_BYTES));
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint32_t sf_id = (j & 1) * 2;
-                        mma_mxf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j,
+                        mma_mxf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j,
                                       idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + (j >> 1) * 4,
-                                      sfb_t + (j >> 1) * 8, (kt > 0 || j > 0) ? 1u : 0u);
+                                      sfb_t + (j >> 1) * 4 * PC::SFB_RB + q_off,
+                                      (kt > 0 || j > 0) ? 1u : 0u);
                     }
                     mma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) {
@@ -344,8 +396,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
                         phase ^= 1u;
                     }
                 }
-                mma_commit_pair(acc_full, 0x3);
-                acc_phase ^= 1u;
+                mma_commit_pair(&acc_full[acc], 0x3);
+                acc_phase ^= 1u << acc;
+                acc = acc + 1 == NACC ? 0 : acc + 1;
             }
             if (*abort_flag) {
                 mma_commit_pair(&drain[0], 0x1);
@@ -354,31 +407,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
         }
     } else {
         // ------------------------------------------------------ epilogue --
-        // warps 0-3: columns 0-127, warps 8-11: columns 128-255.
+        // warps 0-3: columns [0, HALF), warps 8-11: columns [HALF, BN).
         const int quarter = warp & 3;
         const int half = warp >> 3;
         const int row = quarter * 32 + lane;
-        const uint32_t lead_acc_empty = map_to_rank(smem_addr(acc_empty), 0);
-        const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * PC::HALF;
+        int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < tiles; t += npairs) {
-            bool ok = mbar_wait(acc_full, acc_phase, abort_flag, a.wait_limit, &g_device_status);
+            bool ok = mbar_wait(&acc_full[acc], (acc_phase >> acc) & 1u, abort_flag, a.wait_limit,
+                                &g_device_status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
-            acc_phase ^= 1u;
+            acc_phase ^= 1u << acc;
             tc_fence_after();
             int pt, qt;
             pair_tile_coords(ps, t, pt, qt);
             const int m = pt * 256 + static_cast<int>(rank) * kTileM + row;
-            const int n0 = qt * 256 + half * 128;
-            uint32_t out[64];
+            const int n0 = qt * BN + half * PC::HALF;
+            const uint32_t t_row = t_lane + acc * BN;
+            uint32_t out[PC::HALF / 2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c + 32 <= PC::HALF; c += 32) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_ld_32x32b_x32(t_row + c, r);
                 tmem_ld_wait();
-                pair_round_chunk(a, m, n0 + c * 32, r, out + c * 16);
+                pair_round_chunk<32>(a, m, n0 + c, r, out + c / 2);
+            }
+            if constexpr (PC::HALF % 32 != 0) {
+                constexpr int c = PC::HALF - 16;
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(t_row + c, r);
+                tmem_ld_wait();
+                pair_round_chunk<16>(a, m, n0 + c, r, out + c / 2);
             }
             // This warp's accumulator cells are read (tcgen05.wait::ld has
             // returned, so no TMEM read is outstanding): release them to the
@@ -389,11 +451,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES>::THR
             __syncwarp();
             if (lane == 0) {
                 if (leader)
-                    mbar_arrive(acc_empty);
+                    mbar_arrive(&acc_empty[acc]);
                 else
-                    mbar_arrive_cluster_relaxed(lead_acc_empty);
+                    mbar_arrive_cluster_relaxed(map_to_rank(smem_addr(&acc_empty[acc]), 0));
             }
-            pair_store_row(a, m, n0, out);
+            pair_store_row<PC::HALF>(a, m, n0, out);
+            acc = acc + 1 == NACC ? 0 : acc + 1;
         }
     }
 

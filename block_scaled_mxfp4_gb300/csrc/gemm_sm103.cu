@@ -762,17 +762,20 @@ cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sch, const CU
     return cudaErrorInvalidConfiguration;
 }
 
-constexpr int kPairStages = 6;
-
-size_t gemm_pair_smem_bytes() { return PairCfg<kPairStages>::SMEM_BYTES; }
-
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
-                             const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
-                             cudaStream_t stream)
+// (tile N, accumulators, stages) of the compiled pair configurations.
+size_t gemm_pair_smem_bytes(int tile_n)
 {
-    using PC = PairCfg<kPairStages>;
-    auto kern = gemm_mxf4_pair<kPairStages>;
+    return tile_n == 192 ? PairCfg<7, 192, 2>::SMEM_BYTES : PairCfg<6, 256, 1>::SMEM_BYTES;
+}
+
+template <int STAGES, int BN, int NACC>
+static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int ctas,
+                                   const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                   const CUtensorMap &tmSA, const CUtensorMap &tmSB,
+                                   bool after_relayout, cudaStream_t stream)
+{
+    using PC = PairCfg<STAGES, BN, NACC>;
+    auto kern = gemm_mxf4_pair<STAGES, BN, NACC>;
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -784,11 +787,6 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
             return e;
         configured[dev] = 1;
     }
-    PairSched ps;
-    ps.tiles_p = tiles_p;
-    ps.tiles_q = tiles_q;
-    ps.kt = a.kt_total;
-    ps.group = tiles_p < 8 ? tiles_p : 8;
     if (!after_relayout) {
         kern<<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
         return cudaGetLastError();
@@ -807,6 +805,23 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a, ps, tmA, tmB, tmSA, tmSB);
+}
+
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int tiles_p, int tiles_q, int ctas,
+                             const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
+                             cudaStream_t stream)
+{
+    PairSched ps;
+    ps.tiles_p = tiles_p;
+    ps.tiles_q = tiles_q;
+    ps.kt = a.kt_total;
+    ps.group = tiles_p < 8 ? tiles_p : 8;
+    if (tile_n == 192)
+        return launch_pair_cfg<7, 192, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256)
+        return launch_pair_cfg<6, 256, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    return cudaErrorInvalidConfiguration;
 }
 
 // Test hook: one wait on an mbarrier nobody arrives at.

@@ -101,11 +101,12 @@ cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sched, const 
                                    const CUtensorMap &tmSQ, const GemmShape &s,
                                    cudaStream_t stream);
 
-// CTA-pair kernel (relaid scales): grid = ctas (even), tiles of 256 x 256.
-size_t gemm_pair_smem_bytes();
-// after_relayout: launched right after this library's scale relayout on the
-// same stream (programmatic dependent launch; only the scale loads wait).
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
+// CTA-pair kernel (relaid scales): grid = ctas (even), tiles of 256 x tile_n
+// (tile_n 256: one accumulator; 224: two).  after_relayout: launched right
+// after this library's scale relayout on the same stream (programmatic
+// dependent launch; only the scale loads wait).
+size_t gemm_pair_smem_bytes(int tile_n);
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int tiles_p, int tiles_q, int ctas,
                              const CUtensorMap &tmA, const CUtensorMap &tmB,
                              const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
                              cudaStream_t stream);

@@ -72,8 +72,8 @@ typedef struct mxfp4_plan {
     int ctas;               /* persistent: CTAs (all resident at once) */
     int dp_waves;           /* persistent: whole tiles per CTA before stream-K */
     long long sk_units;     /* persistent: K stages shared out stream-K */
-    int pair;               /* 1: CTA-pair kernel (256 x 256 tiles over two SMs;
-                               MXFP4_KERNEL override) */
+    int pair;               /* 1: CTA-pair kernel (256 x tile_n tiles over two
+                               SMs, tile_n 256 or 192) */
     int gemv;               /* 1: CUDA-core GEMV kernel for M <= 2 (tile_m = M,
                                tile_n = 4 rows of B per warp, tile_k = 1024) */
 } mxfp4_plan;
@@ -90,7 +90,9 @@ typedef struct mxfp4_plan {
  * each call, overrides the kernel for split_k = 0 (tuning and tests only):
  * "persistent" = persistent stream-K kernel, "pair" = CTA-pair kernel for
  * M, N >= 256 without swap, "gemv" = CUDA-core GEMV kernel for M <= 2 and
- * N >= 4 * SMs.  num_sms = 0
+ * N >= 4 * SMs.  MXFP4_PAIR_N = 192 makes the pair kernel use 256 x 192
+ * tiles with two TMEM accumulators (the next tile's MMAs overlap the
+ * previous tile's drain); the default 256 uses one.  num_sms = 0
  * uses the current device's SM count (or 152 when no device is visible).
  * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
  */

@@ -127,6 +127,18 @@ def test_plan_pair_override(L, monkeypatch):
     assert mx.mxfp4_plan_gemm(128, 8192, 8192, 0, 152).pair == 0
 
 
+def test_plan_pair_tile_n_192(L, monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "pair")
+    monkeypatch.setenv("MXFP4_PAIR_N", "192")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert p.pair == 1 and (p.tile_m, p.tile_n, p.stages) == (256, 192, 7)
+    # 32 x 43 tiles over 76 pairs: 19 tiles per pair at most.
+    assert p.dp_waves == (32 * 43 + 75) // 76 and p.ctas == 152
+    # Any other value keeps 256-column tiles.
+    monkeypatch.setenv("MXFP4_PAIR_N", "224")
+    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).tile_n == 256
+
+
 def test_plan_heuristic_prefers_fewer_waves(L):
     # 8192^2 output: 128x256 tiles need 14 waves on 152 SMs, 128x128 need 27.
     assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 152).tile_n == 256

@@ -346,17 +346,22 @@ def test_bounded_wait_times_out_cleanly():
 
 # ------------------------------------------------------ CTA-pair kernel --
 
-@pytest.fixture
-def force_pair(monkeypatch):
+@pytest.fixture(params=[256, 192], ids=["n256", "n192"])
+def force_pair(monkeypatch, request):
+    """The CTA-pair kernel with 256-wide tiles (one accumulator) and with
+    192-wide tiles (two accumulators, five scale slots; tiles start 0 or 64
+    rows into a 128-row scale block)."""
     monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    yield
+    monkeypatch.setenv("MXFP4_PAIR_N", str(request.param))
+    yield request.param
 
 
 @pytest.mark.parametrize("M,N", [(256, 256), (512, 512)])
 def test_pair_kernel_single_scale_probes(force_pair, M, N):
     """Scale placement through the two-SM MMA: each CTA's scale-A rows and the
     full scale-B must reach the right accumulator rows / columns."""
-    assert mx.mxfp4_plan_gemm(M, N, 512, 0, 0).pair == 1
+    plan = mx.mxfp4_plan_gemm(M, N, 512, 0, 0)
+    assert plan.pair == 1 and plan.tile_n == force_pair
     K = 512
     bad = []
     for which, rows in (("A", [0, 31, 127, 128, 200, M - 1]), ("B", [0, 64, 127, 128, 255, N - 1])):
@@ -381,7 +386,8 @@ def test_pair_kernel_single_scale_probes(force_pair, M, N):
 def test_pair_kernel_parity(force_pair, oracle_mod, M, N, K):
     p = inputs.make_problem("pair", M, N, K, seed=M + N + K, values="codes", alpha=0.5,
                             beta=1.0, c_sigma=1.0)
-    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).pair == 1
+    plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
+    assert plan.pair == 1 and plan.tile_n == force_pair
     Dref, sabs = full_oracle(oracle_mod, p)
     assert_within_bound(run_gemm(Dev(p)), Dref, sabs, p.alpha, f"pair {M}x{N}x{K}")
 

@@ -53,7 +53,8 @@ class Plan(ctypes.Structure):
                 ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t), ("relayout_pass", ctypes.c_int),
                 ("persistent", ctypes.c_int), ("ctas", ctypes.c_int), ("dp_waves", ctypes.c_int),
-                ("sk_units", ctypes.c_longlong), ("pair", ctypes.c_int), ("gemv", ctypes.c_int)]
+                ("sk_units", ctypes.c_longlong), ("pair", ctypes.c_int), ("gemv", ctypes.c_int),
+                ("pair_cluster", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

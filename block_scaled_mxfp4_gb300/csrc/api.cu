@@ -121,7 +121,7 @@ bool encode_scales(CUtensorMap *map, const void *base, int rows, int K, int64_t 
 
 // Relaid scale atoms viewed as 2-D uint32 [atoms, 128] (one 512-byte atom per
 // row); a box of 2 rows = the two atoms of one 256-K stage of a 128-row block.
-bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K)
+bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K, int box_atoms = 2)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
@@ -129,7 +129,7 @@ bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K)
     const int64_t atoms = sf_row_blocks(rows) * sf_groups(K);
     cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(atoms)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kSfAtomBytes)};
-    cuuint32_t box[2] = {128u, 2u};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_atoms)};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -375,23 +375,34 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         partials = 0;
     }
     int pair_n = 256;
+    int pair_cluster = 0;
     if (use_pair) {
         // Tile N: 256 (one accumulator) or 192 (two accumulators, so a tile's
         // MMAs overlap the previous tile's epilogue); MXFP4_PAIR_N overrides.
         if (const char *env = std::getenv("MXFP4_PAIR_N"))
             pair_n = std::atoi(env) == 192 ? 192 : 256;
-        const int64_t ptiles = ((static_cast<int64_t>(M) + 255) / 256) *
-                               ((static_cast<int64_t>(N) + pair_n - 1) / pair_n);
-        const int64_t pairs = sms / 2;
+        // Pairs per cluster: 2 shares the A panel between two pairs on
+        // adjacent tiles (256-column tiles, at least two tile columns);
+        // MXFP4_PAIR_CLUSTER overrides.
+        const int64_t tiles_q = (static_cast<int64_t>(N) + pair_n - 1) / pair_n;
+        pair_cluster = 1;
+        if (const char *env = std::getenv("MXFP4_PAIR_CLUSTER"))
+            pair_cluster = std::atoi(env) == 2 ? 2 : 1;
+        if (pair_n != 256 || tiles_q < 2)
+            pair_cluster = 1;
+        const int64_t groups = ((static_cast<int64_t>(M) + 255) / 256) *
+                               ((tiles_q + pair_cluster - 1) / pair_cluster);
+        const int64_t clusters = sms / (2 * pair_cluster);
         out->tile_m = 256;
         out->tile_n = pair_n;
         out->stages = pair_n == 192 ? 7 : 6;
-        out->dp_waves = static_cast<int>((ptiles + pairs - 1) / pairs);
+        out->dp_waves = static_cast<int>((groups + clusters - 1) / clusters);
         out->sk_units = 0;
-        out->ctas = 2 * static_cast<int>(ptiles < pairs ? ptiles : pairs);
+        out->ctas = 2 * pair_cluster * static_cast<int>(groups < clusters ? groups : clusters);
         out->grid_x = out->ctas;
         partials = 0;
     }
+    out->pair_cluster = pair_cluster;
     // Every workspace starts with the reserved stream-K flag bytes.
     out->workspace_bytes = partials ? kFlagBytes + align_up(partials) : 0;
     // With enough tiles to fill the GPU the GEMM is compute-bound: mxfp4_gemm
@@ -411,6 +422,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         shape->pair = use_pair;
         shape->gemv = use_gemv ? 1 : 0;
         shape->pair_ctas = out->ctas;
+        shape->pair_cluster = pair_cluster;
     }
     return MXFP4_OK;
 }
@@ -503,8 +515,11 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
             return MXFP4_ERR_INVALID_ARG;            // the pair kernel reads relaid atoms
         CUtensorMap tmA, tmB, tmSA, tmSB;
         const int bn = shape.tile_n;
-        if (!encode_operand(&tmA, A, M, K, lda, kTileM) ||
-            !encode_operand(&tmB, B, N, K, ldb, bn / 2) || !encode_atoms(&tmSA, sc.a, M, K) ||
+        const int cp = shape.pair_cluster == 2 ? 2 : 1;
+        // With two pairs per cluster each CTA loads half of its A rows and one
+        // of its two scale-A atoms per stage (multicast to both pairs).
+        if (!encode_operand(&tmA, A, M, K, lda, kTileM / cp) ||
+            !encode_operand(&tmB, B, N, K, ldb, bn / 2) || !encode_atoms(&tmSA, sc.a, M, K, 2 / cp) ||
             !encode_atoms_3d(&tmSB, sc.b, N, K, 2))
             return MXFP4_ERR_CUDA;
         GemmArgs a;
@@ -524,7 +539,7 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
         a.wait_limit = g_wait_limit.load();
         const int tiles_p = (M + 255) / 256, tiles_q = (N + bn - 1) / bn;
-        if (launch_gemm_pair(a, bn, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
+        if (launch_gemm_pair(a, bn, cp, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
                              after_relayout, stream) !=
             cudaSuccess)
             return MXFP4_ERR_CUDA;

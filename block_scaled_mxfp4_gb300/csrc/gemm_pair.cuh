@@ -38,17 +38,28 @@
 //                      sf_ready barrier.  Copies issued by a thread other than
 //                      the MMA issuer run alongside the MMAs.
 //   warp 5 (leader)    waits for an accumulator buffer to be free, then per
-//                      stage for the operands and scales; issues four K=64
+//                      stage for the scales (whose barrier the copiers commit
+//                      only after the stage's operands landed); issues four K=64
 //                      M=256 N=BN MMAs and commits the stage to BOTH CTAs'
 //                      empty barriers, and each tile to both CTAs'
 //                      accumulator-full barriers.
 //   warps 0-3 / 8-11 (each CTA)  epilogue, columns [0, BN/2) / [BN/2, BN):
 //                      read the accumulator (warp w owns TMEM lanes
-//                      32(w%4)..+31 = tile rows), form alpha*acc + beta*C and
-//                      round once to bf16 in registers, release the buffer to
-//                      the leader (8 warps x 2 CTAs), then store D -- so the
-//                      next tile's MMAs do not wait for the stores.
-// Persistent over tiles: pair i takes tiles i, i + pairs, ...  Scales are
+//                      32(w%4)..+31 = tile rows), release the buffer to the
+//                      leader as soon as the reads are done (8 warps x 2
+//                      CTAs), form alpha*acc + beta*C and round once to bf16
+//                      in registers, then store D -- so the next tile's MMAs
+//                      wait for neither the arithmetic nor the stores.
+// Clusters of CP = 1 or 2 pairs.  With CP = 2 the two pairs of a cluster take
+// horizontally adjacent tiles (same 256 rows of A, N columns qt = 2 qq and
+// 2 qq + 1) and share their A panel: CTA r of each pair loads half of the
+// 128 A rows (and one of the two scale-A atoms) that both pairs' CTA r need
+// and multicasts it to both, so each CTA pulls 8 KB of A per stage from L2
+// instead of 16 KB (26.5 KB per stage instead of 35).  A stage's slot is then
+// written by both pairs, so every CTA's empty barrier collects the MMA
+// commits of both pairs.  A second tile past the last column (odd tile
+// count) is computed on zero-filled B and not stored.
+// Persistent over tiles: cluster i takes tile groups i, i + clusters, ...  Scales are
 // relaid atoms (a 2-D uint32 view for scale-A, 3-D for scale-B: 128 words =
 // one atom).  A scale slot in tensor memory is rewritten only after the MMAs
 // that read it completed: with a slot per stage that is implied by the
@@ -58,8 +69,10 @@
 
 namespace mxfp4 {
 
-template <int STAGES, int BN, int NACC>
+template <int STAGES, int BN, int NACC, int CP>
 struct PairCfg {
+    static constexpr int CLUSTER = 2 * CP;                // CTAs per cluster
+    static constexpr int A_LOAD_ROWS = kTileM / CP;       // A rows this CTA loads per stage
     static constexpr int B_ROWS = BN / 2;                 // this CTA's rows of the B tile
     static constexpr int A_BYTES = kTileM * 128;          // 128 rows x 128 bytes
     static constexpr int B_BYTES = B_ROWS * 128;
@@ -87,6 +100,7 @@ struct PairCfg {
     static_assert(BN == 256 || BN == 192, "tile N");
     static_assert(SF_SLOTS >= 2, "scale slots");
     static_assert(NACC == 1 || NACC == 2, "accumulator buffers");
+    static_assert(CP == 1 || CP == 2, "pairs per cluster");
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -99,14 +113,17 @@ struct PairSched {
     int group;              // raster: groups of `group` tile rows
 };
 
-__device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int &pt, int &qt)
+// Tile group t (one tile per pair of the cluster) -> its row of tiles pt and
+// group column qq, over tiles_p x cols groups, rastered in bands of `group`
+// tile rows.
+__device__ __forceinline__ void pair_tile_coords(const PairSched &s, int cols, int t, int &pt, int &qq)
 {
-    const int per_group = s.group * s.tiles_q;
+    const int per_group = s.group * cols;
     const int g = t / per_group;
     const int within = t - g * per_group;
     const int gh = min(s.group, s.tiles_p - g * s.group);
     pt = g * s.group + within % gh;
-    qt = within / gh;
+    qq = within / gh;
 }
 
 // One epilogue thread's HALF columns of one accumulator row, rounded: out[j]
@@ -182,13 +199,13 @@ __device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n
         out[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 }
 
-template <int STAGES, int BN, int NACC>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
+template <int STAGES, int BN, int NACC, int CP>
+__global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
 {
-    using PC = PairCfg<STAGES, BN, NACC>;
+    using PC = PairCfg<STAGES, BN, NACC, CP>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -203,17 +220,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1u;          // rank within the pair
+    const uint32_t pidx = crank >> 1;          // pair within the cluster
+    const uint32_t lead = crank & ~1u;         // cluster rank of this pair's leader
     const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
-    const int tiles = ps.tiles_p * ps.tiles_q;
-    const int my_tiles = pair < tiles ? (tiles - 1 - pair) / npairs + 1 : 0;
+    const int cl = blockIdx.x / PC::CLUSTER;
+    const int ncl = gridDim.x / PC::CLUSTER;
+    const int gcols = (ps.tiles_q + CP - 1) / CP;   // tile groups per row of tiles
+    const int tiles = ps.tiles_p * gcols;           // tile groups
+    const int my_tiles = cl < tiles ? (tiles - 1 - cl) / ncl + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 3);          // the leader's three producers (both CTAs' bytes)
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CP);        // the MMA commit of every pair of the cluster
             mbar_init(&sf_ready[s], 2);      // the leader's two scale copiers
         }
         for (int i = 0; i < NACC; ++i) {
@@ -256,9 +277,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
             uint32_t phase = 0;
             int issued = 0;
             bool stop = false;
-            for (int t = pair; t < tiles && !stop; t += npairs) {
-                int pt, qt;
-                pair_tile_coords(ps, t, pt, qt);
+            // A (and scale-A) go to this CTA's counterpart in every pair.
+            const uint16_t mc_mask = static_cast<uint16_t>(CP == 2 ? (1u << rank) | (4u << rank) : 0u);
+            for (int t = cl; t < tiles && !stop; t += ncl) {
+                int pt, qq;
+                pair_tile_coords(ps, gcols, t, pt, qq);
+                const int qt = qq * CP + static_cast<int>(pidx);
                 const int arow = pt * 256 + static_cast<int>(rank) * kTileM;
                 const int brow = qt * BN + static_cast<int>(rank) * PC::B_ROWS;
                 const int sfa_atom = static_cast<int>(static_cast<int64_t>(pt * 2 + rank) * groups);
@@ -270,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
                         break;
                     }
                     uint8_t *st = smem + stage * PC::STAGE_BYTES;
-                    const uint32_t lbar = map_to_rank(smem_addr(&full[stage]), 0);
+                    const uint32_t lbar = map_to_rank(smem_addr(&full[stage]), lead);
                     // Only the leader arrives (a cluster-scope arrive from the
                     // peer costs ~0.5 us); the peer's copies just complete
                     // their bytes on the leader's barrier, which cannot start
@@ -278,12 +302,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
                     if (leader)
                         mbar_arrive_expect_tx(&full[stage], 2 * bytes);
                     if (role == 0) {
-                        tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
+                        if constexpr (CP == 1)
+                            tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
+                        else
+                            tma_load_2d_pair_mc(st + pidx * (PC::A_BYTES / 2), &tmA, lbar, kt * 128,
+                                                arow + static_cast<int>(pidx) * PC::A_LOAD_ROWS, mc_mask, pol);
                     } else if (role == 1) {
                         tma_load_2d_pair(st + PC::A_BYTES, &tmB, lbar, kt * 128, brow, pol);
                     } else {
                         uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
-                        tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
+                        if constexpr (CP == 1)
+                            tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
+                        else
+                            tma_load_2d_pair_mc(sf + pidx * kSfAtomBytes, &tmSA, lbar, 0,
+                                                sfa_atom + 2 * kt + static_cast<int>(pidx), mc_mask, pol);
                         tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, sfb_rb, pol);
                     }
                     ++issued;
@@ -337,14 +369,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
                             sdesc_sf_block(sfb_s + (rb * 2 + g) * kSfAtomBytes));
                     }
                 }
-                mma_commit_pair(&sf_ready[stage], 0x1);
+                mma_commit_pair(&sf_ready[stage], static_cast<uint16_t>(1u << lead));
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (*abort_flag) {
-                mma_commit_pair(&drain[1 + which], 0x1);
+                mma_commit_pair(&drain[1 + which], static_cast<uint16_t>(1u << lead));
                 mbar_wait_drain(&drain[1 + which], 0, a.wait_limit);
             }
         }
@@ -359,19 +391,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
             uint32_t acc_phase = 0;         // bit b: parity of buffer b's next use
             int i = 0;                      // stages consumed so far (scale slot index)
             bool stop = false;
-            for (int t = pair; t < tiles && !stop; t += npairs) {
+            for (int t = cl; t < tiles && !stop; t += ncl) {
                 if (!mbar_wait(&acc_empty[acc], ((acc_phase >> acc) & 1u) ^ 1u, abort_flag,
                                a.wait_limit, &g_device_status))
                     break;
                 tc_fence_after();
-                int pt, qt;
-                pair_tile_coords(ps, t, pt, qt);
+                int pt, qq;
+                pair_tile_coords(ps, gcols, t, pt, qq);
+                const int qt = qq * CP + static_cast<int>(pidx);
                 const uint32_t q_off = static_cast<uint32_t>(((qt * BN) % kSfRowBlock) / 32);
                 const uint32_t d_tmem = tmem + acc * BN;
                 for (int kt = 0; kt < ps.kt; ++kt, ++i) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit,
-                                   &g_device_status) ||
-                        !mbar_wait(&sf_ready[stage], phase, abort_flag, a.wait_limit,
+                    // sf_ready completes after the copiers observed the
+                    // stage's full barrier (all of its bytes landed), so it
+                    // stands for both: one poll per stage, because every
+                    // mbarrier poll on this thread delays the next MMA issue.
+                    if (!mbar_wait(&sf_ready[stage], phase, abort_flag, a.wait_limit,
                                    &g_device_status)) {
                         stop = true;
                         break;
@@ -390,18 +425,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
                                       sfb_t + (j >> 1) * 4 * PC::SFB_RB + q_off,
                                       (kt > 0 || j > 0) ? 1u : 0u);
                     }
-                    mma_commit_pair(&empty[stage], 0x3);
+                    // Frees the stage in every CTA that loads into this pair's slots.
+                    mma_commit_pair(&empty[stage], static_cast<uint16_t>((1u << PC::CLUSTER) - 1u));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                mma_commit_pair(&acc_full[acc], 0x3);
+                mma_commit_pair(&acc_full[acc], static_cast<uint16_t>(3u << lead));
                 acc_phase ^= 1u << acc;
                 acc = acc + 1 == NACC ? 0 : acc + 1;
             }
             if (*abort_flag) {
-                mma_commit_pair(&drain[0], 0x1);
+                mma_commit_pair(&drain[0], static_cast<uint16_t>(1u << lead));
                 mbar_wait_drain(&drain[0], 0, a.wait_limit);
             }
         }
@@ -414,7 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * PC::HALF;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = pair; t < tiles; t += npairs) {
+        for (int t = cl; t < tiles; t += ncl) {
             bool ok = mbar_wait(&acc_full[acc], (acc_phase >> acc) & 1u, abort_flag, a.wait_limit,
                                 &g_device_status);
             ok = __all_sync(0xffffffffu, ok);
@@ -422,38 +458,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<STAGES, BN, 
                 break;
             acc_phase ^= 1u << acc;
             tc_fence_after();
-            int pt, qt;
-            pair_tile_coords(ps, t, pt, qt);
+            int pt, qq;
+            pair_tile_coords(ps, gcols, t, pt, qq);
+            const int qt = qq * CP + static_cast<int>(pidx);
             const int m = pt * 256 + static_cast<int>(rank) * kTileM + row;
             const int n0 = qt * BN + half * PC::HALF;
             const uint32_t t_row = t_lane + acc * BN;
             uint32_t out[PC::HALF / 2];
+            // Once this warp's accumulator cells are read (tcgen05.wait::ld
+            // has returned, so no TMEM read is outstanding) they are released
+            // to the leader.  No memory fence is needed for that, and a
+            // cluster-scope release arrive costs ~1000 cycles, so the leader's
+            // warps arrive locally and the peer's with a relaxed remote arrive.
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(&acc_empty[acc]);
+                    else
+                        mbar_arrive_cluster_relaxed(map_to_rank(smem_addr(&acc_empty[acc]), lead));
+                }
+            };
+            if constexpr (PC::HALF == 128) {
+                // Columns 0-63 are read and rounded; 64-127 are read, the
+                // accumulator released, and only then rounded: the next
+                // tile's MMAs wait for the reads alone, not the arithmetic.
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(t_row, r0);
+                tmem_ld_32x32b_x32(t_row + 32, r1);
+                tmem_ld_wait(r0, r1);
+                pair_round_chunk<32>(a, m, n0, r0, out);
+                pair_round_chunk<32>(a, m, n0 + 32, r1, out + 16);
+                tmem_ld_32x32b_x32(t_row + 64, r0);
+                tmem_ld_32x32b_x32(t_row + 96, r1);
+                tmem_ld_wait(r0, r1);
+                release();
+                pair_round_chunk<32>(a, m, n0 + 64, r0, out + 32);
+                pair_round_chunk<32>(a, m, n0 + 96, r1, out + 48);
+            } else {
 #pragma unroll
-            for (int c = 0; c + 32 <= PC::HALF; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c, r);
-                tmem_ld_wait();
-                pair_round_chunk<32>(a, m, n0 + c, r, out + c / 2);
-            }
-            if constexpr (PC::HALF % 32 != 0) {
-                constexpr int c = PC::HALF - 16;
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(t_row + c, r);
-                tmem_ld_wait();
-                pair_round_chunk<16>(a, m, n0 + c, r, out + c / 2);
-            }
-            // This warp's accumulator cells are read (tcgen05.wait::ld has
-            // returned, so no TMEM read is outstanding): release them to the
-            // leader.  No memory fence is needed for that, and a cluster-scope
-            // release arrive costs ~1000 cycles, so the leader's warps arrive
-            // locally and the peer's with a relaxed remote arrive.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (leader)
-                    mbar_arrive(&acc_empty[acc]);
-                else
-                    mbar_arrive_cluster_relaxed(map_to_rank(smem_addr(&acc_empty[acc]), 0));
+                for (int c = 0; c + 32 <= PC::HALF; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c, r);
+                    tmem_ld_wait(r);
+                    pair_round_chunk<32>(a, m, n0 + c, r, out + c / 2);
+                }
+                if constexpr (PC::HALF % 32 != 0) {
+                    constexpr int c = PC::HALF - 16;
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(t_row + c, r);
+                    tmem_ld_wait();
+                    pair_round_chunk<16>(a, m, n0 + c, r, out + c / 2);
+                }
+                release();
             }
             pair_store_row<PC::HALF>(a, m, n0, out);
             acc = acc + 1 == NACC ? 0 : acc + 1;

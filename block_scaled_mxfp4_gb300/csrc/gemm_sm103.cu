@@ -765,50 +765,69 @@ cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sch, const CU
 // (tile N, accumulators, stages) of the compiled pair configurations.
 size_t gemm_pair_smem_bytes(int tile_n)
 {
-    return tile_n == 192 ? PairCfg<7, 192, 2>::SMEM_BYTES : PairCfg<6, 256, 1>::SMEM_BYTES;
+    return tile_n == 192 ? PairCfg<7, 192, 2, 1>::SMEM_BYTES : PairCfg<6, 256, 1, 1>::SMEM_BYTES;
 }
 
-template <int STAGES, int BN, int NACC>
+template <int STAGES, int BN, int NACC, int CP>
 static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int ctas,
                                    const CUtensorMap &tmA, const CUtensorMap &tmB,
                                    const CUtensorMap &tmSA, const CUtensorMap &tmSB,
                                    bool after_relayout, cudaStream_t stream)
 {
-    using PC = PairCfg<STAGES, BN, NACC>;
-    auto kern = gemm_mxf4_pair<STAGES, BN, NACC>;
-    static int configured[64] = {0};
+    using PC = PairCfg<STAGES, BN, NACC, CP>;
+    auto kern = gemm_mxf4_pair<STAGES, BN, NACC, CP>;
+    static int max_clusters[64] = {0};      // per device; 0 = not yet queried
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
-    if (!after_relayout) {
-        kern<<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(a, ps, tmA, tmB, tmSA, tmSB);
-        return cudaGetLastError();
-    }
-    // Right after this library's scale relayout: programmatic stream
-    // serialisation lets the GEMM's prologue and operand loads overlap the
-    // relayout; only the scale producers wait for it (griddepcontrol.wait).
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(PC::THREADS);
     cfg.dynamicSmemBytes = PC::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PC::CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    int limit = dev < 64 ? max_clusters[dev] : 0;
+    if (limit == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        // The kernel is persistent: every cluster must be resident at once.
+        // Clusters of four fit fewer times than the SM count suggests when a
+        // GPC's SM count is not a multiple of four.
+        cfg.gridDim = dim3(PC::CLUSTER);
+        e = cudaOccupancyMaxActiveClusters(&limit, kern, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        if (limit <= 0)
+            return cudaErrorInvalidConfiguration;
+        if (dev < 64)
+            max_clusters[dev] = limit;
+    }
+    int clusters = ctas / PC::CLUSTER;
+    clusters = clusters < limit ? clusters : limit;
+    if (clusters <= 0)
+        return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * PC::CLUSTER));
+    if (after_relayout) {
+        // Right after this library's scale relayout: programmatic stream
+        // serialisation lets the GEMM's prologue and operand loads overlap
+        // the relayout; only the scale producers wait for it
+        // (griddepcontrol.wait).
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kern, a, ps, tmA, tmB, tmSA, tmSB);
 }
 
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int tiles_p, int tiles_q, int ctas,
-                             const CUtensorMap &tmA, const CUtensorMap &tmB,
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, int tiles_p, int tiles_q,
+                             int ctas, const CUtensorMap &tmA, const CUtensorMap &tmB,
                              const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
                              cudaStream_t stream)
 {
@@ -817,10 +836,12 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int tiles_p, int til
     ps.tiles_q = tiles_q;
     ps.kt = a.kt_total;
     ps.group = tiles_p < 8 ? tiles_p : 8;
-    if (tile_n == 192)
-        return launch_pair_cfg<7, 192, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256)
-        return launch_pair_cfg<6, 256, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 192 && cluster_pairs == 1)
+        return launch_pair_cfg<7, 192, 2, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256 && cluster_pairs == 1)
+        return launch_pair_cfg<6, 256, 1, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256 && cluster_pairs == 2)
+        return launch_pair_cfg<6, 256, 1, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
     return cudaErrorInvalidConfiguration;
 }
 

@@ -76,6 +76,11 @@ typedef struct mxfp4_plan {
                                SMs, tile_n 256 or 192) */
     int gemv;               /* 1: CUDA-core GEMV kernel for M <= 2 (tile_m = M,
                                tile_n = 4 rows of B per warp, tile_k = 1024) */
+    int pair_cluster;       /* pair kernel: pairs per thread-block cluster (1, or
+                               2 = two pairs on adjacent tiles share their A
+                               panel by TMA multicast); ctas is then an upper
+                               bound: the launch uses at most as many clusters
+                               as the GPU can hold at once */
 } mxfp4_plan;
 
 /*

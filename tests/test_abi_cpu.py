@@ -139,6 +139,24 @@ def test_plan_pair_tile_n_192(L, monkeypatch):
     assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).tile_n == 256
 
 
+def test_plan_pair_cluster(L, monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "pair")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert p.pair_cluster == 1
+    monkeypatch.setenv("MXFP4_PAIR_CLUSTER", "2")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    # 32 x 16 tile groups (two adjacent 256-column tiles each) over 38 clusters.
+    assert p.pair_cluster == 2 and p.ctas == 152 and p.dp_waves == (512 + 37) // 38
+    # One tile column: nothing to share.
+    assert mx.mxfp4_plan_gemm(1024, 256, 1024, 0, 152).pair_cluster == 1
+    # Only 256-column tiles are compiled in clusters of two pairs.
+    monkeypatch.setenv("MXFP4_PAIR_N", "192")
+    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).pair_cluster == 1
+    # Other kernels report no cluster.
+    monkeypatch.setenv("MXFP4_KERNEL", "persistent")
+    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).pair_cluster == 0
+
+
 def test_plan_heuristic_prefers_fewer_waves(L):
     # 8192^2 output: 128x256 tiles need 14 waves on 152 SMs, 128x128 need 27.
     assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 152).tile_n == 256

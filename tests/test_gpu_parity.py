@@ -346,14 +346,18 @@ def test_bounded_wait_times_out_cleanly():
 
 # ------------------------------------------------------ CTA-pair kernel --
 
-@pytest.fixture(params=[256, 192], ids=["n256", "n192"])
+@pytest.fixture(params=[(256, 1), (192, 1), (256, 2)], ids=["n256", "n192", "n256c2"])
 def force_pair(monkeypatch, request):
-    """The CTA-pair kernel with 256-wide tiles (one accumulator) and with
+    """The CTA-pair kernel with 256-wide tiles (one accumulator), with
     192-wide tiles (two accumulators, five scale slots; tiles start 0 or 64
-    rows into a 128-row scale block)."""
+    rows into a 128-row scale block), and with 256-wide tiles in clusters of
+    two pairs that share A by TMA multicast (an odd tile-column count leaves
+    the second pair of the last column group a tile past the edge)."""
+    tile_n, cluster = request.param
     monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    monkeypatch.setenv("MXFP4_PAIR_N", str(request.param))
-    yield request.param
+    monkeypatch.setenv("MXFP4_PAIR_N", str(tile_n))
+    monkeypatch.setenv("MXFP4_PAIR_CLUSTER", str(cluster))
+    yield tile_n
 
 
 @pytest.mark.parametrize("M,N", [(256, 256), (512, 512)])
@@ -390,6 +394,23 @@ def test_pair_kernel_parity(force_pair, oracle_mod, M, N, K):
     assert plan.pair == 1 and plan.tile_n == force_pair
     Dref, sabs = full_oracle(oracle_mod, p)
     assert_within_bound(run_gemm(Dev(p)), Dref, sabs, p.alpha, f"pair {M}x{N}x{K}")
+
+
+def test_pair_kernel_many_tiles_sampled(force_pair, oracle_mod):
+    """More tile groups than resident clusters (several tiles per pair, the
+    accumulator reused), ragged in M and N, checked on sampled outputs."""
+    M, N, K = 4400, 4700, 1024
+    p = inputs.make_problem("pair_many", M, N, K, seed=17, values="codes", alpha=1.0, beta=0.5,
+                            c_sigma=1.0)
+    plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
+    assert plan.pair == 1 and plan.tile_n == force_pair
+    pairs = sample_pairs(M, N, 3000, 5, tile_m=256, tile_n=force_pair)
+    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
+                                                   alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    D = run_gemm(Dev(p))
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, f"pair {M}x{N}x{K}")
+    assert not np.isnan(bf16_bits_to_f64(D)).any()
 
 
 # ---------------------------------------------- persistent stream-K kernel --

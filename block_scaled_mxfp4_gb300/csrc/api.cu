@@ -138,10 +138,11 @@ bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K, int box_a
 }
 
 // Relaid scale atoms viewed as 3-D uint32 [row blocks][k-groups][128]; a box
-// of 2 k-groups x box_rb row blocks = the 128-row blocks a pair tile's B rows
-// touch for one 256-K stage, in smem order (row block, k-group); a tile that
-// starts inside a block reads past its last rows (zero fill beyond the end).
-bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K, int box_rb)
+// of box_groups k-groups (2 per 256 K of a stage) x box_rb row blocks = the
+// 128-row blocks a pair tile's B rows touch for one stage, in smem order (row
+// block, k-group); a tile that starts inside a block reads past its last rows
+// (zero fill beyond the end).
+bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K, int box_rb, int box_groups = 2)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
@@ -151,7 +152,7 @@ bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K, int bo
                           static_cast<cuuint64_t>(sf_row_blocks(rows))};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kSfAtomBytes),
                              static_cast<cuuint64_t>(groups * kSfAtomBytes)};
-    cuuint32_t box[3] = {128u, 2u, static_cast<cuuint32_t>(box_rb)};
+    cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_groups), static_cast<cuuint32_t>(box_rb)};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -376,6 +377,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     }
     int pair_n = 256;
     int pair_cluster = 0;
+    int pair_kc = 0;
     if (use_pair) {
         // Tile N: 256 (one accumulator) or 192 (two accumulators, so a tile's
         // MMAs overlap the previous tile's epilogue); MXFP4_PAIR_N overrides.
@@ -390,12 +392,21 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
             pair_cluster = std::atoi(env) == 2 ? 2 : 1;
         if (pair_n != 256 || tiles_q < 2)
             pair_cluster = 1;
+        // K per pipeline stage: 256 (six stages) or 512 (three stages of
+        // twice the size: half the barrier round trips per MMA);
+        // MXFP4_PAIR_KS overrides.  256-column tiles only.
+        pair_kc = 1;
+        if (const char *env = std::getenv("MXFP4_PAIR_KS"))
+            pair_kc = std::atoi(env) == 512 ? 2 : 1;
+        if (pair_n != 256)
+            pair_kc = 1;
         const int64_t groups = ((static_cast<int64_t>(M) + 255) / 256) *
                                ((tiles_q + pair_cluster - 1) / pair_cluster);
         const int64_t clusters = sms / (2 * pair_cluster);
         out->tile_m = 256;
         out->tile_n = pair_n;
-        out->stages = pair_n == 192 ? 7 : 6;
+        out->tile_k = 256 * pair_kc;
+        out->stages = pair_n == 192 ? 7 : (pair_kc == 2 ? 3 : 6);
         out->dp_waves = static_cast<int>((groups + clusters - 1) / clusters);
         out->sk_units = 0;
         out->ctas = 2 * pair_cluster * static_cast<int>(groups < clusters ? groups : clusters);
@@ -423,6 +434,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         shape->gemv = use_gemv ? 1 : 0;
         shape->pair_ctas = out->ctas;
         shape->pair_cluster = pair_cluster;
+        shape->pair_kc = pair_kc;
     }
     return MXFP4_OK;
 }
@@ -516,11 +528,13 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         CUtensorMap tmA, tmB, tmSA, tmSB;
         const int bn = shape.tile_n;
         const int cp = shape.pair_cluster == 2 ? 2 : 1;
-        // With two pairs per cluster each CTA loads half of its A rows and one
-        // of its two scale-A atoms per stage (multicast to both pairs).
+        const int kc = shape.pair_kc == 2 ? 2 : 1;
+        // With two pairs per cluster each CTA loads half of its A rows and
+        // half of its scale-A atoms per stage (multicast to both pairs).
         if (!encode_operand(&tmA, A, M, K, lda, kTileM / cp) ||
-            !encode_operand(&tmB, B, N, K, ldb, bn / 2) || !encode_atoms(&tmSA, sc.a, M, K, 2 / cp) ||
-            !encode_atoms_3d(&tmSB, sc.b, N, K, 2))
+            !encode_operand(&tmB, B, N, K, ldb, bn / 2) ||
+            !encode_atoms(&tmSA, sc.a, M, K, 2 * kc / cp) ||
+            !encode_atoms_3d(&tmSB, sc.b, N, K, 2, 2 * kc))
             return MXFP4_ERR_CUDA;
         GemmArgs a;
         std::memset(&a, 0, sizeof(a));
@@ -539,7 +553,7 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
         a.wait_limit = g_wait_limit.load();
         const int tiles_p = (M + 255) / 256, tiles_q = (N + bn - 1) / bn;
-        if (launch_gemm_pair(a, bn, cp, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
+        if (launch_gemm_pair(a, bn, cp, kc, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
                              after_relayout, stream) !=
             cudaSuccess)
             return MXFP4_ERR_CUDA;

@@ -69,29 +69,32 @@
 
 namespace mxfp4 {
 
-template <int STAGES, int BN, int NACC, int CP>
+template <int STAGES, int BN, int NACC, int CP, int KC>
 struct PairCfg {
     static constexpr int CLUSTER = 2 * CP;                // CTAs per cluster
-    static constexpr int A_LOAD_ROWS = kTileM / CP;       // A rows this CTA loads per stage
+    static constexpr int A_LOAD_ROWS = kTileM / CP;       // A rows this CTA loads per chunk
     static constexpr int B_ROWS = BN / 2;                 // this CTA's rows of the B tile
-    static constexpr int A_BYTES = kTileM * 128;          // 128 rows x 128 bytes
-    static constexpr int B_BYTES = B_ROWS * 128;
+    static constexpr int GROUPS = 2 * KC;                 // scale k-groups (128 K) per stage
+    static constexpr int A_CHUNK = kTileM * 128;          // 128 rows x 128 bytes (256 K)
+    static constexpr int B_CHUNK = B_ROWS * 128;
+    static constexpr int A_BYTES = KC * A_CHUNK;
+    static constexpr int B_BYTES = KC * B_CHUNK;
     static constexpr int SFB_RB = 2;                      // 128-row scale blocks a tile can touch
-    static constexpr int SFA_BYTES = 2 * kSfAtomBytes;    // 128 rows, 2 k-groups
-    static constexpr int SFB_BYTES = SFB_RB * 2 * kSfAtomBytes;
+    static constexpr int SFA_BYTES = GROUPS * kSfAtomBytes;           // 128 rows
+    static constexpr int SFB_BYTES = SFB_RB * GROUPS * kSfAtomBytes;
     static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;
-    static constexpr int SF_COLS_A = 8;                   // 2 groups x 4 columns
-    static constexpr int SF_COLS_B = 8 * SFB_RB;          // 2 groups x SFB_RB blocks x 4 columns
+    static constexpr int SF_COLS_A = 4 * GROUPS;          // 4 columns per k-group
+    static constexpr int SF_COLS_B = 4 * GROUPS * SFB_RB; // and per 128-row block
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
     // One scale slot per stage if the accumulators leave room, else as many
     // as fit in the 512 tensor-memory columns.
     static constexpr int SF_FIT = (512 - NACC * BN) / SF_COLS;
     static constexpr int SF_SLOTS = SF_FIT < STAGES ? SF_FIT : STAGES;
-    static constexpr int SF_COPIES = 2 + 2 * SFB_RB;      // tcgen05.cp per stage
+    static constexpr int SF_COPIES = GROUPS + GROUPS * SFB_RB;   // tcgen05.cp per stage
     static constexpr int HALF = BN / 2;                   // columns per epilogue warp
     static constexpr int TMEM_USED = NACC * BN + SF_SLOTS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
@@ -101,6 +104,7 @@ struct PairCfg {
     static_assert(SF_SLOTS >= 2, "scale slots");
     static_assert(NACC == 1 || NACC == 2, "accumulator buffers");
     static_assert(CP == 1 || CP == 2, "pairs per cluster");
+    static_assert(KC == 1 || KC == 2, "256-K chunks per stage");
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -110,6 +114,7 @@ struct PairCfg {
 struct PairSched {
     int tiles_p, tiles_q;   // 256 x BN output tiles
     int kt;                 // K stages per tile
+    int kchunks;            // 256-K chunks per tile (the last stage may hold fewer than KC)
     int group;              // raster: groups of `group` tile rows
 };
 
@@ -133,7 +138,9 @@ __device__ __forceinline__ void pair_tile_coords(const PairSched &s, int cols, i
 // loop, and global stores share the memory-instruction queue with the
 // mbarrier polls of the producer, copier and MMA threads: a burst of 64 KB of
 // stores per CTA delays those polls by thousands of cycles, so the epilogue
-// uses the widest stores and spreads them out.
+// uses the widest stores and spreads them out.  D goes to L2 as evict-first:
+// written once and not read back, it should not push out the A and B panels
+// that later tiles load again (the operands are loaded as evict-last).
 template <int HALF>
 __device__ __forceinline__ void pair_store_row(const GemmArgs &a, int m, int n0,
                                                const uint32_t (&out)[HALF / 2])
@@ -142,10 +149,11 @@ __device__ __forceinline__ void pair_store_row(const GemmArgs &a, int m, int n0,
         return;
     uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
     if (a.vec32_ok && n0 + HALF <= a.N) {
+        const uint64_t pol = l2_policy_evict_first();
 #pragma unroll
         for (int j = 0; j < HALF / 2; j += 8) {
-            st_global_v8(d + 2 * j, out[j], out[j + 1], out[j + 2], out[j + 3], out[j + 4],
-                         out[j + 5], out[j + 6], out[j + 7]);
+            st_global_v8_hint(d + 2 * j, out[j], out[j + 1], out[j + 2], out[j + 3], out[j + 4],
+                              out[j + 5], out[j + 6], out[j + 7], pol);
             if ((j & 15) == 8)
                 __nanosleep(400);
         }
@@ -199,13 +207,13 @@ __device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n
         out[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 }
 
-template <int STAGES, int BN, int NACC, int CP>
-__global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP>::THREADS, 1)
+template <int STAGES, int BN, int NACC, int CP, int KC>
+__global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
 {
-    using PC = PairCfg<STAGES, BN, NACC, CP>;
+    using PC = PairCfg<STAGES, BN, NACC, CP, KC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -272,7 +280,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP>::THREADS, 1)
             // serialisation), only the relaid scales depend on it.
             if (role == 2)
                 pdl_wait_prerequisites();
-            const uint32_t bytes = role == 0 ? PC::A_BYTES : role == 1 ? PC::B_BYTES : PC::SF_BYTES;
+            // Bytes per 256-K chunk (A, B) or per stage (scales: the boxes
+            // always have the full stage's shape; past K they read atoms no
+            // MMA uses, or zero fill).
+            const uint32_t unit = role == 0 ? PC::A_CHUNK : role == 1 ? PC::B_CHUNK : PC::SF_BYTES;
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
@@ -299,24 +310,32 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP>::THREADS, 1)
                     // peer costs ~0.5 us); the peer's copies just complete
                     // their bytes on the leader's barrier, which cannot start
                     // this stage's next phase before the MMAs freed the stage.
+                    const int c0 = kt * KC;                        // first 256-K chunk
+                    const int nc = min(KC, ps.kchunks - c0);       // chunks inside K
                     if (leader)
-                        mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+                        mbar_arrive_expect_tx(&full[stage], 2 * (role == 2 ? unit : nc * unit));
                     if (role == 0) {
-                        if constexpr (CP == 1)
-                            tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
-                        else
-                            tma_load_2d_pair_mc(st + pidx * (PC::A_BYTES / 2), &tmA, lbar, kt * 128,
-                                                arow + static_cast<int>(pidx) * PC::A_LOAD_ROWS, mc_mask, pol);
+                        for (int c = 0; c < nc; ++c) {
+                            if constexpr (CP == 1)
+                                tma_load_2d_pair(st + c * PC::A_CHUNK, &tmA, lbar, (c0 + c) * 128, arow, pol);
+                            else
+                                tma_load_2d_pair_mc(st + c * PC::A_CHUNK + pidx * (PC::A_CHUNK / 2), &tmA,
+                                                    lbar, (c0 + c) * 128,
+                                                    arow + static_cast<int>(pidx) * PC::A_LOAD_ROWS, mc_mask,
+                                                    pol);
+                        }
                     } else if (role == 1) {
-                        tma_load_2d_pair(st + PC::A_BYTES, &tmB, lbar, kt * 128, brow, pol);
+                        for (int c = 0; c < nc; ++c)
+                            tma_load_2d_pair(st + PC::A_BYTES + c * PC::B_CHUNK, &tmB, lbar, (c0 + c) * 128,
+                                             brow, pol);
                     } else {
                         uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
                         if constexpr (CP == 1)
-                            tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
+                            tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * c0, pol);
                         else
-                            tma_load_2d_pair_mc(sf + pidx * kSfAtomBytes, &tmSA, lbar, 0,
-                                                sfa_atom + 2 * kt + static_cast<int>(pidx), mc_mask, pol);
-                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, sfb_rb, pol);
+                            tma_load_2d_pair_mc(sf + pidx * (PC::SFA_BYTES / 2), &tmSA, lbar, 0,
+                                                sfa_atom + 2 * c0 + static_cast<int>(pidx) * KC, mc_mask, pol);
+                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * c0, sfb_rb, pol);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -353,20 +372,21 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP>::THREADS, 1)
                 const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
                 const uint32_t sfa_s = smem_addr(smem + stage * PC::STAGE_BYTES + PC::A_BYTES + PC::B_BYTES);
                 const uint32_t sfb_s = sfa_s + PC::SFA_BYTES;
-                // Copy c: c < 2 -> scale-A k-group c; else scale-B atom
-                // (k-group g, row block rb) -> columns g*4*SFB_RB + rb*4.
+                // Copy c: c < GROUPS -> scale-A k-group c; else scale-B atom
+                // (k-group g, row block rb; in shared memory at rb*GROUPS + g)
+                // -> columns g*4*SFB_RB + rb*4.
 #pragma unroll
                 for (int c = 0; c < PC::SF_COPIES; ++c) {
                     if ((c & 1) != which)
                         continue;
-                    if (c < 2) {
+                    if (c < PC::GROUPS) {
                         tmem_cp_32x128b_x4_pair(sfa_t + c * 4, sdesc_sf_block(sfa_s + c * kSfAtomBytes));
                     } else {
-                        const int g = (c - 2) / PC::SFB_RB;
-                        const int rb = (c - 2) % PC::SFB_RB;
+                        const int g = (c - PC::GROUPS) / PC::SFB_RB;
+                        const int rb = (c - PC::GROUPS) % PC::SFB_RB;
                         tmem_cp_32x128b_x4_pair(
                             sfb_t + g * 4 * PC::SFB_RB + rb * 4,
-                            sdesc_sf_block(sfb_s + (rb * 2 + g) * kSfAtomBytes));
+                            sdesc_sf_block(sfb_s + (rb * PC::GROUPS + g) * kSfAtomBytes));
                     }
                 }
                 mma_commit_pair(&sf_ready[stage], static_cast<uint16_t>(1u << lead));
@@ -417,13 +437,23 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP>::THREADS, 1)
                     const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(st));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + PC::A_BYTES));
+                    // Four K=64 MMAs per 256-K chunk; the last stage of a
+                    // tile may hold fewer than KC chunks.
+                    const int nc = min(KC, ps.kchunks - kt * KC);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t sf_id = (j & 1) * 2;
-                        mma_mxf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j,
-                                      idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + (j >> 1) * 4,
-                                      sfb_t + (j >> 1) * 4 * PC::SFB_RB + q_off,
-                                      (kt > 0 || j > 0) ? 1u : 0u);
+                    for (int c = 0; c < KC; ++c) {
+                        if (c >= nc)
+                            break;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t sf_id = (j & 1) * 2;
+                            const int g = 2 * c + (j >> 1);          // scale k-group
+                            mma_mxf4_pair(d_tmem, adesc + c * (PC::A_CHUNK >> 4) + 2 * j,
+                                          bdesc + c * (PC::B_CHUNK >> 4) + 2 * j,
+                                          idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
+                                          sfb_t + g * 4 * PC::SFB_RB + q_off,
+                                          (kt > 0 || c > 0 || j > 0) ? 1u : 0u);
+                        }
                     }
                     // Frees the stage in every CTA that loads into this pair's slots.
                     mma_commit_pair(&empty[stage], static_cast<uint16_t>((1u << PC::CLUSTER) - 1u));

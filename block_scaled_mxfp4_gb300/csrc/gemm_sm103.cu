@@ -763,19 +763,21 @@ cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sch, const CU
 }
 
 // (tile N, accumulators, stages) of the compiled pair configurations.
-size_t gemm_pair_smem_bytes(int tile_n)
+size_t gemm_pair_smem_bytes(int tile_n, int k_chunks)
 {
-    return tile_n == 192 ? PairCfg<7, 192, 2, 1>::SMEM_BYTES : PairCfg<6, 256, 1, 1>::SMEM_BYTES;
+    if (tile_n == 192)
+        return PairCfg<7, 192, 2, 1, 1>::SMEM_BYTES;
+    return k_chunks == 2 ? PairCfg<3, 256, 1, 1, 2>::SMEM_BYTES : PairCfg<6, 256, 1, 1, 1>::SMEM_BYTES;
 }
 
-template <int STAGES, int BN, int NACC, int CP>
+template <int STAGES, int BN, int NACC, int CP, int KC>
 static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int ctas,
                                    const CUtensorMap &tmA, const CUtensorMap &tmB,
                                    const CUtensorMap &tmSA, const CUtensorMap &tmSB,
                                    bool after_relayout, cudaStream_t stream)
 {
-    using PC = PairCfg<STAGES, BN, NACC, CP>;
-    auto kern = gemm_mxf4_pair<STAGES, BN, NACC, CP>;
+    using PC = PairCfg<STAGES, BN, NACC, CP, KC>;
+    auto kern = gemm_mxf4_pair<STAGES, BN, NACC, CP, KC>;
     static int max_clusters[64] = {0};      // per device; 0 = not yet queried
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -823,11 +825,13 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, kern, a, ps, tmA, tmB, tmSA, tmSB);
+    PairSched sched = ps;
+    sched.kt = (ps.kchunks + KC - 1) / KC;
+    return cudaLaunchKernelEx(&cfg, kern, a, sched, tmA, tmB, tmSA, tmSB);
 }
 
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, int tiles_p, int tiles_q,
-                             int ctas, const CUtensorMap &tmA, const CUtensorMap &tmB,
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, int k_chunks, int tiles_p,
+                             int tiles_q, int ctas, const CUtensorMap &tmA, const CUtensorMap &tmB,
                              const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
                              cudaStream_t stream)
 {
@@ -835,13 +839,18 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, i
     ps.tiles_p = tiles_p;
     ps.tiles_q = tiles_q;
     ps.kt = a.kt_total;
+    ps.kchunks = a.kt_total;
     ps.group = tiles_p < 8 ? tiles_p : 8;
-    if (tile_n == 192 && cluster_pairs == 1)
-        return launch_pair_cfg<7, 192, 2, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256 && cluster_pairs == 1)
-        return launch_pair_cfg<6, 256, 1, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256 && cluster_pairs == 2)
-        return launch_pair_cfg<6, 256, 1, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 192 && cluster_pairs == 1 && k_chunks == 1)
+        return launch_pair_cfg<7, 192, 2, 1, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256 && cluster_pairs == 1 && k_chunks == 1)
+        return launch_pair_cfg<6, 256, 1, 1, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256 && cluster_pairs == 2 && k_chunks == 1)
+        return launch_pair_cfg<6, 256, 1, 2, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256 && cluster_pairs == 1 && k_chunks == 2)
+        return launch_pair_cfg<3, 256, 1, 1, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
+    if (tile_n == 256 && cluster_pairs == 2 && k_chunks == 2)
+        return launch_pair_cfg<3, 256, 1, 2, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
     return cudaErrorInvalidConfiguration;
 }
 

@@ -61,6 +61,7 @@ struct GemmShape {
     int pair;               // 1: CTA-pair kernel (256 x 256 tiles, cta_group::2)
     int pair_ctas;          // pair kernel: grid size (upper bound; 2 x pairs)
     int pair_cluster;       // pair kernel: pairs per cluster (1 or 2)
+    int pair_kc;            // pair kernel: 256-K chunks per pipeline stage (1 or 2)
     int gemv;               // 1: GEMV kernel for M <= 2 (gemv.cu)
 };
 
@@ -104,13 +105,13 @@ cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sched, const 
 
 // CTA-pair kernel (relaid scales): grid of up to `ctas` CTAs in clusters of
 // cluster_pairs pairs (clamped to the clusters the GPU holds at once), tiles
-// of 256 x tile_n (256: one accumulator, 1 or 2 pairs per cluster; 192: two
-// accumulators, 1 pair).  after_relayout: launched right after this
+// of 256 x tile_n (256: one accumulator, 1 or 2 pairs per cluster, stages
+// of 256 or 512 K; 192: two accumulators, 1 pair, 256-K stages).  after_relayout: launched right after this
 // library's scale relayout on the same stream (programmatic dependent launch;
 // only the scale loads wait).
-size_t gemm_pair_smem_bytes(int tile_n);
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, int tiles_p, int tiles_q,
-                             int ctas, const CUtensorMap &tmA, const CUtensorMap &tmB,
+size_t gemm_pair_smem_bytes(int tile_n, int k_chunks);
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, int k_chunks, int tiles_p,
+                             int tiles_q, int ctas, const CUtensorMap &tmA, const CUtensorMap &tmB,
                              const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
                              cudaStream_t stream);
 

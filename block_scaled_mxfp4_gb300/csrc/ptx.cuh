@@ -309,6 +309,18 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32], uint32_t (&q)[32
                  : "memory");
 }
 
+// 32-byte global store (8 x 32-bit) under an L2 eviction policy, not
+// allocated in L1; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8_hint(void *p, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                                  uint32_t a7, uint64_t policy)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                 ::"l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7),
+                 "l"(policy)
+                 : "memory");
+}
+
 // 32-byte global store (8 x 32-bit); the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,

@@ -95,9 +95,13 @@ typedef struct mxfp4_plan {
  * each call, overrides the kernel for split_k = 0 (tuning and tests only):
  * "persistent" = persistent stream-K kernel, "pair" = CTA-pair kernel for
  * M, N >= 256 without swap, "gemv" = CUDA-core GEMV kernel for M <= 2 and
- * N >= 4 * SMs.  MXFP4_PAIR_N = 192 makes the pair kernel use 256 x 192
- * tiles with two TMEM accumulators (the next tile's MMAs overlap the
- * previous tile's drain); the default 256 uses one.  num_sms = 0
+ * N >= 4 * SMs.  Pair-kernel variants, also read at each call (all tested
+ * for parity; the defaults measured fastest on GB300): MXFP4_PAIR_N = 192
+ * uses 256 x 192 tiles with two TMEM accumulators (the next tile's MMAs
+ * overlap the previous tile's drain; default 256, one accumulator);
+ * MXFP4_PAIR_CLUSTER = 2 puts two pairs on adjacent tiles in one cluster that
+ * share their A panel by TMA multicast (default 1); MXFP4_PAIR_KS = 512 uses
+ * three 512-K pipeline stages instead of six 256-K ones.  num_sms = 0
  * uses the current device's SM count (or 152 when no device is visible).
  * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
  */

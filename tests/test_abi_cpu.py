@@ -157,6 +157,19 @@ def test_plan_pair_cluster(L, monkeypatch):
     assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).pair_cluster == 0
 
 
+def test_plan_pair_stage_k(L, monkeypatch):
+    monkeypatch.setenv("MXFP4_KERNEL", "pair")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert (p.tile_k, p.stages) == (256, 6)
+    monkeypatch.setenv("MXFP4_PAIR_KS", "512")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert (p.tile_k, p.stages) == (512, 3)
+    # 192-column tiles keep 256-K stages.
+    monkeypatch.setenv("MXFP4_PAIR_N", "192")
+    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert (p.tile_k, p.stages) == (256, 7)
+
+
 def test_plan_heuristic_prefers_fewer_waves(L):
     # 8192^2 output: 128x256 tiles need 14 waves on 152 SMs, 128x128 need 27.
     assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 152).tile_n == 256

@@ -346,17 +346,21 @@ def test_bounded_wait_times_out_cleanly():
 
 # ------------------------------------------------------ CTA-pair kernel --
 
-@pytest.fixture(params=[(256, 1), (192, 1), (256, 2)], ids=["n256", "n192", "n256c2"])
+@pytest.fixture(params=[(256, 1, 256), (192, 1, 256), (256, 2, 256), (256, 1, 512), (256, 2, 512)],
+                ids=["n256", "n192", "n256c2", "n256k512", "n256c2k512"])
 def force_pair(monkeypatch, request):
     """The CTA-pair kernel with 256-wide tiles (one accumulator), with
     192-wide tiles (two accumulators, five scale slots; tiles start 0 or 64
-    rows into a 128-row scale block), and with 256-wide tiles in clusters of
-    two pairs that share A by TMA multicast (an odd tile-column count leaves
-    the second pair of the last column group a tile past the edge)."""
-    tile_n, cluster = request.param
+    rows into a 128-row scale block), with 256-wide tiles in clusters of two
+    pairs that share A by TMA multicast (an odd tile-column count leaves the
+    second pair of the last column group a tile past the edge), and with
+    512-K pipeline stages (an odd number of 256-K chunks leaves the last
+    stage half full)."""
+    tile_n, cluster, ks = request.param
     monkeypatch.setenv("MXFP4_KERNEL", "pair")
     monkeypatch.setenv("MXFP4_PAIR_N", str(tile_n))
     monkeypatch.setenv("MXFP4_PAIR_CLUSTER", str(cluster))
+    monkeypatch.setenv("MXFP4_PAIR_KS", str(ks))
     yield tile_n
 
 
@@ -386,7 +390,7 @@ def test_pair_kernel_single_scale_probes(force_pair, M, N):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 520, 1024), (1000, 700, 288),
-                                   (512, 1024, 2048)])
+                                   (512, 1024, 2048), (520, 768, 1280)])
 def test_pair_kernel_parity(force_pair, oracle_mod, M, N, K):
     p = inputs.make_problem("pair", M, N, K, seed=M + N + K, values="codes", alpha=0.5,
                             beta=1.0, c_sigma=1.0)

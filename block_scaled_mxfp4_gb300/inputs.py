@@ -22,6 +22,14 @@ large, skinny-M wide-K), plus an identity case.  Values follow each recipe:
     sign(x).
 Draw order within a workload: A, then B, then C, each drawn row-chunk by
 row-chunk in C order from one numpy PCG64 generator seeded per workload.
+
+MXFP8 problems (page "CDNA4 dense MFMA builtins": FP8 = E4M3, BF8 = E5M2,
+scaled per block like FP4) hold one 8-bit code per element, A [M, K] and
+B [N, K], with the same E8M0 scales [rows, K/32].  Their values are
+x ~ N(0,1) (or U[-1,1]) with the OCP MX scale rule per 1x32 block,
+s = floor(log2(max|x|)) - emax (emax 8 for E4M3, 15 for E5M2; s = 0 for an
+all-zero block), and x / 2^s cast to the format by torch's float8 conversion
+(nearest, ties to even) after clamping to the largest finite value.
 """
 from __future__ import annotations
 
@@ -192,3 +200,89 @@ def identity_problem(M: int = 128, N: int = 256, K: int = 512, seed: int = 0) ->
     B = pack_fp4(bcodes)
     SB = np.full((N, K // 32), 127, dtype=np.uint8)
     return Problem("identity", M, N, K, A, B, SA, SB, None, 1.0, 0.0, seed)
+
+
+# ---------------------------------------------------------------- MXFP8 --
+
+# format name -> (oracle format code, largest element exponent, largest finite)
+FP8_FORMATS = {"e4m3": (1, 8, 448.0), "e5m2": (2, 15, 57344.0)}
+
+
+@dataclasses.dataclass
+class Problem8:
+    """One MXFP8 GEMM instance: A [M, K] and B [N, K] 8-bit element codes."""
+
+    name: str
+    M: int
+    N: int
+    K: int
+    fmt_a: str               # "e4m3" or "e5m2"
+    fmt_b: str
+    A: np.ndarray            # uint8 [M, K]
+    B: np.ndarray            # uint8 [N, K]
+    SA: np.ndarray           # uint8 [M, K/32] E8M0
+    SB: np.ndarray           # uint8 [N, K/32] E8M0
+    C: Optional[np.ndarray]  # uint16 [M, N] bf16 bits, or None
+    alpha: float
+    beta: float
+    seed: int
+
+
+def quantize_rows_fp8(x: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
+    """Quantise float64 rows [rows, K] (K % 32 == 0) to (8-bit codes, E8M0)."""
+    import torch
+    rows, K = x.shape
+    assert K % 32 == 0
+    _, emax, top = FP8_FORMATS[fmt]
+    amax = np.abs(x).reshape(rows, K // 32, 32).max(axis=2)
+    _, e = np.frexp(amax)                 # amax = f * 2^e, f in [0.5, 1)
+    s = (e - 1 - emax).astype(np.int64)   # floor(log2(amax)) - emax
+    s[amax == 0] = 0
+    s = np.clip(s, -127, 127)
+    y = np.ldexp(x.reshape(rows, K // 32, 32), -s[:, :, None]).reshape(rows, K)
+    y = np.clip(y, -top, top)
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    codes = torch.from_numpy(np.ascontiguousarray(y)).to(dt).view(torch.uint8).numpy()
+    return codes.astype(np.uint8), (s + 127).astype(np.uint8)
+
+
+def _quantized_operand8(rng: np.random.Generator, rows: int, K: int, dist: str, fmt: str):
+    codes = np.empty((rows, K), dtype=np.uint8)
+    scales = np.empty((rows, K // 32), dtype=np.uint8)
+    for r0 in range(0, rows, _ROW_CHUNK):
+        r1 = min(rows, r0 + _ROW_CHUNK)
+        if dist == "normal":
+            x = rng.standard_normal((r1 - r0, K))
+        elif dist == "uniform":
+            x = rng.uniform(-1.0, 1.0, size=(r1 - r0, K))
+        else:
+            raise ValueError(dist)
+        codes[r0:r1], scales[r0:r1] = quantize_rows_fp8(x, fmt)
+    return codes, scales
+
+
+def make_problem8(name: str, M: int, N: int, K: int, seed: int, fmt_a: str, fmt_b: str,
+                  values: str, alpha: float, beta: float, c_sigma: Optional[float]) -> Problem8:
+    """Draw one MXFP8 problem (A in fmt_a, B in fmt_b)."""
+    if K % 32 != 0:
+        raise ValueError("K must be a multiple of 32 (one E8M0 scale per 32)")
+    if fmt_a not in FP8_FORMATS or fmt_b not in FP8_FORMATS:
+        raise ValueError("formats are 'e4m3' or 'e5m2'")
+    rng = np.random.default_rng(seed)
+    A, SA = _quantized_operand8(rng, M, K, values, fmt_a)
+    B, SB = _quantized_operand8(rng, N, K, values, fmt_b)
+    C = _bf16_normal(rng, M, N, c_sigma) if c_sigma is not None else None
+    return Problem8(name, M, N, K, fmt_a, fmt_b, A, B, SA, SB, C, float(alpha), float(beta), seed)
+
+
+# name -> (M, N, K, seed, fmt A, fmt B, value recipe, alpha, beta, C sigma or None)
+WORKLOADS8 = {
+    "large8":  (8192, 8192, 8192, 5, "e4m3", "e4m3", "normal", 1.0, 0.0, None),
+    "decode8": (1, 8192, 8192, 6, "e4m3", "e4m3", "normal", 1.0, 0.0, None),
+    "mixed8":  (512, 1024, 2048, 7, "e4m3", "e5m2", "normal", 0.5, 0.5, 1.0),
+}
+
+
+def workload8(name: str) -> Problem8:
+    M, N, K, seed, fa, fb, values, alpha, beta, c_sigma = WORKLOADS8[name]
+    return make_problem8(name, M, N, K, seed, fa, fb, values, alpha, beta, c_sigma)

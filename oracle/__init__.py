@@ -78,6 +78,19 @@ def bind(path: str) -> ctypes.CDLL:
                                       ctypes.c_double, ctypes.c_double, u16p, i64,
                                       ctypes.POINTER(ctypes.c_int64), i64,
                                       u16p, dp, dp, ctypes.c_int]
+    L.oracle_fp8_value.restype = ctypes.c_double
+    L.oracle_fp8_value.argtypes = [ctypes.c_uint, ctypes.c_int]
+    L.oracle_gemm8.restype = i64
+    L.oracle_gemm8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               u8p, i64, u8p, i64, u8p, i64, u8p, i64,
+                               ctypes.c_double, ctypes.c_double, u16p, i64,
+                               u16p, i64, dp, dp, ctypes.c_int]
+    L.oracle_gemm8_sampled.restype = i64
+    L.oracle_gemm8_sampled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, u8p, i64, u8p, i64, u8p, i64, u8p, i64,
+                                       ctypes.c_double, ctypes.c_double, u16p, i64,
+                                       ctypes.POINTER(ctypes.c_int64), i64,
+                                       u16p, dp, dp, ctypes.c_int]
     L.oracle_quantize.restype = ctypes.c_int
     L.oracle_quantize.argtypes = [ctypes.c_int, ctypes.c_int, u16p, i64, u8p, i64, u8p, i64]
     return L
@@ -103,6 +116,15 @@ def e2m1_value(code: int) -> float:
 
 def e8m0_value(code: int) -> float:
     return lib().oracle_e8m0_value(code)
+
+
+# MXFP8 element formats (the codes the oracle's fmt arguments take).
+E4M3, E5M2 = 1, 2
+
+
+def fp8_value(code: int, fmt: int) -> float:
+    """Value of an 8-bit E4M3 (fmt 1) or E5M2 (fmt 2) element code."""
+    return lib().oracle_fp8_value(int(code), int(fmt))
 
 
 def fp4_code(packed_row: np.ndarray, k: int) -> int:
@@ -174,6 +196,63 @@ def gemm_sampled(A, B, SA, SB, M, N, K, pairs, alpha=1.0, beta=0.0, C=None,
                                   _ptr(sabs, ctypes.c_double), int(nthreads))
     if r < 0:
         raise ValueError("oracle_gemm_sampled rejected its arguments")
+    return D, acc, sabs, int(r)
+
+
+def _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b):
+    if fmt_a not in (E4M3, E5M2) or fmt_b not in (E4M3, E5M2):
+        raise ValueError("fmt_a / fmt_b must be E4M3 (1) or E5M2 (2)")
+    for name, arr, rows, cols in (("A", A, M, K), ("B", B, N, K),
+                                  ("SA", SA, M, K // 32), ("SB", SB, N, K // 32)):
+        if arr.dtype != np.uint8 or arr.ndim != 2 or arr.shape[0] < rows or arr.shape[1] < cols:
+            raise ValueError(f"{name}: bad shape {arr.shape} / dtype {arr.dtype}")
+
+
+def gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha=1.0, beta=0.0, C=None, want_acc=False,
+          nthreads=0):
+    """Full MXFP8 oracle GEMM (A [M, K], B [N, K] element codes, one per byte).
+    Returns (D bf16 bits [M,N], acc or None, sum|ab| [M,N], inexact)."""
+    A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
+    _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b)
+    Cc = None if beta == 0.0 or C is None else np.ascontiguousarray(C, dtype=np.uint16)
+    D = np.zeros((M, N), dtype=np.uint16)
+    acc = np.zeros((M, N), dtype=np.float64) if want_acc else None
+    sabs = np.zeros((M, N), dtype=np.float64)
+    r = lib().oracle_gemm8(M, N, K, int(fmt_a), int(fmt_b), _ptr(A, ctypes.c_uint8), A.shape[1],
+                           _ptr(B, ctypes.c_uint8), B.shape[1],
+                           _ptr(SA, ctypes.c_uint8), SA.shape[1],
+                           _ptr(SB, ctypes.c_uint8), SB.shape[1],
+                           float(alpha), float(beta), _ptr(Cc, ctypes.c_uint16),
+                           0 if Cc is None else Cc.shape[1],
+                           _ptr(D, ctypes.c_uint16), N, _ptr(acc, ctypes.c_double),
+                           _ptr(sabs, ctypes.c_double), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_gemm8 rejected its arguments")
+    return D, acc, sabs, int(r)
+
+
+def gemm8_sampled(A, B, SA, SB, M, N, K, fmt_a, fmt_b, pairs, alpha=1.0, beta=0.0, C=None,
+                  nthreads=0):
+    """MXFP8 oracle at (m, n) pairs [P, 2]. Returns (D bits [P], acc [P], sum|ab| [P], inexact)."""
+    A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
+    _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    Cc = None if beta == 0.0 or C is None else np.ascontiguousarray(C, dtype=np.uint16)
+    P = pairs.shape[0]
+    D = np.zeros(P, dtype=np.uint16)
+    acc = np.zeros(P, dtype=np.float64)
+    sabs = np.zeros(P, dtype=np.float64)
+    r = lib().oracle_gemm8_sampled(M, N, K, int(fmt_a), int(fmt_b), _ptr(A, ctypes.c_uint8),
+                                   A.shape[1], _ptr(B, ctypes.c_uint8), B.shape[1],
+                                   _ptr(SA, ctypes.c_uint8), SA.shape[1],
+                                   _ptr(SB, ctypes.c_uint8), SB.shape[1],
+                                   float(alpha), float(beta), _ptr(Cc, ctypes.c_uint16),
+                                   0 if Cc is None else Cc.shape[1],
+                                   pairs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), P,
+                                   _ptr(D, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
+                                   _ptr(sabs, ctypes.c_double), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_gemm8_sampled rejected its arguments")
     return D, acc, sabs, int(r)
 
 

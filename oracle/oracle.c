@@ -1,5 +1,5 @@
 /*
- * Plain CPU oracle for the block-scaled MXFP4 GEMM.
+ * Plain CPU oracle for the block-scaled MXFP4 GEMM (and its MXFP8 form).
  *
  *     D[M,N] (bf16) = alpha * A[M,K] (mxfp4) * B[N,K]^T (mxfp4) + beta * C[M,N]
  *
@@ -33,11 +33,18 @@
  * every output and checks with an exact product/sum test that step 5 did not
  * round; outputs that fail either check are counted and reported.
  *
+ * MXFP8 form (oracle_gemm8): the same steps with one 8-bit E4M3 or E5M2
+ * element per byte (oracle_fp8_value_q gives the encodings read from the
+ * MFMA page).  A product's granule is 2^(qa + qb + ea + eb - 254), where
+ * qa, qb are the elements' ulp exponents, and the same 2^52 bound applies.
+ *
  * Readings where the pages are silent or at odds:
  *   - E8M0 code 0: the page writes both 2^(e-127) and "0 -> 2^-126"; the
  *     formula is taken (code 0 -> 2^-127).  Code 255 decodes to NaN.
  *   - D is rounded to nearest, ties to even (the MFMA page's rounding mode).
  *   - C is bf16.  C is not read when beta == 0 (it may be NULL).
+ *   - FP8 / BF8 biases and special codes: the OCP 8-bit formats (the page
+ *     gives the field widths only); see oracle_fp8_value_q.
  */
 #define _GNU_SOURCE
 #include <math.h>
@@ -65,6 +72,47 @@ double oracle_e8m0_value(unsigned code)
     if (code == 0xFFu)
         return NAN;
     return ldexp(1.0, (int)code - 127);
+}
+
+/*
+ * MXFP8 elements (page "CDNA4 dense MFMA builtins", section "FP8 and BF8
+ * matrix inputs": FP8 is E4M3 = 1 sign, 4 exponent, 3 mantissa bits; BF8 is
+ * E5M2 = 1, 5, 2; section "Mixed-precision with scaling": the scaled
+ * builtins take either with one scale per block).  The pages give the field
+ * widths only; the encodings read here are the OCP 8-bit formats those
+ * builtins use: E4M3 with bias 7, no infinities and NaN at S.1111.111
+ * (largest 448); E5M2 with bias 15, infinities at S.11111.00 and NaN at
+ * S.11111.{01,10,11} (largest 57344).  Exponent field 0 is subnormal:
+ * (m / 2^mbits) * 2^(1 - bias).
+ *
+ * fmt: 1 = E4M3, 2 = E5M2.  *ulp_exp (optional) receives q such that the value
+ * is an integer multiple of 2^q (the spacing of its binade).
+ */
+double oracle_fp8_value_q(unsigned code, int fmt, int *ulp_exp)
+{
+    const int ebits = fmt == 1 ? 4 : 5, mbits = fmt == 1 ? 3 : 2, bias = fmt == 1 ? 7 : 15;
+    const unsigned s = (code >> 7) & 1u;
+    const unsigned e = (code >> mbits) & ((1u << ebits) - 1u);
+    const unsigned m = code & ((1u << mbits) - 1u);
+    const unsigned emax = (1u << ebits) - 1u;
+    double v;
+    if (fmt == 1 && e == emax && m == (1u << mbits) - 1u)
+        v = NAN;
+    else if (fmt == 2 && e == emax)
+        v = m == 0 ? INFINITY : NAN;
+    else {
+        const int ee = e == 0 ? 1 : (int)e;
+        const double frac = (e == 0 ? 0.0 : 1.0) + ldexp((double)m, -mbits);
+        v = ldexp(frac, ee - bias);
+    }
+    if (ulp_exp)
+        *ulp_exp = (e == 0 ? 1 : (int)e) - bias - mbits;
+    return s ? -v : v;
+}
+
+double oracle_fp8_value(unsigned code, int fmt)
+{
+    return oracle_fp8_value_q(code, fmt, NULL);
 }
 
 /* Step 1: element k of a packed row. */
@@ -138,6 +186,7 @@ static int two_sum_exact(double a, double b, double s)
 
 struct gemm_job {
     int M, N, K;
+    int fmt_a, fmt_b;  /* 0: E2M1 packed two per byte; 1: E4M3, 2: E5M2 bytes */
     const uint8_t *A; int64_t lda_bytes;
     const uint8_t *B; int64_t ldb_bytes;
     const uint8_t *SA; int64_t ldsa;
@@ -162,17 +211,27 @@ static int one_output(struct gemm_job *j, int m, int n, uint16_t *d,
     const uint8_t *sarow = j->SA + (int64_t)m * j->ldsa;
     const uint8_t *sbrow = j->SB + (int64_t)n * j->ldsb;
     double acc = 0.0, sabs = 0.0;
-    int min_g = 1 << 30;               /* min over products of ea+eb-256 */
+    int min_g = 1 << 30;               /* min over products of their granule exponent */
     for (int64_t k = 0; k < j->K; ++k) {
-        unsigned ca = nibble(arow, k), cb = nibble(brow, k);
+        /* E2M1 values are multiples of 2^-1; FP8 values of 2^(ulp exponent). */
+        int qa = -1, qb = -1;
+        double va, vb;
+        if (j->fmt_a == 0)
+            va = oracle_e2m1_value(nibble(arow, k));
+        else
+            va = oracle_fp8_value_q(arow[k], j->fmt_a, &qa);
+        if (j->fmt_b == 0)
+            vb = oracle_e2m1_value(nibble(brow, k));
+        else
+            vb = oracle_fp8_value_q(brow[k], j->fmt_b, &qb);
         unsigned ea = sarow[k / 32], eb = sbrow[k / 32];
-        double a = oracle_e2m1_value(ca) * oracle_e8m0_value(ea);
-        double b = oracle_e2m1_value(cb) * oracle_e8m0_value(eb);
+        double a = va * oracle_e8m0_value(ea);
+        double b = vb * oracle_e8m0_value(eb);
         double p = a * b;
         acc += p;
         sabs += fabs(p);
         if (p != 0.0) {
-            int g = (int)ea + (int)eb - 256;
+            int g = qa + qb + (int)ea + (int)eb - 254;
             if (g < min_g)
                 min_g = g;
         }
@@ -320,6 +379,64 @@ int64_t oracle_gemm_sampled(int M, int N, int K,
     memset(&j, 0, sizeof(j));
     j.M = M; j.N = N; j.K = K;
     j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;
+    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
+    j.D = D; j.ldd = 0; j.acc_out = acc_out; j.abs_out = abs_out;
+    j.pairs = pairs; j.npairs = npairs;
+    return run(&j, nthreads);
+}
+
+/*
+ * MXFP8 forms of oracle_gemm / oracle_gemm_sampled: A and B hold one 8-bit
+ * element per byte (lda, ldb in elements = bytes), fmt_a / fmt_b = 1 (E4M3)
+ * or 2 (E5M2), one E8M0 scale per 32 K as before.  Same steps 2-6, with the
+ * element decoded by oracle_fp8_value_q.
+ */
+static int fp8_args_ok(int M, int N, int K, int fmt_a, int fmt_b, double beta, const uint16_t *C)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 32 != 0)
+        return 0;
+    if ((fmt_a != 1 && fmt_a != 2) || (fmt_b != 1 && fmt_b != 2))
+        return 0;
+    return !(beta != 0.0 && C == NULL);
+}
+
+int64_t oracle_gemm8(int M, int N, int K, int fmt_a, int fmt_b,
+                     const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                     const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                     double alpha, double beta, const uint16_t *C, int64_t ldc,
+                     uint16_t *D, int64_t ldd, double *acc_out, double *abs_out,
+                     int nthreads)
+{
+    if (!fp8_args_ok(M, N, K, fmt_a, fmt_b, beta, C))
+        return -1;
+    struct gemm_job j;
+    memset(&j, 0, sizeof(j));
+    j.M = M; j.N = N; j.K = K; j.fmt_a = fmt_a; j.fmt_b = fmt_b;
+    j.A = A; j.lda_bytes = lda; j.B = B; j.ldb_bytes = ldb;
+    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
+    j.D = D; j.ldd = ldd; j.acc_out = acc_out; j.abs_out = abs_out;
+    return run(&j, nthreads);
+}
+
+int64_t oracle_gemm8_sampled(int M, int N, int K, int fmt_a, int fmt_b,
+                             const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                             const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                             double alpha, double beta, const uint16_t *C, int64_t ldc,
+                             const int64_t *pairs, int64_t npairs,
+                             uint16_t *D, double *acc_out, double *abs_out, int nthreads)
+{
+    if (!fp8_args_ok(M, N, K, fmt_a, fmt_b, beta, C))
+        return -1;
+    for (int64_t i = 0; i < npairs; ++i)
+        if (pairs[2 * i] < 0 || pairs[2 * i] >= M || pairs[2 * i + 1] < 0 ||
+            pairs[2 * i + 1] >= N)
+            return -1;
+    struct gemm_job j;
+    memset(&j, 0, sizeof(j));
+    j.M = M; j.N = N; j.K = K; j.fmt_a = fmt_a; j.fmt_b = fmt_b;
+    j.A = A; j.lda_bytes = lda; j.B = B; j.ldb_bytes = ldb;
     j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
     j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
     j.D = D; j.ldd = 0; j.acc_out = acc_out; j.abs_out = abs_out;

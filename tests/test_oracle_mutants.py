@@ -24,8 +24,8 @@ MUTANTS = {
     "e8m0_bias_off_by_one": (
         "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 126);"),
     "scale_b_dropped": (
-        "double b = oracle_e2m1_value(cb) * oracle_e8m0_value(eb);",
-        "double b = oracle_e2m1_value(cb);"),
+        "double b = vb * oracle_e8m0_value(eb);",
+        "double b = vb;"),
     "scale_block_16": (
         "unsigned ea = sarow[k / 32], eb = sbrow[k / 32];",
         "unsigned ea = sarow[k / 16], eb = sbrow[k / 32];"),
@@ -58,6 +58,22 @@ MUTANTS = {
         "for (int i = 0; i < 32; ++i) {\n                const double v = fabs(",
         "for (int i = 0; i < 16; ++i) {\n                const double v = fabs("),
     "quant_sign_dropped_for_zero": ("if (signbit(v))", "if (v < 0.0)"),
+    "fp8_e4m3_bias_8": (
+        "bias = fmt == 1 ? 7 : 15;", "bias = fmt == 1 ? 8 : 15;"),
+    "fp8_e5m2_three_mantissa_bits": (
+        "mbits = fmt == 1 ? 3 : 2,", "mbits = fmt == 1 ? 3 : 3,"),
+    "fp8_subnormal_implicit_one": (
+        "(e == 0 ? 0.0 : 1.0) + ldexp", "1.0 + ldexp"),
+    "fp8_e4m3_nan_whole_top_binade": (
+        "if (fmt == 1 && e == emax && m == (1u << mbits) - 1u)", "if (fmt == 1 && e == emax)"),
+    "fp8_adjacent_elements_swapped": (
+        "va = oracle_fp8_value_q(arow[k], j->fmt_a, &qa);",
+        "va = oracle_fp8_value_q(arow[k ^ 1], j->fmt_a, &qa);"),
+    "fp8_b_decoded_in_a_format": (
+        "vb = oracle_fp8_value_q(brow[k], j->fmt_b, &qb);",
+        "vb = oracle_fp8_value_q(brow[k], j->fmt_a, &qb);"),
+    "fp8_granule_of_fp4": (
+        "int g = qa + qb + (int)ea + (int)eb - 254;", "int g = (int)ea + (int)eb - 256;"),
     "transposed_d_store": (
         "if (!one_output(j, m, n, &j->D[(int64_t)m * j->ldd + n],",
         "if (!one_output(j, m, n, &j->D[(int64_t)(n % j->M) * j->ldd + (m % j->N)],"),

@@ -432,13 +432,185 @@ def check_quant_matches_generator(o):
     assert np.array_equal(Qo, Qg)
 
 
+# --- MXFP8 (E4M3 / E5M2 elements, E8M0 per 32) -----------------------------
+
+def fp8_fraction(code, fmt):
+    """Exact value of an 8-bit code from the format's field widths (test-side
+    decoder): E4M3 = 1/4/3 bits, bias 7; E5M2 = 1/5/2 bits, bias 15.  Returns
+    None for the NaN / infinity codes."""
+    mbits, ebits, bias = (3, 4, 7) if fmt == 1 else (2, 5, 15)
+    e = (code >> mbits) & ((1 << ebits) - 1)
+    m = code & ((1 << mbits) - 1)
+    if fmt == 1 and e == 15 and m == 7:
+        return None
+    if fmt == 2 and e == 31:
+        return None
+    if e == 0:
+        v = Fraction(m, 2 ** mbits) * Fraction(2) ** (1 - bias)
+    else:
+        v = (1 + Fraction(m, 2 ** mbits)) * Fraction(2) ** (e - bias)
+    return -v if code & 0x80 else v
+
+
+def fp8_torch_decode(codes, fmt):
+    import torch
+    dt = torch.float8_e4m3fn if fmt == 1 else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(dt).double().numpy()
+
+
+def random_case8(rng, M, N, K, fmt_a, fmt_b, scale_lo=124, scale_hi=130):
+    """Random codes of each format with magnitudes in [2^-4, 2^5) (plus
+    zeros and, for E4M3, subnormals), scales near 1, C with exponents
+    2^-8 .. 2^8: exact in double at these sizes.  (Codes spanning a whole
+    format would not be: E5M2 alone spans 2^-16 .. 2^15.8.)"""
+    def finite_codes(fmt, shape):
+        mbits, bias = (3, 7) if fmt == 1 else (2, 15)
+        e = rng.integers(bias - 4, bias + 5, size=shape)
+        m = rng.integers(0, 1 << mbits, size=shape)
+        c = (e << mbits) | m
+        kind = rng.random(shape)
+        c = np.where(kind < 0.08, 0, c)
+        if fmt == 1:
+            c = np.where((kind >= 0.08) & (kind < 0.14), m, c)      # subnormals
+        c = c | (rng.integers(0, 2, size=shape) << 7)
+        return c.astype(np.uint8)
+    A = finite_codes(fmt_a, (M, K))
+    B = finite_codes(fmt_b, (N, K))
+    SA = rng.integers(scale_lo, scale_hi + 1, size=(M, K // 32)).astype(np.uint8)
+    SB = rng.integers(scale_lo, scale_hi + 1, size=(N, K // 32)).astype(np.uint8)
+    e = rng.integers(119, 136, size=(M, N)).astype(np.uint16)
+    f = rng.integers(0, 128, size=(M, N)).astype(np.uint16)
+    sgn = rng.integers(0, 2, size=(M, N)).astype(np.uint16)
+    C = (sgn << 15) | (e << 7) | f
+    return A, B, SA, SB, C
+
+
+def check_fp8_golden(o):
+    for fmt, code, v in read_golden("fp8_values.txt"):
+        got = o.fp8_value(int(code, 16), int(fmt))
+        if v == "nan":
+            assert got != got, (fmt, code)
+        elif v in ("inf", "-inf"):
+            assert got == float(v), (fmt, code, got)
+        else:
+            assert got == float(v) and math.copysign(1.0, got) == math.copysign(1.0, float(v)), \
+                (fmt, code, got, v)
+
+
+def check_fp8_all_codes(o):
+    """Every code of both formats: the oracle's decode equals the test-side
+    field decoder and torch's float8 decoding (NaN and infinity included)."""
+    codes = np.arange(256, dtype=np.uint8)
+    for fmt in (1, 2):
+        ref = fp8_torch_decode(codes.reshape(1, -1), fmt)[0]
+        for c in range(256):
+            got = o.fp8_value(c, fmt)
+            want = fp8_fraction(c, fmt)
+            if want is None:
+                assert (got != got and ref[c] != ref[c]) or (math.isinf(got) and got == ref[c]), (fmt, c)
+            else:
+                assert math.isfinite(got) and Fraction(got) == want and got == ref[c], \
+                    (fmt, c, got, want, ref[c])
+
+
+def brute_force_gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha, beta, C):
+    two = Fraction(2)
+    D = np.zeros((M, N), dtype=np.uint16)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                a = fp8_fraction(int(A[m, k]), fmt_a) * two ** (int(SA[m, k // 32]) - 127)
+                b = fp8_fraction(int(B[n, k]), fmt_b) * two ** (int(SB[n, k // 32]) - 127)
+                acc += a * b
+            y = Fraction(alpha) * acc
+            if beta != 0.0:
+                y += Fraction(beta) * bf16_bits_to_fraction(int(C[m, n]))
+            D[m, n] = bf16_rne_by_search(y)
+    return D
+
+
+def check_fp8_brute_force(o, cases=8):
+    rng = np.random.default_rng(81)
+    for i in range(cases):
+        fmt_a, fmt_b = [(1, 1), (1, 2), (2, 1), (2, 2)][i % 4]
+        M, N, K = 3, 4, 64
+        A, B, SA, SB, C = random_case8(rng, M, N, K, fmt_a, fmt_b)
+        alpha, beta = [(1.0, 0.0), (0.5, 0.25), (-2.0, 1.0), (0.75, -0.5)][i % 4]
+        D, _, _, inexact = o.gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha=alpha, beta=beta, C=C)
+        assert inexact == 0
+        want = brute_force_gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha, beta, C)
+        assert same_value(D, want), (i, D, want)
+
+
+def check_fp8_torch_crosscheck(o):
+    """The exact double sum equals one float64 matmul of torch-decoded,
+    scaled operands (exact at these sizes)."""
+    rng = np.random.default_rng(82)
+    for fmt_a, fmt_b in ((1, 1), (2, 1)):
+        M, N, K = 24, 40, 256
+        A, B, SA, SB, _ = random_case8(rng, M, N, K, fmt_a, fmt_b)
+        _, acc, _, inexact = o.gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, want_acc=True)
+        assert inexact == 0
+        sa = np.repeat(np.ldexp(1.0, SA.astype(np.int64) - 127), 32, axis=1)
+        sb = np.repeat(np.ldexp(1.0, SB.astype(np.int64) - 127), 32, axis=1)
+        ref = (fp8_torch_decode(A, fmt_a) * sa) @ (fp8_torch_decode(B, fmt_b) * sb).T
+        assert np.array_equal(acc, ref)
+
+
+def check_fp8_identity(o):
+    """B = I (E4M3 1.0 = 0x38, all scales 1): D is A's values, which bf16
+    holds exactly (3 mantissa bits), scaled by A's block scale."""
+    rng = np.random.default_rng(83)
+    M, N, K = 16, 64, 96
+    A, _, SA, _, _ = random_case8(rng, M, N, K, 1, 1, 125, 129)
+    B = np.zeros((N, K), dtype=np.uint8)
+    idx = np.arange(min(N, K))
+    B[idx, idx] = 0x38
+    SB = np.full((N, K // 32), 127, dtype=np.uint8)
+    D, _, _, inexact = o.gemm8(A, B, SA, SB, M, N, K, 1, 1)
+    assert inexact == 0
+    vals = fp8_torch_decode(A[:, :N], 1) * np.ldexp(1.0, SA[:, np.arange(N) // 32].astype(np.int64) - 127)
+    want = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert same_value(D, want)
+
+
+def check_fp8_sampled_matches_full(o):
+    rng = np.random.default_rng(84)
+    M, N, K = 20, 30, 128
+    A, B, SA, SB, C = random_case8(rng, M, N, K, 2, 1)
+    D, _, _, _ = o.gemm8(A, B, SA, SB, M, N, K, 2, 1, alpha=0.5, beta=1.0, C=C)
+    pairs = np.stack([rng.integers(0, M, 50), rng.integers(0, N, 50)], axis=1)
+    Ds, _, _, _ = o.gemm8_sampled(A, B, SA, SB, M, N, K, 2, 1, pairs, alpha=0.5, beta=1.0, C=C)
+    assert np.array_equal(Ds, D[pairs[:, 0], pairs[:, 1]])
+
+
+def check_fp8_exactness_flag(o):
+    """E5M2 products from 57344^2 (~2^31.6) down to (2^-16)^2 = 2^-32 in one
+    sum: sum|ab| / granule exceeds 2^52, which the oracle must report; a row
+    of moderate values must not be flagged."""
+    K = 64
+    A = np.zeros((2, K), dtype=np.uint8)
+    B = np.zeros((1, K), dtype=np.uint8)
+    A[0, 0], A[0, 1] = 0x7B, 0x01          # 57344 and 2^-16
+    B[0, 0], B[0, 1] = 0x7B, 0x01
+    A[1, :4] = 0x3C                        # 1.0
+    B[0, 2:6] = 0x3D                       # 1.25
+    S = np.full((2, K // 32), 127, dtype=np.uint8)
+    _, _, _, inexact = o.gemm8(A, B, S, S[:1], 2, 1, K, 2, 2)
+    assert inexact == 1, inexact
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
               check_brute_force, check_all_code_pairs, check_numpy_crosscheck,
               check_rounding_is_only_error, check_sampled_matches_full,
               check_quant_golden, check_quant_scale_rule, check_quant_nearest_brute_force,
-              check_quant_matches_generator]
+              check_quant_matches_generator,
+              check_fp8_golden, check_fp8_all_codes, check_fp8_brute_force,
+              check_fp8_torch_crosscheck, check_fp8_identity, check_fp8_sampled_matches_full,
+              check_fp8_exactness_flag]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

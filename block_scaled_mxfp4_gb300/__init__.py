@@ -22,6 +22,7 @@ __all__ = [
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
+    "mxfp8_gemm", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size", "MXFP8_E4M3", "MXFP8_E5M2",
     "gemm", "Plan",
 ]
 
@@ -31,6 +32,7 @@ HEADER = os.path.join(_ROOT, "include", "mxfp4_gemm.h")
 _LIB_NAME = "libmxfp4_gb300.so"
 
 MXFP4_OK = 0
+MXFP8_E4M3, MXFP8_E5M2 = 0, 1
 STATUS_NAMES = {0: "MXFP4_OK", -1: "MXFP4_ERR_INVALID_ARG", -2: "MXFP4_ERR_UNSUPPORTED_SHAPE",
                 -3: "MXFP4_ERR_MISALIGNED", -4: "MXFP4_ERR_WORKSPACE", -5: "MXFP4_ERR_CUDA",
                 -6: "MXFP4_ERR_TIMEOUT", -7: "MXFP4_ERR_ARCH"}
@@ -85,6 +87,10 @@ def lib() -> ctypes.CDLL:
             "mxfp4_quantize": (i32, [vp, i64, vp, i64, vp, i64, i32, i32, vp]),
             "mxfp4_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                  f32, f32, i32, i32, i32, i32, vp, sz, vp]),
+            "mxfp8_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                 i32, i32, f32, f32, i32, i32, i32, i32, vp, sz, vp]),
+            "mxfp8_plan_gemm": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]),
+            "mxfp8_gemm_workspace_size": (sz, [i32, i32, i32, i32]),
             "mxfp4_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
                                            f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp4_gemm_noalloc": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
@@ -184,6 +190,25 @@ def mxfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alp
     return _check(lib().mxfp4_gemm(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
                                    ld_sa, _p(scaleB), ld_sb, alpha, beta, M, N, K, split_k,
                                    _p(workspace), workspace_bytes, _stream(stream)), "mxfp4_gemm")
+
+
+def mxfp8_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, fmt_a, fmt_b,
+               alpha, beta, M, N, K, split_k, workspace, workspace_bytes, stream=None):
+    """MXFP8 GEMM (A, B: one E4M3 / E5M2 code per byte, lda / ldb in elements)."""
+    return _check(lib().mxfp8_gemm(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
+                                   ld_sa, _p(scaleB), ld_sb, fmt_a, fmt_b, alpha, beta, M, N, K,
+                                   split_k, _p(workspace), workspace_bytes, _stream(stream)),
+                  "mxfp8_gemm")
+
+
+def mxfp8_plan_gemm(M, N, K, split_k=0, num_sms=0) -> Plan:
+    plan = Plan()
+    _check(lib().mxfp8_plan_gemm(M, N, K, split_k, num_sms, ctypes.byref(plan)), "mxfp8_plan_gemm")
+    return plan
+
+
+def mxfp8_gemm_workspace_size(M, N, K, split_k=0) -> int:
+    return lib().mxfp8_gemm_workspace_size(M, N, K, split_k)
 
 
 def mxfp4_gemm_noalloc(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha,

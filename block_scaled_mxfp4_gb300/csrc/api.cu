@@ -233,7 +233,10 @@ KernelChoice kernel_override()
     return KernelChoice::Auto;
 }
 
-int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape)
+// fp8: plan an MXFP8 GEMM whose rows hold as many bytes as this K of fp4
+// elements (the caller passes twice its 8-bit K): the one-tile kernel only.
+int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape,
+              bool fp8 = false)
 {
     if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_req < 0 || split_req > kMaxSplit)
         return MXFP4_ERR_INVALID_ARG;
@@ -243,11 +246,11 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     const int64_t P = swap ? N : M;
     const int64_t Q = swap ? M : N;
     const int kt = (K + kTileK - 1) / kTileK;
-    const KernelChoice choice = split_req == 0 ? kernel_override() : KernelChoice::Auto;
+    const KernelChoice choice = (split_req == 0 && !fp8) ? kernel_override() : KernelChoice::Auto;
     const int64_t tiles256 = ((static_cast<int64_t>(M) + 255) / 256) * ((static_cast<int64_t>(N) + 255) / 256);
     // The CTA-pair kernel takes shapes whose 256 x 256 tiles fill at least one
     // wave of SM pairs (and any shape of at least 256 x 256 when forced).
-    const bool pair_fits = !swap && M >= 256 && N >= 256;
+    const bool pair_fits = !fp8 && !swap && M >= 256 && N >= 256;
     const bool use_pair = pair_fits && (choice == KernelChoice::Pair ||
                                         (choice == KernelChoice::Auto && split_req == 0 &&
                                          tiles256 >= (sms > 0 ? sms : kDefaultSms) / 2));
@@ -435,6 +438,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         shape->pair_ctas = out->ctas;
         shape->pair_cluster = pair_cluster;
         shape->pair_kc = pair_kc;
+        shape->fp8 = fp8 ? 1 : 0;
     }
     return MXFP4_OK;
 }
@@ -496,7 +500,7 @@ int next_epoch()
 int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
              const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M, int N,
              int K, const mxfp4_plan &plan, const GemmShape &shape, uint8_t *ws, int sms,
-             cudaStream_t stream, bool after_relayout = false)
+             cudaStream_t stream, bool after_relayout = false, int fmt_a = 0, int fmt_b = 0)
 {
     float *partials = ws ? reinterpret_cast<float *>(ws + kFlagBytes) : nullptr;
     if (shape.gemv) {
@@ -565,8 +569,10 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     const void *Qp = swap ? A : B;
     const int Prows = swap ? N : M, Qrows = swap ? M : N;
     const int64_t ldP = swap ? ldb : lda, ldQ = swap ? lda : ldb;
-    if (!encode_operand(&tmP, Pp, Prows, K, ldP, kTileM) ||
-        !encode_operand(&tmQ, Qp, Qrows, K, ldQ, shape.tile_n))
+    // An 8-bit row of K elements holds the bytes of an fp4 row of 2K.
+    const int kx = shape.fp8 ? 2 : 1;
+    if (!encode_operand(&tmP, Pp, Prows, K * kx, ldP * kx, kTileM) ||
+        !encode_operand(&tmQ, Qp, Qrows, K * kx, ldQ * kx, shape.tile_n))
         return MXFP4_ERR_CUDA;
 
     GemmArgs a;
@@ -592,8 +598,10 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.M = M;
     a.N = N;
     a.K = K;
-    a.kt_total = (K + kTileK - 1) / kTileK;
+    a.kt_total = (K * kx + kTileK - 1) / kTileK;
     a.kt_per_split = plan.k_tiles_per_split;
+    a.fmt_p = swap ? fmt_b : fmt_a;
+    a.fmt_q = swap ? fmt_a : fmt_b;
     a.split_k = plan.split_k;
     a.alpha = alpha;
     a.beta = beta;
@@ -796,22 +804,34 @@ int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const
                       workspace_bytes, stream);
 }
 
-int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
-               const void *B, int64_t ldb, const void *scaleA, int64_t ld_sa, const void *scaleB,
-               int64_t ld_sb, float alpha, float beta, int M, int N, int K, int split_k,
-               void *workspace, size_t workspace_bytes, void *stream)
+// mxfp4_gemm and mxfp8_gemm: row-major scales, relaid into the workspace
+// first when the plan asks for it.  fp8: K counts 8-bit elements (the plan
+// is that of an fp4 GEMM of 2K, which has the same bytes per row).
+static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
+                         int64_t lda, const void *B, int64_t ldb, const void *scaleA,
+                         int64_t ld_sa, const void *scaleB, int64_t ld_sb, float alpha, float beta,
+                         int M, int N, int K, int split_k, void *workspace, size_t workspace_bytes,
+                         void *stream, bool fp8, int fmt_a, int fmt_b)
 {
-    int st = check_common(D, ldd, C, ldc, A, lda, B, ldb, beta, M, N, K, split_k);
+    const int kx = fp8 ? 2 : 1;
+    if (fp8 && (K > (1 << 29) || lda > (INT64_MAX / 4) || ldb > (INT64_MAX / 4)))
+        return MXFP4_ERR_INVALID_ARG;
+    int st = check_common(D, ldd, C, ldc, A, lda * kx, B, ldb * kx, beta, M, N, K * kx, split_k);
     if (st != MXFP4_OK)
         return st;
+    if (K < 32 || (K % 32) != 0)
+        return MXFP4_ERR_INVALID_ARG;
     if (!scaleA || !scaleB || ld_sa < K / 32 || ld_sb < K / 32)
+        return MXFP4_ERR_INVALID_ARG;
+    if (fp8 && ((fmt_a != MXFP8_E4M3 && fmt_a != MXFP8_E5M2) ||
+                (fmt_b != MXFP8_E4M3 && fmt_b != MXFP8_E5M2)))
         return MXFP4_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, kAlign))
         return MXFP4_ERR_MISALIGNED;
     const int sms = device_sms_or_default();
     mxfp4_plan plan;
     GemmShape shape;
-    st = make_plan(M, N, K, split_k, sms, &plan, &shape);
+    st = make_plan(M, N, K * kx, split_k, sms, &plan, &shape, fp8);
     if (st != MXFP4_OK)
         return st;
     const size_t sfa_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(M, K)) : 0;
@@ -838,8 +858,51 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
         sc = Scales{sfa, sfb, 0, 0, false};
     }
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
-                    plan.workspace_bytes ? ws : nullptr, sms, s,
-                    plan.relayout_pass != 0);
+                    plan.workspace_bytes ? ws : nullptr, sms, s, plan.relayout_pass != 0, fmt_a,
+                    fmt_b);
+}
+
+int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+               const void *B, int64_t ldb, const void *scaleA, int64_t ld_sa, const void *scaleB,
+               int64_t ld_sb, float alpha, float beta, int M, int N, int K, int split_k,
+               void *workspace, size_t workspace_bytes, void *stream)
+{
+    return gemm_rowmajor(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
+                         M, N, K, split_k, workspace, workspace_bytes, stream, false, 0, 0);
+}
+
+int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+               const void *B, int64_t ldb, const void *scaleA, int64_t ld_sa, const void *scaleB,
+               int64_t ld_sb, int fmt_a, int fmt_b, float alpha, float beta, int M, int N, int K,
+               int split_k, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return gemm_rowmajor(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
+                         M, N, K, split_k, workspace, workspace_bytes, stream, true, fmt_a, fmt_b);
+}
+
+int mxfp8_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out)
+{
+    if (!out || K < 32 || (K % 32) != 0 || K > (1 << 29))
+        return MXFP4_ERR_INVALID_ARG;
+    if (num_sms <= 0)
+        num_sms = device_sms_or_default();
+    const int st = make_plan(M, N, 2 * K, split_k, num_sms, out, nullptr, true);
+    if (st == MXFP4_OK)
+        out->tile_k = kTileK / 2;           // 8-bit elements per stage
+    return st;
+}
+
+size_t mxfp8_gemm_workspace_size(int M, int N, int K, int split_k)
+{
+    mxfp4_plan plan;
+    if (K < 32 || (K % 32) != 0 || K > (1 << 29) ||
+        make_plan(M, N, 2 * K, split_k, device_sms_or_default(), &plan, nullptr, true) != MXFP4_OK)
+        return 0;
+    size_t ws = plan.workspace_bytes;
+    if (plan.relayout_pass)
+        ws = (ws ? ws : kFlagBytes) + align_up(sf_relaid_bytes(M, K)) +
+             align_up(sf_relaid_bytes(N, K));
+    return ws;
 }
 
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)

@@ -47,21 +47,25 @@ namespace mxfp4 {
 
 __device__ int g_device_status = 0;
 
-template <int BN, int STAGES>
+// G = scale k-groups (4 blocks of 32 K) per stage of 128 bytes per row: 2 for
+// fp4 elements (256 K per stage), 1 for 8-bit elements (128 K per stage).
+template <int BN, int STAGES, int G = 2>
 struct Cfg {
     static constexpr int BM = kTileM;
     static constexpr int BN_COLS = BN;
     static constexpr int STAGE_COUNT = STAGES;
+    static constexpr int GROUPS = G;
     static constexpr int P_BYTES = BM * 128;
     static constexpr int Q_BYTES = BN * 128;
     static constexpr int NQ = BN >= 128 ? BN / 128 : 1;      // 128-row scale blocks of Q
-    static constexpr int SFP_BYTES = 2 * kSfAtomBytes;       // 2 atoms per 256-K stage
-    static constexpr int SFQ_BYTES = NQ * 2 * kSfAtomBytes;
-    static constexpr int STAGE_BYTES = P_BYTES + Q_BYTES + SFP_BYTES + SFQ_BYTES;
+    static constexpr int SFP_BYTES = G * kSfAtomBytes;       // G atoms per stage
+    static constexpr int SFQ_BYTES = NQ * G * kSfAtomBytes;
+    // Stages start on 1024-byte boundaries (128-byte swizzle atoms).
+    static constexpr int STAGE_BYTES = (P_BYTES + Q_BYTES + SFP_BYTES + SFQ_BYTES + 1023) / 1024 * 1024;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-    static constexpr int SF_COLS_P = 8;                      // 2 groups x 4 columns
-    static constexpr int SF_COLS_Q = 8 * NQ;
+    static constexpr int SF_COLS_P = 4 * G;                  // G groups x 4 columns
+    static constexpr int SF_COLS_Q = 4 * G * NQ;
     static constexpr int SF_COLS = SF_COLS_P + SF_COLS_Q;
     static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -72,6 +76,7 @@ struct Cfg {
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+    static_assert(G == 1 || G == 2, "scale groups per stage");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -202,34 +207,46 @@ __device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int z, int m0
 }
 
 // Row-major scales -> one lane's share of a 128-row block for stage kt: rows
-// row0 + lane + 32j (j = 0..3), K blocks 8kt .. 8kt+7 as two 4-byte words
-// (byte b of word g = block 8kt + 4g + b).  Missing rows / blocks read 0x7F.
+// row0 + lane + 32j (j = 0..3), K blocks 4G kt .. 4G kt + 4G - 1 as G 4-byte
+// words (byte b of word g = block 4G kt + 4g + b).  Missing rows / blocks
+// read 0x7F.
+template <int G>
 __device__ __forceinline__ void load_sf_rows(const uint8_t *S, int64_t ld, int rows, int kblocks,
                                              int row0, int kt, int vec8, int lane,
-                                             uint32_t (&w)[4][2])
+                                             uint32_t (&w)[4][G])
 {
-    const int kb0 = kt * 8;
+    const int kb0 = kt * 4 * G;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int r = row0 + lane + 32 * j;
         if (r < rows) {
             const uint8_t *p = S + static_cast<int64_t>(r) * ld + kb0;
-            if (vec8 && kb0 + 8 <= kblocks) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
-                w[j][0] = v.x;
-                w[j][1] = v.y;
+            if (vec8 && kb0 + 4 * G <= kblocks) {
+                if constexpr (G == 2) {
+                    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+                    w[j][0] = v.x;
+                    w[j][1] = v.y;
+                } else {
+                    w[j][0] = __ldg(reinterpret_cast<const uint32_t *>(p));
+                }
             } else {
-                uint32_t x[2] = {0u, 0u};
+                uint32_t x[G];
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
+                for (int g = 0; g < G; ++g)
+                    x[g] = 0u;
+#pragma unroll
+                for (int b = 0; b < 4 * G; ++b) {
                     const uint32_t v = (kb0 + b < kblocks) ? static_cast<uint32_t>(p[b]) : 0x7Fu;
                     x[b >> 2] |= v << (8 * (b & 3));
                 }
-                w[j][0] = x[0];
-                w[j][1] = x[1];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    w[j][g] = x[g];
             }
         } else {
-            w[j][0] = w[j][1] = 0x7F7F7F7Fu;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                w[j][g] = 0x7F7F7F7Fu;
         }
     }
 }
@@ -238,16 +255,17 @@ __device__ __forceinline__ void load_sf_rows(const uint8_t *S, int64_t ld, int r
 // goes straight from global memory to its place in the atom (row lane + 32j,
 // word g -> atom g, line lane, word j).  Missing rows / blocks are zero-filled
 // (their operand data is zero-filled by TMA too, so the product is 0).
+template <int G = 2>
 __device__ __forceinline__ void copy_sf_rows_async(uint8_t *atoms, const uint8_t *S, int64_t ld,
                                                    int rows, int kblocks, int row0, int kt,
                                                    int lane)
 {
-    const int kb0 = kt * 8;
+    const int kb0 = kt * 4 * G;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int r = row0 + lane + 32 * j;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G; ++g) {
             const int have = kblocks - (kb0 + 4 * g);
             const uint32_t bytes = (r < rows && have > 0) ? static_cast<uint32_t>(min(have, 4)) : 0u;
             const uint8_t *src = bytes ? S + static_cast<int64_t>(r) * ld + kb0 + 4 * g : S;
@@ -256,12 +274,13 @@ __device__ __forceinline__ void copy_sf_rows_async(uint8_t *atoms, const uint8_t
     }
 }
 
-// Line `lane` of the two atoms of a stage: 16 bytes = rows lane, lane+32,
+// Line `lane` of the G atoms of a stage: 16 bytes = rows lane, lane+32,
 // lane+64, lane+96, four K blocks each.
-__device__ __forceinline__ void store_sf_lines(uint8_t *atoms, const uint32_t (&w)[4][2], int lane)
+template <int G>
+__device__ __forceinline__ void store_sf_lines(uint8_t *atoms, const uint32_t (&w)[4][G], int lane)
 {
 #pragma unroll
-    for (int g = 0; g < 2; ++g)
+    for (int g = 0; g < G; ++g)
         *reinterpret_cast<uint4 *>(atoms + g * kSfAtomBytes + 16 * lane) =
             make_uint4(w[0][g], w[1][g], w[2][g], w[3][g]);
 }
@@ -285,11 +304,12 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
         bool ok = mbar_wait(&full[stage], phase, abort_flag, limit, &g_device_status);
         if (!__all_sync(0xffffffffu, ok))
             return;
+        constexpr int G = Cf::GROUPS;
         const uint8_t *sf_s = smem + stage * Cf::STAGE_BYTES + Cf::P_BYTES + Cf::Q_BYTES;
-        uint32_t wp[8];
-        uint32_t wq[8 * Cf::NQ];
+        uint32_t wp[4 * G];
+        uint32_t wq[4 * G * Cf::NQ];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G; ++g) {
             const uint4 v = *reinterpret_cast<const uint4 *>(sf_s + g * kSfAtomBytes + 16 * lane);
             wp[4 * g] = v.x;
             wp[4 * g + 1] = v.y;
@@ -298,7 +318,7 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
 #pragma unroll
             for (int r = 0; r < Cf::NQ; ++r) {
                 const uint4 u = *reinterpret_cast<const uint4 *>(
-                    sf_s + Cf::SFP_BYTES + r * 2 * kSfAtomBytes + g * kSfAtomBytes + 16 * lane);
+                    sf_s + Cf::SFP_BYTES + r * G * kSfAtomBytes + g * kSfAtomBytes + 16 * lane);
                 const int o = (g * Cf::NQ + r) * 4;
                 wq[o] = u.x;
                 wq[o + 1] = u.y;
@@ -307,11 +327,16 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
             }
         }
         const uint32_t slot = t_sf + stage * Cf::SF_COLS;
-        tmem_st_32x32b_x8(slot, wp);
-        if constexpr (Cf::NQ == 2)
-            tmem_st_32x32b_x16(slot + Cf::SF_COLS_P, wq);
+        if constexpr (G == 2)
+            tmem_st_32x32b_x8(slot, wp);
         else
+            tmem_st_32x32b_x4(slot, wp);
+        if constexpr (4 * G * Cf::NQ == 16)
+            tmem_st_32x32b_x16(slot + Cf::SF_COLS_P, wq);
+        else if constexpr (4 * G * Cf::NQ == 8)
             tmem_st_32x32b_x8(slot + Cf::SF_COLS_P, wq);
+        else
+            tmem_st_32x32b_x4(slot + Cf::SF_COLS_P, wq);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -326,12 +351,15 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
 
 constexpr int kGemmThreads = 256;
 
-template <int BN, int STAGES, bool SWAP>
+// FMT 0: fp4 (E2M1) elements, kind::mxf4; FMT 1: 8-bit (E4M3 / E5M2)
+// elements, kind::mxf8f6f4 with the element types in a.idesc8.
+template <int BN, int STAGES, bool SWAP, int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_mxf4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmP,
                      const __grid_constant__ CUtensorMap tmQ)
 {
-    using Cf = Cfg<BN, STAGES>;
+    using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
+    constexpr int G = Cf::GROUPS;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the ring (128-byte swizzle atoms).
     const uint32_t raw = smem_addr(smem_raw);
@@ -404,11 +432,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
                 }
                 uint8_t *sf_s = st + Cf::P_BYTES + Cf::Q_BYTES;
-                copy_sf_rows_async(sf_s, a.sfP, a.ldsP, a.rowsP, kblocks, p0, kt, lane);
+                copy_sf_rows_async<G>(sf_s, a.sfP, a.ldsP, a.rowsP, kblocks, p0, kt, lane);
 #pragma unroll
                 for (int r = 0; r < Cf::NQ; ++r)
-                    copy_sf_rows_async(sf_s + Cf::SFP_BYTES + r * 2 * kSfAtomBytes, a.sfQ, a.ldsQ,
-                                       a.rowsQ, kblocks, q0 + r * kSfRowBlock, kt, lane);
+                    copy_sf_rows_async<G>(sf_s + Cf::SFP_BYTES + r * G * kSfAtomBytes, a.sfQ, a.ldsQ,
+                                          a.rowsQ, kblocks, q0 + r * kSfRowBlock, kt, lane);
                 cp_async_mbar_arrive(&full[stage]);
                 ++issued;
                 if (++stage == STAGES) {
@@ -427,8 +455,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t pol_p = a.stream_p ? l2_policy_evict_first() : l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_last();
             const int kblocks = a.K / 32;
-            uint32_t wp[4][2];
-            uint32_t wq[Cf::NQ][4][2];
+            uint32_t wp[4][G];
+            uint32_t wq[Cf::NQ][4][G];
             auto load_sf = [&](int kt) {
                 load_sf_rows(a.sfP, a.ldsP, a.rowsP, kblocks, p0, kt, a.sf_vec8, lane, wp);
 #pragma unroll
@@ -456,7 +484,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 store_sf_lines(sf_s, wp, lane);
 #pragma unroll
                 for (int r = 0; r < Cf::NQ; ++r)
-                    store_sf_lines(sf_s + Cf::SFP_BYTES + r * 2 * kSfAtomBytes, wq[r], lane);
+                    store_sf_lines(sf_s + Cf::SFP_BYTES + r * G * kSfAtomBytes, wq[r], lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
@@ -499,14 +527,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
                 } else {
                     mbar_arrive_expect_tx(&full[stage], Cf::SFP_BYTES + Cf::SFQ_BYTES);
-                    const int64_t sf_off = static_cast<int64_t>(kt) * 2 * kSfAtomBytes;
+                    // Stage kt's G k-groups: atoms G kt .. G kt + G - 1 of each block.
+                    const int64_t sf_off = static_cast<int64_t>(kt) * G * kSfAtomBytes;
                     bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES, sfp + sf_off, Cf::SFP_BYTES,
                               &full[stage], pol_p);
 #pragma unroll
                     for (int r = 0; r < Cf::NQ; ++r)
                         bulk_load(st + Cf::P_BYTES + Cf::Q_BYTES + Cf::SFP_BYTES +
-                                      r * 2 * kSfAtomBytes,
-                                  sfq + r * a.sf_rb_stride + sf_off, 2 * kSfAtomBytes,
+                                      r * G * kSfAtomBytes,
+                                  sfq + r * a.sf_rb_stride + sf_off, G * kSfAtomBytes,
                                   &full[stage], pol_q);
                 }
                 ++issued;
@@ -524,7 +553,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ---------------------------------------------------- MMA issuer --
         if (lane == 0 && nkt > 0) {
-            const uint32_t idesc = idesc_mxf4(kTileM, BN);
+            const uint32_t idesc = FMT == 0 ? idesc_mxf4(kTileM, BN) : a.idesc8;
             const uint32_t t_sf = tmem + BN;
             // A 64-row Q tile uses the upper or lower half of its 128-row atom.
             // (Row-major scales are built relative to q0, so no offset there.)
@@ -545,10 +574,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + Cf::P_BYTES));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t sf_id = (j & 1) * 2;
-                    mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_sf_ids(idesc, sf_id, sf_id),
-                             sfp_t + (j >> 1) * 4, sfq_t + (j >> 1) * 4 * Cf::NQ + q_off,
-                             (i > 0 || j > 0) ? 1u : 0u);
+                    if constexpr (FMT == 0) {
+                        // K=64: bytes 0-1 / 2-3 of k-group j / 2.
+                        const uint32_t sf_id = (j & 1) * 2;
+                        mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_sf_ids(idesc, sf_id, sf_id),
+                                 sfp_t + (j >> 1) * 4, sfq_t + (j >> 1) * 4 * Cf::NQ + q_off,
+                                 (i > 0 || j > 0) ? 1u : 0u);
+                    } else {
+                        // K=32: byte j of the stage's single k-group.
+                        mma_mxf8(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_sf_ids(idesc, j, j), sfp_t,
+                                 sfq_t + q_off, (i > 0 || j > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(&empty[stage]);
                 if (++stage == STAGES) {
@@ -607,12 +643,12 @@ namespace mxfp4 {
 
 // ----------------------------------------------------------- host side --
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, int FMT>
 static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
                               dim3 grid, cudaStream_t stream)
 {
-    using Cf = Cfg<BN, STAGES>;
-    auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP>;
+    using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
+    auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP, FMT>;
     // Opt in to the large dynamic shared memory once per device.
     static int configured[64] = {0};
     int dev = 0;
@@ -648,23 +684,37 @@ bool gemm_config_exists(const GemmShape &s)
     return s.tile_n == 64 && (s.stages == 4 || s.stages == 8);
 }
 
-cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
-                        const GemmShape &s, dim3 grid, cudaStream_t stream)
+template <int FMT>
+static cudaError_t launch_gemm_fmt(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                                   const GemmShape &s, dim3 grid, cudaStream_t stream)
 {
     if (!s.swap) {
         if (s.tile_n == 256 && s.stages == 4)
-            return launch_cfg<256, 4, false>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<256, 4, false, FMT>(a, tmP, tmQ, grid, stream);
         if (s.tile_n == 128 && s.stages == 6)
-            return launch_cfg<128, 6, false>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<128, 6, false, FMT>(a, tmP, tmQ, grid, stream);
         if (s.tile_n == 64 && s.stages == 8)
-            return launch_cfg<64, 8, false>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 8, false, FMT>(a, tmP, tmQ, grid, stream);
     } else {
         if (s.tile_n == 64 && s.stages == 4)
-            return launch_cfg<64, 4, true>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 4, true, FMT>(a, tmP, tmQ, grid, stream);
         if (s.tile_n == 64 && s.stages == 8)
-            return launch_cfg<64, 8, true>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 8, true, FMT>(a, tmP, tmQ, grid, stream);
     }
     return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                        const GemmShape &s, dim3 grid, cudaStream_t stream)
+{
+    if (!s.fp8)
+        return launch_gemm_fmt<0>(a, tmP, tmQ, s, grid, stream);
+    if ((a.fmt_p != 0 && a.fmt_p != 1) || (a.fmt_q != 0 && a.fmt_q != 1))
+        return cudaErrorInvalidValue;
+    GemmArgs b = a;
+    b.idesc8 = idesc_mxf8(kTileM, s.tile_n, static_cast<uint32_t>(a.fmt_p),
+                          static_cast<uint32_t>(a.fmt_q));
+    return launch_gemm_fmt<1>(b, tmP, tmQ, s, grid, stream);
 }
 
 template <int BN, int STAGES, bool SWAP, int NACC, int NSLOT>

@@ -36,7 +36,7 @@ struct GemmArgs {
     int64_t ldsP, ldsQ;     // row-major: row strides in bytes
     int rowsP, rowsQ;       // rows of P and Q
     int M, N, K;
-    int kt_total;           // ceil(K / 256)
+    int kt_total;           // stages of 128 bytes per row: ceil(K / 256) fp4, ceil(K / 128) fp8
     int kt_per_split;
     int split_k;
     float alpha, beta;
@@ -49,6 +49,8 @@ struct GemmArgs {
     int vec32_ok;           // D allows aligned 32-byte row stores
     int stream_p;           // P is read once: hint L2 evict-first
     long long wait_limit;   // SM cycles before a wait gives up
+    uint32_t idesc8;        // fp8: kind::mxf8f6f4 instruction descriptor (set at launch)
+    int fmt_p, fmt_q;       // fp8: element types of P and Q (0 = E4M3, 1 = E5M2)
 };
 
 struct GemmShape {
@@ -63,6 +65,7 @@ struct GemmShape {
     int pair_cluster;       // pair kernel: pairs per cluster (1 or 2)
     int pair_kc;            // pair kernel: 256-K chunks per pipeline stage (1 or 2)
     int gemv;               // 1: GEMV kernel for M <= 2 (gemv.cu)
+    int fp8;                // 1: 8-bit elements (one-tile kernel, kind::mxf8f6f4)
 };
 
 // Work schedule of the persistent stream-K kernel.  Tile t (raster below)

@@ -196,6 +196,22 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdes
 
 // D(tmem) (+)= (A(smem) x scaleA) . (B(smem) x scaleB)^T, E2M1 inputs, one
 // E8M0 scale per 32 K (two per K=64 instruction), fp32 accumulate.
+// D[tmem] (+)= A[smem] . B[smem]^T for 8-bit E4M3 / E5M2 elements, one E8M0
+// scale per 32 K (scale_vec::1X: a K=32 instruction reads one scale byte per
+// row, the byte chosen by the descriptor's scale-factor ids).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                          uint32_t accumulate)
@@ -249,6 +265,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 // Each lane writes 8 / 16 consecutive 32-bit columns of its own TMEM lane
 // (the warp's 32-lane quarter, selected by the lane field of taddr).
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
@@ -384,6 +407,17 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N)
            | (static_cast<uint32_t>(N >> 3) << 17)         // N / 8
            | (1u << 23)                                    // scale format: UE8M0
            | (static_cast<uint32_t>(M >> 4) << 24);        // M / 16
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with UE8M0 scales: element type
+// codes 0 = E4M3, 1 = E5M2 for A and B (fields as in idesc_mxf4).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, uint32_t a_type, uint32_t b_type)
+{
+    return (a_type << 7)                                    // A format
+           | (b_type << 10)                                 // B format
+           | (static_cast<uint32_t>(N >> 3) << 17)          // N / 8
+           | (1u << 23)                                     // scale format: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24);         // M / 16
 }
 
 __device__ __forceinline__ uint32_t idesc_sf_ids(uint32_t idesc, uint32_t sfa_id, uint32_t sfb_id)

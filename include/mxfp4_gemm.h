@@ -173,6 +173,33 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * MXFP8 form of mxfp4_gemm: D[M,N] = alpha * A[M,K] . B[N,K]^T + beta * C[M,N]
+ * with 8-bit elements, one E8M0 scale per 32 K as for MXFP4 (page "CDNA4
+ * dense MFMA builtins", section "FP8 and BF8 matrix inputs": FP8 = E4M3,
+ * BF8 = E5M2; section "Mixed-precision with scaling": scaled per block, A
+ * and B formats chosen independently).  Encodings: the OCP 8-bit formats
+ * (E4M3: bias 7, no infinity, NaN = S.1111.111, largest 448; E5M2: bias 15,
+ * IEEE-style infinities and NaNs, largest 57344).
+ *   A: uint8 [M, lda] device, one code per element, lda >= K elements
+ *      (= bytes), lda % 16 == 0, 16-byte aligned; B likewise [N, ldb].
+ *   fmt_a, fmt_b: MXFP8_E4M3 or MXFP8_E5M2.
+ *   Scales, C, D, alpha, beta, split_k, workspace, stream: as for
+ *   mxfp4_gemm (mxfp8_gemm_workspace_size gives the workspace).
+ * Runs the one-tile tcgen05 kernel (kind::mxf8f6f4, K = 32 per MMA) with the
+ * same tile / split-K / swap-AB plan as an MXFP4 GEMM whose rows hold as many
+ * bytes (mxfp8_plan_gemm reports it; tile_k there counts 8-bit elements).
+ * Errors: as for mxfp4_gemm, plus MXFP4_ERR_INVALID_ARG for a bad format.
+ */
+enum { MXFP8_E4M3 = 0, MXFP8_E5M2 = 1 };
+int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
+               const void *A, int64_t lda, const void *B, int64_t ldb,
+               const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,
+               int fmt_a, int fmt_b, float alpha, float beta, int M, int N, int K, int split_k,
+               void *workspace, size_t workspace_bytes, void *stream);
+int mxfp8_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out);
+size_t mxfp8_gemm_workspace_size(int M, int N, int K, int split_k);
+
+/*
  * As mxfp4_gemm, with both scale buffers already in the relaid layout
  * produced by mxfp4_scale_relayout (scaleA for M rows, scaleB for N rows, at
  * the same K); the GEMM then copies whole scale atoms with bulk copies.  The

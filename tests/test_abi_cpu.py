@@ -230,6 +230,52 @@ def test_gemm_argument_validation(L, kw, status):
     assert _call_gemm(L, **kw) == status
 
 
+def _call_gemm8(L, **kw):
+    args = dict(D=0x1000, ldd=256, C=None, ldc=0, A=0x2000, lda=512, B=0x3000, ldb=512,
+                SA=0x4000, ld_sa=16, SB=0x5000, ld_sb=16, fa=0, fb=1, alpha=1.0, beta=0.0,
+                M=128, N=256, K=512, split=0, ws=0x10000, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return L.mxfp8_gemm(args["D"], args["ldd"], args["C"], args["ldc"], args["A"], args["lda"],
+                        args["B"], args["ldb"], args["SA"], args["ld_sa"], args["SB"],
+                        args["ld_sb"], args["fa"], args["fb"], args["alpha"], args["beta"],
+                        args["M"], args["N"], args["K"], args["split"], args["ws"], args["wsb"],
+                        args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=None), -1), (dict(A=None), -1), (dict(SA=None), -1),
+    (dict(fa=2), -1), (dict(fb=-1), -1),
+    (dict(M=0), -1), (dict(K=48, lda=64, ldb=64), -1), (dict(K=0), -1),
+    (dict(lda=500), -1), (dict(ldb=256), -1), (dict(ld_sa=15), -1),
+    (dict(beta=1.0), -1), (dict(split=17), -1),
+    (dict(lda=520), -3), (dict(ldb=536), -3), (dict(A=0x2008), -3),
+    (dict(ws=None, split=4), -4), (dict(ws=0x10010), -3),
+])
+def test_mxfp8_argument_validation(L, kw, status):
+    # lda / ldb count 8-bit elements (bytes): >= K and a multiple of 16.
+    assert _call_gemm8(L, **kw) == status
+
+
+def test_mxfp8_plan(L):
+    p = mx.mxfp8_plan_gemm(8192, 8192, 8192, 0, 152)
+    assert (p.tile_m, p.tile_n, p.tile_k, p.stages, p.pair, p.persistent) == (128, 256, 128, 4, 0, 0)
+    assert p.relayout_pass == 1
+    # The plan of an fp4 GEMM whose rows hold as many bytes (K doubled).
+    for M, N, K in [(1, 8192, 8192), (64, 7168, 16384), (512, 1024, 2048), (300, 520, 1024)]:
+        a = mx.mxfp8_plan_gemm(M, N, K, 0, 152).as_dict()
+        monkey = mx.mxfp4_plan_gemm(M, N, 2 * K, 0, 152).as_dict()
+        a.pop("tile_k"), monkey.pop("tile_k")
+        if not monkey["pair"] and not monkey["persistent"]:
+            assert a == monkey, (M, N, K)
+    # The kernel overrides do not apply to MXFP8.
+    assert mx.mxfp8_plan_gemm(8192, 8192, 8192, 0, 152).pair == 0
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp8_plan_gemm(128, 256, 48, 0, 152)
+    assert mx.mxfp8_gemm_workspace_size(128, 256, 512, 1) == 0
+    assert mx.mxfp8_gemm_workspace_size(8192, 8192, 8192, 0) == \
+        4096 + 2 * mx.mxfp4_scale_relayout_size(8192, 8192)
+
+
 def test_other_entry_points_validate_before_device(L):
     assert L.mxfp4_scale_relayout(None, 0x1000, 4, 64, 2, None) == -1
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 48, 2, None) == -1

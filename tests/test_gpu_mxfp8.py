@@ -1,0 +1,127 @@
+"""MXFP8 GEMM (E4M3 / E5M2 elements, one E8M0 scale per 32) on the GPU
+through the C ABI, element by element against the oracle.
+
+Bound, as for MXFP4: |D_gpu - D_ref| <= ulp_bf16(D_ref) + 2^-20 * sum|a_k b_k|.
+"""
+import numpy as np
+import pytest
+
+import block_scaled_mxfp4_gb300 as mx
+from block_scaled_mxfp4_gb300 import inputs
+from parity_util import assert_within_bound, bf16_bits_to_f64, d_to_bits, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+ABI_FMT = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2}
+ORACLE_FMT = {"e4m3": 1, "e5m2": 2}
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    from block_scaled_mxfp4_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+class Dev8:
+    """A problem's operands on the GPU."""
+
+    def __init__(self, p):
+        self.p = p
+        d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        self.A, self.B, self.SA, self.SB = d(p.A), d(p.B), d(p.SA), d(p.SB)
+        self.C = None
+        if p.C is not None:
+            self.C = d(np.ascontiguousarray(p.C).view(np.int16)).view(torch.bfloat16)
+
+
+def run8(dev, split_k=0):
+    p = dev.p
+    D = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = mx.mxfp8_gemm_workspace_size(p.M, p.N, p.K, split_k)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    C = dev.C if p.beta != 0.0 else None
+    mx.mxfp8_gemm(D, D.stride(0), C, 0 if C is None else C.stride(0), dev.A, dev.A.stride(0),
+                  dev.B, dev.B.stride(0), dev.SA, dev.SA.stride(0), dev.SB, dev.SB.stride(0),
+                  ABI_FMT[p.fmt_a], ABI_FMT[p.fmt_b], float(p.alpha), float(p.beta),
+                  p.M, p.N, p.K, split_k, ws if ws_bytes else None, ws_bytes)
+    torch.cuda.synchronize()
+    return d_to_bits(D)
+
+
+def oracle_full(oracle_mod, p):
+    D, _, sabs, inexact = oracle_mod.gemm8(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K,
+                                           ORACLE_FMT[p.fmt_a], ORACLE_FMT[p.fmt_b],
+                                           alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    return D, sabs
+
+
+# (M, N, K, fmt A, fmt B, alpha, beta, C sigma): one-tile configurations
+# 128x256, 128x128 and 128x64 tiles, swap-AB for M <= 64, K with a half-full
+# last stage (K % 128 != 0), ragged M and N, mixed formats, alpha / beta with C,
+# and a grid of more tiles than SMs (scales relaid in a separate pass).
+CASES = [
+    (128, 256, 512, "e4m3", "e4m3", 1.0, 0.0, None),
+    (300, 520, 1024, "e4m3", "e5m2", 0.5, 1.0, 1.0),
+    (1000, 700, 288, "e5m2", "e4m3", 1.0, 0.0, None),
+    (257, 300, 160, "e5m2", "e5m2", 2.0, 0.0, None),
+    (1, 4096, 2048, "e4m3", "e4m3", 1.0, 0.0, None),
+    (2, 1000, 1024, "e4m3", "e5m2", 1.0, 0.5, 0.1),
+    (33, 100, 384, "e4m3", "e4m3", 1.0, 0.0, None),
+    (64, 2048, 4096, "e5m2", "e4m3", 1.0, 1.0, 0.1),
+    (2000, 2600, 256, "e4m3", "e4m3", 1.0, 0.0, None),
+]
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb,alpha,beta,cs", CASES,
+                         ids=[f"{c[0]}x{c[1]}x{c[2]}-{c[3]}x{c[4]}" for c in CASES])
+def test_mxfp8_parity(oracle_mod, M, N, K, fa, fb, alpha, beta, cs):
+    p = inputs.make_problem8("p8", M, N, K, M + N + K, fa, fb, "normal", alpha, beta, cs)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p)), Dref, sabs, p.alpha, f"mxfp8 {M}x{N}x{K} {fa}x{fb}")
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_mxfp8_split_k(oracle_mod, split):
+    p = inputs.make_problem8("p8s", 48, 1536, 4096, 11, "e4m3", "e4m3", "normal", 1.0, 0.5, 1.0)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p), split_k=split), Dref, sabs, p.alpha, f"mxfp8 split {split}")
+
+
+def test_mxfp8_plan_uses_one_tile_kernel():
+    for M, N, K in [(8192, 8192, 8192), (1, 8192, 8192), (512, 1024, 2048)]:
+        p = mx.mxfp8_plan_gemm(M, N, K, 0, 0)
+        assert p.pair == 0 and p.persistent == 0 and p.gemv == 0 and p.tile_k == 128
+
+
+@pytest.mark.parametrize("name", ["decode8", "mixed8"])
+def test_mxfp8_workloads_full(oracle_mod, name):
+    p = inputs.workload8(name)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p)), Dref, sabs, p.alpha, name)
+
+
+def test_mxfp8_large_sampled(oracle_mod):
+    """The 8192^3 E4M3 workload, as the benchmark runs it, on sampled outputs."""
+    p = inputs.workload8("large8")
+    pairs = sample_pairs(p.M, p.N, 3000, 9)
+    Dr, _, sabs, inexact = oracle_mod.gemm8_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K,
+                                                    ORACLE_FMT[p.fmt_a], ORACLE_FMT[p.fmt_b],
+                                                    pairs, alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    D = run8(Dev8(p))
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "large8")
+    assert not np.isnan(bf16_bits_to_f64(D)).any()
+
+
+def test_mxfp8_nan_scale_propagates(oracle_mod):
+    """Scale code 0xFF (NaN) in one block of A row 3: that row is NaN, others not."""
+    p = inputs.make_problem8("nan8", 128, 256, 256, 5, "e4m3", "e4m3", "normal", 1.0, 0.0, None)
+    p.SA[3, 2] = 0xFF
+    D = bf16_bits_to_f64(run8(Dev8(p)))
+    assert np.isnan(D[3]).all()
+    assert not np.isnan(np.delete(D, 3, axis=0)).any()

@@ -93,7 +93,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large",
-                    choices=["tiny", "decode", "mid", "large", "skinny", "quantize"])
+                    choices=["tiny", "decode", "mid", "large", "skinny", "quantize",
+                             "large8", "decode8", "mixed8"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -192,8 +193,13 @@ def oracle_throughput(p, seconds, seed):
     def run(count):
         pairs = np.stack([rng.integers(0, p.M, count), rng.integers(0, p.N, count)], axis=1)
         t0 = time.perf_counter()
-        oracle.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs, alpha=p.alpha,
-                            beta=p.beta, C=p.C)
+        if hasattr(p, "fmt_a"):          # MXFP8 problem
+            fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+            oracle.gemm8_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, fmt[p.fmt_a], fmt[p.fmt_b],
+                                 pairs, alpha=p.alpha, beta=p.beta, C=p.C)
+        else:
+            oracle.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs, alpha=p.alpha,
+                                beta=p.beta, C=p.C)
         return time.perf_counter() - t0
 
     cores = oracle.host_cores()
@@ -215,7 +221,8 @@ def run_reference(args, rank):
     if args.workload == "quantize":
         run_reference_quantize(args)
         return
-    p = inputs.workload(args.workload)
+    fp8 = args.workload in inputs.WORKLOADS8
+    p = inputs.workload8(args.workload) if fp8 else inputs.workload(args.workload)
     per_step = 4.0 if args.steps <= 20 else max(0.5, 80.0 / args.steps)
     for i in range(args.warmup):
         oracle_throughput(p, min(per_step, 1.0), 1000 + i)
@@ -226,7 +233,7 @@ def run_reference(args, rank):
         times.append(t)
     value = len(vals) / sum(1.0 / v for v in vals)        # total FLOPs / total time
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": METRIC8 if fp8 else METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -238,6 +245,136 @@ def run_reference(args, rank):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+METRIC8 = "MXFP8 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP8 peak / HBM roofline"
+FP8_PER_BF16 = 2.0                   # nominal dense FP8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def run_mxfp8(args, world, rank, local_rank):
+    """--workload large8 | decode8 | mixed8: one mxfp8_gemm call per step
+    (scale relayout + one-tile tcgen05 GEMM, or split-K GEMM + reduce), device
+    timed with L2 flushed between steps; each rank of a multi-GPU launch runs
+    the whole problem as a replica."""
+    import numpy as np
+    import torch
+
+    import block_scaled_mxfp4_gb300 as mx
+    from block_scaled_mxfp4_gb300 import build, inputs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    p = inputs.workload8(args.workload)
+    M, N, K = p.M, p.N, p.K
+    fmt = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2}
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    A, B, SA, SB = d(p.A), d(p.B), d(p.SA), d(p.SB)
+    C = d(p.C.view(np.int16)).view(torch.bfloat16) if p.C is not None else None
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    split = args.split_k
+    plan = mx.mxfp8_plan_gemm(M, N, K, split, 0)
+    ws_bytes = mx.mxfp8_gemm_workspace_size(M, N, K, split)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    Cs = C if p.beta != 0.0 else None
+
+    def step():
+        mx.mxfp8_gemm(D, N, Cs, 0 if Cs is None else N, A, K, B, K, SA, K // 32, SB, K // 32,
+                      fmt[p.fmt_a], fmt[p.fmt_b], p.alpha, p.beta, M, N, K, split,
+                      ws if ws_bytes else None, ws_bytes, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    tot_ms = max_over_ranks([sum(e[0].elapsed_time(e[1]) for e in ev)], dist, dev)[0]
+    ms = tot_ms / args.steps
+    flops = 2.0 * M * N * K
+    nbytes = M * K + N * K + (M + N) * K // 32 + 2 * M * N + (2 * M * N if p.beta != 0.0 else 0)
+    value = world * flops * args.steps / (tot_ms * 1e-3) / 1e12
+    # end to end: operands from pinned host memory, D back to the host
+    pin = lambda t: t.cpu().pin_memory()
+    hA, hB, hSA, hSB = pin(A), pin(B), pin(SA), pin(SB)
+    hC = pin(C) if Cs is not None else None
+    hD = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for dst, src in ((A, hA), (B, hB), (SA, hSA), (SB, hSB)) + (((C, hC),) if hC is not None else ()):
+            dst.copy_(src, non_blocking=True)
+        step()
+        hD.copy_(D, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / args.e2e_steps], dist, dev)[0]
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    hbm_bound = M <= 64
+    kernels = ("scale_relayout_kernel + " if plan.relayout_pass else "") + \
+        f"gemm_mxf4_kernel<{plan.tile_n}, {plan.stages}, {'true' if plan.swap_ab else 'false'}, 1>" + \
+        (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
+    else:
+        peak = peaks["bf16_tflops"] * FP8_PER_BF16
+        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peak,
+                "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
+                               f"{FP8_PER_BF16:g} (nominal dense FP8/bf16 ratio)"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None,
+                 "traffic_source": "not captured for the MXFP8 kernels",
+                 "kernel": kernels + " (one mxfp8_gemm call, timed together)", "kernel_ms": ms,
+                 "algorithmic_bytes": nbytes, "flops": flops})
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_throughput(p, 10.0, 77)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hB, hSA, hSB) + ((hC,) if hC is not None else ()))
+    line = {
+        "metric": METRIC8, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": f"mxfp8 ({p.fmt_a} x {p.fmt_b})", "data": "synthetic",
+        "config": {"workload": f"{args.workload} M={M} N={N} K={K}", "M": M, "N": N, "K": K,
+                   "fmt_a": p.fmt_a, "fmt_b": p.fmt_b, "alpha": p.alpha, "beta": p.beta,
+                   "seed": p.seed, "split_k": plan.split_k, "swap_ab": plan.swap_ab,
+                   "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
+                   "grid": [plan.grid_x, plan.grid_y, plan.grid_z],
+                   "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "step": "one mxfp8_gemm call",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
+                "api": "mxfp8_gemm (pinned host copies around it)"},
+        "gpu_launches": args.steps * (1 + plan.relayout_pass + (1 if plan.split_k > 1 else 0)),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 QUANT_ROWS, QUANT_K = 8192, 8192     # the large GEMM's activations, bf16
@@ -397,6 +534,9 @@ def main():
         return
     if args.workload == "quantize":
         run_quantize(args, world, rank, local_rank)
+        return
+    if args.workload in ("large8", "decode8", "mixed8"):
+        run_mxfp8(args, world, rank, local_rank)
         return
 
     import numpy as np

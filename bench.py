@@ -343,8 +343,11 @@ def run_mxfp8(args, world, rank, local_rank):
                 "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
                                f"{FP8_PER_BF16:g} (nominal dense FP8/bf16 ratio)"}
-    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None,
-                 "traffic_source": "not captured for the MXFP8 kernels",
+    traffic = recorded_traffic(args.workload, "gemm_mxf4_kernel")
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic,
+                 "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one GEMM "
+                                    "launch (profiles/traffic.json)") if traffic else
+                                   "no capture for these sources",
                  "kernel": kernels + " (one mxfp8_gemm call, timed together)", "kernel_ms": ms,
                  "algorithmic_bytes": nbytes, "flops": flops})
     cpu = None

@@ -118,13 +118,17 @@ __device__ __forceinline__ void store_d_row(const GemmArgs &a, int m, int n0, fl
     }
     uint16_t *d = a.D + static_cast<int64_t>(m) * a.ldd + n0;
     if (a.vec32_ok && full) {
-        // 32-byte stores: half the store instructions of 16-byte ones.
+        // 32-byte stores: half the store instructions of 16-byte ones.  D is
+        // written once and not read back: evict-first, so it does not push
+        // the operand panels that other tiles still load out of L2.
+        const uint64_t pol = l2_policy_evict_first();
 #pragma unroll
         for (int i = 0; i < 32; i += 16)
-            st_global_v8(d + i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
-                         pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]),
-                         pack_bf16x2(v[i + 8], v[i + 9]), pack_bf16x2(v[i + 10], v[i + 11]),
-                         pack_bf16x2(v[i + 12], v[i + 13]), pack_bf16x2(v[i + 14], v[i + 15]));
+            st_global_v8_hint(d + i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
+                              pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]),
+                              pack_bf16x2(v[i + 8], v[i + 9]), pack_bf16x2(v[i + 10], v[i + 11]),
+                              pack_bf16x2(v[i + 12], v[i + 13]), pack_bf16x2(v[i + 14], v[i + 15]),
+                              pol);
     } else if (a.vec_ok && full) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8)
@@ -373,8 +377,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int p0 = blockIdx.x * kTileM;
-    const int q0 = blockIdx.y * BN;
+    // Tile of this CTA.  Launch order runs x fastest; consecutive CTAs walk a
+    // band of up to 8 tile columns (Q) before the next tile row (P), so the
+    // CTAs resident at once share a few P and Q panels in L2 instead of
+    // sweeping all of P for every column.
+    int pt, qt;
+    {
+        const int tp = static_cast<int>(gridDim.x), tq = static_cast<int>(gridDim.y);
+        const int lin = static_cast<int>(blockIdx.y) * tp + static_cast<int>(blockIdx.x);
+        const int band = tq < 8 ? tq : 8;
+        const int b = lin / (band * tp);
+        const int within = lin - b * band * tp;
+        const int bw = min(band, tq - b * band);
+        pt = within / bw;
+        qt = b * band + within % bw;
+    }
+    const int p0 = pt * kTileM;
+    const int q0 = qt * BN;
     const int z = blockIdx.z;
     const int kt0 = z * a.kt_per_split;
     const int nkt = min(a.kt_per_split, a.kt_total - kt0);

@@ -1,20 +1,25 @@
-"""Run the prepacked MXFP4 GEMM on one seeded random shape (for profilers).
+"""Run the GEMM on one seeded random shape (for profilers).
 
     python -m block_scaled_mxfp4_gb300.run_shape M N K [--calls C] [--seed S]
+                                                 [--format mxfp4|e4m3|e5m2]
 
-Draws random fp4x2 codes for A [M, K/2] and B [N, K/2] and E8M0 scales in
-[120, 127] on the current CUDA device, relays the scales out once with
-mxfp4_scale_relayout, then makes C calls of mxfp4_gemm_prepacked (alpha 1,
-beta 0) with the heuristic's plan, synchronising after the last.  Nothing is
-checked: this only gives a profiler a short program with a known number of
-GEMM launches.
+mxfp4 (default): random fp4x2 codes for A [M, K/2] and B [N, K/2] and E8M0
+scales in [120, 127] on the current CUDA device; the scales are relaid once
+with mxfp4_scale_relayout, then C calls of mxfp4_gemm_prepacked follow.
+e4m3 / e5m2: random 8-bit codes (the format's NaN codes avoided) for A
+[M, K] and B [N, K], C calls of mxfp8_gemm with row-major scales (each call
+relays them itself when its plan asks for it).  alpha 1, beta 0, the
+heuristic's plan, a synchronise after the last call.  Nothing is checked:
+this only gives a profiler a short program with a known number of GEMM
+launches.
 """
 import argparse
 
 import torch
 
-from . import (mxfp4_gemm_prepacked, mxfp4_gemm_prepacked_workspace_size, mxfp4_plan_gemm,
-               mxfp4_scale_relayout, mxfp4_scale_relayout_size)
+from . import (MXFP8_E4M3, MXFP8_E5M2, mxfp4_gemm_prepacked, mxfp4_gemm_prepacked_workspace_size,
+               mxfp4_plan_gemm, mxfp4_scale_relayout, mxfp4_scale_relayout_size, mxfp8_gemm,
+               mxfp8_gemm_workspace_size, mxfp8_plan_gemm)
 
 
 def main(argv=None):
@@ -24,10 +29,28 @@ def main(argv=None):
     ap.add_argument("K", type=int)
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--format", choices=["mxfp4", "e4m3", "e5m2"], default="mxfp4")
     args = ap.parse_args(argv)
     M, N, K = args.M, args.N, args.K
     dev = torch.device("cuda")
     g = torch.Generator(device=dev).manual_seed(args.seed)
+    if args.format != "mxfp4":
+        fmt = MXFP8_E4M3 if args.format == "e4m3" else MXFP8_E5M2
+        # Codes with exponent fields below the top: no NaN or infinity codes.
+        A = torch.randint(0, 0x70, (M, K), dtype=torch.uint8, device=dev, generator=g)
+        B = torch.randint(0, 0x70, (N, K), dtype=torch.uint8, device=dev, generator=g)
+        SA = torch.randint(120, 128, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)
+        SB = torch.randint(120, 128, (N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsb = mxfp8_gemm_workspace_size(M, N, K, 0)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        plan = mxfp8_plan_gemm(M, N, K, 0, 0)
+        for _ in range(args.calls):
+            mxfp8_gemm(D, N, None, N, A, K, B, K, SA, K // 32, SB, K // 32, fmt, fmt, 1.0, 0.0,
+                       M, N, K, 0, ws if wsb else None, wsb)
+        torch.cuda.synchronize()
+        print(f"{M}x{N}x{K} {args.format}: {args.calls} calls, plan {plan.as_dict()}")
+        return
     A = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev, generator=g)
     B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev, generator=g)
     SA = torch.randint(120, 128, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)

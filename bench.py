@@ -86,6 +86,21 @@ def recorded_traffic(workload, kernel):
     return rec["dram_bytes_read"] + rec["dram_bytes_write"]
 
 
+def reduce_kernel_runs(plan):
+    """Whether a plan's split-K runs the separate reduce kernel: its partials
+    need workspace (MXFP4_SPLIT_REDUCE=cluster reduces inside each tile's
+    cluster instead, with none)."""
+    return plan.split_k > 1 and plan.workspace_bytes > 0
+
+
+def split_note(plan):
+    if plan.split_k <= 1:
+        return ""
+    if reduce_kernel_runs(plan):
+        return " + split-K reduce (launched as its dependent)"
+    return f" (split-K reduced inside each tile's cluster of {plan.split_k} CTAs)"
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -333,7 +348,7 @@ def run_mxfp8(args, world, rank, local_rank):
     hbm_bound = M <= 64
     kernels = ("scale_relayout_kernel + " if plan.relayout_pass else "") + \
         f"gemm_mxf4_kernel<{plan.tile_n}, {plan.stages}, {'true' if plan.swap_ab else 'false'}, 1>" + \
-        (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
+        (" + splitk_reduce_kernel" if reduce_kernel_runs(plan) else "")
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
@@ -365,14 +380,14 @@ def run_mxfp8(args, world, rank, local_rank):
                    "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
                    "grid": [plan.grid_x, plan.grid_y, plan.grid_z],
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
-                   "step": "one mxfp8_gemm call",
+                   "step": "one mxfp8_gemm call" + split_note(plan),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "api": "mxfp8_gemm (pinned host copies around it)"},
-        "gpu_launches": args.steps * (1 + plan.relayout_pass + (1 if plan.split_k > 1 else 0)),
+        "gpu_launches": args.steps * (1 + plan.relayout_pass + (1 if reduce_kernel_runs(plan) else 0)),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -637,7 +652,7 @@ def main():
     ms_per_step = tot_ms / args.steps
     value = replica_throughput(world, flops, args.steps, tot_ms)
     launches_per_step = (2 if plan.relayout_pass or args.prepacked else 1) + \
-        (1 if plan.split_k > 1 else 0)
+        (1 if reduce_kernel_runs(plan) else 0)
 
     # ---- end to end: host buffers through the C ABI, copies in the timed region
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -713,7 +728,7 @@ def main():
                               if roof["traffic"] is not None else None)
     if stream_floor is not None:
         roof["stream_floor"] = stream_floor
-    roof["kernel"] = (kname + (" + splitk_reduce_kernel" if plan.split_k > 1 else "")
+    roof["kernel"] = (kname + (" + splitk_reduce_kernel" if reduce_kernel_runs(plan) else "")
                       + (" (GEMM alone on relaid scales, timed in its own loop)"
                          if gemm_alone else " (scale layout built in-kernel)"))
     roof["kernel_ms"] = gemm_avg
@@ -741,8 +756,7 @@ def main():
                             "on relaid scales (launched as its dependent)"
                             if plan.relayout_pass else
                             "one mxfp4_gemm call: GEMM with in-kernel scale layout")
-                           + (" + split-K reduce (launched as its dependent)"
-                              if plan.split_k > 1 else ""),
+                           + split_note(plan),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -19,6 +19,7 @@ using namespace mxfp4;
 namespace {
 
 constexpr int kMaxSplit = 16;
+constexpr int kMaxClusterSplit = 8;   // splits that can reduce inside one (portable) cluster
 constexpr int kDefaultSms = 152;
 constexpr size_t kAlign = 256;
 
@@ -235,6 +236,14 @@ KernelChoice kernel_override()
 
 // fp8: plan an MXFP8 GEMM whose rows hold as many bytes as this K of fp4
 // elements (the caller passes twice its 8-bit K): the one-tile kernel only.
+// MXFP4_SPLIT_REDUCE=cluster: reduce split-K partials inside each tile's
+// cluster (read at each call; tuning and tests only).
+bool split_reduce_cluster()
+{
+    const char *env = std::getenv("MXFP4_SPLIT_REDUCE");
+    return env && std::strcmp(env, "cluster") == 0;
+}
+
 int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape,
               bool fp8 = false)
 {
@@ -337,9 +346,17 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     out->grid_x = static_cast<int>(gx);
     out->grid_y = static_cast<int>(gy);
     out->grid_z = split;
-    size_t partials = split > 1 ? static_cast<size_t>(split) * static_cast<size_t>(M) *
-                                      static_cast<size_t>(N) * sizeof(float)
-                                : 0;
+    // Split-K partials go to fp32 workspace and a fixed-order reduce kernel;
+    // with MXFP4_SPLIT_REDUCE=cluster (up to kMaxClusterSplit splits) the
+    // splits of a tile form one cluster and reduce through distributed shared
+    // memory instead, with no workspace.  That form measured slower on GB300
+    // (decode 22 vs 19 us, skinny 56 vs 26 us: clusters of 4-5 CTAs at two
+    // CTAs per SM co-schedule fewer tiles), so it is an option only.
+    const bool cluster_reduce = split > 1 && split <= kMaxClusterSplit && split_reduce_cluster();
+    size_t partials = (split > 1 && !cluster_reduce)
+                          ? static_cast<size_t>(split) * static_cast<size_t>(M) *
+                                static_cast<size_t>(N) * sizeof(float)
+                          : 0;
     // Persistent stream-K over all resident CTA slots (override only).
     out->persistent = persistent ? 1 : 0;
     out->ctas = 0;
@@ -439,6 +456,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         shape->pair_cluster = pair_cluster;
         shape->pair_kc = pair_kc;
         shape->fp8 = fp8 ? 1 : 0;
+        shape->split_cluster = (!out->persistent && !use_pair && !use_gemv && cluster_reduce) ? 1 : 0;
     }
     return MXFP4_OK;
 }
@@ -610,6 +628,10 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.D = static_cast<uint16_t *>(D);
     a.ldd = ldd;
     a.ws = partials;
+    a.cluster_split = (!shape.persistent && plan.split_k > 1 && plan.split_k <= kMaxClusterSplit &&
+                       shape.split_cluster)
+                          ? plan.split_k
+                          : 0;
     a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
                (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
     a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
@@ -654,7 +676,9 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     if (launch_gemm(a, tmP, tmQ, shape, grid, stream) != cudaSuccess)
         return MXFP4_ERR_CUDA;
-    if (plan.split_k > 1) {
+    if (plan.split_k > 1 && !a.cluster_split) {
+        if (!partials)
+            return MXFP4_ERR_WORKSPACE;
         if (launch_splitk_reduce(partials, plan.split_k, M, N, alpha, beta, a.C, ldc, a.D, ldd, sms,
                                  stream) != cudaSuccess)
             return MXFP4_ERR_CUDA;

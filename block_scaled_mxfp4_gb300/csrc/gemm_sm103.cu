@@ -77,6 +77,11 @@ struct Cfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(G == 1 || G == 2, "scale groups per stage");
+    // Cluster split-K: the fp32 partial tile parked in the idle ring, rows
+    // padded by 4 floats (16-byte vector stores without bank conflicts).
+    static constexpr int PART_STRIDE = BN + 4;
+    static constexpr int PART_BYTES = kTileM * PART_STRIDE * 4;
+    static_assert(PART_BYTES <= STAGES * STAGE_BYTES, "partial tile fits the ring");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -623,7 +628,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------ epilogue --
         bool ok = nkt > 0 && mbar_wait(acc_full, 0, abort_flag, a.wait_limit, &g_device_status);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        if (a.cluster_split > 1) {
+            // Park this split's fp32 partial (valid columns, rounded up to
+            // 32) in the ring, which the MMAs no longer read; the cluster
+            // reduces the partials below.
+            float *part = reinterpret_cast<float *>(smem);
+            const int row = warp * 32 + lane;
+            const int cols = SWAP ? min(BN, a.M - q0) : min(BN, a.N - q0);
+            const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+            if (ok)
+                tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < cols; c0 += 32) {
+                uint32_t r[32];
+                if (ok) {
+                    tmem_ld_32x32b_x32(t_row + c0, r);
+                    tmem_ld_wait(r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = 0u;
+                }
+                float *dst = part + row * Cf::PART_STRIDE + c0;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<uint4 *>(dst + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+            }
+        } else if (ok) {
             tc_fence_after();
             const int row = warp * 32 + lane;
             const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -643,6 +674,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
+    }
+
+    if (a.cluster_split > 1) {
+        // Split-K inside the cluster: rank r of the S CTAs of this tile sums
+        // rows r, r + S, ... of all S partials in rank order (the order of the
+        // separate reduce kernel) and stores them as D.  Barrier 1 makes the
+        // partials visible; barrier 2 keeps every CTA's shared memory alive
+        // until its peers have read it.
+        tc_fence_before();
+        cluster_sync();
+        const int S = a.cluster_split;
+        const int rank = static_cast<int>(cluster_ctarank());
+        const int row = warp * 32 + lane;
+        if (warp < 4 && row % S == rank) {
+            const int cols = SWAP ? min(BN, a.M - q0) : min(BN, a.N - q0);
+            const uint32_t mine = smem_addr(smem) + static_cast<uint32_t>(row * Cf::PART_STRIDE * 4);
+#pragma unroll 1
+            for (int c0 = 0; c0 < cols; c0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = 0.0f;
+#pragma unroll 1
+                for (int j = 0; j < S; ++j) {
+                    const uint32_t src = map_to_rank(mine, static_cast<uint32_t>(j)) + c0 * 4;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 x = ld_dsmem_v4(src + i * 4);
+                        v[i] += x.x;
+                        v[i + 1] += x.y;
+                        v[i + 2] += x.z;
+                        v[i + 3] += x.w;
+                    }
+                }
+                if (!SWAP) {
+                    const int m = p0 + row;
+                    if (m < a.M)
+                        store_d_row(a, m, q0 + c0, v);
+                } else {
+                    store_d_col(a, q0 + c0, p0 + row, v);
+                }
+            }
+        }
+        cluster_sync();
     }
 
     tc_fence_before();
@@ -679,6 +754,24 @@ static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const C
         if (e != cudaSuccess)
             return e;
         configured[dev] = 1;
+    }
+    if (a.cluster_split > 1) {
+        // The split_k CTAs of a tile (grid z) form one cluster.
+        if (static_cast<int>(grid.z) != a.cluster_split || a.cluster_split > 8)
+            return cudaErrorInvalidConfiguration;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = static_cast<unsigned>(a.cluster_split);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, a, tmP, tmQ);
     }
     kern<<<grid, kGemmThreads, Cf::SMEM_BYTES, stream>>>(a, tmP, tmQ);
     return cudaGetLastError();

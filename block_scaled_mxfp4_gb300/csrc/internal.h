@@ -51,6 +51,8 @@ struct GemmArgs {
     long long wait_limit;   // SM cycles before a wait gives up
     uint32_t idesc8;        // fp8: kind::mxf8f6f4 instruction descriptor (set at launch)
     int fmt_p, fmt_q;       // fp8: element types of P and Q (0 = E4M3, 1 = E5M2)
+    int cluster_split;      // > 1: the split_k CTAs of a tile form one cluster and reduce
+                            // their partials through distributed shared memory (no ws)
 };
 
 struct GemmShape {
@@ -66,6 +68,7 @@ struct GemmShape {
     int pair_kc;            // pair kernel: 256-K chunks per pipeline stage (1 or 2)
     int gemv;               // 1: GEMV kernel for M <= 2 (gemv.cu)
     int fp8;                // 1: 8-bit elements (one-tile kernel, kind::mxf8f6f4)
+    int split_cluster;      // 1: split-K reduced inside each tile's cluster (no partials)
 };
 
 // Work schedule of the persistent stream-K kernel.  Tile t (raster below)

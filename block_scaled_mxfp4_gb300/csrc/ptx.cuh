@@ -448,6 +448,18 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
     return d;
 }
 
+// 16-byte load from the shared memory of a CTA of this cluster (a
+// shared::cluster address, e.g. from map_to_rank).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t caddr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(caddr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"

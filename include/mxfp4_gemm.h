@@ -101,7 +101,13 @@ typedef struct mxfp4_plan {
  * overlap the previous tile's drain; default 256, one accumulator);
  * MXFP4_PAIR_CLUSTER = 2 puts two pairs on adjacent tiles in one cluster that
  * share their A panel by TMA multicast (default 1); MXFP4_PAIR_KS = 512 uses
- * three 512-K pipeline stages instead of six 256-K ones.  num_sms = 0
+ * three 512-K pipeline stages instead of six 256-K ones.
+ * MXFP4_SPLIT_REDUCE = cluster (any kernel choice, splits 2..8): the splits
+ * of a tile form one thread-block cluster and sum their fp32 partials
+ * through distributed shared memory in split order (bit-identical to the
+ * default two-launch form, no workspace); the default writes partials to
+ * the workspace and reduces them in a second, dependent launch, which
+ * measured faster.  num_sms = 0
  * uses the current device's SM count (or 152 when no device is visible).
  * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
  */

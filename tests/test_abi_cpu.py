@@ -127,6 +127,16 @@ def test_plan_pair_override(L, monkeypatch):
     assert mx.mxfp4_plan_gemm(128, 8192, 8192, 0, 152).pair == 0
 
 
+def test_plan_cluster_split_reduce(L, monkeypatch):
+    # MXFP4_SPLIT_REDUCE=cluster: up to 8 splits reduce inside each tile's
+    # cluster and need no partials; 16 still do.
+    monkeypatch.setenv("MXFP4_SPLIT_REDUCE", "cluster")
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 0
+    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152).workspace_bytes == 0
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 16) == 4096 + 16 * 8192 * 4
+    assert mx.mxfp8_gemm_workspace_size(1, 8192, 8192, 4) == 0
+
+
 def test_plan_pair_tile_n_192(L, monkeypatch):
     monkeypatch.setenv("MXFP4_KERNEL", "pair")
     monkeypatch.setenv("MXFP4_PAIR_N", "192")
@@ -223,7 +233,10 @@ def _call_gemm(L, **kw):
     (dict(beta=1.0), -1), (dict(beta=1.0, C=0x6000, ldc=100), -1),
     (dict(split=17), -1), (dict(split=-1), -1),
     (dict(lda=528), -3), (dict(ldb=520), -3), (dict(A=0x2008), -3), (dict(B=0x3004), -3),
-    (dict(ws=None, split=4), -4), (dict(ws=0x10010), -3), (dict(wsb=1000, split=2), -4),
+    # Splits beyond 8 keep fp32 partials in the workspace (K = 4096: 16 stages).
+    (dict(ws=None, split=16, K=4096, lda=4096, ldb=4096, ld_sa=128, ld_sb=128), -4),
+    (dict(ws=0x10010), -3),
+    (dict(wsb=1000, split=16, K=4096, lda=4096, ldb=4096, ld_sa=128, ld_sb=128), -4),
 ])
 def test_gemm_argument_validation(L, kw, status):
     # These return before any device call, so they run without a GPU.
@@ -249,7 +262,8 @@ def _call_gemm8(L, **kw):
     (dict(lda=500), -1), (dict(ldb=256), -1), (dict(ld_sa=15), -1),
     (dict(beta=1.0), -1), (dict(split=17), -1),
     (dict(lda=520), -3), (dict(ldb=536), -3), (dict(A=0x2008), -3),
-    (dict(ws=None, split=4), -4), (dict(ws=0x10010), -3),
+    (dict(ws=None, split=16, K=2048, lda=2048, ldb=2048, ld_sa=64, ld_sb=64), -4),
+    (dict(ws=0x10010), -3),
 ])
 def test_mxfp8_argument_validation(L, kw, status):
     # lda / ldb count 8-bit elements (bytes): >= K and a multiple of 16.

@@ -276,6 +276,21 @@ def test_strides_and_in_place(oracle_mod):
     assert np.all(d_to_bits(DC[:, N:]) == 0)
 
 
+@pytest.mark.parametrize("name,split", [("decode", 2), ("decode", 4), ("decode", 8),
+                                        ("skinny", 5), ("mid", 2)])
+def test_cluster_split_reduce_matches_reduce_kernel(monkeypatch, name, split):
+    """MXFP4_SPLIT_REDUCE=cluster: the splits of a tile sum through
+    distributed shared memory in the reduce kernel's order, so D is
+    bit-identical to the two-launch form (whose parity the sweeps check)."""
+    p = problem(name)
+    dev = Dev(p)
+    ref = run_gemm(dev, split_k=split)
+    monkeypatch.setenv("MXFP4_SPLIT_REDUCE", "cluster")
+    assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, split, 0).workspace_bytes == 0
+    got = run_gemm(dev, split_k=split)
+    assert np.array_equal(got, ref)
+
+
 def test_split_k_is_deterministic():
     p = problem("decode") if "decode" in _PROBLEMS else inputs.workload("decode")
     dev = Dev(p)
@@ -313,16 +328,20 @@ def test_prepacked_and_host_entry_points_match():
 
 
 def test_device_errors_are_reported():
-    p = problem("tiny")
-    dev = Dev(p)
-    D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
-    need = mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 2)     # split-K partials
+    # Split-K keeps fp32 partials in the workspace: one byte short is an error.
+    q = inputs.make_problem("ws16", 256, 512, 4096, 3, "normal", 1.0, 0.0, None)
+    dq = Dev(q)
+    Dq = torch.empty((q.M, q.N), dtype=torch.bfloat16, device="cuda")
+    need = mx.mxfp4_gemm_workspace_size(q.M, q.N, q.K, 16)
     assert need > 0
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     with pytest.raises(mx.Mxfp4Error) as e:
-        mx.mxfp4_gemm(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32, dev.SB,
-                      p.K // 32, 1.0, 0.0, p.M, p.N, p.K, 2, ws, need - 1)
+        mx.mxfp4_gemm(Dq, q.N, None, 0, dq.A, q.K, dq.B, q.K, dq.SA, q.K // 32, dq.SB,
+                      q.K // 32, 1.0, 0.0, q.M, q.N, q.K, 16, ws, need - 1)
     assert e.value.status == -4
+    p = problem("tiny")
+    dev = Dev(p)
+    D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
     # Without split the GEMM needs no workspace at all.
     assert mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 1) == 0
     mx.mxfp4_gemm(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32, dev.SB,
@@ -502,20 +521,28 @@ def test_gemv_strided_operands(force_gemv, oracle_mod):
 
 # ------------------------------------------------------ split-K reduce --
 
-def test_splitk_reduce_kernel_for_large_grids(oracle_mod):
-    """A wide grid (over 1000 output tiles) split two ways: the fixed-order
-    fp32 reduce completes every tile (same bound, sampled)."""
-    M, N, K = 4224, 8192, 512
-    p = inputs.make_problem("wide", M, N, K, seed=9, values="normal", alpha=1.0, beta=0.0,
-                            c_sigma=None)
-    plan = mx.mxfp4_plan_gemm(M, N, K, 2, 0)
-    assert plan.split_k == 2 and plan.grid_x * plan.grid_y > 1024
-    pairs = sample_pairs(M, N, 3000, 11)
-    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
-                                                   alpha=p.alpha, beta=p.beta, C=p.C)
-    assert inexact == 0
-    D = run_gemm(Dev(p), split_k=2)
-    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "wide s=2")
+@pytest.mark.parametrize("split,mode", [(2, "kernel"), (10, "kernel"), (2, "cluster")])
+def test_splitk_for_large_grids(oracle_mod, monkeypatch, split, mode):
+    """A wide grid (over 1000 output tiles), its splits reduced by the
+    fixed-order reduce kernel or inside each tile's cluster; every tile
+    completes (same bound, sampled)."""
+    if mode == "cluster":
+        monkeypatch.setenv("MXFP4_SPLIT_REDUCE", "cluster")
+    M, N, K = 4224, 8192, 2560
+    if "wide" not in _PROBLEMS:
+        p = inputs.make_problem("wide", M, N, K, seed=9, values="normal", alpha=1.0, beta=0.0,
+                                c_sigma=None)
+        pairs = sample_pairs(M, N, 3000, 11)
+        Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
+                                                       alpha=p.alpha, beta=p.beta, C=p.C)
+        assert inexact == 0
+        _PROBLEMS["wide"] = (p, Dev(p), pairs, Dr, sabs)
+    p, dev, pairs, Dr, sabs = _PROBLEMS["wide"]
+    plan = mx.mxfp4_plan_gemm(M, N, K, split, 0)
+    assert plan.split_k == split and plan.grid_x * plan.grid_y > 1024
+    assert (plan.workspace_bytes > 0) == (mode == "kernel")
+    D = run_gemm(dev, split_k=split)
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, f"wide s={split}")
 
 
 @pytest.mark.parametrize("kernel", ["auto", "pair"])

@@ -929,16 +929,73 @@ size_t mxfp8_gemm_workspace_size(int M, int N, int K, int split_k)
     return ws;
 }
 
+// Rows per panel of the pipelined host call: eight panels of a multiple of
+// 256 rows once M reaches 2048 (each panel still fills the GPU with 256-row
+// pair tiles); one panel below that.
+static int host_panel_rows(int M)
+{
+    if (M < 2048)
+        return M;
+    const int rows = (M + 7) / 8;
+    return (rows + 255) / 256 * 256;
+}
+
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
 {
-    const size_t ws = mxfp4_gemm_workspace_size(M, N, K, split_k);
     if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_k < 0 || split_k > kMaxSplit)
         return 0;
+    // Workspace of the panel GEMMs: the largest over the panel shapes.
+    const int mp = host_panel_rows(M);
+    size_t ws = mxfp4_gemm_workspace_size(mp, N, K, split_k);
+    const int last = M - (M - 1) / mp * mp;
+    const size_t ws_last = mxfp4_gemm_workspace_size(last, N, K, split_k);
+    ws = ws > ws_last ? ws : ws_last;
     const size_t mn2 = align_up(static_cast<size_t>(M) * N * 2);
     return align_up(static_cast<size_t>(M) * K / 2) + align_up(static_cast<size_t>(N) * K / 2) +
            align_up(static_cast<size_t>(M) * K / 32) + align_up(static_cast<size_t>(N) * K / 32) +
            (with_c ? mn2 : 0) + mn2 + ws;
 }
+
+namespace {
+
+// Per-device copy streams and events of the pipelined host call, created on
+// first use and reused under a lock (a later record of an event does not
+// affect waits enqueued before it).
+constexpr int kHostMaxPanels = 8;
+struct HostPipe {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, operands = nullptr, done = nullptr;
+    cudaEvent_t in[kHostMaxPanels] = {}, out[kHostMaxPanels] = {};
+    std::mutex lock;
+};
+
+HostPipe *host_pipe(int dev)
+{
+    static HostPipe pipes[64];
+    static std::mutex init_lock;
+    if (dev < 0 || dev >= 64)
+        return nullptr;
+    HostPipe *p = &pipes[dev];
+    std::lock_guard<std::mutex> g(init_lock);
+    if (!p->h2d) {
+        auto ev = [](cudaEvent_t *e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming); };
+        if (cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+            ev(&p->start) != cudaSuccess || ev(&p->operands) != cudaSuccess ||
+            ev(&p->done) != cudaSuccess) {
+            p->h2d = nullptr;
+            return nullptr;
+        }
+        for (int i = 0; i < kHostMaxPanels; ++i)
+            if (ev(&p->in[i]) != cudaSuccess || ev(&p->out[i]) != cudaSuccess) {
+                p->h2d = nullptr;
+                return nullptr;
+            }
+    }
+    return p;
+}
+
+}  // namespace
 
 int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
                     const void *scaleA_host, const void *scaleB_host, float alpha, float beta,
@@ -951,8 +1008,6 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
         return MXFP4_ERR_INVALID_ARG;
     if (beta != 0.0f && !C_host)
         return MXFP4_ERR_INVALID_ARG;
-    if ((K % 32) != 0)
-        return MXFP4_ERR_MISALIGNED;
     if (!aligned(device_arena, kAlign))
         return MXFP4_ERR_MISALIGNED;
     const int with_c = beta != 0.0f;
@@ -962,10 +1017,18 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
     int st = check_device();
     if (st != MXFP4_OK)
         return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    HostPipe *pipe = host_pipe(dev);
+    if (!pipe)
+        return MXFP4_ERR_CUDA;
     uint8_t *p = static_cast<uint8_t *>(device_arena);
-    const size_t a_b = static_cast<size_t>(M) * K / 2, b_b = static_cast<size_t>(N) * K / 2;
-    const size_t sa_b = static_cast<size_t>(M) * K / 32, sb_b = static_cast<size_t>(N) * K / 32;
-    const size_t mn2 = static_cast<size_t>(M) * N * 2;
+    const size_t arow = static_cast<size_t>(K) / 2, srow = static_cast<size_t>(K) / 32;
+    const size_t drow = static_cast<size_t>(N) * 2;
+    const size_t a_b = static_cast<size_t>(M) * arow, b_b = static_cast<size_t>(N) * arow;
+    const size_t sa_b = static_cast<size_t>(M) * srow, sb_b = static_cast<size_t>(N) * srow;
+    const size_t mn2 = static_cast<size_t>(M) * drow;
     uint8_t *dA = p;
     p += align_up(a_b);
     uint8_t *dB = p;
@@ -984,17 +1047,49 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
     uint8_t *ws = p;
     const size_t ws_bytes = arena_bytes - static_cast<size_t>(p - static_cast<uint8_t *>(device_arena));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(dA, A_host, a_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dB, B_host, b_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dSA, scaleA_host, sa_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dSB, scaleB_host, sb_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        (with_c && cudaMemcpyAsync(dC, C_host, mn2, cudaMemcpyHostToDevice, s) != cudaSuccess))
+    const auto *hA = static_cast<const uint8_t *>(A_host);
+    const auto *hSA = static_cast<const uint8_t *>(scaleA_host);
+    const auto *hC = static_cast<const uint8_t *>(C_host);
+    auto *hD = static_cast<uint8_t *>(D_host);
+
+    // Row panels: B and its scales go over first, then panel i's rows of A,
+    // its scales and C on the copy-in stream; the GEMM of panel i runs on
+    // `stream` once they landed; its D rows go back on the copy-out stream
+    // while the next panel computes.  The copy streams start after the work
+    // already on `stream` and `stream` ends after the last copy of D.
+    const int mp = host_panel_rows(M);
+    const int panels = (M + mp - 1) / mp;
+    std::lock_guard<std::mutex> g(pipe->lock);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!ok(cudaEventRecord(pipe->start, s)) || !ok(cudaStreamWaitEvent(pipe->h2d, pipe->start, 0)) ||
+        !ok(cudaStreamWaitEvent(pipe->d2h, pipe->start, 0)) ||
+        !ok(cudaMemcpyAsync(dB, B_host, b_b, cudaMemcpyHostToDevice, pipe->h2d)) ||
+        !ok(cudaMemcpyAsync(dSB, scaleB_host, sb_b, cudaMemcpyHostToDevice, pipe->h2d)) ||
+        !ok(cudaEventRecord(pipe->operands, pipe->h2d)) ||
+        !ok(cudaStreamWaitEvent(s, pipe->operands, 0)))
         return MXFP4_ERR_CUDA;
-    st = mxfp4_gemm(dD, N, dC, N, dA, K, dB, K, dSA, K / 32, dSB, K / 32, alpha, beta, M, N, K,
-                    split_k, ws, ws_bytes, stream);
-    if (st != MXFP4_OK)
-        return st;
-    if (cudaMemcpyAsync(D_host, dD, mn2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    for (int i = 0; i < panels; ++i) {
+        const size_t m0 = static_cast<size_t>(i) * mp;
+        const int rows = static_cast<int>(M - m0 < static_cast<size_t>(mp) ? M - m0 : mp);
+        if (!ok(cudaMemcpyAsync(dA + m0 * arow, hA + m0 * arow, rows * arow, cudaMemcpyHostToDevice,
+                                pipe->h2d)) ||
+            !ok(cudaMemcpyAsync(dSA + m0 * srow, hSA + m0 * srow, rows * srow,
+                                cudaMemcpyHostToDevice, pipe->h2d)) ||
+            (with_c && !ok(cudaMemcpyAsync(dC + m0 * drow, hC + m0 * drow, rows * drow,
+                                           cudaMemcpyHostToDevice, pipe->h2d))) ||
+            !ok(cudaEventRecord(pipe->in[i], pipe->h2d)) || !ok(cudaStreamWaitEvent(s, pipe->in[i], 0)))
+            return MXFP4_ERR_CUDA;
+        st = mxfp4_gemm(dD + m0 * drow, N, with_c ? dC + m0 * drow : nullptr, N, dA + m0 * arow, K,
+                        dB, K, dSA + m0 * srow, K / 32, dSB, K / 32, alpha, beta, rows, N, K, split_k,
+                        ws, ws_bytes, stream);
+        if (st != MXFP4_OK)
+            return st;
+        if (!ok(cudaEventRecord(pipe->out[i], s)) || !ok(cudaStreamWaitEvent(pipe->d2h, pipe->out[i], 0)) ||
+            !ok(cudaMemcpyAsync(hD + m0 * drow, dD + m0 * drow, rows * drow, cudaMemcpyDeviceToHost,
+                                pipe->d2h)))
+            return MXFP4_ERR_CUDA;
+    }
+    if (!ok(cudaEventRecord(pipe->done, pipe->d2h)) || !ok(cudaStreamWaitEvent(s, pipe->done, 0)))
         return MXFP4_ERR_CUDA;
     return MXFP4_OK;
 }

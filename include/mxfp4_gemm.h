@@ -223,8 +223,14 @@ size_t mxfp4_gemm_prepacked_workspace_size(int M, int N, int K, int split_k);
 /*
  * End-to-end call on HOST buffers: copies A, B, scaleA, scaleB (and C when
  * beta != 0) from host memory into `device_arena`, runs mxfp4_gemm there and
- * copies D back to host memory, all enqueued on `stream` (cudaMemcpyAsync
- * per buffer; pinned host memory makes the copies asynchronous).  Host
+ * copies D back to host memory.  For M >= 2048 the rows go in eight panels
+ * (multiples of 256 rows) so the copies overlap the compute: B and its
+ * scales are copied first, then each panel's A, scales and C rows on an
+ * internal copy stream; each panel's GEMM runs on `stream`; its D rows return
+ * on a second internal copy stream while the next panel computes.  The
+ * internal streams start after the work already enqueued on `stream`, and
+ * `stream` waits for the last copy of D, so the call is ordered on `stream`
+ * as a whole (pinned host memory makes the copies asynchronous).  Host
  * arrays are dense (ld = K for A/B, K/32 for scales, N for C/D).  The call
  * returns after enqueueing; synchronise `stream` before reading D_host.
  * device_arena: >= mxfp4_gemm_host_arena_size(M, N, K, split_k, beta != 0)

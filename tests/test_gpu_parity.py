@@ -327,6 +327,32 @@ def test_prepacked_and_host_entry_points_match():
     assert np.array_equal(hD.numpy().view(np.uint16), ref)
 
 
+def test_host_entry_pipelined_panels(oracle_mod):
+    """Host buffers with M >= 2048: the call copies B once, then pipelines row
+    panels (copy in, GEMM, copy out on separate streams).  2304 rows make five
+    panels of 512 / 256 rows; with split_k = 1 each panel runs the same kernel
+    and K order as the whole matrix, so D matches the device call bit for bit."""
+    M, N, K = 2304, 1024, 1024
+    p = inputs.make_problem("panels", M, N, K, seed=21, values="normal", alpha=0.5, beta=0.5,
+                            c_sigma=1.0)
+    ref = run_gemm(Dev(p), split_k=1)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hA, hB, hSA, hSB = pin(p.A), pin(p.B), pin(p.SA), pin(p.SB)
+    hC = pin(p.C.view(np.int16))
+    hD = torch.zeros((M, N), dtype=torch.int16).pin_memory()
+    arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, 1, True)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm_host(hD, hC, hA, hB, hSA, hSB, p.alpha, p.beta, M, N, K, 1, arena, arena_b)
+    torch.cuda.synchronize()
+    got = hD.numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    pairs = sample_pairs(M, N, 2000, 21)
+    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
+                                                   alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    assert_within_bound(got[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "host panels")
+
+
 def test_device_errors_are_reported():
     # Split-K keeps fp32 partials in the workspace: one byte short is an error.
     q = inputs.make_problem("ws16", 256, 512, 4096, 3, "normal", 1.0, 0.0, None)

@@ -22,7 +22,8 @@ __all__ = [
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
-    "mxfp8_gemm", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size", "MXFP8_E4M3", "MXFP8_E5M2",
+    "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
+    "mxfp8_gemm_prepacked_workspace_size", "MXFP8_E4M3", "MXFP8_E5M2",
     "gemm", "Plan",
 ]
 
@@ -89,6 +90,9 @@ def lib() -> ctypes.CDLL:
                                  f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp8_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                  i32, i32, f32, f32, i32, i32, i32, i32, vp, sz, vp]),
+            "mxfp8_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, i32, i32,
+                                           f32, f32, i32, i32, i32, i32, vp, sz, vp]),
+            "mxfp8_gemm_prepacked_workspace_size": (sz, [i32, i32, i32, i32]),
             "mxfp8_plan_gemm": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]),
             "mxfp8_gemm_workspace_size": (sz, [i32, i32, i32, i32]),
             "mxfp4_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
@@ -199,6 +203,21 @@ def mxfp8_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, fmt
                                    ld_sa, _p(scaleB), ld_sb, fmt_a, fmt_b, alpha, beta, M, N, K,
                                    split_k, _p(workspace), workspace_bytes, _stream(stream)),
                   "mxfp8_gemm")
+
+
+def mxfp8_gemm_prepacked(D, ldd, C, ldc, A, lda, B, ldb, scaleA_relaid, scaleB_relaid, fmt_a,
+                         fmt_b, alpha, beta, M, N, K, split_k, workspace, workspace_bytes,
+                         stream=None):
+    """MXFP8 GEMM on scales relaid by mxfp4_scale_relayout (with this K)."""
+    return _check(lib().mxfp8_gemm_prepacked(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb,
+                                             _p(scaleA_relaid), _p(scaleB_relaid), fmt_a, fmt_b,
+                                             alpha, beta, M, N, K, split_k, _p(workspace),
+                                             workspace_bytes, _stream(stream)),
+                  "mxfp8_gemm_prepacked")
+
+
+def mxfp8_gemm_prepacked_workspace_size(M, N, K, split_k=0) -> int:
+    return lib().mxfp8_gemm_prepacked_workspace_size(M, N, K, split_k)
 
 
 def mxfp8_plan_gemm(M, N, K, split_k=0, num_sms=0) -> Plan:

@@ -785,15 +785,16 @@ int mxfp4_scale_relayout2(void *dst_a, const void *src_a, int rows_a, int64_t ld
 }
 
 // Shared body of mxfp4_gemm and mxfp4_gemm_prepacked after their own checks.
+// fp8: K counts 8-bit elements (the plan is that of an fp4 GEMM of 2K).
 static int gemm_entry(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
                       const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M,
                       int N, int K, int split_k, void *workspace, size_t workspace_bytes,
-                      void *stream)
+                      void *stream, bool fp8 = false, int fmt_a = 0, int fmt_b = 0)
 {
     const int sms = device_sms_or_default();
     mxfp4_plan plan;
     GemmShape shape;
-    int st = make_plan(M, N, K, split_k, sms, &plan, &shape);
+    int st = make_plan(M, N, fp8 ? 2 * K : K, split_k, sms, &plan, &shape, fp8);
     if (st != MXFP4_OK)
         return st;
     if (plan.workspace_bytes > 0) {
@@ -807,7 +808,7 @@ static int gemm_entry(void *D, int64_t ldd, const void *C, int64_t ldc, const vo
         return st;
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
                     plan.workspace_bytes ? static_cast<uint8_t *>(workspace) : nullptr, sms,
-                    static_cast<cudaStream_t>(stream));
+                    static_cast<cudaStream_t>(stream), false, fmt_a, fmt_b);
 }
 
 int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
@@ -902,6 +903,38 @@ int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
 {
     return gemm_rowmajor(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
                          M, N, K, split_k, workspace, workspace_bytes, stream, true, fmt_a, fmt_b);
+}
+
+int mxfp8_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
+                         int64_t lda, const void *B, int64_t ldb, const void *scaleA_relaid,
+                         const void *scaleB_relaid, int fmt_a, int fmt_b, float alpha, float beta,
+                         int M, int N, int K, int split_k, void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    if (K > (1 << 29) || lda > (INT64_MAX / 4) || ldb > (INT64_MAX / 4))
+        return MXFP4_ERR_INVALID_ARG;
+    int st = check_common(D, ldd, C, ldc, A, lda * 2, B, ldb * 2, beta, M, N, K * 2, split_k);
+    if (st != MXFP4_OK)
+        return st;
+    if (K < 32 || (K % 32) != 0 || !scaleA_relaid || !scaleB_relaid)
+        return MXFP4_ERR_INVALID_ARG;
+    if ((fmt_a != MXFP8_E4M3 && fmt_a != MXFP8_E5M2) || (fmt_b != MXFP8_E4M3 && fmt_b != MXFP8_E5M2))
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(scaleA_relaid, 16) || !aligned(scaleB_relaid, 16))
+        return MXFP4_ERR_MISALIGNED;
+    const Scales sc{static_cast<const uint8_t *>(scaleA_relaid),
+                    static_cast<const uint8_t *>(scaleB_relaid), 0, 0, false};
+    return gemm_entry(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, split_k, workspace,
+                      workspace_bytes, stream, true, fmt_a, fmt_b);
+}
+
+size_t mxfp8_gemm_prepacked_workspace_size(int M, int N, int K, int split_k)
+{
+    mxfp4_plan plan;
+    if (K < 32 || (K % 32) != 0 || K > (1 << 29) ||
+        make_plan(M, N, 2 * K, split_k, device_sms_or_default(), &plan, nullptr, true) != MXFP4_OK)
+        return 0;
+    return plan.workspace_bytes;
 }
 
 int mxfp8_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out)

@@ -206,6 +206,20 @@ int mxfp8_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *o
 size_t mxfp8_gemm_workspace_size(int M, int N, int K, int split_k);
 
 /*
+ * mxfp8_gemm on scales already relaid by mxfp4_scale_relayout(dst, src, rows,
+ * K, ...) with this call's K (the relaid layout depends only on rows and the
+ * number of 32-K blocks, not on the element format), e.g. weights prepared
+ * once.  Arguments as mxfp8_gemm without the scale strides; workspace:
+ * mxfp8_gemm_prepacked_workspace_size.
+ */
+int mxfp8_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc,
+                         const void *A, int64_t lda, const void *B, int64_t ldb,
+                         const void *scaleA_relaid, const void *scaleB_relaid,
+                         int fmt_a, int fmt_b, float alpha, float beta, int M, int N, int K,
+                         int split_k, void *workspace, size_t workspace_bytes, void *stream);
+size_t mxfp8_gemm_prepacked_workspace_size(int M, int N, int K, int split_k);
+
+/*
  * As mxfp4_gemm, with both scale buffers already in the relaid layout
  * produced by mxfp4_scale_relayout (scaleA for M rows, scaleB for N rows, at
  * the same K); the GEMM then copies whole scale atoms with bulk copies.  The

@@ -91,6 +91,9 @@ def bind(path: str) -> ctypes.CDLL:
                                        ctypes.c_double, ctypes.c_double, u16p, i64,
                                        ctypes.POINTER(ctypes.c_int64), i64,
                                        u16p, dp, dp, ctypes.c_int]
+    L.oracle_quantize8.restype = ctypes.c_int
+    L.oracle_quantize8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, u16p, i64, u8p, i64,
+                                   u8p, i64]
     L.oracle_quantize.restype = ctypes.c_int
     L.oracle_quantize.argtypes = [ctypes.c_int, ctypes.c_int, u16p, i64, u8p, i64, u8p, i64]
     return L
@@ -291,4 +294,17 @@ def quantize(X_bits, rows, K):
                               _ptr(Q, ctypes.c_uint8), K // 2, _ptr(S, ctypes.c_uint8), K // 32)
     if r != 0:
         raise ValueError("oracle_quantize rejected the sizes")
+    return Q, S
+
+
+def quantize8(X_bits, rows, K, fmt):
+    """MXFP8 quantiser (fmt E4M3 / E5M2): bf16 bits [rows, K] -> (codes
+    uint8 [rows, K], E8M0 scales uint8 [rows, K/32])."""
+    X = np.ascontiguousarray(X_bits, dtype=np.uint16)
+    Q = np.zeros((rows, K), dtype=np.uint8)
+    S = np.zeros((rows, K // 32), dtype=np.uint8)
+    r = lib().oracle_quantize8(rows, K, int(fmt), _ptr(X, ctypes.c_uint16), X.shape[1],
+                               _ptr(Q, ctypes.c_uint8), K, _ptr(S, ctypes.c_uint8), K // 32)
+    if r != 0:
+        raise ValueError("oracle_quantize8 rejected its arguments")
     return Q, S

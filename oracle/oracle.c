@@ -533,3 +533,80 @@ int oracle_quantize(int rows, int K, const uint16_t *X, int64_t ldx, uint8_t *Q,
     }
     return 0;
 }
+
+/*
+ * MXFP8 quantiser, the counterpart of oracle_quantize for 8-bit elements
+ * (fmt 1 = E4M3, 2 = E5M2, decoded by oracle_fp8_value_q).  Per 1x32 block:
+ *   1. amax = the largest magnitude of the block's 32 bf16 values;
+ *   2. s = the largest integer with 2^(s + emax) <= amax, where emax is the
+ *      exponent of the format's largest binade (8 for E4M3, whose largest
+ *      value is 448; 15 for E5M2, 57344) -- the OCP MX scale rule, the plain
+ *      reading where the pages only say the scaled builtins take one scale
+ *      per block; s = 0 for an all-zero block; clamped to [-127, 127];
+ *      scale code s + 127;
+ *   3. each element: |x| / 2^s rounded to the nearest finite value of the
+ *      format, ties to the even code (round-half-even), saturating at the
+ *      largest finite value, with the sign of x.
+ * Q holds one code per byte (row stride ldq bytes).
+ */
+static int quant8_exponent(double amax, int emax)
+{
+    if (amax == 0.0)
+        return 0;
+    int e = 0;
+    frexp(amax, &e);
+    int s = e - 1 - emax;
+    while (ldexp(1.0, s + emax) > amax)
+        --s;
+    while (ldexp(1.0, s + emax + 1) <= amax)
+        ++s;
+    if (s < -127)
+        s = -127;
+    if (s > 127)
+        s = 127;
+    return s;
+}
+
+static unsigned quant8_magnitude_code(double y, int fmt)
+{
+    const unsigned top = fmt == 1 ? 0x7Eu : 0x7Bu;     /* largest finite code */
+    if (y >= oracle_fp8_value(top, fmt))
+        return top;
+    unsigned best = 0u;
+    double best_d = y;                                /* distance to code 0 (= 0.0) */
+    for (unsigned c = 1u; c <= top; ++c) {
+        const double d = fabs(y - oracle_fp8_value(c, fmt));
+        if (d < best_d || (d == best_d && !(c & 1u))) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+int oracle_quantize8(int rows, int K, int fmt, const uint16_t *X, int64_t ldx, uint8_t *Q,
+                     int64_t ldq, uint8_t *S, int64_t lds)
+{
+    if (rows < 0 || K < 0 || (K % 32) != 0 || ldx < K || ldq < K || lds < K / 32 ||
+        (fmt != 1 && fmt != 2))
+        return -1;
+    const int emax = fmt == 1 ? 8 : 15;
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *x = X + (int64_t)r * ldx;
+        for (int b = 0; b < K / 32; ++b) {
+            double amax = 0.0;                        /* step 1 */
+            for (int i = 0; i < 32; ++i)
+                amax = fmax(amax, fabs(oracle_bf16_to_double(x[b * 32 + i])));
+            const int s = quant8_exponent(amax, emax);
+            S[(int64_t)r * lds + b] = (uint8_t)(127 + s);
+            for (int i = 0; i < 32; ++i) {
+                const double v = oracle_bf16_to_double(x[b * 32 + i]);
+                unsigned code = quant8_magnitude_code(ldexp(fabs(v), -s), fmt);
+                if (signbit(v) != 0)
+                    code |= 0x80u;
+                Q[(int64_t)r * ldq + b * 32 + i] = (uint8_t)code;
+            }
+        }
+    }
+    return 0;
+}

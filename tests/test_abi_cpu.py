@@ -270,6 +270,22 @@ def test_mxfp8_argument_validation(L, kw, status):
     assert _call_gemm8(L, **kw) == status
 
 
+def test_mxfp8_prepacked_validates_before_device(L):
+    f = L.mxfp8_gemm_prepacked
+    ok = (0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, 0x4000, 0x5000, 0, 1, 1.0, 0.0, 128, 256,
+          512, 0, 0x10000, 1 << 30, None)
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a10=3) == -1                      # format
+    assert call(a8=None) == -1                    # relaid scale A
+    assert call(a8=0x4008) == -3                  # relaid scales 16-byte aligned
+    assert call(a5=520) == -3                     # lda % 16
+    assert call(a16=48, a5=64, a7=64) == -1       # K % 32
+
+
 def test_mxfp8_plan(L):
     p = mx.mxfp8_plan_gemm(8192, 8192, 8192, 0, 152)
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages, p.pair, p.persistent) == (128, 256, 128, 4, 0, 0)

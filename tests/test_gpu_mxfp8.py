@@ -125,3 +125,25 @@ def test_mxfp8_nan_scale_propagates(oracle_mod):
     D = bf16_bits_to_f64(run8(Dev8(p)))
     assert np.isnan(D[3]).all()
     assert not np.isnan(np.delete(D, 3, axis=0)).any()
+
+
+@pytest.mark.parametrize("M,N,K,split", [(300, 520, 1024, 0), (1, 4096, 2048, 0), (2000, 2600, 256, 0),
+                                         (48, 1536, 4096, 4)])
+def test_mxfp8_prepacked_matches(M, N, K, split):
+    """Scales relaid once with mxfp4_scale_relayout (K in 8-bit elements):
+    mxfp8_gemm_prepacked equals mxfp8_gemm bit for bit."""
+    p = inputs.make_problem8("pp8", M, N, K, 3, "e4m3", "e5m2", "normal", 1.0, 0.5, 1.0)
+    dev = Dev8(p)
+    ref = run8(dev, split_k=split)
+    sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device="cuda")
+    sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_scale_relayout(sfa, dev.SA, M, K, K // 32)
+    mx.mxfp4_scale_relayout(sfb, dev.SB, N, K, K // 32)
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.mxfp8_gemm_prepacked_workspace_size(M, N, K, split)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    mx.mxfp8_gemm_prepacked(D, N, dev.C, N, dev.A, K, dev.B, K, sfa, sfb, ABI_FMT[p.fmt_a],
+                            ABI_FMT[p.fmt_b], p.alpha, p.beta, M, N, K, split, ws if wsb else None,
+                            wsb)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), ref)

@@ -74,6 +74,16 @@ MUTANTS = {
         "vb = oracle_fp8_value_q(brow[k], j->fmt_a, &qb);"),
     "fp8_granule_of_fp4": (
         "int g = qa + qb + (int)ea + (int)eb - 254;", "int g = (int)ea + (int)eb - 256;"),
+    "quant8_ties_to_odd": (
+        "if (d < best_d || (d == best_d && !(c & 1u))) {",
+        "if (d < best_d || (d == best_d && (c & 1u))) {"),
+    "quant8_e4m3_emax_7": (
+        "const int emax = fmt == 1 ? 8 : 15;", "const int emax = fmt == 1 ? 7 : 15;"),
+    "quant8_scale_bias_126": ("(uint8_t)(127 + s);", "(uint8_t)(126 + s);"),
+    "quant8_sign_dropped_for_zero": ("if (signbit(v) != 0)", "if (v < 0.0)"),
+    "quant8_amax_half_block": (
+        "for (int i = 0; i < 32; ++i)\n                amax = fmax(",
+        "for (int i = 0; i < 16; ++i)\n                amax = fmax("),
     "transposed_d_store": (
         "if (!one_output(j, m, n, &j->D[(int64_t)m * j->ldd + n],",
         "if (!one_output(j, m, n, &j->D[(int64_t)(n % j->M) * j->ldd + (m % j->N)],"),

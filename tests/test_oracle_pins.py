@@ -601,6 +601,86 @@ def check_fp8_exactness_flag(o):
     assert inexact == 1, inexact
 
 
+def check_quant8_golden(o):
+    for fmt, bmax, x, code in read_golden("quantize8_rounding.txt"):
+        blk = np.zeros((1, 32), dtype=np.float64)
+        blk[0, 0] = float(bmax)
+        blk[0, 1] = float(x)
+        Q, S = o.quantize8(_bf16_bits(blk), 1, 32, int(fmt))
+        assert S[0, 0] == 127, (fmt, x, S[0, 0])
+        assert int(Q[0, 1]) == int(code, 16), (fmt, x, hex(Q[0, 1]), code)
+
+
+def check_quant8_scale_rule(o):
+    # 2^(s + emax) <= amax < 2^(s + emax + 1), s = 0 for an all-zero block,
+    # and the clamps at -127 / 127.
+    rng = np.random.default_rng(17)
+    rows, K = 20, 256
+    x = rng.standard_normal((rows, K)) * np.ldexp(1.0, rng.integers(-70, 70, size=(rows, 1)))
+    x[3, 32:64] = 0.0
+    x[5, :32] = np.ldexp(1.0, -133)
+    x[6, :32] = 255.0                        # bf16-exact, just below 256: s = -1 for E4M3
+    bits = _bf16_bits(x)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for fmt, emax in ((1, 8), (2, 15)):
+        Q, S = o.quantize8(bits, rows, K, fmt)
+        for r in range(rows):
+            for b in range(K // 32):
+                amax = float(np.max(np.abs(xv[r, 32 * b:32 * b + 32])))
+                s = int(S[r, b]) - 127
+                if amax == 0.0:
+                    assert s == 0
+                elif s == -127:
+                    assert amax < 2.0 ** (-126 + emax)
+                else:
+                    assert 2.0 ** (s + emax) <= amax < 2.0 ** (s + emax + 1), (fmt, r, b, amax, s)
+
+
+def check_quant8_nearest_brute_force(o):
+    # Every code is the nearest finite value of the format to |x| / 2^s
+    # (exact rational distances over all codes), ties to the even code,
+    # saturating at the largest finite value, with the sign of x.
+    rng = np.random.default_rng(18)
+    rows, K = 4, 96
+    x = rng.standard_normal((rows, K)) * 5.0
+    x[0, :6] = [0.0, -0.0, 1.0625, -3.0, 1e-3, 250.0]
+    bits = _bf16_bits(x)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for fmt in (1, 2):
+        top = 0x7E if fmt == 1 else 0x7B
+        vals = [fp8_fraction(c, fmt) for c in range(top + 1)]
+        Q, S = o.quantize8(bits, rows, K, fmt)
+        for r in range(rows):
+            for k in range(K):
+                s = int(S[r, k // 32]) - 127
+                y = abs(Fraction(xv[r, k])) / Fraction(2) ** s
+                if y >= vals[top]:
+                    want = top
+                else:
+                    d = [abs(y - v) for v in vals]
+                    best = min(d)
+                    cands = [c for c in range(top + 1) if d[c] == best]
+                    want = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+                if np.signbit(xv[r, k]):
+                    want |= 0x80
+                assert int(Q[r, k]) == want, (fmt, r, k, xv[r, k], s, hex(Q[r, k]), hex(want))
+
+
+def check_quant8_matches_generator(o):
+    # The input generator's MXFP8 rule (numpy scale + torch's float8 cast,
+    # an independent implementation) gives the same bytes on bf16 data.
+    from block_scaled_mxfp4_gb300 import inputs
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((16, 512)) * np.ldexp(1.0, rng.integers(-8, 8, size=(16, 1)))
+    bits = _bf16_bits(x)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for name, fmt in (("e4m3", 1), ("e5m2", 2)):
+        Qg, Sg = inputs.quantize_rows_fp8(xv, name)
+        Qo, So = o.quantize8(bits, 16, 512, fmt)
+        assert np.array_equal(So, Sg)
+        assert np.array_equal(Qo, Qg)
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
@@ -610,7 +690,8 @@ ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfield
               check_quant_matches_generator,
               check_fp8_golden, check_fp8_all_codes, check_fp8_brute_force,
               check_fp8_torch_crosscheck, check_fp8_identity, check_fp8_sampled_matches_full,
-              check_fp8_exactness_flag]
+              check_fp8_exactness_flag, check_quant8_golden, check_quant8_scale_rule,
+              check_quant8_nearest_brute_force, check_quant8_matches_generator]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

@@ -108,7 +108,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large",
-                    choices=["tiny", "decode", "mid", "large", "skinny", "quantize",
+                    choices=["tiny", "decode", "mid", "large", "skinny", "quantize", "quantize8",
                              "large8", "decode8", "mixed8"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -233,7 +233,7 @@ def run_reference(args, rank):
     if rank != 0:
         return
     from block_scaled_mxfp4_gb300 import inputs
-    if args.workload == "quantize":
+    if args.workload in ("quantize", "quantize8"):
         run_reference_quantize(args)
         return
     fp8 = args.workload in inputs.WORKLOADS8
@@ -409,21 +409,33 @@ def run_reference_quantize(args):
     xbits = inputs.f32_to_bf16_bits(
         np.random.default_rng(5).standard_normal((rows, K), dtype=np.float32))
     nrows = 64
-    per_elem = 2 + 17 / 32
+    fp8 = args.workload == "quantize8"
+    per_elem = 2 + (1 if fp8 else 0.5) + 1 / 32
+
+    def one(i):
+        chunk = xbits[(i * nrows) % rows:][:nrows]
+        if fp8:
+            oracle.quantize8(chunk, nrows, K, oracle.E4M3)
+        else:
+            oracle.quantize(chunk, nrows, K)
+
     for i in range(args.warmup):
-        oracle.quantize(xbits[i * nrows % rows:][:nrows], nrows, K)
+        one(i)
     times = []
     for i in range(args.steps):
         t0 = time.perf_counter()
-        oracle.quantize(xbits[(i * nrows) % rows:][:nrows], nrows, K)
+        one(i)
         times.append(time.perf_counter() - t0)
     value = args.steps * nrows * K * per_elem / sum(times) / 1e9
     line = {
-        "impl": "reference", "metric": "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)",
+        "impl": "reference",
+        "metric": ("MXFP8 quantiser bandwidth (bf16 -> E4M3 codes + E8M0 scales)" if fp8 else
+                   "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)"),
         "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"quantize rows={rows} K={K}", "rows": rows, "K": K},
+        "data": "synthetic", "config": {"workload": f"{args.workload} rows={rows} K={K}", "rows": rows,
+                                        "K": K},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"per step: {nrows} rows of the {rows}x{K} input"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -454,14 +466,19 @@ def run_quantize(args, world, rank, local_rank):
     rng = np.random.default_rng(5)
     xbits = inputs.f32_to_bf16_bits(rng.standard_normal((rows, K), dtype=np.float32))
     X = torch.from_numpy(xbits.view(np.int16)).to(dev)
-    Q = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    fp8 = args.workload == "quantize8"          # E4M3 codes, one per byte
+    qcols = K if fp8 else K // 2
+    Q = torch.empty((rows, qcols), dtype=torch.uint8, device=dev)
     S = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    nbytes = rows * K * 2 + rows * K // 2 + rows * K // 32
+    nbytes = rows * K * 2 + rows * qcols + rows * K // 32
 
     def step():
-        mx.mxfp4_quantize(Q, K, S, K // 32, X, K, rows, K, stream)
+        if fp8:
+            mx.mxfp8_quantize(Q, K, S, K // 32, X, K, rows, K, mx.MXFP8_E4M3, stream)
+        else:
+            mx.mxfp4_quantize(Q, K, S, K // 32, X, K, rows, K, stream)
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
@@ -485,7 +502,7 @@ def run_quantize(args, world, rank, local_rank):
     value = world * nbytes * args.steps / (tot_ms * 1e-3) / 1e9
     # end to end: host bf16 in, host codes and scales out, copies timed
     hX = torch.from_numpy(xbits.view(np.int16)).pin_memory()
-    hQ = torch.empty((rows, K // 2), dtype=torch.uint8).pin_memory()
+    hQ = torch.empty((rows, qcols), dtype=torch.uint8).pin_memory()
     hS = torch.empty((rows, K // 32), dtype=torch.uint8).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -509,30 +526,36 @@ def run_quantize(args, world, rank, local_rank):
         t0 = time.perf_counter()
         reps = 0
         while time.perf_counter() - t0 < 10.0:
-            oracle.quantize(xbits[reps * nrows % rows:][:nrows], nrows, K)
+            if fp8:
+                oracle.quantize8(xbits[reps * nrows % rows:][:nrows], nrows, K, oracle.E4M3)
+            else:
+                oracle.quantize(xbits[reps * nrows % rows:][:nrows], nrows, K)
             reps += 1
         dt = time.perf_counter() - t0
-        cpu = {"value": reps * nrows * K * (2 + 17 / 32) / dt / 1e9, "unit": "GB/s", "cores": 1,
+        cpu = {"value": reps * nbytes / rows * nrows / dt / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": f"{reps} x {nrows} rows of the {rows}x{K} input "
                                            f"({dt:.1f} s, one thread)"}
     line = {
-        "metric": "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)",
+        "metric": ("MXFP8 quantiser bandwidth (bf16 -> E4M3 codes + E8M0 scales)" if fp8 else
+                   "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)"),
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->mxfp4", "data": "synthetic",
-        "config": {"workload": f"quantize rows={rows} K={K}", "rows": rows, "K": K,
+        "vs_baseline": None, "dtype": "bf16->mxfp8 e4m3" if fp8 else "bf16->mxfp4",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} rows={rows} K={K}", "rows": rows, "K": K,
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "traffic": recorded_traffic("quantize", "quantize_kernel"),
-                     "kernel": "quantize_kernel", "kernel_ms": ms,
+                     "traffic": None if fp8 else recorded_traffic("quantize", "quantize_kernel"),
+                     "kernel": "quantize8_kernel<0>" if fp8 else "quantize_kernel", "kernel_ms": ms,
                      "algorithmic_bytes": nbytes, "peak_source": f"{peak_src} HBM copy bandwidth"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": rows * K * 2, "d2h_bytes_per_step": rows * K // 2 + rows * K // 32,
-                "ms_per_step": e2e_ms, "api": "mxfp4_quantize (pinned host copies around it)"},
+                "h2d_bytes_per_step": rows * K * 2, "d2h_bytes_per_step": rows * qcols + rows * K // 32,
+                "ms_per_step": e2e_ms,
+                "api": f"{'mxfp8' if fp8 else 'mxfp4'}_quantize (pinned host copies around it)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
@@ -550,7 +573,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
-    if args.workload == "quantize":
+    if args.workload in ("quantize", "quantize8"):
         run_quantize(args, world, rank, local_rank)
         return
     if args.workload in ("large8", "decode8", "mixed8"):

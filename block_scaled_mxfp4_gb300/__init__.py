@@ -23,7 +23,7 @@ __all__ = [
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
-    "mxfp8_gemm_prepacked_workspace_size", "MXFP8_E4M3", "MXFP8_E5M2",
+    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "MXFP8_E4M3", "MXFP8_E5M2",
     "gemm", "Plan",
 ]
 
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
                                            f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp8_gemm_prepacked_workspace_size": (sz, [i32, i32, i32, i32]),
             "mxfp8_plan_gemm": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]),
+            "mxfp8_quantize": (i32, [vp, i64, vp, i64, vp, i64, i32, i32, i32, vp]),
             "mxfp8_gemm_workspace_size": (sz, [i32, i32, i32, i32]),
             "mxfp4_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
                                            f32, f32, i32, i32, i32, i32, vp, sz, vp]),
@@ -214,6 +215,12 @@ def mxfp8_gemm_prepacked(D, ldd, C, ldc, A, lda, B, ldb, scaleA_relaid, scaleB_r
                                              alpha, beta, M, N, K, split_k, _p(workspace),
                                              workspace_bytes, _stream(stream)),
                   "mxfp8_gemm_prepacked")
+
+
+def mxfp8_quantize(Q, ldq, S, lds, X, ldx, rows, K, fmt, stream=None):
+    """bf16 rows -> E4M3 / E5M2 codes (one per byte) + E8M0 scales."""
+    return _check(lib().mxfp8_quantize(_p(Q), ldq, _p(S), lds, _p(X), ldx, rows, K, fmt,
+                                       _stream(stream)), "mxfp8_quantize")
 
 
 def mxfp8_gemm_prepacked_workspace_size(M, N, K, split_k=0) -> int:

@@ -1149,6 +1149,24 @@ int mxfp4_wait_timeout_probe(long long limit_cycles, void *stream)
                : MXFP4_ERR_CUDA;
 }
 
+int mxfp8_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, int64_t ldx,
+                   int rows, int K, int fmt, void *stream)
+{
+    if (!Q || !S || !X || rows < 1 || K < 32 || (K % 32) != 0 || ldx < K || ldq < K ||
+        lds < K / 32 || (fmt != MXFP8_E4M3 && fmt != MXFP8_E5M2))
+        return MXFP4_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || (ldx % 8) != 0 || !aligned(Q, 16) || (ldq % 16) != 0)
+        return MXFP4_ERR_MISALIGNED;
+    int st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    return launch_quantize8(static_cast<uint8_t *>(Q), ldq, static_cast<uint8_t *>(S), lds,
+                            static_cast<const uint16_t *>(X), ldx, rows, K, fmt,
+                            device_sms_or_default(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
 int mxfp4_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, int64_t ldx,
                    int rows, int K, void *stream)
 {

@@ -162,6 +162,10 @@ cudaError_t launch_stream_read(const void *src, size_t bytes, unsigned *sink, in
 
 // MXFP4 quantiser (quantize.cu): X bf16 [rows, ldx] -> Q [rows, ldq_bytes],
 // S [rows, lds]; K % 32 == 0, X rows and Q rows 16-byte aligned.
+// MXFP8 quantiser: bf16 [rows, K] -> codes [rows, ldq bytes] (fmt 0 E4M3,
+// 1 E5M2) + E8M0 scales.
+cudaError_t launch_quantize8(uint8_t *Q, int64_t ldq, uint8_t *S, int64_t lds, const uint16_t *X,
+                             int64_t ldx, int rows, int K, int fmt, int sms, cudaStream_t stream);
 cudaError_t launch_quantize(uint8_t *Q, int64_t ldq_bytes, uint8_t *S, int64_t lds,
                             const uint16_t *X, int64_t ldx, int rows, int K, int sms,
                             cudaStream_t stream);

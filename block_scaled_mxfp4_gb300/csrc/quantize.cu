@@ -106,7 +106,111 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
 }
 
+// ---------------------------------------------------------------- MXFP8 --
+// bf16 rows -> one E4M3 / E5M2 code per element [rows, K] + E8M0 scales.
+// Per 1x32 block: s = floor(log2 amax) - emax (emax 8 for E4M3, 15 for
+// E5M2: the exponent of the format's largest binade, the OCP MX rule;
+// s = 0 for an all-zero block; clamped to [-127, 127]); codes = x / 2^s
+// converted with cvt.rn.satfinite (nearest, ties to even, saturating at the
+// largest finite value).  One thread per block; its 32 codes leave in two
+// 16-byte stores.
+
+// floor(log2 amax) - emax from amax's float exponent (a subnormal amax is
+// below 2^-126 and clamps).
+__device__ __forceinline__ int block_exponent8(float amax, int emax)
+{
+    if (amax == 0.0f)
+        return 0;
+    const int biased = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+    const int s = biased == 0 ? -127 : biased - 127 - emax;
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// Two floats -> two 8-bit codes: `lo` in bits 0-7, `hi` in bits 8-15.
+template <int FMT>
+__device__ __forceinline__ uint32_t f8x2(float lo, float hi)
+{
+    uint32_t r;
+    if constexpr (FMT == 0)
+        asm("{\n\t.reg .b16 t;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\t"
+            "cvt.u32.u16 %0, t;\n\t}"
+            : "=r"(r)
+            : "f"(hi), "f"(lo));
+    else
+        asm("{\n\t.reg .b16 t;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 t, %1, %2;\n\t"
+            "cvt.u32.u16 %0, t;\n\t}"
+            : "=r"(r)
+            : "f"(hi), "f"(lo));
+    return r;
+}
+
+// FMT 0: E4M3, 1: E5M2 (the ABI's format codes).
+template <int FMT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize8_kernel(uint8_t *__restrict__ Q, int64_t ldq, uint8_t *__restrict__ S, int64_t lds,
+                     const uint16_t *__restrict__ X, int64_t ldx, int rows, int kblocks)
+{
+    constexpr int kEmax = FMT == 0 ? 8 : 15;
+    const int64_t total = static_cast<int64_t>(rows) * kblocks;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = g / kblocks;
+        const int b = static_cast<int>(g - r * kblocks);
+        const uint4 *src = reinterpret_cast<const uint4 *>(X + r * ldx + b * 32);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldcs(src + i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        const int s = block_exponent8(amax, kEmax);
+        const float inv = s == 127 ? __uint_as_float(0x00400000u)
+                                   : __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+        uint32_t out[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            // elements 4q .. 4q+3 (two bf16 pairs) -> one 32-bit word of codes
+            const uint32_t lo = f8x2<FMT>(bf16_lo(w[2 * q]) * inv, bf16_hi(w[2 * q]) * inv);
+            const uint32_t hi = f8x2<FMT>(bf16_lo(w[2 * q + 1]) * inv, bf16_hi(w[2 * q + 1]) * inv);
+            out[q] = lo | (hi << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(Q + r * ldq + b * 32);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        S[r * lds + b] = static_cast<uint8_t>(s + 127);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize8(uint8_t *Q, int64_t ldq, uint8_t *S, int64_t lds, const uint16_t *X,
+                             int64_t ldx, int rows, int K, int fmt, int sms, cudaStream_t stream)
+{
+    const int kblocks = K / 32;
+    const int64_t total = static_cast<int64_t>(rows) * kblocks;
+    int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    if (fmt == 0)
+        quantize8_kernel<0><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
+            Q, ldq, S, lds, X, ldx, rows, kblocks);
+    else
+        quantize8_kernel<1><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
+            Q, ldq, S, lds, X, ldx, rows, kblocks);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(uint8_t *Q, int64_t ldq_bytes, uint8_t *S, int64_t lds,
                             const uint16_t *X, int64_t ldx, int rows, int K, int sms,

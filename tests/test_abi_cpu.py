@@ -286,6 +286,18 @@ def test_mxfp8_prepacked_validates_before_device(L):
     assert call(a16=48, a5=64, a7=64) == -1       # K % 32
 
 
+def test_mxfp8_quantize_validates_before_device(L):
+    q = L.mxfp8_quantize
+    assert q(0x1000, 64, 0x2000, 2, 0x3000, 64, 4, 64, 2, None) == -1   # format
+    assert q(0x1000, 64, 0x2000, 2, 0x3000, 64, 4, 48, 0, None) == -1   # K % 32
+    assert q(0x1000, 32, 0x2000, 2, 0x3000, 64, 4, 64, 0, None) == -1   # ldq < K
+    assert q(0x1000, 64, 0x2000, 1, 0x3000, 64, 4, 64, 1, None) == -1   # lds < K/32
+    assert q(None, 64, 0x2000, 2, 0x3000, 64, 4, 64, 0, None) == -1
+    assert q(0x1000, 72, 0x2000, 2, 0x3000, 72, 4, 64, 0, None) == -3   # ldq % 16
+    assert q(0x1008, 64, 0x2000, 2, 0x3000, 64, 4, 64, 0, None) == -3   # Q alignment
+    assert q(0x1000, 64, 0x2000, 2, 0x3008, 64, 4, 64, 0, None) == -3   # X alignment
+
+
 def test_mxfp8_plan(L):
     p = mx.mxfp8_plan_gemm(8192, 8192, 8192, 0, 152)
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages, p.pair, p.persistent) == (128, 256, 128, 4, 0, 0)

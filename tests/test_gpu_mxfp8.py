@@ -147,3 +147,78 @@ def test_mxfp8_prepacked_matches(M, N, K, split):
                             wsb)
     torch.cuda.synchronize()
     assert np.array_equal(d_to_bits(D), ref)
+
+
+# ------------------------------------------------------------ quantiser --
+
+def _special_rows(K):
+    """Rows that exercise the quantiser's edges: an all-zero block, signed
+    zeros, ties at both formats' block maxima, saturation, bf16 extremes and
+    subnormal-range blocks."""
+    rows = np.zeros((8, K))
+    rows[1, ::2] = -0.0
+    rows[1, 1::4] = 1.0
+    rows[2, :32] = 256.0
+    rows[2, 1:8] = [1.0625, 1.1875, 460.0, 480.0, 0.0029296875, 0.0009765625, -1.5]
+    rows[3, :32] = 32768.0
+    rows[3, 1:8] = [1.125, 1.375, 61440.0, 57344.0, 2.288818359375e-05, 7.62939453125e-06, -1.25]
+    rows[4, :] = 3.3895313892515355e38          # bf16 max
+    rows[4, 1::3] = -1e38
+    rows[5, :] = np.ldexp(1.0, -133)             # bf16 subnormal: the scale clamps at -127
+    rows[6, :] = np.ldexp(1.0, -126) * 3.0
+    rows[7, :] = 511.0                           # just below 512: E4M3 saturates at 448
+    return rows
+
+
+def _bf16(x):
+    return inputs.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def _run_q8(bits, fmt, ldq_pad=0, ldx_pad=0, lds_pad=0):
+    rows, K = bits.shape
+    Xh = np.zeros((rows, K + ldx_pad), dtype=np.uint16)
+    Xh[:, :K] = bits
+    X = torch.from_numpy(Xh.view(np.int16)).cuda()
+    Q = torch.full((rows, K + ldq_pad), 0xAB, dtype=torch.uint8, device="cuda")
+    S = torch.full((rows, K // 32 + lds_pad), 0xCD, dtype=torch.uint8, device="cuda")
+    mx.mxfp8_quantize(Q, Q.stride(0), S, S.stride(0), X, X.stride(0), rows, K, ABI_FMT[fmt])
+    torch.cuda.synchronize()
+    return Q.cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_mxfp8_quantize_bit_exact(oracle_mod, fmt):
+    rng = np.random.default_rng(31 if fmt == "e4m3" else 32)
+    K = 1024
+    x = rng.standard_normal((120, K)) * np.ldexp(1.0, rng.integers(-40, 40, size=(120, 1)))
+    bits = _bf16(np.concatenate([x, _special_rows(K)]))
+    Q, S = _run_q8(bits, fmt)
+    Qr, Sr = oracle_mod.quantize8(bits, bits.shape[0], K, ORACLE_FMT[fmt])
+    assert np.array_equal(S, Sr)
+    bad = np.argwhere(Q != Qr)
+    assert bad.size == 0, [(tuple(i), hex(Q[tuple(i)]), hex(Qr[tuple(i)])) for i in bad[:8]]
+
+
+def test_mxfp8_quantize_strided(oracle_mod):
+    rng = np.random.default_rng(33)
+    K = 512
+    bits = _bf16(rng.standard_normal((40, K)) * 7.0)
+    Q, S = _run_q8(bits, "e5m2", ldq_pad=48, ldx_pad=64, lds_pad=5)
+    Qr, Sr = oracle_mod.quantize8(bits, 40, K, 2)
+    assert np.array_equal(Q[:, :K], Qr) and np.array_equal(S[:, :K // 32], Sr)
+    assert (Q[:, K:] == 0xAB).all() and (S[:, K // 32:] == 0xCD).all()   # padding untouched
+
+
+def test_mxfp8_quantize_then_gemm(oracle_mod):
+    """Activations quantised on the GPU (E4M3) times E5M2 weights: the GEMM
+    on the GPU's codes matches the oracle GEMM on the oracle's codes."""
+    rng = np.random.default_rng(34)
+    M, N, K = 200, 384, 1024
+    xa = _bf16(rng.standard_normal((M, K)))
+    QA, SA = _run_q8(xa, "e4m3")
+    QAr, SAr = oracle_mod.quantize8(xa, M, K, 1)
+    assert np.array_equal(QA, QAr) and np.array_equal(SA, SAr)
+    w = inputs.make_problem8("qw", N, 32, K, 35, "e5m2", "e5m2", "normal", 1.0, 0.0, None)
+    p = inputs.Problem8("q8gemm", M, N, K, "e4m3", "e5m2", QA, w.A, SA, w.SA, None, 1.0, 0.0, 0)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p)), Dref, sabs, 1.0, "quantise -> mxfp8 gemm")

@@ -23,7 +23,10 @@ namespace mxfp4 {
 // memory (rows padded to an odd word count, so the column reads below hit 32
 // different banks), and writes the atoms as 16-byte lines, consecutive
 // threads on consecutive lines.
-constexpr int kGroupsPerCta = 16;
+// 8 groups (32 scale bytes of each of 128 rows) per CTA: measured fastest for
+// 8192 x 8192 scales (6.5 us for both operands, against 7.5 at 16, 10.8 at 32
+// and 8.2 at 4 groups): enough CTAs to keep DRAM busy, 4 words per thread.
+constexpr int kGroupsPerCta = 8;
 constexpr int kRelayoutThreads = 256;
 
 // One or two operands per launch: row blocks [0, rblocks0) of grid x belong to
@@ -55,7 +58,13 @@ __global__ void __launch_bounds__(kRelayoutThreads)
     const int64_t g0 = static_cast<int64_t>(blockIdx.y) * kGroupsPerCta;
     const int ng = static_cast<int>(groups - g0 < kGroupsPerCta ? groups - g0 : kGroupsPerCta);
 
-    for (int e = t; e < 128 * kGroupsPerCta; e += kRelayoutThreads) {
+    // All of a thread's loads are issued before any is stored, so each thread
+    // keeps its 8 words in flight at once (the scales come cold from DRAM).
+    constexpr int kPerThread = 128 * kGroupsPerCta / kRelayoutThreads;
+    uint32_t words[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int e = t + k * kRelayoutThreads;
         const int r = e / kGroupsPerCta;
         const int w = e % kGroupsPerCta;
         const int64_t row = rb * 128 + r;
@@ -72,7 +81,12 @@ __global__ void __launch_bounds__(kRelayoutThreads)
                     word |= (kb + b < kblocks ? static_cast<uint32_t>(p[b]) : 0x7Fu) << (8 * b);
             }
         }
-        tile[r][w] = word;
+        words[k] = word;
+    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int e = t + k * kRelayoutThreads;
+        tile[e / kGroupsPerCta][e % kGroupsPerCta] = words[k];
     }
     __syncthreads();
     uint8_t *out = job.dst[op] + (rb * groups + g0) * kSfAtomBytes;

@@ -22,8 +22,9 @@
 //           arrives on the stage's sf_full barrier.  This keeps tcgen05.cp,
 //           which occupies the tensor pipe for tens of cycles per copy, off
 //           the MMA's critical path;
-//   warp 5  allocates tensor memory; one thread waits for a stage's operands
-//           and scales and issues four K=64 block-scaled MMAs into an fp32
+//   warp 5  allocates tensor memory; one thread waits for a stage's scales
+//           (whose barrier the scale writers complete only after the stage's
+//           operands landed) and issues four block-scaled MMAs into an fp32
 //           TMEM accumulator, then commits the stage back to the producers;
 //   warps 0-3  then the epilogue: tcgen05.ld the accumulator (warp w owns TMEM
 //           lanes 32w..32w+31 = tile rows), apply alpha/beta with C, round to
@@ -587,8 +588,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int i = 0; i < nkt; ++i) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status) ||
-                    !mbar_wait(&sf_full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
+                // The scale writers arrive on sf_full only after they saw the
+                // stage's full barrier, so it stands for both: one poll per
+                // stage (each poll delays this thread's next MMA issue).
+                if (!mbar_wait(&sf_full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
                     break;
                 tc_fence_after();
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;

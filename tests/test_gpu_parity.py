@@ -685,3 +685,91 @@ def test_quantize_then_gemm(oracle_mod):
     p = inputs.Problem("qgemm", M, N, K, QA, QB, SA, SB, None, 1.0, 0.0, 12)
     Dref, sabs = full_oracle(oracle_mod, p)
     assert_within_bound(run_gemm(Dev(p)), Dref, sabs, 1.0, "quantised operands")
+
+
+# ---------------------------------------------------------- CUDA graphs --
+
+def _gemm_call(dev, D, ws, wsb, split, stream):
+    p = dev.p
+    C = dev.C if p.beta != 0.0 else None
+    mx.mxfp4_gemm(D, D.stride(0), C, 0 if C is None else C.stride(0), dev.A, dev.A.stride(0) * 2,
+                  dev.B, dev.B.stride(0) * 2, dev.SA, dev.SA.stride(0), dev.SB, dev.SB.stride(0),
+                  float(p.alpha), float(p.beta), p.M, p.N, p.K, split, ws if wsb else None, wsb,
+                  stream)
+
+
+@pytest.mark.parametrize("case", ["decode", "mid", "pair"])
+def test_cuda_graph_capture_and_replay(case):
+    """mxfp4_gemm captured into a CUDA graph (dependent launches, cluster
+    launches and split-K reduce included) replays to the eager result, and
+    reads its inputs at replay time."""
+    if case == "pair":
+        p = inputs.make_problem("gpair", 2048, 4096, 2048, 41, "normal", 1.0, 0.0, None)
+        assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, 0, 0).pair == 1
+    else:
+        p = problem(case)
+    dev = Dev(p)
+    split = 0
+    wsb = mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, split)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
+    ref = run_gemm(dev)                                   # eager; also the first-use setup
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _gemm_call(dev, D, ws, wsb, split, s)
+    D.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), ref)
+    # New B values, same buffers: the replay sees them.
+    dev.B.copy_(torch.roll(dev.B, 1, 0))
+    ref2 = run_gemm(dev)
+    D.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), ref2)
+
+
+def test_cuda_graph_host_entry_and_mxfp8():
+    """The pipelined host-buffer call (copy streams forked from and joined
+    to the captured stream) and mxfp8_gemm, captured and replayed."""
+    M, N, K = 2304, 1024, 1024
+    p = inputs.make_problem("ghost", M, N, K, seed=43, values="normal", alpha=1.0, beta=0.0,
+                            c_sigma=None)
+    ref = run_gemm(Dev(p), split_k=1)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hA, hB, hSA, hSB = pin(p.A), pin(p.B), pin(p.SA), pin(p.SB)
+    hD = torch.zeros((M, N), dtype=torch.int16).pin_memory()
+    arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, 1, False)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm_host(hD, None, hA, hB, hSA, hSB, 1.0, 0.0, M, N, K, 1, arena, arena_b)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.mxfp4_gemm_host(hD, None, hA, hB, hSA, hSB, 1.0, 0.0, M, N, K, 1, arena, arena_b, s)
+    hD.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(hD.numpy().view(np.uint16), ref)
+
+    q = inputs.make_problem8("g8", 300, 520, 1024, 44, "e4m3", "e5m2", "normal", 1.0, 0.0, None)
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    A8, B8, SA8, SB8 = d(q.A), d(q.B), d(q.SA), d(q.SB)
+    D8 = torch.empty((q.M, q.N), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.mxfp8_gemm_workspace_size(q.M, q.N, q.K, 0)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    call = lambda st: mx.mxfp8_gemm(D8, q.N, None, 0, A8, q.K, B8, q.K, SA8, q.K // 32, SB8,
+                                    q.K // 32, mx.MXFP8_E4M3, mx.MXFP8_E5M2, 1.0, 0.0, q.M, q.N,
+                                    q.K, 0, ws if wsb else None, wsb, st)
+    call(None)
+    torch.cuda.synchronize()
+    ref8 = d_to_bits(D8)
+    g8 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g8, stream=s):
+        call(s)
+    D8.fill_(float("nan"))
+    g8.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D8), ref8)

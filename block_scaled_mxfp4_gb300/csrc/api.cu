@@ -973,16 +973,31 @@ static int host_panel_rows(int M)
     return (rows + 255) / 256 * 256;
 }
 
+// Columns per block of the pipelined host call: with row panels and N >= 2048
+// two halves (a multiple of 256 columns each), so that the first GEMM waits
+// for half of B rather than all of it; otherwise all N columns.
+static int host_block_cols(int M, int N)
+{
+    if (M < 2048 || N < 2048)
+        return N;
+    return ((N + 1) / 2 + 255) / 256 * 256;
+}
+
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
 {
     if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_k < 0 || split_k > kMaxSplit)
         return 0;
-    // Workspace of the panel GEMMs: the largest over the panel shapes.
-    const int mp = host_panel_rows(M);
-    size_t ws = mxfp4_gemm_workspace_size(mp, N, K, split_k);
-    const int last = M - (M - 1) / mp * mp;
-    const size_t ws_last = mxfp4_gemm_workspace_size(last, N, K, split_k);
-    ws = ws > ws_last ? ws : ws_last;
+    // Workspace of the block GEMMs: the largest over the block shapes (full
+    // and last row panel x full and last column block).
+    const int mp = host_panel_rows(M), nc = host_block_cols(M, N);
+    const int rows[2] = {mp, M - (M - 1) / mp * mp};
+    const int cols[2] = {nc, N - (N - 1) / nc * nc};
+    size_t ws = 0;
+    for (int r : rows)
+        for (int c : cols) {
+            const size_t w = mxfp4_gemm_workspace_size(r, c, K, split_k);
+            ws = w > ws ? w : ws;
+        }
     const size_t mn2 = align_up(static_cast<size_t>(M) * N * 2);
     return align_up(static_cast<size_t>(M) * K / 2) + align_up(static_cast<size_t>(N) * K / 2) +
            align_up(static_cast<size_t>(M) * K / 32) + align_up(static_cast<size_t>(N) * K / 32) +
@@ -995,10 +1010,12 @@ namespace {
 // first use and reused under a lock (a later record of an event does not
 // affect waits enqueued before it).
 constexpr int kHostMaxPanels = 8;
+constexpr int kHostMaxColBlocks = 2;
 struct HostPipe {
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t start = nullptr, operands = nullptr, done = nullptr;
-    cudaEvent_t in[kHostMaxPanels] = {}, out[kHostMaxPanels] = {};
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t b_in[kHostMaxColBlocks] = {}, in[kHostMaxPanels] = {};
+    cudaEvent_t out[kHostMaxPanels * kHostMaxColBlocks] = {};
     std::mutex lock;
 };
 
@@ -1014,16 +1031,21 @@ HostPipe *host_pipe(int dev)
         auto ev = [](cudaEvent_t *e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming); };
         if (cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) != cudaSuccess ||
-            ev(&p->start) != cudaSuccess || ev(&p->operands) != cudaSuccess ||
-            ev(&p->done) != cudaSuccess) {
+            ev(&p->start) != cudaSuccess || ev(&p->done) != cudaSuccess) {
             p->h2d = nullptr;
             return nullptr;
         }
-        for (int i = 0; i < kHostMaxPanels; ++i)
-            if (ev(&p->in[i]) != cudaSuccess || ev(&p->out[i]) != cudaSuccess) {
-                p->h2d = nullptr;
-                return nullptr;
-            }
+        bool made = true;
+        for (cudaEvent_t &e : p->b_in)
+            made = made && ev(&e) == cudaSuccess;
+        for (cudaEvent_t &e : p->in)
+            made = made && ev(&e) == cudaSuccess;
+        for (cudaEvent_t &e : p->out)
+            made = made && ev(&e) == cudaSuccess;
+        if (!made) {
+            p->h2d = nullptr;
+            return nullptr;
+        }
     }
     return p;
 }
@@ -1085,42 +1107,67 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
     const auto *hC = static_cast<const uint8_t *>(C_host);
     auto *hD = static_cast<uint8_t *>(D_host);
 
-    // Row panels: B and its scales go over first, then panel i's rows of A,
-    // its scales and C on the copy-in stream; the GEMM of panel i runs on
-    // `stream` once they landed; its D rows go back on the copy-out stream
-    // while the next panel computes.  The copy streams start after the work
-    // already on `stream` and `stream` ends after the last copy of D.
-    const int mp = host_panel_rows(M);
-    const int panels = (M + mp - 1) / mp;
+    // Blocks of row panels x column blocks.  On the copy-in stream: column
+    // block 0 of B and its scales, then each row panel of A with its scales
+    // and C, then the other column blocks of B.  The GEMMs run on `stream`,
+    // column block by column block, each row panel once its rows (and the
+    // block's B) landed; each block of D goes back on the copy-out stream
+    // while the next computes.  The copy streams start after the work
+    // already on `stream`, and `stream` ends after the last copy of D.
+    const int mp = host_panel_rows(M), nc = host_block_cols(M, N);
+    const int panels = (M + mp - 1) / mp, blocks = (N + nc - 1) / nc;
     std::lock_guard<std::mutex> g(pipe->lock);
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    auto copy_b = [&](int j) {
+        const size_t n0 = static_cast<size_t>(j) * nc;
+        const size_t cols = N - n0 < static_cast<size_t>(nc) ? N - n0 : nc;
+        return ok(cudaMemcpyAsync(dB + n0 * arow, static_cast<const uint8_t *>(B_host) + n0 * arow,
+                                  cols * arow, cudaMemcpyHostToDevice, pipe->h2d)) &&
+               ok(cudaMemcpyAsync(dSB + n0 * srow,
+                                  static_cast<const uint8_t *>(scaleB_host) + n0 * srow,
+                                  cols * srow, cudaMemcpyHostToDevice, pipe->h2d)) &&
+               ok(cudaEventRecord(pipe->b_in[j], pipe->h2d));
+    };
     if (!ok(cudaEventRecord(pipe->start, s)) || !ok(cudaStreamWaitEvent(pipe->h2d, pipe->start, 0)) ||
-        !ok(cudaStreamWaitEvent(pipe->d2h, pipe->start, 0)) ||
-        !ok(cudaMemcpyAsync(dB, B_host, b_b, cudaMemcpyHostToDevice, pipe->h2d)) ||
-        !ok(cudaMemcpyAsync(dSB, scaleB_host, sb_b, cudaMemcpyHostToDevice, pipe->h2d)) ||
-        !ok(cudaEventRecord(pipe->operands, pipe->h2d)) ||
-        !ok(cudaStreamWaitEvent(s, pipe->operands, 0)))
+        !ok(cudaStreamWaitEvent(pipe->d2h, pipe->start, 0)) || !copy_b(0))
         return MXFP4_ERR_CUDA;
     for (int i = 0; i < panels; ++i) {
         const size_t m0 = static_cast<size_t>(i) * mp;
-        const int rows = static_cast<int>(M - m0 < static_cast<size_t>(mp) ? M - m0 : mp);
+        const size_t rows = M - m0 < static_cast<size_t>(mp) ? M - m0 : mp;
         if (!ok(cudaMemcpyAsync(dA + m0 * arow, hA + m0 * arow, rows * arow, cudaMemcpyHostToDevice,
                                 pipe->h2d)) ||
             !ok(cudaMemcpyAsync(dSA + m0 * srow, hSA + m0 * srow, rows * srow,
                                 cudaMemcpyHostToDevice, pipe->h2d)) ||
             (with_c && !ok(cudaMemcpyAsync(dC + m0 * drow, hC + m0 * drow, rows * drow,
                                            cudaMemcpyHostToDevice, pipe->h2d))) ||
-            !ok(cudaEventRecord(pipe->in[i], pipe->h2d)) || !ok(cudaStreamWaitEvent(s, pipe->in[i], 0)))
+            !ok(cudaEventRecord(pipe->in[i], pipe->h2d)))
             return MXFP4_ERR_CUDA;
-        st = mxfp4_gemm(dD + m0 * drow, N, with_c ? dC + m0 * drow : nullptr, N, dA + m0 * arow, K,
-                        dB, K, dSA + m0 * srow, K / 32, dSB, K / 32, alpha, beta, rows, N, K, split_k,
-                        ws, ws_bytes, stream);
-        if (st != MXFP4_OK)
-            return st;
-        if (!ok(cudaEventRecord(pipe->out[i], s)) || !ok(cudaStreamWaitEvent(pipe->d2h, pipe->out[i], 0)) ||
-            !ok(cudaMemcpyAsync(hD + m0 * drow, dD + m0 * drow, rows * drow, cudaMemcpyDeviceToHost,
-                                pipe->d2h)))
+    }
+    for (int j = 1; j < blocks; ++j)
+        if (!copy_b(j))
             return MXFP4_ERR_CUDA;
+    for (int j = 0; j < blocks; ++j) {
+        const size_t n0 = static_cast<size_t>(j) * nc;
+        const int cols = static_cast<int>(N - n0 < static_cast<size_t>(nc) ? N - n0 : nc);
+        if (!ok(cudaStreamWaitEvent(s, pipe->b_in[j], 0)))
+            return MXFP4_ERR_CUDA;
+        for (int i = 0; i < panels; ++i) {
+            const size_t m0 = static_cast<size_t>(i) * mp;
+            const int rows = static_cast<int>(M - m0 < static_cast<size_t>(mp) ? M - m0 : mp);
+            const size_t d_off = m0 * drow + n0 * 2;
+            if (j == 0 && !ok(cudaStreamWaitEvent(s, pipe->in[i], 0)))
+                return MXFP4_ERR_CUDA;
+            st = mxfp4_gemm(dD + d_off, N, with_c ? dC + d_off : nullptr, N, dA + m0 * arow, K,
+                            dB + n0 * arow, K, dSA + m0 * srow, K / 32, dSB + n0 * srow, K / 32,
+                            alpha, beta, rows, cols, K, split_k, ws, ws_bytes, stream);
+            if (st != MXFP4_OK)
+                return st;
+            cudaEvent_t out = pipe->out[j * kHostMaxPanels + i];
+            if (!ok(cudaEventRecord(out, s)) || !ok(cudaStreamWaitEvent(pipe->d2h, out, 0)) ||
+                !ok(cudaMemcpy2DAsync(hD + d_off, drow, dD + d_off, drow, static_cast<size_t>(cols) * 2,
+                                      rows, cudaMemcpyDeviceToHost, pipe->d2h)))
+                return MXFP4_ERR_CUDA;
+        }
     }
     if (!ok(cudaEventRecord(pipe->done, pipe->d2h)) || !ok(cudaStreamWaitEvent(s, pipe->done, 0)))
         return MXFP4_ERR_CUDA;

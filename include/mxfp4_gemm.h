@@ -243,11 +243,13 @@ size_t mxfp4_gemm_prepacked_workspace_size(int M, int N, int K, int split_k);
 /*
  * End-to-end call on HOST buffers: copies A, B, scaleA, scaleB (and C when
  * beta != 0) from host memory into `device_arena`, runs mxfp4_gemm there and
- * copies D back to host memory.  For M >= 2048 the rows go in eight panels
- * (multiples of 256 rows) so the copies overlap the compute: B and its
- * scales are copied first, then each panel's A, scales and C rows on an
- * internal copy stream; each panel's GEMM runs on `stream`; its D rows return
- * on a second internal copy stream while the next panel computes.  The
+ * copies D back to host memory.  For M >= 2048 the work goes in blocks so
+ * the copies overlap the compute: the rows in eight panels (multiples of 256
+ * rows) and, when N >= 2048 too, the columns in two halves (a multiple of 256
+ * columns each).  On an internal copy stream: the first column block of B
+ * and its scales, then each panel's A, scales and C rows, then the rest of
+ * B.  The block GEMMs run on `stream`, first column block first; each block
+ * of D returns on a second internal copy stream while the next computes.  The
  * internal streams start after the work already enqueued on `stream`, and
  * `stream` waits for the last copy of D, so the call is ordered on `stream`
  * as a whole (pinned host memory makes the copies asynchronous).  Host

@@ -353,6 +353,40 @@ def test_host_entry_pipelined_panels(oracle_mod):
     assert_within_bound(got[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "host panels")
 
 
+def test_host_entry_column_blocks(oracle_mod):
+    """M and N >= 2048: the host call also splits the columns in two blocks
+    (1536 + a ragged 1064 here), so D returns in strided 2-D copies and the
+    second half of B arrives after all of A.  With split_k = 1 every block runs
+    the whole K in order, so D matches the device call bit for bit."""
+    M, N, K = 2304, 2600, 1024
+    p = inputs.make_problem("colblocks", M, N, K, seed=23, values="normal", alpha=0.5, beta=0.5,
+                            c_sigma=1.0)
+    ref = run_gemm(Dev(p), split_k=1)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hA, hB, hSA, hSB = pin(p.A), pin(p.B), pin(p.SA), pin(p.SB)
+    hC = pin(p.C.view(np.int16))
+    hD = torch.zeros((M, N), dtype=torch.int16).pin_memory()
+    arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, 1, True)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm_host(hD, hC, hA, hB, hSA, hSB, p.alpha, p.beta, M, N, K, 1, arena, arena_b)
+    torch.cuda.synchronize()
+    got = hD.numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    pairs = sample_pairs(M, N, 2000, 23)
+    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
+                                                   alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    assert_within_bound(got[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "host column blocks")
+    # The heuristic's own split choice per block: within the bound everywhere.
+    arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, 0, True)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device="cuda")
+    hD.zero_()
+    mx.mxfp4_gemm_host(hD, hC, hA, hB, hSA, hSB, p.alpha, p.beta, M, N, K, 0, arena, arena_b)
+    torch.cuda.synchronize()
+    got = hD.numpy().view(np.uint16)
+    assert_within_bound(got[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "host blocks, split 0")
+
+
 def test_device_errors_are_reported():
     # Split-K keeps fp32 partials in the workspace: one byte short is an error.
     q = inputs.make_problem("ws16", 256, 512, 4096, 3, "normal", 1.0, 0.0, None)

@@ -17,6 +17,9 @@ objects", sections "Data layouts" and "Verification"):
   used as one step).  Both are exact at the test sizes, so their double sums
   agree bit for bit.
 
+``gemm8`` / ``gemm8_sampled`` take 8-bit (E4M3, E5M2) or 6-bit (E2M3, E3M2)
+elements with the same scales.
+
 ``quantize`` is the oracle of the MXFP4 quantiser (bf16 rows -> packed E2M1
 codes + E8M0 scales) that produces the GEMM's operands.
 """
@@ -80,6 +83,10 @@ def bind(path: str) -> ctypes.CDLL:
                                       u16p, dp, dp, ctypes.c_int]
     L.oracle_fp8_value.restype = ctypes.c_double
     L.oracle_fp8_value.argtypes = [ctypes.c_uint, ctypes.c_int]
+    L.oracle_fp6_value.restype = ctypes.c_double
+    L.oracle_fp6_value.argtypes = [ctypes.c_uint, ctypes.c_int]
+    L.oracle_fp6_code.restype = ctypes.c_uint
+    L.oracle_fp6_code.argtypes = [u8p, ctypes.c_int64]
     L.oracle_gemm8.restype = i64
     L.oracle_gemm8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                u8p, i64, u8p, i64, u8p, i64, u8p, i64,
@@ -121,13 +128,25 @@ def e8m0_value(code: int) -> float:
     return lib().oracle_e8m0_value(code)
 
 
-# MXFP8 element formats (the codes the oracle's fmt arguments take).
-E4M3, E5M2 = 1, 2
+# MXFP8 / MXFP6 element formats (the codes the oracle's fmt arguments take).
+E4M3, E5M2, E2M3, E3M2 = 1, 2, 3, 4
 
 
 def fp8_value(code: int, fmt: int) -> float:
     """Value of an 8-bit E4M3 (fmt 1) or E5M2 (fmt 2) element code."""
     return lib().oracle_fp8_value(int(code), int(fmt))
+
+
+def fp6_value(code: int, fmt: int) -> float:
+    """Value of a 6-bit E2M3 (fmt 3) or E3M2 (fmt 4) element code."""
+    return lib().oracle_fp6_value(int(code), int(fmt))
+
+
+def fp6_code(row: np.ndarray, k: int) -> int:
+    """Code of element k of an FP6 row in the padded form (16 codes packed
+    little-endian into the first 12 of every 16 bytes), as the oracle reads it."""
+    r = np.ascontiguousarray(row, dtype=np.uint8)
+    return int(lib().oracle_fp6_code(_ptr(r, ctypes.c_uint8), int(k)))
 
 
 def fp4_code(packed_row: np.ndarray, k: int) -> int:
@@ -203,8 +222,9 @@ def gemm_sampled(A, B, SA, SB, M, N, K, pairs, alpha=1.0, beta=0.0, C=None,
 
 
 def _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b):
-    if fmt_a not in (E4M3, E5M2) or fmt_b not in (E4M3, E5M2):
-        raise ValueError("fmt_a / fmt_b must be E4M3 (1) or E5M2 (2)")
+    fmts = (E4M3, E5M2, E2M3, E3M2)
+    if fmt_a not in fmts or fmt_b not in fmts:
+        raise ValueError("fmt_a / fmt_b must be E4M3 (1), E5M2 (2), E2M3 (3) or E3M2 (4)")
     for name, arr, rows, cols in (("A", A, M, K), ("B", B, N, K),
                                   ("SA", SA, M, K // 32), ("SB", SB, N, K // 32)):
         if arr.dtype != np.uint8 or arr.ndim != 2 or arr.shape[0] < rows or arr.shape[1] < cols:
@@ -213,7 +233,8 @@ def _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b):
 
 def gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha=1.0, beta=0.0, C=None, want_acc=False,
           nthreads=0):
-    """Full MXFP8 oracle GEMM (A [M, K], B [N, K] element codes, one per byte).
+    """Full MXFP8 / MXFP6 oracle GEMM (A [M, K], B [N, K]: one byte per element;
+    FP6 rows in the padded 16-codes-per-16-bytes form).
     Returns (D bf16 bits [M,N], acc or None, sum|ab| [M,N], inexact)."""
     A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
     _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b)

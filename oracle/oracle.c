@@ -33,9 +33,10 @@
  * every output and checks with an exact product/sum test that step 5 did not
  * round; outputs that fail either check are counted and reported.
  *
- * MXFP8 form (oracle_gemm8): the same steps with one 8-bit E4M3 or E5M2
- * element per byte (oracle_fp8_value_q gives the encodings read from the
- * MFMA page).  A product's granule is 2^(qa + qb + ea + eb - 254), where
+ * MXFP8 / MXFP6 form (oracle_gemm8): the same steps with one 8-bit E4M3 or
+ * E5M2 element per byte, or E2M3 / E3M2 elements in the padded 6-bit form
+ * (oracle_fp8_value_q and oracle_fp6_value_q give the encodings read from
+ * the MFMA page).  A product's granule is 2^(qa + qb + ea + eb - 254), where
  * qa, qb are the elements' ulp exponents, and the same 2^52 bound applies.
  *
  * Readings where the pages are silent or at odds:
@@ -44,7 +45,9 @@
  *   - D is rounded to nearest, ties to even (the MFMA page's rounding mode).
  *   - C is bf16.  C is not read when beta == 0 (it may be NULL).
  *   - FP8 / BF8 biases and special codes: the OCP 8-bit formats (the page
- *     gives the field widths only); see oracle_fp8_value_q.
+ *     gives the field widths only); see oracle_fp8_value_q.  FP6 likewise:
+ *     the OCP 6-bit formats (oracle_fp6_value_q), stored 16 codes per 16
+ *     bytes (oracle_fp6_code).
  */
 #define _GNU_SOURCE
 #include <math.h>
@@ -113,6 +116,61 @@ double oracle_fp8_value_q(unsigned code, int fmt, int *ulp_exp)
 double oracle_fp8_value(unsigned code, int fmt)
 {
     return oracle_fp8_value_q(code, fmt, NULL);
+}
+
+/*
+ * MXFP6 elements (page "CDNA4 dense MFMA builtins", section "Mixed-precision
+ * with scaling": FP6 is E2M3 or E3M2, 6 bits per element, scaled per block
+ * like the others).  The pages give the field widths only; the encodings
+ * read here are the OCP 6-bit formats: E2M3 with bias 1 (largest 7.5), E3M2
+ * with bias 3 (largest 28), no infinities or NaNs, exponent field 0
+ * subnormal: (m / 2^mbits) * 2^(1 - bias).  Bit 5 is the sign.
+ *
+ * fmt: 3 = E2M3, 4 = E3M2.  *ulp_exp as for oracle_fp8_value_q.
+ */
+double oracle_fp6_value_q(unsigned code, int fmt, int *ulp_exp)
+{
+    const int ebits = fmt == 3 ? 2 : 3, mbits = fmt == 3 ? 3 : 2, bias = fmt == 3 ? 1 : 3;
+    const unsigned s = (code >> 5) & 1u;
+    const unsigned e = (code >> mbits) & ((1u << ebits) - 1u);
+    const unsigned m = code & ((1u << mbits) - 1u);
+    /* Integer significand (the implicit 1 only for a non-zero exponent
+     * field) times the binade's spacing. */
+    const unsigned sig = e == 0 ? m : (m | (1u << mbits));
+    const int q = (e == 0 ? 1 : (int)e) - bias - mbits;
+    const double v = ldexp((double)sig, q);
+    if (ulp_exp)
+        *ulp_exp = q;
+    return s ? -v : v;
+}
+
+double oracle_fp6_value(unsigned code, int fmt)
+{
+    return oracle_fp6_value_q(code, fmt, NULL);
+}
+
+/*
+ * FP6 storage: the rows hold K bytes, 16 bytes per 16 consecutive elements:
+ * the 16 codes packed little-endian (element i of the group in bits 6i ..
+ * 6i+5 of the first 12 bytes) and 4 bytes of padding that are not read.
+ * This is the operand form the scaled tensor-core instruction reads, so the
+ * GEMM loads it as bytes; the pages' own FP6 operands are packed 6-bit
+ * register fragments.
+ */
+unsigned oracle_fp6_code(const uint8_t *row, int64_t k)
+{
+    const uint8_t *g = row + (k >> 4) * 16;
+    const int bit = 6 * (int)(k & 15);
+    const unsigned two = (unsigned)g[bit >> 3] | ((unsigned)g[(bit >> 3) + 1] << 8);
+    return (two >> (bit & 7)) & 63u;
+}
+
+/* Any element format of the one-byte-footprint forms (fmt 1-4). */
+static double byte_form_value(const uint8_t *row, int64_t k, int fmt, int *q)
+{
+    if (fmt >= 3)
+        return oracle_fp6_value_q(oracle_fp6_code(row, k), fmt, q);
+    return oracle_fp8_value_q(row[k], fmt, q);
 }
 
 /* Step 1: element k of a packed row. */
@@ -186,7 +244,8 @@ static int two_sum_exact(double a, double b, double s)
 
 struct gemm_job {
     int M, N, K;
-    int fmt_a, fmt_b;  /* 0: E2M1 packed two per byte; 1: E4M3, 2: E5M2 bytes */
+    int fmt_a, fmt_b;  /* 0: E2M1 packed two per byte; 1: E4M3, 2: E5M2 bytes;
+                          3: E2M3, 4: E3M2 in the padded 16-per-16-bytes form */
     const uint8_t *A; int64_t lda_bytes;
     const uint8_t *B; int64_t ldb_bytes;
     const uint8_t *SA; int64_t ldsa;
@@ -219,11 +278,11 @@ static int one_output(struct gemm_job *j, int m, int n, uint16_t *d,
         if (j->fmt_a == 0)
             va = oracle_e2m1_value(nibble(arow, k));
         else
-            va = oracle_fp8_value_q(arow[k], j->fmt_a, &qa);
+            va = byte_form_value(arow, k, j->fmt_a, &qa);
         if (j->fmt_b == 0)
             vb = oracle_e2m1_value(nibble(brow, k));
         else
-            vb = oracle_fp8_value_q(brow[k], j->fmt_b, &qb);
+            vb = byte_form_value(brow, k, j->fmt_b, &qb);
         unsigned ea = sarow[k / 32], eb = sbrow[k / 32];
         double a = va * oracle_e8m0_value(ea);
         double b = vb * oracle_e8m0_value(eb);
@@ -387,16 +446,20 @@ int64_t oracle_gemm_sampled(int M, int N, int K,
 }
 
 /*
- * MXFP8 forms of oracle_gemm / oracle_gemm_sampled: A and B hold one 8-bit
- * element per byte (lda, ldb in elements = bytes), fmt_a / fmt_b = 1 (E4M3)
- * or 2 (E5M2), one E8M0 scale per 32 K as before.  Same steps 2-6, with the
- * element decoded by oracle_fp8_value_q.
+ * MXFP8 / MXFP6 forms of oracle_gemm / oracle_gemm_sampled: A and B hold one
+ * 8-bit element per byte, or 6-bit elements in the padded form above (one
+ * byte of footprint per element either way: lda, ldb in elements = bytes);
+ * fmt_a / fmt_b = 1 (E4M3), 2 (E5M2), 3 (E2M3) or 4 (E3M2), one E8M0 scale
+ * per 32 K as before.  Same steps 2-6, with the element decoded by
+ * oracle_fp8_value_q or oracle_fp6_value_q.
  */
 static int fp8_args_ok(int M, int N, int K, int fmt_a, int fmt_b, double beta, const uint16_t *C)
 {
     if (M < 0 || N < 0 || K < 0 || K % 32 != 0)
         return 0;
-    if ((fmt_a != 1 && fmt_a != 2) || (fmt_b != 1 && fmt_b != 2))
+    if (fmt_a < 1 || fmt_a > 4 || fmt_b < 1 || fmt_b > 4)
+        return 0;
+    if ((fmt_a >= 3 || fmt_b >= 3) && K % 16 != 0)
         return 0;
     return !(beta != 0.0 && C == NULL);
 }

@@ -67,11 +67,25 @@ MUTANTS = {
     "fp8_e4m3_nan_whole_top_binade": (
         "if (fmt == 1 && e == emax && m == (1u << mbits) - 1u)", "if (fmt == 1 && e == emax)"),
     "fp8_adjacent_elements_swapped": (
-        "va = oracle_fp8_value_q(arow[k], j->fmt_a, &qa);",
-        "va = oracle_fp8_value_q(arow[k ^ 1], j->fmt_a, &qa);"),
+        "return oracle_fp8_value_q(row[k], fmt, q);",
+        "return oracle_fp8_value_q(row[k ^ 1], fmt, q);"),
     "fp8_b_decoded_in_a_format": (
-        "vb = oracle_fp8_value_q(brow[k], j->fmt_b, &qb);",
-        "vb = oracle_fp8_value_q(brow[k], j->fmt_a, &qb);"),
+        "vb = byte_form_value(brow, k, j->fmt_b, &qb);",
+        "vb = byte_form_value(brow, k, j->fmt_a, &qb);"),
+    "fp6_e2m3_bias_0": ("bias = fmt == 3 ? 1 : 3;", "bias = fmt == 3 ? 0 : 3;"),
+    "fp6_e3m2_bias_4": ("bias = fmt == 3 ? 1 : 3;", "bias = fmt == 3 ? 1 : 4;"),
+    "fp6_sign_bit_7": ("const unsigned s = (code >> 5) & 1u;", "const unsigned s = (code >> 7) & 1u;"),
+    "fp6_subnormal_implicit_one": (
+        "const unsigned sig = e == 0 ? m : (m | (1u << mbits));",
+        "const unsigned sig = m | (1u << mbits);"),
+    "fp6_field_widths_swapped": (
+        "const int ebits = fmt == 3 ? 2 : 3, mbits = fmt == 3 ? 3 : 2,",
+        "const int ebits = fmt == 3 ? 3 : 2, mbits = fmt == 3 ? 2 : 3,"),
+    "fp6_padding_read_as_data": (
+        "const uint8_t *g = row + (k >> 4) * 16;", "const uint8_t *g = row + (k >> 4) * 12;"),
+    "fp6_codes_msb_first": (
+        "const int bit = 6 * (int)(k & 15);", "const int bit = 6 * (int)(15 - (k & 15));"),
+    "fp6_decoded_as_fp8": ("    if (fmt >= 3)\n        return oracle_fp6", "    if (fmt > 3)\n        return oracle_fp6"),
     "fp8_granule_of_fp4": (
         "int g = qa + qb + (int)ea + (int)eb - 254;", "int g = (int)ea + (int)eb - 256;"),
     "quant8_ties_to_odd": (

@@ -681,6 +681,157 @@ def check_quant8_matches_generator(o):
         assert np.array_equal(Qo, Qg)
 
 
+# --- MXFP6 (E2M3 / E3M2 elements, 16 codes per 16 bytes, E8M0 per 32) -----
+
+def fp6_fraction(code, fmt):
+    """Exact value of a 6-bit code from the format's field widths (test-side
+    decoder): E2M3 = 1/2/3 bits, bias 1; E3M2 = 1/3/2 bits, bias 3."""
+    ebits, mbits, bias = (2, 3, 1) if fmt == 3 else (3, 2, 3)
+    e = (code >> mbits) & ((1 << ebits) - 1)
+    m = code & ((1 << mbits) - 1)
+    if e == 0:
+        v = Fraction(m, 2 ** mbits) * Fraction(2) ** (1 - bias)
+    else:
+        v = (1 + Fraction(m, 2 ** mbits)) * Fraction(2) ** (e - bias)
+    return -v if code & 0x20 else v
+
+
+def pack_fp6(codes, pad=None):
+    """Test-side packer: [rows, K] 6-bit codes -> [rows, K] bytes, each 16
+    codes little-endian in 12 bytes followed by 4 padding bytes (`pad`
+    [rows, K/16, 4] or zeros)."""
+    rows, K = codes.shape
+    bits = ((np.asarray(codes, dtype=np.int64)[..., None] >> np.arange(6)) & 1).astype(np.uint8)
+    body = np.packbits(bits.reshape(rows, K // 16, 96), axis=2, bitorder="little")
+    out = np.zeros((rows, K // 16, 16), dtype=np.uint8)
+    out[:, :, :12] = body
+    if pad is not None:
+        out[:, :, 12:] = pad
+    return out.reshape(rows, K)
+
+
+def unpack_fp6(rows_bytes):
+    """Test-side unpacker (np.unpackbits), the inverse of pack_fp6."""
+    rows, K = rows_bytes.shape
+    bits = np.unpackbits(rows_bytes.reshape(rows, K // 16, 16)[:, :, :12], axis=2,
+                         bitorder="little")
+    return (bits.reshape(rows, K // 16, 16, 6).astype(np.int64) << np.arange(6)).sum(axis=3) \
+        .reshape(rows, K)
+
+
+def random_case6(rng, M, N, K, fmt_a, fmt_b, scale_lo=122, scale_hi=132):
+    """Codes uniform over all 64 values of each FP6 format (an FP8 operand,
+    fmt 1 or 2, takes random_case8's codes) with random padding bytes,
+    scales near 1 and C with exponents 2^-8 .. 2^8."""
+    A8, B8, SA, SB, C = random_case8(rng, M, N, K, 1 if fmt_a >= 3 else fmt_a,
+                                     1 if fmt_b >= 3 else fmt_b, scale_lo, scale_hi)
+    def operand(fmt, rows, fp8):
+        if fmt < 3:
+            return fp8, None
+        codes = rng.integers(0, 64, size=(rows, K))
+        pad = rng.integers(0, 256, size=(rows, K // 16, 4)).astype(np.uint8)
+        return pack_fp6(codes, pad), codes
+    A, ca = operand(fmt_a, M, A8)
+    B, cb = operand(fmt_b, N, B8)
+    return A, B, SA, SB, C, ca, cb
+
+
+def element_fraction(row_bytes, codes, k, fmt):
+    if fmt >= 3:
+        return fp6_fraction(int(codes[k]), fmt)
+    return fp8_fraction(int(row_bytes[k]), fmt)
+
+
+def check_fp6_golden(o):
+    for fmt, code, v in read_golden("fp6_values.txt"):
+        got = o.fp6_value(int(code, 2), int(fmt))
+        assert got == float(v) and math.copysign(1.0, got) == math.copysign(1.0, float(v)), \
+            (fmt, code, got, v)
+
+
+def check_fp6_all_codes(o):
+    """Every code of both formats: the oracle's decode equals the test-side
+    field decoder; codes 0..31 increase strictly, bit 5 negates; the largest
+    values are 7.5 and 28; and every value is exactly representable in the
+    8-bit format with the same mantissa width and a wider exponent range
+    (E2M3 in E4M3, E3M2 in E5M2, by torch's float8 types)."""
+    import torch
+    for fmt, top, dt in ((3, 7.5, torch.float8_e4m3fn), (4, 28.0, torch.float8_e5m2)):
+        vals = [o.fp6_value(c, fmt) for c in range(64)]
+        for c in range(64):
+            assert Fraction(vals[c]) == fp6_fraction(c, fmt), (fmt, c, vals[c])
+            assert vals[c ^ 0x20] == -vals[c] and math.copysign(1, vals[c ^ 0x20]) != \
+                math.copysign(1, vals[c]), (fmt, c)
+        assert all(vals[c] < vals[c + 1] for c in range(31)), fmt
+        assert vals[31] == top and vals[63] == -top
+        t = torch.tensor(vals, dtype=torch.float64)
+        assert torch.equal(t.to(dt).double(), t), fmt
+
+
+def check_fp6_layout(o):
+    """The oracle reads element k of a padded FP6 row where an independent
+    unpacker does, ignores the padding bytes, and a lone code at any
+    position reads back only there."""
+    rng = np.random.default_rng(91)
+    codes = rng.integers(0, 64, size=(3, 96))
+    pad = rng.integers(0, 256, size=(3, 6, 4)).astype(np.uint8)
+    rows = pack_fp6(codes, pad)
+    assert np.array_equal(unpack_fp6(rows), codes)
+    for r in range(3):
+        assert [o.fp6_code(rows[r], k) for k in range(96)] == codes[r].tolist()
+    for k in range(32):
+        one = np.zeros((1, 32), dtype=np.int64)
+        one[0, k] = 0b101101
+        row = pack_fp6(one)[0]
+        assert [o.fp6_code(row, i) for i in range(32)] == one[0].tolist(), k
+
+
+def brute_force_gemm6(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha, beta, C, ca, cb):
+    two = Fraction(2)
+    D = np.zeros((M, N), dtype=np.uint16)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                a = element_fraction(A[m], None if ca is None else ca[m], k, fmt_a)
+                b = element_fraction(B[n], None if cb is None else cb[n], k, fmt_b)
+                acc += a * two ** (int(SA[m, k // 32]) - 127) * b * two ** (int(SB[n, k // 32]) - 127)
+            y = Fraction(alpha) * acc
+            if beta != 0.0:
+                y += Fraction(beta) * bf16_bits_to_fraction(int(C[m, n]))
+            D[m, n] = bf16_rne_by_search(y)
+    return D
+
+
+def check_fp6_brute_force(o, cases=8):
+    rng = np.random.default_rng(92)
+    for i in range(cases):
+        fmt_a, fmt_b = [(3, 3), (4, 4), (3, 4), (1, 3), (4, 2), (3, 1), (4, 3), (2, 4)][i % 8]
+        M, N, K = 3, 4, 64
+        A, B, SA, SB, C, ca, cb = random_case6(rng, M, N, K, fmt_a, fmt_b)
+        alpha, beta = [(1.0, 0.0), (0.5, 0.25), (-2.0, 1.0), (0.75, -0.5)][i % 4]
+        D, _, _, inexact = o.gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha=alpha, beta=beta, C=C)
+        assert inexact == 0
+        want = brute_force_gemm6(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha, beta, C, ca, cb)
+        assert same_value(D, want), (i, fmt_a, fmt_b, D, want)
+
+
+def check_fp6_numpy_crosscheck(o):
+    """The exact double sum equals one float64 matmul of operands decoded by
+    the test-side unpacker and field decoder (exact at these sizes)."""
+    rng = np.random.default_rng(93)
+    for fmt_a, fmt_b in ((3, 4), (4, 3)):
+        M, N, K = 24, 40, 256
+        A, B, SA, SB, _, ca, cb = random_case6(rng, M, N, K, fmt_a, fmt_b)
+        _, acc, _, inexact = o.gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, want_acc=True)
+        assert inexact == 0
+        table = {f: np.array([float(fp6_fraction(c, f)) for c in range(64)]) for f in (3, 4)}
+        sa = np.repeat(np.ldexp(1.0, SA.astype(np.int64) - 127), 32, axis=1)
+        sb = np.repeat(np.ldexp(1.0, SB.astype(np.int64) - 127), 32, axis=1)
+        ref = (table[fmt_a][unpack_fp6(A)] * sa) @ (table[fmt_b][unpack_fp6(B)] * sb).T
+        assert np.array_equal(acc, ref)
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
@@ -691,7 +842,9 @@ ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfield
               check_fp8_golden, check_fp8_all_codes, check_fp8_brute_force,
               check_fp8_torch_crosscheck, check_fp8_identity, check_fp8_sampled_matches_full,
               check_fp8_exactness_flag, check_quant8_golden, check_quant8_scale_rule,
-              check_quant8_nearest_brute_force, check_quant8_matches_generator]
+              check_quant8_nearest_brute_force, check_quant8_matches_generator,
+              check_fp6_golden, check_fp6_all_codes, check_fp6_layout, check_fp6_brute_force,
+              check_fp6_numpy_crosscheck]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

@@ -109,7 +109,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large",
                     choices=["tiny", "decode", "mid", "large", "skinny", "quantize", "quantize8",
-                             "large8", "decode8", "mixed8"])
+                             "large8", "decode8", "mixed8", "large6", "mixed6"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -203,13 +203,14 @@ def oracle_throughput(p, seconds, seed):
     import numpy as np
 
     import oracle
+    from block_scaled_mxfp4_gb300 import inputs
     rng = np.random.default_rng(seed)
 
     def run(count):
         pairs = np.stack([rng.integers(0, p.M, count), rng.integers(0, p.N, count)], axis=1)
         t0 = time.perf_counter()
         if hasattr(p, "fmt_a"):          # MXFP8 problem
-            fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+            fmt = inputs.BYTE_FORMATS
             oracle.gemm8_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, fmt[p.fmt_a], fmt[p.fmt_b],
                                  pairs, alpha=p.alpha, beta=p.beta, C=p.C)
         else:
@@ -248,7 +249,9 @@ def run_reference(args, rank):
         times.append(t)
     value = len(vals) / sum(1.0 / v for v in vals)        # total FLOPs / total time
     line = {
-        "impl": "reference", "metric": METRIC8 if fp8 else METRIC, "value": value, "unit": UNIT,
+        "impl": "reference",
+        "metric": (METRIC6 if args.workload.endswith("6") else METRIC8) if fp8 else METRIC,
+        "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -263,11 +266,13 @@ def run_reference(args, rank):
 
 
 METRIC8 = "MXFP8 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP8 peak / HBM roofline"
+METRIC6 = "MXFP6 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP6 peak (the FP8 rate)"
 FP8_PER_BF16 = 2.0                   # nominal dense FP8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
 def run_mxfp8(args, world, rank, local_rank):
-    """--workload large8 | decode8 | mixed8: one mxfp8_gemm call per step
+    """--workload large8 | decode8 | mixed8 | large6 | mixed6: one mxfp8_gemm
+    call per step (FP6 operands in the padded 16-codes-per-16-bytes form)
     (scale relayout + one-tile tcgen05 GEMM, or split-K GEMM + reduce), device
     timed with L2 flushed between steps; each rank of a multi-GPU launch runs
     the whole problem as a replica."""
@@ -286,7 +291,9 @@ def run_mxfp8(args, world, rank, local_rank):
     dev = torch.device("cuda", local_rank)
     p = inputs.workload8(args.workload)
     M, N, K = p.M, p.N, p.K
-    fmt = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2}
+    fmt = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2, "e2m3": mx.MXFP6_E2M3,
+           "e3m2": mx.MXFP6_E3M2}
+    fp6 = p.fmt_a in inputs.FP6_FORMATS or p.fmt_b in inputs.FP6_FORMATS
     d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
     A, B, SA, SB = d(p.A), d(p.B), d(p.SA), d(p.SB)
     C = d(p.C.view(np.int16)).view(torch.bfloat16) if p.C is not None else None
@@ -357,7 +364,8 @@ def run_mxfp8(args, world, rank, local_rank):
         roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peak,
                 "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
-                               f"{FP8_PER_BF16:g} (nominal dense FP8/bf16 ratio)"}
+                               f"{FP8_PER_BF16:g} (nominal dense FP8/bf16 ratio"
+                               + ("; FP6 runs at the FP8 rate in kind::mxf8f6f4)" if fp6 else ")")}
     traffic = recorded_traffic(args.workload, "gemm_mxf4_kernel")
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic,
                  "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one GEMM "
@@ -371,9 +379,10 @@ def run_mxfp8(args, world, rank, local_rank):
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
     h2d = sum(t.numel() * t.element_size() for t in (hA, hB, hSA, hSB) + ((hC,) if hC is not None else ()))
     line = {
-        "metric": METRIC8, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": f"mxfp8 ({p.fmt_a} x {p.fmt_b})", "data": "synthetic",
+        "metric": METRIC6 if fp6 else METRIC8, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{'mxfp6' if fp6 else 'mxfp8'} ({p.fmt_a} x {p.fmt_b})", "data": "synthetic",
         "config": {"workload": f"{args.workload} M={M} N={N} K={K}", "M": M, "N": N, "K": K,
                    "fmt_a": p.fmt_a, "fmt_b": p.fmt_b, "alpha": p.alpha, "beta": p.beta,
                    "seed": p.seed, "split_k": plan.split_k, "swap_ab": plan.swap_ab,
@@ -576,7 +585,7 @@ def main():
     if args.workload in ("quantize", "quantize8"):
         run_quantize(args, world, rank, local_rank)
         return
-    if args.workload in ("large8", "decode8", "mixed8"):
+    if args.workload in ("large8", "decode8", "mixed8", "large6", "mixed6"):
         run_mxfp8(args, world, rank, local_rank)
         return
 

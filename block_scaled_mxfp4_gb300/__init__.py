@@ -23,7 +23,7 @@ __all__ = [
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
-    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "MXFP8_E4M3", "MXFP8_E5M2",
+    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "MXFP8_E4M3", "MXFP8_E5M2", "MXFP6_E2M3", "MXFP6_E3M2",
     "gemm", "Plan",
 ]
 
@@ -33,7 +33,7 @@ HEADER = os.path.join(_ROOT, "include", "mxfp4_gemm.h")
 _LIB_NAME = "libmxfp4_gb300.so"
 
 MXFP4_OK = 0
-MXFP8_E4M3, MXFP8_E5M2 = 0, 1
+MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3, MXFP6_E3M2 = 0, 1, 3, 4
 STATUS_NAMES = {0: "MXFP4_OK", -1: "MXFP4_ERR_INVALID_ARG", -2: "MXFP4_ERR_UNSUPPORTED_SHAPE",
                 -3: "MXFP4_ERR_MISALIGNED", -4: "MXFP4_ERR_WORKSPACE", -5: "MXFP4_ERR_CUDA",
                 -6: "MXFP4_ERR_TIMEOUT", -7: "MXFP4_ERR_ARCH"}
@@ -199,7 +199,7 @@ def mxfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alp
 
 def mxfp8_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, fmt_a, fmt_b,
                alpha, beta, M, N, K, split_k, workspace, workspace_bytes, stream=None):
-    """MXFP8 GEMM (A, B: one E4M3 / E5M2 code per byte, lda / ldb in elements)."""
+    """MXFP8 / MXFP6 GEMM (A, B: one byte per element, lda / ldb in elements)."""
     return _check(lib().mxfp8_gemm(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
                                    ld_sa, _p(scaleB), ld_sb, fmt_a, fmt_b, alpha, beta, M, N, K,
                                    split_k, _p(workspace), workspace_bytes, _stream(stream)),

@@ -832,6 +832,13 @@ int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const
 // mxfp4_gemm and mxfp8_gemm: row-major scales, relaid into the workspace
 // first when the plan asks for it.  fp8: K counts 8-bit elements (the plan
 // is that of an fp4 GEMM of 2K, which has the same bytes per row).
+// Element formats of the one-byte-per-element GEMM; each enum value is the
+// format's code in the kind::mxf8f6f4 instruction descriptor.
+static bool byte_format_ok(int fmt)
+{
+    return fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2 || fmt == MXFP6_E2M3 || fmt == MXFP6_E3M2;
+}
+
 static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,
                          int64_t lda, const void *B, int64_t ldb, const void *scaleA,
                          int64_t ld_sa, const void *scaleB, int64_t ld_sb, float alpha, float beta,
@@ -848,8 +855,7 @@ static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const
         return MXFP4_ERR_INVALID_ARG;
     if (!scaleA || !scaleB || ld_sa < K / 32 || ld_sb < K / 32)
         return MXFP4_ERR_INVALID_ARG;
-    if (fp8 && ((fmt_a != MXFP8_E4M3 && fmt_a != MXFP8_E5M2) ||
-                (fmt_b != MXFP8_E4M3 && fmt_b != MXFP8_E5M2)))
+    if (fp8 && (!byte_format_ok(fmt_a) || !byte_format_ok(fmt_b)))
         return MXFP4_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, kAlign))
         return MXFP4_ERR_MISALIGNED;
@@ -918,7 +924,7 @@ int mxfp8_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const
         return st;
     if (K < 32 || (K % 32) != 0 || !scaleA_relaid || !scaleB_relaid)
         return MXFP4_ERR_INVALID_ARG;
-    if ((fmt_a != MXFP8_E4M3 && fmt_a != MXFP8_E5M2) || (fmt_b != MXFP8_E4M3 && fmt_b != MXFP8_E5M2))
+    if (!byte_format_ok(fmt_a) || !byte_format_ok(fmt_b))
         return MXFP4_ERR_INVALID_ARG;
     if (!aligned(scaleA_relaid, 16) || !aligned(scaleB_relaid, 16))
         return MXFP4_ERR_MISALIGNED;

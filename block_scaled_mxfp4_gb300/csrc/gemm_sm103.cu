@@ -824,7 +824,9 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
 {
     if (!s.fp8)
         return launch_gemm_fmt<0>(a, tmP, tmQ, s, grid, stream);
-    if ((a.fmt_p != 0 && a.fmt_p != 1) || (a.fmt_q != 0 && a.fmt_q != 1))
+    // kind::mxf8f6f4 element codes: E4M3 0, E5M2 1, E2M3 3, E3M2 4.
+    auto known = [](int f) { return f == 0 || f == 1 || f == 3 || f == 4; };
+    if (!known(a.fmt_p) || !known(a.fmt_q))
         return cudaErrorInvalidValue;
     GemmArgs b = a;
     b.idesc8 = idesc_mxf8(kTileM, s.tile_n, static_cast<uint32_t>(a.fmt_p),

@@ -206,18 +206,23 @@ def identity_problem(M: int = 128, N: int = 256, K: int = 512, seed: int = 0) ->
 
 # format name -> (oracle format code, largest element exponent, largest finite)
 FP8_FORMATS = {"e4m3": (1, 8, 448.0), "e5m2": (2, 15, 57344.0)}
+# 6-bit formats: (oracle format code, largest element exponent, largest
+# finite, exponent bits, mantissa bits, bias).  Stored 16 codes per 16 bytes.
+FP6_FORMATS = {"e2m3": (3, 2, 7.5, 2, 3, 1), "e3m2": (4, 4, 28.0, 3, 2, 3)}
+BYTE_FORMATS = {**{k: v[0] for k, v in FP8_FORMATS.items()},
+                **{k: v[0] for k, v in FP6_FORMATS.items()}}
 
 
 @dataclasses.dataclass
 class Problem8:
-    """One MXFP8 GEMM instance: A [M, K] and B [N, K] 8-bit element codes."""
+    """One MXFP8 / MXFP6 GEMM instance: A [M, K] and B [N, K] bytes."""
 
     name: str
     M: int
     N: int
     K: int
-    fmt_a: str               # "e4m3" or "e5m2"
-    fmt_b: str
+    fmt_a: str               # "e4m3", "e5m2" (one code per byte) or "e2m3", "e3m2"
+    fmt_b: str               # (6-bit: 16 codes packed in 12 of every 16 bytes)
     A: np.ndarray            # uint8 [M, K]
     B: np.ndarray            # uint8 [N, K]
     SA: np.ndarray           # uint8 [M, K/32] E8M0
@@ -246,6 +251,46 @@ def quantize_rows_fp8(x: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
     return codes.astype(np.uint8), (s + 127).astype(np.uint8)
 
 
+def pack_fp6(codes: np.ndarray) -> np.ndarray:
+    """[rows, K] 6-bit codes (K % 16 == 0) -> [rows, K] bytes: every 16 codes
+    packed little-endian (code i in bits 6i..6i+5) into 12 bytes, then 4
+    zero bytes -- the FP6 operand layout of the GEMM."""
+    rows, K = codes.shape
+    bits = ((codes.astype(np.int64)[..., None] >> np.arange(6)) & 1).astype(np.uint8)
+    body = np.packbits(bits.reshape(rows, K // 16, 96), axis=2, bitorder="little")
+    out = np.zeros((rows, K // 16, 16), dtype=np.uint8)
+    out[:, :, :12] = body
+    return out.reshape(rows, K)
+
+
+def quantize_rows_fp6(x: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
+    """Quantise float64 rows [rows, K] (K % 32 == 0) to (packed FP6 bytes,
+    E8M0): scale 2^(floor(log2 amax) - emax) per 32 (the OCP MX rule), then
+    each element to the nearest FP6 value, ties to the even code, saturating
+    at the largest."""
+    rows, K = x.shape
+    assert K % 32 == 0
+    _, emax, top, ebits, mbits, bias = FP6_FORMATS[fmt]
+    amax = np.abs(x).reshape(rows, K // 32, 32).max(axis=2)
+    _, e = np.frexp(amax)
+    s = (e - 1 - emax).astype(np.int64)
+    s[amax == 0] = 0
+    s = np.clip(s, -127, 127)
+    y = np.ldexp(x.reshape(rows, K // 32, 32), -s[:, :, None]).reshape(rows, K)
+    a = np.minimum(np.abs(y), top)
+    _, ea = np.frexp(a)
+    binade = np.maximum(ea - 1, 1 - bias)               # exponent of a's binade
+    sig = np.rint(np.ldexp(a, mbits - binade)).astype(np.int64)   # ties to even
+    carry = sig >= (2 << mbits)                         # rounded up into the next binade
+    binade = np.where(carry, binade + 1, binade)
+    sig = np.where(carry, sig >> 1, sig)
+    normal = sig >= (1 << mbits)
+    efield = np.where(normal, binade + bias, 0)
+    mfield = np.where(normal, sig - (1 << mbits), sig)
+    codes = (np.signbit(y).astype(np.int64) << 5) | (efield << mbits) | mfield
+    return pack_fp6(codes), (s + 127).astype(np.uint8)
+
+
 def _quantized_operand8(rng: np.random.Generator, rows: int, K: int, dist: str, fmt: str):
     codes = np.empty((rows, K), dtype=np.uint8)
     scales = np.empty((rows, K // 32), dtype=np.uint8)
@@ -257,17 +302,18 @@ def _quantized_operand8(rng: np.random.Generator, rows: int, K: int, dist: str, 
             x = rng.uniform(-1.0, 1.0, size=(r1 - r0, K))
         else:
             raise ValueError(dist)
-        codes[r0:r1], scales[r0:r1] = quantize_rows_fp8(x, fmt)
+        quant = quantize_rows_fp6 if fmt in FP6_FORMATS else quantize_rows_fp8
+        codes[r0:r1], scales[r0:r1] = quant(x, fmt)
     return codes, scales
 
 
 def make_problem8(name: str, M: int, N: int, K: int, seed: int, fmt_a: str, fmt_b: str,
                   values: str, alpha: float, beta: float, c_sigma: Optional[float]) -> Problem8:
-    """Draw one MXFP8 problem (A in fmt_a, B in fmt_b)."""
+    """Draw one MXFP8 / MXFP6 problem (A in fmt_a, B in fmt_b)."""
     if K % 32 != 0:
         raise ValueError("K must be a multiple of 32 (one E8M0 scale per 32)")
-    if fmt_a not in FP8_FORMATS or fmt_b not in FP8_FORMATS:
-        raise ValueError("formats are 'e4m3' or 'e5m2'")
+    if fmt_a not in BYTE_FORMATS or fmt_b not in BYTE_FORMATS:
+        raise ValueError("formats are 'e4m3', 'e5m2', 'e2m3' or 'e3m2'")
     rng = np.random.default_rng(seed)
     A, SA = _quantized_operand8(rng, M, K, values, fmt_a)
     B, SB = _quantized_operand8(rng, N, K, values, fmt_b)
@@ -280,6 +326,8 @@ WORKLOADS8 = {
     "large8":  (8192, 8192, 8192, 5, "e4m3", "e4m3", "normal", 1.0, 0.0, None),
     "decode8": (1, 8192, 8192, 6, "e4m3", "e4m3", "normal", 1.0, 0.0, None),
     "mixed8":  (512, 1024, 2048, 7, "e4m3", "e5m2", "normal", 0.5, 0.5, 1.0),
+    "large6":  (8192, 8192, 8192, 8, "e2m3", "e2m3", "normal", 1.0, 0.0, None),
+    "mixed6":  (512, 1024, 2048, 9, "e3m2", "e4m3", "normal", 0.5, 0.5, 1.0),
 }
 
 

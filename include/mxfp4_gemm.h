@@ -185,24 +185,33 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * MXFP8 form of mxfp4_gemm: D[M,N] = alpha * A[M,K] . B[N,K]^T + beta * C[M,N]
- * with 8-bit elements, one E8M0 scale per 32 K as for MXFP4 (page "CDNA4
- * dense MFMA builtins", section "FP8 and BF8 matrix inputs": FP8 = E4M3,
- * BF8 = E5M2; section "Mixed-precision with scaling": scaled per block, A
- * and B formats chosen independently).  Encodings: the OCP 8-bit formats
- * (E4M3: bias 7, no infinity, NaN = S.1111.111, largest 448; E5M2: bias 15,
- * IEEE-style infinities and NaNs, largest 57344).
- *   A: uint8 [M, lda] device, one code per element, lda >= K elements
- *      (= bytes), lda % 16 == 0, 16-byte aligned; B likewise [N, ldb].
- *   fmt_a, fmt_b: MXFP8_E4M3 or MXFP8_E5M2.
+ * MXFP8 / MXFP6 form of mxfp4_gemm: D[M,N] = alpha * A[M,K] . B[N,K]^T +
+ * beta * C[M,N] with 8-bit or 6-bit elements, one E8M0 scale per 32 K as for
+ * MXFP4 (page "CDNA4 dense MFMA builtins", section "FP8 and BF8 matrix
+ * inputs": FP8 = E4M3, BF8 = E5M2; section "Mixed-precision with scaling":
+ * also FP6 = E2M3 or E3M2, scaled per block, A and B formats chosen
+ * independently).  Encodings: the OCP formats (E4M3: bias 7, no infinity,
+ * NaN = S.1111.111, largest 448; E5M2: bias 15, IEEE-style infinities and
+ * NaNs, largest 57344; E2M3: bias 1, largest 7.5; E3M2: bias 3, largest 28;
+ * the 6-bit formats have no infinity or NaN).
+ *   A: uint8 [M, lda] device, lda >= K elements (= bytes), lda % 16 == 0,
+ *      16-byte aligned; B likewise [N, ldb].  8-bit formats: one code per
+ *      byte.  6-bit formats: the layout the tensor cores read -- every 16
+ *      consecutive elements of a row take 16 bytes, their codes packed
+ *      little-endian into the first 12 (element i of the group in bits
+ *      6i .. 6i+5, sign in the top bit of each code) and 4 padding bytes
+ *      that are not read.  Either way one byte per element of footprint.
+ *   fmt_a, fmt_b: MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3 or MXFP6_E3M2 (each
+ *      value is the format's code in the kind::mxf8f6f4 instruction).
  *   Scales, C, D, alpha, beta, split_k, workspace, stream: as for
  *   mxfp4_gemm (mxfp8_gemm_workspace_size gives the workspace).
- * Runs the one-tile tcgen05 kernel (kind::mxf8f6f4, K = 32 per MMA) with the
- * same tile / split-K / swap-AB plan as an MXFP4 GEMM whose rows hold as many
- * bytes (mxfp8_plan_gemm reports it; tile_k there counts 8-bit elements).
+ * Runs the one-tile tcgen05 kernel (kind::mxf8f6f4, K = 32 per MMA; FP6 at
+ * the FP8 rate) with the same tile / split-K / swap-AB plan as an MXFP4 GEMM
+ * whose rows hold as many bytes (mxfp8_plan_gemm reports it; tile_k there
+ * counts elements).
  * Errors: as for mxfp4_gemm, plus MXFP4_ERR_INVALID_ARG for a bad format.
  */
-enum { MXFP8_E4M3 = 0, MXFP8_E5M2 = 1 };
+enum { MXFP8_E4M3 = 0, MXFP8_E5M2 = 1, MXFP6_E2M3 = 3, MXFP6_E3M2 = 4 };
 int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                const void *A, int64_t lda, const void *B, int64_t ldb,
                const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,

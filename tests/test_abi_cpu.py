@@ -279,7 +279,9 @@ def test_mxfp8_prepacked_validates_before_device(L):
         for i, v in kw.items():
             a[int(i[1:])] = v
         return f(*a)
-    assert call(a10=3) == -1                      # format
+    for bad in (2, 5, -1):                        # format codes other than 0, 1, 3, 4
+        assert call(a10=bad) == -1
+        assert call(a11=bad) == -1
     assert call(a8=None) == -1                    # relaid scale A
     assert call(a8=0x4008) == -3                  # relaid scales 16-byte aligned
     assert call(a5=520) == -3                     # lda % 16

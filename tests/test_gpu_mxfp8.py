@@ -1,5 +1,5 @@
-"""MXFP8 GEMM (E4M3 / E5M2 elements, one E8M0 scale per 32) on the GPU
-through the C ABI, element by element against the oracle.
+"""MXFP8 / MXFP6 GEMM (E4M3 / E5M2 / E2M3 / E3M2 elements, one E8M0 scale per
+32) on the GPU through the C ABI, element by element against the oracle.
 
 Bound, as for MXFP4: |D_gpu - D_ref| <= ulp_bf16(D_ref) + 2^-20 * sum|a_k b_k|.
 """
@@ -14,8 +14,9 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-ABI_FMT = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2}
-ORACLE_FMT = {"e4m3": 1, "e5m2": 2}
+ABI_FMT = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2, "e2m3": mx.MXFP6_E2M3,
+           "e3m2": mx.MXFP6_E3M2}
+ORACLE_FMT = inputs.BYTE_FORMATS
 
 
 @pytest.fixture(scope="session", autouse=True)
@@ -85,6 +86,50 @@ def test_mxfp8_parity(oracle_mod, M, N, K, fa, fb, alpha, beta, cs):
     assert_within_bound(run8(Dev8(p)), Dref, sabs, p.alpha, f"mxfp8 {M}x{N}x{K} {fa}x{fb}")
 
 
+# FP6 (16 codes packed in 12 of every 16 bytes): both formats, mixed with
+# each other and with FP8, on the same kernel paths as CASES.
+CASES6 = [
+    (128, 256, 512, "e2m3", "e2m3", 1.0, 0.0, None),
+    (300, 520, 1024, "e3m2", "e4m3", 0.5, 1.0, 1.0),
+    (1000, 700, 288, "e2m3", "e3m2", 1.0, 0.0, None),
+    (1, 4096, 2048, "e2m3", "e2m3", 1.0, 0.0, None),
+    (33, 100, 384, "e5m2", "e2m3", 1.0, 0.0, None),
+    (64, 2048, 4096, "e3m2", "e3m2", 1.0, 1.0, 0.1),
+    (2000, 2600, 256, "e2m3", "e4m3", 1.0, 0.0, None),
+]
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb,alpha,beta,cs", CASES6,
+                         ids=[f"{c[0]}x{c[1]}x{c[2]}-{c[3]}x{c[4]}" for c in CASES6])
+def test_mxfp6_parity(oracle_mod, M, N, K, fa, fb, alpha, beta, cs):
+    p = inputs.make_problem8("p6", M, N, K, M + N + K + 6, fa, fb, "normal", alpha, beta, cs)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p)), Dref, sabs, p.alpha, f"mxfp6 {M}x{N}x{K} {fa}x{fb}")
+
+
+def test_mxfp6_padding_bytes_are_not_read():
+    """Random bytes in the 4 padding bytes of every 16: D is unchanged."""
+    p = inputs.make_problem8("pad6", 256, 384, 512, 17, "e2m3", "e3m2", "normal", 1.0, 0.0, None)
+    want = run8(Dev8(p))
+    rng = np.random.default_rng(17)
+    for X in (p.A, p.B):
+        v = X.reshape(X.shape[0], -1, 16)
+        v[:, :, 12:] = rng.integers(0, 256, size=v[:, :, 12:].shape, dtype=np.uint8)
+    assert np.array_equal(run8(Dev8(p)), want)
+
+
+def test_mxfp6_large_sampled(oracle_mod):
+    """The 8192^3 E2M3 workload, as the benchmark runs it, on sampled outputs."""
+    p = inputs.workload8("large6")
+    pairs = sample_pairs(p.M, p.N, 3000, 10)
+    Dr, _, sabs, inexact = oracle_mod.gemm8_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K,
+                                                    ORACLE_FMT[p.fmt_a], ORACLE_FMT[p.fmt_b],
+                                                    pairs, alpha=p.alpha, beta=p.beta, C=p.C)
+    assert inexact == 0
+    D = run8(Dev8(p))
+    assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, "large6")
+
+
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
 def test_mxfp8_split_k(oracle_mod, split):
     p = inputs.make_problem8("p8s", 48, 1536, 4096, 11, "e4m3", "e4m3", "normal", 1.0, 0.5, 1.0)
@@ -98,7 +143,7 @@ def test_mxfp8_plan_uses_one_tile_kernel():
         assert p.pair == 0 and p.persistent == 0 and p.gemv == 0 and p.tile_k == 128
 
 
-@pytest.mark.parametrize("name", ["decode8", "mixed8"])
+@pytest.mark.parametrize("name", ["decode8", "mixed8", "mixed6"])
 def test_mxfp8_workloads_full(oracle_mod, name):
     p = inputs.workload8(name)
     Dref, sabs = oracle_full(oracle_mod, p)

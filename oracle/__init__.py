@@ -87,6 +87,8 @@ def bind(path: str) -> ctypes.CDLL:
     L.oracle_fp6_value.argtypes = [ctypes.c_uint, ctypes.c_int]
     L.oracle_fp6_code.restype = ctypes.c_uint
     L.oracle_fp6_code.argtypes = [u8p, ctypes.c_int64]
+    L.oracle_fp4_padded_code.restype = ctypes.c_uint
+    L.oracle_fp4_padded_code.argtypes = [u8p, ctypes.c_int64]
     L.oracle_gemm8.restype = i64
     L.oracle_gemm8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                u8p, i64, u8p, i64, u8p, i64, u8p, i64,
@@ -128,8 +130,9 @@ def e8m0_value(code: int) -> float:
     return lib().oracle_e8m0_value(code)
 
 
-# MXFP8 / MXFP6 element formats (the codes the oracle's fmt arguments take).
-E4M3, E5M2, E2M3, E3M2 = 1, 2, 3, 4
+# MXFP8 / MXFP6 element formats, and E2M1 in the padded form (the codes the
+# oracle's fmt arguments take).
+E4M3, E5M2, E2M3, E3M2, E2M1P = 1, 2, 3, 4, 5
 
 
 def fp8_value(code: int, fmt: int) -> float:
@@ -140,6 +143,13 @@ def fp8_value(code: int, fmt: int) -> float:
 def fp6_value(code: int, fmt: int) -> float:
     """Value of a 6-bit E2M3 (fmt 3) or E3M2 (fmt 4) element code."""
     return lib().oracle_fp6_value(int(code), int(fmt))
+
+
+def fp4_padded_code(row: np.ndarray, k: int) -> int:
+    """Code of element k of an E2M1 row in the padded form (16 codes, two per
+    byte, in the first 8 of every 16 bytes), as the oracle reads it."""
+    r = np.ascontiguousarray(row, dtype=np.uint8)
+    return int(lib().oracle_fp4_padded_code(_ptr(r, ctypes.c_uint8), int(k)))
 
 
 def fp6_code(row: np.ndarray, k: int) -> int:
@@ -222,9 +232,10 @@ def gemm_sampled(A, B, SA, SB, M, N, K, pairs, alpha=1.0, beta=0.0, C=None,
 
 
 def _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b):
-    fmts = (E4M3, E5M2, E2M3, E3M2)
+    fmts = (E4M3, E5M2, E2M3, E3M2, E2M1P)
     if fmt_a not in fmts or fmt_b not in fmts:
-        raise ValueError("fmt_a / fmt_b must be E4M3 (1), E5M2 (2), E2M3 (3) or E3M2 (4)")
+        raise ValueError("fmt_a / fmt_b must be E4M3 (1), E5M2 (2), E2M3 (3), E3M2 (4) "
+                         "or E2M1P (5)")
     for name, arr, rows, cols in (("A", A, M, K), ("B", B, N, K),
                                   ("SA", SA, M, K // 32), ("SB", SB, N, K // 32)):
         if arr.dtype != np.uint8 or arr.ndim != 2 or arr.shape[0] < rows or arr.shape[1] < cols:

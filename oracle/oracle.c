@@ -165,9 +165,27 @@ unsigned oracle_fp6_code(const uint8_t *row, int64_t k)
     return (two >> (bit & 7)) & 63u;
 }
 
-/* Any element format of the one-byte-footprint forms (fmt 1-4). */
+/*
+ * E2M1 in the same padded form (fmt 5): every 16 elements take 16 bytes, the
+ * first 8 holding two codes each -- element 2i of the group in the low
+ * nibble of byte i, element 2i+1 in its high nibble, the order of the packed
+ * MXFP4 rows -- and 8 padding bytes that are not read.  This lets E2M1 be
+ * mixed with the 8- and 6-bit formats, which the page's scaled builtins
+ * allow (A and B formats chosen independently).
+ */
+unsigned oracle_fp4_padded_code(const uint8_t *row, int64_t k)
+{
+    const unsigned pair = row[(k >> 4) * 16 + ((k & 15) >> 1)];
+    return (k & 1) ? pair >> 4 : pair & 15u;
+}
+
+/* Any element format of the one-byte-footprint forms (fmt 1-5). */
 static double byte_form_value(const uint8_t *row, int64_t k, int fmt, int *q)
 {
+    if (fmt == 5) {
+        *q = -1;                       /* E2M1 values are multiples of 1/2 */
+        return oracle_e2m1_value(oracle_fp4_padded_code(row, k));
+    }
     if (fmt >= 3)
         return oracle_fp6_value_q(oracle_fp6_code(row, k), fmt, q);
     return oracle_fp8_value_q(row[k], fmt, q);
@@ -245,7 +263,8 @@ static int two_sum_exact(double a, double b, double s)
 struct gemm_job {
     int M, N, K;
     int fmt_a, fmt_b;  /* 0: E2M1 packed two per byte; 1: E4M3, 2: E5M2 bytes;
-                          3: E2M3, 4: E3M2 in the padded 16-per-16-bytes form */
+                          3: E2M3, 4: E3M2, 5: E2M1 in the padded
+                          16-per-16-bytes forms */
     const uint8_t *A; int64_t lda_bytes;
     const uint8_t *B; int64_t ldb_bytes;
     const uint8_t *SA; int64_t ldsa;
@@ -449,15 +468,16 @@ int64_t oracle_gemm_sampled(int M, int N, int K,
  * MXFP8 / MXFP6 forms of oracle_gemm / oracle_gemm_sampled: A and B hold one
  * 8-bit element per byte, or 6-bit elements in the padded form above (one
  * byte of footprint per element either way: lda, ldb in elements = bytes);
- * fmt_a / fmt_b = 1 (E4M3), 2 (E5M2), 3 (E2M3) or 4 (E3M2), one E8M0 scale
- * per 32 K as before.  Same steps 2-6, with the element decoded by
- * oracle_fp8_value_q or oracle_fp6_value_q.
+ * fmt_a / fmt_b = 1 (E4M3), 2 (E5M2), 3 (E2M3), 4 (E3M2) or 5 (E2M1,
+ * padded), one E8M0 scale per 32 K as before.  Same steps 2-6, with the
+ * element decoded by oracle_fp8_value_q, oracle_fp6_value_q or
+ * oracle_e2m1_value.
  */
 static int fp8_args_ok(int M, int N, int K, int fmt_a, int fmt_b, double beta, const uint16_t *C)
 {
     if (M < 0 || N < 0 || K < 0 || K % 32 != 0)
         return 0;
-    if (fmt_a < 1 || fmt_a > 4 || fmt_b < 1 || fmt_b > 4)
+    if (fmt_a < 1 || fmt_a > 5 || fmt_b < 1 || fmt_b > 5)
         return 0;
     if ((fmt_a >= 3 || fmt_b >= 3) && K % 16 != 0)
         return 0;

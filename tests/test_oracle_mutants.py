@@ -85,6 +85,12 @@ MUTANTS = {
         "const uint8_t *g = row + (k >> 4) * 16;", "const uint8_t *g = row + (k >> 4) * 12;"),
     "fp6_codes_msb_first": (
         "const int bit = 6 * (int)(k & 15);", "const int bit = 6 * (int)(15 - (k & 15));"),
+    "fp4_padded_nibbles_swapped": (
+        "return (k & 1) ? pair >> 4 : pair & 15u;", "return (k & 1) ? pair & 15u : pair >> 4;"),
+    "fp4_padded_padding_read_as_data": (
+        "const unsigned pair = row[(k >> 4) * 16 + ((k & 15) >> 1)];",
+        "const unsigned pair = row[(k >> 4) * 8 + ((k & 15) >> 1)];"),
+    "fp4_padded_granule_too_coarse": ("*q = -1;                       /* E2M1", "*q = 1;                       /* E2M1"),
     "fp6_decoded_as_fp8": ("    if (fmt >= 3)\n        return oracle_fp6", "    if (fmt > 3)\n        return oracle_fp6"),
     "fp8_granule_of_fp4": (
         "int g = qa + qb + (int)ea + (int)eb - 254;", "int g = (int)ea + (int)eb - 256;"),

@@ -832,6 +832,115 @@ def check_fp6_numpy_crosscheck(o):
         assert np.array_equal(acc, ref)
 
 
+# --- E2M1 in the padded form (16 codes per 16 bytes), mixed with FP8 / FP6 ---
+
+def pack_fp4_padded(codes, pad=None):
+    """Test-side packer: [rows, K] 4-bit codes -> [rows, K] bytes, each 16
+    codes two per byte (even element in the low nibble) in 8 bytes followed
+    by 8 padding bytes (`pad` [rows, K/16, 8] or zeros)."""
+    rows, K = codes.shape
+    c = np.asarray(codes, dtype=np.uint8).reshape(rows, K // 16, 8, 2)
+    out = np.zeros((rows, K // 16, 16), dtype=np.uint8)
+    out[:, :, :8] = c[..., 0] | (c[..., 1] << 4)
+    if pad is not None:
+        out[:, :, 8:] = pad
+    return out.reshape(rows, K)
+
+
+def random_case4p(rng, M, N, K, fmt_a, fmt_b):
+    """Padded E2M1 operands (fmt 5; random codes and padding) with the other
+    side from random_case6; returns the codes of padded operands too."""
+    A, B, SA, SB, C, ca, cb = random_case6(rng, M, N, K, 1 if fmt_a == 5 else fmt_a,
+                                           1 if fmt_b == 5 else fmt_b)
+    def operand(fmt, rows, X, codes):
+        if fmt != 5:
+            return X, codes
+        c = rng.integers(0, 16, size=(rows, K))
+        return pack_fp4_padded(c, rng.integers(0, 256, size=(rows, K // 16, 8))), c
+    A, ca = operand(fmt_a, M, A, ca)
+    B, cb = operand(fmt_b, N, B, cb)
+    return A, B, SA, SB, C, ca, cb
+
+
+def check_fp4_padded_layout(o):
+    """The oracle reads element k of a padded E2M1 row where the packer put
+    it, ignores the padding bytes, and a lone code reads back only there."""
+    rng = np.random.default_rng(95)
+    codes = rng.integers(0, 16, size=(3, 64))
+    rows = pack_fp4_padded(codes, rng.integers(0, 256, size=(3, 4, 8)))
+    for r in range(3):
+        assert [o.fp4_padded_code(rows[r], k) for k in range(64)] == codes[r].tolist()
+    for k in range(32):
+        one = np.zeros((1, 32), dtype=np.int64)
+        one[0, k] = 0b1011
+        row = pack_fp4_padded(one)[0]
+        assert [o.fp4_padded_code(row, i) for i in range(32)] == one[0].tolist(), k
+
+
+def check_fp4_padded_equals_packed(o):
+    """E2M1 x E2M1 through the padded form equals the MXFP4 oracle on the
+    same codes in packed rows: D and the exact sum, bit for bit."""
+    rng = np.random.default_rng(96)
+    M, N, K = 12, 20, 128
+    ca = rng.integers(0, 16, size=(M, K))
+    cb = rng.integers(0, 16, size=(N, K))
+    _, _, SA, SB, C = random_case(rng, M, N, K)
+    packed = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    D1, acc1, _, i1 = o.gemm(packed(ca), packed(cb), SA, SB, M, N, K, alpha=0.5, beta=1.0, C=C,
+                             want_acc=True)
+    D2, acc2, _, i2 = o.gemm8(pack_fp4_padded(ca), pack_fp4_padded(cb), SA, SB, M, N, K, 5, 5,
+                              alpha=0.5, beta=1.0, C=C, want_acc=True)
+    assert i1 == 0 and i2 == 0
+    assert np.array_equal(D1, D2) and np.array_equal(acc1, acc2)
+
+
+def check_fp4_padded_brute_force(o, cases=6):
+    """Padded E2M1 mixed with FP8 and FP6 on either side: exact rational
+    brute force with the page's E2M1 values."""
+    rng = np.random.default_rng(97)
+    e2m1 = page_e2m1_values()
+    two = Fraction(2)
+    for i in range(cases):
+        fmt_a, fmt_b = [(5, 1), (3, 5), (5, 4), (2, 5), (5, 5), (5, 3)][i % 6]
+        M, N, K = 3, 4, 64
+        A, B, SA, SB, C, ca, cb = random_case4p(rng, M, N, K, fmt_a, fmt_b)
+        D, _, _, inexact = o.gemm8(A, B, SA, SB, M, N, K, fmt_a, fmt_b, alpha=0.75, beta=-0.5,
+                                   C=C)
+        assert inexact == 0
+        def val(X, codes, r, k, fmt):
+            if fmt == 5:
+                return e2m1[int(codes[r, k])]
+            return element_fraction(X[r], None if codes is None else codes[r], k, fmt)
+        want = np.zeros((M, N), dtype=np.uint16)
+        for m in range(M):
+            for n in range(N):
+                acc = sum(val(A, ca, m, k, fmt_a) * two ** (int(SA[m, k // 32]) - 127) *
+                          val(B, cb, n, k, fmt_b) * two ** (int(SB[n, k // 32]) - 127)
+                          for k in range(K))
+                y = Fraction(0.75) * acc + Fraction(-0.5) * bf16_bits_to_fraction(int(C[m, n]))
+                want[m, n] = bf16_rne_by_search(y)
+        assert same_value(D, want), (i, fmt_a, fmt_b, D, want)
+
+
+def check_fp4_padded_exactness_flag(o):
+    """E2M1 0.5 x E5M2 2^-16 (granule 2^-17) in one sum with 6 x 57344 x 2^17
+    (~2^35.4): sum|ab| / granule ~ 2^52.4, which the oracle must report; a
+    granule taken two binades too coarse would miss it."""
+    K = 64
+    ca = np.zeros((1, K), dtype=np.int64)
+    ca[0, 0], ca[0, 32] = 1, 7                      # 0.5 and 6
+    A = pack_fp4_padded(ca)
+    B = np.zeros((1, K), dtype=np.uint8)
+    B[0, 0], B[0, 32] = 0x01, 0x7B                  # 2^-16 and 57344
+    SA = np.full((1, 2), 127, dtype=np.uint8)
+    SB = np.array([[127, 144]], dtype=np.uint8)     # second block x 2^17
+    _, _, _, inexact = o.gemm8(A, B, SA, SB, 1, 1, K, 5, 2)
+    assert inexact == 1, inexact
+    SB[0, 1] = 140                                  # ~2^48.4 granules: exact
+    _, _, _, inexact = o.gemm8(A, B, SA, SB, 1, 1, K, 5, 2)
+    assert inexact == 0, inexact
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
@@ -844,7 +953,8 @@ ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfield
               check_fp8_exactness_flag, check_quant8_golden, check_quant8_scale_rule,
               check_quant8_nearest_brute_force, check_quant8_matches_generator,
               check_fp6_golden, check_fp6_all_codes, check_fp6_layout, check_fp6_brute_force,
-              check_fp6_numpy_crosscheck]
+              check_fp6_numpy_crosscheck, check_fp4_padded_layout, check_fp4_padded_equals_packed,
+              check_fp4_padded_brute_force, check_fp4_padded_exactness_flag]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

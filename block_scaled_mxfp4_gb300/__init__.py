@@ -24,6 +24,7 @@ __all__ = [
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
     "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "MXFP8_E4M3", "MXFP8_E5M2", "MXFP6_E2M3", "MXFP6_E3M2",
+    "MXFP4_E2M1_PADDED",
     "gemm", "Plan",
 ]
 
@@ -33,7 +34,7 @@ HEADER = os.path.join(_ROOT, "include", "mxfp4_gemm.h")
 _LIB_NAME = "libmxfp4_gb300.so"
 
 MXFP4_OK = 0
-MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3, MXFP6_E3M2 = 0, 1, 3, 4
+MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3, MXFP6_E3M2, MXFP4_E2M1_PADDED = 0, 1, 3, 4, 5
 STATUS_NAMES = {0: "MXFP4_OK", -1: "MXFP4_ERR_INVALID_ARG", -2: "MXFP4_ERR_UNSUPPORTED_SHAPE",
                 -3: "MXFP4_ERR_MISALIGNED", -4: "MXFP4_ERR_WORKSPACE", -5: "MXFP4_ERR_CUDA",
                 -6: "MXFP4_ERR_TIMEOUT", -7: "MXFP4_ERR_ARCH"}

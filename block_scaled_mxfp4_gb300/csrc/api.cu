@@ -836,7 +836,8 @@ int mxfp4_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const
 // format's code in the kind::mxf8f6f4 instruction descriptor.
 static bool byte_format_ok(int fmt)
 {
-    return fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2 || fmt == MXFP6_E2M3 || fmt == MXFP6_E3M2;
+    return fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2 || fmt == MXFP6_E2M3 || fmt == MXFP6_E3M2 ||
+           fmt == MXFP4_E2M1_PADDED;
 }
 
 static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,

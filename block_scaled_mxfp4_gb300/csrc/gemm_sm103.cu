@@ -824,8 +824,8 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
 {
     if (!s.fp8)
         return launch_gemm_fmt<0>(a, tmP, tmQ, s, grid, stream);
-    // kind::mxf8f6f4 element codes: E4M3 0, E5M2 1, E2M3 3, E3M2 4.
-    auto known = [](int f) { return f == 0 || f == 1 || f == 3 || f == 4; };
+    // kind::mxf8f6f4 element codes: E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5.
+    auto known = [](int f) { return f == 0 || f == 1 || (f >= 3 && f <= 5); };
     if (!known(a.fmt_p) || !known(a.fmt_q))
         return cudaErrorInvalidValue;
     GemmArgs b = a;

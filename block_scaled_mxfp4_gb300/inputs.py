@@ -209,8 +209,12 @@ FP8_FORMATS = {"e4m3": (1, 8, 448.0), "e5m2": (2, 15, 57344.0)}
 # 6-bit formats: (oracle format code, largest element exponent, largest
 # finite, exponent bits, mantissa bits, bias).  Stored 16 codes per 16 bytes.
 FP6_FORMATS = {"e2m3": (3, 2, 7.5, 2, 3, 1), "e3m2": (4, 4, 28.0, 3, 2, 3)}
+# E2M1 in the same padded form (16 codes in the first 8 of every 16 bytes),
+# the form in which it mixes with the 8- and 6-bit formats.
+FP4P_FORMATS = {"e2m1": (5, 2, 6.0, 2, 1, 1)}
+SUBBYTE_FORMATS = {**FP6_FORMATS, **FP4P_FORMATS}
 BYTE_FORMATS = {**{k: v[0] for k, v in FP8_FORMATS.items()},
-                **{k: v[0] for k, v in FP6_FORMATS.items()}}
+                **{k: v[0] for k, v in SUBBYTE_FORMATS.items()}}
 
 
 @dataclasses.dataclass
@@ -221,8 +225,8 @@ class Problem8:
     M: int
     N: int
     K: int
-    fmt_a: str               # "e4m3", "e5m2" (one code per byte) or "e2m3", "e3m2"
-    fmt_b: str               # (6-bit: 16 codes packed in 12 of every 16 bytes)
+    fmt_a: str               # "e4m3", "e5m2" (one code per byte), "e2m3", "e3m2" (16
+    fmt_b: str               # codes in 12 of every 16 bytes) or "e2m1" (16 in 8 of 16)
     A: np.ndarray            # uint8 [M, K]
     B: np.ndarray            # uint8 [N, K]
     SA: np.ndarray           # uint8 [M, K/32] E8M0
@@ -263,14 +267,25 @@ def pack_fp6(codes: np.ndarray) -> np.ndarray:
     return out.reshape(rows, K)
 
 
+def pack_fp4_padded(codes: np.ndarray) -> np.ndarray:
+    """[rows, K] 4-bit codes (K % 16 == 0) -> [rows, K] bytes: every 16 codes
+    two per byte (element 2i in the low nibble of byte i) in 8 bytes, then 8
+    zero bytes."""
+    rows, K = codes.shape
+    c = codes.astype(np.uint8).reshape(rows, K // 16, 8, 2)
+    out = np.zeros((rows, K // 16, 16), dtype=np.uint8)
+    out[:, :, :8] = c[..., 0] | (c[..., 1] << 4)
+    return out.reshape(rows, K)
+
+
 def quantize_rows_fp6(x: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
-    """Quantise float64 rows [rows, K] (K % 32 == 0) to (packed FP6 bytes,
-    E8M0): scale 2^(floor(log2 amax) - emax) per 32 (the OCP MX rule), then
-    each element to the nearest FP6 value, ties to the even code, saturating
-    at the largest."""
+    """Quantise float64 rows [rows, K] (K % 32 == 0) to (padded FP6 or E2M1
+    bytes, E8M0): scale 2^(floor(log2 amax) - emax) per 32 (the OCP MX rule),
+    then each element to the nearest value of the format, ties to the even
+    code, saturating at the largest."""
     rows, K = x.shape
     assert K % 32 == 0
-    _, emax, top, ebits, mbits, bias = FP6_FORMATS[fmt]
+    _, emax, top, ebits, mbits, bias = SUBBYTE_FORMATS[fmt]
     amax = np.abs(x).reshape(rows, K // 32, 32).max(axis=2)
     _, e = np.frexp(amax)
     s = (e - 1 - emax).astype(np.int64)
@@ -287,8 +302,10 @@ def quantize_rows_fp6(x: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
     normal = sig >= (1 << mbits)
     efield = np.where(normal, binade + bias, 0)
     mfield = np.where(normal, sig - (1 << mbits), sig)
-    codes = (np.signbit(y).astype(np.int64) << 5) | (efield << mbits) | mfield
-    return pack_fp6(codes), (s + 127).astype(np.uint8)
+    width = 1 + ebits + mbits
+    codes = (np.signbit(y).astype(np.int64) << (width - 1)) | (efield << mbits) | mfield
+    packed = pack_fp6(codes) if width == 6 else pack_fp4_padded(codes)
+    return packed, (s + 127).astype(np.uint8)
 
 
 def _quantized_operand8(rng: np.random.Generator, rows: int, K: int, dist: str, fmt: str):
@@ -302,7 +319,7 @@ def _quantized_operand8(rng: np.random.Generator, rows: int, K: int, dist: str, 
             x = rng.uniform(-1.0, 1.0, size=(r1 - r0, K))
         else:
             raise ValueError(dist)
-        quant = quantize_rows_fp6 if fmt in FP6_FORMATS else quantize_rows_fp8
+        quant = quantize_rows_fp6 if fmt in SUBBYTE_FORMATS else quantize_rows_fp8
         codes[r0:r1], scales[r0:r1] = quant(x, fmt)
     return codes, scales
 
@@ -313,7 +330,7 @@ def make_problem8(name: str, M: int, N: int, K: int, seed: int, fmt_a: str, fmt_
     if K % 32 != 0:
         raise ValueError("K must be a multiple of 32 (one E8M0 scale per 32)")
     if fmt_a not in BYTE_FORMATS or fmt_b not in BYTE_FORMATS:
-        raise ValueError("formats are 'e4m3', 'e5m2', 'e2m3' or 'e3m2'")
+        raise ValueError("formats are 'e4m3', 'e5m2', 'e2m3', 'e3m2' or 'e2m1'")
     rng = np.random.default_rng(seed)
     A, SA = _quantized_operand8(rng, M, K, values, fmt_a)
     B, SB = _quantized_operand8(rng, N, K, values, fmt_b)

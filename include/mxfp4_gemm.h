@@ -200,9 +200,16 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
  *      consecutive elements of a row take 16 bytes, their codes packed
  *      little-endian into the first 12 (element i of the group in bits
  *      6i .. 6i+5, sign in the top bit of each code) and 4 padding bytes
- *      that are not read.  Either way one byte per element of footprint.
- *   fmt_a, fmt_b: MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3 or MXFP6_E3M2 (each
- *      value is the format's code in the kind::mxf8f6f4 instruction).
+ *      that are not read.  MXFP4_E2M1_PADDED: E2M1 (the MXFP4 element) in
+ *      the same kind of layout, so that it mixes with the formats above --
+ *      every 16 elements take 16 bytes, the first 8 holding two codes each
+ *      (element 2i of the group in the low nibble of byte i, as in packed
+ *      MXFP4 rows) and 8 padding bytes that are not read.  Either way one
+ *      byte per element of footprint.
+ *   fmt_a, fmt_b: MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3, MXFP6_E3M2 or
+ *      MXFP4_E2M1_PADDED (each value is the format's code in the
+ *      kind::mxf8f6f4 instruction).  For E2M1 x E2M1 with packed rows,
+ *      mxfp4_gemm is the faster path (kind::mxf4, twice the rate).
  *   Scales, C, D, alpha, beta, split_k, workspace, stream: as for
  *   mxfp4_gemm (mxfp8_gemm_workspace_size gives the workspace).
  * Runs the one-tile tcgen05 kernel (kind::mxf8f6f4, K = 32 per MMA; FP6 at
@@ -211,7 +218,7 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
  * counts elements).
  * Errors: as for mxfp4_gemm, plus MXFP4_ERR_INVALID_ARG for a bad format.
  */
-enum { MXFP8_E4M3 = 0, MXFP8_E5M2 = 1, MXFP6_E2M3 = 3, MXFP6_E3M2 = 4 };
+enum { MXFP8_E4M3 = 0, MXFP8_E5M2 = 1, MXFP6_E2M3 = 3, MXFP6_E3M2 = 4, MXFP4_E2M1_PADDED = 5 };
 int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                const void *A, int64_t lda, const void *B, int64_t ldb,
                const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,

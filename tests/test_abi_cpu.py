@@ -279,7 +279,7 @@ def test_mxfp8_prepacked_validates_before_device(L):
         for i, v in kw.items():
             a[int(i[1:])] = v
         return f(*a)
-    for bad in (2, 5, -1):                        # format codes other than 0, 1, 3, 4
+    for bad in (2, 6, -1):                        # format codes other than 0, 1, 3, 4, 5
         assert call(a10=bad) == -1
         assert call(a11=bad) == -1
     assert call(a8=None) == -1                    # relaid scale A

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 ABI_FMT = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2, "e2m3": mx.MXFP6_E2M3,
-           "e3m2": mx.MXFP6_E3M2}
+           "e3m2": mx.MXFP6_E3M2, "e2m1": mx.MXFP4_E2M1_PADDED}
 ORACLE_FMT = inputs.BYTE_FORMATS
 
 
@@ -115,6 +115,34 @@ def test_mxfp6_padding_bytes_are_not_read():
     for X in (p.A, p.B):
         v = X.reshape(X.shape[0], -1, 16)
         v[:, :, 12:] = rng.integers(0, 256, size=v[:, :, 12:].shape, dtype=np.uint8)
+    assert np.array_equal(run8(Dev8(p)), want)
+
+
+# E2M1 in the padded form (16 codes in 8 of every 16 bytes), mixed with the
+# 8- and 6-bit formats on either side.
+CASES4P = [
+    (128, 256, 512, "e2m1", "e4m3", 1.0, 0.0, None),
+    (300, 520, 1024, "e5m2", "e2m1", 0.5, 1.0, 1.0),
+    (1, 4096, 2048, "e2m1", "e2m3", 1.0, 0.0, None),
+    (64, 2048, 4096, "e3m2", "e2m1", 1.0, 1.0, 0.1),
+    (1000, 700, 288, "e2m1", "e2m1", 1.0, 0.0, None),
+]
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb,alpha,beta,cs", CASES4P,
+                         ids=[f"{c[0]}x{c[1]}x{c[2]}-{c[3]}x{c[4]}" for c in CASES4P])
+def test_padded_e2m1_mixed_parity(oracle_mod, M, N, K, fa, fb, alpha, beta, cs):
+    p = inputs.make_problem8("p4p", M, N, K, M + N + K + 4, fa, fb, "normal", alpha, beta, cs)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p)), Dref, sabs, p.alpha, f"padded e2m1 {M}x{N}x{K} {fa}x{fb}")
+
+
+def test_padded_e2m1_padding_bytes_are_not_read():
+    p = inputs.make_problem8("pad4", 256, 384, 512, 19, "e2m1", "e4m3", "normal", 1.0, 0.0, None)
+    want = run8(Dev8(p))
+    v = p.A.reshape(p.A.shape[0], -1, 16)
+    v[:, :, 8:] = np.random.default_rng(19).integers(0, 256, size=v[:, :, 8:].shape,
+                                                     dtype=np.uint8)
     assert np.array_equal(run8(Dev8(p)), want)
 
 

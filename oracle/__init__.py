@@ -329,11 +329,12 @@ def quantize(X_bits, rows, K):
     return Q, S
 
 
-def quantize8(X_bits, rows, K, fmt):
-    """MXFP8 quantiser (fmt E4M3 / E5M2): bf16 bits [rows, K] -> (codes
-    uint8 [rows, K], E8M0 scales uint8 [rows, K/32])."""
+def quantize8(X_bits, rows, K, fmt, fill=0):
+    """MXFP8 quantiser (fmt E4M3 / E5M2, or E2M3 / E3M2 / E2M1P into the
+    padded 16-per-16-bytes forms): bf16 bits [rows, K] -> (bytes uint8
+    [rows, K], E8M0 scales uint8 [rows, K/32])."""
     X = np.ascontiguousarray(X_bits, dtype=np.uint16)
-    Q = np.zeros((rows, K), dtype=np.uint8)
+    Q = np.full((rows, K), fill, dtype=np.uint8)       # fill: what the output held before
     S = np.zeros((rows, K // 32), dtype=np.uint8)
     r = lib().oracle_quantize8(rows, K, int(fmt), _ptr(X, ctypes.c_uint16), X.shape[1],
                                _ptr(Q, ctypes.c_uint8), K, _ptr(S, ctypes.c_uint8), K // 32)

@@ -619,7 +619,9 @@ int oracle_quantize(int rows, int K, const uint16_t *X, int64_t ldx, uint8_t *Q,
 
 /*
  * MXFP8 quantiser, the counterpart of oracle_quantize for 8-bit elements
- * (fmt 1 = E4M3, 2 = E5M2, decoded by oracle_fp8_value_q).  Per 1x32 block:
+ * (fmt 1 = E4M3, 2 = E5M2, decoded by oracle_fp8_value_q), and for the
+ * padded 6- and 4-bit forms (fmt 3 = E2M3, 4 = E3M2, 5 = E2M1; emax 2, 4
+ * and 2).  Per 1x32 block:
  *   1. amax = the largest magnitude of the block's 32 bf16 values;
  *   2. s = the largest integer with 2^(s + emax) <= amax, where emax is the
  *      exponent of the format's largest binade (8 for E4M3, whose largest
@@ -630,7 +632,8 @@ int oracle_quantize(int rows, int K, const uint16_t *X, int64_t ldx, uint8_t *Q,
  *   3. each element: |x| / 2^s rounded to the nearest finite value of the
  *      format, ties to the even code (round-half-even), saturating at the
  *      largest finite value, with the sign of x.
- * Q holds one code per byte (row stride ldq bytes).
+ * Q holds one code per byte (row stride ldq bytes), or for fmt 3-5 the
+ * padded form the GEMM reads, with zero padding bytes.
  */
 static int quant8_exponent(double amax, int emax)
 {
@@ -650,15 +653,25 @@ static int quant8_exponent(double amax, int emax)
     return s;
 }
 
+static double quant8_value(unsigned code, int fmt)
+{
+    if (fmt == 5)
+        return oracle_e2m1_value(code);
+    if (fmt >= 3)
+        return oracle_fp6_value(code, fmt);
+    return oracle_fp8_value(code, fmt);
+}
+
 static unsigned quant8_magnitude_code(double y, int fmt)
 {
-    const unsigned top = fmt == 1 ? 0x7Eu : 0x7Bu;     /* largest finite code */
-    if (y >= oracle_fp8_value(top, fmt))
+    static const unsigned kTop[6] = {0u, 0x7Eu, 0x7Bu, 0x1Fu, 0x1Fu, 0x7u};
+    const unsigned top = kTop[fmt];                   /* largest finite code */
+    if (y >= quant8_value(top, fmt))
         return top;
     unsigned best = 0u;
     double best_d = y;                                /* distance to code 0 (= 0.0) */
     for (unsigned c = 1u; c <= top; ++c) {
-        const double d = fabs(y - oracle_fp8_value(c, fmt));
+        const double d = fabs(y - quant8_value(c, fmt));
         if (d < best_d || (d == best_d && !(c & 1u))) {
             best = c;
             best_d = d;
@@ -667,13 +680,35 @@ static unsigned quant8_magnitude_code(double y, int fmt)
     return best;
 }
 
+/* Write element k's code into a row of the format's storage form. */
+static void quant8_store(uint8_t *row, int64_t k, unsigned code, int fmt)
+{
+    if (fmt <= 2) {
+        row[k] = (uint8_t)code;
+        return;
+    }
+    uint8_t *g = row + (k >> 4) * 16;
+    if ((k & 15) == 0)
+        memset(g, 0, 16);                             /* codes and padding */
+    if (fmt == 5) {
+        g[(k & 15) >> 1] |= (uint8_t)((k & 1) ? code << 4 : code);
+        return;
+    }
+    const int at = (int)(k & 15) * 6;                 /* first bit of the code */
+    g[at / 8] |= (uint8_t)(code << (at % 8));
+    if (at % 8 > 2)                                   /* it runs into the next byte */
+        g[at / 8 + 1] |= (uint8_t)(code >> (8 - at % 8));
+}
+
 int oracle_quantize8(int rows, int K, int fmt, const uint16_t *X, int64_t ldx, uint8_t *Q,
                      int64_t ldq, uint8_t *S, int64_t lds)
 {
     if (rows < 0 || K < 0 || (K % 32) != 0 || ldx < K || ldq < K || lds < K / 32 ||
-        (fmt != 1 && fmt != 2))
+        fmt < 1 || fmt > 5)
         return -1;
-    const int emax = fmt == 1 ? 8 : 15;
+    static const int kEmax[6] = {0, 8, 15, 2, 4, 2};
+    static const unsigned kSign[6] = {0u, 0x80u, 0x80u, 0x20u, 0x20u, 0x8u};
+    const int emax = kEmax[fmt];
     for (int r = 0; r < rows; ++r) {
         const uint16_t *x = X + (int64_t)r * ldx;
         for (int b = 0; b < K / 32; ++b) {
@@ -686,8 +721,8 @@ int oracle_quantize8(int rows, int K, int fmt, const uint16_t *X, int64_t ldx, u
                 const double v = oracle_bf16_to_double(x[b * 32 + i]);
                 unsigned code = quant8_magnitude_code(ldexp(fabs(v), -s), fmt);
                 if (signbit(v) != 0)
-                    code |= 0x80u;
-                Q[(int64_t)r * ldq + b * 32 + i] = (uint8_t)code;
+                    code |= kSign[fmt];
+                quant8_store(Q + (int64_t)r * ldq, b * 32 + i, code, fmt);
             }
         }
     }

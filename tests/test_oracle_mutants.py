@@ -91,14 +91,25 @@ MUTANTS = {
         "const unsigned pair = row[(k >> 4) * 16 + ((k & 15) >> 1)];",
         "const unsigned pair = row[(k >> 4) * 8 + ((k & 15) >> 1)];"),
     "fp4_padded_granule_too_coarse": ("*q = -1;                       /* E2M1", "*q = 1;                       /* E2M1"),
-    "fp6_decoded_as_fp8": ("    if (fmt >= 3)\n        return oracle_fp6", "    if (fmt > 3)\n        return oracle_fp6"),
+    "fp6_decoded_as_fp8": ("    if (fmt >= 3)\n        return oracle_fp6_value_q(",
+                           "    if (fmt > 3)\n        return oracle_fp6_value_q("),
     "fp8_granule_of_fp4": (
         "int g = qa + qb + (int)ea + (int)eb - 254;", "int g = (int)ea + (int)eb - 256;"),
     "quant8_ties_to_odd": (
         "if (d < best_d || (d == best_d && !(c & 1u))) {",
         "if (d < best_d || (d == best_d && (c & 1u))) {"),
     "quant8_e4m3_emax_7": (
-        "const int emax = fmt == 1 ? 8 : 15;", "const int emax = fmt == 1 ? 7 : 15;"),
+        "static const int kEmax[6] = {0, 8, 15, 2, 4, 2};",
+        "static const int kEmax[6] = {0, 7, 15, 2, 4, 2};"),
+    "quant8_e3m2_emax_3": (
+        "static const int kEmax[6] = {0, 8, 15, 2, 4, 2};",
+        "static const int kEmax[6] = {0, 8, 15, 2, 3, 2};"),
+    "quant8_e2m1_sign_bit_7": (
+        "static const unsigned kSign[6] = {0u, 0x80u, 0x80u, 0x20u, 0x20u, 0x8u};",
+        "static const unsigned kSign[6] = {0u, 0x80u, 0x80u, 0x20u, 0x20u, 0x80u};"),
+    "quant8_fp6_straddle_dropped": (
+        "if (at % 8 > 2)", "if (at % 8 > 4)"),
+    "quant8_padding_not_cleared": ("        memset(g, 0, 16);", "        memset(g, 0, 12);"),
     "quant8_scale_bias_126": ("(uint8_t)(127 + s);", "(uint8_t)(126 + s);"),
     "quant8_sign_dropped_for_zero": ("if (signbit(v) != 0)", "if (v < 0.0)"),
     "quant8_amax_half_block": (

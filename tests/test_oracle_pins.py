@@ -941,6 +941,69 @@ def check_fp4_padded_exactness_flag(o):
     assert inexact == 0, inexact
 
 
+def _sub_codes(Q, fmt):
+    """Test-side unpacking of a quantiser's padded output into codes."""
+    if fmt == 5:
+        rows, K = Q.shape
+        g = Q.reshape(rows, K // 16, 16)[:, :, :8].astype(np.int64)
+        return np.stack([g & 15, g >> 4], axis=3).reshape(rows, K)
+    return unpack_fp6(Q)
+
+
+def check_quant_sub_nearest_and_scale(o):
+    """FP6 and padded E2M1 quantisation: the scale satisfies 2^(s + emax) <=
+    amax < 2^(s + emax + 1) (emax 2, 4, 2); every code is the nearest value
+    of the format to |x| / 2^s, ties to the even code, saturating, with the
+    sign of x; the padding bytes are written as zeros."""
+    rng = np.random.default_rng(24)
+    rows, K = 4, 96
+    x = rng.standard_normal((rows, K)) * 5.0
+    x[0, :7] = [0.0, -0.0, 1.0625, -3.0, 1e-3, 250.0, -1e-30]
+    bits = _bf16_bits(x)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    e2m1 = page_e2m1_values()
+    for fmt, emax, sign in ((3, 2, 0x20), (4, 4, 0x20), (5, 2, 0x8)):
+        top = 7 if fmt == 5 else 31
+        vals = [e2m1[c] if fmt == 5 else fp6_fraction(c, fmt) for c in range(top + 1)]
+        Q, S = o.quantize8(bits, rows, K, fmt, fill=0xA5)
+        pad = Q.reshape(rows, K // 16, 16)[:, :, (8 if fmt == 5 else 12):]
+        assert not pad.any(), fmt
+        codes = _sub_codes(Q, fmt)
+        for r in range(rows):
+            for b in range(K // 32):
+                s = int(S[r, b]) - 127
+                amax = max(abs(Fraction(v)) for v in xv[r, 32 * b:32 * b + 32])
+                if amax:
+                    assert Fraction(2) ** (s + emax) <= amax < Fraction(2) ** (s + emax + 1)
+            for k in range(K):
+                s = int(S[r, k // 32]) - 127
+                y = abs(Fraction(xv[r, k])) / Fraction(2) ** s
+                if y >= vals[top]:
+                    want = top
+                else:
+                    d = [abs(y - v) for v in vals]
+                    cands = [c for c in range(top + 1) if d[c] == min(d)]
+                    want = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+                if np.signbit(xv[r, k]):
+                    want |= sign
+                assert int(codes[r, k]) == want, (fmt, r, k, xv[r, k], s, codes[r, k], want)
+
+
+def check_quant_sub_matches_generator(o):
+    """The input generator's sub-byte rule (numpy: scale, round half to even
+    on the significand, field assembly, packing) gives the same bytes."""
+    from block_scaled_mxfp4_gb300 import inputs
+    rng = np.random.default_rng(25)
+    x = rng.standard_normal((16, 512)) * np.ldexp(1.0, rng.integers(-8, 8, size=(16, 1)))
+    bits = _bf16_bits(x)
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for name, fmt in (("e2m3", 3), ("e3m2", 4), ("e2m1", 5)):
+        Qg, Sg = inputs.quantize_rows_fp6(xv, name)
+        Qo, So = o.quantize8(bits, 16, 512, fmt)
+        assert np.array_equal(So, Sg), name
+        assert np.array_equal(Qo, Qg), name
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
@@ -954,7 +1017,8 @@ ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfield
               check_quant8_nearest_brute_force, check_quant8_matches_generator,
               check_fp6_golden, check_fp6_all_codes, check_fp6_layout, check_fp6_brute_force,
               check_fp6_numpy_crosscheck, check_fp4_padded_layout, check_fp4_padded_equals_packed,
-              check_fp4_padded_brute_force, check_fp4_padded_exactness_flag]
+              check_fp4_padded_brute_force, check_fp4_padded_exactness_flag,
+              check_quant_sub_nearest_and_scale, check_quant_sub_matches_generator]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

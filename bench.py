@@ -109,6 +109,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="large",
                     choices=["tiny", "decode", "mid", "large", "skinny", "quantize", "quantize8",
+                             "quantize6",
                              "large8", "decode8", "mixed8", "large6", "mixed6"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -234,7 +235,7 @@ def run_reference(args, rank):
     if rank != 0:
         return
     from block_scaled_mxfp4_gb300 import inputs
-    if args.workload in ("quantize", "quantize8"):
+    if args.workload in ("quantize", "quantize8", "quantize6"):
         run_reference_quantize(args)
         return
     fp8 = args.workload in inputs.WORKLOADS8
@@ -263,6 +264,19 @@ def run_reference(args, rank):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+# --workload -> (format name, ABI code, oracle code, kernel) of mxfp8_quantize runs.
+QUANT_BYTE = {"quantize8": ("mxfp8 e4m3", 0, 1, "quantize8_kernel<0>"),
+              "quantize6": ("mxfp6 e2m3 (padded)", 3, 3, "quantize8_kernel<3>")}
+
+
+def quant_metric(workload):
+    if workload == "quantize8":
+        return "MXFP8 quantiser bandwidth (bf16 -> E4M3 codes + E8M0 scales)"
+    if workload == "quantize6":
+        return "MXFP6 quantiser bandwidth (bf16 -> padded E2M3 codes + E8M0 scales)"
+    return "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)"
 
 
 METRIC8 = "MXFP8 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP8 peak / HBM roofline"
@@ -418,13 +432,14 @@ def run_reference_quantize(args):
     xbits = inputs.f32_to_bf16_bits(
         np.random.default_rng(5).standard_normal((rows, K), dtype=np.float32))
     nrows = 64
-    fp8 = args.workload == "quantize8"
+    fp8 = args.workload in QUANT_BYTE
+    name, _, ofmt, _ = QUANT_BYTE.get(args.workload, (None, None, None, None))
     per_elem = 2 + (1 if fp8 else 0.5) + 1 / 32
 
     def one(i):
         chunk = xbits[(i * nrows) % rows:][:nrows]
         if fp8:
-            oracle.quantize8(chunk, nrows, K, oracle.E4M3)
+            oracle.quantize8(chunk, nrows, K, ofmt)
         else:
             oracle.quantize(chunk, nrows, K)
 
@@ -438,8 +453,7 @@ def run_reference_quantize(args):
     value = args.steps * nrows * K * per_elem / sum(times) / 1e9
     line = {
         "impl": "reference",
-        "metric": ("MXFP8 quantiser bandwidth (bf16 -> E4M3 codes + E8M0 scales)" if fp8 else
-                   "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)"),
+        "metric": quant_metric(args.workload),
         "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -475,7 +489,8 @@ def run_quantize(args, world, rank, local_rank):
     rng = np.random.default_rng(5)
     xbits = inputs.f32_to_bf16_bits(rng.standard_normal((rows, K), dtype=np.float32))
     X = torch.from_numpy(xbits.view(np.int16)).to(dev)
-    fp8 = args.workload == "quantize8"          # E4M3 codes, one per byte
+    fp8 = args.workload in QUANT_BYTE           # one byte per element (8-bit or padded 6-bit)
+    name, afmt, ofmt, kname = QUANT_BYTE.get(args.workload, (None, None, None, "quantize_kernel"))
     qcols = K if fp8 else K // 2
     Q = torch.empty((rows, qcols), dtype=torch.uint8, device=dev)
     S = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev)
@@ -485,7 +500,7 @@ def run_quantize(args, world, rank, local_rank):
 
     def step():
         if fp8:
-            mx.mxfp8_quantize(Q, K, S, K // 32, X, K, rows, K, mx.MXFP8_E4M3, stream)
+            mx.mxfp8_quantize(Q, K, S, K // 32, X, K, rows, K, afmt, stream)
         else:
             mx.mxfp4_quantize(Q, K, S, K // 32, X, K, rows, K, stream)
 
@@ -536,7 +551,7 @@ def run_quantize(args, world, rank, local_rank):
         reps = 0
         while time.perf_counter() - t0 < 10.0:
             if fp8:
-                oracle.quantize8(xbits[reps * nrows % rows:][:nrows], nrows, K, oracle.E4M3)
+                oracle.quantize8(xbits[reps * nrows % rows:][:nrows], nrows, K, ofmt)
             else:
                 oracle.quantize(xbits[reps * nrows % rows:][:nrows], nrows, K)
             reps += 1
@@ -545,11 +560,10 @@ def run_quantize(args, world, rank, local_rank):
                "kind": "oracle", "sample": f"{reps} x {nrows} rows of the {rows}x{K} input "
                                            f"({dt:.1f} s, one thread)"}
     line = {
-        "metric": ("MXFP8 quantiser bandwidth (bf16 -> E4M3 codes + E8M0 scales)" if fp8 else
-                   "MXFP4 quantiser bandwidth (bf16 -> E2M1 codes + E8M0 scales)"),
+        "metric": quant_metric(args.workload),
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->mxfp8 e4m3" if fp8 else "bf16->mxfp4",
+        "vs_baseline": None, "dtype": f"bf16->{name}" if fp8 else "bf16->mxfp4",
         "data": "synthetic",
         "config": {"workload": f"{args.workload} rows={rows} K={K}", "rows": rows, "K": K,
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
@@ -558,7 +572,7 @@ def run_quantize(args, world, rank, local_rank):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                      "traffic": None if fp8 else recorded_traffic("quantize", "quantize_kernel"),
-                     "kernel": "quantize8_kernel<0>" if fp8 else "quantize_kernel", "kernel_ms": ms,
+                     "kernel": kname, "kernel_ms": ms,
                      "algorithmic_bytes": nbytes, "peak_source": f"{peak_src} HBM copy bandwidth"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -582,7 +596,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
-    if args.workload in ("quantize", "quantize8"):
+    if args.workload in ("quantize", "quantize8", "quantize6"):
         run_quantize(args, world, rank, local_rank)
         return
     if args.workload in ("large8", "decode8", "mixed8", "large6", "mixed6"):

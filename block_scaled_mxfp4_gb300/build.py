@@ -9,6 +9,7 @@ is newer than the library.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import shutil
@@ -55,6 +56,16 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if not force and not verbose_ptxas and up_to_date():
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)
+    # One builder at a time (parallel test workers share the object files);
+    # a process that waited finds the library fresh and returns.
+    with open(os.path.join(OBJDIR, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not verbose_ptxas and up_to_date():
+            return LIB
+        return _build_locked(verbose_ptxas)
+
+
+def _build_locked(verbose_ptxas: bool) -> str:
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 

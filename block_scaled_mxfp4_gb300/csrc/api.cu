@@ -1207,7 +1207,7 @@ int mxfp8_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, in
                    int rows, int K, int fmt, void *stream)
 {
     if (!Q || !S || !X || rows < 1 || K < 32 || (K % 32) != 0 || ldx < K || ldq < K ||
-        lds < K / 32 || (fmt != MXFP8_E4M3 && fmt != MXFP8_E5M2))
+        lds < K / 32 || !byte_format_ok(fmt))
         return MXFP4_ERR_INVALID_ARG;
     if (!aligned(X, 16) || (ldx % 8) != 0 || !aligned(Q, 16) || (ldq % 16) != 0)
         return MXFP4_ERR_MISALIGNED;

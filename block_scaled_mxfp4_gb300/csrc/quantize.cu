@@ -107,9 +107,11 @@ __global__ void __launch_bounds__(kQuantThreads)
 }
 
 // ---------------------------------------------------------------- MXFP8 --
-// bf16 rows -> one E4M3 / E5M2 code per element [rows, K] + E8M0 scales.
+// bf16 rows -> one E4M3 / E5M2 code per element [rows, K] (or E2M3 / E3M2 /
+// E2M1 codes in the padded forms the GEMM reads) + E8M0 scales.
 // Per 1x32 block: s = floor(log2 amax) - emax (emax 8 for E4M3, 15 for
-// E5M2: the exponent of the format's largest binade, the OCP MX rule;
+// E5M2, 2 for E2M3 and E2M1, 4 for E3M2: the exponent of the format's
+// largest binade, the OCP MX rule;
 // s = 0 for an all-zero block; clamped to [-127, 127]); codes = x / 2^s
 // converted with cvt.rn.satfinite (nearest, ties to even, saturating at the
 // largest finite value).  One thread per block; its 32 codes leave in two
@@ -146,13 +148,49 @@ __device__ __forceinline__ uint32_t f8x2(float lo, float hi)
     return r;
 }
 
-// FMT 0: E4M3, 1: E5M2 (the ABI's format codes).
+// Two floats -> two 6-bit codes: `lo` in bits 0-5, `hi` in bits 8-13
+// (FMT 3: E2M3, 4: E3M2).
+template <int FMT>
+__device__ __forceinline__ uint32_t f6x2(float lo, float hi)
+{
+    uint32_t r;
+    if constexpr (FMT == 3)
+        asm("{\n\t.reg .b16 t;\n\t"
+            "cvt.rn.satfinite.e2m3x2.f32 t, %1, %2;\n\t"
+            "cvt.u32.u16 %0, t;\n\t}"
+            : "=r"(r)
+            : "f"(hi), "f"(lo));
+    else
+        asm("{\n\t.reg .b16 t;\n\t"
+            "cvt.rn.satfinite.e3m2x2.f32 t, %1, %2;\n\t"
+            "cvt.u32.u16 %0, t;\n\t}"
+            : "=r"(r)
+            : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16 six-bit codes (c[i] < 64) -> the padded 16-byte group the GEMM reads:
+// code i in bits 6i .. 6i+5 of the first 12 bytes (little-endian), then 4
+// zero bytes.
+__device__ __forceinline__ uint4 pack_fp6_group(const uint32_t *c)
+{
+    uint4 g;
+    g.x = c[0] | (c[1] << 6) | (c[2] << 12) | (c[3] << 18) | (c[4] << 24) | (c[5] << 30);
+    g.y = (c[5] >> 2) | (c[6] << 4) | (c[7] << 10) | (c[8] << 16) | (c[9] << 22) | (c[10] << 28);
+    g.z = (c[10] >> 4) | (c[11] << 2) | (c[12] << 8) | (c[13] << 14) | (c[14] << 20) |
+          (c[15] << 26);
+    g.w = 0u;
+    return g;
+}
+
+// FMT: the ABI's format codes -- 0: E4M3, 1: E5M2 (one code per byte);
+// 3: E2M3, 4: E3M2, 5: E2M1 (the padded 16-elements-per-16-bytes forms).
 template <int FMT>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize8_kernel(uint8_t *__restrict__ Q, int64_t ldq, uint8_t *__restrict__ S, int64_t lds,
                      const uint16_t *__restrict__ X, int64_t ldx, int rows, int kblocks)
 {
-    constexpr int kEmax = FMT == 0 ? 8 : 15;
+    constexpr int kEmax = FMT == 0 ? 8 : FMT == 1 ? 15 : FMT == 4 ? 4 : 2;
     const int64_t total = static_cast<int64_t>(rows) * kblocks;
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -175,17 +213,47 @@ __global__ void __launch_bounds__(kQuantThreads)
         const int s = block_exponent8(amax, kEmax);
         const float inv = s == 127 ? __uint_as_float(0x00400000u)
                                    : __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-        uint32_t out[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            // elements 4q .. 4q+3 (two bf16 pairs) -> one 32-bit word of codes
-            const uint32_t lo = f8x2<FMT>(bf16_lo(w[2 * q]) * inv, bf16_hi(w[2 * q]) * inv);
-            const uint32_t hi = f8x2<FMT>(bf16_lo(w[2 * q + 1]) * inv, bf16_hi(w[2 * q + 1]) * inv);
-            out[q] = lo | (hi << 16);
-        }
         uint4 *dst = reinterpret_cast<uint4 *>(Q + r * ldq + b * 32);
-        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        if constexpr (FMT <= 1) {
+            uint32_t out[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                // elements 4q .. 4q+3 (two bf16 pairs) -> one 32-bit word of codes
+                const uint32_t lo = f8x2<FMT>(bf16_lo(w[2 * q]) * inv, bf16_hi(w[2 * q]) * inv);
+                const uint32_t hi =
+                    f8x2<FMT>(bf16_lo(w[2 * q + 1]) * inv, bf16_hi(w[2 * q + 1]) * inv);
+                out[q] = lo | (hi << 16);
+            }
+            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        } else if constexpr (FMT == 5) {
+            // Each 16 elements: 8 bytes of nibble pairs, then 8 zero bytes.
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t word[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t v = 0u;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t p = w[8 * h + 4 * q + j];
+                        v |= e2m1x2(bf16_lo(p) * inv, bf16_hi(p) * inv) << (8 * j);
+                    }
+                    word[q] = v;
+                }
+                dst[h] = make_uint4(word[0], word[1], 0u, 0u);
+            }
+        } else {
+            uint32_t c[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t v = f6x2<FMT>(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv);
+                c[2 * i] = v & 0x3Fu;
+                c[2 * i + 1] = (v >> 8) & 0x3Fu;
+            }
+            dst[0] = pack_fp6_group(c);
+            dst[1] = pack_fp6_group(c + 16);
+        }
         S[r * lds + b] = static_cast<uint8_t>(s + 127);
     }
 }
@@ -203,12 +271,15 @@ cudaError_t launch_quantize8(uint8_t *Q, int64_t ldq, uint8_t *S, int64_t lds, c
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    if (fmt == 0)
-        quantize8_kernel<0><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
-            Q, ldq, S, lds, X, ldx, rows, kblocks);
-    else
-        quantize8_kernel<1><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
-            Q, ldq, S, lds, X, ldx, rows, kblocks);
+    const unsigned g = static_cast<unsigned>(blocks);
+    switch (fmt) {
+    case 0: quantize8_kernel<0><<<g, kQuantThreads, 0, stream>>>(Q, ldq, S, lds, X, ldx, rows, kblocks); break;
+    case 1: quantize8_kernel<1><<<g, kQuantThreads, 0, stream>>>(Q, ldq, S, lds, X, ldx, rows, kblocks); break;
+    case 3: quantize8_kernel<3><<<g, kQuantThreads, 0, stream>>>(Q, ldq, S, lds, X, ldx, rows, kblocks); break;
+    case 4: quantize8_kernel<4><<<g, kQuantThreads, 0, stream>>>(Q, ldq, S, lds, X, ldx, rows, kblocks); break;
+    case 5: quantize8_kernel<5><<<g, kQuantThreads, 0, stream>>>(Q, ldq, S, lds, X, ldx, rows, kblocks); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -343,15 +343,18 @@ int mxfp4_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, in
 /*
  * MXFP8 quantiser: bf16 rows -> the operand format mxfp8_gemm takes.
  *   X  bf16 [rows, ldx]   input, ldx >= K, ldx % 8 == 0, 16-byte aligned
- *   Q  uint8 [rows, ldq]  output codes, one per element (E4M3 or E5M2 by
- *                         fmt = MXFP8_E4M3 / MXFP8_E5M2), ldq >= K,
- *                         ldq % 16 == 0, 16-byte aligned
+ *   Q  uint8 [rows, ldq]  output codes in mxfp8_gemm's operand form for
+ *                         fmt: one per byte (MXFP8_E4M3 / MXFP8_E5M2), or
+ *                         the padded 16-per-16-bytes forms (MXFP6_E2M3 /
+ *                         MXFP6_E3M2 / MXFP4_E2M1_PADDED, padding written as
+ *                         zeros), ldq >= K, ldq % 16 == 0, 16-byte aligned
  *   S  uint8 [rows, lds]  output E8M0 scale codes, one per 1x32 block
  * Per block: s = floor(log2 amax) - emax, with emax the exponent of the
- * format's largest binade (8 for E4M3, 15 for E5M2: the OCP MX scale rule);
- * 0 for an all-zero block; clamped to [-127, 127]; scale code s + 127.  Each
- * element is x / 2^s rounded to the nearest finite value of the format
- * (ties to even, saturating at 448 / 57344) with the sign of x.  Inputs must
+ * format's largest binade (8 for E4M3, 15 for E5M2, 2 for E2M3 and E2M1, 4
+ * for E3M2: the OCP MX scale rule); 0 for an all-zero block; clamped to
+ * [-127, 127]; scale code s + 127.  Each element is x / 2^s rounded to the
+ * nearest finite value of the format (ties to even, saturating at 448 /
+ * 57344 / 7.5 / 28 / 6) with the sign of x.  Inputs must
  * be finite.  rows >= 1, K >= 32, K % 32 == 0.  Errors: MXFP4_ERR_INVALID_ARG
  * (null pointer, sizes, strides, format), MXFP4_ERR_MISALIGNED, device
  * errors.  Enqueued on `stream`.

@@ -259,9 +259,9 @@ def _run_q8(bits, fmt, ldq_pad=0, ldx_pad=0, lds_pad=0):
     return Q.cpu().numpy(), S.cpu().numpy()
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m3", "e3m2", "e2m1"])
 def test_mxfp8_quantize_bit_exact(oracle_mod, fmt):
-    rng = np.random.default_rng(31 if fmt == "e4m3" else 32)
+    rng = np.random.default_rng(31 + list(ABI_FMT).index(fmt))
     K = 1024
     x = rng.standard_normal((120, K)) * np.ldexp(1.0, rng.integers(-40, 40, size=(120, 1)))
     bits = _bf16(np.concatenate([x, _special_rows(K)]))
@@ -295,3 +295,24 @@ def test_mxfp8_quantize_then_gemm(oracle_mod):
     p = inputs.Problem8("q8gemm", M, N, K, "e4m3", "e5m2", QA, w.A, SA, w.SA, None, 1.0, 0.0, 0)
     Dref, sabs = oracle_full(oracle_mod, p)
     assert_within_bound(run8(Dev8(p)), Dref, sabs, 1.0, "quantise -> mxfp8 gemm")
+
+
+@pytest.mark.parametrize("fa,fb", [("e2m3", "e3m2"), ("e2m1", "e2m3")])
+def test_subbyte_quantize_strided_then_gemm(oracle_mod, fa, fb):
+    """Both operands quantised on the GPU into padded forms, with row strides
+    and a pre-filled output: bit-exact codes (padding written as zeros, the
+    bytes past K untouched), then the GEMM on them within the bound."""
+    rng = np.random.default_rng(36)
+    M, N, K = 96, 320, 512
+    xa = _bf16(rng.standard_normal((M, K)) * 3.0)
+    xb = _bf16(rng.standard_normal((N, K)) * 0.25)
+    QA, SA = _run_q8(xa, fa, ldq_pad=32, ldx_pad=8, lds_pad=3)
+    QB, SB = _run_q8(xb, fb)
+    for Q, S, x, f, rows in ((QA, SA, xa, fa, M), (QB, SB, xb, fb, N)):
+        Qr, Sr = oracle_mod.quantize8(x, rows, K, ORACLE_FMT[f])
+        assert np.array_equal(Q[:, :K], Qr) and np.array_equal(S[:, :K // 32], Sr), f
+    assert (QA[:, K:] == 0xAB).all() and (SA[:, K // 32:] == 0xCD).all()
+    p = inputs.Problem8("qsub", M, N, K, fa, fb, np.ascontiguousarray(QA[:, :K]), QB,
+                        np.ascontiguousarray(SA[:, :K // 32]), SB, None, 1.0, 0.0, 0)
+    Dref, sabs = oracle_full(oracle_mod, p)
+    assert_within_bound(run8(Dev8(p)), Dref, sabs, 1.0, f"quantise -> {fa} x {fb} gemm")

@@ -18,13 +18,15 @@ from typing import Optional
 
 __all__ = [
     "Mxfp4Error", "lib", "library_path", "header_functions",
-    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host", "mxfp4_scale_relayout", "mxfp4_scale_relayout2", "mxfp4_quantize",
+    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host",
+    "mxfp4_scale_relayout", "mxfp4_scale_relayout2", "mxfp4_quantize",
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
-    "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit", "mxfp4_strerror", "mxfp4_version",
+    "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit",
+    "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
-    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "MXFP8_E4M3", "MXFP8_E5M2", "MXFP6_E2M3", "MXFP6_E3M2",
-    "MXFP4_E2M1_PADDED",
+    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize",
+    "MXFP8_E4M3", "MXFP8_E5M2", "MXFP6_E2M3", "MXFP6_E3M2", "MXFP4_E2M1_PADDED",
     "gemm", "Plan",
 ]
 

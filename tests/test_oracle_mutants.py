@@ -90,7 +90,8 @@ MUTANTS = {
     "fp4_padded_padding_read_as_data": (
         "const unsigned pair = row[(k >> 4) * 16 + ((k & 15) >> 1)];",
         "const unsigned pair = row[(k >> 4) * 8 + ((k & 15) >> 1)];"),
-    "fp4_padded_granule_too_coarse": ("*q = -1;                       /* E2M1", "*q = 1;                       /* E2M1"),
+    "fp4_padded_granule_too_coarse": ("*q = -1;                       /* E2M1",
+                                      "*q = 1;                       /* E2M1"),
     "fp6_decoded_as_fp8": ("    if (fmt >= 3)\n        return oracle_fp6_value_q(",
                            "    if (fmt > 3)\n        return oracle_fp6_value_q("),
     "fp8_granule_of_fp4": (

@@ -1004,7 +1004,8 @@ def check_quant_sub_matches_generator(o):
         assert np.array_equal(Qo, Qg), name
 
 
-ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0, check_nibble_order,
+ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0,
+              check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
               check_identity, check_identity_scaled, check_alpha_beta,
               check_brute_force, check_all_code_pairs, check_numpy_crosscheck,

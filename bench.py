@@ -220,10 +220,15 @@ def oracle_throughput(p, seconds, seed):
         return time.perf_counter() - t0
 
     cores = oracle.host_cores()
-    probe = max(cores * 4, 64)
-    t = run(probe)
-    count = int(max(probe, probe * seconds / max(t, 1e-6)))
+    count = max(cores * 4, 64)
     t = run(count)
+    # A small probe is dominated by thread start-up, so scale up until the
+    # timed sample itself lasts most of the requested time.
+    for _ in range(4):
+        if t >= 0.7 * seconds:
+            break
+        count = int(max(2 * count, count * seconds / max(t, 1e-6)))
+        t = run(count)
     flops = 2.0 * p.K * count
     desc = (f"{count} random (m, n) outputs of the {p.M}x{p.N}x{p.K} workload, full K each "
             f"({flops / 2:.3g} MACs, {t:.1f} s)")

@@ -245,7 +245,8 @@ def run_reference(args, rank):
         return
     fp8 = args.workload in inputs.WORKLOADS8
     p = inputs.workload8(args.workload) if fp8 else inputs.workload(args.workload)
-    per_step = 4.0 if args.steps <= 20 else max(0.5, 80.0 / args.steps)
+    # About 2.5 minutes of oracle time in all, at most 4 s per step.
+    per_step = min(4.0, 150.0 / max(1, args.steps))
     for i in range(args.warmup):
         oracle_throughput(p, min(per_step, 1.0), 1000 + i)
     vals, times, desc, cores = [], [], "", 0

@@ -284,6 +284,10 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     int64_t best_waves = 0;
     double best_occ = 0, best_ratio = 0;
     for (int i = 0; i < nc; ++i) {
+        // The one-tile launch puts the tile columns on grid.y (at most 65535):
+        // a tile that needs more columns than that is not a candidate.
+        if (!persistent && (Q + cands[i].tile_n - 1) / cands[i].tile_n > 65535)
+            continue;
         const int64_t tiles = ((P + kTileM - 1) / kTileM) * ((Q + cands[i].tile_n - 1) / cands[i].tile_n);
         const int64_t slots = static_cast<int64_t>(sms) * cands[i].ctas_per_sm;
         const int64_t waves = (tiles + slots - 1) / slots;
@@ -299,6 +303,8 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
             best_ratio = ratio;
         }
     }
+    if (best < 0)
+        return MXFP4_ERR_UNSUPPORTED_SHAPE;
     Candidate c = cands[best];
     // Tuning override for sweeps: MXFP4_TILE="tile_n:stages" picks another
     // compiled configuration of the same swap mode (ignored if there is none).
@@ -315,7 +321,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     }
     const int64_t gx = (P + kTileM - 1) / kTileM;
     const int64_t gy = (Q + c.tile_n - 1) / c.tile_n;
-    if (gy > 65535 || gx > 0x7FFFFFFF)
+    if ((!persistent && gy > 65535) || gx > 0x7FFFFFFF || gx * gy > 0x7FFFFFFF)
         return MXFP4_ERR_UNSUPPORTED_SHAPE;
     const int64_t tiles = gx * gy;
     const int64_t slots = static_cast<int64_t>(sms) * c.ctas_per_sm;

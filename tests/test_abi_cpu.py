@@ -386,3 +386,16 @@ def test_plan_gemv_override(L, monkeypatch):
     assert mx.mxfp4_plan_gemm(3, 8192, 8192, 0, 152).gemv == 0
     assert mx.mxfp4_plan_gemm(1, 600, 8192, 0, 152).gemv == 0
     assert mx.mxfp4_plan_gemm(1, 8192, 8192, 2, 152).gemv == 0
+
+
+def test_plan_respects_the_grid_limit():
+    """The one-tile launch puts tile columns on grid.y (<= 65535): the plan
+    takes a wider tile when the narrower one would exceed it, rejects the
+    shape when no tile fits, and the persistent pair kernel has no such limit."""
+    p = mx.mxfp4_plan_gemm(100, 65535 * 256, 64, 0, 152)
+    assert p.tile_n == 256 and p.grid_y == 65535 and p.pair == 0
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.mxfp4_plan_gemm(100, 65535 * 256 + 1, 64, 0, 152)
+    assert e.value.status == -2                       # MXFP4_ERR_UNSUPPORTED_SHAPE
+    q = mx.mxfp4_plan_gemm(300, 65535 * 256 + 1, 256, 0, 152)
+    assert q.pair == 1 and q.grid_y == 1

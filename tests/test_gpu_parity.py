@@ -807,3 +807,33 @@ def test_cuda_graph_host_entry_and_mxfp8():
     g8.replay()
     torch.cuda.synchronize()
     assert np.array_equal(d_to_bits(D8), ref8)
+
+
+@pytest.mark.parametrize("M,N,K", [(100, 65535 * 256, 64), (1 << 22, 1024, 64)],
+                         ids=["grid-y-65535", "D-beyond-2^31-elements"])
+def test_maximum_sizes_sampled(oracle_mod, M, N, K):
+    """The largest one-tile grid (65535 tile columns of 256) and an output of
+    more than 2^31 elements (64-bit row offsets, pair kernel), checked on
+    sampled outputs that include the first and last rows and columns."""
+    rng = np.random.default_rng(M + N)
+    A = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    SA = rng.integers(120, 135, size=(M, K // 32), dtype=np.uint8)
+    SB = rng.integers(120, 135, size=(N, K // 32), dtype=np.uint8)
+    d = lambda x: torch.from_numpy(x).cuda()
+    dA, dB, dSA, dSB = d(A), d(B), d(SA), d(SB)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.mxfp4_gemm_workspace_size(M, N, K, 0)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_gemm(D, N, None, 0, dA, K, dB, K, dSA, K // 32, dSB, K // 32, 1.0, 0.0,
+                  M, N, K, 0, ws, wsb)
+    torch.cuda.synchronize()
+    pairs = np.concatenate([sample_pairs(M, N, 600, 7),
+                            np.array([[M - 1, N - 1], [M - 1, 0], [0, N - 1]], dtype=np.int64)])
+    idx = torch.from_numpy(pairs).cuda()
+    got = D[idx[:, 0], idx[:, 1]].view(torch.int16).cpu().numpy().view(np.uint16)
+    del D
+    torch.cuda.empty_cache()
+    Dr, _, sabs, inexact = oracle_mod.gemm_sampled(A, B, SA, SB, M, N, K, pairs)
+    assert inexact == 0
+    assert_within_bound(got, Dr, sabs, 1.0, f"maximum sizes {M}x{N}x{K}")

@@ -55,8 +55,17 @@ def replica_throughput(world, flops_per_step, steps, total_ms):
     return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
+# Device code and launchers of the GEMM kernels: a DRAM counter capture stays
+# valid while these are unchanged and the plan launches the same configuration.
 KERNEL_SOURCES = ("gemm_pair.cuh", "gemm_sm103.cu", "gemm_persistent.cuh", "ptx.cuh",
-                  "internal.h", "api.cu")
+                  "internal.h")
+
+
+def plan_key(plan):
+    """The launch configuration a traffic capture was taken with."""
+    return (f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k} stages {plan.stages} split "
+            f"{plan.split_k} swap {plan.swap_ab} pair {plan.pair} cluster {plan.pair_cluster} "
+            f"relayout {plan.relayout_pass} grid {plan.grid_x}x{plan.grid_y}x{plan.grid_z}")
 
 
 def kernel_sources_sha1(names=KERNEL_SOURCES):
@@ -70,10 +79,10 @@ def kernel_sources_sha1(names=KERNEL_SOURCES):
     return h.hexdigest()
 
 
-def recorded_traffic(workload, kernel):
+def recorded_traffic(workload, kernel, plan=None):
     """DRAM bytes (read + write) of one launch of `kernel` on `workload` from
     profiles/traffic.json (an ncu counter capture), or None if there is no
-    capture for these sources."""
+    capture for these sources and, when the record names one, this plan."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(workload)
@@ -82,6 +91,8 @@ def recorded_traffic(workload, kernel):
     if not rec or rec.get("kernel") != kernel:
         return None
     if rec.get("sources_sha1") != kernel_sources_sha1(tuple(rec.get("sources", KERNEL_SOURCES))):
+        return None
+    if plan is not None and "plan" in rec and rec["plan"] != plan_key(plan):
         return None
     return rec["dram_bytes_read"] + rec["dram_bytes_write"]
 
@@ -386,7 +397,7 @@ def run_mxfp8(args, world, rank, local_rank):
                 "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
                                f"{FP8_PER_BF16:g} (nominal dense FP8/bf16 ratio"
                                + ("; FP6 runs at the FP8 rate in kind::mxf8f6f4)" if fp6 else ")")}
-    traffic = recorded_traffic(args.workload, "gemm_mxf4_kernel")
+    traffic = recorded_traffic(args.workload, "gemm_mxf4_kernel", plan)
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic,
                  "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one GEMM "
                                     "launch (profiles/traffic.json)") if traffic else
@@ -774,9 +785,10 @@ def main():
     roof["frac"] = roof["achieved"] / roof["peak"]
     kname = ("gemv_mxf4_kernel" if plan.gemv else "gemm_mxf4_pair" if plan.pair else
              "gemm_mxf4_persistent" if plan.persistent else "gemm_mxf4_kernel")
-    roof["traffic"] = recorded_traffic(args.workload, kname)
+    roof["traffic"] = recorded_traffic(args.workload, kname, plan)
     roof["traffic_source"] = ("profiles/traffic.json (ncu dram__bytes_read.sum + "
-                              "dram__bytes_write.sum of one launch, same kernel sources)"
+                              "dram__bytes_write.sum of one launch, same kernel sources "
+                              "and launch configuration)"
                               if roof["traffic"] is not None else None)
     if stream_floor is not None:
         roof["stream_floor"] = stream_floor

@@ -588,7 +588,8 @@ def run_quantize(args, world, rank, local_rank):
         "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "traffic": None if fp8 else recorded_traffic("quantize", "quantize_kernel"),
+                     "traffic": recorded_traffic(args.workload, "quantize8_kernel" if fp8
+                                                 else "quantize_kernel"),
                      "kernel": kname, "kernel_ms": ms,
                      "algorithmic_bytes": nbytes, "peak_source": f"{peak_src} HBM copy bandwidth"},
         "cpu_baseline": cpu,

@@ -25,7 +25,8 @@ __all__ = [
     "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit",
     "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
-    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize",
+    "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "mxfp8_gemm_host",
+    "mxfp8_gemm_host_arena_size",
     "MXFP8_E4M3", "MXFP8_E5M2", "MXFP6_E2M3", "MXFP6_E3M2", "MXFP4_E2M1_PADDED",
     "gemm", "Plan",
 ]
@@ -105,6 +106,9 @@ def lib() -> ctypes.CDLL:
                                          f32, f32, i32, i32, i32, i32, vp]),
             "mxfp4_gemm_host": (i32, [vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32,
                                       vp, sz, vp]),
+            "mxfp8_gemm_host": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, f32, f32, i32, i32, i32,
+                                      i32, vp, sz, vp]),
+            "mxfp8_gemm_host_arena_size": (sz, [i32, i32, i32, i32, i32]),
             "mxfp4_device_status": (i32, [ctypes.POINTER(ctypes.c_int), i32]),
             "mxfp4_wait_timeout_probe": (i32, [ctypes.c_longlong, vp]),
             "mxfp4_stream_read_probe": (i32, [vp, sz, vp, vp]),
@@ -258,6 +262,19 @@ def mxfp4_gemm_prepacked(D, ldd, C, ldc, A, lda, B, ldb, scaleA_relaid, scaleB_r
                                              _p(scaleA_relaid), _p(scaleB_relaid), alpha, beta,
                                              M, N, K, split_k, _p(workspace), workspace_bytes,
                                              _stream(stream)), "mxfp4_gemm_prepacked")
+
+
+def mxfp8_gemm_host(D_host, C_host, A_host, B_host, scaleA_host, scaleB_host, fmt_a, fmt_b,
+                    alpha, beta, M, N, K, split_k, device_arena, arena_bytes, stream=None):
+    """mxfp4_gemm_host for the byte forms of mxfp8_gemm (host arrays in and out)."""
+    return _check(lib().mxfp8_gemm_host(_p(D_host), _p(C_host), _p(A_host), _p(B_host),
+                                        _p(scaleA_host), _p(scaleB_host), fmt_a, fmt_b, alpha,
+                                        beta, M, N, K, split_k, _p(device_arena), arena_bytes,
+                                        _stream(stream)), "mxfp8_gemm_host")
+
+
+def mxfp8_gemm_host_arena_size(M, N, K, split_k=0, with_c=False) -> int:
+    return lib().mxfp8_gemm_host_arena_size(M, N, K, split_k, int(bool(with_c)))
 
 
 def mxfp4_gemm_host(D_host, C_host, A_host, B_host, scaleA_host, scaleB_host, alpha, beta,

@@ -996,7 +996,14 @@ static int host_block_cols(int M, int N)
     return ((N + 1) / 2 + 255) / 256 * 256;
 }
 
-size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
+// Element form of a host-buffer call: packed E2M1 (two per byte) or one of
+// the byte forms of mxfp8_gemm (fmt_a / fmt_b are then its format codes).
+struct HostForm {
+    bool bytes;
+    int fmt_a, fmt_b;
+};
+
+static size_t host_arena_size(int M, int N, int K, int split_k, int with_c, HostForm f)
 {
     if (M < 1 || N < 1 || K < 32 || (K % 32) != 0 || split_k < 0 || split_k > kMaxSplit)
         return 0;
@@ -1008,13 +1015,25 @@ size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
     size_t ws = 0;
     for (int r : rows)
         for (int c : cols) {
-            const size_t w = mxfp4_gemm_workspace_size(r, c, K, split_k);
+            const size_t w = f.bytes ? mxfp8_gemm_workspace_size(r, c, K, split_k)
+                                     : mxfp4_gemm_workspace_size(r, c, K, split_k);
             ws = w > ws ? w : ws;
         }
+    const size_t row = f.bytes ? static_cast<size_t>(K) : static_cast<size_t>(K) / 2;
     const size_t mn2 = align_up(static_cast<size_t>(M) * N * 2);
-    return align_up(static_cast<size_t>(M) * K / 2) + align_up(static_cast<size_t>(N) * K / 2) +
+    return align_up(static_cast<size_t>(M) * row) + align_up(static_cast<size_t>(N) * row) +
            align_up(static_cast<size_t>(M) * K / 32) + align_up(static_cast<size_t>(N) * K / 32) +
            (with_c ? mn2 : 0) + mn2 + ws;
+}
+
+size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
+{
+    return host_arena_size(M, N, K, split_k, with_c, HostForm{false, 0, 0});
+}
+
+size_t mxfp8_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c)
+{
+    return host_arena_size(M, N, K, split_k, with_c, HostForm{true, 0, 0});
 }
 
 namespace {
@@ -1065,10 +1084,10 @@ HostPipe *host_pipe(int dev)
 
 }  // namespace
 
-int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
-                    const void *scaleA_host, const void *scaleB_host, float alpha, float beta,
-                    int M, int N, int K, int split_k, void *device_arena, size_t arena_bytes,
-                    void *stream)
+static int gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
+                     const void *scaleA_host, const void *scaleB_host, float alpha, float beta,
+                     int M, int N, int K, int split_k, void *device_arena, size_t arena_bytes,
+                     void *stream, HostForm form)
 {
     if (!D_host || !A_host || !B_host || !scaleA_host || !scaleB_host || !device_arena)
         return MXFP4_ERR_INVALID_ARG;
@@ -1076,10 +1095,12 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
         return MXFP4_ERR_INVALID_ARG;
     if (beta != 0.0f && !C_host)
         return MXFP4_ERR_INVALID_ARG;
+    if (form.bytes && (!byte_format_ok(form.fmt_a) || !byte_format_ok(form.fmt_b)))
+        return MXFP4_ERR_INVALID_ARG;
     if (!aligned(device_arena, kAlign))
         return MXFP4_ERR_MISALIGNED;
     const int with_c = beta != 0.0f;
-    const size_t need = mxfp4_gemm_host_arena_size(M, N, K, split_k, with_c);
+    const size_t need = host_arena_size(M, N, K, split_k, with_c, form);
     if (need == 0 || arena_bytes < need)
         return MXFP4_ERR_WORKSPACE;
     int st = check_device();
@@ -1092,7 +1113,8 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
     if (!pipe)
         return MXFP4_ERR_CUDA;
     uint8_t *p = static_cast<uint8_t *>(device_arena);
-    const size_t arow = static_cast<size_t>(K) / 2, srow = static_cast<size_t>(K) / 32;
+    const size_t arow = form.bytes ? static_cast<size_t>(K) : static_cast<size_t>(K) / 2;
+    const size_t srow = static_cast<size_t>(K) / 32;
     const size_t drow = static_cast<size_t>(N) * 2;
     const size_t a_b = static_cast<size_t>(M) * arow, b_b = static_cast<size_t>(N) * arow;
     const size_t sa_b = static_cast<size_t>(M) * srow, sb_b = static_cast<size_t>(N) * srow;
@@ -1170,9 +1192,15 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
             const size_t d_off = m0 * drow + n0 * 2;
             if (j == 0 && !ok(cudaStreamWaitEvent(s, pipe->in[i], 0)))
                 return MXFP4_ERR_CUDA;
-            st = mxfp4_gemm(dD + d_off, N, with_c ? dC + d_off : nullptr, N, dA + m0 * arow, K,
-                            dB + n0 * arow, K, dSA + m0 * srow, K / 32, dSB + n0 * srow, K / 32,
-                            alpha, beta, rows, cols, K, split_k, ws, ws_bytes, stream);
+            if (form.bytes)
+                st = mxfp8_gemm(dD + d_off, N, with_c ? dC + d_off : nullptr, N, dA + m0 * arow,
+                                K, dB + n0 * arow, K, dSA + m0 * srow, K / 32, dSB + n0 * srow,
+                                K / 32, form.fmt_a, form.fmt_b, alpha, beta, rows, cols, K,
+                                split_k, ws, ws_bytes, stream);
+            else
+                st = mxfp4_gemm(dD + d_off, N, with_c ? dC + d_off : nullptr, N, dA + m0 * arow,
+                                K, dB + n0 * arow, K, dSA + m0 * srow, K / 32, dSB + n0 * srow,
+                                K / 32, alpha, beta, rows, cols, K, split_k, ws, ws_bytes, stream);
             if (st != MXFP4_OK)
                 return st;
             cudaEvent_t out = pipe->out[j * kHostMaxPanels + i];
@@ -1185,6 +1213,24 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
     if (!ok(cudaEventRecord(pipe->done, pipe->d2h)) || !ok(cudaStreamWaitEvent(s, pipe->done, 0)))
         return MXFP4_ERR_CUDA;
     return MXFP4_OK;
+}
+
+int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
+                    const void *scaleA_host, const void *scaleB_host, float alpha, float beta,
+                    int M, int N, int K, int split_k, void *device_arena, size_t arena_bytes,
+                    void *stream)
+{
+    return gemm_host(D_host, C_host, A_host, B_host, scaleA_host, scaleB_host, alpha, beta, M, N,
+                     K, split_k, device_arena, arena_bytes, stream, HostForm{false, 0, 0});
+}
+
+int mxfp8_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
+                    const void *scaleA_host, const void *scaleB_host, int fmt_a, int fmt_b,
+                    float alpha, float beta, int M, int N, int K, int split_k,
+                    void *device_arena, size_t arena_bytes, void *stream)
+{
+    return gemm_host(D_host, C_host, A_host, B_host, scaleA_host, scaleB_host, alpha, beta, M, N,
+                     K, split_k, device_arena, arena_bytes, stream, HostForm{true, fmt_a, fmt_b});
 }
 
 int mxfp4_device_status(int *status, int reset)

@@ -282,6 +282,22 @@ int mxfp4_gemm_host(void *D_host, const void *C_host, const void *A_host, const 
 size_t mxfp4_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
 
 /*
+ * mxfp4_gemm_host for the operand forms of mxfp8_gemm: the same pipelined
+ * copies and blocks, with A [M, K] and B [N, K] host arrays of one byte per
+ * element (fmt_a / fmt_b as for mxfp8_gemm: MXFP8_E4M3, MXFP8_E5M2,
+ * MXFP6_E2M3, MXFP6_E3M2, MXFP4_E2M1_PADDED) and each block computed by
+ * mxfp8_gemm.  device_arena: >= mxfp8_gemm_host_arena_size(M, N, K, split_k,
+ * beta != 0) bytes, 256-byte aligned.  Errors: as mxfp4_gemm_host, plus
+ * MXFP4_ERR_INVALID_ARG for a bad format.
+ */
+int mxfp8_gemm_host(void *D_host, const void *C_host, const void *A_host, const void *B_host,
+                    const void *scaleA_host, const void *scaleB_host, int fmt_a, int fmt_b,
+                    float alpha, float beta, int M, int N, int K, int split_k,
+                    void *device_arena, size_t arena_bytes, void *stream);
+
+size_t mxfp8_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
+
+/*
  * mxfp4_gemm for callers that cannot allocate device memory (the page has no
  * counterpart: it exists for users whose allocator is owned by someone else
  * or who may not synchronise the device through a cudaMalloc mid-run).  Same

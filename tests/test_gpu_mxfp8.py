@@ -316,3 +316,23 @@ def test_subbyte_quantize_strided_then_gemm(oracle_mod, fa, fb):
                         np.ascontiguousarray(SA[:, :K // 32]), SB, None, 1.0, 0.0, 0)
     Dref, sabs = oracle_full(oracle_mod, p)
     assert_within_bound(run8(Dev8(p)), Dref, sabs, 1.0, f"quantise -> {fa} x {fb} gemm")
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [(2304, 2600, 1024, "e4m3", "e2m3"),
+                                         (300, 520, 512, "e2m1", "e5m2")])
+def test_mxfp8_host_entry_matches_device_call(M, N, K, fa, fb):
+    """Host buffers in and out through mxfp8_gemm_host (row panels x column
+    halves at M, N >= 2048; one block below): with split_k = 1 every block
+    runs the whole K in order, so D matches the device call bit for bit."""
+    p = inputs.make_problem8("h8", M, N, K, M + N, fa, fb, "normal", 0.5, 0.5, 1.0)
+    ref = run8(Dev8(p), split_k=1)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hA, hB, hSA, hSB = pin(p.A), pin(p.B), pin(p.SA), pin(p.SB)
+    hC = pin(p.C.view(np.int16))
+    hD = torch.zeros((M, N), dtype=torch.int16).pin_memory()
+    arena_b = mx.mxfp8_gemm_host_arena_size(M, N, K, 1, True)
+    arena = torch.empty(arena_b, dtype=torch.uint8, device="cuda")
+    mx.mxfp8_gemm_host(hD, hC, hA, hB, hSA, hSB, ABI_FMT[fa], ABI_FMT[fb], p.alpha, p.beta,
+                       M, N, K, 1, arena, arena_b)
+    torch.cuda.synchronize()
+    assert np.array_equal(hD.numpy().view(np.uint16), ref)

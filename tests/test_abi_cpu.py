@@ -399,3 +399,27 @@ def test_plan_respects_the_grid_limit():
     assert e.value.status == -2                       # MXFP4_ERR_UNSUPPORTED_SHAPE
     q = mx.mxfp4_plan_gemm(300, 65535 * 256 + 1, 256, 0, 152)
     assert q.pair == 1 and q.grid_y == 1
+
+
+def test_mxfp8_host_entry_validates_before_device(L):
+    """mxfp8_gemm_host checks pointers, C with beta, the formats and the
+    arena size before touching a device; its arena holds one byte per
+    element of A and B (twice the MXFP4 operand bytes)."""
+    f = L.mxfp8_gemm_host
+    base = [1, None, 1, 1, 1, 1, 0, 0, 1.0, 0.0, 1, 1, 32, 0, 0x1000, 1 << 20, None]
+    def call(**kw):
+        a = list(base)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a0=None) == -1                       # D_host
+    assert call(a9=1.0) == -1                        # beta != 0 without C
+    for bad in (2, 6, -1):
+        assert call(a6=bad) == -1 and call(a7=bad) == -1
+    assert call(a15=16) == -4                        # arena too small
+    assert call(a14=0x1008) == -3                    # arena alignment
+    M, N, K = 4096, 3072, 2048
+    a8 = mx.mxfp8_gemm_host_arena_size(M, N, K, 1, False)
+    a4 = mx.mxfp4_gemm_host_arena_size(M, N, K, 1, False)
+    assert a8 - a4 >= (M + N) * K // 2
+    assert mx.mxfp8_gemm_host_arena_size(M, N, 33, 1, False) == 0

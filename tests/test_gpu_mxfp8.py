@@ -200,12 +200,14 @@ def test_mxfp8_nan_scale_propagates(oracle_mod):
     assert not np.isnan(np.delete(D, 3, axis=0)).any()
 
 
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e5m2"), ("e2m3", "e2m1")])
 @pytest.mark.parametrize("M,N,K,split", [(300, 520, 1024, 0), (1, 4096, 2048, 0), (2000, 2600, 256, 0),
                                          (48, 1536, 4096, 4)])
-def test_mxfp8_prepacked_matches(M, N, K, split):
-    """Scales relaid once with mxfp4_scale_relayout (K in 8-bit elements):
-    mxfp8_gemm_prepacked equals mxfp8_gemm bit for bit."""
-    p = inputs.make_problem8("pp8", M, N, K, 3, "e4m3", "e5m2", "normal", 1.0, 0.5, 1.0)
+def test_mxfp8_prepacked_matches(M, N, K, split, fa, fb):
+    """Scales relaid once with mxfp4_scale_relayout (K in elements):
+    mxfp8_gemm_prepacked equals mxfp8_gemm bit for bit, for 8-bit operands
+    and for the padded 6- and 4-bit forms."""
+    p = inputs.make_problem8("pp8", M, N, K, 3, fa, fb, "normal", 1.0, 0.5, 1.0)
     dev = Dev8(p)
     ref = run8(dev, split_k=split)
     sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device="cuda")

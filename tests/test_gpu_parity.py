@@ -766,7 +766,7 @@ def test_cuda_graph_capture_and_replay(case):
 
 
 def test_cuda_graph_host_entry_and_mxfp8():
-    """The pipelined host-buffer call (copy streams forked from and joined
+    """The pipelined host-buffer calls (copy streams forked from and joined
     to the captured stream) and mxfp8_gemm, captured and replayed."""
     M, N, K = 2304, 1024, 1024
     p = inputs.make_problem("ghost", M, N, K, seed=43, values="normal", alpha=1.0, beta=0.0,
@@ -787,6 +787,25 @@ def test_cuda_graph_host_entry_and_mxfp8():
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(hD.numpy().view(np.uint16), ref)
+
+    # The same pipeline on the byte forms (mxfp8_gemm_host), E2M3 x E4M3.
+    q = inputs.make_problem8("gh8", M, N, K, 45, "e2m3", "e4m3", "normal", 1.0, 0.0, None)
+    qA, qB, qSA, qSB = pin(q.A), pin(q.B), pin(q.SA), pin(q.SB)
+    arena8_b = mx.mxfp8_gemm_host_arena_size(M, N, K, 1, False)
+    arena8 = torch.empty(arena8_b, dtype=torch.uint8, device="cuda")
+    hcall = lambda st: mx.mxfp8_gemm_host(hD, None, qA, qB, qSA, qSB, mx.MXFP6_E2M3,
+                                          mx.MXFP8_E4M3, 1.0, 0.0, M, N, K, 1, arena8, arena8_b,
+                                          st)
+    hcall(None)
+    torch.cuda.synchronize()
+    ref8 = hD.numpy().copy()
+    gh = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gh, stream=s):
+        hcall(s)
+    hD.zero_()
+    gh.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(hD.numpy(), ref8)
 
     q = inputs.make_problem8("g8", 300, 520, 1024, 44, "e4m3", "e5m2", "normal", 1.0, 0.0, None)
     d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()

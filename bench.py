@@ -256,8 +256,9 @@ def run_reference(args, rank):
         return
     fp8 = args.workload in inputs.WORKLOADS8
     p = inputs.workload8(args.workload) if fp8 else inputs.workload(args.workload)
-    # About 2.5 minutes of oracle time in all, at most 4 s per step.
-    per_step = min(4.0, 150.0 / max(1, args.steps))
+    # About 100 s of oracle time in all (2.5 - 4 minutes with the per-step
+    # overheads on 16 host cores), at most 4 s per step.
+    per_step = min(4.0, 100.0 / max(1, args.steps))
     for i in range(args.warmup):
         oracle_throughput(p, min(per_step, 1.0), 1000 + i)
     vals, times, desc, cores = [], [], "", 0

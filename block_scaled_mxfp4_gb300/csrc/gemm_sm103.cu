@@ -39,6 +39,7 @@
 // Every stage has its own TMEM scale slot.  A slot is rewritten only after the
 // stage's full barrier completed again, which needs the producers to have
 // seen the stage's previous MMAs commit, so no write overtakes a read.
+#include <atomic>
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -747,16 +748,16 @@ static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const C
     using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
     auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP, FMT>;
     // Opt in to the large dynamic shared memory once per device.
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 64 && !configured[dev]) {
+    if (dev < 64 && !configured[dev].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_relaxed);
     }
     if (a.cluster_split > 1) {
         // The split_k CTAs of a tile (grid z) form one cluster.
@@ -842,7 +843,7 @@ static cudaError_t launch_persistent_cfg(const GemmArgs &a, const Sched &sch,
 {
     using PC = PCfg<BN, STAGES, NACC, NSLOT>;
     auto kern = gemm_mxf4_persistent<BN, STAGES, SWAP, NACC, NSLOT>;
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -861,7 +862,7 @@ template <int BN, int STAGES, bool SWAP, int NACC, int NSLOT>
 static int occupancy_cfg()
 {
     // The occupancy calculator is slow on the host: ask once per device.
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -945,7 +946,7 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
 {
     using PC = PairCfg<STAGES, BN, NACC, CP, KC>;
     auto kern = gemm_mxf4_pair<STAGES, BN, NACC, CP, KC>;
-    static int max_clusters[64] = {0};      // per device; 0 = not yet queried
+    static std::atomic<int> max_clusters[64];   // per device; 0 = not yet queried
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -961,7 +962,7 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int limit = dev < 64 ? max_clusters[dev] : 0;
+    int limit = dev < 64 ? max_clusters[dev].load() : 0;
     if (limit == 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
         if (e != cudaSuccess)

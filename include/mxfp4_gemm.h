@@ -186,7 +186,8 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
 
 /*
  * MXFP8 / MXFP6 form of mxfp4_gemm: D[M,N] = alpha * A[M,K] . B[N,K]^T +
- * beta * C[M,N] with 8-bit or 6-bit elements, one E8M0 scale per 32 K as for
+ * beta * C[M,N] with 8-bit, 6-bit or padded 4-bit elements (one byte of
+ * footprint each), one E8M0 scale per 32 K as for
  * MXFP4 (page "CDNA4 dense MFMA builtins", section "FP8 and BF8 matrix
  * inputs": FP8 = E4M3, BF8 = E5M2; section "Mixed-precision with scaling":
  * also FP6 = E2M3 or E3M2, scaled per block, A and B formats chosen

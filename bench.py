@@ -3,20 +3,25 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--split-k S]
     python bench.py --impl reference ...     # the CPU oracle on a bounded sample
+    python bench.py --profile-shape M,N,K [--calls C] [--format F]   # for profilers
 
 One step is the whole hot path on one batch of resident inputs: one
 mxfp4_gemm call, as a user makes it -- for compute-bound shapes the scale
 relayout of A and B (one launch) and the GEMM on the relaid scales, launched
-as its programmatic dependent; otherwise the GEMM that builds the tcgen05
-scale layout itself, plus the split-K reduce (a dependent launch) when K is
-split.  (--prepacked times mxfp4_scale_relayout2 + mxfp4_gemm_prepacked.)
-The roofline's kernel time is the GEMM alone on relaid scales, timed in a
-second event loop when the step holds more than the GEMM.  Steps are timed
-with CUDA events on the launching stream; L2 is flushed (a 512 MiB write)
-between timed steps, outside the events.  Rank 0 prints one JSON line.  With
-N > 1 (torchrun) every rank runs an independent replica of the workload (the
-GEMM needs no exchange), the barrier + max over ranks times the job, and
-value counts all ranks' FLOPs.
+as its programmatic dependent; otherwise the GEMM alone, which builds the
+tcgen05 scale layout itself and sums its split-K partials in-kernel.  Steps
+rotate over copies of the inputs whose total exceeds three times the L2, so
+no step finds its operands in L2, and K steps run back to back between one
+pair of CUDA events on the launching stream (each launch waits in-kernel for
+the one before it).  The roofline's kernel time is the GEMM alone on relaid
+scales, timed the same way in a second loop that runs for at least a second
+while nvidia-smi samples the clocks.  The default run (the large 8192^3
+workload) also times the bandwidth-bound decode (1 x 8192 x 8192) and skinny
+(64 x 7168 x 16384) workloads and reports them under "hbm_bound", each next
+to a plain streaming read of its bytes timed the same way.  Rank 0 prints one
+JSON line.  With N > 1 (torchrun) every rank runs an independent replica of
+the workload (the GEMM needs no exchange), the barrier + max over ranks
+times the job, and value counts all ranks' FLOPs.
 """
 from __future__ import annotations
 
@@ -57,14 +62,13 @@ def replica_throughput(world, flops_per_step, steps, total_ms):
 
 # Device code and launchers of the GEMM kernels: a DRAM counter capture stays
 # valid while these are unchanged and the plan launches the same configuration.
-KERNEL_SOURCES = ("gemm_pair.cuh", "gemm_sm103.cu", "gemm_persistent.cuh", "ptx.cuh",
-                  "internal.h")
+KERNEL_SOURCES = ("gemm_pair.cuh", "gemm_sm103.cu", "ptx.cuh", "internal.h")
 
 
 def plan_key(plan):
     """The launch configuration a traffic capture was taken with."""
     return (f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k} stages {plan.stages} split "
-            f"{plan.split_k} swap {plan.swap_ab} pair {plan.pair} cluster {plan.pair_cluster} "
+            f"{plan.split_k} swap {plan.swap_ab} pair {plan.pair} "
             f"relayout {plan.relayout_pass} grid {plan.grid_x}x{plan.grid_y}x{plan.grid_z}")
 
 
@@ -97,19 +101,11 @@ def recorded_traffic(workload, kernel, plan=None):
     return rec["dram_bytes_read"] + rec["dram_bytes_write"]
 
 
-def reduce_kernel_runs(plan):
-    """Whether a plan's split-K runs the separate reduce kernel: its partials
-    need workspace (MXFP4_SPLIT_REDUCE=cluster reduces inside each tile's
-    cluster instead, with none)."""
-    return plan.split_k > 1 and plan.workspace_bytes > 0
-
-
 def split_note(plan):
     if plan.split_k <= 1:
         return ""
-    if reduce_kernel_runs(plan):
-        return " + split-K reduce (launched as its dependent)"
-    return f" (split-K reduced inside each tile's cluster of {plan.split_k} CTAs)"
+    return (f" (K split {plan.split_k} ways; the CTA that finishes a tile last sums its "
+            "partials in split order)")
 
 
 def parse_args():
@@ -127,6 +123,14 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prepacked", action="store_true",
                     help="step = scale relayout A + B kernels + GEMM on relaid scales")
+    ap.add_argument("--no-hbm-bound", action="store_true",
+                    help="skip the decode / skinny sub-benchmarks of the default run")
+    ap.add_argument("--profile-shape", default=None,
+                    help="M,N,K: run a few GEMMs of a random shape for a profiler, no timing")
+    ap.add_argument("--calls", type=int, default=3, help="--profile-shape: GEMM calls")
+    ap.add_argument("--format", default="mxfp4",
+                    choices=["mxfp4", "e4m3", "e5m2", "e2m3", "e3m2", "e2m1"],
+                    help="--profile-shape: element format")
     return ap.parse_args()
 
 
@@ -305,7 +309,7 @@ FP8_PER_BF16 = 2.0                   # nominal dense FP8 / bf16 tensor rate (4.5
 def run_mxfp8(args, world, rank, local_rank):
     """--workload large8 | decode8 | mixed8 | large6 | mixed6: one mxfp8_gemm
     call per step (FP6 operands in the padded 16-codes-per-16-bytes form)
-    (scale relayout + one-tile tcgen05 GEMM, or split-K GEMM + reduce), device
+    (scale relayout + one-tile tcgen05 GEMM, or the split-K GEMM), device
     timed with L2 flushed between steps; each rank of a multi-GPU launch runs
     the whole problem as a replica."""
     import numpy as np
@@ -394,8 +398,7 @@ def run_mxfp8(args, world, rank, local_rank):
     peaks, peak_src = load_peaks()
     hbm_bound = M <= 64
     kernels = ("scale_relayout_kernel + " if plan.relayout_pass else "") + \
-        f"gemm_mxf4_kernel<{plan.tile_n}, {plan.stages}, {'true' if plan.swap_ab else 'false'}, 1>" + \
-        (" + splitk_reduce_kernel" if reduce_kernel_runs(plan) else "")
+        f"gemm_mxf4_kernel<{plan.tile_n}, {plan.stages}, {'true' if plan.swap_ab else 'false'}, 1>"
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
@@ -436,7 +439,7 @@ def run_mxfp8(args, world, rank, local_rank):
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "api": "mxfp8_gemm_host (pinned host buffers)"},
-        "gpu_launches": args.steps * (1 + plan.relayout_pass + (1 if reduce_kernel_runs(plan) else 0)),
+        "gpu_launches": args.steps * (1 + plan.relayout_pass),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -614,22 +617,204 @@ def run_quantize(args, world, rank, local_rank):
         dist.destroy_process_group()
 
 
-def main():
-    args = parse_args()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+L2_BYTES = 129 * 1024 * 1024          # GB300 L2; rotation keeps > 3x this in flight
 
-    if args.impl == "reference":
-        run_reference(args, rank)
-        return
-    if args.workload in ("quantize", "quantize8", "quantize6"):
-        run_quantize(args, world, rank, local_rank)
-        return
-    if args.workload in ("large8", "decode8", "mixed8", "large6", "mixed6"):
-        run_mxfp8(args, world, rank, local_rank)
-        return
 
+def rotation_copies(nbytes):
+    """Input copies a rotation needs so that their total exceeds 3 x L2."""
+    return max(2, -(-3 * L2_BYTES // max(1, nbytes)) + 1)
+
+
+class Operands:
+    """`copies` device copies of a problem's inputs (each its own allocation,
+    so every step of a rotation reads bytes that no recent step touched)."""
+
+    def __init__(self, p, copies, dev):
+        import numpy as np
+        import torch
+        to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.A = [to_dev(p.A) for _ in range(copies)]
+        self.B = [to_dev(p.B) for _ in range(copies)]
+        self.SA = [to_dev(p.SA) for _ in range(copies)]
+        self.SB = [to_dev(p.SB) for _ in range(copies)]
+        self.C = None if p.C is None else \
+            [to_dev(p.C.view(np.int16)).view(torch.bfloat16) for _ in range(copies)]
+        self.copies = copies
+
+
+def timed_back_to_back(stream, n, launch, dist=None, device=None):
+    """Total ms of n launches (launch(i)) enqueued back to back between one
+    pair of CUDA events on `stream`, bracketed by a barrier + synchronize."""
+    import torch
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        launch(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    return e0.elapsed_time(e1)
+
+
+def probe_lib():
+    """The benchmark's streaming-read helper (not part of the library)."""
+    import ctypes
+    from block_scaled_mxfp4_gb300 import build
+    L = ctypes.CDLL(build.build_probe())
+    L.mxfp4_probe_stream_read.restype = ctypes.c_int
+    L.mxfp4_probe_stream_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                          ctypes.c_int, ctypes.c_void_p]
+    return L
+
+
+def stream_floor(nbytes, steps, stream, dev):
+    """A plain streaming read of nbytes, over a rotation of buffers like the
+    GEMM's, launched back to back (mode 1: each read waits for the one before
+    it, as mxfp4_gemm does; mode 2: reads overlap, as with MXFP4_FLAG_B_STATIC)."""
+    import torch
+    L = probe_lib()
+    per = -(-nbytes // 4096) * 4096
+    copies = rotation_copies(per)
+    pool = torch.empty(per * copies, dtype=torch.uint8, device=dev)
+    pool.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {"what": "one streaming read of the algorithmic bytes (16-byte loads, every SM), "
+                   f"rotating over {copies} buffers, back to back between one event pair"}
+    for mode, key in ((1, "ordered"), (2, "overlapped")):
+        def launch(i):
+            rc = L.mxfp4_probe_stream_read(pool.data_ptr() + (i % copies) * per, nbytes,
+                                           sink.data_ptr(), mode, stream.cuda_stream)
+            assert rc == 0, rc
+        for i in range(20):
+            launch(i)
+        ms = timed_back_to_back(stream, steps, launch) / steps
+        out[key] = {"us": ms * 1e3, "GB/s": nbytes / (ms * 1e-3) / 1e9}
+    del pool
+    return out
+
+
+def hbm_bound_run(name, steps, dev, stream, peaks, peak_src, dist=None):
+    """Decode / skinny sub-benchmark of the default run: K back-to-back
+    mxfp4_gemm calls over rotating input copies, plain and with
+    MXFP4_FLAG_B_STATIC, against the HBM copy peak and a streaming read of
+    the same bytes timed the same way; plus one cold call after a flush."""
+    import torch
+
+    import block_scaled_mxfp4_gb300 as mx
+    from block_scaled_mxfp4_gb300 import inputs
+    p = inputs.workload(name)
+    flops, algo_bytes = workload_geometry(p)
+    M, N, K = p.M, p.N, p.K
+    copies = rotation_copies(algo_bytes)
+    ops = Operands(p, copies, dev)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
+    wsb = mx.mxfp4_gemm_workspace_size(M, N, K, 0)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+
+    def launch(i, flags):
+        c = i % copies
+        C = ops.C[c] if p.beta != 0.0 else None
+        mx.mxfp4_gemm_ex(D, N, C, N, ops.A[c], K, ops.B[c], K, ops.SA[c], K // 32, ops.SB[c],
+                         K // 32, p.alpha, p.beta, M, N, K, 0, flags, ws, wsb, stream)
+
+    res = {"workload": f"{name} M={M} N={N} K={K}", "split_k": plan.split_k,
+           "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "swap_ab": plan.swap_ab,
+           "grid": [plan.grid_x, plan.grid_y, plan.grid_z], "rotation_copies": copies,
+           "algorithmic_bytes": algo_bytes, "steps": steps}
+    for flags, key in ((0, "default"), (mx.MXFP4_FLAG_B_STATIC, "b_static")):
+        for i in range(max(20, steps // 10)):
+            launch(i, flags)
+        ms = max_over_ranks([timed_back_to_back(stream, steps, lambda i: launch(i, flags), dist,
+                                                dev) / steps], dist, dev)[0]
+        gbs = algo_bytes / (ms * 1e-3) / 1e9
+        res[key] = {"us_per_gemm": ms * 1e3, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                 "peak_source": f"{peak_src} HBM copy bandwidth"}}
+    res["b_static"]["api"] = ("mxfp4_gemm_ex(..., MXFP4_FLAG_B_STATIC): B and its scales are "
+                              "prefetched into L2 before the in-kernel wait on the previous call")
+    res["default"]["api"] = "mxfp4_gemm"
+    floor = stream_floor(algo_bytes, steps, stream, dev)
+    floor["default_over_ordered"] = res["default"]["us_per_gemm"] / floor["ordered"]["us"]
+    floor["b_static_over_overlapped"] = res["b_static"]["us_per_gemm"] / floor["overlapped"]["us"]
+    res["stream_floor"] = floor
+    # One call alone after a 512 MiB flush (launch latency included).
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    cold = []
+    for i in range(13):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch(i, 0)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            cold.append(e0.elapsed_time(e1))
+    res["cold_single_call_us"] = statistics.median(cold) * 1e3
+    del flush, ops
+    return res
+
+
+def profile_shape(args):
+    """Run a few GEMMs of a seeded random shape for a profiler (no timing,
+    nothing checked): mxfp4 = random fp4x2 codes and E8M0 scales in
+    [120, 127], then --calls mxfp4_gemm calls (--prepacked: scales relaid
+    once, then mxfp4_gemm_prepacked calls) with the heuristic's plan; the
+    byte formats = random codes (the 8-bit formats' NaN codes avoided; every
+    byte is a valid padded 6- or 4-bit group), then --calls mxfp8_gemm calls."""
+    import torch
+
+    import block_scaled_mxfp4_gb300 as mx
+    from block_scaled_mxfp4_gb300 import build
+    build.build()
+    M, N, K = (int(x) for x in args.profile_shape.split(","))
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(0)
+    SA = torch.randint(120, 128, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)
+    SB = torch.randint(120, 128, (N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if args.format != "mxfp4":
+        fmt = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2, "e2m3": mx.MXFP6_E2M3,
+               "e3m2": mx.MXFP6_E3M2, "e2m1": mx.MXFP4_E2M1_PADDED}[args.format]
+        top = 0x70 if args.format in ("e4m3", "e5m2") else 256
+        A = torch.randint(0, top, (M, K), dtype=torch.uint8, device=dev, generator=g)
+        B = torch.randint(0, top, (N, K), dtype=torch.uint8, device=dev, generator=g)
+        wsb = mx.mxfp8_gemm_workspace_size(M, N, K, 0)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        for _ in range(args.calls):
+            mx.mxfp8_gemm(D, N, None, N, A, K, B, K, SA, K // 32, SB, K // 32, fmt, fmt, 1.0, 0.0,
+                          M, N, K, 0, ws if wsb else None, wsb)
+        plan = mx.mxfp8_plan_gemm(M, N, K, 0, 0)
+    else:
+        A = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        if args.prepacked:
+            sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device=dev)
+            sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device=dev)
+            mx.mxfp4_scale_relayout(sfa, SA, M, K, K // 32)
+            mx.mxfp4_scale_relayout(sfb, SB, N, K, K // 32)
+            wsb = mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, 0)
+            ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+            for _ in range(args.calls):
+                mx.mxfp4_gemm_prepacked(D, N, None, N, A, K, B, K, sfa, sfb, 1.0, 0.0, M, N, K,
+                                        0, ws if wsb else None, wsb)
+        else:
+            wsb = mx.mxfp4_gemm_workspace_size(M, N, K, 0)
+            ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+            for _ in range(args.calls):
+                mx.mxfp4_gemm(D, N, None, N, A, K, B, K, SA, K // 32, SB, K // 32, 1.0, 0.0,
+                              M, N, K, 0, ws if wsb else None, wsb)
+        plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
+    torch.cuda.synchronize()
+    print(f"{M}x{N}x{K} {args.format}: {args.calls} calls, plan {plan.as_dict()}")
+
+
+def run_mxfp4(args, world, rank, local_rank):
     import numpy as np
     import torch
 
@@ -647,85 +832,72 @@ def main():
     p = inputs.workload(args.workload)
     flops, algo_bytes = workload_geometry(p)
     dev = torch.device("cuda", local_rank)
-    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    A, B, SA, SB = to_dev(p.A), to_dev(p.B), to_dev(p.SA), to_dev(p.SB)
-    C = None if p.C is None else to_dev(p.C.view(np.int16)).view(torch.bfloat16)
     M, N, K = p.M, p.N, p.K
+    in_bytes = M * K // 2 + N * K // 2 + (M + N) * K // 32 + (2 * M * N if p.C is not None else 0)
+    copies = rotation_copies(in_bytes)
+    ops = Operands(p, copies, dev)
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device=dev)
-    sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device=dev)
     plan = mx.mxfp4_plan_gemm(M, N, K, args.split_k, 0)
     wsb = mx.mxfp4_gemm_workspace_size(M, N, K, args.split_k)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     wpb = mx.mxfp4_gemm_prepacked_workspace_size(M, N, K, args.split_k)
     wp = torch.empty(max(wpb, 256), dtype=torch.uint8, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    # Compute-bound shapes relay the scales out first (plan.relayout_pass); the
-    # roofline then needs the GEMM kernel alone, timed on relaid scales.
+    # Relaid scales of every copy, for the GEMM-alone loop (and --prepacked).
+    sfa = [torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device=dev)
+           for _ in range(copies)]
+    sfb = [torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device=dev)
+           for _ in range(copies)]
+    for c in range(copies):
+        mx.mxfp4_scale_relayout2(sfa[c], ops.SA[c], M, K // 32, sfb[c], ops.SB[c], N, K // 32, K,
+                                 stream)
+    Cs = lambda c: ops.C[c] if p.beta != 0.0 else None
     gemm_alone = args.prepacked or plan.relayout_pass
-    mx.mxfp4_scale_relayout2(sfa, SA, M, K // 32, sfb, SB, N, K // 32, K, stream)
 
-    def step():
+    def step(i):
+        c = i % copies
         if args.prepacked:
-            mx.mxfp4_scale_relayout2(sfa, SA, M, K // 32, sfb, SB, N, K // 32, K, stream)
-            mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
-                                    args.split_k, wp, wpb, stream)
+            mx.mxfp4_scale_relayout2(sfa[c], ops.SA[c], M, K // 32, sfb[c], ops.SB[c], N,
+                                     K // 32, K, stream)
+            mx.mxfp4_gemm_prepacked(D, N, Cs(c), N, ops.A[c], K, ops.B[c], K, sfa[c], sfb[c],
+                                    p.alpha, p.beta, M, N, K, args.split_k, wp, wpb, stream)
         else:
-            mx.mxfp4_gemm(D, N, C, N, A, K, B, K, SA, K // 32, SB, K // 32, p.alpha, p.beta,
-                          M, N, K, args.split_k, ws, wsb, stream)
+            mx.mxfp4_gemm(D, N, Cs(c), N, ops.A[c], K, ops.B[c], K, ops.SA[c], K // 32, ops.SB[c],
+                          K // 32, p.alpha, p.beta, M, N, K, args.split_k, ws, wsb, stream)
 
-    def gemm_kernel():
-        mx.mxfp4_gemm_prepacked(D, N, C, N, A, K, B, K, sfa, sfb, p.alpha, p.beta, M, N, K,
-                                args.split_k, wp, wpb, stream)
+    def gemm_kernel(i):
+        c = i % copies
+        mx.mxfp4_gemm_prepacked(D, N, Cs(c), N, ops.A[c], K, ops.B[c], K, sfa[c], sfb[c], p.alpha,
+                                p.beta, M, N, K, args.split_k, wp, wpb, stream)
 
-    for _ in range(max(3, args.warmup)):
-        flush.fill_(1)
-        step()
+    for i in range(max(3, args.warmup)):
+        step(i)
         if gemm_alone:
-            flush.fill_(1)
-            gemm_kernel()
+            gemm_kernel(i)
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    tot_ms = timed_back_to_back(stream, args.steps, step, dist, dev)
     t_wall = time.perf_counter() - t_wall
-    # The GEMM kernel alone (relaid scales, same flush) for the roofline, when
-    # the step holds more than the GEMM and its reduce.
+    # The GEMM kernel alone (relaid scales) for the roofline, timed the same
+    # way; it runs for at least a second so that the clock sampler sees the
+    # GPU under sustained load.
     if gemm_alone:
-        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            kev[i][0].record(stream)
-            gemm_kernel()
-            kev[i][1].record(stream)
-        torch.cuda.synchronize()
+        per = tot_ms / args.steps
+        n_alone = max(args.steps, int(1200.0 / max(per, 1e-3)))
+        gemm_tot = timed_back_to_back(stream, n_alone, gemm_kernel, dist, dev)
+        gemm_avg = gemm_tot / n_alone
+    else:
+        n_alone = 0
+        gemm_tot = 0.0
+        gemm_avg = tot_ms / args.steps
     clocks = sampler.stop()
-    if dist:
-        dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    gemm_ms = ([kev[i][0].elapsed_time(kev[i][1]) for i in range(args.steps)] if gemm_alone
-               else step_ms)
-    tot_ms = sum(step_ms)
-    gemm_avg = sum(gemm_ms) / len(gemm_ms)
     tot_ms, gemm_avg = max_over_ranks([tot_ms, gemm_avg], dist, dev)
     ms_per_step = tot_ms / args.steps
     value = replica_throughput(world, flops, args.steps, tot_ms)
-    launches_per_step = (2 if plan.relayout_pass or args.prepacked else 1) + \
-        (1 if reduce_kernel_runs(plan) else 0)
+    launches_per_step = 2 if plan.relayout_pass or args.prepacked else 1
 
     # ---- end to end: host buffers through the C ABI, copies in the timed region
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -735,53 +907,32 @@ def main():
     arena_b = mx.mxfp4_gemm_host_arena_size(M, N, K, args.split_k, p.beta != 0.0)
     arena = torch.empty(arena_b, dtype=torch.uint8, device=dev)
 
-    def e2e_step():
+    def e2e_step(i):
         mx.mxfp4_gemm_host(hD, hC, hA, hB, hSA, hSB, p.alpha, p.beta, M, N, K, args.split_k,
                            arena, arena_b, stream)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    for i in range(3):
+        e2e_step(i)
+    e2e_ms = timed_back_to_back(stream, args.e2e_steps, e2e_step, dist, dev) / args.e2e_steps
     e2e_ms = max_over_ranks([e2e_ms], dist, dev)[0]
-    # A plain streaming read of the same bytes after the same flush: the
-    # floor a single pass over this much data reaches on this GPU.
-    stream_floor = None
-    if args.workload in ("decode", "skinny"):
-        src = torch.ones(algo_bytes // 8, dtype=torch.int64, device=dev)
-        sink = torch.zeros(1, dtype=torch.int32, device=dev)
-        fts = []
-        for i in range(23):
-            flush.fill_(i & 0xFF)
-            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            f0.record(stream)
-            mx.mxfp4_stream_read_probe(src, algo_bytes // 16 * 16, sink, stream)
-            f1.record(stream)
-            torch.cuda.synchronize()
-            if i >= 3:
-                fts.append(f0.elapsed_time(f1))
-        fl = statistics.median(fts)
-        stream_floor = {"what": "mxfp4_stream_read_probe (one streaming read of the "
-                                "algorithmic bytes, 16-byte loads from every SM) after the "
-                                "same 512 MiB flush",
-                        "us": fl * 1e3, "GB/s": algo_bytes / (fl * 1e-3) / 1e9,
-                        "gemm_over_floor": gemm_avg / fl}
-        del src
     h2d = hA.numel() + hB.numel() + hSA.numel() + hSB.numel() + (hC.numel() * 2 if hC is not None else 0)
     d2h = hD.numel() * 2
+    del arena
+
+    peaks, peak_src = load_peaks()
+    # The bandwidth-bound workloads of the target, in the same process.
+    hbm = None
+    if args.workload == "large" and not args.no_hbm_bound and not args.prepacked:
+        del ops, sfa, sfb
+        torch.cuda.empty_cache()
+        hbm = {w: hbm_bound_run(w, max(args.steps, 1000), dev, stream, peaks, peak_src, dist)
+               for w in ("decode", "skinny")}
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
-    peaks, peak_src = load_peaks()
     if args.workload in ("large", "mid", "tiny"):
         peak = peaks["bf16_tflops"] * FP4_OVER_BF16
         roof = {"bound": "tensor", "achieved": flops / (gemm_avg * 1e-3) / 1e12, "peak": peak,
@@ -793,18 +944,15 @@ def main():
         roof = {"bound": "hbm", "achieved": algo_bytes / (gemm_avg * 1e-3) / 1e9, "peak": peak,
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    kname = ("gemv_mxf4_kernel" if plan.gemv else "gemm_mxf4_pair" if plan.pair else
-             "gemm_mxf4_persistent" if plan.persistent else "gemm_mxf4_kernel")
+    kname = "gemm_mxf4_pair" if plan.pair else "gemm_mxf4_kernel"
     roof["traffic"] = recorded_traffic(args.workload, kname, plan)
     roof["traffic_source"] = ("profiles/traffic.json (ncu dram__bytes_read.sum + "
                               "dram__bytes_write.sum of one launch, same kernel sources "
                               "and launch configuration)"
                               if roof["traffic"] is not None else None)
-    if stream_floor is not None:
-        roof["stream_floor"] = stream_floor
-    roof["kernel"] = (kname + (" + splitk_reduce_kernel" if reduce_kernel_runs(plan) else "")
-                      + (" (GEMM alone on relaid scales, timed in its own loop)"
-                         if gemm_alone else " (scale layout built in-kernel)"))
+    roof["kernel"] = kname + (f" (GEMM alone on relaid scales: {n_alone} launches back to back, "
+                              f"{gemm_tot / 1e3:.2f} s)" if gemm_alone else
+                              " (scale layout built in-kernel)")
     roof["kernel_ms"] = gemm_avg
     roof["algorithmic_bytes"] = algo_bytes
     roof["flops"] = flops
@@ -816,14 +964,16 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4", "data": "synthetic",
         "config": {"workload": f"{args.workload} M={M} N={N} K={K}", "M": M, "N": N, "K": K,
                    "alpha": p.alpha, "beta": p.beta, "seed": p.seed,
                    "split_k": plan.split_k, "swap_ab": plan.swap_ab,
                    "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
                    "grid": [plan.grid_x, plan.grid_y, plan.grid_z],
-                   "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "l2": f"inputs larger than L2: steps rotate over {copies} copies of the "
+                         f"inputs ({copies * in_bytes / 2**20:.0f} MiB > 3 x L2), back to back "
+                         "between one pair of events",
                    "step": ("mxfp4_scale_relayout2 + mxfp4_gemm_prepacked"
                             if args.prepacked else
                             "one mxfp4_gemm call: scale relayout of A and B (one launch) + GEMM "
@@ -838,15 +988,40 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "api": "mxfp4_gemm_host (pinned host buffers)"},
         "gpu_launches": launches_per_step * args.steps,
-        "gpu_launches_note": "our kernels in the timed step loop; the roofline's GEMM-alone loop "
-                             "(same count of GEMM launches) runs after it" if gemm_alone else
-                             "our kernels in the timed step loop",
+        "gpu_launches_note": ("our kernels in the timed step loop; the roofline's GEMM-alone "
+                              f"loop ({n_alone} launches) runs after it" if gemm_alone else
+                              "our kernels in the timed step loop"),
         "clocks": clocks,
+        "clocks_window": ("nvidia-smi every 50 ms over the timed steps and the GEMM-alone loop "
+                          f"({(t_wall * 1e3 + gemm_tot) / 1e3:.2f} s of GPU work)"),
         "wall_s_timed_loop": t_wall,
     }
+    if hbm is not None:
+        line["hbm_bound"] = hbm
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.profile_shape:
+        profile_shape(args)
+        return
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if args.workload in ("quantize", "quantize8", "quantize6"):
+        run_quantize(args, world, rank, local_rank)
+        return
+    if args.workload in ("large8", "decode8", "mixed8", "large6", "mixed6"):
+        run_mxfp8(args, world, rank, local_rank)
+        return
+    run_mxfp4(args, world, rank, local_rank)
 
 
 if __name__ == "__main__":

@@ -18,11 +18,12 @@ from typing import Optional
 
 __all__ = [
     "Mxfp4Error", "lib", "library_path", "header_functions",
-    "mxfp4_gemm", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc", "mxfp4_gemm_host",
+    "mxfp4_gemm", "mxfp4_gemm_ex", "mxfp4_gemm_prepacked", "mxfp4_gemm_noalloc",
+    "mxfp4_gemm_host", "MXFP4_FLAG_B_STATIC",
     "mxfp4_scale_relayout", "mxfp4_scale_relayout2", "mxfp4_quantize",
     "mxfp4_plan_gemm", "mxfp4_gemm_workspace_size", "mxfp4_gemm_prepacked_workspace_size",
     "mxfp4_scale_relayout_size", "mxfp4_gemm_host_arena_size", "mxfp4_device_status",
-    "mxfp4_wait_timeout_probe", "mxfp4_stream_read_probe", "mxfp4_set_wait_limit",
+    "mxfp4_wait_timeout_probe", "mxfp4_set_wait_limit",
     "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
     "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "mxfp8_gemm_host",
@@ -37,6 +38,7 @@ HEADER = os.path.join(_ROOT, "include", "mxfp4_gemm.h")
 _LIB_NAME = "libmxfp4_gb300.so"
 
 MXFP4_OK = 0
+MXFP4_FLAG_B_STATIC = 1
 MXFP8_E4M3, MXFP8_E5M2, MXFP6_E2M3, MXFP6_E3M2, MXFP4_E2M1_PADDED = 0, 1, 3, 4, 5
 STATUS_NAMES = {0: "MXFP4_OK", -1: "MXFP4_ERR_INVALID_ARG", -2: "MXFP4_ERR_UNSUPPORTED_SHAPE",
                 -3: "MXFP4_ERR_MISALIGNED", -4: "MXFP4_ERR_WORKSPACE", -5: "MXFP4_ERR_CUDA",
@@ -59,9 +61,7 @@ class Plan(ctypes.Structure):
                 ("k_tiles_per_split", ctypes.c_int), ("grid_x", ctypes.c_int),
                 ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t), ("relayout_pass", ctypes.c_int),
-                ("persistent", ctypes.c_int), ("ctas", ctypes.c_int), ("dp_waves", ctypes.c_int),
-                ("sk_units", ctypes.c_longlong), ("pair", ctypes.c_int), ("gemv", ctypes.c_int),
-                ("pair_cluster", ctypes.c_int)]
+                ("pair", ctypes.c_int), ("ctas", ctypes.c_int), ("waves", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
             "mxfp4_quantize": (i32, [vp, i64, vp, i64, vp, i64, i32, i32, vp]),
             "mxfp4_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                  f32, f32, i32, i32, i32, i32, vp, sz, vp]),
+            "mxfp4_gemm_ex": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                    f32, f32, i32, i32, i32, i32, ctypes.c_uint, vp, sz, vp]),
             "mxfp8_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                  i32, i32, f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp8_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, i32, i32,
@@ -111,7 +113,6 @@ def lib() -> ctypes.CDLL:
             "mxfp8_gemm_host_arena_size": (sz, [i32, i32, i32, i32, i32]),
             "mxfp4_device_status": (i32, [ctypes.POINTER(ctypes.c_int), i32]),
             "mxfp4_wait_timeout_probe": (i32, [ctypes.c_longlong, vp]),
-            "mxfp4_stream_read_probe": (i32, [vp, sz, vp, vp]),
             "mxfp4_set_wait_limit": (None, [ctypes.c_longlong]),
             "mxfp4_strerror": (ctypes.c_char_p, [i32]),
             "mxfp4_version": (i32, []),
@@ -204,6 +205,16 @@ def mxfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alp
                                    _p(workspace), workspace_bytes, _stream(stream)), "mxfp4_gemm")
 
 
+def mxfp4_gemm_ex(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
+                  M, N, K, split_k, flags, workspace, workspace_bytes, stream=None):
+    """mxfp4_gemm with flags (MXFP4_FLAG_B_STATIC: the work before this call
+    on the stream does not write B or scaleB, so B may be prefetched early)."""
+    return _check(lib().mxfp4_gemm_ex(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
+                                      ld_sa, _p(scaleB), ld_sb, alpha, beta, M, N, K, split_k,
+                                      flags, _p(workspace), workspace_bytes, _stream(stream)),
+                  "mxfp4_gemm_ex")
+
+
 def mxfp8_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, fmt_a, fmt_b,
                alpha, beta, M, N, K, split_k, workspace, workspace_bytes, stream=None):
     """MXFP8 / MXFP6 GEMM (A, B: one byte per element, lda / ldb in elements)."""
@@ -294,11 +305,6 @@ def mxfp4_device_status(reset=False) -> int:
 def mxfp4_wait_timeout_probe(limit_cycles, stream=None):
     return _check(lib().mxfp4_wait_timeout_probe(limit_cycles, _stream(stream)),
                   "mxfp4_wait_timeout_probe")
-
-
-def mxfp4_stream_read_probe(src, nbytes, sink, stream=None):
-    return _check(lib().mxfp4_stream_read_probe(_p(src), nbytes, _p(sink), _stream(stream)),
-                  "mxfp4_stream_read_probe")
 
 
 def mxfp4_set_wait_limit(cycles):

@@ -3,8 +3,9 @@
     python -m block_scaled_mxfp4_gb300.build [--force] [--verbose-ptxas]
 
 Each .cu under csrc/ compiles to an object in parallel, then one link makes
-libmxfp4_gb300.so next to this file.  Rebuilds only when a source or header
-is newer than the library.
+libmxfp4_gb300.so next to this file.  The benchmark's streaming-read helper
+(probe/stream_read.cu, not part of the library) links into libmxfp4_probe.so.
+Rebuilds only when a source or header is newer than its library.
 """
 from __future__ import annotations
 
@@ -21,6 +22,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmxfp4_gb300.so")
+PROBE_SRC = os.path.join(PKG, "probe", "stream_read.cu")
+PROBE_LIB = os.path.join(PKG, "libmxfp4_probe.so")
 OBJDIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -50,6 +53,21 @@ def up_to_date() -> bool:
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
+
+
+def build_probe(force: bool = False) -> str:
+    """The benchmark's streaming-read helper library."""
+    if not force and os.path.exists(PROBE_LIB) and \
+            os.path.getmtime(PROBE_SRC) <= os.path.getmtime(PROBE_LIB):
+        return PROBE_LIB
+    tmp = PROBE_LIB + ".tmp%d" % os.getpid()
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-shared", "-o", tmp, PROBE_SRC, "-cudart", "static"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError("nvcc failed on the stream-read helper")
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
@@ -95,3 +113,4 @@ def _build_locked(verbose_ptxas: bool) -> str:
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv))
+    print(build_probe(force="--force" in sys.argv))

@@ -1,7 +1,7 @@
 // C ABI of the block-scaled MXFP4 GEMM: argument checks, the tile / split-K
-// plan, TMA tensor maps and the launch sequence (GEMM -> optional split-K
-// reduce; the scale relayout runs inside the GEMM, or beforehand through
-// mxfp4_scale_relayout for prepacked scales).  Declared in include/mxfp4_gemm.h.
+// plan, TMA tensor maps and the launch sequence (optional scale relayout ->
+// GEMM, whose split-K partials are summed inside the GEMM; prepacked scales
+// come from mxfp4_scale_relayout).  Declared in include/mxfp4_gemm.h.
 #include <atomic>
 #include <chrono>
 #include <cstdio>
@@ -19,7 +19,6 @@ using namespace mxfp4;
 namespace {
 
 constexpr int kMaxSplit = 16;
-constexpr int kMaxClusterSplit = 8;   // splits that can reduce inside one (portable) cluster
 constexpr int kDefaultSms = 152;
 constexpr size_t kAlign = 256;
 
@@ -103,23 +102,6 @@ bool encode_operand(CUtensorMap *map, const void *base, int rows, int K, int64_t
     return r == CUDA_SUCCESS;
 }
 
-// 2-D uint8 view [rows, K/32] of row-major E8M0 scales (row stride ld bytes);
-// box 16 bytes (16 scale blocks = two 256-K stages) x box_rows, no swizzle.
-bool encode_scales(CUtensorMap *map, const void *base, int rows, int K, int64_t ld, int box_rows)
-{
-    auto enc = tensor_map_encoder();
-    if (!enc)
-        return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-    cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 // Relaid scale atoms viewed as 2-D uint32 [atoms, 128] (one 512-byte atom per
 // row); a box of 2 rows = the two atoms of one 256-K stage of a 128-row block.
 bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K, int box_atoms = 2)
@@ -165,83 +147,27 @@ struct Candidate {
     int tile_n;
     int stages;
     int ctas_per_sm;
-    int nacc;               // accumulator buffers of the persistent form
 };
-
-// Stream-K schedule for `slots` resident CTAs (see Sched in internal.h).
-struct SkPlan {
-    int tiles_p, tiles_q, kt, ctas, dp_waves, sk_tile0, pcols;
-    long long sk_units;
-    size_t partial_bytes;
-};
-
-SkPlan stream_k_plan(int64_t P, int64_t Q, int K, int tile_n, int64_t slots)
-{
-    SkPlan k;
-    k.tiles_p = static_cast<int>((P + kTileM - 1) / kTileM);
-    k.tiles_q = static_cast<int>((Q + tile_n - 1) / tile_n);
-    k.kt = (K + kTileK - 1) / kTileK;
-    const int64_t T = static_cast<int64_t>(k.tiles_p) * k.tiles_q;
-    if (slots > kMaxPersistentCtas)
-        slots = kMaxPersistentCtas;
-    if (T >= slots) {
-        k.dp_waves = static_cast<int>(T / slots);
-        k.ctas = static_cast<int>(slots);
-    } else {
-        k.dp_waves = 0;
-        const int64_t units = T * k.kt;
-        k.ctas = static_cast<int>(units < slots ? units : slots);
-    }
-    k.sk_tile0 = k.dp_waves * k.ctas;
-    k.sk_units = (T - k.sk_tile0) * static_cast<long long>(k.kt);
-    // A partial holds the tile's columns that exist (Q can be narrower than a
-    // tile: a skinny M has only M of the swapped tile's columns).
-    k.pcols = static_cast<int>(Q < tile_n ? Q : tile_n);
-    k.partial_bytes =
-        k.sk_units > 0 ? static_cast<size_t>(k.ctas) * k.pcols * kTileM * sizeof(float) : 0;
-    return k;
-}
 
 // Tile / swap / split-K choice.  Candidates are scored as the page's section
 // "Tile selection heuristic" scores its tiles: fewest waves (ceil(tiles /
 // resident CTA slots)), then the fullest last wave, then the larger
 // tile_m*tile_n/(tile_m+tile_n); the fixed candidate order breaks ties.
-// split_k >= 1 runs one CTA per (tile, K split) and, for split_k > 1, the
-// fixed-order fp32 reduce.  split_k == 0 picks the split itself: 1 when the
-// tiles fill at least half a wave, else enough splits to fill the resident
-// CTA slots, each split keeping at least kMinSplitStages K stages.
-// Shapes whose 256 x 256 tiles fill every SM pair at least once run the
-// CTA-pair kernel instead (split_k == 0 only).  MXFP4_KERNEL=persistent|pair
-// (a tuning / test override, read per call) routes split_k == 0 to the
-// persistent stream-K kernel or, for shapes of at least 256 x 256 without
-// swap, the CTA-pair kernel; MXFP4_KERNEL=gemv runs M <= 2 (N >= 4 * SMs) on
-// the CUDA-core GEMV kernel.
+// split_k >= 1 runs one CTA per (tile, K split); for split_k > 1 the CTA that
+// completes a tile sums the fp32 partials in split order.  split_k == 0 picks
+// the split itself: 1 when the tiles fill at least half a wave, else enough
+// splits to fill the resident CTA slots, each split keeping at least
+// kMinSplitStages K stages.  Shapes whose 256 x 256 tiles fill every SM pair
+// at least once run the CTA-pair kernel instead (split_k == 0 only).
 constexpr int kMinSplitStages = 8;
 
-enum class KernelChoice { Auto, Persistent, Pair, Gemv };
-
-KernelChoice kernel_override()
+// Bytes of the split-K area of a workspace: one 8-byte counter per tile, then
+// one partial slot (128 x part_cols fp32) per tile and split, each part
+// 256-byte aligned.
+size_t splitk_bytes(int64_t tiles, int split, int part_cols)
 {
-    const char *env = std::getenv("MXFP4_KERNEL");
-    if (!env)
-        return KernelChoice::Auto;
-    if (std::strcmp(env, "persistent") == 0)
-        return KernelChoice::Persistent;
-    if (std::strcmp(env, "pair") == 0)
-        return KernelChoice::Pair;
-    if (std::strcmp(env, "gemv") == 0)
-        return KernelChoice::Gemv;
-    return KernelChoice::Auto;
-}
-
-// fp8: plan an MXFP8 GEMM whose rows hold as many bytes as this K of fp4
-// elements (the caller passes twice its 8-bit K): the one-tile kernel only.
-// MXFP4_SPLIT_REDUCE=cluster: reduce split-K partials inside each tile's
-// cluster (read at each call; tuning and tests only).
-bool split_reduce_cluster()
-{
-    const char *env = std::getenv("MXFP4_SPLIT_REDUCE");
-    return env && std::strcmp(env, "cluster") == 0;
+    return align_up(static_cast<size_t>(tiles) * 8) +
+           align_up(static_cast<size_t>(tiles) * split * kTileM * part_cols * sizeof(float));
 }
 
 int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape,
@@ -255,30 +181,21 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     const int64_t P = swap ? N : M;
     const int64_t Q = swap ? M : N;
     const int kt = (K + kTileK - 1) / kTileK;
-    const KernelChoice choice = (split_req == 0 && !fp8) ? kernel_override() : KernelChoice::Auto;
     const int64_t tiles256 = ((static_cast<int64_t>(M) + 255) / 256) * ((static_cast<int64_t>(N) + 255) / 256);
     // The CTA-pair kernel takes shapes whose 256 x 256 tiles fill at least one
-    // wave of SM pairs (and any shape of at least 256 x 256 when forced).
-    const bool pair_fits = !fp8 && !swap && M >= 256 && N >= 256;
-    const bool use_pair = pair_fits && (choice == KernelChoice::Pair ||
-                                        (choice == KernelChoice::Auto && split_req == 0 &&
-                                         tiles256 >= (sms > 0 ? sms : kDefaultSms) / 2));
-    const bool persistent = choice == KernelChoice::Persistent || use_pair;
-    // M <= 2 with enough 4-row groups of B to give every SM a warp: the GEMV
-    // kernel (override only until it beats the tensor-core split path).
-    const bool use_gemv = choice == KernelChoice::Gemv && split_req == 0 && M <= kGemvMaxM &&
-                          (static_cast<int64_t>(N) + 3) / 4 >= (sms > 0 ? sms : kDefaultSms);
+    // wave of SM pairs.
+    const bool use_pair = !fp8 && !swap && split_req == 0 && M >= 256 && N >= 256 &&
+                          tiles256 >= sms / 2;
 
     Candidate cands[3];
     int nc = 0;
     if (swap) {
-        // Persistent: one 8-stage CTA per SM; one-tile split: two 4-stage CTAs.
-        cands[nc++] = persistent ? Candidate{64, 8, 1, 2} : Candidate{64, 4, 2, 2};
+        cands[nc++] = {64, 4, 2};             // two 4-stage CTAs per SM
     } else {
-        cands[nc++] = {256, 4, 1, 1};
-        cands[nc++] = {128, 6, 1, 2};
+        cands[nc++] = {256, 4, 1};
+        cands[nc++] = {128, 6, 1};
         if (Q <= 64)
-            cands[nc++] = {64, 8, 1, 2};
+            cands[nc++] = {64, 8, 1};
     }
     int best = -1;
     int64_t best_waves = 0;
@@ -286,7 +203,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     for (int i = 0; i < nc; ++i) {
         // The one-tile launch puts the tile columns on grid.y (at most 65535):
         // a tile that needs more columns than that is not a candidate.
-        if (!persistent && (Q + cands[i].tile_n - 1) / cands[i].tile_n > 65535)
+        if ((Q + cands[i].tile_n - 1) / cands[i].tile_n > 65535)
             continue;
         const int64_t tiles = ((P + kTileM - 1) / kTileM) * ((Q + cands[i].tile_n - 1) / cands[i].tile_n);
         const int64_t slots = static_cast<int64_t>(sms) * cands[i].ctas_per_sm;
@@ -303,25 +220,12 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
             best_ratio = ratio;
         }
     }
-    if (best < 0)
+    if (best < 0 && !use_pair)
         return MXFP4_ERR_UNSUPPORTED_SHAPE;
-    Candidate c = cands[best];
-    // Tuning override for sweeps: MXFP4_TILE="tile_n:stages" picks another
-    // compiled configuration of the same swap mode (ignored if there is none).
-    if (const char *env = std::getenv("MXFP4_TILE")) {
-        int tn = 0, st = 0;
-        if (std::sscanf(env, "%d:%d", &tn, &st) == 2) {
-            const int nacc = tn == 256 ? 1 : 2;
-            GemmShape probe{tn, st, swap, persistent ? 1 : 0, nacc, 1};
-            const bool have = persistent ? gemm_persistent_smem_bytes(probe) > 0
-                                             : (gemm_smem_bytes(probe) > 0 && gemm_config_exists(probe));
-            if (have)
-                c = {tn, st, gemm_smem_bytes(probe) * 2 <= 227 * 1024 ? 2 : 1, nacc};
-        }
-    }
+    const Candidate c = best >= 0 ? cands[best] : Candidate{256, 4, 1};
     const int64_t gx = (P + kTileM - 1) / kTileM;
     const int64_t gy = (Q + c.tile_n - 1) / c.tile_n;
-    if ((!persistent && gy > 65535) || gx > 0x7FFFFFFF || gx * gy > 0x7FFFFFFF)
+    if (!use_pair && (gy > 65535 || gx > 0x7FFFFFFF || gx * gy > 0x7FFFFFFF))
         return MXFP4_ERR_UNSUPPORTED_SHAPE;
     const int64_t tiles = gx * gy;
     const int64_t slots = static_cast<int64_t>(sms) * c.ctas_per_sm;
@@ -329,7 +233,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     int split = 1;
     if (split_req > 0) {
         split = split_req;
-    } else if (!persistent && 2 * tiles < slots) {
+    } else if (!use_pair && 2 * tiles < slots) {
         const int64_t by_slots = slots / tiles;
         const int64_t by_k = kt / kMinSplitStages;
         int64_t s = by_slots < by_k ? by_slots : by_k;
@@ -342,6 +246,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     const int per = (kt + split - 1) / split;
     split = (kt + per - 1) / per;   // every split gets >= 1 stage
 
+    std::memset(out, 0, sizeof(*out));
     out->swap_ab = swap;
     out->tile_m = kTileM;
     out->tile_n = c.tile_n;
@@ -352,117 +257,42 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     out->grid_x = static_cast<int>(gx);
     out->grid_y = static_cast<int>(gy);
     out->grid_z = split;
-    // Split-K partials go to fp32 workspace and a fixed-order reduce kernel;
-    // with MXFP4_SPLIT_REDUCE=cluster (up to kMaxClusterSplit splits) the
-    // splits of a tile form one cluster and reduce through distributed shared
-    // memory instead, with no workspace.  That form measured slower on GB300
-    // (decode 22 vs 19 us, skinny 56 vs 26 us: clusters of 4-5 CTAs at two
-    // CTAs per SM co-schedule fewer tiles), so it is an option only.
-    const bool cluster_reduce = split > 1 && split <= kMaxClusterSplit && split_reduce_cluster();
-    size_t partials = (split > 1 && !cluster_reduce)
-                          ? static_cast<size_t>(split) * static_cast<size_t>(M) *
-                                static_cast<size_t>(N) * sizeof(float)
-                          : 0;
-    // Persistent stream-K over all resident CTA slots (override only).
-    out->persistent = persistent ? 1 : 0;
-    out->ctas = 0;
-    out->dp_waves = 0;
-    out->sk_units = 0;
-    if (out->persistent) {
-        const SkPlan k = stream_k_plan(P, Q, K, c.tile_n, slots);
+    const int part_cols = static_cast<int>(Q < c.tile_n ? Q : c.tile_n);
+    out->workspace_bytes = split > 1 ? splitk_bytes(tiles, split, part_cols) : 0;
+    out->pair = use_pair ? 1 : 0;
+    if (use_pair) {
+        // Persistent: one CTA pair per two SMs, each taking every pairs-th
+        // 256 x 256 tile.
+        const int64_t tiles_q = (static_cast<int64_t>(N) + 255) / 256;
+        const int64_t ptiles = ((static_cast<int64_t>(M) + 255) / 256) * tiles_q;
+        const int64_t pairs = sms / 2;
+        out->tile_m = 256;
+        out->tile_n = 256;
+        out->tile_k = 256;
+        out->stages = 6;
         out->split_k = 1;
         out->k_tiles_per_split = kt;
-        out->ctas = k.ctas;
-        out->dp_waves = k.dp_waves;
-        out->sk_units = k.sk_units;
-        out->grid_x = k.ctas;
-        out->grid_y = 1;
-        out->grid_z = 1;
-        partials = k.partial_bytes;
-    }
-    out->pair = use_pair;
-    out->gemv = use_gemv ? 1 : 0;
-    if (use_gemv) {
-        int ctas = 0, threads = 0;
-        gemv_launch_shape(N, sms > 0 ? sms : kDefaultSms, &ctas, &threads);
-        out->swap_ab = 0;
-        out->tile_m = M;
-        out->tile_n = 4;
-        out->tile_k = 1024;
-        out->stages = 1;
-        out->split_k = 1;
-        out->k_tiles_per_split = (K + 1023) / 1024;
-        out->grid_x = ctas;
-        out->grid_y = 1;
-        out->grid_z = 1;
-        out->persistent = 0;
-        out->ctas = ctas;
-        out->dp_waves = 0;
-        out->sk_units = 0;
-        partials = 0;
-    }
-    int pair_n = 256;
-    int pair_cluster = 0;
-    int pair_kc = 0;
-    if (use_pair) {
-        // Tile N: 256 (one accumulator) or 192 (two accumulators, so a tile's
-        // MMAs overlap the previous tile's epilogue); MXFP4_PAIR_N overrides.
-        if (const char *env = std::getenv("MXFP4_PAIR_N"))
-            pair_n = std::atoi(env) == 192 ? 192 : 256;
-        // Pairs per cluster: 2 shares the A panel between two pairs on
-        // adjacent tiles (256-column tiles, at least two tile columns);
-        // MXFP4_PAIR_CLUSTER overrides.
-        const int64_t tiles_q = (static_cast<int64_t>(N) + pair_n - 1) / pair_n;
-        pair_cluster = 1;
-        if (const char *env = std::getenv("MXFP4_PAIR_CLUSTER"))
-            pair_cluster = std::atoi(env) == 2 ? 2 : 1;
-        if (pair_n != 256 || tiles_q < 2)
-            pair_cluster = 1;
-        // K per pipeline stage: 256 (six stages) or 512 (three stages of
-        // twice the size: half the barrier round trips per MMA);
-        // MXFP4_PAIR_KS overrides.  256-column tiles only.
-        pair_kc = 1;
-        if (const char *env = std::getenv("MXFP4_PAIR_KS"))
-            pair_kc = std::atoi(env) == 512 ? 2 : 1;
-        if (pair_n != 256)
-            pair_kc = 1;
-        const int64_t groups = ((static_cast<int64_t>(M) + 255) / 256) *
-                               ((tiles_q + pair_cluster - 1) / pair_cluster);
-        const int64_t clusters = sms / (2 * pair_cluster);
-        out->tile_m = 256;
-        out->tile_n = pair_n;
-        out->tile_k = 256 * pair_kc;
-        out->stages = pair_n == 192 ? 7 : (pair_kc == 2 ? 3 : 6);
-        out->dp_waves = static_cast<int>((groups + clusters - 1) / clusters);
-        out->sk_units = 0;
-        out->ctas = 2 * pair_cluster * static_cast<int>(groups < clusters ? groups : clusters);
+        out->waves = static_cast<int>((ptiles + pairs - 1) / pairs);
+        out->ctas = 2 * static_cast<int>(ptiles < pairs ? ptiles : pairs);
         out->grid_x = out->ctas;
-        partials = 0;
+        out->grid_y = 1;
+        out->grid_z = 1;
+        out->workspace_bytes = 0;
     }
-    out->pair_cluster = pair_cluster;
-    // Every workspace starts with the reserved stream-K flag bytes.
-    out->workspace_bytes = partials ? kFlagBytes + align_up(partials) : 0;
     // With enough tiles to fill the GPU the GEMM is compute-bound: mxfp4_gemm
     // then relays the row-major scales out in a separate pass (a few us) so
     // the mainloop can move whole scale atoms with bulk copies.  Skinny and
     // small shapes build the atoms inside the GEMM instead (no extra launches).
-    // (The persistent kernel stages row-major scales by TMA itself; the
-    // CTA-pair kernel reads relaid atoms.)
-    out->relayout_pass = (use_pair || (!use_gemv && !persistent && !swap && tiles >= sms)) ? 1 : 0;
+    // (The CTA-pair kernel always reads relaid atoms.)
+    out->relayout_pass = (use_pair || (!swap && tiles >= sms)) ? 1 : 0;
     if (shape) {
-        shape->tile_n = use_pair ? pair_n : c.tile_n;
-        shape->stages = c.stages;
+        shape->tile_n = use_pair ? 256 : c.tile_n;
+        shape->stages = out->stages;
         shape->swap = swap;
-        shape->persistent = out->persistent;
-        shape->nacc = c.nacc;
         shape->ctas_per_sm = c.ctas_per_sm;
         shape->pair = use_pair;
-        shape->gemv = use_gemv ? 1 : 0;
         shape->pair_ctas = out->ctas;
-        shape->pair_cluster = pair_cluster;
-        shape->pair_kc = pair_kc;
         shape->fp8 = fp8 ? 1 : 0;
-        shape->split_cluster = (!out->persistent && !use_pair && !use_gemv && cluster_reduce) ? 1 : 0;
     }
     return MXFP4_OK;
 }
@@ -491,7 +321,7 @@ int check_common(const void *D, int64_t ldd, const void *C, int64_t ldc, const v
     return MXFP4_OK;
 }
 
-// Scale relayout (if needed) has been done; run the GEMM (+ reduce).
+// Scale relayout (if needed) has been done; run the GEMM.
 // Scales as the kernel will read them: row-major [rows, ld] (atoms built in
 // the kernel) or already relaid into atoms.
 struct Scales {
@@ -503,66 +333,38 @@ struct Scales {
 std::atomic<unsigned> g_epoch{0};
 std::once_flag g_epoch_once;
 
-// Next per-call flag value for the stream-K handshake (never 0).  The count
-// starts from a clock-derived value so that a fresh workspace holding small
-// integers does not look ready by chance; stale flags of earlier calls hold
-// earlier values and never match.
-int next_epoch()
+// Next per-call tag of the split-K tile counters (never 0).  The count starts
+// from a clock-derived value so that a fresh workspace holding small integers
+// does not look tagged by chance; counters of earlier calls hold earlier
+// tags and never match.
+uint32_t next_epoch()
 {
     std::call_once(g_epoch_once, [] {
         const auto t = std::chrono::steady_clock::now().time_since_epoch().count();
         g_epoch.store(static_cast<unsigned>((t ^ (t >> 29)) * 2654435761u) | 0x40000000u);
     });
     unsigned e = ++g_epoch;
-    while ((e & 0x7FFFFFFFu) == 0)
+    while (e == 0)
         e = ++g_epoch;
-    return static_cast<int>(e & 0x7FFFFFFFu);
+    return e;
 }
 
-// ws: workspace base (flags at offset 0, partials after kFlagBytes), or
-// nullptr when the plan needs none.
+// ws: workspace base (split-K counters and partials), or nullptr when the
+// plan needs none.  flags: MXFP4_FLAG_* of the call.
 int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
              const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M, int N,
-             int K, const mxfp4_plan &plan, const GemmShape &shape, uint8_t *ws, int sms,
-             cudaStream_t stream, bool after_relayout = false, int fmt_a = 0, int fmt_b = 0)
+             int K, const mxfp4_plan &plan, const GemmShape &shape, uint8_t *ws,
+             cudaStream_t stream, bool after_relayout = false, int fmt_a = 0, int fmt_b = 0,
+             unsigned flags = 0)
 {
-    float *partials = ws ? reinterpret_cast<float *>(ws + kFlagBytes) : nullptr;
-    if (shape.gemv) {
-        GemvArgs g;
-        std::memset(&g, 0, sizeof(g));
-        g.A = static_cast<const uint8_t *>(A);
-        g.B = static_cast<const uint8_t *>(B);
-        g.SA = sc.a;
-        g.SB = sc.b;
-        g.lda_bytes = lda / 2;
-        g.ldb_bytes = ldb / 2;
-        g.ld_sa = sc.ld_a;
-        g.ld_sb = sc.ld_b;
-        g.sf_relaid = sc.rowmajor ? 0 : 1;
-        g.M = M;
-        g.N = N;
-        g.K = K;
-        g.alpha = alpha;
-        g.beta = beta;
-        g.C = static_cast<const uint16_t *>(beta != 0.0f ? C : nullptr);
-        g.ldc = ldc;
-        g.D = static_cast<uint16_t *>(D);
-        g.ldd = ldd;
-        return launch_gemv(g, sms, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
-    }
     if (shape.pair) {
         if (sc.rowmajor)
             return MXFP4_ERR_INVALID_ARG;            // the pair kernel reads relaid atoms
         CUtensorMap tmA, tmB, tmSA, tmSB;
-        const int bn = shape.tile_n;
-        const int cp = shape.pair_cluster == 2 ? 2 : 1;
-        const int kc = shape.pair_kc == 2 ? 2 : 1;
-        // With two pairs per cluster each CTA loads half of its A rows and
-        // half of its scale-A atoms per stage (multicast to both pairs).
-        if (!encode_operand(&tmA, A, M, K, lda, kTileM / cp) ||
-            !encode_operand(&tmB, B, N, K, ldb, bn / 2) ||
-            !encode_atoms(&tmSA, sc.a, M, K, 2 * kc / cp) ||
-            !encode_atoms_3d(&tmSB, sc.b, N, K, 2, 2 * kc))
+        if (!encode_operand(&tmA, A, M, K, lda, kTileM) ||
+            !encode_operand(&tmB, B, N, K, ldb, 128) ||
+            !encode_atoms(&tmSA, sc.a, M, K, 2) ||
+            !encode_atoms_3d(&tmSB, sc.b, N, K, 2, 2))
             return MXFP4_ERR_CUDA;
         GemmArgs a;
         std::memset(&a, 0, sizeof(a));
@@ -579,11 +381,11 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
                    (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
         a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
+        a.ab_early = after_relayout ? 1 : 0;
         a.wait_limit = g_wait_limit.load();
-        const int tiles_p = (M + 255) / 256, tiles_q = (N + bn - 1) / bn;
-        if (launch_gemm_pair(a, bn, cp, kc, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
-                             after_relayout, stream) !=
-            cudaSuccess)
+        const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
+        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
+                             after_relayout, stream) != cudaSuccess)
             return MXFP4_ERR_CUDA;
         return MXFP4_OK;
     }
@@ -611,12 +413,6 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
                 (sc.ld_b % 8) == 0;
     a.sf_async = sc.rowmajor && aligned(sc.a, 4) && aligned(sc.b, 4) && (sc.ld_a % 4) == 0 &&
                  (sc.ld_b % 4) == 0;
-    // The persistent kernel prefers one 2-D TMA per pair of stages for
-    // row-major scales (16-byte aligned rows), over per-word copies.
-    a.sf_tma = shape.persistent && sc.rowmajor && aligned(sc.a, 16) && aligned(sc.b, 16) &&
-               (sc.ld_a % 16) == 0 && (sc.ld_b % 16) == 0;
-    if (a.sf_tma)
-        a.sf_async = 0;
     a.rowsP = Prows;
     a.rowsQ = Qrows;
     a.M = M;
@@ -633,65 +429,31 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.ldc = ldc;
     a.D = static_cast<uint16_t *>(D);
     a.ldd = ldd;
-    a.ws = partials;
-    a.cluster_split = (!shape.persistent && plan.split_k > 1 && plan.split_k <= kMaxClusterSplit &&
-                       shape.split_cluster)
-                          ? plan.split_k
-                          : 0;
+    if (plan.split_k > 1) {
+        if (!ws)
+            return MXFP4_ERR_WORKSPACE;
+        const int64_t tiles = static_cast<int64_t>(plan.grid_x) * plan.grid_y;
+        a.part_cols = Qrows < shape.tile_n ? Qrows : shape.tile_n;
+        a.tile_count = reinterpret_cast<unsigned long long *>(ws);
+        a.partials = reinterpret_cast<float *>(ws + align_up(static_cast<size_t>(tiles) * 8));
+        a.epoch = next_epoch();
+    }
     a.vec_ok = aligned(D, 16) && (ldd % 8) == 0 &&
                (beta == 0.0f || (aligned(C, 16) && (ldc % 8) == 0));
     a.vec32_ok = a.vec_ok && aligned(D, 32) && (ldd % 16) == 0;
     a.stream_p = swap ? 1 : 0;
+    a.p_is_b = swap ? 1 : 0;
+    // B (and its scales) may be read before the preceding work ends only
+    // when the caller says that work does not write them, and when no
+    // relayout pass of this call is that work.
+    a.b_early = ((flags & MXFP4_FLAG_B_STATIC) && !after_relayout) ? 1 : 0;
     a.wait_limit = g_wait_limit.load();
 
-    if (shape.persistent) {
-        // The plan assumed shape.ctas_per_sm resident CTAs per SM; if the
-        // occupancy calculator allows fewer here, shrink the grid so every
-        // CTA is resident (the stream-K handshake waits on other CTAs).
-        int64_t slots = static_cast<int64_t>(sms) * shape.ctas_per_sm;
-        const int occ = gemm_persistent_occupancy(shape);
-        if (occ <= 0)
-            return MXFP4_ERR_CUDA;
-        if (occ < shape.ctas_per_sm)
-            slots = static_cast<int64_t>(sms) * occ;
-        const SkPlan k = stream_k_plan(Prows, Qrows, K, shape.tile_n, slots);
-        if (k.partial_bytes && !ws)
-            return MXFP4_ERR_WORKSPACE;
-        Sched sch;
-        sch.tiles_p = k.tiles_p;
-        sch.tiles_q = k.tiles_q;
-        sch.kt = k.kt;
-        sch.ctas = k.ctas;
-        sch.dp_waves = k.dp_waves;
-        sch.sk_tile0 = k.sk_tile0;
-        sch.sk_units = k.sk_units;
-        sch.group = k.tiles_p < 8 ? k.tiles_p : 8;
-        sch.flags = ws ? reinterpret_cast<int *>(ws) : nullptr;
-        sch.partials = partials;
-        sch.pcols = k.pcols;
-        sch.epoch = next_epoch();
-        CUtensorMap tmSP = tmP, tmSQ = tmQ;   // unused unless a.sf_tma
-        if (a.sf_tma &&
-            (!encode_scales(&tmSP, a.sfP, Prows, K, a.ldsP, kTileM) ||
-             !encode_scales(&tmSQ, a.sfQ, Qrows, K, a.ldsQ, shape.tile_n)))
-            return MXFP4_ERR_CUDA;
-        if (launch_gemm_persistent(a, sch, tmP, tmQ, tmSP, tmSQ, shape, stream) != cudaSuccess)
-            return MXFP4_ERR_CUDA;
-        return MXFP4_OK;
-    }
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     if (launch_gemm(a, tmP, tmQ, shape, grid, stream) != cudaSuccess)
         return MXFP4_ERR_CUDA;
-    if (plan.split_k > 1 && !a.cluster_split) {
-        if (!partials)
-            return MXFP4_ERR_WORKSPACE;
-        if (launch_splitk_reduce(partials, plan.split_k, M, N, alpha, beta, a.C, ldc, a.D, ldd, sms,
-                                 stream) != cudaSuccess)
-            return MXFP4_ERR_CUDA;
-    }
     return MXFP4_OK;
 }
-
 
 }  // namespace
 
@@ -747,8 +509,7 @@ size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k)
         return 0;
     size_t ws = plan.workspace_bytes;
     if (plan.relayout_pass)
-        ws = (ws ? ws : kFlagBytes) + align_up(sf_relaid_bytes(M, K)) +
-             align_up(sf_relaid_bytes(N, K));
+        ws += align_up(sf_relaid_bytes(M, K)) + align_up(sf_relaid_bytes(N, K));
     return ws;
 }
 
@@ -813,7 +574,7 @@ static int gemm_entry(void *D, int64_t ldd, const void *C, int64_t ldc, const vo
     if (st != MXFP4_OK)
         return st;
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
-                    plan.workspace_bytes ? static_cast<uint8_t *>(workspace) : nullptr, sms,
+                    plan.workspace_bytes ? static_cast<uint8_t *>(workspace) : nullptr,
                     static_cast<cudaStream_t>(stream), false, fmt_a, fmt_b);
 }
 
@@ -850,7 +611,7 @@ static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const
                          int64_t lda, const void *B, int64_t ldb, const void *scaleA,
                          int64_t ld_sa, const void *scaleB, int64_t ld_sb, float alpha, float beta,
                          int M, int N, int K, int split_k, void *workspace, size_t workspace_bytes,
-                         void *stream, bool fp8, int fmt_a, int fmt_b)
+                         void *stream, bool fp8, int fmt_a, int fmt_b, unsigned flags = 0)
 {
     const int kx = fp8 ? 2 : 1;
     if (fp8 && (K > (1 << 29) || lda > (INT64_MAX / 4) || ldb > (INT64_MAX / 4)))
@@ -874,10 +635,8 @@ static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const
         return st;
     const size_t sfa_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(M, K)) : 0;
     const size_t sfb_bytes = plan.relayout_pass ? align_up(sf_relaid_bytes(N, K)) : 0;
-    // Layout: [flags + partials (plan.workspace_bytes)][relaid A][relaid B];
-    // the flag bytes are reserved even when only the relaid buffers are used.
-    const size_t head = plan.workspace_bytes ? plan.workspace_bytes
-                                             : (plan.relayout_pass ? kFlagBytes : 0);
+    // Layout: [split-K counters + partials (plan.workspace_bytes)][relaid A][relaid B].
+    const size_t head = plan.workspace_bytes;
     const size_t need = head + sfa_bytes + sfb_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need))
         return MXFP4_ERR_WORKSPACE;
@@ -896,8 +655,8 @@ static int gemm_rowmajor(void *D, int64_t ldd, const void *C, int64_t ldc, const
         sc = Scales{sfa, sfb, 0, 0, false};
     }
     return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
-                    plan.workspace_bytes ? ws : nullptr, sms, s, plan.relayout_pass != 0, fmt_a,
-                    fmt_b);
+                    plan.workspace_bytes ? ws : nullptr, s, plan.relayout_pass != 0, fmt_a,
+                    fmt_b, flags);
 }
 
 int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
@@ -907,6 +666,17 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
 {
     return gemm_rowmajor(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
                          M, N, K, split_k, workspace, workspace_bytes, stream, false, 0, 0);
+}
+
+int mxfp4_gemm_ex(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+                  const void *B, int64_t ldb, const void *scaleA, int64_t ld_sa, const void *scaleB,
+                  int64_t ld_sb, float alpha, float beta, int M, int N, int K, int split_k,
+                  unsigned flags, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if ((flags & ~static_cast<unsigned>(MXFP4_FLAG_B_STATIC)) != 0)
+        return MXFP4_ERR_INVALID_ARG;
+    return gemm_rowmajor(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
+                         M, N, K, split_k, workspace, workspace_bytes, stream, false, 0, 0, flags);
 }
 
 int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
@@ -970,8 +740,7 @@ size_t mxfp8_gemm_workspace_size(int M, int N, int K, int split_k)
         return 0;
     size_t ws = plan.workspace_bytes;
     if (plan.relayout_pass)
-        ws = (ws ? ws : kFlagBytes) + align_up(sf_relaid_bytes(M, K)) +
-             align_up(sf_relaid_bytes(N, K));
+        ws += align_up(sf_relaid_bytes(M, K)) + align_up(sf_relaid_bytes(N, K));
     return ws;
 }
 
@@ -1287,21 +1056,6 @@ int mxfp4_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, in
     return launch_quantize(static_cast<uint8_t *>(Q), ldq / 2, static_cast<uint8_t *>(S), lds,
                            static_cast<const uint16_t *>(X), ldx, rows, K, device_sms_or_default(),
                            static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? MXFP4_OK
-               : MXFP4_ERR_CUDA;
-}
-
-int mxfp4_stream_read_probe(const void *src, size_t bytes, void *sink, void *stream)
-{
-    if (!src || !sink || bytes < 16)
-        return MXFP4_ERR_INVALID_ARG;
-    if (!aligned(src, 16) || !aligned(sink, 4))
-        return MXFP4_ERR_MISALIGNED;
-    int st = check_device();
-    if (st != MXFP4_OK)
-        return st;
-    return launch_stream_read(src, bytes, static_cast<unsigned *>(sink), device_sms_or_default(),
-                              static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MXFP4_OK
                : MXFP4_ERR_CUDA;
 }

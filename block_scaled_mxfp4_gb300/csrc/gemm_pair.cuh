@@ -50,35 +50,25 @@
 //                      CTAs), form alpha*acc + beta*C and round once to bf16
 //                      in registers, then store D -- so the next tile's MMAs
 //                      wait for neither the arithmetic nor the stores.
-// Clusters of CP = 1 or 2 pairs.  With CP = 2 the two pairs of a cluster take
-// horizontally adjacent tiles (same 256 rows of A, N columns qt = 2 qq and
-// 2 qq + 1) and share their A panel: CTA r of each pair loads half of the
-// 128 A rows (and one of the two scale-A atoms) that both pairs' CTA r need
-// and multicasts it to both, so each CTA pulls 8 KB of A per stage from L2
-// instead of 16 KB (26.5 KB per stage instead of 35).  A stage's slot is then
-// written by both pairs, so every CTA's empty barrier collects the MMA
-// commits of both pairs.  A second tile past the last column (odd tile
-// count) is computed on zero-filled B and not stored.
-// Persistent over tiles: cluster i takes tile groups i, i + clusters, ...  Scales are
+// Persistent over tiles: pair i takes tiles i, i + pairs, ...  Scales are
 // relaid atoms (a 2-D uint32 view for scale-A, 3-D for scale-B: 128 words =
 // one atom).  A scale slot in tensor memory is rewritten only after the MMAs
 // that read it completed: with a slot per stage that is implied by the
 // stage's full barrier (the producers waited for the stage's previous MMAs);
 // with S slots the copier waits for the empty barrier of the stage S back.
+// Launched as a programmatic dependent: right after this library's scale
+// relayout (whose grid waits for the work before it), only the scale loads
+// wait for the preceding grid; otherwise every load, and the epilogue, waits.
 #pragma once
 
 namespace mxfp4 {
 
-template <int STAGES, int BN, int NACC, int CP, int KC>
+template <int STAGES, int BN, int NACC>
 struct PairCfg {
-    static constexpr int CLUSTER = 2 * CP;                // CTAs per cluster
-    static constexpr int A_LOAD_ROWS = kTileM / CP;       // A rows this CTA loads per chunk
     static constexpr int B_ROWS = BN / 2;                 // this CTA's rows of the B tile
-    static constexpr int GROUPS = 2 * KC;                 // scale k-groups (128 K) per stage
-    static constexpr int A_CHUNK = kTileM * 128;          // 128 rows x 128 bytes (256 K)
-    static constexpr int B_CHUNK = B_ROWS * 128;
-    static constexpr int A_BYTES = KC * A_CHUNK;
-    static constexpr int B_BYTES = KC * B_CHUNK;
+    static constexpr int GROUPS = 2;                      // scale k-groups (128 K) per stage
+    static constexpr int A_BYTES = kTileM * 128;          // 128 rows x 128 bytes (256 K)
+    static constexpr int B_BYTES = B_ROWS * 128;
     static constexpr int SFB_RB = 2;                      // 128-row scale blocks a tile can touch
     static constexpr int SFA_BYTES = GROUPS * kSfAtomBytes;           // 128 rows
     static constexpr int SFB_BYTES = SFB_RB * GROUPS * kSfAtomBytes;
@@ -103,8 +93,6 @@ struct PairCfg {
     static_assert(BN == 256 || BN == 192, "tile N");
     static_assert(SF_SLOTS >= 2, "scale slots");
     static_assert(NACC == 1 || NACC == 2, "accumulator buffers");
-    static_assert(CP == 1 || CP == 2, "pairs per cluster");
-    static_assert(KC == 1 || KC == 2, "256-K chunks per stage");
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -113,22 +101,20 @@ struct PairCfg {
 
 struct PairSched {
     int tiles_p, tiles_q;   // 256 x BN output tiles
-    int kt;                 // K stages per tile
-    int kchunks;            // 256-K chunks per tile (the last stage may hold fewer than KC)
+    int kt;                 // K stages (256 K each) per tile
     int group;              // raster: groups of `group` tile rows
 };
 
-// Tile group t (one tile per pair of the cluster) -> its row of tiles pt and
-// group column qq, over tiles_p x cols groups, rastered in bands of `group`
-// tile rows.
-__device__ __forceinline__ void pair_tile_coords(const PairSched &s, int cols, int t, int &pt, int &qq)
+// Tile t -> its row of tiles pt and column qt, over tiles_p x tiles_q tiles
+// rastered in bands of `group` tile rows.
+__device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int &pt, int &qt)
 {
-    const int per_group = s.group * cols;
+    const int per_group = s.group * s.tiles_q;
     const int g = t / per_group;
     const int within = t - g * per_group;
     const int gh = min(s.group, s.tiles_p - g * s.group);
     pt = g * s.group + within % gh;
-    qq = within / gh;
+    qt = within / gh;
 }
 
 // One epilogue thread's HALF columns of one accumulator row, rounded: out[j]
@@ -207,13 +193,13 @@ __device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n
         out[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 }
 
-template <int STAGES, int BN, int NACC, int CP, int KC>
-__global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
+template <int STAGES, int BN, int NACC>
+__global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
 {
-    using PC = PairCfg<STAGES, BN, NACC, CP, KC>;
+    using PC = PairCfg<STAGES, BN, NACC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -228,21 +214,18 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = cluster_ctarank();
-    const uint32_t rank = crank & 1u;          // rank within the pair
-    const uint32_t pidx = crank >> 1;          // pair within the cluster
-    const uint32_t lead = crank & ~1u;         // cluster rank of this pair's leader
+    const uint32_t rank = cluster_ctarank() & 1u;   // rank within the pair
+    const uint32_t lead = 0;                        // cluster rank of the leader
     const bool leader = rank == 0;
-    const int cl = blockIdx.x / PC::CLUSTER;
-    const int ncl = gridDim.x / PC::CLUSTER;
-    const int gcols = (ps.tiles_q + CP - 1) / CP;   // tile groups per row of tiles
-    const int tiles = ps.tiles_p * gcols;           // tile groups
+    const int cl = blockIdx.x / 2;
+    const int ncl = gridDim.x / 2;
+    const int tiles = ps.tiles_p * ps.tiles_q;
     const int my_tiles = cl < tiles ? (tiles - 1 - cl) / ncl + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 3);          // the leader's three producers (both CTAs' bytes)
-            mbar_init(&empty[s], CP);        // the MMA commit of every pair of the cluster
+            mbar_init(&empty[s], 1);         // the pair's MMA commit
             mbar_init(&sf_ready[s], 2);      // the leader's two scale copiers
         }
         for (int i = 0; i < NACC; ++i) {
@@ -270,30 +253,28 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const int64_t groups = sf_groups(a.K);
     const int total_stages = my_tiles * ps.kt;
+    // The next kernel on the stream may launch; it waits in-kernel for this
+    // grid before touching anything this grid writes.
+    if (threadIdx.x == 0)
+        pdl_launch_dependents();
 
     if (warp == 4 || warp == 6 || warp == 7) {
         // ------------------------------------------------------ producers --
         if (lane == 0) {
             const int role = warp == 4 ? 0 : warp - 5;   // 0: A, 1: B, 2: scales
             const uint64_t pol = l2_policy_evict_last();
-            // Launched right after the scale relayout (programmatic stream
-            // serialisation), only the relaid scales depend on it.
-            if (role == 2)
+            // After this library's relayout (whose grid waited for the work
+            // before it) only the relaid scales depend on the preceding grid.
+            if (role == 2 || !a.ab_early)
                 pdl_wait_prerequisites();
-            // Bytes per 256-K chunk (A, B) or per stage (scales: the boxes
-            // always have the full stage's shape; past K they read atoms no
-            // MMA uses, or zero fill).
-            const uint32_t unit = role == 0 ? PC::A_CHUNK : role == 1 ? PC::B_CHUNK : PC::SF_BYTES;
+            const uint32_t unit = role == 0 ? PC::A_BYTES : role == 1 ? PC::B_BYTES : PC::SF_BYTES;
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
             bool stop = false;
-            // A (and scale-A) go to this CTA's counterpart in every pair.
-            const uint16_t mc_mask = static_cast<uint16_t>(CP == 2 ? (1u << rank) | (4u << rank) : 0u);
             for (int t = cl; t < tiles && !stop; t += ncl) {
-                int pt, qq;
-                pair_tile_coords(ps, gcols, t, pt, qq);
-                const int qt = qq * CP + static_cast<int>(pidx);
+                int pt, qt;
+                pair_tile_coords(ps, t, pt, qt);
                 const int arow = pt * 256 + static_cast<int>(rank) * kTileM;
                 const int brow = qt * BN + static_cast<int>(rank) * PC::B_ROWS;
                 const int sfa_atom = static_cast<int>(static_cast<int64_t>(pt * 2 + rank) * groups);
@@ -310,32 +291,16 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
                     // peer costs ~0.5 us); the peer's copies just complete
                     // their bytes on the leader's barrier, which cannot start
                     // this stage's next phase before the MMAs freed the stage.
-                    const int c0 = kt * KC;                        // first 256-K chunk
-                    const int nc = min(KC, ps.kchunks - c0);       // chunks inside K
                     if (leader)
-                        mbar_arrive_expect_tx(&full[stage], 2 * (role == 2 ? unit : nc * unit));
+                        mbar_arrive_expect_tx(&full[stage], 2 * unit);
                     if (role == 0) {
-                        for (int c = 0; c < nc; ++c) {
-                            if constexpr (CP == 1)
-                                tma_load_2d_pair(st + c * PC::A_CHUNK, &tmA, lbar, (c0 + c) * 128, arow, pol);
-                            else
-                                tma_load_2d_pair_mc(st + c * PC::A_CHUNK + pidx * (PC::A_CHUNK / 2), &tmA,
-                                                    lbar, (c0 + c) * 128,
-                                                    arow + static_cast<int>(pidx) * PC::A_LOAD_ROWS, mc_mask,
-                                                    pol);
-                        }
+                        tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
                     } else if (role == 1) {
-                        for (int c = 0; c < nc; ++c)
-                            tma_load_2d_pair(st + PC::A_BYTES + c * PC::B_CHUNK, &tmB, lbar, (c0 + c) * 128,
-                                             brow, pol);
+                        tma_load_2d_pair(st + PC::A_BYTES, &tmB, lbar, kt * 128, brow, pol);
                     } else {
                         uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
-                        if constexpr (CP == 1)
-                            tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * c0, pol);
-                        else
-                            tma_load_2d_pair_mc(sf + pidx * (PC::SFA_BYTES / 2), &tmSA, lbar, 0,
-                                                sfa_atom + 2 * c0 + static_cast<int>(pidx) * KC, mc_mask, pol);
-                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * c0, sfb_rb, pol);
+                        tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
+                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, sfb_rb, pol);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -416,9 +381,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
                                a.wait_limit, &g_device_status))
                     break;
                 tc_fence_after();
-                int pt, qq;
-                pair_tile_coords(ps, gcols, t, pt, qq);
-                const int qt = qq * CP + static_cast<int>(pidx);
+                int pt, qt;
+                pair_tile_coords(ps, t, pt, qt);
                 const uint32_t q_off = static_cast<uint32_t>(((qt * BN) % kSfRowBlock) / 32);
                 const uint32_t d_tmem = tmem + acc * BN;
                 for (int kt = 0; kt < ps.kt; ++kt, ++i) {
@@ -437,32 +401,24 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
                     const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(st));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + PC::A_BYTES));
-                    // Four K=64 MMAs per 256-K chunk; the last stage of a
-                    // tile may hold fewer than KC chunks.
-                    const int nc = min(KC, ps.kchunks - kt * KC);
+                    // Four K=64 MMAs per 256-K stage.
 #pragma unroll
-                    for (int c = 0; c < KC; ++c) {
-                        if (c >= nc)
-                            break;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t sf_id = (j & 1) * 2;
-                            const int g = 2 * c + (j >> 1);          // scale k-group
-                            mma_mxf4_pair(d_tmem, adesc + c * (PC::A_CHUNK >> 4) + 2 * j,
-                                          bdesc + c * (PC::B_CHUNK >> 4) + 2 * j,
-                                          idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
-                                          sfb_t + g * 4 * PC::SFB_RB + q_off,
-                                          (kt > 0 || c > 0 || j > 0) ? 1u : 0u);
-                        }
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t sf_id = (j & 1) * 2;
+                        const int g = j >> 1;                        // scale k-group
+                        mma_mxf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j,
+                                      idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
+                                      sfb_t + g * 4 * PC::SFB_RB + q_off,
+                                      (kt > 0 || j > 0) ? 1u : 0u);
                     }
-                    // Frees the stage in every CTA that loads into this pair's slots.
-                    mma_commit_pair(&empty[stage], static_cast<uint16_t>((1u << PC::CLUSTER) - 1u));
+                    // Frees the stage in both CTAs of the pair.
+                    mma_commit_pair(&empty[stage], static_cast<uint16_t>(3u));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                mma_commit_pair(&acc_full[acc], static_cast<uint16_t>(3u << lead));
+                mma_commit_pair(&acc_full[acc], static_cast<uint16_t>(3u));
                 acc_phase ^= 1u << acc;
                 acc = acc + 1 == NACC ? 0 : acc + 1;
             }
@@ -474,6 +430,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
     } else {
         // ------------------------------------------------------ epilogue --
         // warps 0-3: columns [0, HALF), warps 8-11: columns [HALF, BN).
+        // C and D may belong to the work before this grid.
+        pdl_wait_prerequisites();
         const int quarter = warp & 3;
         const int half = warp >> 3;
         const int row = quarter * 32 + lane;
@@ -488,9 +446,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC, CP, KC>::THREADS, 1)
                 break;
             acc_phase ^= 1u << acc;
             tc_fence_after();
-            int pt, qq;
-            pair_tile_coords(ps, gcols, t, pt, qq);
-            const int qt = qq * CP + static_cast<int>(pidx);
+            int pt, qt;
+            pair_tile_coords(ps, t, pt, qt);
             const int m = pt * 256 + static_cast<int>(rank) * kTileM + row;
             const int n0 = qt * BN + half * PC::HALF;
             const uint32_t t_row = t_lane + acc * BN;

@@ -28,7 +28,19 @@
 //           TMEM accumulator, then commits the stage back to the producers;
 //   warps 0-3  then the epilogue: tcgen05.ld the accumulator (warp w owns TMEM
 //           lanes 32w..32w+31 = tile rows), apply alpha/beta with C, round to
-//           bf16 and store; with split-K they store fp32 partials instead.
+//           bf16 and store.  With split-K they park the fp32 partial tile in
+//           the workspace instead; the CTA that completes a tile's count (an
+//           epoch-tagged counter per tile) then sums the tile's partials in
+//           split order 0, 1, ..., applies alpha/beta with C and rounds once,
+//           with all of its 256 threads -- no second launch, and the result
+//           does not depend on which split finished last.
+// The kernel is launched as a programmatic dependent of the preceding work on
+// the stream: it starts while that work drains and waits for it in-kernel
+// (griddepcontrol.wait) before the first read of A, C or the scales and
+// before any write.  With b_early, B's tiles (and its row-major or prepacked
+// scales) are first prefetched into L2: callers whose weights the preceding
+// work does not write let the weight stream of one GEMM overlap the tail of
+// the one before it.
 // With swap (skinny M), P = B and Q = A, so the tile holds D^T: TMEM lane = n,
 // column = m, and a warp's 32 lanes write 32 consecutive n of one row of D.
 //
@@ -79,11 +91,6 @@ struct Cfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(G == 1 || G == 2, "scale groups per stage");
-    // Cluster split-K: the fp32 partial tile parked in the idle ring, rows
-    // padded by 4 floats (16-byte vector stores without bank conflicts).
-    static constexpr int PART_STRIDE = BN + 4;
-    static constexpr int PART_BYTES = kTileM * PART_STRIDE * 4;
-    static_assert(PART_BYTES <= STAGES * STAGE_BYTES, "partial tile fits the ring");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -151,43 +158,40 @@ __device__ __forceinline__ void store_d_row(const GemmArgs &a, int m, int n0, fl
 }
 
 // D[m0 + i][n] = bf16(alpha * v[i] + beta * C) for the valid i (swap: one n
-// per lane, consecutive across the warp).
+// per lane, consecutive across the warp).  All of C is loaded before the
+// first store: C may alias D, so a load after a store could not be issued
+// early, and 32 dependent DRAM round trips would follow.
 __device__ __forceinline__ void store_d_col(const GemmArgs &a, int m0, int n, const float (&v)[32])
 {
     if (n >= a.N)
         return;
     const int mcount = min(32, a.M - m0);
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        x[i] = a.alpha * v[i];
+    if (a.beta != 0.0f) {
+        uint16_t c[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            c[i] = i < mcount ? a.C[(static_cast<int64_t>(m0) + i) * a.ldc + n] : uint16_t(0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            x[i] = fmaf(a.beta, bf16_bits_to_float(c[i]), x[i]);
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         if (i < mcount) {
-            const int64_t m = m0 + i;
-            float x = a.alpha * v[i];
-            if (a.beta != 0.0f)
-                x = fmaf(a.beta, bf16_bits_to_float(a.C[m * a.ldc + n]), x);
-            __nv_bfloat16 b = __float2bfloat16_rn(x);
-            a.D[m * a.ldd + n] = *reinterpret_cast<uint16_t *>(&b);
+            __nv_bfloat16 b = __float2bfloat16_rn(x[i]);
+            a.D[(static_cast<int64_t>(m0) + i) * a.ldd + n] = *reinterpret_cast<uint16_t *>(&b);
         }
     }
 }
 
 // One-tile kernel epilogue of one 32-column chunk of one row (no swap): r[i]
-// is the fp32 accumulator of D[m][n0 + i]; with split-K it goes to the
-// partials instead.
-__device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int z, int m, int n0,
-                                                const uint32_t (&r)[32])
+// is the fp32 accumulator of D[m][n0 + i].
+__device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int m, int n0, const uint32_t (&r)[32])
 {
-    if (a.split_k > 1) {
-        float *dst = a.ws + (static_cast<int64_t>(z) * a.M + m) * a.N + n0;
-        if ((a.N & 3) == 0 && n0 + 32 <= a.N) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<uint4 *>(dst + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
-        } else {
-            for (int i = 0; i < 32 && n0 + i < a.N; ++i)
-                dst[i] = __uint_as_float(r[i]);
-        }
-        return;
-    }
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -196,25 +200,152 @@ __device__ __forceinline__ void store_row_chunk(const GemmArgs &a, int z, int m,
 }
 
 // Same with swap: r[i] is the accumulator of D[m0 + i][n].
-__device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int z, int m0, int n,
-                                                const uint32_t (&r)[32])
+__device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int m0, int n, const uint32_t (&r)[32])
 {
-    if (n >= a.N)
-        return;
-    const int mcount = min(32, a.M - m0);
-    if (a.split_k > 1) {
-        float *dst = a.ws + (static_cast<int64_t>(z) * a.M + m0) * a.N + n;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < mcount)
-                dst[static_cast<int64_t>(i) * a.N] = __uint_as_float(r[i]);
-        return;
-    }
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i)
         v[i] = __uint_as_float(r[i]);
     store_d_col(a, m0, n, v);
+}
+
+// Split-K: slot (tile, z) of the partials holds 128 rows x part_cols fp32
+// values, row-major by tile row (TMEM lane).  Row `row` of this CTA's
+// partial, columns [c0, c0 + 32) of the accumulator (those below part_cols).
+__device__ __forceinline__ float *partial_slot(const GemmArgs &a, int64_t tile, int z)
+{
+    return a.partials + (tile * a.split_k + z) * static_cast<int64_t>(kTileM * a.part_cols);
+}
+
+__device__ __forceinline__ void park_partial_chunk(const GemmArgs &a, float *row_ptr, int c0,
+                                                   const uint32_t (&r)[32])
+{
+    const int cn = min(32, a.part_cols - c0);
+    float *dst = row_ptr + c0;
+    if ((a.part_cols & 3) == 0 && cn == 32) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+            __stcg(reinterpret_cast<float4 *>(dst + i),
+                   make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < cn)
+                __stcg(dst + i, __uint_as_float(r[i]));
+    }
+}
+
+// Count this CTA into its tile and report whether it completed the count.
+// The word holds (epoch << 32) | done; a word tagged with another call's
+// epoch (never written, or left by a call that stopped on a timeout) counts
+// as zero, so the workspace needs no clearing.  The CTA that completes the
+// count resets the word to 0, so a replay of a captured call, which repeats
+// the tag, starts from zero too.  Lock-free: each failed exchange means
+// another CTA of the tile got its increment in.
+__device__ __forceinline__ bool tile_count_done(unsigned long long *word, uint32_t epoch, int split)
+{
+    unsigned long long cur = atomicAdd(word, 0ull);
+    for (;;) {
+        const unsigned long long next = (static_cast<uint32_t>(cur >> 32) == epoch)
+                                            ? cur + 1ull
+                                            : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(word, cur, next);
+        if (prev == cur)
+            return static_cast<int>(next & 0xFFFFFFFFull) == split;
+        cur = prev;
+    }
+}
+
+// The CTA that completed a tile's count: thread t sums row (t & 127), one
+// half of the columns (t >> 7), over the tile's split partials in the fixed
+// order z = 0, 1, ..., split-1, then applies alpha / beta with C and rounds
+// once to bf16 (swap: the row is n, the columns are m).
+template <bool SWAP>
+__device__ __forceinline__ void reduce_tile(const GemmArgs &a, int64_t tile, int p0, int q0, int t)
+{
+    const int row = t & (kTileM - 1);
+    const int prows = SWAP ? a.N : a.M;
+    if (p0 + row >= prows)
+        return;
+    const int qvalid = min(a.part_cols, (SWAP ? a.M : a.N) - q0);
+    // Halves on 32-column boundaries: a chunk's stores (bounded by M and N
+    // only) never reach the other half's columns.
+    const int half = ((a.part_cols + 63) / 64) * 32;
+    const int c_begin = (t >> 7) * half;
+    const int c_end = min(qvalid, c_begin + half);
+    const bool vec = (a.part_cols & 3) == 0;
+    const float *base = partial_slot(a, tile, 0) + static_cast<int64_t>(row) * a.part_cols;
+    const int64_t zstride = static_cast<int64_t>(kTileM) * a.part_cols;
+    for (int cg = c_begin; cg < c_end; cg += 32) {
+        const int cn = min(32, c_end - cg);
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            acc[i] = 0.0f;
+        // Every split's loads of a step are issued before any is added, and
+        // each column adds its splits in the order z = 0, 1, ... whatever
+        // the path (so both paths give the same bits).
+        if (vec) {
+            // Rows of 16-byte aligned float4s; two splits per step.
+            const int nv = (cn + 3) / 4;
+            for (int z = 0; z < a.split_k; z += 2) {
+                const bool two = z + 1 < a.split_k;
+                const float4 *s0 = reinterpret_cast<const float4 *>(base + z * zstride + cg);
+                const float4 *s1 = reinterpret_cast<const float4 *>(base + (z + 1) * zstride + cg);
+                float4 x[8], y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    x[i] = i < nv ? __ldcg(s0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    y[i] = (two && i < nv) ? __ldcg(s1 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc[4 * i] += x[i].x;
+                    acc[4 * i + 1] += x[i].y;
+                    acc[4 * i + 2] += x[i].z;
+                    acc[4 * i + 3] += x[i].w;
+                }
+                if (two) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        acc[4 * i] += y[i].x;
+                        acc[4 * i + 1] += y[i].y;
+                        acc[4 * i + 2] += y[i].z;
+                        acc[4 * i + 3] += y[i].w;
+                    }
+                }
+            }
+        } else {
+            // Scalar columns, eight at a time, four splits per step.
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (g * 8 >= cn)
+                    break;
+                for (int z0 = 0; z0 < a.split_k; z0 += 4) {
+                    float t[4][8];
+#pragma unroll
+                    for (int zz = 0; zz < 4; ++zz)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            t[zz][i] = (z0 + zz < a.split_k && g * 8 + i < cn)
+                                           ? __ldcg(base + (z0 + zz) * zstride + cg + g * 8 + i)
+                                           : 0.0f;
+#pragma unroll
+                    for (int zz = 0; zz < 4; ++zz)
+                        if (z0 + zz < a.split_k)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                acc[g * 8 + i] += t[zz][i];
+                }
+            }
+        }
+        if (!SWAP)
+            store_d_row(a, p0 + row, q0 + cg, acc);
+        else
+            store_d_col(a, q0 + cg, p0 + row, acc);
+    }
 }
 
 // Row-major scales -> one lane's share of a 128-row block for stage kt: rows
@@ -362,10 +493,45 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
 
 constexpr int kGemmThreads = 256;
 
-// FMT 0: fp4 (E2M1) elements, kind::mxf4; FMT 1: 8-bit (E4M3 / E5M2)
-// elements, kind::mxf8f6f4 with the element types in a.idesc8.
-template <int BN, int STAGES, bool SWAP, int FMT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// L2 prefetch of this CTA's share of B (b_early): its operand tiles for the
+// K stages [kt0, kt0 + nkt) and their scales.  Called by one whole warp;
+// lane 0 issues the tile prefetches, every lane some scale rows.
+template <int G>
+__device__ __forceinline__ void prefetch_b_share(const GemmArgs &a, const CUtensorMap *tmB, int row0,
+                                                 int nrows, int kt0, int nkt, int lane)
+{
+    if (lane == 0)
+        for (int i = 0; i < nkt; ++i)
+            tma_prefetch_2d(tmB, (kt0 + i) * 128, row0);
+    const uint8_t *sfb = a.p_is_b ? a.sfP : a.sfQ;
+    if (a.sf_rowmajor) {
+        // Row-major scales: 4G bytes per stage and row.
+        const int64_t ld = a.p_is_b ? a.ldsP : a.ldsQ;
+        const int rows = a.p_is_b ? a.rowsP : a.rowsQ;
+        const int64_t b0 = static_cast<int64_t>(kt0) * 4 * G;
+        const int64_t b1 = min(static_cast<int64_t>(kt0 + nkt) * 4 * G, static_cast<int64_t>(a.K / 32)) - 1;
+        for (int r = lane; r < nrows; r += 32) {
+            if (row0 + r >= rows)
+                break;
+            const uint8_t *p = sfb + static_cast<int64_t>(row0 + r) * ld;
+            prefetch_l2(p + b0);
+            if (((reinterpret_cast<uintptr_t>(p + b0) ^ reinterpret_cast<uintptr_t>(p + b1)) >> 7) != 0)
+                prefetch_l2(p + b1);
+        }
+    } else if (lane == 0) {
+        // Relaid atoms: G per stage, contiguous along K within a row block.
+        for (int rb = 0; rb * kSfRowBlock < nrows; ++rb)
+            bulk_prefetch_l2(sfb + static_cast<int64_t>(row0 / kSfRowBlock + rb) * a.sf_rb_stride +
+                                 static_cast<int64_t>(kt0) * G * kSfAtomBytes,
+                             static_cast<uint32_t>(nkt * G * kSfAtomBytes));
+    }
+}
+
+// FMT 0: fp4 (E2M1) elements, kind::mxf4; FMT 1: one byte per element
+// (E4M3 / E5M2 / padded E2M3, E3M2, E2M1), kind::mxf8f6f4 with the element
+// types in a.idesc8.  MINB: CTAs per SM the configuration is planned for.
+template <int BN, int STAGES, bool SWAP, int FMT, int MINB>
+__global__ void __launch_bounds__(kGemmThreads, MINB)
     gemm_mxf4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmP,
                      const __grid_constant__ CUtensorMap tmQ)
 {
@@ -381,6 +547,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *acc_full = sf_full + STAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -388,9 +555,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // band of up to 8 tile columns (Q) before the next tile row (P), so the
     // CTAs resident at once share a few P and Q panels in L2 instead of
     // sweeping all of P for every column.
+    const int tp = static_cast<int>(gridDim.x), tq = static_cast<int>(gridDim.y);
     int pt, qt;
     {
-        const int tp = static_cast<int>(gridDim.x), tq = static_cast<int>(gridDim.y);
         const int lin = static_cast<int>(blockIdx.y) * tp + static_cast<int>(blockIdx.x);
         const int band = tq < 8 ? tq : 8;
         const int b = lin / (band * tp);
@@ -399,6 +566,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         pt = within / bw;
         qt = b * band + within % bw;
     }
+    const int64_t tile = static_cast<int64_t>(pt) * tq + qt;
     const int p0 = pt * kTileM;
     const int q0 = qt * BN;
     const int z = blockIdx.z;
@@ -413,6 +581,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
+        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 5) {
@@ -427,13 +596,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // A split-K reduce launched after this kernel may start its prologue; it
-    // waits for this grid's completion before reading the partials.
+    // The next kernel on the stream may launch now; it waits in-kernel for
+    // this grid before it touches anything this grid writes.
     if (threadIdx.x == 0)
         pdl_launch_dependents();
 
     if (warp == 4 || warp >= 6) {
         // ------------------------------------------------------ producer --
+        if (a.b_early && nkt > 0 && warp == (a.sf_rowmajor ? 4 : (a.p_is_b ? 4 : 6)))
+            prefetch_b_share<G>(a, a.p_is_b ? &tmP : &tmQ, a.p_is_b ? p0 : q0,
+                                a.p_is_b ? kTileM : BN, kt0, nkt, lane);
+        // Everything below may read the preceding work's output.
+        pdl_wait_prerequisites();
         if (a.sf_rowmajor && a.sf_async && nkt > 0 && warp == 4) {
             // Whole warp: lane 0 issues the operand TMAs; every lane copies its
             // lines of the stage's scale atoms with 4-byte cp.async straight
@@ -632,100 +806,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------ epilogue --
         bool ok = nkt > 0 && mbar_wait(acc_full, 0, abort_flag, a.wait_limit, &g_device_status);
         ok = __all_sync(0xffffffffu, ok);
-        if (a.cluster_split > 1) {
-            // Park this split's fp32 partial (valid columns, rounded up to
-            // 32) in the ring, which the MMAs no longer read; the cluster
-            // reduces the partials below.
-            float *part = reinterpret_cast<float *>(smem);
-            const int row = warp * 32 + lane;
-            const int cols = SWAP ? min(BN, a.M - q0) : min(BN, a.N - q0);
-            const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-            if (ok)
-                tc_fence_after();
-#pragma unroll 1
-            for (int c0 = 0; c0 < cols; c0 += 32) {
-                uint32_t r[32];
-                if (ok) {
-                    tmem_ld_32x32b_x32(t_row + c0, r);
-                    tmem_ld_wait(r);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = 0u;
-                }
-                float *dst = part + row * Cf::PART_STRIDE + c0;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<uint4 *>(dst + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
-            }
-        } else if (ok) {
+        // C, D and the workspace may belong to the preceding work.
+        pdl_wait_prerequisites();
+        if (ok) {
             tc_fence_after();
             const int row = warp * 32 + lane;
             const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+            if (a.split_k > 1) {
+                // Park this split's partial (its valid columns) in the tile's slot.
+                float *row_ptr = partial_slot(a, tile, z) + static_cast<int64_t>(row) * a.part_cols;
+                const int cols = min(a.part_cols, (SWAP ? a.M : a.N) - q0);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                if (SWAP && q0 + c0 >= a.M)
-                    break;                                   // padding columns of D^T
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c0, r);
-                tmem_ld_wait();
-                if (!SWAP) {
-                    const int m = p0 + row;
-                    if (m < a.M && q0 + c0 < a.N)
-                        store_row_chunk(a, z, m, q0 + c0, r);
-                } else {
-                    store_col_chunk(a, z, q0 + c0, p0 + row, r);
+                for (int c0 = 0; c0 < cols; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c0, r);
+                    tmem_ld_wait(r);
+                    park_partial_chunk(a, row_ptr, c0, r);
                 }
-            }
-        }
-    }
-
-    if (a.cluster_split > 1) {
-        // Split-K inside the cluster: rank r of the S CTAs of this tile sums
-        // rows r, r + S, ... of all S partials in rank order (the order of the
-        // separate reduce kernel) and stores them as D.  Barrier 1 makes the
-        // partials visible; barrier 2 keeps every CTA's shared memory alive
-        // until its peers have read it.
-        tc_fence_before();
-        cluster_sync();
-        const int S = a.cluster_split;
-        const int rank = static_cast<int>(cluster_ctarank());
-        const int row = warp * 32 + lane;
-        if (warp < 4 && row % S == rank) {
-            const int cols = SWAP ? min(BN, a.M - q0) : min(BN, a.N - q0);
-            const uint32_t mine = smem_addr(smem) + static_cast<uint32_t>(row * Cf::PART_STRIDE * 4);
+                __threadfence();
+            } else {
 #pragma unroll 1
-            for (int c0 = 0; c0 < cols; c0 += 32) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] = 0.0f;
-#pragma unroll 1
-                for (int j = 0; j < S; ++j) {
-                    const uint32_t src = map_to_rank(mine, static_cast<uint32_t>(j)) + c0 * 4;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 x = ld_dsmem_v4(src + i * 4);
-                        v[i] += x.x;
-                        v[i + 1] += x.y;
-                        v[i + 2] += x.z;
-                        v[i + 3] += x.w;
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    if (SWAP && q0 + c0 >= a.M)
+                        break;                                   // padding columns of D^T
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c0, r);
+                    tmem_ld_wait(r);
+                    if (!SWAP) {
+                        const int m = p0 + row;
+                        if (m < a.M && q0 + c0 < a.N)
+                            store_row_chunk(a, m, q0 + c0, r);
+                    } else {
+                        store_col_chunk(a, q0 + c0, p0 + row, r);
                     }
                 }
-                if (!SWAP) {
-                    const int m = p0 + row;
-                    if (m < a.M)
-                        store_d_row(a, m, q0 + c0, v);
-                } else {
-                    store_d_col(a, q0 + c0, p0 + row, v);
-                }
             }
         }
-        cluster_sync();
     }
 
     tc_fence_before();
     __syncthreads();
+    if (a.split_k > 1 && nkt > 0) {
+        // Count this CTA into its tile (its partial rows are written and
+        // fenced); the CTA that completes the count reduces the tile.
+        if (threadIdx.x == 0 && !*abort_flag) {
+            const bool last = tile_count_done(a.tile_count + tile, a.epoch, a.split_k);
+            // The tile is complete: clear its counter for the next use of the
+            // workspace (a CUDA-graph replay repeats this call's tag).
+            if (last)
+                atomicExch(a.tile_count + tile, 0ull);
+            *last_flag = last ? 1 : 0;
+        }
+        __syncthreads();
+        if (*last_flag) {
+            __threadfence();
+            pdl_wait_prerequisites();
+            reduce_tile<SWAP>(a, tile, p0, q0, threadIdx.x);
+        }
+    }
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, Cf::TMEM_COLS);
@@ -734,19 +872,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 }  // namespace mxfp4
 
-#include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
 
 namespace mxfp4 {
 
 // ----------------------------------------------------------- host side --
 
-template <int BN, int STAGES, bool SWAP, int FMT>
+template <int BN, int STAGES, bool SWAP, int FMT, int MINB>
 static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
                               dim3 grid, cudaStream_t stream)
 {
     using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
-    auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP, FMT>;
+    auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP, FMT, MINB>;
     // Opt in to the large dynamic shared memory once per device.
     static std::atomic<int> configured[64];
     int dev = 0;
@@ -759,26 +896,20 @@ static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const C
             return e;
         configured[dev].store(1, std::memory_order_relaxed);
     }
-    if (a.cluster_split > 1) {
-        // The split_k CTAs of a tile (grid z) form one cluster.
-        if (static_cast<int>(grid.z) != a.cluster_split || a.cluster_split > 8)
-            return cudaErrorInvalidConfiguration;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(kGemmThreads);
-        cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = static_cast<unsigned>(a.cluster_split);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, a, tmP, tmQ);
-    }
-    kern<<<grid, kGemmThreads, Cf::SMEM_BYTES, stream>>>(a, tmP, tmQ);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the grid may start while the preceding
+    // work on the stream drains; the kernel waits for it (griddepcontrol.wait)
+    // before the accesses that depend on it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, tmP, tmQ);
 }
 
 size_t gemm_smem_bytes(const GemmShape &s)
@@ -797,7 +928,7 @@ bool gemm_config_exists(const GemmShape &s)
     if (!s.swap)
         return (s.tile_n == 256 && s.stages == 4) || (s.tile_n == 128 && s.stages == 6) ||
                (s.tile_n == 64 && s.stages == 8);
-    return s.tile_n == 64 && (s.stages == 4 || s.stages == 8);
+    return s.tile_n == 64 && s.stages == 4;
 }
 
 template <int FMT>
@@ -806,16 +937,15 @@ static cudaError_t launch_gemm_fmt(const GemmArgs &a, const CUtensorMap &tmP, co
 {
     if (!s.swap) {
         if (s.tile_n == 256 && s.stages == 4)
-            return launch_cfg<256, 4, false, FMT>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<256, 4, false, FMT, 1>(a, tmP, tmQ, grid, stream);
         if (s.tile_n == 128 && s.stages == 6)
-            return launch_cfg<128, 6, false, FMT>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<128, 6, false, FMT, 1>(a, tmP, tmQ, grid, stream);
         if (s.tile_n == 64 && s.stages == 8)
-            return launch_cfg<64, 8, false, FMT>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 8, false, FMT, 1>(a, tmP, tmQ, grid, stream);
     } else {
+        // Two CTAs per SM (the plan's slots for skinny shapes).
         if (s.tile_n == 64 && s.stages == 4)
-            return launch_cfg<64, 4, true, FMT>(a, tmP, tmQ, grid, stream);
-        if (s.tile_n == 64 && s.stages == 8)
-            return launch_cfg<64, 8, true, FMT>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 4, true, FMT, 2>(a, tmP, tmQ, grid, stream);
     }
     return cudaErrorInvalidConfiguration;
 }
@@ -835,117 +965,18 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
     return launch_gemm_fmt<1>(b, tmP, tmQ, s, grid, stream);
 }
 
-template <int BN, int STAGES, bool SWAP, int NACC, int NSLOT>
-static cudaError_t launch_persistent_cfg(const GemmArgs &a, const Sched &sch,
-                                         const CUtensorMap &tmP, const CUtensorMap &tmQ,
-                                         const CUtensorMap &tmSP, const CUtensorMap &tmSQ,
-                                         cudaStream_t stream)
-{
-    using PC = PCfg<BN, STAGES, NACC, NSLOT>;
-    auto kern = gemm_mxf4_persistent<BN, STAGES, SWAP, NACC, NSLOT>;
-    static std::atomic<int> configured[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
-    kern<<<sch.ctas, 192, PC::SMEM_BYTES, stream>>>(a, sch, tmP, tmQ, tmSP, tmSQ);
-    return cudaGetLastError();
-}
+// The compiled pair configuration: 6 stages, 256 x 256 tiles, one accumulator.
+using PairDefault = PairCfg<6, 256, 1>;
 
-template <int BN, int STAGES, bool SWAP, int NACC, int NSLOT>
-static int occupancy_cfg()
-{
-    // The occupancy calculator is slow on the host: ask once per device.
-    static std::atomic<int> cached[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    if (dev >= 0 && dev < 64 && cached[dev] > 0)
-        return cached[dev];
-    using PC = PCfg<BN, STAGES, NACC, NSLOT>;
-    auto kern = gemm_mxf4_persistent<BN, STAGES, SWAP, NACC, NSLOT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 192, PC::SMEM_BYTES) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    // Tensor memory: each resident CTA holds TMEM_COLS of the SM's 512.
-    const int by_tmem = 512 / PC::TMEM_COLS;
-    const int occ = n < by_tmem ? n : by_tmem;
-    if (dev >= 0 && dev < 64)
-        cached[dev] = occ;
-    return occ;
-}
+size_t gemm_pair_smem_bytes() { return PairDefault::SMEM_BYTES; }
 
-// Compiled persistent configurations:
-// (tile_n, stages, swap, accumulator buffers, scale staging slots).
-#define MXFP4_PERSISTENT_CONFIGS(X) \
-    X(256, 4, false, 1, 3)          \
-    X(128, 6, false, 2, 3)          \
-    X(64, 8, false, 2, 4)           \
-    X(64, 8, true, 2, 4)
-
-size_t gemm_persistent_smem_bytes(const GemmShape &s)
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
+                             const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
+                             cudaStream_t stream)
 {
-#define X(BN, ST, SW, NA, NS)                                                    \
-    if (s.tile_n == BN && s.stages == ST && (s.swap != 0) == SW && s.nacc == NA) \
-        return PCfg<BN, ST, NA, NS>::SMEM_BYTES;
-    MXFP4_PERSISTENT_CONFIGS(X)
-#undef X
-    return 0;
-}
-
-int gemm_persistent_occupancy(const GemmShape &s)
-{
-#define X(BN, ST, SW, NA, NS)                                                    \
-    if (s.tile_n == BN && s.stages == ST && (s.swap != 0) == SW && s.nacc == NA) \
-        return occupancy_cfg<BN, ST, SW, NA, NS>();
-    MXFP4_PERSISTENT_CONFIGS(X)
-#undef X
-    return 0;
-}
-
-cudaError_t launch_gemm_persistent(const GemmArgs &a, const Sched &sch, const CUtensorMap &tmP,
-                                   const CUtensorMap &tmQ, const CUtensorMap &tmSP,
-                                   const CUtensorMap &tmSQ, const GemmShape &s, cudaStream_t stream)
-{
-#define X(BN, ST, SW, NA, NS)                                                    \
-    if (s.tile_n == BN && s.stages == ST && (s.swap != 0) == SW && s.nacc == NA) \
-        return launch_persistent_cfg<BN, ST, SW, NA, NS>(a, sch, tmP, tmQ, tmSP, tmSQ, stream);
-    MXFP4_PERSISTENT_CONFIGS(X)
-#undef X
-    return cudaErrorInvalidConfiguration;
-}
-
-// (tile N, accumulators, stages) of the compiled pair configurations.
-size_t gemm_pair_smem_bytes(int tile_n, int k_chunks)
-{
-    if (tile_n == 192)
-        return PairCfg<7, 192, 2, 1, 1>::SMEM_BYTES;
-    return k_chunks == 2 ? PairCfg<3, 256, 1, 1, 2>::SMEM_BYTES : PairCfg<6, 256, 1, 1, 1>::SMEM_BYTES;
-}
-
-template <int STAGES, int BN, int NACC, int CP, int KC>
-static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int ctas,
-                                   const CUtensorMap &tmA, const CUtensorMap &tmB,
-                                   const CUtensorMap &tmSA, const CUtensorMap &tmSB,
-                                   bool after_relayout, cudaStream_t stream)
-{
-    using PC = PairCfg<STAGES, BN, NACC, CP, KC>;
-    auto kern = gemm_mxf4_pair<STAGES, BN, NACC, CP, KC>;
+    using PC = PairDefault;
+    auto kern = gemm_mxf4_pair<6, 256, 1>;
     static std::atomic<int> max_clusters[64];   // per device; 0 = not yet queried
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -957,7 +988,7 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = PC::CLUSTER;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -968,9 +999,7 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
         if (e != cudaSuccess)
             return e;
         // The kernel is persistent: every cluster must be resident at once.
-        // Clusters of four fit fewer times than the SM count suggests when a
-        // GPC's SM count is not a multiple of four.
-        cfg.gridDim = dim3(PC::CLUSTER);
+        cfg.gridDim = dim3(2);
         e = cudaOccupancyMaxActiveClusters(&limit, kern, &cfg);
         if (e != cudaSuccess)
             return e;
@@ -979,11 +1008,11 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
         if (dev < 64)
             max_clusters[dev] = limit;
     }
-    int clusters = ctas / PC::CLUSTER;
+    int clusters = ctas / 2;
     clusters = clusters < limit ? clusters : limit;
     if (clusters <= 0)
         return cudaErrorInvalidConfiguration;
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * PC::CLUSTER));
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2));
     if (after_relayout) {
         // Right after this library's scale relayout: programmatic stream
         // serialisation lets the GEMM's prologue and operand loads overlap
@@ -993,33 +1022,12 @@ static cudaError_t launch_pair_cfg(const GemmArgs &a, const PairSched &ps, int c
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;
     }
-    PairSched sched = ps;
-    sched.kt = (ps.kchunks + KC - 1) / KC;
-    return cudaLaunchKernelEx(&cfg, kern, a, sched, tmA, tmB, tmSA, tmSB);
-}
-
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tile_n, int cluster_pairs, int k_chunks, int tiles_p,
-                             int tiles_q, int ctas, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
-                             cudaStream_t stream)
-{
     PairSched ps;
     ps.tiles_p = tiles_p;
     ps.tiles_q = tiles_q;
     ps.kt = a.kt_total;
-    ps.kchunks = a.kt_total;
     ps.group = tiles_p < 8 ? tiles_p : 8;
-    if (tile_n == 192 && cluster_pairs == 1 && k_chunks == 1)
-        return launch_pair_cfg<7, 192, 2, 1, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256 && cluster_pairs == 1 && k_chunks == 1)
-        return launch_pair_cfg<6, 256, 1, 1, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256 && cluster_pairs == 2 && k_chunks == 1)
-        return launch_pair_cfg<6, 256, 1, 2, 1>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256 && cluster_pairs == 1 && k_chunks == 2)
-        return launch_pair_cfg<3, 256, 1, 1, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    if (tile_n == 256 && cluster_pairs == 2 && k_chunks == 2)
-        return launch_pair_cfg<3, 256, 1, 2, 2>(a, ps, ctas, tmA, tmB, tmSA, tmSB, after_relayout, stream);
-    return cudaErrorInvalidConfiguration;
+    return cudaLaunchKernelEx(&cfg, kern, a, ps, tmA, tmB, tmSA, tmSB);
 }
 
 // Test hook: one wait on an mbarrier nobody arrives at.

@@ -12,8 +12,10 @@
 // library holds it until the process exits.  All calls share it, so calls
 // whose work overlaps on the GPU (different streams, or different host
 // threads on the same device) race on it and must be serialised by the
-// caller.  Each call rewrites every byte of scratch it reads, so nothing
-// carried over from the previous call needs clearing first.
+// caller.  Nothing carried over from the previous call needs clearing: each
+// call writes its relaid scales and split-K partials before reading them, and
+// the split-K tile counters carry a per-call tag, so a counter left behind by
+// an earlier call reads as zero.
 #include <mutex>
 
 #include "../../include/mxfp4_gemm.h"
@@ -62,6 +64,16 @@ extern "C" int mxfp4_gemm_noalloc(void *D, int64_t ldd, const void *C, int64_t l
     const size_t need = mxfp4_gemm_workspace_size(M, N, K, split_k);
     if (need > static_cast<size_t>(MXFP4_NOALLOC_SCRATCH_BYTES))
         return MXFP4_ERR_WORKSPACE;   // this shape needs more scratch than the fixed array
+    // The array's address is per device: the stream must run on the device
+    // whose copy is passed to the kernels.
+    int cur = -1, sdev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess ||
+        cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+        cudaGetLastError();
+        return MXFP4_ERR_CUDA;
+    }
+    if (sdev != cur)
+        return MXFP4_ERR_INVALID_ARG;
     void *scratch = scratch_on_current_device();
     if (!scratch)
         return MXFP4_ERR_CUDA;

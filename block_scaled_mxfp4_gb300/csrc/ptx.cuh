@@ -131,6 +131,34 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Bring one 2-D box of a tensor into L2 (no shared-memory destination, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Bring the L2 line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
+// Barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Asynchronous 4-byte global -> shared copy; bytes past src_bytes (0..4) are
 // zero-filled and not read.
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)
@@ -500,20 +528,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
-// Multicast form of tma_load_2d_pair: the box lands at the same offset in
-// the shared memory of every CTA in cta_mask, and each destination's bytes
-// complete on the barrier at cbar's offset in the leader (even) CTA of that
-// destination's pair; cbar addresses the issuing pair's leader.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void *dst, const CUtensorMap *map, uint32_t cbar,
-                                                    int x, int y, uint16_t cta_mask, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
         : "memory");
 }
 

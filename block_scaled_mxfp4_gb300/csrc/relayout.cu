@@ -1,6 +1,4 @@
-// Scale-factor relayout and split-K reduction kernels.
-#include <cuda_bf16.h>
-
+// Scale-factor relayout kernel.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -45,8 +43,12 @@ __global__ void __launch_bounds__(kRelayoutThreads)
 {
     __shared__ uint32_t tile[128][kGroupsPerCta + 1];
     const int t = threadIdx.x;
-    // The GEMM that follows may start its prologue (it waits for this grid
-    // before reading the relaid scales).
+    // Launched as a programmatic dependent of the preceding work on the
+    // stream: the scales may be that work's output, so wait for it first.
+    // Only then let the GEMM that follows launch: it reads A and B before its
+    // own wait (on this grid), which is safe once the work before this grid
+    // has finished.
+    pdl_wait_prerequisites();
     if (t == 0)
         pdl_launch_dependents();
     const int op = static_cast<int64_t>(blockIdx.x) < job.rblocks0 ? 0 : 1;
@@ -114,10 +116,17 @@ static cudaError_t launch_relayout_job(RelayoutJob &job, int nops, int K, cudaSt
         job.ld[1] = job.ld[0];
         job.vec4[1] = job.vec4[0];
     }
-    dim3 grid(static_cast<unsigned>(total),
-              static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
-    scale_relayout_kernel<<<grid, kRelayoutThreads, 0, stream>>>(job, K / 32, groups);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(total),
+                       static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
+    cfg.blockDim = dim3(kRelayoutThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, scale_relayout_kernel, job, K / 32, groups);
 }
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
@@ -145,104 +154,6 @@ cudaError_t launch_scale_relayout2(uint8_t *dst0, const uint8_t *src0, int rows0
     job.rows[1] = rows1;
     job.ld[1] = ld1;
     return launch_relayout_job(job, 2, K, stream);
-}
-
-// --------------------------------------------------------- split-K reduce --
-//
-// D[m][n] = bf16(alpha * sum_{z=0..split-1} ws[z][m][n] + beta * C[m][n]),
-// summing the fp32 partials in the fixed order z = 0, 1, ..., so the result
-// does not depend on scheduling (the page's bf16-atomic split-K, section
-// "Verification", loses precision; this keeps fp32 until the one rounding).
-// Each thread owns 4 consecutive n of one row.
-
-__device__ __forceinline__ uint16_t to_bf16_bits(float v)
-{
-    __nv_bfloat16 b = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t *>(&b);
-}
-
-constexpr int kReduceThreads = 128;
-constexpr int kReduceMaxSplit = 16;
-
-// Each thread owns 4 consecutive n of one row and loads all its split
-// partials before adding them (in split order), so a thread waits for one
-// memory round trip rather than one per split.
-__global__ void __launch_bounds__(kReduceThreads)
-    splitk_reduce_kernel(const float *__restrict__ ws, int split, int M, int N, float alpha,
-                         float beta, const uint16_t *__restrict__ C, int64_t ldc,
-                         uint16_t *__restrict__ D, int64_t ldd)
-{
-    // Launched right after the GEMM with programmatic stream serialisation:
-    // the partials are complete and visible once the GEMM grid has finished.
-    pdl_wait_prerequisites();
-    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
-    const int64_t total = quads * M;
-    const int64_t plane = static_cast<int64_t>(M) * N;
-    const bool vec = (N & 3) == 0;
-    for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < total;
-         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t m = q / quads;
-        const int n = static_cast<int>(q - m * quads) * 4;
-        const int cnt = min(4, N - n);
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        const float *p = ws + m * N + n;
-        if (vec) {
-            float4 v[kReduceMaxSplit];
-#pragma unroll
-            for (int z = 0; z < kReduceMaxSplit; ++z)
-                if (z < split)
-                    v[z] = __ldcs(reinterpret_cast<const float4 *>(p + z * plane));
-#pragma unroll
-            for (int z = 0; z < kReduceMaxSplit; ++z) {
-                if (z < split) {
-                    s[0] += v[z].x;
-                    s[1] += v[z].y;
-                    s[2] += v[z].z;
-                    s[3] += v[z].w;
-                }
-            }
-        } else {
-            for (int z = 0; z < split; ++z)
-                for (int i = 0; i < cnt; ++i)
-                    s[i] += p[z * plane + i];
-        }
-        for (int i = 0; i < cnt; ++i) {
-            float v = alpha * s[i];
-            if (beta != 0.0f)
-                v = fmaf(beta, __uint_as_float(static_cast<uint32_t>(C[m * ldc + n + i]) << 16), v);
-            D[m * ldd + n + i] = to_bf16_bits(v);
-        }
-    }
-}
-
-cudaError_t launch_splitk_reduce(const float *ws, int split, int M, int N, float alpha, float beta,
-                                 const uint16_t *C, int64_t ldc, uint16_t *D, int64_t ldd, int sms,
-                                 cudaStream_t stream)
-{
-    if (split > kReduceMaxSplit)
-        return cudaErrorInvalidValue;
-    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4 * M;
-    int64_t blocks = (quads + kReduceThreads - 1) / kReduceThreads;
-    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 16;
-    if (blocks > cap)
-        blocks = cap;
-    if (blocks < 1)
-        blocks = 1;
-    // Programmatic stream serialisation: the reduce grid is scheduled while
-    // the GEMM (which triggers early) still runs and waits in-kernel for its
-    // completion, hiding the launch gap between the two.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(kReduceThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, split, M, N, alpha, beta, C, ldc, D,
-                              ldd);
 }
 
 }  // namespace mxfp4

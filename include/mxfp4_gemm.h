@@ -67,26 +67,17 @@ typedef struct mxfp4_plan {
     int tile_n;             /* MMA N columns per tile */
     int tile_k;             /* K elements per pipeline stage */
     int stages;             /* shared-memory ring depth */
-    int split_k;            /* K splits; > 1 adds the fp32 reduce kernel */
+    int split_k;            /* K splits; > 1: fp32 partials summed in the GEMM */
     int k_tiles_per_split;  /* tile_k blocks handled by one split */
     int grid_x, grid_y, grid_z;
-    size_t workspace_bytes; /* split-K partials (what mxfp4_gemm_prepacked needs) */
+    size_t workspace_bytes; /* split-K tile counters and partials (what
+                               mxfp4_gemm_prepacked needs) */
     int relayout_pass;      /* 1: mxfp4_gemm relays the scales out in a separate
                                pass into its workspace (compute-bound shapes);
                                0: the GEMM builds the scale layout itself */
-    int persistent;         /* 1: persistent stream-K kernel (MXFP4_KERNEL override) */
-    int ctas;               /* persistent: CTAs (all resident at once) */
-    int dp_waves;           /* persistent: whole tiles per CTA before stream-K */
-    long long sk_units;     /* persistent: K stages shared out stream-K */
-    int pair;               /* 1: CTA-pair kernel (256 x tile_n tiles over two
-                               SMs, tile_n 256 or 192) */
-    int gemv;               /* 1: CUDA-core GEMV kernel for M <= 2 (tile_m = M,
-                               tile_n = 4 rows of B per warp, tile_k = 1024) */
-    int pair_cluster;       /* pair kernel: pairs per thread-block cluster (1, or
-                               2 = two pairs on adjacent tiles share their A
-                               panel by TMA multicast); ctas is then an upper
-                               bound: the launch uses at most as many clusters
-                               as the GPU can hold at once */
+    int pair;               /* 1: CTA-pair kernel (256 x 256 tiles over two SMs) */
+    int ctas;               /* pair kernel: CTAs launched (persistent) */
+    int waves;              /* pair kernel: most tiles one CTA pair computes */
 } mxfp4_plan;
 
 /*
@@ -97,34 +88,19 @@ typedef struct mxfp4_plan {
  * CTA-pair kernel (256 x 256 tiles over two SMs) when those tiles fill every
  * SM pair at least once; else no split when the tiles fill at least half a
  * wave, or enough splits to fill the SMs with at least 8 K stages each.
- * 1..16 forces that many splits (clamped to the number of K blocks).  The environment variable MXFP4_KERNEL, read at
- * each call, overrides the kernel for split_k = 0 (tuning and tests only):
- * "persistent" = persistent stream-K kernel, "pair" = CTA-pair kernel for
- * M, N >= 256 without swap, "gemv" = CUDA-core GEMV kernel for M <= 2 and
- * N >= 4 * SMs.  Pair-kernel variants, also read at each call (all tested
- * for parity; the defaults measured fastest on GB300): MXFP4_PAIR_N = 192
- * uses 256 x 192 tiles with two TMEM accumulators (the next tile's MMAs
- * overlap the previous tile's drain; default 256, one accumulator);
- * MXFP4_PAIR_CLUSTER = 2 puts two pairs on adjacent tiles in one cluster that
- * share their A panel by TMA multicast (default 1); MXFP4_PAIR_KS = 512 uses
- * three 512-K pipeline stages instead of six 256-K ones.
- * MXFP4_SPLIT_REDUCE = cluster (any kernel choice, splits 2..8): the splits
- * of a tile form one thread-block cluster and sum their fp32 partials
- * through distributed shared memory in split order (bit-identical to the
- * default two-launch form, no workspace); the default writes partials to
- * the workspace and reduces them in a second, dependent launch, which
- * measured faster.  num_sms = 0
- * uses the current device's SM count (or 152 when no device is visible).
- * Pure host logic: no GPU work.  Returns MXFP4_OK or MXFP4_ERR_INVALID_ARG.
+ * 1..16 forces that many splits (clamped to the number of K blocks) on the
+ * one-tile kernel.  num_sms = 0 uses the current device's SM count (or 152
+ * when no device is visible).  Pure host logic: no GPU work.  Returns
+ * MXFP4_OK or MXFP4_ERR_INVALID_ARG.
  */
 int mxfp4_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *out);
 
 /*
- * Bytes of device workspace mxfp4_gemm needs: the fp32 partial sums
- * [split, M, N] when the plan splits K, plus both relaid scale buffers when
- * the plan has a relayout pass; 0 when neither applies (then the workspace
- * may be NULL).  Returns 0 for invalid sizes too (mxfp4_plan_gemm tells them
- * apart).
+ * Bytes of device workspace mxfp4_gemm needs: when the plan splits K, one
+ * 8-byte counter per output tile and one fp32 partial tile per (tile, split);
+ * plus both relaid scale buffers when the plan has a relayout pass; 0 when
+ * neither applies (then the workspace may be NULL).  Returns 0 for invalid
+ * sizes too (mxfp4_plan_gemm tells them apart).
  */
 size_t mxfp4_gemm_workspace_size(int M, int N, int K, int split_k);
 
@@ -169,20 +145,49 @@ int mxfp4_scale_relayout2(void *dst_a, const void *src_a, int rows_a, int64_t ld
  *   scaleA  uint8 [M, ld_sa]        ld_sa >= K/32
  *   scaleB  uint8 [N, ld_sb]        ld_sb >= K/32
  *   M, N >= 1; K >= 32, K % 32 == 0 (the scale block).  A, B 16-byte aligned.
- *   split_k  0 = heuristic, else 1..16.  Splits reduce in fp32 in a fixed
- *            order, so results are bitwise reproducible run to run.
+ *   split_k  0 = heuristic, else 1..16.  Each split parks an fp32 partial
+ *            tile in the workspace; the CTA that finishes a tile last sums
+ *            its partials in split order 0, 1, ... (whichever split finished
+ *            last), so results are bitwise reproducible run to run.
  *   workspace  device, >= mxfp4_gemm_workspace_size(M, N, K, split_k) bytes,
- *              256-byte aligned, contents need not be initialised; NULL when
- *              that size is 0.
+ *              256-byte aligned, contents need not be initialised (counters
+ *              carry a per-call tag and are reset by the call that completes
+ *              them); NULL when that size is 0.  Calls that may run at the
+ *              same time need workspaces of their own.  After a call stopped
+ *              on MXFP4_ERR_TIMEOUT, re-capture graphs that hold split-K
+ *              calls on the same workspace (a replay repeats the tag).
  * The scales are read row-major.  Compute-bound shapes (plan.relayout_pass)
  * first relay them out into the workspace with the relayout kernel; the
  * others build the tcgen05 scale layout inside the GEMM itself.
+ * Every kernel is launched as a programmatic dependent of the work already on
+ * `stream`: it may start while that work drains (its set-up overlaps the
+ * other kernel's tail) and waits for it in-kernel before reading any input or
+ * writing any output, so ordering on the stream is as for plain launches.
  */
 int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                const void *A, int64_t lda, const void *B, int64_t ldb,
                const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,
                float alpha, float beta, int M, int N, int K, int split_k,
                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mxfp4_gemm with flags.  MXFP4_FLAG_B_STATIC: the caller guarantees that the
+ * work enqueued on `stream` before this call does not write B or scaleB (for
+ * example weights that stay fixed across a decode loop).  The GEMM then
+ * prefetches its share of B and of scaleB into L2 before waiting for that
+ * work, so the weight stream of one call overlaps the tail of the kernel
+ * before it; A, C and D are still touched only after that work has finished.
+ * The flag has no effect on plans with a relayout pass (their B scales come
+ * from this call's own relayout).  Other arguments and results as for
+ * mxfp4_gemm (bit-identical output); unknown flag bits: MXFP4_ERR_INVALID_ARG.
+ */
+#define MXFP4_FLAG_B_STATIC 1u
+
+int mxfp4_gemm_ex(void *D, int64_t ldd, const void *C, int64_t ldc,
+                  const void *A, int64_t lda, const void *B, int64_t ldb,
+                  const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,
+                  float alpha, float beta, int M, int N, int K, int split_k, unsigned flags,
+                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * MXFP8 / MXFP6 form of mxfp4_gemm: D[M,N] = alpha * A[M,K] . B[N,K]^T +
@@ -303,15 +308,19 @@ size_t mxfp8_gemm_host_arena_size(int M, int N, int K, int split_k, int with_c);
  * counterpart: it exists for users whose allocator is owned by someone else
  * or who may not synchronise the device through a cudaMalloc mid-run).  Same
  * arguments and results as mxfp4_gemm minus the workspace: the scratch (relaid
- * scales, split-K / stream-K partials) lives in one array of MXFP4_NOALLOC_SCRATCH_BYTES
- * inside the library's device image, held by every GPU that loads the library
- * until exit.  Shapes whose mxfp4_gemm_workspace_size exceeds it are rejected
- * with MXFP4_ERR_WORKSPACE before anything is enqueued.  The first call on a
- * device looks up the array's device address (a runtime query); make that
- * first call before capturing the stream into a graph.  All calls share the
- * array: calls that overlap on the GPU race on it and must be serialised by
- * the caller.  Each call rewrites all the scratch it reads, so leftovers from
- * the previous call never leak into a result.
+ * scales, split-K tile counters and partials) lives in one array of
+ * MXFP4_NOALLOC_SCRATCH_BYTES inside the library's device image, held by
+ * every GPU that loads the library until exit.  Shapes whose
+ * mxfp4_gemm_workspace_size exceeds it are rejected with MXFP4_ERR_WORKSPACE
+ * before anything is enqueued.  `stream` must belong to the current device
+ * (MXFP4_ERR_INVALID_ARG otherwise), whose copy of the array is used.  The
+ * first call on a device looks up the array's device address (a runtime
+ * query); make that first call before capturing the stream into a graph.  All
+ * calls share the array: calls that overlap on the GPU race on it and must be
+ * serialised by the caller.  Nothing needs clearing between calls: each call
+ * rewrites the relaid scales and partials before it reads them, and the tile
+ * counters carry a per-call tag, so a counter left by an earlier call reads as
+ * zero.
  */
 #define MXFP4_NOALLOC_SCRATCH_BYTES (32u << 20)
 
@@ -378,17 +387,6 @@ int mxfp4_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, in
  */
 int mxfp8_quantize(void *Q, int64_t ldq, void *S, int64_t lds, const void *X, int64_t ldx,
                    int rows, int K, int fmt, void *stream);
-
-/*
- * Measurement hook: reads `bytes` (rounded down to a multiple of 16) of the
- * device buffer `src` (16-byte aligned) once with 16-byte loads from every
- * SM, several in flight per thread -- the time a single streaming pass over
- * that much data takes on this GPU, the floor for the GEMM's bandwidth-bound
- * shapes.  `sink` is a device word the kernel may write (practically never).
- * The pages have no counterpart.  Returns MXFP4_OK, MXFP4_ERR_INVALID_ARG
- * (null pointer or bytes < 16), MXFP4_ERR_MISALIGNED or a device error.
- */
-int mxfp4_stream_read_probe(const void *src, size_t bytes, void *sink, void *stream);
 
 /* Set the in-kernel wait limit in SM clock cycles (default 2^32, ~2 s). */
 void mxfp4_set_wait_limit(long long cycles);

@@ -1,11 +1,12 @@
 """Shared helpers of the GPU parity tests: device upload, C-ABI calls and the
 element-wise bound against the oracle.
 
-Bound (per output element, stated by the target):
-    |D_gpu - D_ref| <= ulp_bf16(D_ref) + 2^-20 * max(1, |alpha|) * sum_k |a_k b_k|
-with ulp_bf16(x) = 2^(max(floor(log2|x|), -126) - 7) and ulp_bf16(0) = 2^-133.
-The first term is one bf16 rounding of the output; the second covers fp32
-accumulation order inside the tensor cores and the split-K partial sums.
+Bound (per output element, as the target states it):
+    |D_gpu - D_ref| <= ulp_bf16(D_ref) + 2^-20 * sum_k |a_k b_k|
+with ulp_bf16(x) = 2^(max(floor(log2|x|), -126) - 7) and ulp_bf16(0) = 2^-133,
+and a_k, b_k the scaled inputs.  The first term is one bf16 rounding of the
+output; the second covers fp32 accumulation order inside the tensor cores
+and the split-K partial sums.  alpha does not enter it.
 """
 import numpy as np
 
@@ -25,17 +26,17 @@ def ulp_bf16(x):
     return np.where(a == 0, 2.0 ** -133, u)
 
 
-def error_ratio(d_gpu_bits, d_ref_bits, sabs, alpha):
+def error_ratio(d_gpu_bits, d_ref_bits, sabs, alpha=None):
     g = bf16_bits_to_f64(d_gpu_bits)
     r = bf16_bits_to_f64(d_ref_bits)
-    bound = ulp_bf16(r) + 2.0 ** -20 * max(1.0, abs(alpha)) * np.asarray(sabs)
+    bound = ulp_bf16(r) + 2.0 ** -20 * np.asarray(sabs)
     err = np.abs(g - r)
     ratio = err / bound
     ratio[np.isnan(g) | np.isnan(r)] = np.inf
     return ratio
 
 
-def assert_within_bound(d_gpu_bits, d_ref_bits, sabs, alpha, what=""):
+def assert_within_bound(d_gpu_bits, d_ref_bits, sabs, alpha=None, what=""):
     ratio = error_ratio(d_gpu_bits, d_ref_bits, sabs, alpha)
     worst = float(ratio.max()) if ratio.size else 0.0
     if not worst <= 1.0:

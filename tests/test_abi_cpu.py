@@ -44,6 +44,19 @@ def test_version_and_strerror(L):
     assert mx.mxfp4_strerror(-99) == "unknown status"
 
 
+def _a256(x):
+    return -(-x // 256) * 256
+
+
+def splitk_ws(tiles, split, part_cols):
+    """Split-K workspace: one 8-byte counter per tile, then one 128-row fp32
+    partial slot of part_cols columns per (tile, split), each part 256-byte
+    aligned; nothing without a split."""
+    if split <= 1:
+        return 0
+    return _a256(tiles * 8) + _a256(tiles * split * 128 * part_cols * 4)
+
+
 WORKLOADS = {"tiny": (128, 256, 512), "decode": (1, 8192, 8192), "mid": (512, 1024, 2048),
              "large": (8192, 8192, 8192), "skinny": (64, 7168, 16384)}
 
@@ -69,115 +82,52 @@ def test_plan_invariants(L, name):
                 assert -(-M // 256) * -(-N // 256) >= 76
                 assert (p.tile_m, p.tile_n, p.split_k, p.ctas) == (256, 256, 1, 152)
                 continue
-            assert p.persistent == 0
             want = 1 if 2 * tiles >= slots else max(1, min(slots // tiles, kt // 8, 16, kt))
             per = -(-kt // want)
             assert p.split_k == -(-kt // per)
             assert p.grid_z == p.split_k
             continue
-        assert p.persistent == 0 and p.split_k <= split
+        assert p.split_k <= split
         assert p.grid_x == -(-P // 128) and p.grid_y == -(-Q // p.tile_n)
         assert p.grid_z == p.split_k
-        want_ws = 0 if p.split_k == 1 else 4096 + p.split_k * M * N * 4
-        assert p.workspace_bytes >= want_ws
-    # Skinny M swaps (the GEMV form has no swap); large uses the pair kernel.
+        assert p.workspace_bytes == splitk_ws(tiles, p.split_k, min(Q, p.tile_n))
+    # Skinny M swaps; large uses the pair kernel.
     p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
     assert p.swap_ab == (1 if M <= 64 else 0)
     if name == "large":
         assert (p.pair, p.tile_m, p.tile_n, p.split_k) == (1, 256, 256, 1)
     else:
         assert p.pair == 0
-    assert p.gemv == 0
     if name in ("decode", "skinny"):
         assert p.split_k == {"decode": 4, "skinny": 5}[name]
 
 
-@pytest.mark.parametrize("name", sorted(WORKLOADS))
-def test_plan_invariants_persistent_override(L, name, monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "persistent")
-    M, N, K = WORKLOADS[name]
-    p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
-    kt = -(-K // p.tile_k)
-    P, Q = (N, M) if p.swap_ab else (M, N)
-    tiles = -(-P // 128) * -(-Q // p.tile_n)
-    # Persistent stream-K: every tile either whole (dp waves) or in the
-    # shared K-stage pool; at most one CTA per resident slot.
-    assert p.persistent == 1 and p.split_k == 1 and p.pair == 0
-    assert (p.grid_x, p.grid_y, p.grid_z) == (p.ctas, 1, 1)
-    slots = 152 * (2 if p.swap_ab else 1)
-    assert 1 <= p.ctas <= slots
-    assert p.dp_waves * p.ctas + p.sk_units // kt == tiles
-    assert p.sk_units % kt == 0
-    if p.sk_units:
-        assert p.workspace_bytes >= 4096 + p.ctas * min(Q, p.tile_n) * 128 * 4
-    if name == "large":
-        assert (p.tile_n, p.dp_waves, p.ctas) == (256, 13, 152)
-    # An explicit split ignores the override.
-    assert mx.mxfp4_plan_gemm(M, N, K, 1, 152).persistent == 0
-    assert mx.mxfp4_plan_gemm(M, N, K, 1, 152).pair == 0
+def test_plan_ignores_the_environment(L, monkeypatch):
+    """The plan is a function of the shape alone: the variables that once
+    switched kernels for tuning have no effect."""
+    shapes = [(8192, 8192, 8192), (1, 8192, 8192), (64, 7168, 16384), (512, 1024, 2048)]
+    before = [mx.mxfp4_plan_gemm(*s, 0, 152).as_dict() for s in shapes]
+    for var, val in [("MXFP4_KERNEL", "persistent"), ("MXFP4_KERNEL", "gemv"),
+                     ("MXFP4_PAIR_N", "192"), ("MXFP4_PAIR_CLUSTER", "2"),
+                     ("MXFP4_PAIR_KS", "512"), ("MXFP4_SPLIT_REDUCE", "cluster"),
+                     ("MXFP4_TILE", "128:6")]:
+        monkeypatch.setenv(var, val)
+    assert [mx.mxfp4_plan_gemm(*s, 0, 152).as_dict() for s in shapes] == before
 
 
-def test_plan_pair_override(L, monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert p.pair == 1 and (p.tile_m, p.tile_n) == (256, 256) and p.ctas == 152
-    assert p.relayout_pass == 1 and p.workspace_bytes == 0
-    # Shapes the pair kernel does not take stay on the automatic path.
-    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152).pair == 0
-    assert mx.mxfp4_plan_gemm(128, 8192, 8192, 0, 152).pair == 0
-
-
-def test_plan_cluster_split_reduce(L, monkeypatch):
-    # MXFP4_SPLIT_REDUCE=cluster: up to 8 splits reduce inside each tile's
-    # cluster and need no partials; 16 still do.
-    monkeypatch.setenv("MXFP4_SPLIT_REDUCE", "cluster")
-    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 0
-    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152).workspace_bytes == 0
-    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 16) == 4096 + 16 * 8192 * 4
-    assert mx.mxfp8_gemm_workspace_size(1, 8192, 8192, 4) == 0
-
-
-def test_plan_pair_tile_n_192(L, monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    monkeypatch.setenv("MXFP4_PAIR_N", "192")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert p.pair == 1 and (p.tile_m, p.tile_n, p.stages) == (256, 192, 7)
-    # 32 x 43 tiles over 76 pairs: 19 tiles per pair at most.
-    assert p.dp_waves == (32 * 43 + 75) // 76 and p.ctas == 152
-    # Any other value keeps 256-column tiles.
-    monkeypatch.setenv("MXFP4_PAIR_N", "224")
-    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).tile_n == 256
-
-
-def test_plan_pair_cluster(L, monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert p.pair_cluster == 1
-    monkeypatch.setenv("MXFP4_PAIR_CLUSTER", "2")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    # 32 x 16 tile groups (two adjacent 256-column tiles each) over 38 clusters.
-    assert p.pair_cluster == 2 and p.ctas == 152 and p.dp_waves == (512 + 37) // 38
-    # One tile column: nothing to share.
-    assert mx.mxfp4_plan_gemm(1024, 256, 1024, 0, 152).pair_cluster == 1
-    # Only 256-column tiles are compiled in clusters of two pairs.
-    monkeypatch.setenv("MXFP4_PAIR_N", "192")
-    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).pair_cluster == 1
-    # Other kernels report no cluster.
-    monkeypatch.setenv("MXFP4_KERNEL", "persistent")
-    assert mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152).pair_cluster == 0
-
-
-def test_plan_pair_stage_k(L, monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert (p.tile_k, p.stages) == (256, 6)
-    monkeypatch.setenv("MXFP4_PAIR_KS", "512")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert (p.tile_k, p.stages) == (512, 3)
-    # 192-column tiles keep 256-K stages.
-    monkeypatch.setenv("MXFP4_PAIR_N", "192")
-    p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert (p.tile_k, p.stages) == (256, 7)
+def test_no_multicast_loads_in_the_library():
+    """No TMA load with cluster multicast anywhere in the library sources
+    (the pair kernel's commit may arrive on both CTAs' barriers)."""
+    import glob
+    import re
+    csrc = os.path.join(os.path.dirname(mx.library_path()), "csrc")
+    for path in glob.glob(os.path.join(csrc, "*")):
+        text = open(path).read()
+        for m in re.finditer(r"multicast::cluster", text):
+            line = text[text.rfind("\n", 0, m.start()) + 1:text.find("\n", m.start())]
+            assert "tcgen05.commit" in line, (path, line)
+        assert "cp.async.bulk.tensor" not in text or \
+            not re.search(r"cp\.async\.bulk\.tensor[^;\"]*multicast", text), path
 
 
 def test_plan_heuristic_prefers_fewer_waves(L):
@@ -199,15 +149,19 @@ def test_sizes(L):
     assert mx.mxfp4_scale_relayout_size(5, 48) == 0
     assert mx.mxfp4_gemm_workspace_size(0, 1, 32, 0) == 0
     assert mx.mxfp4_gemm_workspace_size(1, 1, 32, 17) == 0
-    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 4096 + 4 * 8192 * 4
-    # The decode shape splits K four ways: partials [4, 1, 8192] in fp32.
+    # The decode shape splits K four ways over 64 tiles of 128 rows of B:
+    # 64 counters and 4 x 64 partial slots of 128 rows x 1 column (M = 1).
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 512 + 4 * 64 * 128 * 4
     p = mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152)
-    assert p.split_k == 4 and p.workspace_bytes == 4096 + 4 * 8192 * 4
+    assert p.split_k == 4 and p.workspace_bytes == 512 + 4 * 64 * 128 * 4
+    # Skinny: 56 tiles, 5 splits, 64 columns each.
+    p = mx.mxfp4_plan_gemm(64, 7168, 16384, 0, 152)
+    assert p.split_k == 5 and p.workspace_bytes == 512 + 56 * 5 * 128 * 64 * 4
     # The large shape relays its scales out first: workspace = both relaid buffers.
     p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 0)
     assert p.relayout_pass == 1
     assert mx.mxfp4_gemm_workspace_size(8192, 8192, 8192, 1) == \
-        4096 + 2 * mx.mxfp4_scale_relayout_size(8192, 8192)
+        2 * mx.mxfp4_scale_relayout_size(8192, 8192)
     assert mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 0).relayout_pass == 0
     assert mx.mxfp4_gemm_workspace_size(128, 256, 512, 1) == 0
     assert mx.mxfp4_gemm_host_arena_size(8192, 8192, 8192, 1, False) > 0
@@ -233,7 +187,7 @@ def _call_gemm(L, **kw):
     (dict(beta=1.0), -1), (dict(beta=1.0, C=0x6000, ldc=100), -1),
     (dict(split=17), -1), (dict(split=-1), -1),
     (dict(lda=528), -3), (dict(ldb=520), -3), (dict(A=0x2008), -3), (dict(B=0x3004), -3),
-    # Splits beyond 8 keep fp32 partials in the workspace (K = 4096: 16 stages).
+    # Split K keeps fp32 partials in the workspace (K = 4096: 16 stages).
     (dict(ws=None, split=16, K=4096, lda=4096, ldb=4096, ld_sa=128, ld_sb=128), -4),
     (dict(ws=0x10010), -3),
     (dict(wsb=1000, split=16, K=4096, lda=4096, ldb=4096, ld_sa=128, ld_sb=128), -4),
@@ -302,22 +256,22 @@ def test_mxfp8_quantize_validates_before_device(L):
 
 def test_mxfp8_plan(L):
     p = mx.mxfp8_plan_gemm(8192, 8192, 8192, 0, 152)
-    assert (p.tile_m, p.tile_n, p.tile_k, p.stages, p.pair, p.persistent) == (128, 256, 128, 4, 0, 0)
+    assert (p.tile_m, p.tile_n, p.tile_k, p.stages, p.pair) == (128, 256, 128, 4, 0)
     assert p.relayout_pass == 1
     # The plan of an fp4 GEMM whose rows hold as many bytes (K doubled).
     for M, N, K in [(1, 8192, 8192), (64, 7168, 16384), (512, 1024, 2048), (300, 520, 1024)]:
         a = mx.mxfp8_plan_gemm(M, N, K, 0, 152).as_dict()
         monkey = mx.mxfp4_plan_gemm(M, N, 2 * K, 0, 152).as_dict()
         a.pop("tile_k"), monkey.pop("tile_k")
-        if not monkey["pair"] and not monkey["persistent"]:
+        if not monkey["pair"]:
             assert a == monkey, (M, N, K)
-    # The kernel overrides do not apply to MXFP8.
+    # The pair kernel is MXFP4-only.
     assert mx.mxfp8_plan_gemm(8192, 8192, 8192, 0, 152).pair == 0
     with pytest.raises(mx.Mxfp4Error):
         mx.mxfp8_plan_gemm(128, 256, 48, 0, 152)
     assert mx.mxfp8_gemm_workspace_size(128, 256, 512, 1) == 0
     assert mx.mxfp8_gemm_workspace_size(8192, 8192, 8192, 0) == \
-        4096 + 2 * mx.mxfp4_scale_relayout_size(8192, 8192)
+        2 * mx.mxfp4_scale_relayout_size(8192, 8192)
 
 
 def test_other_entry_points_validate_before_device(L):
@@ -325,9 +279,12 @@ def test_other_entry_points_validate_before_device(L):
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 48, 2, None) == -1
     assert L.mxfp4_scale_relayout(0x1000, 0x2000, 4, 64, 1, None) == -1
     assert L.mxfp4_scale_relayout(0x1008, 0x2000, 4, 64, 2, None) == -3
-    assert L.mxfp4_stream_read_probe(None, 64, 0x1000, None) == -1
-    assert L.mxfp4_stream_read_probe(0x1000, 8, 0x2000, None) == -1
-    assert L.mxfp4_stream_read_probe(0x1008, 64, 0x2000, None) == -3
+    ex = L.mxfp4_gemm_ex
+    good = (0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, 0x4000, 16, 0x5000, 16, 1.0, 0.0,
+            128, 256, 512, 0)
+    assert ex(*good, 2, 0x10000, 1 << 30, None) == -1          # unknown flag bit
+    assert ex(*good, 0x80000000, 0x10000, 1 << 30, None) == -1
+    assert ex(None, *good[1:], 1, 0x10000, 1 << 30, None) == -1
     qz = L.mxfp4_quantize
     assert qz(None, 64, 0x2000, 2, 0x3000, 64, 4, 64, None) == -1
     assert qz(0x1000, 64, 0x2000, 2, 0x3000, 64, 4, 48, None) == -1      # K % 32
@@ -372,20 +329,6 @@ def test_no_device_reports_cuda_error_not_crash(L):
             pytest.skip("a GPU is visible")
     st = ctypes.c_int(123)
     assert L.mxfp4_device_status(ctypes.byref(st), 0) in (-5, -7)
-
-
-def test_plan_gemv_override(L, monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "gemv")
-    for M, N, K in ((1, 8192, 8192), (2, 4096, 1056), (1, 608, 32)):
-        p = mx.mxfp4_plan_gemm(M, N, K, 0, 152)
-        # CUDA-core GEMV: 4 rows of B per warp, one launch over the whole K.
-        assert p.gemv == 1 and (p.tile_m, p.tile_n, p.tile_k, p.split_k) == (M, 4, 1024, 1)
-        assert p.workspace_bytes == 0 and p.relayout_pass == 0 and p.pair == 0
-        assert p.k_tiles_per_split == -(-K // 1024) and p.grid_x == p.ctas >= 1
-    # Shapes it does not take stay on the tensor-core path.
-    assert mx.mxfp4_plan_gemm(3, 8192, 8192, 0, 152).gemv == 0
-    assert mx.mxfp4_plan_gemm(1, 600, 8192, 0, 152).gemv == 0
-    assert mx.mxfp4_plan_gemm(1, 8192, 8192, 2, 152).gemv == 0
 
 
 def test_plan_respects_the_grid_limit():

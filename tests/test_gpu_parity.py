@@ -276,21 +276,6 @@ def test_strides_and_in_place(oracle_mod):
     assert np.all(d_to_bits(DC[:, N:]) == 0)
 
 
-@pytest.mark.parametrize("name,split", [("decode", 2), ("decode", 4), ("decode", 8),
-                                        ("skinny", 5), ("mid", 2)])
-def test_cluster_split_reduce_matches_reduce_kernel(monkeypatch, name, split):
-    """MXFP4_SPLIT_REDUCE=cluster: the splits of a tile sum through
-    distributed shared memory in the reduce kernel's order, so D is
-    bit-identical to the two-launch form (whose parity the sweeps check)."""
-    p = problem(name)
-    dev = Dev(p)
-    ref = run_gemm(dev, split_k=split)
-    monkeypatch.setenv("MXFP4_SPLIT_REDUCE", "cluster")
-    assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, split, 0).workspace_bytes == 0
-    got = run_gemm(dev, split_k=split)
-    assert np.array_equal(got, ref)
-
-
 def test_split_k_is_deterministic():
     p = problem("decode") if "decode" in _PROBLEMS else inputs.workload("decode")
     dev = Dev(p)
@@ -424,70 +409,58 @@ def test_bounded_wait_times_out_cleanly():
 
 
 # ------------------------------------------------------ CTA-pair kernel --
+# The heuristic runs the CTA-pair kernel when the 256 x 256 tiles fill every
+# SM pair at least once (76 tiles on 152 SMs): these shapes have 81 or more.
 
-@pytest.fixture(params=[(256, 1, 256), (192, 1, 256), (256, 2, 256), (256, 1, 512), (256, 2, 512)],
-                ids=["n256", "n192", "n256c2", "n256k512", "n256c2k512"])
-def force_pair(monkeypatch, request):
-    """The CTA-pair kernel with 256-wide tiles (one accumulator), with
-    192-wide tiles (two accumulators, five scale slots; tiles start 0 or 64
-    rows into a 128-row scale block), with 256-wide tiles in clusters of two
-    pairs that share A by TMA multicast (an odd tile-column count leaves the
-    second pair of the last column group a tile past the edge), and with
-    512-K pipeline stages (an odd number of 256-K chunks leaves the last
-    stage half full)."""
-    tile_n, cluster, ks = request.param
-    monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    monkeypatch.setenv("MXFP4_PAIR_N", str(tile_n))
-    monkeypatch.setenv("MXFP4_PAIR_CLUSTER", str(cluster))
-    monkeypatch.setenv("MXFP4_PAIR_KS", str(ks))
-    yield tile_n
+PAIR_SHAPES = [(2304, 2304, 512), (2300, 2100, 288), (2560, 2048, 1280), (2304, 2560, 1024)]
 
 
-@pytest.mark.parametrize("M,N", [(256, 256), (512, 512)])
-def test_pair_kernel_single_scale_probes(force_pair, M, N):
+@pytest.mark.parametrize("which", ["A", "B"])
+def test_pair_kernel_single_scale_probes(which):
     """Scale placement through the two-SM MMA: each CTA's scale-A rows and the
     full scale-B must reach the right accumulator rows / columns."""
-    plan = mx.mxfp4_plan_gemm(M, N, 512, 0, 0)
-    assert plan.pair == 1 and plan.tile_n == force_pair
+    M = N = 2304
     K = 512
+    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).pair == 1
+    rows = [0, 31, 127, 128, 200, 255, 256, 1000, M - 1]
     bad = []
-    for which, rows in (("A", [0, 31, 127, 128, 200, M - 1]), ("B", [0, 64, 127, 128, 255, N - 1])):
-        for r in rows:
-            for kb in (0, 3, 8, 15):
-                p = _ones_problem(M, N, K)
-                (p.SA if which == "A" else p.SB)[r, kb] = 128
-                D = bf16_bits_to_f64(run_gemm(Dev(p)))
-                want = np.full((M, N), float(K))
-                if which == "A":
-                    want[r, :] += 32
-                else:
-                    want[:, r] += 32
-                if not np.array_equal(D, want):
-                    wrong = np.argwhere(D != want)
-                    bad.append((which, r, kb, len(wrong), wrong[:4].tolist(), D[tuple(wrong[0])]))
+    for r in rows:
+        for kb in (0, 3, 8, 15):
+            p = _ones_problem(M, N, K)
+            (p.SA if which == "A" else p.SB)[r, kb] = 128
+            D = bf16_bits_to_f64(run_gemm(Dev(p)))
+            want = np.full((M, N), float(K))
+            if which == "A":
+                want[r, :] += 32
+            else:
+                want[:, r] += 32
+            if not np.array_equal(D, want):
+                wrong = np.argwhere(D != want)
+                bad.append((which, r, kb, len(wrong), wrong[:4].tolist(), D[tuple(wrong[0])]))
     assert not bad, bad
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 520, 1024), (1000, 700, 288),
-                                   (512, 1024, 2048), (520, 768, 1280)])
-def test_pair_kernel_parity(force_pair, oracle_mod, M, N, K):
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+def test_pair_kernel_parity(oracle_mod, M, N, K):
+    """Full comparison, ragged M / N (tiles past the edge), K with a partial
+    last stage, alpha / beta with C."""
     p = inputs.make_problem("pair", M, N, K, seed=M + N + K, values="codes", alpha=0.5,
                             beta=1.0, c_sigma=1.0)
     plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
-    assert plan.pair == 1 and plan.tile_n == force_pair
+    assert plan.pair == 1 and plan.tile_n == 256
     Dref, sabs = full_oracle(oracle_mod, p)
     assert_within_bound(run_gemm(Dev(p)), Dref, sabs, p.alpha, f"pair {M}x{N}x{K}")
 
 
-def test_pair_kernel_many_tiles_sampled(force_pair, oracle_mod):
-    """More tile groups than resident clusters (several tiles per pair, the
+def test_pair_kernel_many_tiles_sampled(oracle_mod):
+    """More tiles than resident pairs (several tiles per pair, the
     accumulator reused), ragged in M and N, checked on sampled outputs."""
     M, N, K = 4400, 4700, 1024
     p = inputs.make_problem("pair_many", M, N, K, seed=17, values="codes", alpha=1.0, beta=0.5,
                             c_sigma=1.0)
     plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
-    assert plan.pair == 1 and plan.tile_n == force_pair
-    pairs = sample_pairs(M, N, 3000, 5, tile_m=256, tile_n=force_pair)
+    assert plan.pair == 1 and plan.waves > 1
+    pairs = sample_pairs(M, N, 3000, 5, tile_m=256, tile_n=256)
     Dr, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs,
                                                    alpha=p.alpha, beta=p.beta, C=p.C)
     assert inexact == 0
@@ -496,98 +469,12 @@ def test_pair_kernel_many_tiles_sampled(force_pair, oracle_mod):
     assert not np.isnan(bf16_bits_to_f64(D)).any()
 
 
-# ---------------------------------------------- persistent stream-K kernel --
-
-@pytest.fixture
-def force_persistent(monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "persistent")
-    yield
-
-
-@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (512, 1024, 2048), (1, 4096, 2048),
-                                   (64, 3072, 8192), (63, 200, 288), (129, 520, 1024),
-                                   (2000, 2600, 288), (257, 300, 384)])
-def test_persistent_kernel_parity(force_persistent, oracle_mod, M, N, K):
-    """Whole tiles and stream-K shares of tiles (partials, epoch flags and the
-    fix-up) against the oracle, with and without swap."""
-    p = inputs.make_problem("sk", M, N, K, seed=3 * M + N + K, values="codes", alpha=0.5,
-                            beta=1.0, c_sigma=1.0)
-    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).persistent == 1
-    Dref, sabs = full_oracle(oracle_mod, p)
-    dev = Dev(p)
-    first = run_gemm(dev)
-    assert_within_bound(first, Dref, sabs, p.alpha, f"persistent {M}x{N}x{K}")
-    # A second call reuses the workspace (flags of the earlier epoch).
-    assert np.array_equal(run_gemm(dev), first)
-
-
-# ------------------------------------------------ GEMV kernel (M <= 2) --
-
-GEMV_SHAPES = [(1, 8192, 8192), (2, 8190, 1056), (1, 610, 96), (2, 4096, 4128), (1, 4099, 32)]
-
-
-@pytest.fixture
-def force_gemv(monkeypatch):
-    monkeypatch.setenv("MXFP4_KERNEL", "gemv")
-    yield
-
-
-@pytest.mark.parametrize("M,N,K", GEMV_SHAPES)
-def test_gemv_parity(force_gemv, oracle_mod, M, N, K):
-    """The CUDA-core GEMV form (automatic split, M <= 2): ragged N (not a
-    multiple of the 4 rows a warp takes), K tails that are not a multiple of
-    the 1024-element chunk, alpha/beta with C; run-to-run identical; the
-    prepacked entry point (relaid scales) gives the same bits."""
-    p = inputs.make_problem("gemv", M, N, K, seed=M * 7 + N + K, values="codes", alpha=0.5,
-                            beta=1.0, c_sigma=1.0)
-    plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
-    assert plan.gemv == 1 and plan.workspace_bytes == 0
-    Dref, sabs = full_oracle(oracle_mod, p)
-    dev = Dev(p)
-    got = run_gemm(dev)
-    assert_within_bound(got, Dref, sabs, p.alpha, f"gemv {M}x{N}x{K}")
-    assert np.array_equal(run_gemm(dev), got)
-    sfa = torch.empty(mx.mxfp4_scale_relayout_size(M, K), dtype=torch.uint8, device="cuda")
-    sfb = torch.empty(mx.mxfp4_scale_relayout_size(N, K), dtype=torch.uint8, device="cuda")
-    mx.mxfp4_scale_relayout(sfa, dev.SA, M, K, K // 32)
-    mx.mxfp4_scale_relayout(sfb, dev.SB, N, K, K // 32)
-    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    mx.mxfp4_gemm_prepacked(D, N, dev.C, N, dev.A, K, dev.B, K, sfa, sfb, p.alpha, p.beta,
-                            M, N, K, 0, None, 0)
-    torch.cuda.synchronize()
-    assert np.array_equal(d_to_bits(D), got)
-
-
-def test_gemv_strided_operands(force_gemv, oracle_mod):
-    """Row strides larger than the data (A, B, scales, C, D) through the GEMV."""
-    M, N, K = 2, 1200, 640
-    p = inputs.make_problem("gemv-ld", M, N, K, seed=77, values="normal", alpha=1.0, beta=-0.5,
-                            c_sigma=1.0)
-    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).gemv == 1
-    Dref, sabs = full_oracle(oracle_mod, p)
-    pad = lambda a, extra: np.ascontiguousarray(np.pad(a, ((0, 0), (0, extra))))
-    d = lambda a: torch.from_numpy(a).cuda()
-    A, B = d(pad(p.A, 16)), d(pad(p.B, 48))                 # +32 / +96 K elements
-    SA, SB = d(pad(p.SA, 5)), d(pad(p.SB, 3))
-    C = d(pad(p.C.view(np.int16), 8)).view(torch.bfloat16)
-    D = torch.full((M, N + 24), float("nan"), dtype=torch.bfloat16, device="cuda")
-    mx.mxfp4_gemm(D, N + 24, C, N + 8, A, (K // 2 + 16) * 2, B, (K // 2 + 48) * 2, SA,
-                  K // 32 + 5, SB, K // 32 + 3, p.alpha, p.beta, M, N, K, 0, None, 0)
-    torch.cuda.synchronize()
-    got = d_to_bits(D[:, :N].contiguous())
-    assert_within_bound(got, Dref, sabs, p.alpha, "gemv strided")
-    assert torch.isnan(D[:, N:].float()).all()                # padding untouched
-
-
 # ------------------------------------------------------ split-K reduce --
 
-@pytest.mark.parametrize("split,mode", [(2, "kernel"), (10, "kernel"), (2, "cluster")])
-def test_splitk_for_large_grids(oracle_mod, monkeypatch, split, mode):
-    """A wide grid (over 1000 output tiles), its splits reduced by the
-    fixed-order reduce kernel or inside each tile's cluster; every tile
-    completes (same bound, sampled)."""
-    if mode == "cluster":
-        monkeypatch.setenv("MXFP4_SPLIT_REDUCE", "cluster")
+@pytest.mark.parametrize("split", [2, 10])
+def test_splitk_for_large_grids(oracle_mod, split):
+    """A wide grid (over 1000 output tiles), each tile's splits summed by the
+    CTA that finishes it last; every tile completes (same bound, sampled)."""
     M, N, K = 4224, 8192, 2560
     if "wide" not in _PROBLEMS:
         p = inputs.make_problem("wide", M, N, K, seed=9, values="normal", alpha=1.0, beta=0.0,
@@ -600,18 +487,17 @@ def test_splitk_for_large_grids(oracle_mod, monkeypatch, split, mode):
     p, dev, pairs, Dr, sabs = _PROBLEMS["wide"]
     plan = mx.mxfp4_plan_gemm(M, N, K, split, 0)
     assert plan.split_k == split and plan.grid_x * plan.grid_y > 1024
-    assert (plan.workspace_bytes > 0) == (mode == "kernel")
+    assert plan.workspace_bytes > 0
     D = run_gemm(dev, split_k=split)
     assert_within_bound(D[pairs[:, 0], pairs[:, 1]], Dr, sabs, p.alpha, f"wide s={split}")
 
 
 @pytest.mark.parametrize("kernel", ["auto", "pair"])
-def test_d_only_16_byte_aligned(oracle_mod, monkeypatch, kernel):
+def test_d_only_16_byte_aligned(oracle_mod, kernel):
     """D whose rows are 16- but not 32-byte aligned (base offset 8 elements,
     ldd % 16 == 8): the epilogues fall back from 32- to 16-byte stores."""
-    if kernel == "pair":
-        monkeypatch.setenv("MXFP4_KERNEL", "pair")
-    M, N, K = 384, 512, 512
+    M, N, K = (384, 512, 512) if kernel == "auto" else (2304, 2304, 256)
+    assert mx.mxfp4_plan_gemm(M, N, K, 0, 0).pair == (kernel == "pair")
     p = inputs.make_problem("d16", M, N, K, seed=31, values="codes", alpha=1.0, beta=1.0,
                             c_sigma=1.0)
     Dref, sabs = full_oracle(oracle_mod, p)
@@ -627,17 +513,6 @@ def test_d_only_16_byte_aligned(oracle_mod, monkeypatch, kernel):
     torch.cuda.synchronize()
     assert_within_bound(d_to_bits(D.contiguous()), Dref, sabs, p.alpha, f"d16 {kernel}")
     assert torch.isnan(buf[:, :8].float()).all() and torch.isnan(buf[:, 8 + N:].float()).all()
-
-
-def test_stream_read_probe_runs():
-    """The streaming-read measurement hook reads a buffer and returns cleanly
-    (including a byte count that is not a multiple of the grid's stride)."""
-    buf = torch.ones((40 << 20) // 8 + 3, dtype=torch.int64, device="cuda")
-    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for nbytes in (16, 4096 + 16, buf.numel() * 8 // 16 * 16):
-        mx.mxfp4_stream_read_probe(buf, nbytes, sink)
-    torch.cuda.synchronize()
-    assert mx.mxfp4_device_status() == 0
 
 
 # ------------------------------------------------------------- quantiser --

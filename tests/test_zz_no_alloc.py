@@ -1,10 +1,12 @@
 """mxfp4_gemm_noalloc: the GEMM for callers that cannot allocate device memory.
 
-It must give the same results as mxfp4_gemm (within the parity bound used by
-every GPU test) when called through the C ABI, on consecutive calls that
-reuse the shared scratch array, and must refuse shapes whose scratch need is
-larger than the array.  This file is collected last on purpose and must pass
-both alone in a fresh process and after the other tests.
+Called through the C ABI on consecutive calls that reuse the shared scratch
+array, it must agree with the CPU oracle element by element (the parity bound
+every GPU test uses) and give exactly the bits of mxfp4_gemm, which runs the
+same plan on a workspace the caller allocated.  It must refuse shapes whose
+scratch need is larger than the array, and streams of another device.  This
+file is collected last on purpose and must pass both alone in a fresh
+process and after the other tests.
 """
 import numpy as np
 import pytest
@@ -60,11 +62,12 @@ def test_noalloc_matches_mxfp4_gemm_on_consecutive_calls(oracle_mod):
         got = run_noalloc(dev, split)
         assert mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, split) <= SCRATCH_BYTES
         pairs = np.array([(m, n) for m in range(0, p.M, 7) for n in range(0, p.N, 13)])
-        _, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs,
-                                                      alpha=p.alpha, beta=p.beta, C=p.C)
+        ref, _, sabs, inexact = oracle_mod.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K,
+                                                        pairs, alpha=p.alpha, beta=p.beta, C=p.C)
         assert inexact == 0
         sel = (pairs[:, 0], pairs[:, 1])
-        assert_within_bound(got[sel], want[sel], sabs, p.alpha, f"noalloc {p.name}")
+        assert_within_bound(got[sel], ref, sabs, what=f"noalloc {p.name} against the oracle")
+        assert np.array_equal(got, want), f"noalloc {p.name}: not the bits of mxfp4_gemm"
         assert not np.isnan((got.astype(np.uint32) << 16).view(np.float32)).any()
 
 
@@ -82,3 +85,20 @@ def test_noalloc_rejects_shapes_beyond_the_scratch():
     assert e.value.status == -4                      # MXFP4_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.count_nonzero(D).item() == 0        # nothing was enqueued
+
+
+def test_noalloc_back_to_back_without_sync(oracle_mod):
+    """Split-K calls enqueued with no synchronisation between them share the
+    scratch; each waits for the one before it, so all give the same bits."""
+    p = inputs.make_problem("na-chain", 16, 4096, 8192, 23, "normal", 1.0, 0.0, None)
+    dev = Dev(p)
+    assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, 0, 0).split_k > 1
+    first = run_noalloc(dev, 0)
+    outs = [torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for _ in range(4)]
+    for D in outs:
+        mx.mxfp4_gemm_noalloc(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32,
+                              dev.SB, p.K // 32, p.alpha, p.beta, p.M, p.N, p.K, 0)
+    torch.cuda.synchronize()
+    for D in outs:
+        assert np.array_equal(d_to_bits(D), first)

@@ -737,7 +737,7 @@ def hbm_bound_run(name, steps, dev, stream, peaks, peak_src, dist=None):
                                  "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                                  "peak_source": f"{peak_src} HBM copy bandwidth"}}
     res["b_static"]["api"] = ("mxfp4_gemm_ex(..., MXFP4_FLAG_B_STATIC): B and its scales are "
-                              "prefetched into L2 before the in-kernel wait on the previous call")
+                              "loaded without the in-kernel wait on the previous call")
     res["default"]["api"] = "mxfp4_gemm"
     floor = stream_floor(algo_bytes, steps, stream, dev)
     floor["default_over_ordered"] = res["default"]["us_per_gemm"] / floor["ordered"]["us"]

@@ -208,7 +208,7 @@ def mxfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alp
 def mxfp4_gemm_ex(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
                   M, N, K, split_k, flags, workspace, workspace_bytes, stream=None):
     """mxfp4_gemm with flags (MXFP4_FLAG_B_STATIC: the work before this call
-    on the stream does not write B or scaleB, so B may be prefetched early)."""
+    on the stream does not write B or scaleB, so B may be loaded early)."""
     return _check(lib().mxfp4_gemm_ex(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
                                       ld_sa, _p(scaleB), ld_sb, alpha, beta, M, N, K, split_k,
                                       flags, _p(workspace), workspace_bytes, _stream(stream)),

@@ -19,6 +19,7 @@ using namespace mxfp4;
 namespace {
 
 constexpr int kMaxSplit = 16;
+constexpr int kMaxClusterSplit = 8;   // splits a (portable) cluster holds
 constexpr int kDefaultSms = 152;
 constexpr size_t kAlign = 256;
 
@@ -102,6 +103,23 @@ bool encode_operand(CUtensorMap *map, const void *base, int rows, int K, int64_t
     return r == CUDA_SUCCESS;
 }
 
+// 2-D uint8 view [rows, K/32] of row-major E8M0 scales (row stride ld bytes,
+// a multiple of 16); box 16 bytes x box_rows, no swizzle, zero fill.
+bool encode_scales(CUtensorMap *map, const void *base, int rows, int K, int64_t ld, int box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Relaid scale atoms viewed as 2-D uint32 [atoms, 128] (one 512-byte atom per
 // row); a box of 2 rows = the two atoms of one 256-K stage of a 128-row block.
 bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K, int box_atoms = 2)
@@ -162,12 +180,13 @@ struct Candidate {
 constexpr int kMinSplitStages = 8;
 
 // Bytes of the split-K area of a workspace: one 8-byte counter per tile, then
-// one partial slot (128 x part_cols fp32) per tile and split, each part
-// 256-byte aligned.
+// one partial slot (128 rows x part_cols fp32, columns rounded up to 4) per
+// tile and split, each part 256-byte aligned.
 size_t splitk_bytes(int64_t tiles, int split, int part_cols)
 {
+    const size_t cols4 = static_cast<size_t>((part_cols + 3) / 4 * 4);
     return align_up(static_cast<size_t>(tiles) * 8) +
-           align_up(static_cast<size_t>(tiles) * split * kTileM * part_cols * sizeof(float));
+           align_up(static_cast<size_t>(tiles) * split * kTileM * cols4 * sizeof(float));
 }
 
 int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, GemmShape *shape,
@@ -258,7 +277,9 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
     out->grid_y = static_cast<int>(gy);
     out->grid_z = split;
     const int part_cols = static_cast<int>(Q < c.tile_n ? Q : c.tile_n);
-    out->workspace_bytes = split > 1 ? splitk_bytes(tiles, split, part_cols) : 0;
+    // Up to kMaxClusterSplit splits reduce inside each tile's cluster and need
+    // no workspace; more keep fp32 partials and tile counters in it.
+    out->workspace_bytes = split > kMaxClusterSplit ? splitk_bytes(tiles, split, part_cols) : 0;
     out->pair = use_pair ? 1 : 0;
     if (use_pair) {
         // Persistent: one CTA pair per two SMs, each taking every pairs-th
@@ -397,8 +418,11 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     const int64_t ldP = swap ? ldb : lda, ldQ = swap ? lda : ldb;
     // An 8-bit row of K elements holds the bytes of an fp4 row of 2K.
     const int kx = shape.fp8 ? 2 : 1;
+    // Q tiles copy only the rows Q has (rounded up to 8, the swizzle atom):
+    // a skinny M then moves M rows per stage, not tile_n.
+    const int q_box = Qrows < shape.tile_n ? (Qrows + 7) / 8 * 8 : shape.tile_n;
     if (!encode_operand(&tmP, Pp, Prows, K * kx, ldP * kx, kTileM) ||
-        !encode_operand(&tmQ, Qp, Qrows, K * kx, ldQ * kx, shape.tile_n))
+        !encode_operand(&tmQ, Qp, Qrows, K * kx, ldQ * kx, q_box))
         return MXFP4_ERR_CUDA;
 
     GemmArgs a;
@@ -413,6 +437,15 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
                 (sc.ld_b % 8) == 0;
     a.sf_async = sc.rowmajor && aligned(sc.a, 4) && aligned(sc.b, 4) && (sc.ld_a % 4) == 0 &&
                  (sc.ld_b % 4) == 0;
+    // Row-major scales whose rows are 16-byte aligned come by TMA (one copy
+    // per operand and stage); others are gathered with 4-byte copies.
+    a.sf_tma = sc.rowmajor && aligned(sc.a, 16) && aligned(sc.b, 16) && (sc.ld_a % 16) == 0 &&
+               (sc.ld_b % 16) == 0;
+    a.q_box_rows = q_box;
+    CUtensorMap tmSP = tmP, tmSQ = tmQ;   // unused unless a.sf_tma
+    if (a.sf_tma && (!encode_scales(&tmSP, a.sfP, Prows, K, a.ldsP, kTileM) ||
+                     !encode_scales(&tmSQ, a.sfQ, Qrows, K, a.ldsQ, q_box)))
+        return MXFP4_ERR_CUDA;
     a.rowsP = Prows;
     a.rowsQ = Qrows;
     a.M = M;
@@ -429,7 +462,10 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.ldc = ldc;
     a.D = static_cast<uint16_t *>(D);
     a.ldd = ldd;
-    if (plan.split_k > 1) {
+    if (plan.split_k > 1 && plan.split_k <= kMaxClusterSplit) {
+        a.part_cols = Qrows < shape.tile_n ? Qrows : shape.tile_n;
+        a.cluster_reduce = 1;
+    } else if (plan.split_k > 1) {
         if (!ws)
             return MXFP4_ERR_WORKSPACE;
         const int64_t tiles = static_cast<int64_t>(plan.grid_x) * plan.grid_y;
@@ -450,7 +486,7 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
     a.wait_limit = g_wait_limit.load();
 
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    if (launch_gemm(a, tmP, tmQ, shape, grid, stream) != cudaSuccess)
+    if (launch_gemm(a, tmP, tmQ, tmSP, tmSQ, shape, grid, stream) != cudaSuccess)
         return MXFP4_ERR_CUDA;
     return MXFP4_OK;
 }

@@ -367,14 +367,16 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA (leader) --
-        if (leader && lane == 0) {
+        // The whole warp runs the loop (warp-uniform descriptors and
+        // barrier polls); one elected lane issues each MMA and commit.
+        if (leader) {
             const uint32_t idesc = idesc_mxf4(256, BN);
             const uint32_t t_sf = tmem + NACC * BN;
             int stage = 0;
             uint32_t phase = 0;
+            int slot_i = 0;                 // scale slot of the next stage
             int acc = 0;
             uint32_t acc_phase = 0;         // bit b: parity of buffer b's next use
-            int i = 0;                      // stages consumed so far (scale slot index)
             bool stop = false;
             for (int t = cl; t < tiles && !stop; t += ncl) {
                 if (!mbar_wait(&acc_empty[acc], ((acc_phase >> acc) & 1u) ^ 1u, abort_flag,
@@ -385,45 +387,46 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
                 pair_tile_coords(ps, t, pt, qt);
                 const uint32_t q_off = static_cast<uint32_t>(((qt * BN) % kSfRowBlock) / 32);
                 const uint32_t d_tmem = tmem + acc * BN;
-                for (int kt = 0; kt < ps.kt; ++kt, ++i) {
+                for (int kt = 0; kt < ps.kt; ++kt) {
                     // sf_ready completes after the copiers observed the
                     // stage's full barrier (all of its bytes landed), so it
-                    // stands for both: one poll per stage, because every
-                    // mbarrier poll on this thread delays the next MMA issue.
+                    // stands for both: one poll per stage.
                     if (!mbar_wait(&sf_ready[stage], phase, abort_flag, a.wait_limit,
                                    &g_device_status)) {
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    uint8_t *st = smem + stage * PC::STAGE_BYTES;
-                    const uint32_t sfa_t = t_sf + (i % PC::SF_SLOTS) * PC::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(st));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + PC::A_BYTES));
+                    const uint32_t sfa_t = t_sf + slot_i * PC::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + PC::SF_COLS_A + q_off;
+                    const uint32_t st = smem_addr(smem + stage * PC::STAGE_BYTES);
+                    const uint64_t adesc = sdesc_kmajor_sw128(st);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(st + PC::A_BYTES);
                     // Four K=64 MMAs per 256-K stage.
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint32_t sf_id = (j & 1) * 2;
                         const int g = j >> 1;                        // scale k-group
-                        mma_mxf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j,
-                                      idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
-                                      sfb_t + g * 4 * PC::SFB_RB + q_off,
-                                      (kt > 0 || j > 0) ? 1u : 0u);
+                        mma_mxf4_pair_elect(d_tmem, adesc + 2 * j, bdesc + 2 * j,
+                                            idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
+                                            sfb_t + g * 4 * PC::SFB_RB,
+                                            (kt > 0 || j > 0) ? 1u : 0u);
                     }
                     // Frees the stage in both CTAs of the pair.
-                    mma_commit_pair(&empty[stage], static_cast<uint16_t>(3u));
+                    mma_commit_pair_elect(&empty[stage], static_cast<uint16_t>(3u));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (++slot_i == PC::SF_SLOTS)
+                        slot_i = 0;
                 }
-                mma_commit_pair(&acc_full[acc], static_cast<uint16_t>(3u));
+                mma_commit_pair_elect(&acc_full[acc], static_cast<uint16_t>(3u));
                 acc_phase ^= 1u << acc;
                 acc = acc + 1 == NACC ? 0 : acc + 1;
             }
             if (*abort_flag) {
-                mma_commit_pair(&drain[0], static_cast<uint16_t>(1u << lead));
+                mma_commit_pair_elect(&drain[0], static_cast<uint16_t>(1u << lead));
                 mbar_wait_drain(&drain[0], 0, a.wait_limit);
             }
         }

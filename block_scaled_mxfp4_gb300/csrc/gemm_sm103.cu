@@ -37,10 +37,10 @@
 // The kernel is launched as a programmatic dependent of the preceding work on
 // the stream: it starts while that work drains and waits for it in-kernel
 // (griddepcontrol.wait) before the first read of A, C or the scales and
-// before any write.  With b_early, B's tiles (and its row-major or prepacked
-// scales) are first prefetched into L2: callers whose weights the preceding
-// work does not write let the weight stream of one GEMM overlap the tail of
-// the one before it.
+// before any write.  With b_early, the thread that loads B's tiles and B's
+// scales starts filling the ring without that wait: callers whose weights the
+// preceding work does not write let the weight stream of one GEMM start
+// before the kernel ahead of it has finished.
 // With swap (skinny M), P = B and Q = A, so the tile holds D^T: TMEM lane = n,
 // column = m, and a warp's 32 lanes write 32 consecutive n of one row of D.
 //
@@ -74,8 +74,14 @@ struct Cfg {
     static constexpr int NQ = BN >= 128 ? BN / 128 : 1;      // 128-row scale blocks of Q
     static constexpr int SFP_BYTES = G * kSfAtomBytes;       // G atoms per stage
     static constexpr int SFQ_BYTES = NQ * G * kSfAtomBytes;
+    // Row-major scales copied by TMA: 16 bytes of each row (the aligned
+    // 16-byte window holding the stage's 4G scale bytes).
+    static constexpr int SFRP_BYTES = BM * 16;
+    static constexpr int SFRQ_BYTES = BN * 16;
+    static constexpr int SF_AREA = (SFP_BYTES + SFQ_BYTES) > (SFRP_BYTES + SFRQ_BYTES)
+                                       ? (SFP_BYTES + SFQ_BYTES) : (SFRP_BYTES + SFRQ_BYTES);
     // Stages start on 1024-byte boundaries (128-byte swizzle atoms).
-    static constexpr int STAGE_BYTES = (P_BYTES + Q_BYTES + SFP_BYTES + SFQ_BYTES + 1023) / 1024 * 1024;
+    static constexpr int STAGE_BYTES = (P_BYTES + Q_BYTES + SF_AREA + 1023) / 1024 * 1024;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static constexpr int SF_COLS_P = 4 * G;                  // G groups x 4 columns
@@ -92,6 +98,12 @@ struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(G == 1 || G == 2, "scale groups per stage");
 };
+
+constexpr int kGemmThreadsC = 256;     // threads of the one-tile kernel
+
+// Row stride (floats) of a partial parked in shared memory for the cluster
+// reduction: the columns rounded up to 4, plus 4 against bank conflicts.
+__host__ __device__ inline int cluster_part_stride(int part_cols) { return (part_cols + 3) / 4 * 4 + 4; }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -209,30 +221,28 @@ __device__ __forceinline__ void store_col_chunk(const GemmArgs &a, int m0, int n
     store_d_col(a, m0, n, v);
 }
 
-// Split-K: slot (tile, z) of the partials holds 128 rows x part_cols fp32
-// values, row-major by tile row (TMEM lane).  Row `row` of this CTA's
-// partial, columns [c0, c0 + 32) of the accumulator (those below part_cols).
+// Split-K: slot (tile, z) of the partials holds the tile's fp32 partial as
+// chunks of 4 columns, rows contiguous inside a chunk: value (row r, column
+// c) at float ((c / 4) * 128 + r) * 4 + c % 4.  A warp (32 consecutive rows)
+// then stores or loads one chunk as 512 contiguous bytes.
 __device__ __forceinline__ float *partial_slot(const GemmArgs &a, int64_t tile, int z)
 {
-    return a.partials + (tile * a.split_k + z) * static_cast<int64_t>(kTileM * a.part_cols);
+    return a.partials + (tile * a.split_k + z) * static_cast<int64_t>(kTileM * 4 * ((a.part_cols + 3) / 4));
 }
 
-__device__ __forceinline__ void park_partial_chunk(const GemmArgs &a, float *row_ptr, int c0,
+// Row `row` of this CTA's partial, accumulator columns [c0, c0 + 32) (the
+// chunks below part_cols).
+__device__ __forceinline__ void park_partial_chunk(const GemmArgs &a, float *slot, int row, int c0,
                                                    const uint32_t (&r)[32])
 {
-    const int cn = min(32, a.part_cols - c0);
-    float *dst = row_ptr + c0;
-    if ((a.part_cols & 3) == 0 && cn == 32) {
+    const int nch = (a.part_cols + 3) / 4;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-            __stcg(reinterpret_cast<float4 *>(dst + i),
-                   make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < cn)
-                __stcg(dst + i, __uint_as_float(r[i]));
+    for (int i = 0; i < 8; ++i) {
+        const int ch = c0 / 4 + i;
+        if (ch < nch)
+            __stcg(reinterpret_cast<float4 *>(slot + (static_cast<int64_t>(ch) * kTileM + row) * 4),
+                   make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                               __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
     }
 }
 
@@ -274,70 +284,44 @@ __device__ __forceinline__ void reduce_tile(const GemmArgs &a, int64_t tile, int
     const int half = ((a.part_cols + 63) / 64) * 32;
     const int c_begin = (t >> 7) * half;
     const int c_end = min(qvalid, c_begin + half);
-    const bool vec = (a.part_cols & 3) == 0;
-    const float *base = partial_slot(a, tile, 0) + static_cast<int64_t>(row) * a.part_cols;
-    const int64_t zstride = static_cast<int64_t>(kTileM) * a.part_cols;
+    const int64_t zstride = static_cast<int64_t>(kTileM) * 4 * ((a.part_cols + 3) / 4);
+    const float *base = partial_slot(a, tile, 0) + static_cast<int64_t>(row) * 4;
     for (int cg = c_begin; cg < c_end; cg += 32) {
         const int cn = min(32, c_end - cg);
+        const int nv = (cn + 3) / 4;                 // 4-column chunks of this group
         float acc[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
             acc[i] = 0.0f;
-        // Every split's loads of a step are issued before any is added, and
-        // each column adds its splits in the order z = 0, 1, ... whatever
-        // the path (so both paths give the same bits).
-        if (vec) {
-            // Rows of 16-byte aligned float4s; two splits per step.
-            const int nv = (cn + 3) / 4;
-            for (int z = 0; z < a.split_k; z += 2) {
-                const bool two = z + 1 < a.split_k;
-                const float4 *s0 = reinterpret_cast<const float4 *>(base + z * zstride + cg);
-                const float4 *s1 = reinterpret_cast<const float4 *>(base + (z + 1) * zstride + cg);
-                float4 x[8], y[8];
+        // Two splits' loads in flight per step; each column adds its splits
+        // in the order z = 0, 1, ..., split-1.
+        for (int z = 0; z < a.split_k; z += 2) {
+            const bool two = z + 1 < a.split_k;
+            const float *s0 = base + z * zstride + static_cast<int64_t>(cg / 4) * kTileM * 4;
+            const float *s1 = s0 + zstride;
+            float4 x[8], y[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    x[i] = i < nv ? __ldcg(s0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < 8; ++i)
+                x[i] = i < nv ? __ldcg(reinterpret_cast<const float4 *>(s0 + i * kTileM * 4))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    y[i] = (two && i < nv) ? __ldcg(s1 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < 8; ++i)
+                y[i] = (two && i < nv) ? __ldcg(reinterpret_cast<const float4 *>(s1 + i * kTileM * 4))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                acc[4 * i] += x[i].x;
+                acc[4 * i + 1] += x[i].y;
+                acc[4 * i + 2] += x[i].z;
+                acc[4 * i + 3] += x[i].w;
+            }
+            if (two) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    acc[4 * i] += x[i].x;
-                    acc[4 * i + 1] += x[i].y;
-                    acc[4 * i + 2] += x[i].z;
-                    acc[4 * i + 3] += x[i].w;
-                }
-                if (two) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        acc[4 * i] += y[i].x;
-                        acc[4 * i + 1] += y[i].y;
-                        acc[4 * i + 2] += y[i].z;
-                        acc[4 * i + 3] += y[i].w;
-                    }
-                }
-            }
-        } else {
-            // Scalar columns, eight at a time, four splits per step.
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (g * 8 >= cn)
-                    break;
-                for (int z0 = 0; z0 < a.split_k; z0 += 4) {
-                    float t[4][8];
-#pragma unroll
-                    for (int zz = 0; zz < 4; ++zz)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            t[zz][i] = (z0 + zz < a.split_k && g * 8 + i < cn)
-                                           ? __ldcg(base + (z0 + zz) * zstride + cg + g * 8 + i)
-                                           : 0.0f;
-#pragma unroll
-                    for (int zz = 0; zz < 4; ++zz)
-                        if (z0 + zz < a.split_k)
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                acc[g * 8 + i] += t[zz][i];
+                    acc[4 * i] += y[i].x;
+                    acc[4 * i + 1] += y[i].y;
+                    acc[4 * i + 2] += y[i].z;
+                    acc[4 * i + 3] += y[i].w;
                 }
             }
         }
@@ -345,6 +329,115 @@ __device__ __forceinline__ void reduce_tile(const GemmArgs &a, int64_t tile, int
             store_d_row(a, p0 + row, q0 + cg, acc);
         else
             store_d_col(a, q0 + cg, p0 + row, acc);
+    }
+}
+
+// Split-K inside a cluster: every CTA of the tile has parked its fp32
+// partial in its own shared memory (row r at float r * stride, columns
+// contiguous), and cluster rank z holds split z.  Rank r sums the rows
+// [r * R, (r + 1) * R), R = ceil(128 / split), over ranks 0, 1, ..., split-1
+// in that order, four columns per item, then applies alpha / beta with C
+// and rounds once (swap: the rows are n, the columns m).  Consecutive
+// threads take consecutive rows (swap: consecutive n of a D row) or
+// consecutive column chunks of a row (no swap).
+template <bool SWAP>
+__device__ __forceinline__ void reduce_tile_cluster(const GemmArgs &a, uint32_t part_smem, int stride,
+                                                    int p0, int q0, int t)
+{
+    const int S = a.split_k;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int R = (kTileM + S - 1) / S;
+    const int r0 = rank * R;
+    const int prows = SWAP ? a.N : a.M;
+    const int nrows = max(0, min(min(kTileM, r0 + R), prows - p0) - r0);
+    const int qvalid = min(a.part_cols, (SWAP ? a.M : a.N) - q0);
+    const int nch = (qvalid + 3) / 4;
+    const int items = nrows * nch;
+    // Two items per thread per step: all their shared-memory and C loads are
+    // in flight before either is summed.
+    for (int base = t; base < items; base += 2 * kGemmThreadsC) {
+        float4 v[2][8];
+        uint16_t c[2][4];
+        int64_t m[2][4], n[2][4];
+        int cnt[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int it = base + u * kGemmThreadsC;
+            cnt[u] = 0;
+            if (it >= items)
+                continue;
+            const int k = SWAP ? it % nrows : it / nch;
+            const int ch = SWAP ? it / nrows : it % nch;
+            const int row = r0 + k;
+            cnt[u] = min(4, qvalid - 4 * ch);
+            const uint32_t off = part_smem + static_cast<uint32_t>((row * stride + 4 * ch) * 4);
+#pragma unroll
+            for (int z = 0; z < 8; ++z)
+                if (z < S)
+                    v[u][z] = ld_dsmem_v4(map_to_rank(off, static_cast<uint32_t>(z)));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                m[u][j] = SWAP ? q0 + 4 * ch + j : p0 + row;
+                n[u][j] = SWAP ? p0 + row : q0 + 4 * ch + j;
+                c[u][j] = (a.beta != 0.0f && j < cnt[u]) ? a.C[m[u][j] * a.ldc + n[u][j]] : uint16_t(0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (cnt[u] == 0)
+                continue;
+            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+                if (z < S) {
+                    x0 += v[u][z].x;
+                    x1 += v[u][z].y;
+                    x2 += v[u][z].z;
+                    x3 += v[u][z].w;
+                }
+            }
+            const float xs[4] = {x0, x1, x2, x3};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j < cnt[u]) {
+                    float y = a.alpha * xs[j];
+                    if (a.beta != 0.0f)
+                        y = fmaf(a.beta, bf16_bits_to_float(c[u][j]), y);
+                    __nv_bfloat16 b = __float2bfloat16_rn(y);
+                    a.D[m[u][j] * a.ldd + n[u][j]] = *reinterpret_cast<uint16_t *>(&b);
+                }
+            }
+        }
+    }
+}
+
+// Bring the lines of C that this CTA's share of the cluster reduction reads
+// into L2 (called while the CTA waits for its peers).
+template <bool SWAP>
+__device__ __forceinline__ void prefetch_c_share(const GemmArgs &a, int p0, int q0, int t)
+{
+    const int S = a.split_k;
+    const int R = (kTileM + S - 1) / S;
+    const int r0 = static_cast<int>(cluster_ctarank()) * R;
+    const int prows = SWAP ? a.N : a.M;
+    const int nrows = max(0, min(min(kTileM, r0 + R), prows - p0) - r0);
+    const int qvalid = min(a.part_cols, (SWAP ? a.M : a.N) - q0);
+    if (nrows <= 0 || qvalid <= 0)
+        return;
+    if (SWAP) {
+        // Row m of C: n = p0 + r0 .. + nrows (2 bytes each).
+        for (int i = t; i < qvalid; i += kGemmThreadsC) {
+            const uint16_t *row = a.C + static_cast<int64_t>(q0 + i) * a.ldc + p0 + r0;
+            prefetch_l2(row);
+            prefetch_l2(row + nrows - 1);
+        }
+    } else {
+        for (int i = t; i < nrows; i += kGemmThreadsC) {
+            const uint16_t *row = a.C + static_cast<int64_t>(p0 + r0 + i) * a.ldc + q0;
+            for (int c = 0; c < qvalid; c += 64)
+                prefetch_l2(row + c);
+            prefetch_l2(row + qvalid - 1);
+        }
     }
 }
 
@@ -433,10 +526,14 @@ __device__ __forceinline__ void store_sf_lines(uint8_t *atoms, const uint32_t (&
 // TMEM lane 32w + i of the stage's scale slot: P's two atoms to columns
 // [0, 8), Q's atoms (K group g, row block r) to columns 8 + (g*NQ + r)*4.
 // t_lane = TMEM base address with this warp's lane quarter in its lane field.
+// raw: the stage holds row-major scales (16 bytes per row, the stage's 4G
+// bytes at offset (4G kt) % 16 of each row, P's 128 rows then Q's BN rows),
+// gathered here into the same lines.
 template <class Cf>
 __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full, uint64_t *sf_full,
-                                                   uint32_t t_lane, int nkt, int lane,
-                                                   volatile int *abort_flag, long long limit)
+                                                   uint32_t t_lane, int nkt, int kt0, bool raw,
+                                                   int lane, volatile int *abort_flag,
+                                                   long long limit)
 {
     constexpr int STAGES = Cf::STAGE_COUNT;
     const uint32_t t_sf = t_lane + Cf::BN_COLS;
@@ -450,6 +547,25 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
         const uint8_t *sf_s = smem + stage * Cf::STAGE_BYTES + Cf::P_BYTES + Cf::Q_BYTES;
         uint32_t wp[4 * G];
         uint32_t wq[4 * G * Cf::NQ];
+        if (raw) {
+            const int off = ((kt0 + i) * 4 * G) & 15;
+            const uint8_t *rp = sf_s + off;
+            const uint8_t *rq = sf_s + Cf::SFRP_BYTES + off;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    wp[4 * g + j] = *reinterpret_cast<const uint32_t *>(rp + (lane + 32 * j) * 16 + 4 * g);
+#pragma unroll
+                for (int r = 0; r < Cf::NQ; ++r)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = 128 * r + 32 * j + lane;
+                        wq[(g * Cf::NQ + r) * 4 + j] =
+                            row < Cf::BN_COLS ? *reinterpret_cast<const uint32_t *>(rq + row * 16 + 4 * g) : 0u;
+                    }
+            }
+        } else {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const uint4 v = *reinterpret_cast<const uint4 *>(sf_s + g * kSfAtomBytes + 16 * lane);
@@ -467,6 +583,7 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
                 wq[o + 2] = u.z;
                 wq[o + 3] = u.w;
             }
+        }
         }
         const uint32_t slot = t_sf + stage * Cf::SF_COLS;
         if constexpr (G == 2)
@@ -491,41 +608,7 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
     }
 }
 
-constexpr int kGemmThreads = 256;
-
-// L2 prefetch of this CTA's share of B (b_early): its operand tiles for the
-// K stages [kt0, kt0 + nkt) and their scales.  Called by one whole warp;
-// lane 0 issues the tile prefetches, every lane some scale rows.
-template <int G>
-__device__ __forceinline__ void prefetch_b_share(const GemmArgs &a, const CUtensorMap *tmB, int row0,
-                                                 int nrows, int kt0, int nkt, int lane)
-{
-    if (lane == 0)
-        for (int i = 0; i < nkt; ++i)
-            tma_prefetch_2d(tmB, (kt0 + i) * 128, row0);
-    const uint8_t *sfb = a.p_is_b ? a.sfP : a.sfQ;
-    if (a.sf_rowmajor) {
-        // Row-major scales: 4G bytes per stage and row.
-        const int64_t ld = a.p_is_b ? a.ldsP : a.ldsQ;
-        const int rows = a.p_is_b ? a.rowsP : a.rowsQ;
-        const int64_t b0 = static_cast<int64_t>(kt0) * 4 * G;
-        const int64_t b1 = min(static_cast<int64_t>(kt0 + nkt) * 4 * G, static_cast<int64_t>(a.K / 32)) - 1;
-        for (int r = lane; r < nrows; r += 32) {
-            if (row0 + r >= rows)
-                break;
-            const uint8_t *p = sfb + static_cast<int64_t>(row0 + r) * ld;
-            prefetch_l2(p + b0);
-            if (((reinterpret_cast<uintptr_t>(p + b0) ^ reinterpret_cast<uintptr_t>(p + b1)) >> 7) != 0)
-                prefetch_l2(p + b1);
-        }
-    } else if (lane == 0) {
-        // Relaid atoms: G per stage, contiguous along K within a row block.
-        for (int rb = 0; rb * kSfRowBlock < nrows; ++rb)
-            bulk_prefetch_l2(sfb + static_cast<int64_t>(row0 / kSfRowBlock + rb) * a.sf_rb_stride +
-                                 static_cast<int64_t>(kt0) * G * kSfAtomBytes,
-                             static_cast<uint32_t>(nkt * G * kSfAtomBytes));
-    }
-}
+constexpr int kGemmThreads = kGemmThreadsC;
 
 // FMT 0: fp4 (E2M1) elements, kind::mxf4; FMT 1: one byte per element
 // (E4M3 / E5M2 / padded E2M3, E3M2, E2M1), kind::mxf8f6f4 with the element
@@ -533,7 +616,8 @@ __device__ __forceinline__ void prefetch_b_share(const GemmArgs &a, const CUtens
 template <int BN, int STAGES, bool SWAP, int FMT, int MINB>
 __global__ void __launch_bounds__(kGemmThreads, MINB)
     gemm_mxf4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmP,
-                     const __grid_constant__ CUtensorMap tmQ)
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmSP,
+                     const __grid_constant__ CUtensorMap tmSQ)
 {
     using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
     constexpr int G = Cf::GROUPS;
@@ -575,7 +659,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], !a.sf_rowmajor ? 3 : a.sf_async ? 33 : 2);
+            mbar_init(&full[s], !a.sf_rowmajor ? 3 : a.sf_tma ? 2 : a.sf_async ? 33 : 2);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_full[s], 4);
         }
@@ -591,6 +675,10 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
     if (warp == 4 && lane == 0) {
         prefetch_tensormap(&tmP);
         prefetch_tensormap(&tmQ);
+        if (a.sf_tma) {
+            prefetch_tensormap(&tmSP);
+            prefetch_tensormap(&tmSQ);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -603,12 +691,56 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
 
     if (warp == 4 || warp >= 6) {
         // ------------------------------------------------------ producer --
-        if (a.b_early && nkt > 0 && warp == (a.sf_rowmajor ? 4 : (a.p_is_b ? 4 : 6)))
-            prefetch_b_share<G>(a, a.p_is_b ? &tmP : &tmQ, a.p_is_b ? p0 : q0,
-                                a.p_is_b ? kTileM : BN, kt0, nkt, lane);
-        // Everything below may read the preceding work's output.
-        pdl_wait_prerequisites();
-        if (a.sf_rowmajor && a.sf_async && nkt > 0 && warp == 4) {
+        // Loads may read the preceding work's output, so they wait for it --
+        // except, with b_early, those of the thread that loads only B and its
+        // scales (P with swap, else Q): the caller guarantees the preceding
+        // work does not write them.
+        const bool b_role = a.b_early && (a.sf_tma || !a.sf_rowmajor) &&
+                            warp == (a.p_is_b ? 4 : 6);
+        if (!b_role)
+            pdl_wait_prerequisites();
+        if (a.sf_rowmajor && a.sf_tma && nkt > 0) {
+            // Two issuing threads: warp 4 the P tile and P's row-major scales,
+            // warp 6 the Q tile (a.q_box_rows rows) and Q's; each scale box
+            // is the aligned 16-byte window of 128 (or q_box_rows) rows that
+            // holds the stage's 4G bytes.  Each thread arrives on the stage's
+            // full barrier with its bytes.
+            if (lane == 0 && (warp == 4 || warp == 6)) {
+                const bool is_p = warp == 4;
+                const uint64_t pol = (is_p && a.stream_p) ? l2_policy_evict_first() : l2_policy_evict_last();
+                const uint32_t bytes = is_p ? static_cast<uint32_t>(Cf::P_BYTES + Cf::SFRP_BYTES)
+                                            : static_cast<uint32_t>(a.q_box_rows * (128 + 16));
+                int stage = 0;
+                uint32_t phase = 0;
+                int issued = 0;
+                for (int i = 0; i < nkt; ++i) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_limit,
+                                   &g_device_status))
+                        break;
+                    uint8_t *st = smem + stage * Cf::STAGE_BYTES;
+                    const int kt = kt0 + i;
+                    const int sx = (kt * 4 * G) & ~15;
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    if (is_p) {
+                        tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol);
+                        tma_load_2d(st + Cf::P_BYTES + Cf::Q_BYTES, &tmSP, &full[stage], sx, p0, pol);
+                    } else {
+                        tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol);
+                        tma_load_2d(st + Cf::P_BYTES + Cf::Q_BYTES + Cf::SFRP_BYTES, &tmSQ, &full[stage],
+                                    sx, q0, pol);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (*abort_flag) {
+                    for (int i = max(0, issued - STAGES); i < issued; ++i)
+                        mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
+                }
+            }
+        } else if (a.sf_rowmajor && a.sf_async && nkt > 0 && warp == 4) {
             // Whole warp: lane 0 issues the operand TMAs; every lane copies its
             // lines of the stage's scale atoms with 4-byte cp.async straight
             // from the row-major scales, and the stage's full barrier counts
@@ -627,7 +759,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;
                 const int kt = kt0 + i;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES + Cf::Q_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES + a.q_box_rows * 128);
                     tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
                     tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
                 }
@@ -676,7 +808,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                 uint8_t *st = smem + stage * Cf::STAGE_BYTES;
                 const int kt = kt0 + i;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES + Cf::Q_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES + a.q_box_rows * 128);
                     tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
                     tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
                 }
@@ -723,7 +855,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                     mbar_arrive_expect_tx(&full[stage], Cf::P_BYTES);
                     tma_load_2d(st, &tmP, &full[stage], kt * 128, p0, pol_p);
                 } else if (role == 1) {
-                    mbar_arrive_expect_tx(&full[stage], Cf::Q_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], a.q_box_rows * 128);
                     tma_load_2d(st + Cf::P_BYTES, &tmQ, &full[stage], kt * 128, q0, pol_q);
                 } else {
                     mbar_arrive_expect_tx(&full[stage], Cf::SFP_BYTES + Cf::SFQ_BYTES);
@@ -802,7 +934,8 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
         // ------------------------------------------------- scale writers --
         if (nkt > 0)
             write_stage_scales<Cf>(smem, full, sf_full, tmem + (static_cast<uint32_t>(warp * 32) << 16),
-                                   nkt, lane, abort_flag, a.wait_limit);
+                                   nkt, kt0, a.sf_rowmajor && a.sf_tma, lane, abort_flag,
+                                   a.wait_limit);
         // ------------------------------------------------------ epilogue --
         bool ok = nkt > 0 && mbar_wait(acc_full, 0, abort_flag, a.wait_limit, &g_device_status);
         ok = __all_sync(0xffffffffu, ok);
@@ -812,16 +945,35 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
             tc_fence_after();
             const int row = warp * 32 + lane;
             const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-            if (a.split_k > 1) {
+            if (a.split_k > 1 && a.cluster_reduce) {
+                // Park this split's partial in this CTA's shared memory (the
+                // ring: every MMA has read its last stage).
+                float *part = reinterpret_cast<float *>(smem);
+                const int stride = cluster_part_stride(a.part_cols);
+                const int cols = min(a.part_cols, (SWAP ? a.M : a.N) - q0);
+                const int nch = (cols + 3) / 4;
+#pragma unroll 1
+                for (int c0 = 0; c0 < cols; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c0, r);
+                    tmem_ld_wait(r);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (c0 / 4 + i < nch)
+                            *reinterpret_cast<float4 *>(part + row * stride + c0 + 4 * i) =
+                                make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                }
+            } else if (a.split_k > 1) {
                 // Park this split's partial (its valid columns) in the tile's slot.
-                float *row_ptr = partial_slot(a, tile, z) + static_cast<int64_t>(row) * a.part_cols;
+                float *slot = partial_slot(a, tile, z);
                 const int cols = min(a.part_cols, (SWAP ? a.M : a.N) - q0);
 #pragma unroll 1
                 for (int c0 = 0; c0 < cols; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(t_row + c0, r);
                     tmem_ld_wait(r);
-                    park_partial_chunk(a, row_ptr, c0, r);
+                    park_partial_chunk(a, slot, row, c0, r);
                 }
                 __threadfence();
             } else {
@@ -846,7 +998,18 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
 
     tc_fence_before();
     __syncthreads();
-    if (a.split_k > 1 && nkt > 0) {
+    if (a.split_k > 1 && a.cluster_reduce) {
+        // Every partial of the tile is in its CTA's shared memory once the
+        // cluster barrier completes; the second barrier keeps this CTA's
+        // partial alive until its peers have read it.
+        pdl_wait_prerequisites();
+        if (a.beta != 0.0f)
+            prefetch_c_share<SWAP>(a, p0, q0, threadIdx.x);
+        cluster_sync();
+        reduce_tile_cluster<SWAP>(a, smem_addr(smem), cluster_part_stride(a.part_cols), p0, q0,
+                                  threadIdx.x);
+        cluster_sync();
+    } else if (a.split_k > 1 && nkt > 0) {
         // Count this CTA into its tile (its partial rows are written and
         // fenced); the CTA that completes the count reduces the tile.
         if (threadIdx.x == 0 && !*abort_flag) {
@@ -880,7 +1043,8 @@ namespace mxfp4 {
 
 template <int BN, int STAGES, bool SWAP, int FMT, int MINB>
 static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
-                              dim3 grid, cudaStream_t stream)
+                              const CUtensorMap &tmSP, const CUtensorMap &tmSQ, dim3 grid,
+                              cudaStream_t stream)
 {
     using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
     auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP, FMT, MINB>;
@@ -904,12 +1068,23 @@ static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const C
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, tmP, tmQ);
+    if (a.cluster_reduce) {
+        // The split_k CTAs of a tile (grid z) form one cluster.
+        if (static_cast<int>(grid.z) != a.split_k || a.split_k > 8 ||
+            kTileM * cluster_part_stride(a.part_cols) * 4 > STAGES * Cf::STAGE_BYTES)
+            return cudaErrorInvalidConfiguration;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = static_cast<unsigned>(a.split_k);
+        cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a, tmP, tmQ, tmSP, tmSQ);
 }
 
 size_t gemm_smem_bytes(const GemmShape &s)
@@ -933,28 +1108,30 @@ bool gemm_config_exists(const GemmShape &s)
 
 template <int FMT>
 static cudaError_t launch_gemm_fmt(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
+                                   const CUtensorMap &tmSP, const CUtensorMap &tmSQ,
                                    const GemmShape &s, dim3 grid, cudaStream_t stream)
 {
     if (!s.swap) {
         if (s.tile_n == 256 && s.stages == 4)
-            return launch_cfg<256, 4, false, FMT, 1>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<256, 4, false, FMT, 1>(a, tmP, tmQ, tmSP, tmSQ, grid, stream);
         if (s.tile_n == 128 && s.stages == 6)
-            return launch_cfg<128, 6, false, FMT, 1>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<128, 6, false, FMT, 1>(a, tmP, tmQ, tmSP, tmSQ, grid, stream);
         if (s.tile_n == 64 && s.stages == 8)
-            return launch_cfg<64, 8, false, FMT, 1>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 8, false, FMT, 1>(a, tmP, tmQ, tmSP, tmSQ, grid, stream);
     } else {
         // Two CTAs per SM (the plan's slots for skinny shapes).
         if (s.tile_n == 64 && s.stages == 4)
-            return launch_cfg<64, 4, true, FMT, 2>(a, tmP, tmQ, grid, stream);
+            return launch_cfg<64, 4, true, FMT, 2>(a, tmP, tmQ, tmSP, tmSQ, grid, stream);
     }
     return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
-                        const GemmShape &s, dim3 grid, cudaStream_t stream)
+                        const CUtensorMap &tmSP, const CUtensorMap &tmSQ, const GemmShape &s,
+                        dim3 grid, cudaStream_t stream)
 {
     if (!s.fp8)
-        return launch_gemm_fmt<0>(a, tmP, tmQ, s, grid, stream);
+        return launch_gemm_fmt<0>(a, tmP, tmQ, tmSP, tmSQ, s, grid, stream);
     // kind::mxf8f6f4 element codes: E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5.
     auto known = [](int f) { return f == 0 || f == 1 || (f >= 3 && f <= 5); };
     if (!known(a.fmt_p) || !known(a.fmt_q))
@@ -962,7 +1139,7 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
     GemmArgs b = a;
     b.idesc8 = idesc_mxf8(kTileM, s.tile_n, static_cast<uint32_t>(a.fmt_p),
                           static_cast<uint32_t>(a.fmt_q));
-    return launch_gemm_fmt<1>(b, tmP, tmQ, s, grid, stream);
+    return launch_gemm_fmt<1>(b, tmP, tmQ, tmSP, tmSQ, s, grid, stream);
 }
 
 // The compiled pair configuration: 6 stages, 256 x 256 tiles, one accumulator.

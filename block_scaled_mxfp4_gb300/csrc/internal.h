@@ -32,6 +32,9 @@ struct GemmArgs {
     int sf_rowmajor;        // 1: scales are row-major E8M0 [rows, ld] (atoms built in-kernel)
     int sf_vec8;            // row-major scales allow aligned 8-byte loads per stage
     int sf_async;           // row-major scales allow 4-byte cp.async (aligned rows)
+    int sf_tma;             // row-major scales come by 2-D TMA (16-byte aligned rows)
+    int q_box_rows;         // rows of a Q tile copied per stage (Q's rows rounded up to 8,
+                            // at most tile_n; rows past them are never stored)
     int64_t ldsP, ldsQ;     // row-major: row strides in bytes
     int rowsP, rowsQ;       // rows of P and Q
     int M, N, K;
@@ -50,6 +53,9 @@ struct GemmArgs {
     unsigned long long *tile_count;   // [tiles]: (epoch << 32) | CTAs of the tile done
     int part_cols;          // columns per partial row: min(tile_n, rows of Q)
     uint32_t epoch;         // this call's counter tag (never 0)
+    int cluster_reduce;     // 1: the split_k CTAs of a tile form one thread-block
+                            // cluster and sum their partials through distributed
+                            // shared memory (no partials, counters or workspace)
     int vec_ok;             // D (and C) allow aligned 16-byte row accesses
     int vec32_ok;           // D allows aligned 32-byte row stores
     int stream_p;           // P is read once: hint L2 evict-first
@@ -81,8 +87,10 @@ bool gemm_config_exists(const GemmShape &s);
 // One-tile kernel, launched as a programmatic dependent of the preceding work
 // on `stream`: it waits in-kernel for that work before touching memory the
 // work may write (everything but B and its scales when a.b_early).
+// tmSP / tmSQ: row-major scale maps (used when a.sf_tma).
 cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtensorMap &tmQ,
-                        const GemmShape &s, dim3 grid, cudaStream_t stream);
+                        const CUtensorMap &tmSP, const CUtensorMap &tmSQ, const GemmShape &s,
+                        dim3 grid, cudaStream_t stream);
 
 // CTA-pair kernel (relaid scales): grid of up to `ctas` CTAs in clusters of
 // two (clamped to the clusters the GPU holds at once), persistent over 256 x

@@ -131,22 +131,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Bring one 2-D box of a tensor into L2 (no shared-memory destination, no
-// completion to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// Bring `bytes` (a multiple of 16) at a 16-byte aligned address into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Bring the L2 line holding `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void *p)
 {
@@ -581,6 +565,34 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, u
         "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// mma_mxf4_pair issued by one elected lane of a warp that runs the issue
+// loop together (warp-uniform operands).
+__device__ __forceinline__ void mma_mxf4_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                    uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                    uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// mma_commit_pair issued by one elected lane of the warp.
+__device__ __forceinline__ void mma_commit_pair_elect(uint64_t *bar, uint16_t mask)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+        "h"(mask)
         : "memory");
 }
 

@@ -97,7 +97,8 @@ int mxfp4_plan_gemm(int M, int N, int K, int split_k, int num_sms, mxfp4_plan *o
 
 /*
  * Bytes of device workspace mxfp4_gemm needs: when the plan splits K, one
- * 8-byte counter per output tile and one fp32 partial tile per (tile, split);
+ * 8-byte counter per output tile and one fp32 partial tile per (tile, split)
+ * (its columns rounded up to a multiple of 4);
  * plus both relaid scale buffers when the plan has a relayout pass; 0 when
  * neither applies (then the workspace may be NULL).  Returns 0 for invalid
  * sizes too (mxfp4_plan_gemm tells them apart).
@@ -174,9 +175,10 @@ int mxfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
  * mxfp4_gemm with flags.  MXFP4_FLAG_B_STATIC: the caller guarantees that the
  * work enqueued on `stream` before this call does not write B or scaleB (for
  * example weights that stay fixed across a decode loop).  The GEMM then
- * prefetches its share of B and of scaleB into L2 before waiting for that
- * work, so the weight stream of one call overlaps the tail of the kernel
- * before it; A, C and D are still touched only after that work has finished.
+ * starts copying B and scaleB into its pipeline before waiting for that
+ * work, so the weight stream of one call can start before the kernel ahead
+ * of it has finished; A, C and D are still touched only after that work has
+ * finished.
  * The flag has no effect on plans with a relayout pass (their B scales come
  * from this call's own relayout).  Other arguments and results as for
  * mxfp4_gemm (bit-identical output); unknown flag bits: MXFP4_ERR_INVALID_ARG.

@@ -49,12 +49,13 @@ def _a256(x):
 
 
 def splitk_ws(tiles, split, part_cols):
-    """Split-K workspace: one 8-byte counter per tile, then one 128-row fp32
-    partial slot of part_cols columns per (tile, split), each part 256-byte
-    aligned; nothing without a split."""
-    if split <= 1:
+    """Split-K workspace: up to 8 splits reduce inside each tile's cluster and
+    need none; more keep one 8-byte counter per tile, then one 128-row fp32
+    partial slot of part_cols columns (rounded up to 4) per (tile, split),
+    each part 256-byte aligned."""
+    if split <= 8:
         return 0
-    return _a256(tiles * 8) + _a256(tiles * split * 128 * part_cols * 4)
+    return _a256(tiles * 8) + _a256(tiles * split * 128 * (-(-part_cols // 4) * 4) * 4)
 
 
 WORKLOADS = {"tiny": (128, 256, 512), "decode": (1, 8192, 8192), "mid": (512, 1024, 2048),
@@ -149,14 +150,16 @@ def test_sizes(L):
     assert mx.mxfp4_scale_relayout_size(5, 48) == 0
     assert mx.mxfp4_gemm_workspace_size(0, 1, 32, 0) == 0
     assert mx.mxfp4_gemm_workspace_size(1, 1, 32, 17) == 0
-    # The decode shape splits K four ways over 64 tiles of 128 rows of B:
-    # 64 counters and 4 x 64 partial slots of 128 rows x 1 column (M = 1).
-    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 512 + 4 * 64 * 128 * 4
+    # The decode and skinny shapes split K four and five ways: the splits of a
+    # tile reduce inside their cluster, so no workspace.
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 4) == 0
     p = mx.mxfp4_plan_gemm(1, 8192, 8192, 0, 152)
-    assert p.split_k == 4 and p.workspace_bytes == 512 + 4 * 64 * 128 * 4
-    # Skinny: 56 tiles, 5 splits, 64 columns each.
+    assert p.split_k == 4 and p.workspace_bytes == 0
     p = mx.mxfp4_plan_gemm(64, 7168, 16384, 0, 152)
-    assert p.split_k == 5 and p.workspace_bytes == 512 + 56 * 5 * 128 * 64 * 4
+    assert p.split_k == 5 and p.workspace_bytes == 0
+    # Sixteen splits of decode: 64 counters and 16 x 64 partial slots of 128
+    # rows x 4 columns (M = 1, rounded up to a chunk of 4).
+    assert mx.mxfp4_gemm_workspace_size(1, 8192, 8192, 16) == 512 + 16 * 64 * 128 * 16
     # The large shape relays its scales out first: workspace = both relaid buffers.
     p = mx.mxfp4_plan_gemm(8192, 8192, 8192, 1, 0)
     assert p.relayout_pass == 1

@@ -48,12 +48,14 @@ def test_header_declares_the_scratch_limit():
 
 
 def test_noalloc_matches_mxfp4_gemm_on_consecutive_calls(oracle_mod):
-    # Two different problems back to back (the second reuses scratch the first
-    # left behind), then the first again; split-K ones use the partial-sum
-    # part of the scratch, the others only the relaid scales.
+    # Different problems back to back (each reuses scratch the one before
+    # left behind), then the first again: sixteen splits keep fp32 partials
+    # and tile counters in the scratch, the large one relays its scales into
+    # it, the mid one needs none.
     cases = [
-        (inputs.make_problem("na-skinny", 48, 3072, 4096, 21, "normal", 1.0, 1.0, 0.5), 4),
+        (inputs.make_problem("na-skinny", 48, 3072, 4096, 21, "normal", 1.0, 1.0, 0.5), 16),
         (inputs.make_problem("na-mid", 256, 512, 1024, 22, "codes", 0.5, 0.5, 1.0), 0),
+        (inputs.make_problem("na-big", 2304, 2304, 1024, 24, "codes", 1.0, 0.0, None), 0),
     ]
     cases.append(cases[0])
     for p, split in cases:
@@ -92,13 +94,14 @@ def test_noalloc_back_to_back_without_sync(oracle_mod):
     scratch; each waits for the one before it, so all give the same bits."""
     p = inputs.make_problem("na-chain", 16, 4096, 8192, 23, "normal", 1.0, 0.0, None)
     dev = Dev(p)
-    assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, 0, 0).split_k > 1
-    first = run_noalloc(dev, 0)
+    assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, 16, 0).split_k == 16
+    assert mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, 16) > 0
+    first = run_noalloc(dev, 16)
     outs = [torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
             for _ in range(4)]
     for D in outs:
         mx.mxfp4_gemm_noalloc(D, p.N, None, 0, dev.A, p.K, dev.B, p.K, dev.SA, p.K // 32,
-                              dev.SB, p.K // 32, p.alpha, p.beta, p.M, p.N, p.K, 0)
+                              dev.SB, p.K // 32, p.alpha, p.beta, p.M, p.N, p.K, 16)
     torch.cuda.synchronize()
     for D in outs:
         assert np.array_equal(d_to_bits(D), first)

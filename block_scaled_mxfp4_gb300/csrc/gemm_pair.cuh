@@ -20,26 +20,26 @@
 //       for it.  A 192-row B tile starts 0 or 64 rows into a 128-row scale
 //       block, so its scale-B base column is offset by 0 or 2.
 //
-// Roles (448 threads = 14 warps per CTA):
+// Roles (512 threads = 16 warps per CTA):
 //   warps 4, 6, 7 (each CTA)  TMA producers: A half, B half, and the scale
 //                      atoms (this CTA's 128 rows of scale-A; all BN rows of
-//                      scale-B in one 3-D box of 2 K-groups x 2 row blocks).
-//                      Every copy completes its bytes on the LEADER's full
-//                      barrier (the cta_group::2 form of the TMA); only
-//                      the leader's three producers arrive on it, each
-//                      expecting its copy's bytes for both CTAs.  A thread
-//                      waits out each copy instruction it issues (hundreds of
-//                      cycles), hence three issuing warps.
-//   warps 12, 13 (leader)  scale copiers: once a stage has landed (and, with
-//                      fewer scale slots than stages, once the MMAs that last
-//                      read the slot have completed) each issues half of the
-//                      stage's tcgen05.cp.cta_group::2 (both CTAs' atoms into their
-//                      own tensor memory) and commits them to the stage's
-//                      sf_ready barrier.  Copies issued by a thread other than
-//                      the MMA issuer run alongside the MMAs.
+//                      scale-B in one 3-D box of 2 K-groups x 2 row blocks),
+//                      each completing its bytes on this CTA's full barrier.
+//                      A thread waits out each copy instruction it issues
+//                      (hundreds of cycles), hence three issuing warps.
+//   warps 12-15 (each CTA)  scale writers, warp w for TMEM lanes 32(w%4)..+31:
+//                      once a stage has landed in this CTA, each lane reads
+//                      its 16-byte lines of the stage's atoms from shared
+//                      memory and writes them with tcgen05.st into its TMEM
+//                      lane of the stage's scale slot (the four warps lay
+//                      down the four replicas), waits for the stores, and
+//                      arrives on the LEADER's sf_ready barrier (the peer's
+//                      warps with a relaxed remote arrive).  tcgen05.st does
+//                      not queue behind the MMAs, unlike tcgen05.cp, so the
+//                      scales of later stages are ready well ahead.
 //   warp 5 (leader)    waits for an accumulator buffer to be free, then per
-//                      stage for the scales (whose barrier the copiers commit
-//                      only after the stage's operands landed); issues four K=64
+//                      stage for sf_ready (8 arrivals: both CTAs' data landed
+//                      and both CTAs' scales written); issues four K=64
 //                      M=256 N=BN MMAs and commits the stage to BOTH CTAs'
 //                      empty barriers, and each tile to both CTAs'
 //                      accumulator-full barriers.
@@ -88,7 +88,7 @@ struct PairCfg {
     static constexpr int HALF = BN / 2;                   // columns per epilogue warp
     static constexpr int TMEM_USED = NACC * BN + SF_SLOTS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-    static constexpr int THREADS = 448;
+    static constexpr int THREADS = 512;
     static constexpr int EPI_WARPS = 8;                   // per CTA
     static_assert(BN == 256 || BN == 192, "tile N");
     static_assert(SF_SLOTS >= 2, "scale slots");
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
     uint64_t *sf_ready = empty + STAGES;                                    // leader's are used
     uint64_t *acc_full = sf_ready + STAGES;                                 // [NACC]
     uint64_t *acc_empty = acc_full + NACC;                                  // [NACC], leader's used
-    uint64_t *drain = acc_empty + NACC;                                     // [3]: MMA, copiers
+    uint64_t *drain = acc_empty + NACC;                                     // [3]: MMA
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -224,9 +224,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 3);          // the leader's three producers (both CTAs' bytes)
+            mbar_init(&full[s], 3);          // this CTA's three producers
             mbar_init(&empty[s], 1);         // the pair's MMA commit
-            mbar_init(&sf_ready[s], 2);      // the leader's two scale copiers
+            mbar_init(&sf_ready[s], 8);      // the scale writers of both CTAs (leader's used)
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -286,21 +286,15 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
                         break;
                     }
                     uint8_t *st = smem + stage * PC::STAGE_BYTES;
-                    const uint32_t lbar = map_to_rank(smem_addr(&full[stage]), lead);
-                    // Only the leader arrives (a cluster-scope arrive from the
-                    // peer costs ~0.5 us); the peer's copies just complete
-                    // their bytes on the leader's barrier, which cannot start
-                    // this stage's next phase before the MMAs freed the stage.
-                    if (leader)
-                        mbar_arrive_expect_tx(&full[stage], 2 * unit);
+                    mbar_arrive_expect_tx(&full[stage], unit);
                     if (role == 0) {
-                        tma_load_2d_pair(st, &tmA, lbar, kt * 128, arow, pol);
+                        tma_load_2d(st, &tmA, &full[stage], kt * 128, arow, pol);
                     } else if (role == 1) {
-                        tma_load_2d_pair(st + PC::A_BYTES, &tmB, lbar, kt * 128, brow, pol);
+                        tma_load_2d(st + PC::A_BYTES, &tmB, &full[stage], kt * 128, brow, pol);
                     } else {
                         uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
-                        tma_load_2d_pair(sf, &tmSA, lbar, 0, sfa_atom + 2 * kt, pol);
-                        tma_load_3d_pair(sf + PC::SFA_BYTES, &tmSB, lbar, 0, 2 * kt, sfb_rb, pol);
+                        tma_load_2d(sf, &tmSA, &full[stage], 0, sfa_atom + 2 * kt, pol);
+                        tma_load_3d(sf + PC::SFA_BYTES, &tmSB, &full[stage], 0, 2 * kt, sfb_rb, pol);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -309,60 +303,70 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
                     }
                 }
             }
-            if (*abort_flag && leader) {
+            if (*abort_flag) {
                 // Let the copies already issued land before the CTA exits.
                 for (int i = max(0, issued - STAGES); i < issued; ++i)
                     mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
             }
         }
-    } else if (warp == 12 || warp == 13) {
-        // ------------------------------------------ scale copiers (leader) --
-        if (leader && lane == 0) {
-            const int which = warp - 12;
-            const uint32_t t_sf = tmem + NACC * BN;
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int i = 0; i < total_stages; ++i) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status))
+    } else if (warp >= 12) {
+        // ------------------------------------------- scale writers (each CTA) --
+        const int quarter = warp & 3;
+        const uint32_t t_q = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + NACC * BN;
+        const uint32_t lead_ready = map_to_rank(smem_addr(&sf_ready[0]), lead);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < total_stages; ++i) {
+            bool ok = mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            if (PC::SF_SLOTS < STAGES && i >= PC::SF_SLOTS) {
+                // The slot's previous reader: the MMAs of stage i - SF_SLOTS.
+                const int j = i - PC::SF_SLOTS;
+                ok = mbar_wait(&empty[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u, abort_flag,
+                               a.wait_limit, &g_device_status);
+                if (!__all_sync(0xffffffffu, ok))
                     break;
-                if (PC::SF_SLOTS < STAGES && i >= PC::SF_SLOTS) {
-                    // The slot's previous reader: the MMAs of stage i - SF_SLOTS.
-                    const int j = i - PC::SF_SLOTS;
-                    if (!mbar_wait(&empty[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u,
-                                   abort_flag, a.wait_limit, &g_device_status))
-                        break;
-                }
-                tc_fence_after();
-                const uint32_t sfa_t = t_sf + (i % PC::SF_SLOTS) * PC::SF_COLS;
-                const uint32_t sfb_t = sfa_t + PC::SF_COLS_A;
-                const uint32_t sfa_s = smem_addr(smem + stage * PC::STAGE_BYTES + PC::A_BYTES + PC::B_BYTES);
-                const uint32_t sfb_s = sfa_s + PC::SFA_BYTES;
-                // Copy c: c < GROUPS -> scale-A k-group c; else scale-B atom
-                // (k-group g, row block rb; in shared memory at rb*GROUPS + g)
-                // -> columns g*4*SFB_RB + rb*4.
+            }
+            // Line `lane` of every atom of the stage: scale-A k-groups 0, 1
+            // (columns 0-7); scale-B (k-group g, row block rb; in shared
+            // memory at rb*GROUPS + g) -> columns 8 + g*4*SFB_RB + rb*4.
+            const uint8_t *sf_s = smem + stage * PC::STAGE_BYTES + PC::A_BYTES + PC::B_BYTES;
+            uint32_t wa[4 * PC::GROUPS];
+            uint32_t wb[4 * PC::GROUPS * PC::SFB_RB];
 #pragma unroll
-                for (int c = 0; c < PC::SF_COPIES; ++c) {
-                    if ((c & 1) != which)
-                        continue;
-                    if (c < PC::GROUPS) {
-                        tmem_cp_32x128b_x4_pair(sfa_t + c * 4, sdesc_sf_block(sfa_s + c * kSfAtomBytes));
-                    } else {
-                        const int g = (c - PC::GROUPS) / PC::SFB_RB;
-                        const int rb = (c - PC::GROUPS) % PC::SFB_RB;
-                        tmem_cp_32x128b_x4_pair(
-                            sfb_t + g * 4 * PC::SFB_RB + rb * 4,
-                            sdesc_sf_block(sfb_s + (rb * PC::GROUPS + g) * kSfAtomBytes));
-                    }
-                }
-                mma_commit_pair(&sf_ready[stage], static_cast<uint16_t>(1u << lead));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+            for (int g = 0; g < PC::GROUPS; ++g) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(sf_s + g * kSfAtomBytes + 16 * lane);
+                wa[4 * g] = v.x;
+                wa[4 * g + 1] = v.y;
+                wa[4 * g + 2] = v.z;
+                wa[4 * g + 3] = v.w;
+#pragma unroll
+                for (int rb = 0; rb < PC::SFB_RB; ++rb) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(
+                        sf_s + PC::SFA_BYTES + (rb * PC::GROUPS + g) * kSfAtomBytes + 16 * lane);
+                    const int o = (g * PC::SFB_RB + rb) * 4;
+                    wb[o] = u.x;
+                    wb[o + 1] = u.y;
+                    wb[o + 2] = u.z;
+                    wb[o + 3] = u.w;
                 }
             }
-            if (*abort_flag) {
-                mma_commit_pair(&drain[1 + which], static_cast<uint16_t>(1u << lead));
-                mbar_wait_drain(&drain[1 + which], 0, a.wait_limit);
+            const uint32_t slot = t_q + (i % PC::SF_SLOTS) * PC::SF_COLS;
+            tmem_st_32x32b_x8(slot, wa);
+            tmem_st_32x32b_x16(slot + PC::SF_COLS_A, wb);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&sf_ready[stage]);
+                else
+                    mbar_arrive_cluster_relaxed(lead_ready + static_cast<uint32_t>(stage * sizeof(uint64_t)));
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
             }
         }
     } else if (warp == 5) {

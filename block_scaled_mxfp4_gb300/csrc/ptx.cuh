@@ -515,6 +515,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// 3-D tiled bulk-tensor load into this CTA's shared memory, completing on a
+// barrier of this CTA (x innermost).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
+                                            int y, int z, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
 // 3-D form of tma_load_2d_pair (x innermost).
 __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t cbar,
                                                  int x, int y, int z, uint64_t policy)

@@ -125,6 +125,8 @@ def parse_args():
                     help="step = scale relayout A + B kernels + GEMM on relaid scales")
     ap.add_argument("--no-hbm-bound", action="store_true",
                     help="skip the decode / skinny sub-benchmarks of the default run")
+    ap.add_argument("--sustained-s", type=float, default=1.2,
+                    help="seconds of the sustained GEMM-alone loop (0: skip it)")
     ap.add_argument("--profile-shape", default=None,
                     help="M,N,K: run a few GEMMs of a random shape for a profiler, no timing")
     ap.add_argument("--calls", type=int, default=3, help="--profile-shape: GEMM calls")
@@ -886,16 +888,16 @@ def run_mxfp4(args, world, rank, local_rank):
     # a loop of at least a second (against the sustained peak) so that the
     # clock sampler sees the GPU under sustained load.
     per = tot_ms / args.steps
-    n_sus = max(args.steps, int(1200.0 / max(per, 1e-3)))
+    n_sus = max(1, int(args.sustained_s * 1e3 / max(per, 1e-3))) if args.sustained_s > 0 else 0
     if gemm_alone:
         n_alone = args.steps
         gemm_avg = timed_back_to_back(stream, n_alone, gemm_kernel, dist, dev) / n_alone
-        sus_tot = timed_back_to_back(stream, n_sus, gemm_kernel, dist, dev)
+        sus_tot = timed_back_to_back(stream, n_sus, gemm_kernel, dist, dev) if n_sus else 0.0
     else:
         n_alone = 0
         gemm_avg = tot_ms / args.steps
-        sus_tot = timed_back_to_back(stream, n_sus, step, dist, dev)
-    sus_avg = sus_tot / n_sus
+        sus_tot = timed_back_to_back(stream, n_sus, step, dist, dev) if n_sus else 0.0
+    sus_avg = sus_tot / n_sus if n_sus else gemm_avg
     gemm_tot = sus_tot
     clocks = sampler.stop()
     tot_ms, gemm_avg, sus_avg = max_over_ranks([tot_ms, gemm_avg, sus_avg], dist, dev)
@@ -948,7 +950,7 @@ def run_mxfp4(args, world, rank, local_rank):
         roof = {"bound": "hbm", "achieved": algo_bytes / (gemm_avg * 1e-3) / 1e9, "peak": peak,
                 "unit": "GB/s", "peak_source": f"{peak_src} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    if roof["bound"] == "tensor":
+    if roof["bound"] == "tensor" and n_sus:
         sus_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
         sus_ach = flops / (sus_avg * 1e-3) / 1e12
         roof["sustained"] = {

@@ -338,8 +338,9 @@ __device__ __forceinline__ void reduce_tile(const GemmArgs &a, int64_t tile, int
 // [r * R, (r + 1) * R), R = ceil(128 / split), over ranks 0, 1, ..., split-1
 // in that order, four columns per item, then applies alpha / beta with C
 // and rounds once (swap: the rows are n, the columns m).  Consecutive
-// threads take consecutive rows (swap: consecutive n of a D row) or
-// consecutive column chunks of a row (no swap).
+// threads take consecutive 4-column chunks of a row, so a warp reads whole
+// runs of each peer's partial row (distributed shared memory serves scattered
+// 16-byte reads of many rows far more slowly).
 template <bool SWAP>
 __device__ __forceinline__ void reduce_tile_cluster(const GemmArgs &a, uint32_t part_smem, int stride,
                                                     int p0, int q0, int t)
@@ -366,8 +367,8 @@ __device__ __forceinline__ void reduce_tile_cluster(const GemmArgs &a, uint32_t 
             cnt[u] = 0;
             if (it >= items)
                 continue;
-            const int k = SWAP ? it % nrows : it / nch;
-            const int ch = SWAP ? it / nrows : it % nch;
+            const int k = it / nch;
+            const int ch = it % nch;
             const int row = r0 + k;
             cnt[u] = min(4, qvalid - 4 * ch);
             const uint32_t off = part_smem + static_cast<uint32_t>((row * stride + 4 * ch) * 4);

@@ -104,8 +104,11 @@ def recorded_traffic(workload, kernel, plan=None):
 def split_note(plan):
     if plan.split_k <= 1:
         return ""
+    if plan.split_k <= 8:
+        return (f" (K split {plan.split_k} ways; the splits of a tile form one cluster and sum "
+                "their partials in split order over distributed shared memory)")
     return (f" (K split {plan.split_k} ways; the CTA that finishes a tile last sums its "
-            "partials in split order)")
+            "partials from the workspace in split order)")
 
 
 def parse_args():
@@ -123,6 +126,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prepacked", action="store_true",
                     help="step = scale relayout A + B kernels + GEMM on relaid scales")
+    ap.add_argument("--hbm-steps", type=int, default=0,
+                    help="calls per timed loop of the decode / skinny sub-benchmarks "
+                         "(default: max(steps, 1000))")
     ap.add_argument("--no-hbm-bound", action="store_true",
                     help="skip the decode / skinny sub-benchmarks of the default run")
     ap.add_argument("--sustained-s", type=float, default=1.2,
@@ -737,7 +743,8 @@ def hbm_bound_run(name, steps, dev, stream, peaks, peak_src, dist=None):
         res[key] = {"us_per_gemm": ms * 1e3, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                                 "peak_source": f"{peak_src} HBM copy bandwidth"}}
+                                 "peak_source": f"{peak_src} HBM copy bandwidth",
+                                 "traffic": recorded_traffic(name, "gemm_mxf4_kernel", plan)}}
     res["b_static"]["api"] = ("mxfp4_gemm_ex(..., MXFP4_FLAG_B_STATIC): B and its scales are "
                               "loaded without the in-kernel wait on the previous call")
     res["default"]["api"] = "mxfp4_gemm"
@@ -931,7 +938,8 @@ def run_mxfp4(args, world, rank, local_rank):
     if args.workload == "large" and not args.no_hbm_bound and not args.prepacked:
         del ops, sfa, sfb
         torch.cuda.empty_cache()
-        hbm = {w: hbm_bound_run(w, max(args.steps, 1000), dev, stream, peaks, peak_src, dist)
+        hbm_steps = args.hbm_steps if args.hbm_steps > 0 else max(args.steps, 1000)
+        hbm = {w: hbm_bound_run(w, hbm_steps, dev, stream, peaks, peak_src, dist)
                for w in ("decode", "skinny")}
 
     if rank != 0:

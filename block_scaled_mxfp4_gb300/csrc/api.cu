@@ -405,8 +405,8 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.ab_early = after_relayout ? 1 : 0;
         a.wait_limit = g_wait_limit.load();
         const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
-        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB,
-                             after_relayout, stream) != cudaSuccess)
+        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB, stream) !=
+            cudaSuccess)
             return MXFP4_ERR_CUDA;
         return MXFP4_OK;
     }

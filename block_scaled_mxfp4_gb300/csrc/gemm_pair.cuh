@@ -1,24 +1,16 @@
 // CTA-pair (2-SM) form of the block-scaled MXFP4 GEMM for large shapes
 // (included by gemm_sm103.cu).
 //
-// A cluster of two CTAs computes one 256 x BN output tile with
+// A cluster of two CTAs computes one 256 x 256 output tile with
 // tcgen05.mma.cta_group::2 (M = 256): CTA r of the pair holds rows
-// [128r, 128r+128) of the tile's A panel and rows [r*BN/2, (r+1)*BN/2) of its
-// B panel (half of N) in its own shared memory, and its own 128 rows x BN
+// [128r, 128r+128) of the tile's A panel and rows [128r, 128r+128) of its B
+// panel (half of N) in its own shared memory, and its own 128 rows x 256
 // columns of the fp32 accumulator in its own tensor memory.  Per 256-K stage
-// each CTA therefore stages 16 KB of A and BN/2 x 128 bytes of B (plus the
-// stage's scale atoms) for 128 x BN x 256 multiply-adds -- against 48 KB for
-// a one-CTA 128 x 256 tile -- so that six or seven stages fit, enough to
-// keep the tensor pipe fed across the TMA round trip.
-//
-// Two shapes are compiled:
-//   BN = 256, one accumulator, 6 stages, one tensor-memory scale slot per
-//       stage;
-//   BN = 192, two accumulators (2 x 192 columns), 7 stages and five scale
-//       slots (the rest of the 512 tensor-memory columns): the MMAs of a tile
-//       run while the epilogue drains the previous one, instead of waiting
-//       for it.  A 192-row B tile starts 0 or 64 rows into a 128-row scale
-//       block, so its scale-B base column is offset by 0 or 2.
+// each CTA therefore stages 16 KB of A and 16 KB of B (plus the stage's scale
+// atoms) for 128 x 256 x 256 multiply-adds -- against 48 KB for a one-CTA
+// 128 x 256 tile -- so that six stages fit, enough to keep the tensor pipe
+// fed across the TMA round trip.  One accumulator (256 of the 512 tensor-
+// memory columns) and one scale slot per stage (6 x 24 columns).
 //
 // Roles (512 threads = 16 warps per CTA):
 //   warps 4, 6, 7 (each CTA)  TMA producers: A half, B half, and the scale
@@ -37,13 +29,13 @@
 //                      warps with a relaxed remote arrive).  tcgen05.st does
 //                      not queue behind the MMAs, unlike tcgen05.cp, so the
 //                      scales of later stages are ready well ahead.
-//   warp 5 (leader)    waits for an accumulator buffer to be free, then per
-//                      stage for sf_ready (8 arrivals: both CTAs' data landed
-//                      and both CTAs' scales written); issues four K=64
-//                      M=256 N=BN MMAs and commits the stage to BOTH CTAs'
-//                      empty barriers, and each tile to both CTAs'
-//                      accumulator-full barriers.
-//   warps 0-3 / 8-11 (each CTA)  epilogue, columns [0, BN/2) / [BN/2, BN):
+//   warp 5 (leader)    waits for the accumulator to be free, then per stage
+//                      for sf_ready (8 arrivals: both CTAs' data landed and
+//                      both CTAs' scales written); issues four K=64 M=256
+//                      N=256 MMAs and commits the stage to BOTH CTAs' empty
+//                      barriers, and each tile to both CTAs' accumulator-full
+//                      barriers.
+//   warps 0-3 / 8-11 (each CTA)  epilogue, columns [0, 128) / [128, 256):
 //                      read the accumulator (warp w owns TMEM lanes
 //                      32(w%4)..+31 = tile rows), release the buffer to the
 //                      leader as soon as the reads are done (8 warps x 2
@@ -52,10 +44,9 @@
 //                      wait for neither the arithmetic nor the stores.
 // Persistent over tiles: pair i takes tiles i, i + pairs, ...  Scales are
 // relaid atoms (a 2-D uint32 view for scale-A, 3-D for scale-B: 128 words =
-// one atom).  A scale slot in tensor memory is rewritten only after the MMAs
-// that read it completed: with a slot per stage that is implied by the
-// stage's full barrier (the producers waited for the stage's previous MMAs);
-// with S slots the copier waits for the empty barrier of the stage S back.
+// one atom).  A stage's scale slot in tensor memory is rewritten only after
+// the MMAs that read it completed: that is implied by the stage's full
+// barrier (the producers waited for the stage's previous MMAs).
 // Launched as a programmatic dependent: right after this library's scale
 // relayout (whose grid waits for the work before it), only the scale loads
 // wait for the preceding grid; otherwise every load, and the epilogue, waits.
@@ -63,8 +54,9 @@
 
 namespace mxfp4 {
 
-template <int STAGES, int BN, int NACC>
+template <int STAGES>
 struct PairCfg {
+    static constexpr int BN = 256;                        // tile N
     static constexpr int B_ROWS = BN / 2;                 // this CTA's rows of the B tile
     static constexpr int GROUPS = 2;                      // scale k-groups (128 K) per stage
     static constexpr int A_BYTES = kTileM * 128;          // 128 rows x 128 bytes (256 K)
@@ -79,28 +71,20 @@ struct PairCfg {
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;
     static constexpr int SF_COLS_A = 4 * GROUPS;          // 4 columns per k-group
     static constexpr int SF_COLS_B = 4 * GROUPS * SFB_RB; // and per 128-row block
-    static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
-    // One scale slot per stage if the accumulators leave room, else as many
-    // as fit in the 512 tensor-memory columns.
-    static constexpr int SF_FIT = (512 - NACC * BN) / SF_COLS;
-    static constexpr int SF_SLOTS = SF_FIT < STAGES ? SF_FIT : STAGES;
-    static constexpr int SF_COPIES = GROUPS + GROUPS * SFB_RB;   // tcgen05.cp per stage
+    static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B; // one scale slot per stage
     static constexpr int HALF = BN / 2;                   // columns per epilogue warp
-    static constexpr int TMEM_USED = NACC * BN + SF_SLOTS * SF_COLS;
+    static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static constexpr int THREADS = 512;
     static constexpr int EPI_WARPS = 8;                   // per CTA
-    static_assert(BN == 256 || BN == 192, "tile N");
-    static_assert(SF_SLOTS >= 2, "scale slots");
-    static_assert(NACC == 1 || NACC == 2, "accumulator buffers");
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    static_assert(HALF % 16 == 0, "epilogue columns");
+    static_assert(HALF == 128, "epilogue columns");
 };
 
 struct PairSched {
-    int tiles_p, tiles_q;   // 256 x BN output tiles
+    int tiles_p, tiles_q;   // 256 x 256 output tiles
     int kt;                 // K stages (256 K each) per tile
     int group;              // raster: groups of `group` tile rows
 };
@@ -193,22 +177,23 @@ __device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n
         out[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 }
 
-template <int STAGES, int BN, int NACC>
-__global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
+template <int STAGES>
+__global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
 {
-    using PC = PairCfg<STAGES, BN, NACC>;
+    using PC = PairCfg<STAGES>;
+    constexpr int BN = PC::BN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + PC::RING_BYTES);   // leader's are used
     uint64_t *empty = full + STAGES;
     uint64_t *sf_ready = empty + STAGES;                                    // leader's are used
-    uint64_t *acc_full = sf_ready + STAGES;                                 // [NACC]
-    uint64_t *acc_empty = acc_full + NACC;                                  // [NACC], leader's used
-    uint64_t *drain = acc_empty + NACC;                                     // [3]: MMA
+    uint64_t *acc_full = sf_ready + STAGES;
+    uint64_t *acc_empty = acc_full + 1;                                     // leader's used
+    uint64_t *drain = acc_empty + 1;                                        // [3]: MMA
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -228,10 +213,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
             mbar_init(&empty[s], 1);         // the pair's MMA commit
             mbar_init(&sf_ready[s], 8);      // the scale writers of both CTAs (leader's used)
         }
-        for (int i = 0; i < NACC; ++i) {
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 2 * PC::EPI_WARPS);
-        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 2 * PC::EPI_WARPS);
         for (int i = 0; i < 3; ++i)
             mbar_init(&drain[i], 1);
         *abort_flag = 0;
@@ -312,7 +295,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
     } else if (warp >= 12) {
         // ------------------------------------------- scale writers (each CTA) --
         const int quarter = warp & 3;
-        const uint32_t t_q = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + NACC * BN;
+        const uint32_t t_q = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + BN;
         const uint32_t lead_ready = map_to_rank(smem_addr(&sf_ready[0]), lead);
         int stage = 0;
         uint32_t phase = 0;
@@ -320,14 +303,6 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
             bool ok = mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status);
             if (!__all_sync(0xffffffffu, ok))
                 break;
-            if (PC::SF_SLOTS < STAGES && i >= PC::SF_SLOTS) {
-                // The slot's previous reader: the MMAs of stage i - SF_SLOTS.
-                const int j = i - PC::SF_SLOTS;
-                ok = mbar_wait(&empty[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u, abort_flag,
-                               a.wait_limit, &g_device_status);
-                if (!__all_sync(0xffffffffu, ok))
-                    break;
-            }
             // Line `lane` of every atom of the stage: scale-A k-groups 0, 1
             // (columns 0-7); scale-B (k-group g, row block rb; in shared
             // memory at rb*GROUPS + g) -> columns 8 + g*4*SFB_RB + rb*4.
@@ -352,7 +327,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
                     wb[o + 3] = u.w;
                 }
             }
-            const uint32_t slot = t_q + (i % PC::SF_SLOTS) * PC::SF_COLS;
+            const uint32_t slot = t_q + stage * PC::SF_COLS;
             tmem_st_32x32b_x8(slot, wa);
             tmem_st_32x32b_x16(slot + PC::SF_COLS_A, wb);
             tmem_st_wait();
@@ -375,22 +350,20 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
         // barrier polls); one elected lane issues each MMA and commit.
         if (leader) {
             const uint32_t idesc = idesc_mxf4(256, BN);
-            const uint32_t t_sf = tmem + NACC * BN;
+            const uint32_t t_sf = tmem + BN;
             int stage = 0;
             uint32_t phase = 0;
-            int slot_i = 0;                 // scale slot of the next stage
-            int acc = 0;
-            uint32_t acc_phase = 0;         // bit b: parity of buffer b's next use
+            uint32_t acc_phase = 0;         // parity of the accumulator's next use
             bool stop = false;
             for (int t = cl; t < tiles && !stop; t += ncl) {
-                if (!mbar_wait(&acc_empty[acc], ((acc_phase >> acc) & 1u) ^ 1u, abort_flag,
-                               a.wait_limit, &g_device_status))
+                if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, a.wait_limit,
+                               &g_device_status))
                     break;
                 tc_fence_after();
                 int pt, qt;
                 pair_tile_coords(ps, t, pt, qt);
                 const uint32_t q_off = static_cast<uint32_t>(((qt * BN) % kSfRowBlock) / 32);
-                const uint32_t d_tmem = tmem + acc * BN;
+                const uint32_t d_tmem = tmem;
                 for (int kt = 0; kt < ps.kt; ++kt) {
                     // sf_ready completes after the copiers observed the
                     // stage's full barrier (all of its bytes landed), so it
@@ -401,7 +374,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = t_sf + slot_i * PC::SF_COLS;
+                    const uint32_t sfa_t = t_sf + stage * PC::SF_COLS;
                     const uint32_t sfb_t = sfa_t + PC::SF_COLS_A + q_off;
                     const uint32_t st = smem_addr(smem + stage * PC::STAGE_BYTES);
                     const uint64_t adesc = sdesc_kmajor_sw128(st);
@@ -422,12 +395,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (++slot_i == PC::SF_SLOTS)
-                        slot_i = 0;
                 }
-                mma_commit_pair_elect(&acc_full[acc], static_cast<uint16_t>(3u));
-                acc_phase ^= 1u << acc;
-                acc = acc + 1 == NACC ? 0 : acc + 1;
+                mma_commit_pair_elect(acc_full, static_cast<uint16_t>(3u));
+                acc_phase ^= 1u;
             }
             if (*abort_flag) {
                 mma_commit_pair_elect(&drain[0], static_cast<uint16_t>(1u << lead));
@@ -443,72 +413,48 @@ __global__ void __launch_bounds__(PairCfg<STAGES, BN, NACC>::THREADS, 1)
         const int half = warp >> 3;
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * PC::HALF;
-        int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = cl; t < tiles; t += ncl) {
-            bool ok = mbar_wait(&acc_full[acc], (acc_phase >> acc) & 1u, abort_flag, a.wait_limit,
-                                &g_device_status);
+            bool ok = mbar_wait(acc_full, acc_phase, abort_flag, a.wait_limit, &g_device_status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
-            acc_phase ^= 1u << acc;
+            acc_phase ^= 1u;
             tc_fence_after();
             int pt, qt;
             pair_tile_coords(ps, t, pt, qt);
             const int m = pt * 256 + static_cast<int>(rank) * kTileM + row;
             const int n0 = qt * BN + half * PC::HALF;
-            const uint32_t t_row = t_lane + acc * BN;
+            const uint32_t t_row = t_lane;
             uint32_t out[PC::HALF / 2];
-            // Once this warp's accumulator cells are read (tcgen05.wait::ld
-            // has returned, so no TMEM read is outstanding) they are released
-            // to the leader.  No memory fence is needed for that, and a
+            // Columns 0-63 are read and rounded; 64-127 are read, the
+            // accumulator released, and only then rounded: the next tile's
+            // MMAs wait for the reads alone, not the arithmetic.  Once this
+            // warp's accumulator cells are read (tcgen05.wait::ld has
+            // returned, so no TMEM read is outstanding) they are released to
+            // the leader.  No memory fence is needed for that, and a
             // cluster-scope release arrive costs ~1000 cycles, so the leader's
             // warps arrive locally and the peer's with a relaxed remote arrive.
-            auto release = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (leader)
-                        mbar_arrive(&acc_empty[acc]);
-                    else
-                        mbar_arrive_cluster_relaxed(map_to_rank(smem_addr(&acc_empty[acc]), lead));
-                }
-            };
-            if constexpr (PC::HALF == 128) {
-                // Columns 0-63 are read and rounded; 64-127 are read, the
-                // accumulator released, and only then rounded: the next
-                // tile's MMAs wait for the reads alone, not the arithmetic.
-                uint32_t r0[32], r1[32];
-                tmem_ld_32x32b_x32(t_row, r0);
-                tmem_ld_32x32b_x32(t_row + 32, r1);
-                tmem_ld_wait(r0, r1);
-                pair_round_chunk<32>(a, m, n0, r0, out);
-                pair_round_chunk<32>(a, m, n0 + 32, r1, out + 16);
-                tmem_ld_32x32b_x32(t_row + 64, r0);
-                tmem_ld_32x32b_x32(t_row + 96, r1);
-                tmem_ld_wait(r0, r1);
-                release();
-                pair_round_chunk<32>(a, m, n0 + 64, r0, out + 32);
-                pair_round_chunk<32>(a, m, n0 + 96, r1, out + 48);
-            } else {
-#pragma unroll
-                for (int c = 0; c + 32 <= PC::HALF; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_row + c, r);
-                    tmem_ld_wait(r);
-                    pair_round_chunk<32>(a, m, n0 + c, r, out + c / 2);
-                }
-                if constexpr (PC::HALF % 32 != 0) {
-                    constexpr int c = PC::HALF - 16;
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(t_row + c, r);
-                    tmem_ld_wait();
-                    pair_round_chunk<16>(a, m, n0 + c, r, out + c / 2);
-                }
-                release();
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(t_row, r0);
+            tmem_ld_32x32b_x32(t_row + 32, r1);
+            tmem_ld_wait(r0, r1);
+            pair_round_chunk<32>(a, m, n0, r0, out);
+            pair_round_chunk<32>(a, m, n0 + 32, r1, out + 16);
+            tmem_ld_32x32b_x32(t_row + 64, r0);
+            tmem_ld_32x32b_x32(t_row + 96, r1);
+            tmem_ld_wait(r0, r1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(acc_empty);
+                else
+                    mbar_arrive_cluster_relaxed(map_to_rank(smem_addr(acc_empty), lead));
             }
+            pair_round_chunk<32>(a, m, n0 + 64, r0, out + 32);
+            pair_round_chunk<32>(a, m, n0 + 96, r1, out + 48);
             pair_store_row<PC::HALF>(a, m, n0, out);
-            acc = acc + 1 == NACC ? 0 : acc + 1;
         }
     }
 

@@ -1143,18 +1143,17 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
     return launch_gemm_fmt<1>(b, tmP, tmQ, tmSP, tmSQ, s, grid, stream);
 }
 
-// The compiled pair configuration: 6 stages, 256 x 256 tiles, one accumulator.
-using PairDefault = PairCfg<6, 256, 1>;
+// The compiled pair configuration: 6 stages of 256 K, 256 x 256 tiles.
+using PairDefault = PairCfg<6>;
 
 size_t gemm_pair_smem_bytes() { return PairDefault::SMEM_BYTES; }
 
 cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
                              const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
-                             cudaStream_t stream)
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream)
 {
     using PC = PairDefault;
-    auto kern = gemm_mxf4_pair<6, 256, 1>;
+    auto kern = gemm_mxf4_pair<6>;
     static std::atomic<int> max_clusters[64];   // per device; 0 = not yet queried
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1191,15 +1190,14 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
     if (clusters <= 0)
         return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2));
-    if (after_relayout) {
-        // Right after this library's scale relayout: programmatic stream
-        // serialisation lets the GEMM's prologue and operand loads overlap
-        // the relayout; only the scale producers wait for it
-        // (griddepcontrol.wait).
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
-        cfg.numAttrs = 2;
-    }
+    // A programmatic dependent of the preceding work: the prologue overlaps
+    // it, and every role waits for it (griddepcontrol.wait) before touching
+    // memory it may write.  Right after this library's scale relayout
+    // (a.ab_early) only the scale loads and the epilogue wait: the relayout
+    // itself waited for the work before it.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     PairSched ps;
     ps.tiles_p = tiles_p;
     ps.tiles_q = tiles_q;

@@ -94,14 +94,13 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
 
 // CTA-pair kernel (relaid scales): grid of up to `ctas` CTAs in clusters of
 // two (clamped to the clusters the GPU holds at once), persistent over 256 x
-// 256 tiles.  after_relayout: launched right after this library's scale
-// relayout on the same stream (programmatic dependent launch; only the scale
-// loads wait for it).
+// 256 tiles, launched as a programmatic dependent of the preceding work.
+// a.ab_early: that work is this library's scale relayout, so only the scale
+// loads and the epilogue wait for it.
 size_t gemm_pair_smem_bytes();
 cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
                              const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool after_relayout,
-                             cudaStream_t stream);
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream);
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
                                   cudaStream_t stream);

@@ -32,12 +32,14 @@
  *     the kernel returns instead of hanging.
  *   - Only sm_103 devices are accepted (MXFP4_ERR_ARCH otherwise).
  *   - Functions are safe to call from several host threads.
- *   - Every enqueueing call can be captured into a CUDA graph (stream
- *     capture), including its dependent, cluster and split-K launches and
- *     the host-buffer entry's internal copy streams, which fork from and
- *     join back to `stream`.  The first call on a device sets kernel
- *     attributes and creates those streams: make it before capturing.  A
- *     replay reads the buffers' contents at replay time.
+ *   - mxfp4_gemm, mxfp4_gemm_ex, mxfp4_gemm_prepacked, mxfp4_gemm_host,
+ *     the mxfp8_gemm family, the quantisers and the scale relayout can be
+ *     captured into a CUDA graph (stream capture), including their
+ *     dependent, cluster and split-K launches and the host-buffer entries'
+ *     internal copy streams, which fork from and join back to `stream`.  The
+ *     first call on a device sets kernel attributes and creates those
+ *     streams: make it before capturing.  A replay reads the buffers'
+ *     contents at replay time.
  */
 #ifndef MXFP4_GEMM_H
 #define MXFP4_GEMM_H

@@ -609,33 +609,40 @@ def _gemm_call(dev, D, ws, wsb, split, stream):
                   stream)
 
 
-@pytest.mark.parametrize("case", ["decode", "mid", "pair"])
+@pytest.mark.parametrize("case", ["decode", "mid", "pair", "split16"])
 def test_cuda_graph_capture_and_replay(case):
     """mxfp4_gemm captured into a CUDA graph (dependent launches, cluster
-    launches and split-K reduce included) replays to the eager result, and
-    reads its inputs at replay time."""
+    launches and both split-K reductions included) replays to the eager
+    result, and reads its inputs at replay time.  split16 keeps its partials
+    and per-tile counters in the workspace: the replays show that each call
+    leaves the counters ready for the next one."""
+    split = 0
     if case == "pair":
         p = inputs.make_problem("gpair", 2048, 4096, 2048, 41, "normal", 1.0, 0.0, None)
         assert mx.mxfp4_plan_gemm(p.M, p.N, p.K, 0, 0).pair == 1
+    elif case == "split16":
+        p = problem("decode")
+        split = 16
+        assert mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, split) > 0
     else:
         p = problem(case)
     dev = Dev(p)
-    split = 0
     wsb = mx.mxfp4_gemm_workspace_size(p.M, p.N, p.K, split)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
     D = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
-    ref = run_gemm(dev)                                   # eager; also the first-use setup
+    ref = run_gemm(dev, split_k=split)                    # eager; also the first-use setup
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         _gemm_call(dev, D, ws, wsb, split, s)
-    D.fill_(float("nan"))
-    g.replay()
-    torch.cuda.synchronize()
-    assert np.array_equal(d_to_bits(D), ref)
+    for _ in range(3):
+        D.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(d_to_bits(D), ref)
     # New B values, same buffers: the replay sees them.
     dev.B.copy_(torch.roll(dev.B, 1, 0))
-    ref2 = run_gemm(dev)
+    ref2 = run_gemm(dev, split_k=split)
     D.fill_(float("nan"))
     g.replay()
     torch.cuda.synchronize()

@@ -185,6 +185,23 @@ def workload(name: str) -> Problem:
     return make_problem(name, M, N, K, seed, values, alpha, beta, c_sigma)
 
 
+def make_problem_nv(name: str, M: int, N: int, K: int, seed: int, alpha: float, beta: float,
+                    c_sigma: Optional[float], scale_lo: int = 0x28,
+                    scale_hi: int = 0x48) -> Problem:
+    """An NVFP4 problem: packed E2M1 codes drawn uniformly from all 16, and
+    one UE4M3 scale byte per 16 K drawn uniformly from [scale_lo, scale_hi]
+    (the default 0x28..0x48 spans 0.25 .. 4); SA and SB are [rows, K/16]."""
+    if K % 32 != 0:
+        raise ValueError("K must be a multiple of 32")
+    rng = np.random.default_rng(seed)
+    A = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    SA = rng.integers(scale_lo, scale_hi + 1, size=(M, K // 16)).astype(np.uint8)
+    SB = rng.integers(scale_lo, scale_hi + 1, size=(N, K // 16)).astype(np.uint8)
+    C = _bf16_normal(rng, M, N, c_sigma) if c_sigma is not None else None
+    return Problem(name, M, N, K, A, B, SA, SB, C, float(alpha), float(beta), seed)
+
+
 def identity_problem(M: int = 128, N: int = 256, K: int = 512, seed: int = 0) -> Problem:
     """B[n, k] = 1 iff n == k (code 2, scale code 127); A as in 'tiny'.
 

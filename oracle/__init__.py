@@ -20,6 +20,10 @@ objects", sections "Data layouts" and "Verification"):
 ``gemm8`` / ``gemm8_sampled`` take 8-bit (E4M3, E5M2) or 6-bit (E2M3, E3M2)
 elements with the same scales.
 
+``gemm_nv`` / ``gemm_nv_sampled`` take the same packed E2M1 operands with
+one unsigned-E4M3 (UE4M3) scale per 16 K elements (NVFP4), and
+``dequant_nv`` + ``acc_numpy_nv`` are its numpy counterpart.
+
 ``quantize`` is the oracle of the MXFP4 quantiser (bf16 rows -> packed E2M1
 codes + E8M0 scales) that produces the GEMM's operands.
 """
@@ -105,6 +109,12 @@ def bind(path: str) -> ctypes.CDLL:
                                    u8p, i64]
     L.oracle_quantize.restype = ctypes.c_int
     L.oracle_quantize.argtypes = [ctypes.c_int, ctypes.c_int, u16p, i64, u8p, i64, u8p, i64]
+    L.oracle_ue4m3_value.restype = ctypes.c_double
+    L.oracle_ue4m3_value.argtypes = [ctypes.c_uint]
+    L.oracle_gemm_nv.restype = i64
+    L.oracle_gemm_nv.argtypes = L.oracle_gemm.argtypes
+    L.oracle_gemm_nv_sampled.restype = i64
+    L.oracle_gemm_nv_sampled.argtypes = L.oracle_gemm_sampled.argtypes
     return L
 
 
@@ -138,6 +148,12 @@ E4M3, E5M2, E2M3, E3M2, E2M1P = 1, 2, 3, 4, 5
 def fp8_value(code: int, fmt: int) -> float:
     """Value of an 8-bit E4M3 (fmt 1) or E5M2 (fmt 2) element code."""
     return lib().oracle_fp8_value(int(code), int(fmt))
+
+
+def ue4m3_value(code: int) -> float:
+    """Value of an NVFP4 block-scale byte (unsigned E4M3; NaN for 0x7F and
+    for bytes with bit 7 set, which are not UE4M3 codes)."""
+    return lib().oracle_ue4m3_value(int(code))
 
 
 def fp6_value(code: int, fmt: int) -> float:
@@ -231,6 +247,59 @@ def gemm_sampled(A, B, SA, SB, M, N, K, pairs, alpha=1.0, beta=0.0, C=None,
     return D, acc, sabs, int(r)
 
 
+def _check_operands_nv(A, B, SA, SB, M, N, K):
+    for name, arr, rows, cols in (("A", A, M, K // 2), ("B", B, N, K // 2),
+                                  ("SA", SA, M, K // 16), ("SB", SB, N, K // 16)):
+        if arr.dtype != np.uint8 or arr.ndim != 2 or arr.shape[0] < rows or arr.shape[1] < cols:
+            raise ValueError(f"{name}: bad shape {arr.shape} / dtype {arr.dtype}")
+
+
+def gemm_nv(A, B, SA, SB, M, N, K, alpha=1.0, beta=0.0, C=None, want_acc=False, nthreads=0):
+    """Full NVFP4 oracle GEMM (packed E2M1 A, B; UE4M3 scales [rows, K/16]).
+    Returns (D bf16 bits [M,N], acc or None, sum|ab| [M,N], inexact)."""
+    A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
+    _check_operands_nv(A, B, SA, SB, M, N, K)
+    Cc = None if beta == 0.0 or C is None else np.ascontiguousarray(C, dtype=np.uint16)
+    D = np.zeros((M, N), dtype=np.uint16)
+    acc = np.zeros((M, N), dtype=np.float64) if want_acc else None
+    sabs = np.zeros((M, N), dtype=np.float64)
+    r = lib().oracle_gemm_nv(M, N, K, _ptr(A, ctypes.c_uint8), A.shape[1] * 2,
+                             _ptr(B, ctypes.c_uint8), B.shape[1] * 2,
+                             _ptr(SA, ctypes.c_uint8), SA.shape[1],
+                             _ptr(SB, ctypes.c_uint8), SB.shape[1],
+                             float(alpha), float(beta), _ptr(Cc, ctypes.c_uint16),
+                             0 if Cc is None else Cc.shape[1],
+                             _ptr(D, ctypes.c_uint16), N, _ptr(acc, ctypes.c_double),
+                             _ptr(sabs, ctypes.c_double), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_gemm_nv rejected its arguments")
+    return D, acc, sabs, int(r)
+
+
+def gemm_nv_sampled(A, B, SA, SB, M, N, K, pairs, alpha=1.0, beta=0.0, C=None, nthreads=0):
+    """NVFP4 oracle at (m, n) pairs [P, 2]. Returns (D bits [P], acc [P], sum|ab| [P], inexact)."""
+    A, B, SA, SB = (np.ascontiguousarray(x) for x in (A, B, SA, SB))
+    _check_operands_nv(A, B, SA, SB, M, N, K)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    Cc = None if beta == 0.0 or C is None else np.ascontiguousarray(C, dtype=np.uint16)
+    P = pairs.shape[0]
+    D = np.zeros(P, dtype=np.uint16)
+    acc = np.zeros(P, dtype=np.float64)
+    sabs = np.zeros(P, dtype=np.float64)
+    r = lib().oracle_gemm_nv_sampled(M, N, K, _ptr(A, ctypes.c_uint8), A.shape[1] * 2,
+                                     _ptr(B, ctypes.c_uint8), B.shape[1] * 2,
+                                     _ptr(SA, ctypes.c_uint8), SA.shape[1],
+                                     _ptr(SB, ctypes.c_uint8), SB.shape[1],
+                                     float(alpha), float(beta), _ptr(Cc, ctypes.c_uint16),
+                                     0 if Cc is None else Cc.shape[1],
+                                     pairs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), P,
+                                     _ptr(D, ctypes.c_uint16), _ptr(acc, ctypes.c_double),
+                                     _ptr(sabs, ctypes.c_double), int(nthreads))
+    if r < 0:
+        raise ValueError("oracle_gemm_nv_sampled rejected its arguments")
+    return D, acc, sabs, int(r)
+
+
 def _check_operands8(A, B, SA, SB, M, N, K, fmt_a, fmt_b):
     fmts = (E4M3, E5M2, E2M3, E3M2, E2M1P)
     if fmt_a not in fmts or fmt_b not in fmts:
@@ -312,6 +381,34 @@ def dequant(packed: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
 def acc_numpy(A, B, SA, SB, K) -> np.ndarray:
     """sum_k a(m,k) b(n,k) as one float64 matmul of the dequantised operands."""
     return dequant(A, SA, K) @ dequant(B, SB, K).T
+
+
+def ue4m3_table() -> np.ndarray:
+    """float64 [256]: UE4M3 byte -> value from its bit fields (exponent bits
+    6..3, bias 7, mantissa bits 2..0; exponent 0 subnormal); 0x7F and every
+    byte with bit 7 set -> NaN."""
+    c = np.arange(256)
+    e = (c >> 3) & 15
+    m = c & 7
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    return np.where((c >= 0x7F), np.nan, v)
+
+
+def dequant_nv(packed: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
+    """float64 [rows, K] values: E2M1 value list x the UE4M3 scale of each 1x16 block."""
+    packed = np.asarray(packed, dtype=np.uint8)[:, : K // 2]
+    codes = np.empty((packed.shape[0], K), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    mag = _E2M1_LIST[codes & 7]
+    val = np.where(codes & 8, -mag, mag)
+    sc = ue4m3_table()[np.asarray(scales, dtype=np.uint8)[:, : K // 16]]
+    return val * np.repeat(sc, 16, axis=1)
+
+
+def acc_numpy_nv(A, B, SA, SB, K) -> np.ndarray:
+    """NVFP4 sum_k a(m,k) b(n,k) as one float64 matmul of the dequantised operands."""
+    return dequant_nv(A, SA, K) @ dequant_nv(B, SB, K).T
 
 
 def quantize(X_bits, rows, K):

@@ -39,6 +39,12 @@
  * the MFMA page).  A product's granule is 2^(qa + qb + ea + eb - 254), where
  * qa, qb are the elements' ulp exponents, and the same 2^52 bound applies.
  *
+ * NVFP4 form (oracle_gemm_nv): packed E2M1 elements as in MXFP4 with one
+ * UE4M3 scale per 16 K (oracle_ue4m3_value_q).  The pages do not cover this
+ * format; it follows the E4M3 encoding already read for MXFP8 elements.  A
+ * product's granule is 2^(qa + qb + sa_q + sb_q) with the scales' ulp
+ * exponents, under the same 2^52 bound.
+ *
  * Readings where the pages are silent or at odds:
  *   - E8M0 code 0: the page writes both 2^(e-127) and "0 -> 2^-126"; the
  *     formula is taken (code 0 -> 2^-127).  Code 255 decodes to NaN.
@@ -116,6 +122,31 @@ double oracle_fp8_value_q(unsigned code, int fmt, int *ulp_exp)
 double oracle_fp8_value(unsigned code, int fmt)
 {
     return oracle_fp8_value_q(code, fmt, NULL);
+}
+
+/*
+ * NVFP4 block scales (a member of the block-scaled family beyond the pages:
+ * packed E2M1 elements as in the MXFP4 GEMM, one scale per 16 consecutive K
+ * elements instead of 32).  The scale byte is unsigned E4M3 ("UE4M3"): the
+ * E4M3 encoding of the MXFP8 elements above with the sign bit 0, so
+ * (1 + m/8) * 2^(e-7), exponent field 0 subnormal (m/8) * 2^-6, and 0x7F
+ * NaN.  A byte with bit 7 set is not a UE4M3 code: NaN here, and the GEMM
+ * entry points below reject it.  *ulp_exp as for oracle_fp8_value_q.
+ */
+double oracle_ue4m3_value_q(unsigned code, int *ulp_exp)
+{
+    code &= 0xFFu;
+    if (code & 0x80u) {
+        if (ulp_exp)
+            *ulp_exp = 0;
+        return NAN;
+    }
+    return oracle_fp8_value_q(code, 1, ulp_exp);
+}
+
+double oracle_ue4m3_value(unsigned code)
+{
+    return oracle_ue4m3_value_q(code, NULL);
 }
 
 /*
@@ -265,6 +296,7 @@ struct gemm_job {
     int fmt_a, fmt_b;  /* 0: E2M1 packed two per byte; 1: E4M3, 2: E5M2 bytes;
                           3: E2M3, 4: E3M2, 5: E2M1 in the padded
                           16-per-16-bytes forms */
+    int nv;            /* 1: UE4M3 scales, one per 16 K (NVFP4); 0: E8M0 per 32 */
     const uint8_t *A; int64_t lda_bytes;
     const uint8_t *B; int64_t ldb_bytes;
     const uint8_t *SA; int64_t ldsa;
@@ -302,6 +334,18 @@ static int one_output(struct gemm_job *j, int m, int n, uint16_t *d,
             vb = oracle_e2m1_value(nibble(brow, k));
         else
             vb = byte_form_value(brow, k, j->fmt_b, &qb);
+        if (j->nv) {
+            /* Step 3, NVFP4: the scale of the 16-element block holding k. */
+            int sa_q, sb_q;
+            double an = va * oracle_ue4m3_value_q(sarow[k / 16], &sa_q);
+            double bn = vb * oracle_ue4m3_value_q(sbrow[k / 16], &sb_q);
+            double pn = an * bn;
+            acc += pn;
+            sabs += fabs(pn);
+            if (pn != 0.0 && qa + qb + sa_q + sb_q < min_g)
+                min_g = qa + qb + sa_q + sb_q;
+            continue;
+        }
         unsigned ea = sarow[k / 32], eb = sbrow[k / 32];
         double a = va * oracle_e8m0_value(ea);
         double b = vb * oracle_e8m0_value(eb);
@@ -456,6 +500,74 @@ int64_t oracle_gemm_sampled(int M, int N, int K,
     struct gemm_job j;
     memset(&j, 0, sizeof(j));
     j.M = M; j.N = N; j.K = K;
+    j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;
+    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
+    j.D = D; j.ldd = 0; j.acc_out = acc_out; j.abs_out = abs_out;
+    j.pairs = pairs; j.npairs = npairs;
+    return run(&j, nthreads);
+}
+
+/*
+ * NVFP4 forms of oracle_gemm / oracle_gemm_sampled: A and B as there (packed
+ * E2M1, lda / ldb in elements), SA / SB one UE4M3 byte per 16 K (row strides
+ * in bytes, at least K / 16).  K % 32 == 0 as for the MXFP4 GEMM.  Returns -1
+ * for bad arguments, including a scale byte with bit 7 set.
+ */
+static int nv_args_ok(int M, int N, int K, int64_t lda, int64_t ldb,
+                      const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                      double beta, const uint16_t *C)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || (lda & 1) || (ldb & 1))
+        return 0;
+    if (ldsa < K / 16 || ldsb < K / 16 || (beta != 0.0 && C == NULL))
+        return 0;
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t b = 0; b < K / 16; ++b)
+            if (SA[r * ldsa + b] & 0x80u)
+                return 0;
+    for (int64_t r = 0; r < N; ++r)
+        for (int64_t b = 0; b < K / 16; ++b)
+            if (SB[r * ldsb + b] & 0x80u)
+                return 0;
+    return 1;
+}
+
+int64_t oracle_gemm_nv(int M, int N, int K,
+                       const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                       const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                       double alpha, double beta, const uint16_t *C, int64_t ldc,
+                       uint16_t *D, int64_t ldd, double *acc_out, double *abs_out,
+                       int nthreads)
+{
+    if (!nv_args_ok(M, N, K, lda, ldb, SA, ldsa, SB, ldsb, beta, C))
+        return -1;
+    struct gemm_job j;
+    memset(&j, 0, sizeof(j));
+    j.M = M; j.N = N; j.K = K; j.nv = 1;
+    j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;
+    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
+    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;
+    j.D = D; j.ldd = ldd; j.acc_out = acc_out; j.abs_out = abs_out;
+    return run(&j, nthreads);
+}
+
+int64_t oracle_gemm_nv_sampled(int M, int N, int K,
+                               const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                               const uint8_t *SA, int64_t ldsa, const uint8_t *SB, int64_t ldsb,
+                               double alpha, double beta, const uint16_t *C, int64_t ldc,
+                               const int64_t *pairs, int64_t npairs,
+                               uint16_t *D, double *acc_out, double *abs_out, int nthreads)
+{
+    if (!nv_args_ok(M, N, K, lda, ldb, SA, ldsa, SB, ldsb, beta, C))
+        return -1;
+    for (int64_t i = 0; i < npairs; ++i)
+        if (pairs[2 * i] < 0 || pairs[2 * i] >= M || pairs[2 * i + 1] < 0 ||
+            pairs[2 * i + 1] >= N)
+            return -1;
+    struct gemm_job j;
+    memset(&j, 0, sizeof(j));
+    j.M = M; j.N = N; j.K = K; j.nv = 1;
     j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;
     j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;
     j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;

@@ -116,6 +116,24 @@ MUTANTS = {
     "quant8_amax_half_block": (
         "for (int i = 0; i < 32; ++i)\n                amax = fmax(",
         "for (int i = 0; i < 16; ++i)\n                amax = fmax("),
+    "nv_scale_block_32": (
+        "double an = va * oracle_ue4m3_value_q(sarow[k / 16], &sa_q);",
+        "double an = va * oracle_ue4m3_value_q(sarow[k / 32], &sa_q);"),
+    "nv_b_scale_from_a": (
+        "double bn = vb * oracle_ue4m3_value_q(sbrow[k / 16], &sb_q);",
+        "double bn = vb * oracle_ue4m3_value_q(sarow[k / 16], &sb_q);"),
+    "nv_scale_read_as_e8m0": (
+        "    return oracle_fp8_value_q(code, 1, ulp_exp);\n}",
+        "    if (ulp_exp)\n        *ulp_exp = 0;\n    return oracle_e8m0_value(code);\n}"),
+    "nv_sign_bit_accepted": (
+        "    if (code & 0x80u) {\n        if (ulp_exp)",
+        "    if (code & 0x100u) {\n        if (ulp_exp)"),
+    "nv_granule_without_scales": (
+        "                min_g = qa + qb + sa_q + sb_q;",
+        "                min_g = qa + qb;"),
+    "nv_beta_dropped_only_for_nv": (
+        "    j.M = M; j.N = N; j.K = K; j.nv = 1;\n    j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;\n    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;\n    j.alpha = alpha; j.beta = beta; j.C = C; j.ldc = ldc;\n    j.D = D; j.ldd = ldd;",
+        "    j.M = M; j.N = N; j.K = K; j.nv = 1;\n    j.A = A; j.lda_bytes = lda / 2; j.B = B; j.ldb_bytes = ldb / 2;\n    j.SA = SA; j.ldsa = ldsa; j.SB = SB; j.ldsb = ldsb;\n    j.alpha = alpha; j.beta = 0.0; j.C = C; j.ldc = ldc;\n    j.D = D; j.ldd = ldd;"),
     "transposed_d_store": (
         "if (!one_output(j, m, n, &j->D[(int64_t)m * j->ldd + n],",
         "if (!one_output(j, m, n, &j->D[(int64_t)(n % j->M) * j->ldd + (m % j->N)],"),

@@ -1004,6 +1004,148 @@ def check_quant_sub_matches_generator(o):
         assert np.array_equal(Qo, Qg), name
 
 
+# --- NVFP4: packed E2M1 with one unsigned-E4M3 scale per 16 K -----------
+
+def ue4m3_fraction(code):
+    """Exact value of a UE4M3 scale byte from its fields (test side): the
+    E4M3 field decoder above with the sign bit 0.  None for 0x7F (NaN) and
+    for bytes with bit 7 set (not UE4M3 codes)."""
+    if code & 0x80:
+        return None
+    return fp8_fraction(code, 1)
+
+
+def random_case_nv(rng, M, N, K):
+    """All 16 E2M1 codes; scales from 2^-3 to 2^3 with some zeros and
+    subnormals (codes 0x01-0x07); C with exponents 2^-8 .. 2^8."""
+    A = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+
+    def scales(rows):
+        c = rng.integers(0x20, 0x51, size=(rows, K // 16))
+        kind = rng.random((rows, K // 16))
+        c = np.where(kind < 0.05, 0, c)
+        c = np.where((kind >= 0.05) & (kind < 0.12), rng.integers(1, 8, size=c.shape), c)
+        return c.astype(np.uint8)
+    e = rng.integers(119, 136, size=(M, N)).astype(np.uint16)
+    f = rng.integers(0, 128, size=(M, N)).astype(np.uint16)
+    sgn = rng.integers(0, 2, size=(M, N)).astype(np.uint16)
+    C = (sgn << 15) | (e << 7) | f
+    return A, B, scales(M), scales(N), C
+
+
+def brute_force_gemm_nv(A, B, SA, SB, M, N, K, alpha, beta, C):
+    vals = page_e2m1_values()
+    ra = [page_decode_row(A[m], K) for m in range(M)]
+    rb = [page_decode_row(B[n], K) for n in range(N)]
+    D = np.zeros((M, N), dtype=np.uint16)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                a = vals[ra[m][k]] * ue4m3_fraction(int(SA[m, k // 16]))
+                b = vals[rb[n][k]] * ue4m3_fraction(int(SB[n, k // 16]))
+                acc += a * b
+            y = Fraction(alpha) * acc
+            if beta != 0.0:
+                y += Fraction(beta) * bf16_bits_to_fraction(int(C[m, n]))
+            D[m, n] = bf16_rne_by_search(y)
+    return D
+
+
+def check_ue4m3_values(o):
+    """Every byte: the oracle's UE4M3 decode equals the E4M3 golden values
+    (positive codes), the test-side field decoder and the numpy table; 0x7F
+    and bytes with bit 7 set are NaN."""
+    golden = {int(code, 16): v for fmt, code, v in read_golden("fp8_values.txt") if int(fmt) == 1}
+    table = o.ue4m3_table()
+    for c in range(256):
+        got = o.ue4m3_value(c)
+        want = ue4m3_fraction(c)
+        if want is None:
+            assert got != got and table[c] != table[c], c
+        else:
+            assert math.isfinite(got) and Fraction(got) == want and table[c] == got, (c, got, want)
+            if c in golden:
+                assert golden[c] != "nan" and got == float(golden[c]), (c, got, golden[c])
+
+
+def check_nv_block_16(o):
+    """Closed forms with all elements 1.0: each 16-element block contributes
+    16 * sa_b * sb_b, so scales 1, 2, 4, 8 on A's four blocks give 240, and
+    1, 1/2, 1/4, 1/8 on B's give 30."""
+    K = 64
+    ones = np.full((1, K // 2), 0x22, dtype=np.uint8)          # code 2 = 1.0
+    unit = np.full((1, K // 16), 0x38, dtype=np.uint8)         # UE4M3 1.0
+    up = np.array([[0x38, 0x40, 0x48, 0x50]], dtype=np.uint8)  # 1, 2, 4, 8
+    down = np.array([[0x38, 0x30, 0x28, 0x20]], dtype=np.uint8)
+    D, acc, _, inexact = o.gemm_nv(ones, ones, up, unit, 1, 1, K, want_acc=True)
+    assert inexact == 0 and acc[0, 0] == 240.0 and bf16_to_f64(D)[0, 0] == 240.0
+    D, acc, _, _ = o.gemm_nv(ones, ones, unit, down, 1, 1, K, want_acc=True)
+    assert acc[0, 0] == 30.0 and bf16_to_f64(D)[0, 0] == 30.0
+
+
+def check_nv_brute_force(o, cases=6):
+    rng = np.random.default_rng(91)
+    for i in range(cases):
+        M, N, K = 3, 4, 64
+        A, B, SA, SB, C = random_case_nv(rng, M, N, K)
+        alpha, beta = [(1.0, 0.0), (0.5, 0.25), (-2.0, 1.0)][i % 3]
+        D, _, _, inexact = o.gemm_nv(A, B, SA, SB, M, N, K, alpha=alpha, beta=beta, C=C)
+        assert inexact == 0
+        want = brute_force_gemm_nv(A, B, SA, SB, M, N, K, alpha, beta, C)
+        assert same_value(D, want), (i, D, want)
+
+
+def check_nv_numpy_crosscheck(o):
+    """The exact double sum equals one float64 matmul of the numpy-dequantised
+    operands, and the sampled form equals the full one."""
+    rng = np.random.default_rng(92)
+    M, N, K = 24, 40, 256
+    A, B, SA, SB, C = random_case_nv(rng, M, N, K)
+    D, acc, _, inexact = o.gemm_nv(A, B, SA, SB, M, N, K, alpha=0.5, beta=0.75, C=C, want_acc=True)
+    assert inexact == 0
+    assert np.array_equal(acc, o.acc_numpy_nv(A, B, SA, SB, K))
+    pairs = np.array([(0, 0), (23, 39), (5, 17), (11, 2)])
+    Ds, accs, _, _ = o.gemm_nv_sampled(A, B, SA, SB, M, N, K, pairs, alpha=0.5, beta=0.75, C=C)
+    assert np.array_equal(Ds, D[pairs[:, 0], pairs[:, 1]])
+    assert np.array_equal(accs, acc[pairs[:, 0], pairs[:, 1]])
+
+
+def check_nv_exactness_flag(o):
+    """One block with both scales at the smallest subnormal 2^-9 next to 1008
+    products of (6 * 448)^2: sum|ab| spans more than 2^52 granules of the
+    tiny block's products (2^-20), which the oracle must report -- the
+    scales' ulp exponents enter the granule.  With that block at 448 too
+    the sum is exact."""
+    K = 1024
+    A = np.full((1, K // 2), 0x77, dtype=np.uint8)             # 6.0
+    A[0, :8] = 0x11                                            # block 0: 0.5
+    B = np.full((1, K // 2), 0x77, dtype=np.uint8)
+    SA = np.full((1, K // 16), 0x7E, dtype=np.uint8)           # 448
+    SB = np.full((1, K // 16), 0x7E, dtype=np.uint8)
+    SA[0, 0] = SB[0, 0] = 0x01                                 # 2^-9
+    _, _, _, inexact = o.gemm_nv(A, B, SA, SB, 1, 1, K)
+    assert inexact == 1
+    SA[0, 0] = SB[0, 0] = 0x7E
+    _, _, _, inexact = o.gemm_nv(A, B, SA, SB, 1, 1, K)
+    assert inexact == 0
+
+
+def check_nv_rejects_non_ue4m3(o):
+    A = np.zeros((2, 16), dtype=np.uint8)
+    S = np.full((2, 2), 0x38, dtype=np.uint8)
+    o.gemm_nv(A, A, S, S, 2, 2, 32)
+    bad = S.copy()
+    bad[1, 1] = 0xB8                                           # sign bit set
+    for args in ((bad, S), (S, bad)):
+        try:
+            o.gemm_nv(A, A, args[0], args[1], 2, 2, 32)
+        except ValueError:
+            continue
+        raise AssertionError("a scale byte with bit 7 set was accepted")
+
+
 ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfields, check_e8m0,
               check_nibble_order,
               check_bf16_golden, check_bf16_roundtrip, check_bf16_midpoints,
@@ -1019,7 +1161,9 @@ ALL_CHECKS = [check_gemm_single_rounding, check_e2m1_golden, check_e2m1_bitfield
               check_fp6_golden, check_fp6_all_codes, check_fp6_layout, check_fp6_brute_force,
               check_fp6_numpy_crosscheck, check_fp4_padded_layout, check_fp4_padded_equals_packed,
               check_fp4_padded_brute_force, check_fp4_padded_exactness_flag,
-              check_quant_sub_nearest_and_scale, check_quant_sub_matches_generator]
+              check_quant_sub_nearest_and_scale, check_quant_sub_matches_generator,
+              check_ue4m3_values, check_nv_block_16, check_nv_brute_force,
+              check_nv_numpy_crosscheck, check_nv_exactness_flag, check_nv_rejects_non_ue4m3]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

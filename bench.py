@@ -120,7 +120,7 @@ def parse_args():
     ap.add_argument("--workload", default="large",
                     choices=["tiny", "decode", "mid", "large", "skinny", "quantize", "quantize8",
                              "quantize6",
-                             "large8", "decode8", "mixed8", "large6", "mixed6"])
+                             "large8", "decode8", "mixed8", "large6", "mixed6", "large_nv"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -137,7 +137,7 @@ def parse_args():
                     help="M,N,K: run a few GEMMs of a random shape for a profiler, no timing")
     ap.add_argument("--calls", type=int, default=3, help="--profile-shape: GEMM calls")
     ap.add_argument("--format", default="mxfp4",
-                    choices=["mxfp4", "e4m3", "e5m2", "e2m3", "e3m2", "e2m1"],
+                    choices=["mxfp4", "e4m3", "e5m2", "e2m3", "e3m2", "e2m1", "nvfp4"],
                     help="--profile-shape: element format")
     return ap.parse_args()
 
@@ -237,6 +237,9 @@ def oracle_throughput(p, seconds, seed):
             fmt = inputs.BYTE_FORMATS
             oracle.gemm8_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, fmt[p.fmt_a], fmt[p.fmt_b],
                                  pairs, alpha=p.alpha, beta=p.beta, C=p.C)
+        elif p.SA.shape[1] == p.K // 16:  # NVFP4 problem (one scale per 16 K)
+            oracle.gemm_nv_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs, alpha=p.alpha,
+                                   beta=p.beta, C=p.C)
         else:
             oracle.gemm_sampled(p.A, p.B, p.SA, p.SB, p.M, p.N, p.K, pairs, alpha=p.alpha,
                                 beta=p.beta, C=p.C)
@@ -267,7 +270,10 @@ def run_reference(args, rank):
         run_reference_quantize(args)
         return
     fp8 = args.workload in inputs.WORKLOADS8
-    p = inputs.workload8(args.workload) if fp8 else inputs.workload(args.workload)
+    if args.workload == "large_nv":
+        p = nvfp4_problem()
+    else:
+        p = inputs.workload8(args.workload) if fp8 else inputs.workload(args.workload)
     # About 100 s of oracle time in all (2.5 - 4 minutes with the per-step
     # overheads on 16 host cores), at most 4 s per step.
     per_step = min(4.0, 100.0 / max(1, args.steps))
@@ -281,7 +287,8 @@ def run_reference(args, rank):
     value = len(vals) / sum(1.0 / v for v in vals)        # total FLOPs / total time
     line = {
         "impl": "reference",
-        "metric": (METRIC6 if args.workload.endswith("6") else METRIC8) if fp8 else METRIC,
+        "metric": ((METRIC6 if args.workload.endswith("6") else METRIC8) if fp8 else
+                   METRIC_NV if args.workload == "large_nv" else METRIC),
         "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
@@ -448,6 +455,129 @@ def run_mxfp8(args, world, rank, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "api": "mxfp8_gemm_host (pinned host buffers)"},
         "gpu_launches": args.steps * (1 + plan.relayout_pass),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+METRIC_NV = "NVFP4 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP4 peak"
+
+
+def nvfp4_problem():
+    """The NVFP4 workload: 8192^3, E2M1 codes uniform over all 16, UE4M3
+    scales uniform over 0x28..0x48 (0.25 .. 4), alpha 1, beta 0, seed 13."""
+    from block_scaled_mxfp4_gb300 import inputs
+    return inputs.make_problem_nv("large_nv", 8192, 8192, 8192, seed=13, alpha=1.0, beta=0.0,
+                                  c_sigma=None)
+
+
+def run_nvfp4(args, world, rank, local_rank):
+    """--workload large_nv: one nvfp4_gemm call per step (the NVFP4 scale
+    relayout + the CTA-pair kernel with kind::mxf4nvf4 MMAs, launched as its
+    dependent), steps back to back over rotating input copies, as the MXFP4
+    headline is timed; each rank of a multi-GPU launch runs a replica."""
+    import torch
+
+    import block_scaled_mxfp4_gb300 as mx
+    from block_scaled_mxfp4_gb300 import build
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    p = nvfp4_problem()
+    M, N, K = p.M, p.N, p.K
+    in_bytes = M * K // 2 + N * K // 2 + (M + N) * K // 16
+    copies = rotation_copies(in_bytes)
+    ops = Operands(p, copies, dev)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    wsb = mx.nvfp4_gemm_workspace_size(M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(i):
+        c = i % copies
+        mx.nvfp4_gemm(D, N, None, 0, ops.A[c], K, ops.B[c], K, ops.SA[c], K // 16, ops.SB[c],
+                      K // 16, p.alpha, p.beta, M, N, K, ws, wsb, stream)
+
+    for i in range(max(3, args.warmup)):
+        launch(i)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    tot_ms = max_over_ranks([timed_back_to_back(stream, args.steps, launch, dist, dev)], dist,
+                            dev)[0]
+    clocks = sampler.stop()
+    ms = tot_ms / args.steps
+    flops = 2.0 * M * N * K
+    nbytes = in_bytes + 2 * M * N
+    value = world * flops * args.steps / (tot_ms * 1e-3) / 1e12
+    # End to end through the same entry point from pinned host buffers: the
+    # inputs' copies in, the call, D's copy out, all inside the timed region.
+    pin = lambda t: t.cpu().pin_memory()
+    hA, hB, hSA, hSB = pin(ops.A[0]), pin(ops.B[0]), pin(ops.SA[0]), pin(ops.SB[0])
+    hD = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        for h, d in ((hA, ops.A[0]), (hB, ops.B[0]), (hSA, ops.SA[0]), (hSB, ops.SB[0])):
+            d.copy_(h, non_blocking=True)
+        launch(0)
+        hD.copy_(D, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / args.e2e_steps], dist, dev)[0]
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    achieved = flops / (ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
+                           f"{FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio; NVFP4 runs at the "
+                           "FP4 rate)",
+            "traffic": None, "traffic_source": "no capture for this workload",
+            "kernel": "scale_relayout_kernel + gemm_mxf4_pair<5, true> (one nvfp4_gemm call, "
+                      "timed together)",
+            "kernel_ms": ms, "algorithmic_bytes": nbytes, "flops": flops}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_throughput(p, 10.0, 78)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hB, hSA, hSB))
+    line = {
+        "metric": METRIC_NV, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1, ue4m3 per 16)", "data": "synthetic",
+        "config": {"workload": f"large_nv M={M} N={N} K={K}", "M": M, "N": N, "K": K,
+                   "alpha": p.alpha, "beta": p.beta, "seed": p.seed, "tile": "256x256x256",
+                   "stages": 5,
+                   "l2": f"inputs larger than L2: steps rotate over {copies} copies of the "
+                         "inputs, back to back between one pair of events",
+                   "step": "one nvfp4_gemm call: NVFP4 scale relayout of A and B (one launch) + "
+                           "CTA-pair GEMM launched as its dependent",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
+                "api": "nvfp4_gemm with its inputs copied in and D copied out (pinned host "
+                       "memory) on the same stream"},
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -775,7 +905,9 @@ def profile_shape(args):
     [120, 127], then --calls mxfp4_gemm calls (--prepacked: scales relaid
     once, then mxfp4_gemm_prepacked calls) with the heuristic's plan; the
     byte formats = random codes (the 8-bit formats' NaN codes avoided; every
-    byte is a valid padded 6- or 4-bit group), then --calls mxfp8_gemm calls."""
+    byte is a valid padded 6- or 4-bit group), then --calls mxfp8_gemm calls;
+    nvfp4 = random fp4x2 codes and UE4M3 scales in [0x30, 0x40], then --calls
+    nvfp4_gemm calls."""
     import torch
 
     import block_scaled_mxfp4_gb300 as mx
@@ -787,6 +919,19 @@ def profile_shape(args):
     SA = torch.randint(120, 128, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)
     SB = torch.randint(120, 128, (N, K // 32), dtype=torch.uint8, device=dev, generator=g)
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if args.format == "nvfp4":
+        A = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        SA = torch.randint(0x30, 0x41, (M, K // 16), dtype=torch.uint8, device=dev, generator=g)
+        SB = torch.randint(0x30, 0x41, (N, K // 16), dtype=torch.uint8, device=dev, generator=g)
+        wsb = mx.nvfp4_gemm_workspace_size(M, N, K)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        for _ in range(args.calls):
+            mx.nvfp4_gemm(D, N, None, 0, A, K, B, K, SA, K // 16, SB, K // 16, 1.0, 0.0, M, N, K,
+                          ws, wsb)
+        torch.cuda.synchronize()
+        print(f"{M}x{N}x{K} nvfp4: {args.calls} calls (CTA-pair kernel)")
+        return
     if args.format != "mxfp4":
         fmt = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2, "e2m3": mx.MXFP6_E2M3,
                "e3m2": mx.MXFP6_E3M2, "e2m1": mx.MXFP4_E2M1_PADDED}[args.format]
@@ -1043,6 +1188,9 @@ def main():
         return
     if args.workload in ("large8", "decode8", "mixed8", "large6", "mixed6"):
         run_mxfp8(args, world, rank, local_rank)
+        return
+    if args.workload == "large_nv":
+        run_nvfp4(args, world, rank, local_rank)
         return
     run_mxfp4(args, world, rank, local_rank)
 

@@ -27,7 +27,7 @@ __all__ = [
     "mxfp4_strerror", "mxfp4_version",
     "mxfp8_gemm", "mxfp8_gemm_prepacked", "mxfp8_plan_gemm", "mxfp8_gemm_workspace_size",
     "mxfp8_gemm_prepacked_workspace_size", "mxfp8_quantize", "mxfp8_gemm_host",
-    "mxfp8_gemm_host_arena_size",
+    "mxfp8_gemm_host_arena_size", "nvfp4_gemm", "nvfp4_gemm_workspace_size",
     "MXFP8_E4M3", "MXFP8_E5M2", "MXFP6_E2M3", "MXFP6_E3M2", "MXFP4_E2M1_PADDED",
     "gemm", "Plan",
 ]
@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
             "mxfp8_plan_gemm": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]),
             "mxfp8_quantize": (i32, [vp, i64, vp, i64, vp, i64, i32, i32, i32, vp]),
             "mxfp8_gemm_workspace_size": (sz, [i32, i32, i32, i32]),
+            "nvfp4_gemm": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                 f32, f32, i32, i32, i32, vp, sz, vp]),
+            "nvfp4_gemm_workspace_size": (sz, [i32, i32, i32]),
             "mxfp4_gemm_prepacked": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
                                            f32, f32, i32, i32, i32, i32, vp, sz, vp]),
             "mxfp4_gemm_noalloc": (i32, [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
@@ -233,6 +236,19 @@ def mxfp8_gemm_prepacked(D, ldd, C, ldc, A, lda, B, ldb, scaleA_relaid, scaleB_r
                                              alpha, beta, M, N, K, split_k, _p(workspace),
                                              workspace_bytes, _stream(stream)),
                   "mxfp8_gemm_prepacked")
+
+
+def nvfp4_gemm(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta, M, N,
+               K, workspace, workspace_bytes, stream=None):
+    """NVFP4 GEMM: packed E2M1 A, B; one UE4M3 scale per 16 K (ld_sa, ld_sb >= K/16)."""
+    return _check(lib().nvfp4_gemm(_p(D), ldd, _p(C), ldc, _p(A), lda, _p(B), ldb, _p(scaleA),
+                                   ld_sa, _p(scaleB), ld_sb, alpha, beta, M, N, K,
+                                   _p(workspace), workspace_bytes, _stream(stream)),
+                  "nvfp4_gemm")
+
+
+def nvfp4_gemm_workspace_size(M, N, K) -> int:
+    return lib().nvfp4_gemm_workspace_size(M, N, K)
 
 
 def mxfp8_quantize(Q, ldq, S, lds, X, ldx, rows, K, fmt, stream=None):

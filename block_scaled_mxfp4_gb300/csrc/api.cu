@@ -122,12 +122,13 @@ bool encode_scales(CUtensorMap *map, const void *base, int rows, int K, int64_t 
 
 // Relaid scale atoms viewed as 2-D uint32 [atoms, 128] (one 512-byte atom per
 // row); a box of 2 rows = the two atoms of one 256-K stage of a 128-row block.
-bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K, int box_atoms = 2)
+// groups: atoms per 128-row block (sf_groups(K), or sf_groups_nv(K) for NVFP4).
+bool encode_atoms(CUtensorMap *map, const void *base, int rows, int64_t groups, int box_atoms)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
         return false;
-    const int64_t atoms = sf_row_blocks(rows) * sf_groups(K);
+    const int64_t atoms = sf_row_blocks(rows) * groups;
     cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(atoms)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kSfAtomBytes)};
     cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_atoms)};
@@ -143,12 +144,12 @@ bool encode_atoms(CUtensorMap *map, const void *base, int rows, int K, int box_a
 // 128-row blocks a pair tile's B rows touch for one stage, in smem order (row
 // block, k-group); a tile that starts inside a block reads past its last rows
 // (zero fill beyond the end).
-bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int K, int box_rb, int box_groups = 2)
+bool encode_atoms_3d(CUtensorMap *map, const void *base, int rows, int64_t groups, int box_rb,
+                     int box_groups)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
         return false;
-    const int64_t groups = sf_groups(K);
     cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(groups),
                           static_cast<cuuint64_t>(sf_row_blocks(rows))};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kSfAtomBytes),
@@ -376,16 +377,19 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
              const void *B, int64_t ldb, const Scales &sc, float alpha, float beta, int M, int N,
              int K, const mxfp4_plan &plan, const GemmShape &shape, uint8_t *ws,
              cudaStream_t stream, bool after_relayout = false, int fmt_a = 0, int fmt_b = 0,
-             unsigned flags = 0)
+             unsigned flags = 0, bool nv = false)
 {
     if (shape.pair) {
         if (sc.rowmajor)
             return MXFP4_ERR_INVALID_ARG;            // the pair kernel reads relaid atoms
+        // Atoms per stage and 128-row block: 2 (128 K each), or 4 for NVFP4.
+        const int per_stage = nv ? 4 : 2;
+        const int64_t groups = nv ? sf_groups_nv(K) : sf_groups(K);
         CUtensorMap tmA, tmB, tmSA, tmSB;
         if (!encode_operand(&tmA, A, M, K, lda, kTileM) ||
             !encode_operand(&tmB, B, N, K, ldb, 128) ||
-            !encode_atoms(&tmSA, sc.a, M, K, 2) ||
-            !encode_atoms_3d(&tmSB, sc.b, N, K, 2, 2))
+            !encode_atoms(&tmSA, sc.a, M, groups, per_stage) ||
+            !encode_atoms_3d(&tmSB, sc.b, N, groups, 2, per_stage))
             return MXFP4_ERR_CUDA;
         GemmArgs a;
         std::memset(&a, 0, sizeof(a));
@@ -405,8 +409,8 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
         a.ab_early = after_relayout ? 1 : 0;
         a.wait_limit = g_wait_limit.load();
         const int tiles_p = (M + 255) / 256, tiles_q = (N + 255) / 256;
-        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB, stream) !=
-            cudaSuccess)
+        if (launch_gemm_pair(a, tiles_p, tiles_q, shape.pair_ctas, tmA, tmB, tmSA, tmSB, nv,
+                             stream) != cudaSuccess)
             return MXFP4_ERR_CUDA;
         return MXFP4_OK;
     }
@@ -722,6 +726,59 @@ int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
 {
     return gemm_rowmajor(D, ldd, C, ldc, A, lda, B, ldb, scaleA, ld_sa, scaleB, ld_sb, alpha, beta,
                          M, N, K, split_k, workspace, workspace_bytes, stream, true, fmt_a, fmt_b);
+}
+
+size_t nvfp4_gemm_workspace_size(int M, int N, int K)
+{
+    if (M < 1 || N < 1 || K < 32 || (K % 32) != 0)
+        return 0;
+    return align_up(sf_relaid_bytes_nv(M, K)) + align_up(sf_relaid_bytes_nv(N, K));
+}
+
+// NVFP4: the scales are relaid into the workspace (one launch for both
+// operands), then the CTA-pair kernel runs as its programmatic dependent, for
+// every shape.
+int nvfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, int64_t lda,
+               const void *B, int64_t ldb, const void *scaleA, int64_t ld_sa, const void *scaleB,
+               int64_t ld_sb, float alpha, float beta, int M, int N, int K, void *workspace,
+               size_t workspace_bytes, void *stream)
+{
+    int st = check_common(D, ldd, C, ldc, A, lda, B, ldb, beta, M, N, K, 0);
+    if (st != MXFP4_OK)
+        return st;
+    if (!scaleA || !scaleB || ld_sa < K / 16 || ld_sb < K / 16)
+        return MXFP4_ERR_INVALID_ARG;
+    const int64_t tiles = ((static_cast<int64_t>(M) + 255) / 256) * ((static_cast<int64_t>(N) + 255) / 256);
+    if (tiles > 0x7FFFFFFF)
+        return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    const size_t sfa_bytes = align_up(sf_relaid_bytes_nv(M, K));
+    const size_t sfb_bytes = align_up(sf_relaid_bytes_nv(N, K));
+    if (!workspace || workspace_bytes < sfa_bytes + sfb_bytes)
+        return MXFP4_ERR_WORKSPACE;
+    if (!aligned(workspace, kAlign))
+        return MXFP4_ERR_MISALIGNED;
+    st = check_device();
+    if (st != MXFP4_OK)
+        return st;
+    const int64_t pairs = device_sms_or_default() / 2;
+    mxfp4_plan plan;
+    std::memset(&plan, 0, sizeof(plan));
+    GemmShape shape;
+    std::memset(&shape, 0, sizeof(shape));
+    shape.tile_n = 256;
+    shape.stages = 5;
+    shape.ctas_per_sm = 1;
+    shape.pair = 1;
+    shape.pair_ctas = 2 * static_cast<int>(tiles < pairs ? tiles : pairs);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *sfa = static_cast<uint8_t *>(workspace);
+    uint8_t *sfb = sfa + sfa_bytes;
+    if (launch_scale_relayout2_nv(sfa, static_cast<const uint8_t *>(scaleA), M, ld_sa, sfb,
+                                  static_cast<const uint8_t *>(scaleB), N, ld_sb, K, s) != cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    const Scales sc{sfa, sfb, 0, 0, false};
+    return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape, nullptr,
+                    s, true, 0, 0, 0, true);
 }
 
 int mxfp8_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A,

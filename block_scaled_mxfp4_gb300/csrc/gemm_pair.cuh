@@ -12,6 +12,11 @@
 // fed across the TMA round trip.  One accumulator (256 of the 512 tensor-
 // memory columns) and one scale slot per stage (6 x 24 columns).
 //
+// NV = true is the NVFP4 form: kind::mxf4nvf4 with one UE4M3 scale per 16 K
+// (scale_vec::4X).  A stage then carries four scale atoms per 128-row block
+// instead of two (each atom spans 64 K), a scale slot takes 48 columns, and
+// five stages fit the tensor memory (256 + 5 x 48 = 496 columns).
+//
 // Roles (512 threads = 16 warps per CTA):
 //   warps 4, 6, 7 (each CTA)  TMA producers: A half, B half, and the scale
 //                      atoms (this CTA's 128 rows of scale-A; all BN rows of
@@ -54,11 +59,11 @@
 
 namespace mxfp4 {
 
-template <int STAGES>
+template <int STAGES, bool NV>
 struct PairCfg {
     static constexpr int BN = 256;                        // tile N
     static constexpr int B_ROWS = BN / 2;                 // this CTA's rows of the B tile
-    static constexpr int GROUPS = 2;                      // scale k-groups (128 K) per stage
+    static constexpr int GROUPS = NV ? 4 : 2;             // scale atoms per stage and row block
     static constexpr int A_BYTES = kTileM * 128;          // 128 rows x 128 bytes (256 K)
     static constexpr int B_BYTES = B_ROWS * 128;
     static constexpr int SFB_RB = 2;                      // 128-row scale blocks a tile can touch
@@ -177,13 +182,13 @@ __device__ __forceinline__ void pair_round_chunk(const GemmArgs &a, int m, int n
         out[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
+template <int STAGES, bool NV>
+__global__ void __launch_bounds__(PairCfg<STAGES, NV>::THREADS, 1)
     gemm_mxf4_pair(const __grid_constant__ GemmArgs a, const __grid_constant__ PairSched ps,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB)
 {
-    using PC = PairCfg<STAGES>;
+    using PC = PairCfg<STAGES, NV>;
     constexpr int BN = PC::BN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     cluster_sync();                          // barriers of both CTAs initialised
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int64_t groups = sf_groups(a.K);
+    const int64_t groups = NV ? sf_groups_nv(a.K) : sf_groups(a.K);
     const int total_stages = my_tiles * ps.kt;
     // The next kernel on the stream may launch; it waits in-kernel for this
     // grid before touching anything this grid writes.
@@ -276,8 +281,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         tma_load_2d(st + PC::A_BYTES, &tmB, &full[stage], kt * 128, brow, pol);
                     } else {
                         uint8_t *sf = st + PC::A_BYTES + PC::B_BYTES;
-                        tma_load_2d(sf, &tmSA, &full[stage], 0, sfa_atom + 2 * kt, pol);
-                        tma_load_3d(sf + PC::SFA_BYTES, &tmSB, &full[stage], 0, 2 * kt, sfb_rb, pol);
+                        tma_load_2d(sf, &tmSA, &full[stage], 0, sfa_atom + PC::GROUPS * kt, pol);
+                        tma_load_3d(sf + PC::SFA_BYTES, &tmSB, &full[stage], 0, PC::GROUPS * kt,
+                                    sfb_rb, pol);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -303,9 +309,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             bool ok = mbar_wait(&full[stage], phase, abort_flag, a.wait_limit, &g_device_status);
             if (!__all_sync(0xffffffffu, ok))
                 break;
-            // Line `lane` of every atom of the stage: scale-A k-groups 0, 1
-            // (columns 0-7); scale-B (k-group g, row block rb; in shared
-            // memory at rb*GROUPS + g) -> columns 8 + g*4*SFB_RB + rb*4.
+            // Line `lane` of every atom of the stage: scale-A atoms g (columns
+            // 4g .. 4g+3); scale-B (atom g, row block rb; in shared memory at
+            // rb*GROUPS + g) -> columns SF_COLS_A + g*4*SFB_RB + rb*4.
             const uint8_t *sf_s = smem + stage * PC::STAGE_BYTES + PC::A_BYTES + PC::B_BYTES;
             uint32_t wa[4 * PC::GROUPS];
             uint32_t wb[4 * PC::GROUPS * PC::SFB_RB];
@@ -328,8 +334,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 }
             }
             const uint32_t slot = t_q + stage * PC::SF_COLS;
-            tmem_st_32x32b_x8(slot, wa);
-            tmem_st_32x32b_x16(slot + PC::SF_COLS_A, wb);
+            if constexpr (NV) {
+                tmem_st_32x32b_x16(slot, wa);
+                tmem_st_32x32b_x32(slot + PC::SF_COLS_A, wb);
+            } else {
+                tmem_st_32x32b_x8(slot, wa);
+                tmem_st_32x32b_x16(slot + PC::SF_COLS_A, wb);
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         // The whole warp runs the loop (warp-uniform descriptors and
         // barrier polls); one elected lane issues each MMA and commit.
         if (leader) {
-            const uint32_t idesc = idesc_mxf4(256, BN);
+            const uint32_t idesc = NV ? idesc_nvf4(256, BN) : idesc_mxf4(256, BN);
             const uint32_t t_sf = tmem + BN;
             int stage = 0;
             uint32_t phase = 0;
@@ -382,12 +393,19 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     // Four K=64 MMAs per 256-K stage.
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t sf_id = (j & 1) * 2;
-                        const int g = j >> 1;                        // scale k-group
-                        mma_mxf4_pair_elect(d_tmem, adesc + 2 * j, bdesc + 2 * j,
-                                            idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
-                                            sfb_t + g * 4 * PC::SFB_RB,
-                                            (kt > 0 || j > 0) ? 1u : 0u);
+                        if constexpr (NV) {
+                            // Atom j holds the MMA's four blocks of 16.
+                            mma_nvf4_pair_elect(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc,
+                                                sfa_t + j * 4, sfb_t + j * 4 * PC::SFB_RB,
+                                                (kt > 0 || j > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t sf_id = (j & 1) * 2;
+                            const int g = j >> 1;                    // scale k-group
+                            mma_mxf4_pair_elect(d_tmem, adesc + 2 * j, bdesc + 2 * j,
+                                                idesc_sf_ids(idesc, sf_id, sf_id), sfa_t + g * 4,
+                                                sfb_t + g * 4 * PC::SFB_RB,
+                                                (kt > 0 || j > 0) ? 1u : 0u);
+                        }
                     }
                     // Frees the stage in both CTAs of the pair.
                     mma_commit_pair_elect(&empty[stage], static_cast<uint16_t>(3u));

@@ -1143,17 +1143,21 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
     return launch_gemm_fmt<1>(b, tmP, tmQ, tmSP, tmSQ, s, grid, stream);
 }
 
-// The compiled pair configuration: 6 stages of 256 K, 256 x 256 tiles.
-using PairDefault = PairCfg<6>;
+// The compiled pair configurations: MXFP4 with 6 stages of 256 K, NVFP4 with
+// 5 (its larger scale slots leave room in tensor memory for five).
+constexpr int kPairStages = 6;
+constexpr int kPairStagesNv = 5;
 
-size_t gemm_pair_smem_bytes() { return PairDefault::SMEM_BYTES; }
+size_t gemm_pair_smem_bytes() { return PairCfg<kPairStages, false>::SMEM_BYTES; }
 
-cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
-                             const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream)
+template <int STAGES, bool NV>
+static cudaError_t launch_pair_kernel(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
+                                      const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                      const CUtensorMap &tmSA, const CUtensorMap &tmSB,
+                                      cudaStream_t stream)
 {
-    using PC = PairDefault;
-    auto kern = gemm_mxf4_pair<6>;
+    using PC = PairCfg<STAGES, NV>;
+    auto kern = gemm_mxf4_pair<STAGES, NV>;
     static std::atomic<int> max_clusters[64];   // per device; 0 = not yet queried
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1204,6 +1208,18 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ct
     ps.kt = a.kt_total;
     ps.group = tiles_p < 8 ? tiles_p : 8;
     return cudaLaunchKernelEx(&cfg, kern, a, ps, tmA, tmB, tmSA, tmSB);
+}
+
+cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
+                             const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool nv,
+                             cudaStream_t stream)
+{
+    if (nv)
+        return launch_pair_kernel<kPairStagesNv, true>(a, tiles_p, tiles_q, ctas, tmA, tmB, tmSA,
+                                                       tmSB, stream);
+    return launch_pair_kernel<kPairStages, false>(a, tiles_p, tiles_q, ctas, tmA, tmB, tmSA, tmSB,
+                                                  stream);
 }
 
 // Test hook: one wait on an mbarrier nobody arrives at.

@@ -22,6 +22,13 @@ inline size_t sf_relaid_bytes(int rows, int K)
 {
     return static_cast<size_t>(sf_row_blocks(rows) * sf_groups(K) * kSfAtomBytes);
 }
+// NVFP4 (one UE4M3 scale per 16 K): the same atoms, each holding 4 blocks of
+// 16 (64 K), four per 256-K stage.
+__host__ __device__ inline int64_t sf_groups_nv(int K) { return 4 * ((static_cast<int64_t>(K) + kTileK - 1) / kTileK); }
+inline size_t sf_relaid_bytes_nv(int rows, int K)
+{
+    return static_cast<size_t>(sf_row_blocks(rows) * sf_groups_nv(K) * kSfAtomBytes);
+}
 
 // Arguments of one GEMM launch.  "P" is the operand whose rows feed the MMA's
 // M side (A, or B when swapped), "Q" the operand on the MMA's N side.
@@ -98,9 +105,11 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
 // a.ab_early: that work is this library's scale relayout, so only the scale
 // loads and the epilogue wait for it.
 size_t gemm_pair_smem_bytes();
+// nv: NVFP4 operands (UE4M3 scales per 16 K, relaid with sf_groups_nv).
 cudaError_t launch_gemm_pair(const GemmArgs &a, int tiles_p, int tiles_q, int ctas,
                              const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, cudaStream_t stream);
+                             const CUtensorMap &tmSA, const CUtensorMap &tmSB, bool nv,
+                             cudaStream_t stream);
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
                                   cudaStream_t stream);
@@ -109,6 +118,13 @@ cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, in
 cudaError_t launch_scale_relayout2(uint8_t *dst0, const uint8_t *src0, int rows0, int64_t ld0,
                                    uint8_t *dst1, const uint8_t *src1, int rows1, int64_t ld1,
                                    int K, cudaStream_t stream);
+
+// NVFP4 scales: row-major UE4M3 [rows, ld] (one per 16 K) -> atoms of
+// 128 rows x 4 blocks of 16, sf_groups_nv(K) per 128-row block, padded with
+// 0x38 (UE4M3 1.0; the E8M0 pad 0x7F would be NaN here).
+cudaError_t launch_scale_relayout2_nv(uint8_t *dst0, const uint8_t *src0, int rows0, int64_t ld0,
+                                      uint8_t *dst1, const uint8_t *src1, int rows1, int64_t ld1,
+                                      int K, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(long long limit, cudaStream_t stream);
 

@@ -303,6 +303,19 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, "
+                 "%9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, "
+                 "%25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+                 "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
+                 "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+                 "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -418,6 +431,19 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N)
            | (1u << 10)                                    // B format: E2M1
            | (static_cast<uint32_t>(N >> 3) << 17)         // N / 8
            | (1u << 23)                                    // scale format: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24);        // M / 16
+}
+
+// Instruction descriptor for kind::mxf4nvf4 with UE4M3 scales (NVFP4: E2M1
+// A and B, scale format field 0), M x N.  With scale_vec::4X each MMA of
+// K = 64 reads one 32-bit column of scales per 32 rows (4 blocks of 16), so
+// the scale-factor ids stay 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N)
+{
+    return (1u << 7)                                       // A format: E2M1
+           | (1u << 10)                                    // B format: E2M1
+           | (static_cast<uint32_t>(N >> 3) << 17)         // N / 8
+           | (0u << 23)                                    // scale format: UE4M3
            | (static_cast<uint32_t>(M >> 4) << 24);        // M / 16
 }
 
@@ -591,6 +617,22 @@ __device__ __forceinline__ void mma_mxf4_pair_elect(uint32_t d_tmem, uint64_t ad
         "setp.ne.b32 p, %6, 0;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// NVFP4 form of mma_mxf4_pair_elect: kind::mxf4nvf4 with one UE4M3 scale
+// per 16 K (scale_vec::4X).
+__device__ __forceinline__ void mma_nvf4_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                    uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                    uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");

@@ -21,6 +21,9 @@ namespace mxfp4 {
 // memory (rows padded to an odd word count, so the column reads below hit 32
 // different banks), and writes the atoms as 16-byte lines, consecutive
 // threads on consecutive lines.
+// NVFP4 scales (one UE4M3 byte per 16 K) take the same path with a block of
+// 16 in place of 32: an atom then spans 64 K, and padding is 0x38 (UE4M3 1.0).
+//
 // 8 groups (32 scale bytes of each of 128 rows) per CTA: measured fastest for
 // 8192 x 8192 scales (6.5 us for both operands, against 7.5 at 16, 10.8 at 32
 // and 8.2 at 4 groups): enough CTAs to keep DRAM busy, 4 words per thread.
@@ -36,6 +39,7 @@ struct RelayoutJob {
     int64_t ld[2];
     int64_t rblocks0;
     int vec4[2];
+    uint32_t pad;           // padding byte, replicated into the four bytes of a word
 };
 
 __global__ void __launch_bounds__(kRelayoutThreads)
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(kRelayoutThreads)
         const int w = e % kGroupsPerCta;
         const int64_t row = rb * 128 + r;
         const int64_t kb = (g0 + w) * 4;
-        uint32_t word = 0x7F7F7F7Fu;
+        uint32_t word = job.pad;
         if (row < rows && w < ng) {
             const uint8_t *p = src + row * ld + kb;
             if (vec4 && kb + 4 <= kblocks) {
@@ -80,7 +84,7 @@ __global__ void __launch_bounds__(kRelayoutThreads)
                 word = 0;
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
-                    word |= (kb + b < kblocks ? static_cast<uint32_t>(p[b]) : 0x7Fu) << (8 * b);
+                    word |= (kb + b < kblocks ? static_cast<uint32_t>(p[b]) : (job.pad & 0xFFu)) << (8 * b);
             }
         }
         words[k] = word;
@@ -100,9 +104,11 @@ __global__ void __launch_bounds__(kRelayoutThreads)
     }
 }
 
-static cudaError_t launch_relayout_job(RelayoutJob &job, int nops, int K, cudaStream_t stream)
+// kblocks: scale bytes per row (K / 32, or K / 16 for NVFP4); groups: atoms
+// per 128-row block.
+static cudaError_t launch_relayout_job(RelayoutJob &job, int nops, int kblocks, int64_t groups,
+                                       cudaStream_t stream)
 {
-    const int64_t groups = sf_groups(K);
     int64_t total = 0;
     for (int i = 0; i < nops; ++i) {
         job.vec4[i] = (reinterpret_cast<uintptr_t>(job.src[i]) % 4 == 0) && (job.ld[i] % 4 == 0);
@@ -126,7 +132,7 @@ static cudaError_t launch_relayout_job(RelayoutJob &job, int nops, int K, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scale_relayout_kernel, job, K / 32, groups);
+    return cudaLaunchKernelEx(&cfg, scale_relayout_kernel, job, kblocks, groups);
 }
 
 cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, int K, int64_t ld,
@@ -137,7 +143,8 @@ cudaError_t launch_scale_relayout(uint8_t *dst, const uint8_t *src, int rows, in
     job.src[0] = src;
     job.rows[0] = rows;
     job.ld[0] = ld;
-    return launch_relayout_job(job, 1, K, stream);
+    job.pad = 0x7F7F7F7Fu;
+    return launch_relayout_job(job, 1, K / 32, sf_groups(K), stream);
 }
 
 cudaError_t launch_scale_relayout2(uint8_t *dst0, const uint8_t *src0, int rows0, int64_t ld0,
@@ -153,7 +160,25 @@ cudaError_t launch_scale_relayout2(uint8_t *dst0, const uint8_t *src0, int rows0
     job.src[1] = src1;
     job.rows[1] = rows1;
     job.ld[1] = ld1;
-    return launch_relayout_job(job, 2, K, stream);
+    job.pad = 0x7F7F7F7Fu;
+    return launch_relayout_job(job, 2, K / 32, sf_groups(K), stream);
+}
+
+cudaError_t launch_scale_relayout2_nv(uint8_t *dst0, const uint8_t *src0, int rows0, int64_t ld0,
+                                      uint8_t *dst1, const uint8_t *src1, int rows1, int64_t ld1,
+                                      int K, cudaStream_t stream)
+{
+    RelayoutJob job{};
+    job.dst[0] = dst0;
+    job.src[0] = src0;
+    job.rows[0] = rows0;
+    job.ld[0] = ld0;
+    job.dst[1] = dst1;
+    job.src[1] = src1;
+    job.rows[1] = rows1;
+    job.ld[1] = ld1;
+    job.pad = 0x38383838u;
+    return launch_relayout_job(job, 2, K / 16, sf_groups_nv(K), stream);
 }
 
 }  // namespace mxfp4

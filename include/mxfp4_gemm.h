@@ -252,6 +252,32 @@ int mxfp8_gemm_prepacked(void *D, int64_t ldd, const void *C, int64_t ldc,
 size_t mxfp8_gemm_prepacked_workspace_size(int M, int N, int K, int split_k);
 
 /*
+ * NVFP4 form of the GEMM: the pages describe no such format (they cover
+ * E8M0 block scales only); it is the other block-scaled FP4 variant of the
+ * same tensor-core instruction family.  A and B are packed E2M1 exactly as
+ * for mxfp4_gemm; each row of A and B carries one scale per 16 consecutive K
+ * elements instead of 32, stored as an unsigned E4M3 byte (UE4M3:
+ * (1 + m/8) * 2^(e-7), exponent field 0 subnormal (m/8) * 2^-6, 0x7F NaN;
+ * bit 7 must be 0 -- such bytes are not checked and give undefined
+ * results).  scaleA: [M, ld_sa] bytes, ld_sa >= K / 16; scaleB likewise.
+ * A per-tensor scale, where the caller has one, folds into alpha.
+ *
+ *   D = alpha * (A . B^T) + beta * C, one bf16 rounding, as mxfp4_gemm.
+ *
+ * Runs the CTA-pair kernel (256 x 256 tiles) for every shape after relaying
+ * the scales into `workspace` (>= nvfp4_gemm_workspace_size(M, N, K) bytes,
+ * 256-byte aligned, owned by the caller, free again once the call's work on
+ * `stream` has finished).  K % 32 == 0 and the 16-byte rules of mxfp4_gemm
+ * apply.  Errors as mxfp4_gemm.
+ */
+int nvfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
+               const void *A, int64_t lda, const void *B, int64_t ldb,
+               const void *scaleA, int64_t ld_sa, const void *scaleB, int64_t ld_sb,
+               float alpha, float beta, int M, int N, int K,
+               void *workspace, size_t workspace_bytes, void *stream);
+size_t nvfp4_gemm_workspace_size(int M, int N, int K);
+
+/*
  * As mxfp4_gemm, with both scale buffers already in the relaid layout
  * produced by mxfp4_scale_relayout (scaleA for M rows, scaleB for N rows, at
  * the same K); the GEMM then copies whole scale atoms with bulk copies.  The

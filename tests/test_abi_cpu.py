@@ -227,6 +227,39 @@ def test_mxfp8_argument_validation(L, kw, status):
     assert _call_gemm8(L, **kw) == status
 
 
+def _call_gemm_nv(L, **kw):
+    args = dict(D=0x1000, ldd=256, C=None, ldc=0, A=0x2000, lda=512, B=0x3000, ldb=512,
+                SA=0x4000, ld_sa=32, SB=0x5000, ld_sb=32, alpha=1.0, beta=0.0, M=128, N=256,
+                K=512, ws=0x10000, wsb=1 << 30, stream=None)
+    args.update(kw)
+    return L.nvfp4_gemm(args["D"], args["ldd"], args["C"], args["ldc"], args["A"], args["lda"],
+                        args["B"], args["ldb"], args["SA"], args["ld_sa"], args["SB"],
+                        args["ld_sb"], args["alpha"], args["beta"], args["M"], args["N"],
+                        args["K"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=None), -1), (dict(A=None), -1), (dict(SA=None), -1), (dict(SB=None), -1),
+    (dict(M=0), -1), (dict(K=48), -1), (dict(K=0), -1),
+    (dict(ld_sa=31), -1), (dict(ld_sb=16), -1),          # one scale per 16 K: 32 per row
+    (dict(beta=1.0), -1), (dict(lda=520), -3), (dict(A=0x2008), -3),
+    (dict(ws=None), -4), (dict(wsb=1024), -4), (dict(ws=0x10010), -3),
+])
+def test_nvfp4_argument_validation(L, kw, status):
+    # These return before any device call, so they run without a GPU.
+    assert _call_gemm_nv(L, **kw) == status
+
+
+def test_nvfp4_workspace_size():
+    # Two relaid scale buffers: row blocks (even count) x four 512-byte atoms
+    # per 256 K, each buffer rounded up to 256 bytes.
+    assert mx.nvfp4_gemm_workspace_size(256, 256, 256) == 2 * (2 * 4 * 512)
+    assert mx.nvfp4_gemm_workspace_size(257, 256, 288) == 4 * 8 * 512 + 2 * 8 * 512
+    assert mx.nvfp4_gemm_workspace_size(8192, 8192, 8192) == 2 * (64 * 128 * 512)
+    assert mx.nvfp4_gemm_workspace_size(0, 256, 256) == 0
+    assert mx.nvfp4_gemm_workspace_size(256, 256, 48) == 0
+
+
 def test_mxfp8_prepacked_validates_before_device(L):
     f = L.mxfp8_gemm_prepacked
     ok = (0x1000, 256, None, 0, 0x2000, 512, 0x3000, 512, 0x4000, 0x5000, 0, 1, 1.0, 0.0, 128, 256,

@@ -1,0 +1,153 @@
+"""NVFP4 GEMM (packed E2M1, one UE4M3 scale per 16 K) on the GPU through the
+C ABI, element by element against the oracle (oracle.gemm_nv).
+
+Bound, as for MXFP4: |D_gpu - D_ref| <= ulp_bf16(D_ref) + 2^-20 * sum|a_k b_k|.
+The kernel is the CTA-pair kernel with kind::mxf4nvf4 MMAs, run for every
+shape, after the scales are relaid into the caller's workspace.
+"""
+import numpy as np
+import pytest
+
+import block_scaled_mxfp4_gb300 as mx
+from block_scaled_mxfp4_gb300 import inputs
+from parity_util import assert_within_bound, bf16_bits_to_f64, d_to_bits, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_scaled_mxfp4_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mx.mxfp4_device_status(reset=True)
+    yield
+    assert mx.mxfp4_device_status() == 0, "a bounded wait timed out during the tests"
+
+
+class DevNV:
+    """An NVFP4 problem's operands on the GPU."""
+
+    def __init__(self, p):
+        self.p = p
+        d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        self.A, self.B, self.SA, self.SB = d(p.A), d(p.B), d(p.SA), d(p.SB)
+        self.C = None
+        if p.C is not None:
+            self.C = d(np.ascontiguousarray(p.C).view(np.int16)).view(torch.bfloat16)
+
+
+def run_nv(dev, alpha=None, beta=None, out=None, stream=None):
+    p = dev.p
+    alpha = p.alpha if alpha is None else alpha
+    beta = p.beta if beta is None else beta
+    D = out if out is not None else torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16,
+                                               device="cuda")
+    wsb = mx.nvfp4_gemm_workspace_size(p.M, p.N, p.K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    C = dev.C if beta != 0.0 else None
+    mx.nvfp4_gemm(D, D.stride(0), C, 0 if C is None else C.stride(0), dev.A, dev.A.stride(0) * 2,
+                  dev.B, dev.B.stride(0) * 2, dev.SA, dev.SA.stride(0), dev.SB, dev.SB.stride(0),
+                  float(alpha), float(beta), p.M, p.N, p.K, ws, wsb, stream)
+    torch.cuda.synchronize()
+    return d_to_bits(D)
+
+
+SHAPES = {
+    # (M, N, K, alpha, beta, C sigma)
+    "one-tile": (256, 256, 256, 1.0, 0.0, None),
+    "alpha-beta": (512, 768, 512, 0.5, 0.75, 1.0),
+    "ragged": (300, 520, 288, 1.0, 0.0, None),
+    "ragged-k-tail": (260, 300, 160, -2.0, 1.0, 1.0),
+    "many-tiles": (2304, 2304, 1024, 1.0, 0.0, None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_nvfp4_matches_oracle(oracle_mod, name):
+    M, N, K, alpha, beta, c_sigma = SHAPES[name]
+    p = inputs.make_problem_nv(name, M, N, K, seed=M + N + K, alpha=alpha, beta=beta,
+                               c_sigma=c_sigma)
+    Dref, _, sabs, inexact = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K, alpha=alpha,
+                                                beta=beta, C=p.C)
+    assert inexact == 0
+    got = run_nv(DevNV(p))
+    assert_within_bound(got, Dref, sabs, what=f"NVFP4 {name} {M}x{N}x{K}")
+
+
+def test_nvfp4_large_sampled(oracle_mod):
+    """8192^3 in the configuration the benchmark times, checked at tile edges
+    and random positions."""
+    M = N = K = 8192
+    p = inputs.make_problem_nv("large-nv", M, N, K, seed=11, alpha=1.0, beta=0.0, c_sigma=None)
+    got = run_nv(DevNV(p))
+    pairs = sample_pairs(M, N, 1500, seed=12, tile_m=256, tile_n=256)
+    Dref, _, sabs, inexact = oracle_mod.gemm_nv_sampled(p.A, p.B, p.SA, p.SB, M, N, K, pairs)
+    assert inexact == 0
+    assert_within_bound(got[pairs[:, 0], pairs[:, 1]], Dref, sabs, what="NVFP4 8192^3 sampled")
+
+
+def test_nvfp4_scale_edge_codes(oracle_mod):
+    """Scale bytes 0x00 (zero), 0x01 and 0x07 (subnormals), 0x08 (smallest
+    normal) and 0x7E (448, the largest) in both operands."""
+    M, N, K = 256, 512, 512
+    p = inputs.make_problem_nv("edges", M, N, K, seed=5, alpha=1.0, beta=0.0, c_sigma=None)
+    rng = np.random.default_rng(6)
+    codes = np.array([0x00, 0x01, 0x07, 0x08, 0x7E, 0x38], dtype=np.uint8)
+    p.SA[:] = codes[rng.integers(0, len(codes), p.SA.shape)]
+    p.SB[:] = codes[rng.integers(0, len(codes), p.SB.shape)]
+    Dref, _, sabs, inexact = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K)
+    assert inexact == 0
+    got = run_nv(DevNV(p))
+    assert_within_bound(got, Dref, sabs, what="NVFP4 scale edge codes")
+
+
+def test_nvfp4_nan_scale_poisons_its_row_and_column(oracle_mod):
+    """Scale byte 0x7F is NaN in UE4M3: A's row r and B's column c of D turn
+    NaN, nothing else changes."""
+    M, N, K = 512, 512, 512
+    p = inputs.make_problem_nv("nan", M, N, K, seed=7, alpha=1.0, beta=1.0, c_sigma=1.0)
+    r, c = 100, 301
+    p.SA[r, 9] = 0x7F
+    p.SB[c, K // 16 - 1] = 0x7F
+    Dref, _, sabs, _ = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K, alpha=1.0, beta=1.0,
+                                          C=p.C)
+    got = run_nv(DevNV(p))
+    want_nan = np.zeros((M, N), dtype=bool)
+    want_nan[r, :] = True
+    want_nan[:, c] = True
+    assert np.array_equal(np.isnan(bf16_bits_to_f64(Dref)), want_nan)
+    assert np.array_equal(np.isnan(bf16_bits_to_f64(got)), want_nan)
+    ok = ~want_nan
+    assert_within_bound(got[ok], Dref[ok], sabs[ok], what="NVFP4 outside the NaN row / column")
+
+
+def test_nvfp4_deterministic_and_ordered():
+    """Bit-identical across calls, and a dependent chain (D2 reads D1 as C)
+    enqueued without synchronisation gives the same bits as synchronised."""
+    M, N, K = 1024, 1536, 1024
+    p = inputs.make_problem_nv("chain", M, N, K, seed=9, alpha=1.0, beta=0.0, c_sigma=None)
+    dev = DevNV(p)
+    first = run_nv(dev)
+    assert np.array_equal(run_nv(dev), first)
+    wsb = mx.nvfp4_gemm_workspace_size(M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+
+    def chain(sync):
+        D1 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        D2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        for D, C, beta in ((D1, None, 0.0), (D2, D1, 0.5)):
+            mx.nvfp4_gemm(D, N, C, N if C is not None else 0, dev.A, K, dev.B, K, dev.SA, K // 16,
+                          dev.SB, K // 16, 1.0, beta, M, N, K, ws, wsb)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return d_to_bits(D1), d_to_bits(D2)
+
+    ref = chain(True)
+    assert np.array_equal(ref[0], first)
+    for _ in range(3):
+        got = chain(False)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])

@@ -550,7 +550,9 @@ def run_nvfp4(args, world, rank, local_rank):
             "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
                            f"{FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio; NVFP4 runs at the "
                            "FP4 rate)",
-            "traffic": None, "traffic_source": "no capture for this workload",
+            "traffic": recorded_traffic("large_nv", "gemm_mxf4_pair"),
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one GEMM launch "
+                              "(profiles/traffic.json); null when the sources changed since",
             "kernel": "scale_relayout_kernel + gemm_mxf4_pair<5, true> (one nvfp4_gemm call, "
                       "timed together)",
             "kernel_ms": ms, "algorithmic_bytes": nbytes, "flops": flops}

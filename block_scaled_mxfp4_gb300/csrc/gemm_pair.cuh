@@ -32,8 +32,9 @@
 //                      down the four replicas), waits for the stores, and
 //                      arrives on the LEADER's sf_ready barrier (the peer's
 //                      warps with a relaxed remote arrive).  tcgen05.st does
-//                      not queue behind the MMAs, unlike tcgen05.cp, so the
-//                      scales of later stages are ready well ahead.
+//                      not queue behind the MMAs already issued (a
+//                      shared-to-tensor-memory copy would), so the scales of
+//                      later stages are ready well ahead.
 //   warp 5 (leader)    waits for the accumulator to be free, then per stage
 //                      for sf_ready (8 arrivals: both CTAs' data landed and
 //                      both CTAs' scales written); issues four K=64 M=256
@@ -111,7 +112,7 @@ __device__ __forceinline__ void pair_tile_coords(const PairSched &s, int t, int 
 // row m: 32-byte stores when the row segment is whole and aligned, with a
 // short pause after every 64 bytes.  The stores overlap the next tile's main
 // loop, and global stores share the memory-instruction queue with the
-// mbarrier polls of the producer, copier and MMA threads: a burst of 64 KB of
+// mbarrier polls of the producer, scale-writer and MMA warps: a burst of 64 KB of
 // stores per CTA delays those polls by thousands of cycles, so the epilogue
 // uses the widest stores and spreads them out.  D goes to L2 as evict-first:
 // written once and not read back, it should not push out the A and B panels
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NV>::THREADS, 1)
                 const uint32_t q_off = static_cast<uint32_t>(((qt * BN) % kSfRowBlock) / 32);
                 const uint32_t d_tmem = tmem;
                 for (int kt = 0; kt < ps.kt; ++kt) {
-                    // sf_ready completes after the copiers observed the
+                    // sf_ready completes after the scale writers observed the
                     // stage's full barrier (all of its bytes landed), so it
                     // stands for both: one poll per stage.
                     if (!mbar_wait(&sf_ready[stage], phase, abort_flag, a.wait_limit,

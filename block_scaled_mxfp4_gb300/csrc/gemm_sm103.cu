@@ -7,33 +7,34 @@
 //   with scaling").
 //
 // One CTA computes one 128 x BN output tile over a range of K (a split):
-//   warps 4, 6, 7  TMA producers: per 256-K stage, one 128x128-byte tile of P
-//           (warp 4), one BNx128-byte tile of Q (warp 6; 128-byte swizzle) and
-//           the stage's relaid scale atoms by 1-D bulk copy (warp 7), into an
-//           S-stage shared-memory ring guarded by full/empty mbarriers.  Each
-//           issuing thread waits out its own copy instructions (a few hundred
-//           cycles apiece), so spreading them over three warps keeps the ring
-//           ahead of the tensor core.  With row-major scales warp 4 alone
-//           issues both tiles and builds the atoms;
-//   warps 0-3  scale writers during the main loop: each lane reads its line
-//           of the stage's atoms from shared memory and writes it with
+//   producers  per 256-K stage, one 128x128-byte tile of P and one Q tile
+//           (128-byte swizzle) into an S-stage shared-memory ring guarded by
+//           full/empty mbarriers.  Scales come one of three ways: relaid
+//           atoms by 1-D bulk copy (warps 4, 6, 7 issue P, Q and the atoms);
+//           row-major scales by 2-D TMA as the aligned 16-byte window of
+//           each row that holds the stage's bytes (warp 4 issues P and P's
+//           window, warp 6 Q and Q's); or, when the scale rows are not
+//           16-byte aligned, gathered by warp 4 with cp.async or plain loads.
+//           Each issuing thread waits out its own copy instructions (a few
+//           hundred cycles apiece), hence one thread per copy stream;
+//   warps 0-3  scale writers during the main loop: each lane takes its line
+//           of the stage's scales from shared memory and writes it with
 //           tcgen05.st into its own TMEM lane (warp w owns lanes 32w..32w+31,
 //           so the four warps lay down the four replicas), then the warp
-//           arrives on the stage's sf_full barrier.  This keeps tcgen05.cp,
-//           which occupies the tensor pipe for tens of cycles per copy, off
-//           the MMA's critical path;
+//           arrives on the stage's sf_full barrier;
 //   warp 5  allocates tensor memory; one thread waits for a stage's scales
 //           (whose barrier the scale writers complete only after the stage's
 //           operands landed) and issues four block-scaled MMAs into an fp32
 //           TMEM accumulator, then commits the stage back to the producers;
 //   warps 0-3  then the epilogue: tcgen05.ld the accumulator (warp w owns TMEM
 //           lanes 32w..32w+31 = tile rows), apply alpha/beta with C, round to
-//           bf16 and store.  With split-K they park the fp32 partial tile in
-//           the workspace instead; the CTA that completes a tile's count (an
-//           epoch-tagged counter per tile) then sums the tile's partials in
-//           split order 0, 1, ..., applies alpha/beta with C and rounds once,
-//           with all of its 256 threads -- no second launch, and the result
-//           does not depend on which split finished last.
+//           bf16 and store.  With split-K the splits of a tile sum their fp32
+//           partials in split order 0, 1, ... inside the launch: up to 8
+//           splits form one thread-block cluster and reduce over distributed
+//           shared memory; more park their partials in the workspace and the
+//           CTA that completes the tile's epoch-tagged counter reduces them.
+//           Either way the result does not depend on which split finished
+//           last, and alpha/beta and the bf16 rounding come once, at the end.
 // The kernel is launched as a programmatic dependent of the preceding work on
 // the stream: it starts while that work drains and waits for it in-kernel
 // (griddepcontrol.wait) before the first read of A, C or the scales and

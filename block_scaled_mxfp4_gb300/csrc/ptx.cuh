@@ -137,12 +137,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
-// Barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar_sync(int id, int count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Asynchronous 4-byte global -> shared copy; bytes past src_bytes (0..4) are
 // zero-filled and not read.
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)
@@ -161,7 +155,7 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (TMA, tcgen05.cp) before they are signalled.
+// proxy (TMA, the tensor cores) before they are signalled.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -196,14 +190,6 @@ __device__ __forceinline__ void tc_fence_before()
 __device__ __forceinline__ void tc_fence_after()
 {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Copy 32 rows x 16 bytes of shared memory (described by `sdesc`) into 4
-// tensor-memory columns at `taddr`, replicated into all four 32-lane groups.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
 }
 
 // D(tmem) (+)= (A(smem) x scaleA) . (B(smem) x scaleB)^T, E2M1 inputs, one
@@ -260,18 +246,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
-        : "r"(taddr));
-}
-
-// Each lane reads 16 consecutive 32-bit columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 
@@ -410,17 +384,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
-// Descriptor of a 32-row x 16-byte block (no swizzle; 8-row core matrices
-// 128 B apart) as the source of a 32x128b tcgen05.cp.
-__device__ __forceinline__ uint64_t sdesc_sf_block(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    return d;
-}
-
 // Instruction descriptor for kind::mxf4: A and B E2M1, E8M0 scales, K-major
 // A and B, fp32 accumulate, shape M x N (x K=64).  The scale-factor ids
 // (which byte pair of each 32-bit TMEM scale word an instruction uses) are
@@ -529,18 +492,6 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cbar)
                  : "memory");
 }
 
-// 2-D tiled TMA load into this CTA's shared memory whose completion is
-// counted on an mbarrier of either CTA of the pair (shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t cbar,
-                                                 int x, int y, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
 // 3-D tiled bulk-tensor load into this CTA's shared memory, completing on a
 // barrier of this CTA (x innermost).
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
@@ -550,17 +501,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
-        : "memory");
-}
-
-// 3-D form of tma_load_2d_pair (x innermost).
-__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t cbar,
-                                                 int x, int y, int z, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
 }
 
@@ -581,29 +521,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
-}
-
-// Each CTA of the pair copies its own 32x128b shared-memory block into its
-// own tensor memory (issued once, by the leader).
-__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-// M=256 block-scaled MMA over the pair: A rows 0-127 / 128-255 and B columns
-// 0-127 / 128-255 from the two CTAs' shared memory, D rows split likewise.
-__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                              uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
 }
 
 // mma_mxf4_pair issued by one elected lane of a warp that runs the issue
@@ -646,17 +563,6 @@ __device__ __forceinline__ void mma_commit_pair_elect(uint64_t *bar, uint16_t ma
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-// Arrive on the mbarrier at this offset in every CTA of `mask` once the
-// pair's tcgen05 work issued so far has completed.
-__device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
         "h"(mask)
         : "memory");
 }

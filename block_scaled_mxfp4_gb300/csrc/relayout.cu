@@ -11,8 +11,9 @@ namespace mxfp4 {
 // "A_scale / B_scale", which also pads with 0x7F = 1.0) -> 512-byte atoms of
 // 128 rows x 4 blocks.  Atom (rb, g) sits at (rb * groups + g) * 512; inside
 // it, row 32j + i and block b sit at byte 16i + 4j + b, so that one 16-byte
-// line holds rows i, i+32, i+64, i+96 -- the 32x128b source shape that
-// tcgen05.cp replicates into the four TMEM lane groups.
+// line holds rows i, i+32, i+64, i+96: the four 32-bit tensor-memory columns
+// lane i of every lane group holds (column j <-> row 32j + i), which the
+// GEMM's scale writers store with one tcgen05.st per lane.
 //
 // One CTA of 256 threads handles one 128-row block (of either operand when
 // both are relaid in one launch) and up to kGroupsPerCta

@@ -151,3 +151,60 @@ def test_nvfp4_deterministic_and_ordered():
     for _ in range(3):
         got = chain(False)
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+def test_nvfp4_strided_buffers(oracle_mod):
+    """Row strides larger than the rows: A and B with 64 spare fp4 elements
+    per row, scale rows with 8 spare bytes, C and D with 24 spare columns."""
+    M, N, K = 384, 320, 512
+    p = inputs.make_problem_nv("strided", M, N, K, seed=21, alpha=0.5, beta=1.0, c_sigma=1.0)
+    Dref, _, sabs, inexact = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K, alpha=0.5,
+                                                beta=1.0, C=p.C)
+    assert inexact == 0
+    pad = lambda x, extra: np.concatenate([x, np.full((x.shape[0], extra), 0x5A, np.uint8)], 1)
+    A = torch.from_numpy(pad(p.A, 32)).cuda()
+    B = torch.from_numpy(pad(p.B, 32)).cuda()
+    SA = torch.from_numpy(pad(p.SA, 8)).cuda()
+    SB = torch.from_numpy(pad(p.SB, 8)).cuda()
+    Cw = np.zeros((M, N + 24), dtype=np.uint16)
+    Cw[:, :N] = p.C
+    C = torch.from_numpy(Cw.view(np.int16)).cuda().view(torch.bfloat16)
+    D = torch.full((M, N + 24), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.nvfp4_gemm_workspace_size(M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    mx.nvfp4_gemm(D, N + 24, C, N + 24, A, A.shape[1] * 2, B, B.shape[1] * 2, SA, SA.shape[1],
+                  SB, SB.shape[1], 0.5, 1.0, M, N, K, ws, wsb)
+    torch.cuda.synchronize()
+    got = d_to_bits(D)
+    assert_within_bound(got[:, :N], Dref, sabs, what="NVFP4 strided")
+    assert np.isnan(bf16_bits_to_f64(got[:, N:])).all()          # padding columns untouched
+
+
+def test_nvfp4_cuda_graph_replay():
+    """nvfp4_gemm (relayout + dependent pair launch) captured in a CUDA graph
+    replays to the eager bits and reads its inputs at replay time."""
+    M, N, K = 1024, 768, 512
+    p = inputs.make_problem_nv("graph", M, N, K, seed=31, alpha=1.0, beta=0.0, c_sigma=None)
+    dev = DevNV(p)
+    ref = run_nv(dev)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.nvfp4_gemm_workspace_size(M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.nvfp4_gemm(D, N, None, 0, dev.A, K, dev.B, K, dev.SA, K // 16, dev.SB, K // 16, 1.0,
+                      0.0, M, N, K, ws, wsb, s)
+    for _ in range(2):
+        D.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(d_to_bits(D), ref)
+    dev.B.copy_(torch.roll(dev.B, 1, 0))
+    dev.SB.copy_(torch.roll(dev.SB, 1, 0))
+    ref2 = run_nv(dev)
+    assert not np.array_equal(ref2, ref)
+    D.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(d_to_bits(D), ref2)

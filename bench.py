@@ -120,7 +120,8 @@ def parse_args():
     ap.add_argument("--workload", default="large",
                     choices=["tiny", "decode", "mid", "large", "skinny", "quantize", "quantize8",
                              "quantize6",
-                             "large8", "decode8", "mixed8", "large6", "mixed6", "large_nv"])
+                             "large8", "decode8", "mixed8", "large6", "mixed6", "large_nv",
+                             "decode_nv", "skinny_nv"])
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -270,8 +271,8 @@ def run_reference(args, rank):
         run_reference_quantize(args)
         return
     fp8 = args.workload in inputs.WORKLOADS8
-    if args.workload == "large_nv":
-        p = nvfp4_problem()
+    if args.workload in NV_WORKLOADS:
+        p = nvfp4_problem(args.workload)
     else:
         p = inputs.workload8(args.workload) if fp8 else inputs.workload(args.workload)
     # About 100 s of oracle time in all (2.5 - 4 minutes with the per-step
@@ -288,7 +289,7 @@ def run_reference(args, rank):
     line = {
         "impl": "reference",
         "metric": ((METRIC6 if args.workload.endswith("6") else METRIC8) if fp8 else
-                   METRIC_NV if args.workload == "large_nv" else METRIC),
+                   METRIC_NV if args.workload in NV_WORKLOADS else METRIC),
         "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
@@ -462,21 +463,30 @@ def run_mxfp8(args, world, rank, local_rank):
         dist.destroy_process_group()
 
 
-METRIC_NV = "NVFP4 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP4 peak"
+METRIC_NV = "NVFP4 GEMM TFLOPS (device-timed, 1 GB300) and % of dense FP4 peak / HBM roofline"
+
+# NVFP4 workloads: the MXFP4 large, decode and skinny shapes (alpha, beta and
+# C as there) with E2M1 codes uniform over all 16 and UE4M3 scales uniform
+# over 0x28..0x48 (0.25 .. 4).
+NV_WORKLOADS = {
+    "large_nv": (8192, 8192, 8192, 13, 1.0, 0.0, None),
+    "decode_nv": (1, 8192, 8192, 14, 1.0, 0.0, None),
+    "skinny_nv": (64, 7168, 16384, 15, 1.0, 1.0, 0.1),
+}
 
 
-def nvfp4_problem():
-    """The NVFP4 workload: 8192^3, E2M1 codes uniform over all 16, UE4M3
-    scales uniform over 0x28..0x48 (0.25 .. 4), alpha 1, beta 0, seed 13."""
+def nvfp4_problem(name="large_nv"):
     from block_scaled_mxfp4_gb300 import inputs
-    return inputs.make_problem_nv("large_nv", 8192, 8192, 8192, seed=13, alpha=1.0, beta=0.0,
-                                  c_sigma=None)
+    M, N, K, seed, alpha, beta, c_sigma = NV_WORKLOADS[name]
+    return inputs.make_problem_nv(name, M, N, K, seed=seed, alpha=alpha, beta=beta,
+                                  c_sigma=c_sigma)
 
 
 def run_nvfp4(args, world, rank, local_rank):
-    """--workload large_nv: one nvfp4_gemm call per step (the NVFP4 scale
-    relayout + the CTA-pair kernel with kind::mxf4nvf4 MMAs, launched as its
-    dependent), steps back to back over rotating input copies, as the MXFP4
+    """--workload large_nv | decode_nv | skinny_nv: one nvfp4_gemm call per
+    step (large: the NVFP4 scale relayout + the CTA-pair kernel launched as
+    its dependent; decode / skinny: the one-tile kernel with split-K in the
+    launch), steps back to back over rotating input copies, as the MXFP4
     headline is timed; each rank of a multi-GPU launch runs a replica."""
     import torch
 
@@ -490,9 +500,9 @@ def run_nvfp4(args, world, rank, local_rank):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     build.build()
     dev = torch.device("cuda", local_rank)
-    p = nvfp4_problem()
+    p = nvfp4_problem(args.workload)
     M, N, K = p.M, p.N, p.K
-    in_bytes = M * K // 2 + N * K // 2 + (M + N) * K // 16
+    in_bytes = M * K // 2 + N * K // 2 + (M + N) * K // 16 + (2 * M * N if p.beta != 0.0 else 0)
     copies = rotation_copies(in_bytes)
     ops = Operands(p, copies, dev)
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -502,8 +512,9 @@ def run_nvfp4(args, world, rank, local_rank):
 
     def launch(i):
         c = i % copies
-        mx.nvfp4_gemm(D, N, None, 0, ops.A[c], K, ops.B[c], K, ops.SA[c], K // 16, ops.SB[c],
-                      K // 16, p.alpha, p.beta, M, N, K, ws, wsb, stream)
+        C = ops.C[c] if p.beta != 0.0 else None
+        mx.nvfp4_gemm(D, N, C, N if C is not None else 0, ops.A[c], K, ops.B[c], K, ops.SA[c],
+                      K // 16, ops.SB[c], K // 16, p.alpha, p.beta, M, N, K, ws, wsb, stream)
 
     for i in range(max(3, args.warmup)):
         launch(i)
@@ -520,10 +531,13 @@ def run_nvfp4(args, world, rank, local_rank):
     # inputs' copies in, the call, D's copy out, all inside the timed region.
     pin = lambda t: t.cpu().pin_memory()
     hA, hB, hSA, hSB = pin(ops.A[0]), pin(ops.B[0]), pin(ops.SA[0]), pin(ops.SB[0])
+    copies_in = [(hA, ops.A[0]), (hB, ops.B[0]), (hSA, ops.SA[0]), (hSB, ops.SB[0])]
+    if p.beta != 0.0:
+        copies_in.append((pin(ops.C[0]), ops.C[0]))
     hD = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
 
     def e2e_step():
-        for h, d in ((hA, ops.A[0]), (hB, ops.B[0]), (hSA, ops.SA[0]), (hSB, ops.SB[0])):
+        for h, d in copies_in:
             d.copy_(h, non_blocking=True)
         launch(0)
         hD.copy_(D, non_blocking=True)
@@ -543,35 +557,46 @@ def run_nvfp4(args, world, rank, local_rank):
             dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
-    achieved = flops / (ms * 1e-3) / 1e12
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak,
-            "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
-                           f"{FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio; NVFP4 runs at the "
-                           "FP4 rate)",
-            "traffic": recorded_traffic("large_nv", "gemm_mxf4_pair"),
-            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one GEMM launch "
-                              "(profiles/traffic.json); null when the sources changed since",
-            "kernel": "scale_relayout_kernel + gemm_mxf4_pair<5, true> (one nvfp4_gemm call, "
-                      "timed together)",
-            "kernel_ms": ms, "algorithmic_bytes": nbytes, "flops": flops}
+    skinny = M <= 64
+    if skinny:
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{peak_src} HBM copy bandwidth",
+                "kernel": "gemm_mxf4_kernel<64, 4, true, 2, 2> (one nvfp4_gemm call)"}
+    else:
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"] * FP4_OVER_BF16, "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']:.1f} TFLOP/s x "
+                               f"{FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio; NVFP4 runs at "
+                               "the FP4 rate)",
+                "kernel": "scale_relayout_kernel + gemm_mxf4_pair<5, true> (one nvfp4_gemm "
+                          "call, timed together)"}
+    traffic = recorded_traffic(args.workload, "gemm_mxf4_kernel" if skinny else "gemm_mxf4_pair")
+    roof.update({"frac": achieved / roof["peak"], "traffic": traffic,
+                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one GEMM "
+                                   "launch (profiles/traffic.json); null when the sources changed "
+                                   "since",
+                 "kernel_ms": ms, "algorithmic_bytes": nbytes, "flops": flops})
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v, cores, desc, _ = oracle_throughput(p, 10.0, 78)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
-    h2d = sum(t.numel() * t.element_size() for t in (hA, hB, hSA, hSB))
+    h2d = sum(h.numel() * h.element_size() for h, _ in copies_in)
     line = {
         "metric": METRIC_NV, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4 (e2m1, ue4m3 per 16)", "data": "synthetic",
-        "config": {"workload": f"large_nv M={M} N={N} K={K}", "M": M, "N": N, "K": K,
-                   "alpha": p.alpha, "beta": p.beta, "seed": p.seed, "tile": "256x256x256",
-                   "stages": 5,
+        "config": {"workload": f"{args.workload} M={M} N={N} K={K}", "M": M, "N": N, "K": K,
+                   "alpha": p.alpha, "beta": p.beta, "seed": p.seed,
+                   "tile": "128x64x256 (swap-AB)" if skinny else "256x256x256",
+                   "stages": 4 if skinny else 5,
                    "l2": f"inputs larger than L2: steps rotate over {copies} copies of the "
                          "inputs, back to back between one pair of events",
-                   "step": "one nvfp4_gemm call: NVFP4 scale relayout of A and B (one launch) + "
-                           "CTA-pair GEMM launched as its dependent",
+                   "step": ("one nvfp4_gemm call: the one-tile GEMM, K split across a cluster "
+                            "summed in the launch") if skinny else
+                           ("one nvfp4_gemm call: NVFP4 scale relayout of A and B (one launch) + "
+                            "CTA-pair GEMM launched as its dependent"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -579,7 +604,7 @@ def run_nvfp4(args, world, rank, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "api": "nvfp4_gemm with its inputs copied in and D copied out (pinned host "
                        "memory) on the same stream"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if skinny else 2) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -1191,7 +1216,7 @@ def main():
     if args.workload in ("large8", "decode8", "mixed8", "large6", "mixed6"):
         run_mxfp8(args, world, rank, local_rank)
         return
-    if args.workload == "large_nv":
+    if args.workload in NV_WORKLOADS:
         run_nvfp4(args, world, rank, local_rank)
         return
     run_mxfp4(args, world, rank, local_rank)

@@ -105,12 +105,13 @@ bool encode_operand(CUtensorMap *map, const void *base, int rows, int K, int64_t
 
 // 2-D uint8 view [rows, K/32] of row-major E8M0 scales (row stride ld bytes,
 // a multiple of 16); box 16 bytes x box_rows, no swizzle, zero fill.
-bool encode_scales(CUtensorMap *map, const void *base, int rows, int K, int64_t ld, int box_rows)
+// kbytes: scale bytes per row (K / 32, or K / 16 for NVFP4).
+bool encode_scales(CUtensorMap *map, const void *base, int rows, int kbytes, int64_t ld, int box_rows)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
         return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(rows)};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
     cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
@@ -315,6 +316,7 @@ int make_plan(int M, int N, int K, int split_req, int sms, mxfp4_plan *out, Gemm
         shape->pair = use_pair;
         shape->pair_ctas = out->ctas;
         shape->fp8 = fp8 ? 1 : 0;
+        shape->nv = 0;
     }
     return MXFP4_OK;
 }
@@ -447,8 +449,9 @@ int run_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, in
                (sc.ld_b % 16) == 0;
     a.q_box_rows = q_box;
     CUtensorMap tmSP = tmP, tmSQ = tmQ;   // unused unless a.sf_tma
-    if (a.sf_tma && (!encode_scales(&tmSP, a.sfP, Prows, K, a.ldsP, kTileM) ||
-                     !encode_scales(&tmSQ, a.sfQ, Qrows, K, a.ldsQ, q_box)))
+    const int kbytes = nv ? K / 16 : K / 32;
+    if (a.sf_tma && (!encode_scales(&tmSP, a.sfP, Prows, kbytes, a.ldsP, kTileM) ||
+                     !encode_scales(&tmSQ, a.sfQ, Qrows, kbytes, a.ldsQ, q_box)))
         return MXFP4_ERR_CUDA;
     a.rowsP = Prows;
     a.rowsQ = Qrows;
@@ -728,10 +731,25 @@ int mxfp8_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
                          M, N, K, split_k, workspace, workspace_bytes, stream, true, fmt_a, fmt_b);
 }
 
+// NVFP4 plan: skinny shapes (M <= 64, swap-AB) run the one-tile kernel with
+// the MXFP4 plan's tile and split and the row-major scales read by TMA (no
+// workspace up to 8 splits); every other shape runs the CTA-pair kernel on
+// relaid scales.
+static bool nv_one_tile(int M, int N, int K, mxfp4_plan *plan, GemmShape *shape)
+{
+    if (!(M <= 64 && N > M))
+        return false;
+    return make_plan(M, N, K, 0, device_sms_or_default(), plan, shape, false) == MXFP4_OK &&
+           plan->swap_ab == 1 && plan->pair == 0 && plan->split_k <= kMaxClusterSplit;
+}
+
 size_t nvfp4_gemm_workspace_size(int M, int N, int K)
 {
     if (M < 1 || N < 1 || K < 32 || (K % 32) != 0)
         return 0;
+    // The relaid scales of the pair kernel.  (The skinny path needs none when
+    // the caller's scale rows are 16-byte aligned; with other scale rows it
+    // falls back to the pair kernel, so the size covers that case too.)
     return align_up(sf_relaid_bytes_nv(M, K)) + align_up(sf_relaid_bytes_nv(N, K));
 }
 
@@ -751,6 +769,23 @@ int nvfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc, const void *A, 
     const int64_t tiles = ((static_cast<int64_t>(M) + 255) / 256) * ((static_cast<int64_t>(N) + 255) / 256);
     if (tiles > 0x7FFFFFFF)
         return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    {
+        mxfp4_plan plan;
+        GemmShape shape;
+        if (nv_one_tile(M, N, K, &plan, &shape) && aligned(scaleA, 16) && aligned(scaleB, 16) &&
+            (ld_sa % 16) == 0 && (ld_sb % 16) == 0) {
+            if (workspace && !aligned(workspace, kAlign))
+                return MXFP4_ERR_MISALIGNED;
+            st = check_device();
+            if (st != MXFP4_OK)
+                return st;
+            shape.nv = 1;
+            const Scales sc{static_cast<const uint8_t *>(scaleA), static_cast<const uint8_t *>(scaleB),
+                            ld_sa, ld_sb, true};
+            return run_gemm(D, ldd, C, ldc, A, lda, B, ldb, sc, alpha, beta, M, N, K, plan, shape,
+                            nullptr, static_cast<cudaStream_t>(stream), false, 0, 0, 0, true);
+        }
+    }
     const size_t sfa_bytes = align_up(sf_relaid_bytes_nv(M, K));
     const size_t sfb_bytes = align_up(sf_relaid_bytes_nv(N, K));
     if (!workspace || workspace_bytes < sfa_bytes + sfb_bytes)

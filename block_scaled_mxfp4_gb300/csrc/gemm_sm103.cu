@@ -62,9 +62,12 @@ namespace mxfp4 {
 
 __device__ int g_device_status = 0;
 
-// G = scale k-groups (4 blocks of 32 K) per stage of 128 bytes per row: 2 for
-// fp4 elements (256 K per stage), 1 for 8-bit elements (128 K per stage).
-template <int BN, int STAGES, int G = 2>
+// G = scale words (4 scale bytes each) per row and stage of 128 bytes per
+// row: 2 for fp4 elements with E8M0 per 32 (256 K per stage), 1 for 8-bit
+// elements (128 K per stage), 4 for NVFP4 (UE4M3 per 16, 256 K per stage).
+// RAW_ONLY: scales only ever come as row-major 16-byte windows (the shared
+// memory of a stage is sized for those, not for relaid atoms).
+template <int BN, int STAGES, int G = 2, bool RAW_ONLY = false>
 struct Cfg {
     static constexpr int BM = kTileM;
     static constexpr int BN_COLS = BN;
@@ -79,7 +82,8 @@ struct Cfg {
     // 16-byte window holding the stage's 4G scale bytes).
     static constexpr int SFRP_BYTES = BM * 16;
     static constexpr int SFRQ_BYTES = BN * 16;
-    static constexpr int SF_AREA = (SFP_BYTES + SFQ_BYTES) > (SFRP_BYTES + SFRQ_BYTES)
+    static constexpr bool RAW = RAW_ONLY;
+    static constexpr int SF_AREA = (!RAW_ONLY && (SFP_BYTES + SFQ_BYTES) > (SFRP_BYTES + SFRQ_BYTES))
                                        ? (SFP_BYTES + SFQ_BYTES) : (SFRP_BYTES + SFRQ_BYTES);
     // Stages start on 1024-byte boundaries (128-byte swizzle atoms).
     static constexpr int STAGE_BYTES = (P_BYTES + Q_BYTES + SF_AREA + 1023) / 1024 * 1024;
@@ -97,8 +101,12 @@ struct Cfg {
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
-    static_assert(G == 1 || G == 2, "scale groups per stage");
+    static_assert(G == 1 || G == 2 || G == 4, "scale words per stage");
 };
+
+// The configuration of element format FMT (0 MXFP4, 1 byte formats, 2 NVFP4).
+template <int BN, int STAGES, int FMT>
+using CfgFor = Cfg<BN, STAGES, FMT == 0 ? 2 : FMT == 1 ? 1 : 4, FMT == 2>;
 
 constexpr int kGemmThreadsC = 256;     // threads of the one-tile kernel
 
@@ -567,7 +575,7 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
                             row < Cf::BN_COLS ? *reinterpret_cast<const uint32_t *>(rq + row * 16 + 4 * g) : 0u;
                     }
             }
-        } else {
+        } else if constexpr (!Cf::RAW) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const uint4 v = *reinterpret_cast<const uint4 *>(sf_s + g * kSfAtomBytes + 16 * lane);
@@ -588,11 +596,15 @@ __device__ __forceinline__ void write_stage_scales(uint8_t *smem, uint64_t *full
         }
         }
         const uint32_t slot = t_sf + stage * Cf::SF_COLS;
-        if constexpr (G == 2)
+        if constexpr (G == 4)
+            tmem_st_32x32b_x16(slot, wp);
+        else if constexpr (G == 2)
             tmem_st_32x32b_x8(slot, wp);
         else
             tmem_st_32x32b_x4(slot, wp);
-        if constexpr (4 * G * Cf::NQ == 16)
+        if constexpr (4 * G * Cf::NQ == 32)
+            tmem_st_32x32b_x32(slot + Cf::SF_COLS_P, wq);
+        else if constexpr (4 * G * Cf::NQ == 16)
             tmem_st_32x32b_x16(slot + Cf::SF_COLS_P, wq);
         else if constexpr (4 * G * Cf::NQ == 8)
             tmem_st_32x32b_x8(slot + Cf::SF_COLS_P, wq);
@@ -621,7 +633,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmSP,
                      const __grid_constant__ CUtensorMap tmSQ)
 {
-    using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
+    using Cf = CfgFor<BN, STAGES, FMT>;
     constexpr int G = Cf::GROUPS;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the ring (128-byte swizzle atoms).
@@ -742,7 +754,9 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                         mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
                 }
             }
-        } else if (a.sf_rowmajor && a.sf_async && nkt > 0 && warp == 4) {
+        } else if constexpr (FMT != 2) {
+        // (NVFP4 takes row-major scales by TMA only; these paths are not built for it.)
+        if (a.sf_rowmajor && a.sf_async && nkt > 0 && warp == 4) {
             // Whole warp: lane 0 issues the operand TMAs; every lane copies its
             // lines of the stage's scale atoms with 4-byte cp.async straight
             // from the row-major scales, and the stage's full barrier counts
@@ -884,10 +898,13 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                     mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u, a.wait_limit);
             }
         }
+        }
     } else if (warp == 5) {
         // ---------------------------------------------------- MMA issuer --
         if (lane == 0 && nkt > 0) {
-            const uint32_t idesc = FMT == 0 ? idesc_mxf4(kTileM, BN) : a.idesc8;
+            const uint32_t idesc = FMT == 0   ? idesc_mxf4(kTileM, BN)
+                                   : FMT == 2 ? idesc_nvf4(kTileM, BN)
+                                              : a.idesc8;
             const uint32_t t_sf = tmem + BN;
             // A 64-row Q tile uses the upper or lower half of its 128-row atom.
             // (Row-major scales are built relative to q0, so no offset there.)
@@ -910,7 +927,11 @@ __global__ void __launch_bounds__(kGemmThreads, MINB)
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(st + Cf::P_BYTES));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if constexpr (FMT == 0) {
+                    if constexpr (FMT == 2) {
+                        // K=64: the four 16-K scale bytes of word j.
+                        mma_nvf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfp_t + j * 4,
+                                 sfq_t + j * 4 * Cf::NQ + q_off, (i > 0 || j > 0) ? 1u : 0u);
+                    } else if constexpr (FMT == 0) {
                         // K=64: bytes 0-1 / 2-3 of k-group j / 2.
                         const uint32_t sf_id = (j & 1) * 2;
                         mma_mxf4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_sf_ids(idesc, sf_id, sf_id),
@@ -1048,7 +1069,7 @@ static cudaError_t launch_cfg(const GemmArgs &a, const CUtensorMap &tmP, const C
                               const CUtensorMap &tmSP, const CUtensorMap &tmSQ, dim3 grid,
                               cudaStream_t stream)
 {
-    using Cf = Cfg<BN, STAGES, FMT == 0 ? 2 : 1>;
+    using Cf = CfgFor<BN, STAGES, FMT>;
     auto kern = gemm_mxf4_kernel<BN, STAGES, SWAP, FMT, MINB>;
     // Opt in to the large dynamic shared memory once per device.
     static std::atomic<int> configured[64];
@@ -1132,6 +1153,13 @@ cudaError_t launch_gemm(const GemmArgs &a, const CUtensorMap &tmP, const CUtenso
                         const CUtensorMap &tmSP, const CUtensorMap &tmSQ, const GemmShape &s,
                         dim3 grid, cudaStream_t stream)
 {
+    if (s.nv) {
+        // NVFP4 one-tile form: skinny shapes (swap-AB) with row-major scales
+        // by TMA; everything else runs the CTA-pair kernel.
+        if (!s.swap || s.tile_n != 64 || s.stages != 4 || !a.sf_rowmajor || !a.sf_tma)
+            return cudaErrorInvalidConfiguration;
+        return launch_cfg<64, 4, true, 2, 2>(a, tmP, tmQ, tmSP, tmSQ, grid, stream);
+    }
     if (!s.fp8)
         return launch_gemm_fmt<0>(a, tmP, tmQ, tmSP, tmSQ, s, grid, stream);
     // kind::mxf8f6f4 element codes: E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5.

@@ -83,6 +83,8 @@ struct GemmShape {
     int pair;               // 1: CTA-pair kernel (256 x 256 tiles, cta_group::2)
     int pair_ctas;          // pair kernel: grid size (upper bound; 2 x pairs)
     int fp8;                // 1: 8-bit elements (one-tile kernel, kind::mxf8f6f4)
+    int nv;                 // 1: NVFP4 (kind::mxf4nvf4, UE4M3 per 16 K; one-tile: swap-AB
+                            //    with row-major scales by TMA only)
 };
 
 // Dynamic shared memory one GEMM configuration needs (0 if unsupported).

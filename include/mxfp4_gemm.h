@@ -264,11 +264,14 @@ size_t mxfp8_gemm_prepacked_workspace_size(int M, int N, int K, int split_k);
  *
  *   D = alpha * (A . B^T) + beta * C, one bf16 rounding, as mxfp4_gemm.
  *
- * Runs the CTA-pair kernel (256 x 256 tiles) for every shape after relaying
- * the scales into `workspace` (>= nvfp4_gemm_workspace_size(M, N, K) bytes,
- * 256-byte aligned, owned by the caller, free again once the call's work on
- * `stream` has finished).  K % 32 == 0 and the 16-byte rules of mxfp4_gemm
- * apply.  Errors as mxfp4_gemm.
+ * Skinny shapes (M <= 64 and N > M) whose scale rows are 16-byte aligned
+ * (scaleA, scaleB, ld_sa, ld_sb) run the one-tile kernel with mxfp4_gemm's
+ * plan (swap-AB, split-K inside the launch) and leave the workspace
+ * untouched (it may be NULL).  Every other call relays the scales into
+ * `workspace` (>= nvfp4_gemm_workspace_size(M, N, K) bytes, 256-byte
+ * aligned, owned by the caller, free again once the call's work on `stream`
+ * has finished) and runs the CTA-pair kernel (256 x 256 tiles).  K % 32 == 0
+ * and the 16-byte rules of mxfp4_gemm apply.  Errors as mxfp4_gemm.
  */
 int nvfp4_gemm(void *D, int64_t ldd, const void *C, int64_t ldc,
                const void *A, int64_t lda, const void *B, int64_t ldb,

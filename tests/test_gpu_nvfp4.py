@@ -208,3 +208,81 @@ def test_nvfp4_cuda_graph_replay():
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(d_to_bits(D), ref2)
+
+
+# Skinny shapes (M <= 64) run the one-tile kernel (swap-AB, kind::mxf4nvf4,
+# row-major scales by TMA, split-K summed in the tile's cluster).
+SKINNY = {
+    # (M, N, K, alpha, beta, C sigma)
+    "decode": (1, 8192, 8192, 1.0, 0.0, None),
+    "m8-ragged-n": (8, 3000, 2048, 0.5, 1.0, 0.1),
+    "m33-ragged-k": (33, 1024, 4160, 1.0, 0.0, None),
+    "m64": (64, 2048, 4096, 1.0, 1.0, 0.1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SKINNY))
+def test_nvfp4_skinny_matches_oracle(oracle_mod, name):
+    M, N, K, alpha, beta, c_sigma = SKINNY[name]
+    p = inputs.make_problem_nv(name, M, N, K, seed=M + 3 * N + K, alpha=alpha, beta=beta,
+                               c_sigma=c_sigma)
+    plan = mx.mxfp4_plan_gemm(M, N, K, 0, 0)
+    assert plan.swap_ab == 1
+    Dref, _, sabs, inexact = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K, alpha=alpha,
+                                                beta=beta, C=p.C)
+    assert inexact == 0
+    dev = DevNV(p)
+    # Scale rows padded to a multiple of 16 bytes (a K with a partial last
+    # 256-K stage has K/16 % 16 != 0), as the one-tile path's TMA needs.
+    width = (K // 16 + 15) // 16 * 16
+    pad = lambda x: np.concatenate([x, np.full((x.shape[0], width - K // 16), 0x38, np.uint8)], 1)
+    dev.SA = torch.from_numpy(pad(p.SA)).cuda()
+    dev.SB = torch.from_numpy(pad(p.SB)).cuda()
+    got = run_nv(dev)
+    assert_within_bound(got, Dref, sabs, what=f"NVFP4 skinny {name} {M}x{N}x{K} "
+                                              f"(split {plan.split_k})")
+    assert np.array_equal(run_nv(dev), got)                     # deterministic
+
+
+def test_nvfp4_skinny_scale_codes_and_nan(oracle_mod):
+    """The one-tile path on the scale edge codes, and 0x7F poisoning exactly
+    its row and column."""
+    M, N, K = 16, 1536, 2048
+    p = inputs.make_problem_nv("skinny-edges", M, N, K, seed=41, alpha=1.0, beta=0.0,
+                               c_sigma=None)
+    rng = np.random.default_rng(42)
+    codes = np.array([0x00, 0x01, 0x07, 0x08, 0x7E, 0x38], dtype=np.uint8)
+    p.SA[:] = codes[rng.integers(0, len(codes), p.SA.shape)]
+    p.SB[:] = codes[rng.integers(0, len(codes), p.SB.shape)]
+    r, c = 5, 777
+    p.SA[r, 3] = 0x7F
+    p.SB[c, 100] = 0x7F
+    Dref, _, sabs, _ = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K)
+    got = run_nv(DevNV(p))
+    want_nan = np.zeros((M, N), dtype=bool)
+    want_nan[r, :] = True
+    want_nan[:, c] = True
+    assert np.array_equal(np.isnan(bf16_bits_to_f64(Dref)), want_nan)
+    assert np.array_equal(np.isnan(bf16_bits_to_f64(got)), want_nan)
+    ok = ~want_nan
+    assert_within_bound(got[ok], Dref[ok], sabs[ok], what="NVFP4 skinny edge codes")
+
+
+def test_nvfp4_skinny_misaligned_scales_take_the_pair_path(oracle_mod):
+    """Scale rows that are not 16-byte aligned (ld_sa = K/16 + 4) cannot come
+    by TMA: the call falls back to the pair kernel, same results."""
+    M, N, K = 4, 1024, 1024
+    p = inputs.make_problem_nv("skinny-odd", M, N, K, seed=43, alpha=1.0, beta=0.0, c_sigma=None)
+    Dref, _, sabs, inexact = oracle_mod.gemm_nv(p.A, p.B, p.SA, p.SB, M, N, K)
+    assert inexact == 0
+    pad = lambda x: np.concatenate([x, np.full((x.shape[0], 4), 0x38, np.uint8)], 1)
+    SA = torch.from_numpy(pad(p.SA)).cuda()
+    SB = torch.from_numpy(pad(p.SB)).cuda()
+    dev = DevNV(p)
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wsb = mx.nvfp4_gemm_workspace_size(M, N, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    mx.nvfp4_gemm(D, N, None, 0, dev.A, K, dev.B, K, SA, SA.shape[1], SB, SB.shape[1], 1.0, 0.0,
+                  M, N, K, ws, wsb)
+    torch.cuda.synchronize()
+    assert_within_bound(d_to_bits(D), Dref, sabs, what="NVFP4 skinny, unaligned scale rows")

@@ -957,7 +957,7 @@ def profile_shape(args):
             mx.nvfp4_gemm(D, N, None, 0, A, K, B, K, SA, K // 16, SB, K // 16, 1.0, 0.0, M, N, K,
                           ws, wsb)
         torch.cuda.synchronize()
-        print(f"{M}x{N}x{K} nvfp4: {args.calls} calls (CTA-pair kernel)")
+        print(f"{M}x{N}x{K} nvfp4: {args.calls} calls")
         return
     if args.format != "mxfp4":
         fmt = {"e4m3": mx.MXFP8_E4M3, "e5m2": mx.MXFP8_E5M2, "e2m3": mx.MXFP6_E2M3,

@@ -162,7 +162,7 @@ int mxfp4_scale_relayout2(void *dst_a, const void *src_a, int rows_a, int64_t ld
  * The scales are read row-major.  Compute-bound shapes (plan.relayout_pass)
  * first relay them out into the workspace with the relayout kernel; the
  * others build the tcgen05 scale layout inside the GEMM itself.
- * Every kernel is launched as a programmatic dependent of the work already on
+ * Every kernel of the call is launched as a programmatic dependent of the work on
  * `stream`: it may start while that work drains (its set-up overlaps the
  * other kernel's tail) and waits for it in-kernel before reading any input or
  * writing any output, so ordering on the stream is as for plain launches.
